@@ -1,0 +1,183 @@
+"""RankMixer CPU oracle -- TEST INFRASTRUCTURE ONLY.
+
+A plain double-precision restatement of the RankMixer block forward
+(``rankmixer_oracle.c``), loaded through ctypes.  Only ``tests/``, the smoke
+check in ``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may
+import this package.  It shares no code with the CUDA library and never
+imports it.
+
+Sources: "RankMixer: Scaling Up Ranking Models in Industrial Recommenders",
+section 3.1 Eq. 1, section 3.3 Eq. 3-9, section 3.4 Eq. 10; "RankMixer 详解（1）",
+sections 3.1, 3.3, 4.1 and 5.1.  Every function below forwards to the C loop
+nest of the same name; the docstrings say which passage each follows.
+
+Parity status: every function is pinned by a test under ``tests/`` (printed
+worked examples, closed forms, invariants); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "rankmixer_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP over samples).  Returns the .so path."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fno-fast-math", "-fPIC", "-shared", "-fopenmp", "-std=c11",
+           _SRC, "-o", tmp, "-lm"]
+    subprocess.check_call(cmd)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            dp = ctypes.POINTER(ctypes.c_double)
+            i = ctypes.c_int
+            lib.oracle_token_mix.argtypes = [dp, dp, i, i, i, i]
+            lib.oracle_layernorm.argtypes = [dp, dp, dp, ctypes.c_double, dp, i, i]
+            lib.oracle_gelu.argtypes = [dp, dp, ctypes.c_size_t]
+            lib.oracle_pffn.argtypes = [dp, dp, dp, dp, dp, dp, i, i, i, i]
+            lib.oracle_block_forward.argtypes = [dp] * 11 + [ctypes.c_double, i, i, i, i]
+            lib.oracle_mean_pool.argtypes = [dp, dp, i, i, i]
+            lib.oracle_stack_forward.argtypes = [dp] * 11 + [ctypes.c_double, i, i, i, i, i]
+            lib.oracle_moe_pffn.argtypes = [dp] * 9 + [i, i, i, i, i]
+            lib.oracle_num_threads.restype = ctypes.c_int
+            lib.oracle_set_num_threads.argtypes = [i]
+            _lib = lib
+    return _lib
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def num_threads() -> int:
+    return _load().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    _load().oracle_set_num_threads(int(n))
+
+
+def token_mix(X, H: int | None = None) -> np.ndarray:
+    """TokenMixing ("RankMixer", section 3.3.1 Eq. 3-4; "RankMixer 详解（1）" section 3.1):
+    out[b, h, t*q + r] = X[b, t, h*q + r] with q = D/H.  X is [B, T, D] (or [T, D])."""
+    X = _f64(X)
+    squeeze = X.ndim == 2
+    if squeeze:
+        X = X[None]
+    B, T, D = X.shape
+    H = T if H is None else H
+    if D % H:
+        raise ValueError("D must be divisible by H")
+    out = np.empty((B, H, T * (D // H)), dtype=np.float64)
+    _load().oracle_token_mix(_p(X), _p(out), B, T, D, H)
+    return out[0] if squeeze else out
+
+
+def layernorm(R, gamma=None, beta=None, eps: float = 1e-5) -> np.ndarray:
+    """Row LayerNorm with biased variance ("RankMixer 详解（1）" section 3.3)."""
+    R = _f64(R)
+    D = R.shape[-1]
+    rows = R.size // D
+    g = _f64(np.ones(D) if gamma is None else gamma)
+    b = _f64(np.zeros(D) if beta is None else beta)
+    out = np.empty_like(R)
+    _load().oracle_layernorm(_p(R), _p(g), _p(b), float(eps), _p(out), rows, D)
+    return out
+
+
+def gelu(u) -> np.ndarray:
+    """Gelu(u) = u * Phi(u) ("RankMixer 详解（1）" section 4.1)."""
+    u = _f64(u)
+    out = np.empty_like(u)
+    _load().oracle_gelu(_p(u), _p(out), u.size)
+    return out
+
+
+def pffn(S, W1, b1, W2, b2) -> np.ndarray:
+    """Per-token FFN ("RankMixer" section 3.3.2 Eq. 6-9): V[b,t] = Gelu(S[b,t] W1[t] + b1[t]) W2[t] + b2[t].
+    S [B,T,D], W1 [T,D,F], b1 [T,F], W2 [T,F,D], b2 [T,D]."""
+    S, W1, b1, W2, b2 = map(_f64, (S, W1, b1, W2, b2))
+    B, T, D = S.shape
+    F = W1.shape[-1]
+    V = np.empty_like(S)
+    _load().oracle_pffn(_p(S), _p(W1), _p(b1), _p(W2), _p(b2), _p(V), B, T, D, F)
+    return V
+
+
+def block_forward(X, p: dict, eps: float = 1e-5, return_S: bool = False):
+    """One RankMixer block ("RankMixer" section 3.1 Eq. 1):
+    S = LN1(TokenMixing(X) + X); X' = LN2(PFFN(S) + S).  ``p`` holds one layer:
+    W1 [T,D,F], b1 [T,F], W2 [T,F,D], b2 [T,D], ln1_g, ln1_b, ln2_g, ln2_b [D]."""
+    X = _f64(X)
+    B, T, D = X.shape
+    a = {k: _f64(p[k]) for k in ("W1", "b1", "W2", "b2", "ln1_g", "ln1_b", "ln2_g", "ln2_b")}
+    F = a["W1"].shape[-1]
+    Xo = np.empty_like(X)
+    S = np.empty_like(X)
+    _load().oracle_block_forward(_p(X), _p(Xo), _p(S), _p(a["W1"]), _p(a["b1"]), _p(a["W2"]), _p(a["b2"]),
+                                 _p(a["ln1_g"]), _p(a["ln1_b"]), _p(a["ln2_g"]), _p(a["ln2_b"]),
+                                 float(eps), B, T, D, F)
+    return (Xo, S) if return_S else Xo
+
+
+def mean_pool(X) -> np.ndarray:
+    """o = (1/T) sum_t X[b, t, :] ("RankMixer" section 3.1; "RankMixer 详解（1）" section 5.1)."""
+    X = _f64(X)
+    B, T, D = X.shape
+    o = np.empty((B, D), dtype=np.float64)
+    _load().oracle_mean_pool(_p(X), _p(o), B, T, D)
+    return o
+
+
+def stack_forward(X0, layers: list, eps: float = 1e-5, return_XL: bool = False):
+    """L stacked blocks with per-layer weights, then mean pooling ("RankMixer" section 3.1)."""
+    X0 = _f64(X0)
+    B, T, D = X0.shape
+    L = len(layers)
+    cat = {k: _f64(np.stack([np.asarray(l[k], dtype=np.float64) for l in layers]))
+           for k in ("W1", "b1", "W2", "b2", "ln1_g", "ln1_b", "ln2_g", "ln2_b")}
+    F = cat["W1"].shape[-1]
+    pooled = np.empty((B, D), dtype=np.float64)
+    XL = np.empty_like(X0) if return_XL else None
+    xl_ptr = _p(XL) if return_XL else ctypes.POINTER(ctypes.c_double)()
+    _load().oracle_stack_forward(_p(X0), _p(pooled), xl_ptr, _p(cat["W1"]), _p(cat["b1"]), _p(cat["W2"]),
+                                 _p(cat["b2"]), _p(cat["ln1_g"]), _p(cat["ln1_b"]), _p(cat["ln2_g"]),
+                                 _p(cat["ln2_b"]), float(eps), B, T, D, F, L)
+    return (pooled, XL) if return_XL else pooled
+
+
+def moe_pffn(S, Wg, bg, eW1, eb1, eW2, eb2, return_gates: bool = False):
+    """Sparse-MoE PFFN with ReLU routing ("RankMixer" section 3.4 Eq. 10), all experts
+    evaluated densely.  S [B,T,D], Wg [T,D,E], bg [T,E], eW1 [T,E,D,Fe], eb1 [T,E,Fe],
+    eW2 [T,E,Fe,D], eb2 [T,E,D]."""
+    S, Wg, bg, eW1, eb1, eW2, eb2 = map(_f64, (S, Wg, bg, eW1, eb1, eW2, eb2))
+    B, T, D = S.shape
+    E = Wg.shape[-1]
+    Fe = eW1.shape[-1]
+    V = np.empty_like(S)
+    G = np.empty((B, T, E), dtype=np.float64)
+    _load().oracle_moe_pffn(_p(S), _p(Wg), _p(bg), _p(eW1), _p(eb1), _p(eW2), _p(eb2), _p(V), _p(G),
+                            B, T, D, E, Fe)
+    return (V, G) if return_gates else V

@@ -1,0 +1,299 @@
+/*
+ * RankMixer CPU oracle -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, obviously-correct restatement of the RankMixer block forward
+ * in double precision.  It exists to check the CUDA library; only the test
+ * suite, the smoke check and the benchmark's CPU-baseline leg may load it.
+ * It shares no code, header or table with the CUDA path.
+ *
+ * Sources (the pages this restates):
+ *   [RM]  "RankMixer: Scaling Up Ranking Models in Industrial Recommenders"
+ *         (Zhu et al., ByteDance), section 3.1 Eq. 1, section 3.3.1 Eq. 3-5,
+ *         section 3.3.2 Eq. 6-9, section 3.4 Eq. 10, section 3.5 Eq. 12.
+ *   [WT]  "RankMixer 详解（1）：特征分组与完整计算流程", section 3.1 (the
+ *         element map of TokenMixing), section 3.3 (LayerNorm definition),
+ *         section 4.1 (GELU = u*Phi(u), row-vector FFN), section 5.1 (mean
+ *         pooling).
+ *
+ * Conventions (all arrays row-major, double):
+ *   X      [B][T][D]        token matrix per sample
+ *   W1     [T][D][F]        per-token first layer, u = s W1 + b1   (F = kD)
+ *   b1     [T][F]
+ *   W2     [T][F][D]        per-token second layer, v = a W2 + b2
+ *   b2     [T][D]
+ *   g1,be1,g2,be2 [D]       LayerNorm affine, one pair per LN, shared by tokens
+ *
+ * Every function is a direct loop nest over the definition.  The only
+ * concession to speed is an OpenMP loop over independent samples.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdlib.h>
+#include <string.h>
+
+#if defined(_OPENMP)
+#include <omp.h>
+#endif
+
+#define ORACLE_API __attribute__((visibility("default")))
+
+/* ------------------------------------------------------------------ */
+/* TokenMixing, [RM] Eq. 3-4 and [WT] section 3.1:                     */
+/*   SplitHead cuts each token x_t into H contiguous blocks of q = D/H; */
+/*   mixed row h is Concat(x_1^h, ..., x_T^h), so                       */
+/*   M[h][t*q + r] = X[t][h*q + r]   (0-based t, h, r).                 */
+/* Output is [H][T*q]; with H = T it has the input's shape [T][D].      */
+/* ------------------------------------------------------------------ */
+static void mix_sample(const double *X, double *M, int T, int D, int H)
+{
+    const int q = D / H;
+    for (int h = 0; h < H; ++h)
+        for (int t = 0; t < T; ++t)
+            for (int r = 0; r < q; ++r)
+                M[(size_t)h * T * q + (size_t)t * q + r] = X[(size_t)t * D + (size_t)h * q + r];
+}
+
+ORACLE_API void oracle_token_mix(const double *X, double *M, int B, int T, int D, int H)
+{
+    const size_t per = (size_t)T * D;
+    for (int b = 0; b < B; ++b)
+        mix_sample(X + b * per, M + b * per, T, D, H);
+}
+
+/* ------------------------------------------------------------------ */
+/* LayerNorm over one row of length D, [WT] section 3.3:               */
+/*   mu = (1/D) sum r_j,  var = (1/D) sum (r_j - mu)^2  (biased),       */
+/*   out_j = gamma_j (r_j - mu) / sqrt(var + eps) + beta_j.             */
+/* ------------------------------------------------------------------ */
+static void layernorm_row(const double *r, const double *gamma, const double *beta,
+                          double eps, double *out, int D)
+{
+    double mu = 0.0;
+    for (int j = 0; j < D; ++j) mu += r[j];
+    mu /= (double)D;
+    double var = 0.0;
+    for (int j = 0; j < D; ++j) var += (r[j] - mu) * (r[j] - mu);
+    var /= (double)D;
+    const double inv = 1.0 / sqrt(var + eps);
+    for (int j = 0; j < D; ++j) out[j] = gamma[j] * (r[j] - mu) * inv + beta[j];
+}
+
+ORACLE_API void oracle_layernorm(const double *R, const double *gamma, const double *beta,
+                                 double eps, double *out, int rows, int D)
+{
+    for (int i = 0; i < rows; ++i)
+        layernorm_row(R + (size_t)i * D, gamma, beta, eps, out + (size_t)i * D, D);
+}
+
+/* GELU, [WT] section 4.1: Gelu(u) = u * Phi(u), Phi the standard normal CDF,
+ * Phi(u) = (1 + erf(u / sqrt 2)) / 2. */
+static double gelu(double u)
+{
+    return u * 0.5 * (1.0 + erf(u / sqrt(2.0)));
+}
+
+ORACLE_API void oracle_gelu(const double *u, double *out, size_t n)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = gelu(u[i]);
+}
+
+/* One two-layer FFN on a row vector, [RM] Eq. 6-7:
+ *   u = s W1 + b1 (length F), a = Gelu(u), v = a W2 + b2 (length D). */
+static void ffn_row(const double *s, const double *W1, const double *b1,
+                    const double *W2, const double *b2, double *v, double *a_scratch,
+                    int D, int F)
+{
+    for (int j = 0; j < F; ++j) {
+        double u = b1[j];
+        for (int i = 0; i < D; ++i) u += s[i] * W1[(size_t)i * F + j];
+        a_scratch[j] = gelu(u);
+    }
+    for (int j = 0; j < D; ++j) {
+        double acc = b2[j];
+        for (int i = 0; i < F; ++i) acc += a_scratch[i] * W2[(size_t)i * D + j];
+        v[j] = acc;
+    }
+}
+
+/* Per-token FFN on one sample, [RM] Eq. 8-9: token t uses its own weights. */
+ORACLE_API void oracle_pffn(const double *S, const double *W1, const double *b1,
+                            const double *W2, const double *b2, double *V,
+                            int B, int T, int D, int F)
+{
+#pragma omp parallel
+    {
+        double *a = (double *)malloc(sizeof(double) * (size_t)F);
+#pragma omp for schedule(static)
+        for (int b = 0; b < B; ++b)
+            for (int t = 0; t < T; ++t) {
+                const size_t row = ((size_t)b * T + t) * D;
+                ffn_row(S + row, W1 + (size_t)t * D * F, b1 + (size_t)t * F,
+                        W2 + (size_t)t * F * D, b2 + (size_t)t * D, V + row, a, D, F);
+            }
+        free(a);
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* One RankMixer block on one sample, [RM] Eq. 1:                       */
+/*   S  = LN1(TokenMixing(X) + X)                                       */
+/*   X' = LN2(PFFN(S) + S)                                              */
+/* S_out may be NULL.  Requires H = T (the residual needs equal shape). */
+/* ------------------------------------------------------------------ */
+static void block_sample(const double *X, double *Xout, double *S_keep,
+                         const double *W1, const double *b1, const double *W2, const double *b2,
+                         const double *g1, const double *be1, const double *g2, const double *be2,
+                         double eps, int T, int D, int F, double *work)
+{
+    const size_t TD = (size_t)T * D;
+    double *M = work;            /* [T][D] mixed   */
+    double *S = M + TD;          /* [T][D] LN1 out */
+    double *Y = S + TD;          /* [T][D] residual sums */
+    double *a = Y + TD;          /* [F]   hidden   */
+    double *v = a + F;           /* [D]   FFN out  */
+
+    mix_sample(X, M, T, D, T);
+    for (size_t i = 0; i < TD; ++i) Y[i] = M[i] + X[i];
+    for (int t = 0; t < T; ++t) layernorm_row(Y + (size_t)t * D, g1, be1, eps, S + (size_t)t * D, D);
+
+    for (int t = 0; t < T; ++t) {
+        ffn_row(S + (size_t)t * D, W1 + (size_t)t * D * F, b1 + (size_t)t * F,
+                W2 + (size_t)t * F * D, b2 + (size_t)t * D, v, a, D, F);
+        for (int j = 0; j < D; ++j) Y[(size_t)t * D + j] = v[j] + S[(size_t)t * D + j];
+        layernorm_row(Y + (size_t)t * D, g2, be2, eps, Xout + (size_t)t * D, D);
+    }
+    if (S_keep) memcpy(S_keep, S, sizeof(double) * TD);
+}
+
+ORACLE_API void oracle_block_forward(const double *X, double *Xout, double *S_out,
+                                     const double *W1, const double *b1,
+                                     const double *W2, const double *b2,
+                                     const double *g1, const double *be1,
+                                     const double *g2, const double *be2,
+                                     double eps, int B, int T, int D, int F)
+{
+    const size_t TD = (size_t)T * D;
+#pragma omp parallel
+    {
+        double *work = (double *)malloc(sizeof(double) * (3 * TD + (size_t)F + (size_t)D));
+#pragma omp for schedule(static)
+        for (int b = 0; b < B; ++b)
+            block_sample(X + b * TD, Xout + b * TD, S_out ? S_out + b * TD : NULL,
+                         W1, b1, W2, b2, g1, be1, g2, be2, eps, T, D, F, work);
+        free(work);
+    }
+}
+
+/* Mean pooling, [RM] section 3.1 / [WT] section 5.1: o = (1/T) sum_t X_L[t,:]. */
+ORACLE_API void oracle_mean_pool(const double *X, double *o, int B, int T, int D)
+{
+    for (int b = 0; b < B; ++b)
+        for (int j = 0; j < D; ++j) {
+            double acc = 0.0;
+            for (int t = 0; t < T; ++t) acc += X[((size_t)b * T + t) * D + j];
+            o[(size_t)b * D + j] = acc / (double)T;
+        }
+}
+
+/* ------------------------------------------------------------------ */
+/* L stacked blocks with independent per-layer weights ([RM] Eq. 1 and  */
+/* the factor L in Eq. 12), then mean pooling.  Per-layer parameter     */
+/* arrays are concatenated along a leading layer axis.  XL may be NULL. */
+/* ------------------------------------------------------------------ */
+ORACLE_API void oracle_stack_forward(const double *X0, double *pooled, double *XL,
+                                     const double *W1, const double *b1,
+                                     const double *W2, const double *b2,
+                                     const double *g1, const double *be1,
+                                     const double *g2, const double *be2,
+                                     double eps, int B, int T, int D, int F, int L)
+{
+    const size_t TD = (size_t)T * D;
+#pragma omp parallel
+    {
+        double *work = (double *)malloc(sizeof(double) * (3 * TD + (size_t)F + (size_t)D));
+        double *cur = (double *)malloc(sizeof(double) * TD);
+        double *nxt = (double *)malloc(sizeof(double) * TD);
+#pragma omp for schedule(static)
+        for (int b = 0; b < B; ++b) {
+            memcpy(cur, X0 + b * TD, sizeof(double) * TD);
+            for (int n = 0; n < L; ++n) {
+                block_sample(cur, nxt, NULL,
+                             W1 + (size_t)n * T * D * F, b1 + (size_t)n * T * F,
+                             W2 + (size_t)n * T * F * D, b2 + (size_t)n * T * D,
+                             g1 + (size_t)n * D, be1 + (size_t)n * D,
+                             g2 + (size_t)n * D, be2 + (size_t)n * D,
+                             eps, T, D, F, work);
+                double *tmp = cur; cur = nxt; nxt = tmp;
+            }
+            for (int j = 0; j < D; ++j) {
+                double acc = 0.0;
+                for (int t = 0; t < T; ++t) acc += cur[(size_t)t * D + j];
+                pooled[(size_t)b * D + j] = acc / (double)T;
+            }
+            if (XL) memcpy(XL + b * TD, cur, sizeof(double) * TD);
+        }
+        free(work); free(cur); free(nxt);
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Sparse-MoE PFFN with ReLU routing, [RM] section 3.4 Eq. 10:          */
+/*   G[t][e] = ReLU(h_t(s_t))  with the inference router h_t linear:   */
+/*             h_t(s) = s Wg_t + bg_t,  Wg_t [D][E], bg_t [E];          */
+/*   v_t = sum_e G[t][e] * FFN_{t,e}(s_t), every expert a two-layer     */
+/*   GELU FFN D -> Fe -> D owned by token t alone.                      */
+/* All experts are evaluated densely; a zero gate contributes exactly 0.*/
+/*   S [B][T][D], Wg [T][D][E], bg [T][E], eW1 [T][E][D][Fe],           */
+/*   eb1 [T][E][Fe], eW2 [T][E][Fe][D], eb2 [T][E][D];                  */
+/*   V [B][T][D], G [B][T][E] (G may be NULL).                          */
+/* ------------------------------------------------------------------ */
+ORACLE_API void oracle_moe_pffn(const double *S, const double *Wg, const double *bg,
+                                const double *eW1, const double *eb1,
+                                const double *eW2, const double *eb2,
+                                double *V, double *G, int B, int T, int D, int E, int Fe)
+{
+#pragma omp parallel
+    {
+        double *a = (double *)malloc(sizeof(double) * (size_t)Fe);
+        double *v = (double *)malloc(sizeof(double) * (size_t)D);
+        double *g = (double *)malloc(sizeof(double) * (size_t)E);
+#pragma omp for schedule(static)
+        for (int b = 0; b < B; ++b)
+            for (int t = 0; t < T; ++t) {
+                const double *s = S + ((size_t)b * T + t) * D;
+                double *out = V + ((size_t)b * T + t) * D;
+                for (int e = 0; e < E; ++e) {
+                    double h = bg[(size_t)t * E + e];
+                    for (int i = 0; i < D; ++i) h += s[i] * Wg[((size_t)t * D + i) * E + e];
+                    g[e] = h > 0.0 ? h : 0.0;
+                    if (G) G[((size_t)b * T + t) * E + e] = g[e];
+                }
+                for (int j = 0; j < D; ++j) out[j] = 0.0;
+                for (int e = 0; e < E; ++e) {
+                    const size_t te = (size_t)t * E + e;
+                    ffn_row(s, eW1 + te * D * Fe, eb1 + te * Fe, eW2 + te * Fe * D, eb2 + te * D,
+                            v, a, D, Fe);
+                    for (int j = 0; j < D; ++j) out[j] += g[e] * v[j];
+                }
+            }
+        free(a); free(v); free(g);
+    }
+}
+
+ORACLE_API int oracle_num_threads(void)
+{
+#if defined(_OPENMP)
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+ORACLE_API void oracle_set_num_threads(int n)
+{
+#if defined(_OPENMP)
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
