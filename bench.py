@@ -1,0 +1,366 @@
+"""Throughput of the RankMixer block-stack forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--config rankmixer_1b|rankmixer_100m|moe_1b] [--batch B]
+
+Prints ONE JSON line on rank 0.  A step is one forward pass of the whole hot
+path (L x [token mixing + LN1, per-token FFN GEMM1 + GELU, GEMM2 + residual +
+LN2 statistics], LN2 finalisation + mean pooling) over one batch of
+synthetic input resident in HBM.  `value` = samples/s of the whole job
+(weak scaling: every rank processes its own batch of B samples).  `e2e` is
+the same metric through rm_stack_forward_host (pinned host input, H2D copy,
+forward, D2H of the pooled output inside the timed region).
+
+--impl reference times the CPU oracle (the plain float64 restatement used by
+the tests) on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_BYTES = 129 * 1024 * 1024
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_PATH) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], None, [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------------------------
+# Distributed helpers (one process per GPU; weak scaling, no data-path collective)
+# ----------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def shard_batch(global_batch: int, world: int, rank: int) -> tuple[int, int]:
+    """[start, stop) of the samples rank `rank` owns when `global_batch` samples are split
+    as evenly as possible over `world` ranks (first ranks take the remainder)."""
+    base, rem = divmod(global_batch, world)
+    start = rank * base + min(rank, rem)
+    return start, start + base + (1 if rank < rem else 0)
+
+
+# ----------------------------------------------------------------------------
+# Our arm
+# ----------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from rankmixer_feature_interaction_gb300 import synth
+    from rankmixer_feature_interaction_gb300.api import RankMixer
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    c = dict(synth.CONFIGS[args.config])
+    B = args.batch or c["B"]
+    T, D, k = c["T"], c["D"], c["k"]
+    moe = args.config == "moe_1b"
+    L = c["L"]
+    E, Fe = c.get("E", 0), c.get("Fe", 0)
+    seed = 20260101 + 17 * rank
+    layers = synth.make_stack(T, D, k, L, 4242, "bf16", dev, E=E, Fe=Fe, active=c.get("active", 2.0))
+    m = RankMixer(T, D, k, layers, dtype="bf16", max_batch=B, n_experts=E, expert_hidden=Fe)
+    del layers
+    torch.cuda.empty_cache()
+    X0 = synth.make_input(B, T, D, seed, "bf16", dev)
+    pooled = torch.empty((B, D), dtype=torch.float32, device=dev)
+    S_in = X0  # MoE PFFN input (an LN1 output in the model; same distribution class for timing)
+    V = torch.empty((B, T, D), dtype=torch.float32, device=dev) if moe else None
+
+    def step():
+        if moe:
+            m.moe_pffn_forward(0, S_in, V)
+        else:
+            m.stack_forward(X0, pooled)
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    m.profile(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms_total = ev0.elapsed_time(ev1)
+    kstats = m.profile_read()
+    m.profile(False)
+    clk = clocks.stop()
+    status = m.sync_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+
+    # max over ranks
+    t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    ms_step = ms_max / args.steps
+    samples_per_s = world * B * args.steps / (ms_max / 1e3)
+
+    # ---- e2e through the host-buffer entry point -----------------------------------
+    e2e = None
+    if not moe:
+        Xh = X0.cpu().pin_memory()
+        ph = torch.empty((B, D), dtype=torch.float32).pin_memory()
+        for _ in range(2):
+            m.stack_forward_host(Xh, ph)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            m.stack_forward_host(Xh, ph)
+        t1 = time.perf_counter()
+        tt = torch.tensor([t1 - t0], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e = {"value": round(world * B * args.steps / float(tt.item()), 2), "unit": "samples/s",
+               "h2d_bytes_per_step": int(Xh.numel() * Xh.element_size()),
+               "d2h_bytes_per_step": int(ph.numel() * ph.element_size())}
+
+    # ---- roofline of the dominant kernel ------------------------------------------
+    peaks, peak_src = load_peaks()
+    flops_gemm = 2.0 * B * T * D * (k * D)          # one GEMM launch of the dense PFFN (either layer)
+    gemm_kinds = ["moe_gemm1", "moe_gemm2"] if moe else ["gemm1", "gemm2"]
+    dom = max(gemm_kinds, key=lambda kk: kstats[kk][1])
+    launches, tot_ms = kstats[dom]
+    if moe:
+        # algorithmic flops of the launch class: active rows x 2 D Fe per expert layer
+        active_rows = None
+        flops_launch = None
+    else:
+        flops_launch = flops_gemm
+    roofline = None
+    if launches > 0 and flops_launch:
+        avg_ms = tot_ms / launches
+        achieved = flops_launch / (avg_ms / 1e3) / 1e12
+        peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+        roofline = {"kernel": f"pffn_{dom}_tcgen05", "bound": "tensor", "achieved": round(achieved, 1),
+                    "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                    "peak_source": f"{peak_src} bf16_tflops_sustained",
+                    "avg_launch_ms": round(avg_ms, 4)}
+    flops_step = 4.0 * k * L * T * D * D * B
+    gpu_launches = int(sum(v[0] for kk, v in kstats.items() if kk != "misc"))
+
+    out = {
+        "metric": "samples/s (RankMixer-1B-shape block stack fwd)" if args.config == "rankmixer_1b"
+        else f"samples/s ({args.config} {'MoE PFFN' if moe else 'block stack'} fwd)",
+        "value": round(samples_per_s, 2),
+        "unit": "samples/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) inputs, N(0,1/fan_in) weights; random-init)",
+        "config": {"workload": f"{args.config} B={B} T={T} D={D} k={k} L={L}" + (f" E={E} Fe={Fe}" if moe else ""),
+                   "batch_per_gpu": B, "global_batch": B * world, "parallelism": f"replicas x{world} (batch sharded)",
+                   "l2": "inputs larger than L2 (X0 %.0f MB, weights %.0f MB > 129 MB)" % (
+                       X0.numel() * 2 / 1e6, m.info.weight_bytes / 1e6)},
+        "tflops": None if moe else round(flops_step * args.steps * world / (ms_max / 1e3) / 1e12, 1),
+        "frac_of_peak_step": None if moe else round(
+            flops_step * args.steps / (ms_max / 1e3) / 1e12 / peaks.get("bf16_tflops_sustained", 1700.0), 4),
+        "roofline": roofline,
+        "kernels_ms_per_step": {kk: round(v[1] / args.steps, 4) for kk, v in kstats.items() if v[0]},
+        "gpu_launches": gpu_launches,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(args.config, B, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    m.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample)
+# ----------------------------------------------------------------------------
+def cpu_baseline(config: str, B_full: int, seconds: float, n_steps: int = 1) -> dict:
+    import numpy as np
+
+    import oracle
+    from rankmixer_feature_interaction_gb300 import synth
+
+    c = synth.CONFIGS[config]
+    T, D, k, L = c["T"], c["D"], c["k"], c["L"]
+    moe = config == "moe_1b"
+    layers = synth.to_f64(synth.make_stack(T, D, k, L, 4242, "bf16", "cpu", E=c.get("E", 0), Fe=c.get("Fe", 0),
+                                           active=c.get("active", 2.0)))
+    cores = oracle.num_threads()
+
+    def run(nb):
+        X = synth.to_f64(synth.make_input(nb, T, D, 99, "bf16", "cpu"))
+        t0 = time.perf_counter()
+        if moe:
+            p = layers[0]
+            oracle.moe_pffn(X, p["Wg"], p["bg"], p["eW1"], p["eb1"], p["eW2"], p["eb2"])
+        else:
+            oracle.stack_forward(X, layers)
+        return time.perf_counter() - t0
+
+    probe_n = max(1, cores)
+    dt = run(probe_n)
+    per_sample = dt / probe_n
+    nb = int(max(probe_n, min(4096, (seconds * 0.7) / max(per_sample, 1e-9))))
+    nb = max(probe_n, (nb // probe_n) * probe_n)
+    total_t, total_n = 0.0, 0
+    for _ in range(n_steps):
+        total_t += run(nb)
+        total_n += nb
+    return {"value": round(total_n / total_t, 3), "unit": "samples/s", "cores": cores, "kind": "oracle",
+            "sample": f"{nb} samples of the {config} workload per step (of B={B_full}), float64 oracle, "
+                      f"OpenMP over samples on {cores} host threads, {n_steps} step(s), {total_t:.1f} s"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from rankmixer_feature_interaction_gb300 import synth
+    c = synth.CONFIGS[args.config]
+    B = args.batch or c["B"]
+    steps = max(1, args.steps)
+    # each step is a bounded sample; the whole run is kept to a few minutes
+    per_step_s = min(args.cpu_seconds, 150.0 / (steps + args.warmup))
+    cb = cpu_baseline(args.config, B, per_step_s, n_steps=steps)
+    out = {
+        "impl": "reference",
+        "metric": "samples/s (RankMixer-1B-shape block stack fwd)" if args.config == "rankmixer_1b"
+        else f"samples/s ({args.config})",
+        "value": cb["value"], "unit": "samples/s", "n_gpus": world, "steps": steps, "warmup": args.warmup,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": f"{args.config} B={B} T={c['T']} D={c['D']} k={c['k']} L={c['L']}"},
+        "cpu_baseline": cb,
+        "e2e": {"value": cb["value"], "unit": "samples/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=["rankmixer_1b", "rankmixer_100m", "moe_1b"], default="rankmixer_1b")
+    ap.add_argument("--batch", type=int, default=0, help="override the batch per GPU")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU oracle budget per measurement")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,229 @@
+/*
+ * rankmixer.h -- C ABI of librankmixer.so, a GB300 (sm_103a) implementation of
+ * the RankMixer block forward.
+ *
+ * What is computed (per sample, X_n in R^{T x D}, H = T heads of q = D/H):
+ *   S_{n-1} = LN1(TokenMixing(X_{n-1}) + X_{n-1})
+ *   X_n     = LN2(PFFN(S_{n-1}) + S_{n-1})                      n = 1..L
+ *   o       = (1/T) sum_t X_L[t, :]
+ * "RankMixer: Scaling Up Ranking Models in Industrial Recommenders", section
+ * 3.1 Eq. 1 (block), section 3.3.1 Eq. 3-5 (TokenMixing with H = T), section
+ * 3.3.2 Eq. 6-9 (per-token FFN, row-vector convention u = s W + b, GELU),
+ * section 3.4 Eq. 10 (ReLU-routed Sparse-MoE variant); "RankMixer 详解（1）"
+ * section 3.1 (element map [Mix(X)]_{h, t q + r} = X_{t, h q + r}), section
+ * 3.3 (LayerNorm with biased variance, eps inside the square root) and
+ * section 4.1 (Gelu(u) = u Phi(u)).
+ *
+ * Conventions shared by every call:
+ *   - Activation tensors are row-major [B][T][D] in the context's dtype
+ *     (RM_BF16: __nv_bfloat16 bits, RM_F32: float).  The pooled output and
+ *     the MoE PFFN output are always float32.
+ *   - Pointers named "device" must be CUDA device (or managed) memory of the
+ *     context's device; pointers named "host" must be host memory (pinned for
+ *     full copy speed).  Device pointers must be 16-byte aligned.
+ *   - "stream" is a cudaStream_t passed as void*; NULL means the legacy
+ *     default stream.  Calls taking a stream are asynchronous on it unless
+ *     stated otherwise; the caller keeps inputs alive and unmodified until the
+ *     stream has passed the call.
+ *   - Every call returns an rm_status.  RM_OK means the work was enqueued
+ *     (or done, for synchronous calls).  On any other status nothing was
+ *     enqueued past the failing launch and rm_last_error() describes why.
+ *     No call aborts the process, throws, or prints.
+ *   - Errors detected on the device (a bounded wait that ran out) are latched
+ *     in a per-context error word and reported by the next rm_sync_status().
+ *   - One context may be used by one host thread / one stream at a time; its
+ *     workspace is shared by all calls on it.
+ */
+#ifndef RANKMIXER_H_
+#define RANKMIXER_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RM_ABI_VERSION 1
+
+/* Public symbols are the only ones the shared library exports. */
+#if defined(__GNUC__)
+#define RM_API __attribute__((visibility("default")))
+#else
+#define RM_API
+#endif
+
+typedef enum rm_status {
+    RM_OK = 0,
+    RM_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, bad layer index */
+    RM_ERR_UNSUPPORTED = 2,  /* configuration the method or this build does not cover (e.g. H != T) */
+    RM_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed; message in rm_last_error() */
+    RM_ERR_OOM = 4,          /* device or pinned-host allocation failed */
+    RM_ERR_TIMEOUT = 5,      /* a device-side bounded wait ran out (reported by rm_sync_status) */
+    RM_ERR_DEVICE = 6        /* any other device-side error flag */
+} rm_status;
+
+typedef enum rm_dtype {
+    RM_F32 = 0,   /* float32 activations and weights, float32 arithmetic */
+    RM_BF16 = 1   /* bfloat16 activations and weights, float32 accumulation */
+} rm_dtype;
+
+typedef enum rm_gemm_path {
+    RM_PATH_AUTO = 0,     /* tcgen05 tensor-core GEMMs when dtype and shape allow, else SIMT */
+    RM_PATH_SIMT = 1,     /* CUDA-core GEMMs (any shape, both dtypes) */
+    RM_PATH_TCGEN05 = 2   /* require the tcgen05/TMEM path; RM_ERR_UNSUPPORTED if not possible */
+} rm_gemm_path;
+
+/* Model shape.  T tokens of width D, H heads (must equal T: the residual in
+ * Eq. 5 needs the mixed matrix to keep the [T][D] shape), FFN expansion k
+ * (hidden width kD), L stacked blocks.  n_experts > 0 enables the Sparse-MoE
+ * PFFN (rm_moe_pffn_forward) with experts of hidden width expert_hidden;
+ * moe_layer_mask bit n makes layer n's PFFN the MoE variant inside
+ * rm_block_forward / rm_stack_forward.  ln_eps is the LayerNorm epsilon
+ * (1e-5 in the pages' worked example).  max_batch bounds B for every call
+ * and sizes the context's workspace. */
+typedef struct rm_config {
+    int T;
+    int D;
+    int H;
+    int k;
+    int L;
+    int n_experts;
+    int expert_hidden;
+    unsigned moe_layer_mask;
+    rm_dtype dtype;
+    float ln_eps;
+    int max_batch;
+    rm_gemm_path gemm_path;
+} rm_config;
+
+/* Parameters of one layer, as DEVICE pointers in the context's dtype, laid
+ * out as the pages write them (row-vector convention, u = s W1 + b1):
+ *   W1 [T][D][kD], b1 [T][kD], W2 [T][kD][D], b2 [T][D]    ("RankMixer" Eq. 7)
+ *   ln1_gamma, ln1_beta, ln2_gamma, ln2_beta [D]            (one pair per LN,
+ *                                                            shared by tokens)
+ * Sparse-MoE (only read when n_experts > 0), "RankMixer" Eq. 10:
+ *   Wg [T][D][E], bg [T][E]              router h_t(s) = s Wg_t + bg_t, gate ReLU(h)
+ *   eW1 [T][E][D][Fe], eb1 [T][E][Fe]    expert first layer (Fe = expert_hidden)
+ *   eW2 [T][E][Fe][D], eb2 [T][E][D]     expert second layer
+ * rm_create copies and repacks everything it needs; the caller may free
+ * these buffers once rm_create has returned. */
+typedef struct rm_layer_params {
+    const void *W1, *b1, *W2, *b2;
+    const void *ln1_gamma, *ln1_beta, *ln2_gamma, *ln2_beta;
+    const void *Wg, *bg;
+    const void *eW1, *eb1, *eW2, *eb2;
+} rm_layer_params;
+
+typedef struct rm_ctx rm_ctx;
+
+/* Static facts about a context. */
+typedef struct rm_info {
+    long long params_per_layer;      /* 2 k T D^2 + biases + LN ("RankMixer" Eq. 12, dense part) */
+    long long flops_per_sample;      /* 4 k L T D^2: GEMM flops of the dense stack (Eq. 12) */
+    long long weight_bytes;          /* bytes of packed weights held on the device */
+    long long workspace_bytes;       /* bytes of activation workspace held on the device */
+    int gemm_path;                   /* rm_gemm_path actually used (SIMT or TCGEN05) */
+    int num_sms;
+    int device;
+} rm_info;
+
+/* Kernel classes for rm_profile_read. */
+typedef enum rm_kernel_kind {
+    RM_K_MIX_LN1 = 0,    /* token mixing + residual + LN1 (and the previous layer's LN2) */
+    RM_K_GEMM1 = 1,      /* per-token FFN layer 1 + bias + GELU */
+    RM_K_GEMM2 = 2,      /* per-token FFN layer 2 + bias + residual + LN2 row statistics */
+    RM_K_LN2_OUT = 3,    /* LN2 finalisation into a [B][T][D] output */
+    RM_K_POOL = 4,       /* last LN2 finalisation + mean pooling */
+    RM_K_ROWSTATS = 5,   /* LN2 row statistics (SIMT path only) */
+    RM_K_MOE_ROUTE = 6,  /* router GEMV + ReLU + per-(token, expert) compaction */
+    RM_K_MOE_GEMM1 = 7,  /* expert layer 1 + bias + GELU on gathered rows */
+    RM_K_MOE_GEMM2 = 8,  /* expert layer 2 + bias, gated scatter-add */
+    RM_K_MISC = 9,       /* copies, layout changes */
+    RM_K_COUNT = 10
+} rm_kernel_kind;
+
+typedef struct rm_kernel_stat {
+    long long launches;
+    double total_ms;
+} rm_kernel_stat;
+
+/* ---------------------------------------------------------------------- */
+
+/* Create a context on `device`: validates cfg, allocates workspace for
+ * cfg->max_batch samples, repacks the L layers' parameters (layers[0..L-1])
+ * into device-resident K-major tiles.  Synchronous.  Errors:
+ * RM_ERR_INVALID_ARG (null pointers, non-positive sizes, D % H != 0),
+ * RM_ERR_UNSUPPORTED (H != T, or RM_PATH_TCGEN05 requested for a shape or
+ * dtype it cannot take), RM_ERR_OOM, RM_ERR_CUDA.  On error *out is NULL. */
+RM_API rm_status rm_create(const rm_config *cfg, const rm_layer_params *layers, int device, rm_ctx **out);
+
+/* Release everything the context owns (synchronises its device first). NULL is a no-op. */
+RM_API rm_status rm_destroy(rm_ctx *ctx);
+
+/* One block ("RankMixer" Eq. 1) of layer `layer`: X_out = LN2(PFFN(S) + S) with
+ * S = LN1(Mix(X_in) + X_in).  X_in, X_out: device [B][T][D]; they may not
+ * overlap.  S_out (nullable): device [B][T][D] receives S in the context
+ * dtype.  1 <= B <= max_batch. */
+RM_API rm_status rm_block_forward(rm_ctx *ctx, int layer, const void *X_in, void *X_out, void *S_out,
+                           int B, void *stream);
+
+/* The whole stack and the mean pooling ("RankMixer" section 3.1): pooled
+ * (device float32 [B][D]) = mean_t X_L; XL (nullable, device [B][T][D]) receives
+ * X_L.  X0: device [B][T][D].  Equal, bit for bit, to chaining rm_block_forward
+ * over the layers and averaging the last output in float32 in token order. */
+RM_API rm_status rm_stack_forward(rm_ctx *ctx, const void *X0, float *pooled, void *XL, int B, void *stream);
+
+/* rm_stack_forward from HOST buffers: copies X0_host ([B][T][D], context dtype)
+ * to the device, runs the stack, copies the pooled float32 [B][D] result to
+ * pooled_host.  Returns after the result is in pooled_host (synchronises the
+ * stream).  Uses context-owned device staging buffers. */
+RM_API rm_status rm_stack_forward_host(rm_ctx *ctx, const void *X0_host, float *pooled_host, int B, void *stream);
+
+/* Sparse-MoE per-token FFN of layer `layer` ("RankMixer" Eq. 10, inference
+ * router): V[b,t] = sum_e G[b,t,e] * FFN_{t,e}(S[b,t]) with
+ * G = ReLU(S[b,t] Wg_t + bg_t).  Only experts with G > 0 are computed.
+ * S: device [B][T][D] (context dtype).  V_out: device float32 [B][T][D].
+ * gates (nullable): device float32 [B][T][E] receives G.  Requires
+ * cfg.n_experts > 0. */
+RM_API rm_status rm_moe_pffn_forward(rm_ctx *ctx, int layer, const void *S, float *V_out, float *gates,
+                              int B, void *stream);
+
+/* Standalone TokenMixing ("RankMixer" Eq. 3-4): Y[b][h][t q + r] = X[b][t][h q + r],
+ * q = D / H, for any H dividing D (Y is [B][H][T q]).  A pure permutation of
+ * element bits, exact for both dtypes.  X, Y: device, non-overlapping. */
+RM_API rm_status rm_token_mix(const void *X, void *Y, int B, int T, int D, int H, rm_dtype dtype, void *stream);
+
+/* Synchronise `stream`, then report and clear the context's device error
+ * word: RM_OK, RM_ERR_TIMEOUT or RM_ERR_DEVICE (or RM_ERR_CUDA if the
+ * synchronisation itself failed). */
+RM_API rm_status rm_sync_status(rm_ctx *ctx, void *stream);
+
+/* Fill *out with static facts about the context. */
+RM_API rm_status rm_get_info(const rm_ctx *ctx, rm_info *out);
+
+/* Per-kernel timing with CUDA events recorded around each launch on the
+ * launch stream.  rm_profile_enable(ctx, 1) starts collecting;
+ * rm_profile_read synchronises the recorded events, writes RM_K_COUNT
+ * entries to stats (launch count and summed milliseconds since the last
+ * read) and resets the counters. */
+RM_API rm_status rm_profile_enable(rm_ctx *ctx, int on);
+RM_API rm_status rm_profile_read(rm_ctx *ctx, rm_kernel_stat *stats);
+
+/* Test hook for failure detection: launches one kernel that waits on a
+ * device flag nothing sets, with a bounded wait of timeout_us microseconds;
+ * when the wait runs out the kernel latches RM_ERR_TIMEOUT in the context's
+ * error word and returns.  The next rm_sync_status() reports it. */
+RM_API rm_status rm_debug_wait_timeout(rm_ctx *ctx, int timeout_us, void *stream);
+
+/* Message of the last failing call on this host thread ("" if none). */
+RM_API const char *rm_last_error(void);
+
+/* ABI version of the loaded library (RM_ABI_VERSION). */
+RM_API int rm_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RANKMIXER_H_ */

@@ -98,20 +98,25 @@ ORACLE_API void oracle_gelu(const double *u, double *out, size_t n)
 }
 
 /* One two-layer FFN on a row vector, [RM] Eq. 6-7:
- *   u = s W1 + b1 (length F), a = Gelu(u), v = a W2 + b2 (length D). */
+ *   u = s W1 + b1 (length F), a = Gelu(u), v = a W2 + b2 (length D).
+ * Each output starts from its bias and adds the products in ascending input
+ * index; the loops run over W's rows so the matrices are read in order. */
 static void ffn_row(const double *s, const double *W1, const double *b1,
                     const double *W2, const double *b2, double *v, double *a_scratch,
                     int D, int F)
 {
-    for (int j = 0; j < F; ++j) {
-        double u = b1[j];
-        for (int i = 0; i < D; ++i) u += s[i] * W1[(size_t)i * F + j];
-        a_scratch[j] = gelu(u);
+    for (int j = 0; j < F; ++j) a_scratch[j] = b1[j];
+    for (int i = 0; i < D; ++i) {
+        const double si = s[i];
+        const double *w = W1 + (size_t)i * F;
+        for (int j = 0; j < F; ++j) a_scratch[j] += si * w[j];
     }
-    for (int j = 0; j < D; ++j) {
-        double acc = b2[j];
-        for (int i = 0; i < F; ++i) acc += a_scratch[i] * W2[(size_t)i * D + j];
-        v[j] = acc;
+    for (int j = 0; j < F; ++j) a_scratch[j] = gelu(a_scratch[j]);
+    for (int j = 0; j < D; ++j) v[j] = b2[j];
+    for (int i = 0; i < F; ++i) {
+        const double ai = a_scratch[i];
+        const double *w = W2 + (size_t)i * D;
+        for (int j = 0; j < D; ++j) v[j] += ai * w[j];
     }
 }
 

@@ -1,0 +1,180 @@
+"""ctypes binding of librankmixer.so (include/rankmixer.h), names unchanged.
+
+Argument marshalling only: every function forwards to the C entry point of
+the same name.  Loading fails loudly when the library has not been built --
+there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "librankmixer.so")
+
+# rm_status
+RM_OK = 0
+RM_ERR_INVALID_ARG = 1
+RM_ERR_UNSUPPORTED = 2
+RM_ERR_CUDA = 3
+RM_ERR_OOM = 4
+RM_ERR_TIMEOUT = 5
+RM_ERR_DEVICE = 6
+STATUS_NAMES = {0: "RM_OK", 1: "RM_ERR_INVALID_ARG", 2: "RM_ERR_UNSUPPORTED", 3: "RM_ERR_CUDA",
+                4: "RM_ERR_OOM", 5: "RM_ERR_TIMEOUT", 6: "RM_ERR_DEVICE"}
+
+# rm_dtype
+RM_F32 = 0
+RM_BF16 = 1
+
+# rm_gemm_path
+RM_PATH_AUTO = 0
+RM_PATH_SIMT = 1
+RM_PATH_TCGEN05 = 2
+
+# rm_kernel_kind
+KERNEL_KINDS = ["mix_ln1", "gemm1", "gemm2", "ln2_out", "pool", "rowstats", "moe_route", "moe_gemm1",
+                "moe_gemm2", "misc"]
+RM_K_COUNT = len(KERNEL_KINDS)
+
+EXPORTED = ["rm_create", "rm_destroy", "rm_block_forward", "rm_stack_forward", "rm_stack_forward_host",
+            "rm_moe_pffn_forward", "rm_token_mix", "rm_sync_status", "rm_get_info", "rm_profile_enable",
+            "rm_profile_read", "rm_debug_wait_timeout", "rm_last_error", "rm_abi_version"]
+
+
+class rm_config(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int), ("D", ctypes.c_int), ("H", ctypes.c_int), ("k", ctypes.c_int),
+                ("L", ctypes.c_int), ("n_experts", ctypes.c_int), ("expert_hidden", ctypes.c_int),
+                ("moe_layer_mask", ctypes.c_uint), ("dtype", ctypes.c_int), ("ln_eps", ctypes.c_float),
+                ("max_batch", ctypes.c_int), ("gemm_path", ctypes.c_int)]
+
+
+class rm_layer_params(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("W1", "b1", "W2", "b2", "ln1_gamma", "ln1_beta", "ln2_gamma",
+                                               "ln2_beta", "Wg", "bg", "eW1", "eb1", "eW2", "eb2")]
+
+
+class rm_info(ctypes.Structure):
+    _fields_ = [("params_per_layer", ctypes.c_longlong), ("flops_per_sample", ctypes.c_longlong),
+                ("weight_bytes", ctypes.c_longlong), ("workspace_bytes", ctypes.c_longlong),
+                ("gemm_path", ctypes.c_int), ("num_sms", ctypes.c_int), ("device", ctypes.c_int)]
+
+
+class rm_kernel_stat(ctypes.Structure):
+    _fields_ = [("launches", ctypes.c_longlong), ("total_ms", ctypes.c_double)]
+
+
+class RankMixerError(RuntimeError):
+    def __init__(self, status: int, where: str, msg: str):
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Load librankmixer.so; raise if it is missing (build it with __graft_entry__.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"librankmixer.so not built at {LIB_PATH}; run `python -c 'import __graft_entry__ as g; "
+                           f"g.build()'` (there is no non-CUDA fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i, st = ctypes.c_void_p, ctypes.c_int, ctypes.c_int
+    sig = {
+        "rm_create": (st, [ctypes.POINTER(rm_config), ctypes.POINTER(rm_layer_params), i, ctypes.POINTER(vp)]),
+        "rm_destroy": (st, [vp]),
+        "rm_block_forward": (st, [vp, i, vp, vp, vp, i, vp]),
+        "rm_stack_forward": (st, [vp, vp, vp, vp, i, vp]),
+        "rm_stack_forward_host": (st, [vp, vp, vp, i, vp]),
+        "rm_moe_pffn_forward": (st, [vp, i, vp, vp, vp, i, vp]),
+        "rm_token_mix": (st, [vp, vp, i, i, i, i, i, vp]),
+        "rm_sync_status": (st, [vp, vp]),
+        "rm_get_info": (st, [vp, ctypes.POINTER(rm_info)]),
+        "rm_profile_enable": (st, [vp, i]),
+        "rm_profile_read": (st, [vp, ctypes.POINTER(rm_kernel_stat)]),
+        "rm_debug_wait_timeout": (st, [vp, i, vp]),
+        "rm_last_error": (ctypes.c_char_p, []),
+        "rm_abi_version": (i, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def check(status: int, where: str) -> None:
+    if status != RM_OK:
+        msg = load().rm_last_error()
+        raise RankMixerError(status, where, msg.decode() if msg else "")
+
+
+# ---- thin wrappers with the C names (pointers are ints, streams are ints) ----
+
+def rm_create(cfg: rm_config, layers, device: int = 0) -> int:
+    arr = (rm_layer_params * len(layers))(*layers)
+    out = ctypes.c_void_p()
+    check(load().rm_create(ctypes.byref(cfg), arr, device, ctypes.byref(out)), "rm_create")
+    return out.value
+
+
+def rm_destroy(ctx: int) -> None:
+    check(load().rm_destroy(ctx), "rm_destroy")
+
+
+def rm_block_forward(ctx: int, layer: int, X_in: int, X_out: int, S_out: int | None, B: int, stream: int) -> None:
+    check(load().rm_block_forward(ctx, layer, X_in, X_out, S_out, B, stream), "rm_block_forward")
+
+
+def rm_stack_forward(ctx: int, X0: int, pooled: int, XL: int | None, B: int, stream: int) -> None:
+    check(load().rm_stack_forward(ctx, X0, pooled, XL, B, stream), "rm_stack_forward")
+
+
+def rm_stack_forward_host(ctx: int, X0_host: int, pooled_host: int, B: int, stream: int) -> None:
+    check(load().rm_stack_forward_host(ctx, X0_host, pooled_host, B, stream), "rm_stack_forward_host")
+
+
+def rm_moe_pffn_forward(ctx: int, layer: int, S: int, V_out: int, gates: int | None, B: int, stream: int) -> None:
+    check(load().rm_moe_pffn_forward(ctx, layer, S, V_out, gates, B, stream), "rm_moe_pffn_forward")
+
+
+def rm_token_mix(X: int, Y: int, B: int, T: int, D: int, H: int, dtype: int, stream: int) -> None:
+    check(load().rm_token_mix(X, Y, B, T, D, H, dtype, stream), "rm_token_mix")
+
+
+def rm_sync_status(ctx: int, stream: int) -> int:
+    """Returns the raw status (RM_OK, RM_ERR_TIMEOUT, ...) without raising."""
+    return load().rm_sync_status(ctx, stream)
+
+
+def rm_get_info(ctx: int) -> rm_info:
+    info = rm_info()
+    check(load().rm_get_info(ctx, ctypes.byref(info)), "rm_get_info")
+    return info
+
+
+def rm_profile_enable(ctx: int, on: bool) -> None:
+    check(load().rm_profile_enable(ctx, 1 if on else 0), "rm_profile_enable")
+
+
+def rm_profile_read(ctx: int) -> dict:
+    arr = (rm_kernel_stat * RM_K_COUNT)()
+    check(load().rm_profile_read(ctx, arr), "rm_profile_read")
+    return {KERNEL_KINDS[k]: (arr[k].launches, arr[k].total_ms) for k in range(RM_K_COUNT)}
+
+
+def rm_debug_wait_timeout(ctx: int, timeout_us: int, stream: int) -> None:
+    check(load().rm_debug_wait_timeout(ctx, timeout_us, stream), "rm_debug_wait_timeout")
+
+
+def rm_last_error() -> str:
+    m = load().rm_last_error()
+    return m.decode() if m else ""
+
+
+def rm_abi_version() -> int:
+    return load().rm_abi_version()

@@ -1,0 +1,130 @@
+"""Torch-facing wrapper over the C ABI: allocates output tensors with torch and
+passes raw pointers and the current CUDA stream to librankmixer.so.  No
+arithmetic of the method happens here; every step runs in the CUDA kernels.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+
+_DENSE_KEYS = ("W1", "b1", "W2", "b2", "ln1_g", "ln1_b", "ln2_g", "ln2_b")
+_MOE_KEYS = ("Wg", "bg", "eW1", "eb1", "eW2", "eb2")
+_C_NAMES = {"W1": "W1", "b1": "b1", "W2": "W2", "b2": "b2", "ln1_g": "ln1_gamma", "ln1_b": "ln1_beta",
+            "ln2_g": "ln2_gamma", "ln2_b": "ln2_beta", "Wg": "Wg", "bg": "bg", "eW1": "eW1", "eb1": "eb1",
+            "eW2": "eW2", "eb2": "eb2"}
+_DTYPES = {"bf16": (torch.bfloat16, _lib.RM_BF16), "f32": (torch.float32, _lib.RM_F32)}
+_PATHS = {"auto": _lib.RM_PATH_AUTO, "simt": _lib.RM_PATH_SIMT, "tcgen05": _lib.RM_PATH_TCGEN05}
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to librankmixer must be contiguous")
+    return t.data_ptr()
+
+
+class RankMixer:
+    """A RankMixer block stack held on one GPU (one rm_ctx).
+
+    layers: list of L dicts of contiguous tensors on `device` in `dtype` with the
+    pages' layout -- W1 [T,D,kD], b1 [T,kD], W2 [T,kD,D], b2 [T,D], ln1_g/ln1_b/
+    ln2_g/ln2_b [D]; with experts also Wg [T,D,E], bg [T,E], eW1 [T,E,D,Fe],
+    eb1 [T,E,Fe], eW2 [T,E,Fe,D], eb2 [T,E,D].  The tensors may be freed after
+    construction (the library keeps packed copies)."""
+
+    def __init__(self, T: int, D: int, k: int, layers: list, dtype: str = "bf16", eps: float = 1e-5,
+                 max_batch: int = 4096, n_experts: int = 0, expert_hidden: int = 0, moe_layer_mask: int = 0,
+                 gemm_path: str = "auto", device: int = 0):
+        self.tdtype, cdtype = _DTYPES[dtype]
+        self.T, self.D, self.k, self.L = T, D, k, len(layers)
+        self.E = n_experts
+        self.max_batch = max_batch
+        self.device = torch.device("cuda", device)
+        cfg = _lib.rm_config(T=T, D=D, H=T, k=k, L=len(layers), n_experts=n_experts, expert_hidden=expert_hidden,
+                             moe_layer_mask=moe_layer_mask, dtype=cdtype, ln_eps=eps, max_batch=max_batch,
+                             gemm_path=_PATHS[gemm_path])
+        cl = []
+        for p in layers:
+            lp = _lib.rm_layer_params()
+            for k_ in _DENSE_KEYS + (_MOE_KEYS if n_experts > 0 else ()):
+                setattr(lp, _C_NAMES[k_], _ptr(p[k_]))
+            cl.append(lp)
+        torch.cuda.synchronize(self.device)
+        self.ctx = _lib.rm_create(cfg, cl, device)
+        self.info = _lib.rm_get_info(self.ctx)
+
+    # -- lifetime --------------------------------------------------------------
+    def close(self) -> None:
+        if getattr(self, "ctx", None):
+            _lib.rm_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def path(self) -> str:
+        return "tcgen05" if self.info.gemm_path == _lib.RM_PATH_TCGEN05 else "simt"
+
+    # -- forward calls -----------------------------------------------------------
+    def block_forward(self, layer: int, X: torch.Tensor, out: torch.Tensor | None = None, return_S: bool = False):
+        B = X.shape[0]
+        out = torch.empty_like(X) if out is None else out
+        S = torch.empty_like(X) if return_S else None
+        _lib.rm_block_forward(self.ctx, layer, _ptr(X), _ptr(out), _ptr(S), B, _stream())
+        return (out, S) if return_S else out
+
+    def stack_forward(self, X0: torch.Tensor, pooled: torch.Tensor | None = None, return_XL: bool = False):
+        B = X0.shape[0]
+        pooled = torch.empty((B, self.D), dtype=torch.float32, device=X0.device) if pooled is None else pooled
+        XL = torch.empty_like(X0) if return_XL else None
+        _lib.rm_stack_forward(self.ctx, _ptr(X0), _ptr(pooled), _ptr(XL), B, _stream())
+        return (pooled, XL) if return_XL else pooled
+
+    def stack_forward_host(self, X0_host: torch.Tensor, pooled_host: torch.Tensor | None = None) -> torch.Tensor:
+        """X0_host: CPU tensor (pinned for full speed); returns the pooled CPU float32 [B, D]."""
+        B = X0_host.shape[0]
+        if pooled_host is None:
+            pooled_host = torch.empty((B, self.D), dtype=torch.float32, pin_memory=X0_host.is_pinned())
+        _lib.rm_stack_forward_host(self.ctx, _ptr(X0_host), _ptr(pooled_host), B, _stream())
+        return pooled_host
+
+    def moe_pffn_forward(self, layer: int, S: torch.Tensor, V: torch.Tensor | None = None,
+                         return_gates: bool = False):
+        B = S.shape[0]
+        V = torch.empty(S.shape, dtype=torch.float32, device=S.device) if V is None else V
+        G = torch.empty((B, self.T, self.E), dtype=torch.float32, device=S.device) if return_gates else None
+        _lib.rm_moe_pffn_forward(self.ctx, layer, _ptr(S), _ptr(V), _ptr(G), B, _stream())
+        return (V, G) if return_gates else V
+
+    # -- status / profiling --------------------------------------------------------
+    def sync_status(self) -> int:
+        return _lib.rm_sync_status(self.ctx, _stream())
+
+    def profile(self, on: bool = True) -> None:
+        _lib.rm_profile_enable(self.ctx, on)
+
+    def profile_read(self) -> dict:
+        return _lib.rm_profile_read(self.ctx)
+
+    def debug_wait_timeout(self, timeout_us: int) -> None:
+        _lib.rm_debug_wait_timeout(self.ctx, timeout_us, _stream())
+
+
+def token_mix(X: torch.Tensor, H: int | None = None) -> torch.Tensor:
+    """Y[b, h, t q + r] = X[b, t, h q + r]; X [B, T, D] (bf16 or f32) on the GPU."""
+    B, T, D = X.shape
+    H = T if H is None else H
+    Y = torch.empty((B, H, T * (D // H)), dtype=X.dtype, device=X.device)
+    dt = _lib.RM_BF16 if X.dtype == torch.bfloat16 else _lib.RM_F32
+    _lib.rm_token_mix(_ptr(X), _ptr(Y), B, T, D, H, dt, _stream())
+    return Y

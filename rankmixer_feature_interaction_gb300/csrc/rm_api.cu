@@ -1,0 +1,597 @@
+// C-ABI of librankmixer.so: context creation (validation, weight packing,
+// workspace), the block / stack / MoE entry points, error reporting and the
+// per-kernel event timer.  Declared in include/rankmixer.h.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/rankmixer.h"
+#include "rm_internal.h"
+#include "rm_moe.h"
+
+using namespace rm;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+rm_status fail(rm_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+rm_status cuda_fail(cudaError_t e, const char* what) {
+    if (e == cudaErrorMemoryAllocation) return fail(RM_ERR_OOM, "%s: %s", what, cudaGetErrorString(e));
+    if (e == cudaErrorNotSupported) return fail(RM_ERR_UNSUPPORTED, "%s: shape not supported by this kernel", what);
+    return fail(RM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define RM_CHECK_CUDA(expr, what)                  \
+    do {                                           \
+        cudaError_t _e = (expr);                   \
+        if (_e != cudaSuccess) return cuda_fail(_e, what); \
+    } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Default bound of every device-side wait (2 s of global time).
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
+
+struct LayerW {
+    void* W1p = nullptr;   // [T][F][D]  (K-major for GEMM1)
+    void* W2p = nullptr;   // [T][D][F]  (K-major for GEMM2)
+    float* b1 = nullptr;   // [T][F]
+    float* b2 = nullptr;   // [T][D]
+    float* g1 = nullptr;
+    float* be1 = nullptr;
+    float* g2 = nullptr;
+    float* be2 = nullptr;
+    MoeWeights moe;
+};
+
+struct Event {
+    cudaEvent_t a, b;
+};
+
+}  // namespace
+
+struct rm_ctx {
+    rm_config cfg{};
+    int device = 0;
+    int num_sms = 0;
+    Act act = Act::BF16;
+    size_t esz = 2;
+    int F = 0;           // kD
+    bool use_tc = false;
+    int nchunk = 1, cw = 0;
+    std::vector<LayerW> layers;
+    // workspace (token-major)
+    int Bcap = 0;
+    void* S = nullptr;
+    void* Hid = nullptr;
+    float* Z = nullptr;
+    float2* stats = nullptr;
+    float* V = nullptr;          // MoE PFFN output inside the stack
+    MoeWorkspace moe_ws;
+    // host-entry staging
+    void* X0_dev = nullptr;
+    float* pooled_dev = nullptr;
+    // error word and the debug flag nothing sets
+    int* d_err = nullptr;
+    int* d_flag = nullptr;
+    long long weight_bytes = 0, ws_bytes = 0;
+    // profiling
+    bool prof = false;
+    std::vector<Event> ev_pool;
+    std::vector<std::pair<int, int>> ev_used;   // (kind, pool index)
+    std::vector<cudaEvent_t> spare;
+};
+
+namespace {
+
+rm_status dmalloc(rm_ctx* c, void** p, size_t bytes, long long* counter) {
+    *p = nullptr;
+    if (bytes == 0) return RM_OK;
+    cudaError_t e = cudaMalloc(p, bytes);
+    if (e != cudaSuccess) {
+        *p = nullptr;
+        cudaGetLastError();
+        return fail(RM_ERR_OOM, "cudaMalloc(%zu bytes) failed: %s", bytes, cudaGetErrorString(e));
+    }
+    if (counter) *counter += (long long)bytes;
+    (void)c;
+    return RM_OK;
+}
+
+void free_ctx(rm_ctx* c) {
+    if (!c) return;
+    cudaSetDevice(c->device);
+    cudaDeviceSynchronize();
+    for (auto& l : c->layers) {
+        cudaFree(l.W1p); cudaFree(l.W2p); cudaFree(l.b1); cudaFree(l.b2);
+        cudaFree(l.g1); cudaFree(l.be1); cudaFree(l.g2); cudaFree(l.be2);
+        moe_free_weights(l.moe);
+    }
+    moe_free_workspace(c->moe_ws);
+    cudaFree(c->S); cudaFree(c->Hid); cudaFree(c->Z); cudaFree(c->stats); cudaFree(c->V);
+    cudaFree(c->X0_dev); cudaFree(c->pooled_dev);
+    cudaFree(c->d_err); cudaFree(c->d_flag);
+    for (auto& e : c->ev_pool) { cudaEventDestroy(e.a); cudaEventDestroy(e.b); }
+    delete c;
+}
+
+// ---- profiling --------------------------------------------------------------
+struct ProfScope {
+    rm_ctx* c;
+    int kind;
+    cudaStream_t s;
+    int idx = -1;
+    ProfScope(rm_ctx* c_, int kind_, cudaStream_t s_) : c(c_), kind(kind_), s(s_) {
+        if (!c->prof) return;
+        if (c->ev_used.size() >= c->ev_pool.size()) {
+            Event e;
+            if (cudaEventCreate(&e.a) != cudaSuccess || cudaEventCreate(&e.b) != cudaSuccess) return;
+            c->ev_pool.push_back(e);
+        }
+        idx = (int)c->ev_used.size();
+        c->ev_used.push_back({kind, idx});
+        cudaEventRecord(c->ev_pool[idx].a, s);
+    }
+    ~ProfScope() {
+        if (idx >= 0) cudaEventRecord(c->ev_pool[idx].b, s);
+    }
+};
+
+rm_status validate_cfg(const rm_config* cfg) {
+    if (!cfg) return fail(RM_ERR_INVALID_ARG, "cfg is NULL");
+    if (cfg->T < 1 || cfg->D < 1 || cfg->H < 1 || cfg->k < 1 || cfg->L < 1 || cfg->max_batch < 1)
+        return fail(RM_ERR_INVALID_ARG, "T, D, H, k, L and max_batch must be positive");
+    if (cfg->D % cfg->H != 0) return fail(RM_ERR_INVALID_ARG, "D (%d) must be divisible by H (%d)", cfg->D, cfg->H);
+    if (cfg->H != cfg->T)
+        return fail(RM_ERR_UNSUPPORTED, "H (%d) must equal T (%d): the mixing residual needs a [T][D] result",
+                    cfg->H, cfg->T);
+    if (cfg->dtype != RM_F32 && cfg->dtype != RM_BF16) return fail(RM_ERR_INVALID_ARG, "unknown dtype");
+    if (!(cfg->ln_eps >= 0.f) || !std::isfinite(cfg->ln_eps)) return fail(RM_ERR_INVALID_ARG, "ln_eps must be >= 0");
+    if (cfg->L > 32) return fail(RM_ERR_UNSUPPORTED, "at most 32 layers");
+    if (cfg->T > 128) return fail(RM_ERR_UNSUPPORTED, "at most 128 tokens");
+    const size_t esz = cfg->dtype == RM_F32 ? 4 : 2;
+    if ((size_t)cfg->T * cfg->D * esz > 200 * 1024)
+        return fail(RM_ERR_UNSUPPORTED, "a sample (T*D elements) must fit 200 KB of shared memory");
+    const int q = cfg->D / cfg->H;
+    const bool vec2 = (q % 2 == 0) && (cfg->D % 64 == 0);
+    if ((vec2 && cfg->D > 3072) || (!vec2 && cfg->D > 1536))
+        return fail(RM_ERR_UNSUPPORTED, "D too large for the mixing kernel");
+    if (cfg->gemm_path != RM_PATH_AUTO && cfg->gemm_path != RM_PATH_SIMT && cfg->gemm_path != RM_PATH_TCGEN05)
+        return fail(RM_ERR_INVALID_ARG, "unknown gemm_path");
+    if (cfg->n_experts < 0 || (cfg->n_experts > 0 && cfg->expert_hidden < 1))
+        return fail(RM_ERR_INVALID_ARG, "n_experts > 0 needs expert_hidden >= 1");
+    if (cfg->n_experts == 0 && cfg->moe_layer_mask != 0)
+        return fail(RM_ERR_INVALID_ARG, "moe_layer_mask set without experts");
+    if (cfg->n_experts > kMoeMaxExperts) return fail(RM_ERR_UNSUPPORTED, "at most %d experts", kMoeMaxExperts);
+    return RM_OK;
+}
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+rm_status check_ctx(const rm_ctx* c) {
+    if (!c) return fail(RM_ERR_INVALID_ARG, "ctx is NULL");
+    return RM_OK;
+}
+
+rm_status check_batch(const rm_ctx* c, int B) {
+    if (B < 1 || B > c->Bcap) return fail(RM_ERR_INVALID_ARG, "B (%d) must be in [1, max_batch=%d]", B, c->Bcap);
+    return RM_OK;
+}
+
+// ---- the block steps ---------------------------------------------------------
+rm_status run_pffn(rm_ctx* c, int layer, int B, cudaStream_t s) {
+    const LayerW& w = c->layers[layer];
+    const rm_config& g = c->cfg;
+    if (g.moe_layer_mask & (1u << layer)) {
+        // Sparse-MoE PFFN: V = sum_e gate * expert(S), then Z = V + S and row statistics.
+        rm_status st = RM_OK;
+        {
+            MoeLaunch ml{c->act, c->S, /*S sample-major*/ false, g.T, g.D, g.n_experts, g.expert_hidden, B,
+                         c->Bcap, c->num_sms, c->d_err};
+            cudaError_t e = moe_forward(ml, w.moe, c->moe_ws, c->V, /*V token-major*/ true, nullptr, s,
+                                        [&](int kind) { return (void*)new ProfScope(c, kind, s); },
+                                        [](void* p) { delete (ProfScope*)p; });
+            if (e != cudaSuccess) st = cuda_fail(e, "moe pffn");
+        }
+        if (st != RM_OK) return st;
+        ProfScope ps(c, RM_K_GEMM2, s);
+        RM_CHECK_CUDA(moe_residual_z(c->act, c->V, c->S, c->Z, B, g.T, g.D, c->Bcap, s), "moe residual");
+        ProfScope ps2(c, RM_K_ROWSTATS, s);
+        RM_CHECK_CUDA(launch_rowstats(c->Z, c->stats, B, g.T, g.D, c->Bcap, c->num_sms, s), "row stats");
+        return RM_OK;
+    }
+    if (c->use_tc) {
+        {
+            ProfScope ps(c, RM_K_GEMM1, s);
+            cudaError_t e = launch_gemm1_tc(c->S, w.W1p, w.b1, c->Hid, B, g.T, g.D, c->F, c->Bcap, c->num_sms,
+                                            c->d_err, kWaitTimeoutNs, s);
+            if (e != cudaSuccess) return cuda_fail(e, (std::string("gemm1 (tcgen05) ") + tc_last_error()).c_str());
+        }
+        {
+            ProfScope ps(c, RM_K_GEMM2, s);
+            cudaError_t e = launch_gemm2_tc(c->Hid, w.W2p, w.b2, c->S, c->Z, c->stats, B, g.T, g.D, c->F, c->Bcap,
+                                            c->num_sms, c->d_err, kWaitTimeoutNs, s);
+            if (e != cudaSuccess) return cuda_fail(e, (std::string("gemm2 (tcgen05) ") + tc_last_error()).c_str());
+        }
+    } else {
+        {
+            ProfScope ps(c, RM_K_GEMM1, s);
+            RM_CHECK_CUDA(launch_gemm1_simt(c->act, c->S, w.W1p, w.b1, c->Hid, B, g.T, g.D, c->F, c->Bcap, s),
+                          "gemm1 (simt)");
+        }
+        {
+            ProfScope ps(c, RM_K_GEMM2, s);
+            RM_CHECK_CUDA(launch_gemm2_simt(c->act, c->Hid, w.W2p, w.b2, c->S, c->Z, B, g.T, g.D, c->F, c->Bcap, s),
+                          "gemm2 (simt)");
+        }
+        ProfScope ps(c, RM_K_ROWSTATS, s);
+        RM_CHECK_CUDA(launch_rowstats(c->Z, c->stats, B, g.T, g.D, c->Bcap, c->num_sms, s), "row stats");
+    }
+    return RM_OK;
+}
+
+int layer_nchunk(const rm_ctx* c, int layer) {
+    const bool moe = (c->cfg.moe_layer_mask & (1u << layer)) != 0;
+    return (c->use_tc && !moe) ? c->nchunk : 1;
+}
+int layer_cw(const rm_ctx* c, int layer) {
+    const bool moe = (c->cfg.moe_layer_mask & (1u << layer)) != 0;
+    return (c->use_tc && !moe) ? c->cw : c->cfg.D;
+}
+
+MixLnArgs mix_args(const rm_ctx* c, int layer, int B) {
+    MixLnArgs a{};
+    const rm_config& g = c->cfg;
+    a.S = c->S;
+    a.g1 = c->layers[layer].g1;
+    a.be1 = c->layers[layer].be1;
+    a.B = B;
+    a.T = g.T;
+    a.D = g.D;
+    a.q = g.D / g.H;
+    a.Bcap = c->Bcap;
+    a.eps = g.ln_eps;
+    return a;
+}
+
+rm_status stack_device(rm_ctx* c, const void* X0, float* pooled, void* XL, int B, cudaStream_t s) {
+    const rm_config& g = c->cfg;
+    for (int n = 0; n < g.L; ++n) {
+        MixLnArgs a = mix_args(c, n, B);
+        if (n == 0) {
+            a.X = X0;
+            ProfScope ps(c, RM_K_MIX_LN1, s);
+            RM_CHECK_CUDA(launch_mix_ln1(c->act, false, a, c->num_sms, s), "mix+ln1");
+        } else {
+            a.Z = c->Z;
+            a.stats = c->stats;
+            a.g2 = c->layers[n - 1].g2;
+            a.be2 = c->layers[n - 1].be2;
+            a.nchunk = layer_nchunk(c, n - 1);
+            a.cw = layer_cw(c, n - 1);
+            ProfScope ps(c, RM_K_MIX_LN1, s);
+            RM_CHECK_CUDA(launch_mix_ln1(c->act, true, a, c->num_sms, s), "ln2+mix+ln1");
+        }
+        rm_status st = run_pffn(c, n, B, s);
+        if (st != RM_OK) return st;
+    }
+    const int last = g.L - 1;
+    ProfScope ps(c, RM_K_POOL, s);
+    RM_CHECK_CUDA(launch_pool(c->act, c->Z, c->stats, c->layers[last].g2, c->layers[last].be2, pooled, XL, B, g.T,
+                              g.D, c->Bcap, layer_nchunk(c, last), layer_cw(c, last), g.ln_eps, c->num_sms, s),
+                  "ln2+pool");
+    return RM_OK;
+}
+
+rm_status pack_layer(rm_ctx* c, const rm_layer_params& p, LayerW& w, cudaStream_t s) {
+    const rm_config& g = c->cfg;
+    const int T = g.T, D = g.D, F = c->F;
+    if (!p.W1 || !p.b1 || !p.W2 || !p.b2 || !p.ln1_gamma || !p.ln1_beta || !p.ln2_gamma || !p.ln2_beta)
+        return fail(RM_ERR_INVALID_ARG, "a dense layer parameter pointer is NULL");
+    rm_status st;
+    if ((st = dmalloc(c, &w.W1p, (size_t)T * F * D * c->esz, &c->weight_bytes)) != RM_OK) return st;
+    if ((st = dmalloc(c, &w.W2p, (size_t)T * D * F * c->esz, &c->weight_bytes)) != RM_OK) return st;
+    if ((st = dmalloc(c, (void**)&w.b1, (size_t)T * F * 4, &c->weight_bytes)) != RM_OK) return st;
+    if ((st = dmalloc(c, (void**)&w.b2, (size_t)T * D * 4, &c->weight_bytes)) != RM_OK) return st;
+    float** lnp[4] = {&w.g1, &w.be1, &w.g2, &w.be2};
+    const void* lns[4] = {p.ln1_gamma, p.ln1_beta, p.ln2_gamma, p.ln2_beta};
+    for (int i = 0; i < 4; ++i)
+        if ((st = dmalloc(c, (void**)lnp[i], (size_t)D * 4, &c->weight_bytes)) != RM_OK) return st;
+    // W1 [T][D][F] -> W1p [T][F][D];  W2 [T][F][D] -> W2p [T][D][F]
+    RM_CHECK_CUDA(launch_transpose(p.W1, w.W1p, T, D, F, (int)c->esz, s), "pack W1");
+    RM_CHECK_CUDA(launch_transpose(p.W2, w.W2p, T, F, D, (int)c->esz, s), "pack W2");
+    RM_CHECK_CUDA(launch_to_f32(c->act, p.b1, w.b1, (size_t)T * F, s), "pack b1");
+    RM_CHECK_CUDA(launch_to_f32(c->act, p.b2, w.b2, (size_t)T * D, s), "pack b2");
+    for (int i = 0; i < 4; ++i) RM_CHECK_CUDA(launch_to_f32(c->act, lns[i], *lnp[i], (size_t)D, s), "pack LN");
+    if (g.n_experts > 0) {
+        if (!p.Wg || !p.bg || !p.eW1 || !p.eb1 || !p.eW2 || !p.eb2)
+            return fail(RM_ERR_INVALID_ARG, "a Sparse-MoE parameter pointer is NULL");
+        MoeShape ms{c->act, T, D, g.n_experts, g.expert_hidden};
+        cudaError_t e = moe_pack_weights(ms, p.Wg, p.bg, p.eW1, p.eb1, p.eW2, p.eb2, w.moe, &c->weight_bytes, s);
+        if (e != cudaSuccess) return cuda_fail(e, "pack MoE weights");
+    }
+    return RM_OK;
+}
+
+}  // namespace
+
+// =============================================================================
+// Public entry points
+// =============================================================================
+extern "C" {
+
+int rm_abi_version(void) { return RM_ABI_VERSION; }
+
+const char* rm_last_error(void) { return g_last_error.c_str(); }
+
+rm_status rm_create(const rm_config* cfg, const rm_layer_params* layers, int device, rm_ctx** out) {
+    g_last_error.clear();
+    if (!out) return fail(RM_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    rm_status st = validate_cfg(cfg);
+    if (st != RM_OK) return st;
+    if (!layers) return fail(RM_ERR_INVALID_ARG, "layers is NULL");
+    int ndev = 0;
+    RM_CHECK_CUDA(cudaGetDeviceCount(&ndev), "cudaGetDeviceCount");
+    if (device < 0 || device >= ndev) return fail(RM_ERR_INVALID_ARG, "device %d out of range (%d devices)", device, ndev);
+    RM_CHECK_CUDA(cudaSetDevice(device), "cudaSetDevice");
+    cudaDeviceProp prop;
+    RM_CHECK_CUDA(cudaGetDeviceProperties(&prop, device), "cudaGetDeviceProperties");
+    if (prop.major != 10 || prop.minor != 3)
+        return fail(RM_ERR_UNSUPPORTED, "this library is built for sm_103a only (device is sm_%d%d)", prop.major,
+                    prop.minor);
+
+    rm_ctx* c = new rm_ctx();
+    c->cfg = *cfg;
+    c->device = device;
+    c->num_sms = prop.multiProcessorCount;
+    c->act = cfg->dtype == RM_F32 ? Act::F32 : Act::BF16;
+    c->esz = act_size(c->act);
+    c->F = cfg->k * cfg->D;
+    const bool tc_ok = c->act == Act::BF16 && tc_supported(cfg->D, c->F);
+    if (cfg->gemm_path == RM_PATH_TCGEN05 && !tc_ok) {
+        delete c;
+        return fail(RM_ERR_UNSUPPORTED, "tcgen05 path needs bf16 and D, kD multiples of 64");
+    }
+    c->use_tc = tc_ok && cfg->gemm_path != RM_PATH_SIMT;
+    c->cw = c->use_tc ? tc_stats_chunk_width(cfg->D) : cfg->D;
+    c->nchunk = cfg->D / c->cw;
+    c->Bcap = cfg->max_batch;
+
+    const size_t T = cfg->T, D = cfg->D, F = c->F, Bc = c->Bcap;
+    if ((st = dmalloc(c, &c->S, T * Bc * D * c->esz, &c->ws_bytes)) != RM_OK ||
+        (st = dmalloc(c, &c->Hid, T * Bc * F * c->esz, &c->ws_bytes)) != RM_OK ||
+        (st = dmalloc(c, (void**)&c->Z, T * Bc * D * 4, &c->ws_bytes)) != RM_OK ||
+        (st = dmalloc(c, (void**)&c->stats, T * Bc * (size_t)c->nchunk * sizeof(float2), &c->ws_bytes)) != RM_OK ||
+        (st = dmalloc(c, (void**)&c->d_err, sizeof(int), nullptr)) != RM_OK ||
+        (st = dmalloc(c, (void**)&c->d_flag, sizeof(int), nullptr)) != RM_OK) {
+        free_ctx(c);
+        return st;
+    }
+    if (cfg->moe_layer_mask != 0 &&
+        (st = dmalloc(c, (void**)&c->V, T * Bc * D * 4, &c->ws_bytes)) != RM_OK) {
+        free_ctx(c);
+        return st;
+    }
+    if (cfg->n_experts > 0) {
+        MoeShape ms{c->act, cfg->T, cfg->D, cfg->n_experts, cfg->expert_hidden};
+        cudaError_t e = moe_alloc_workspace(ms, c->Bcap, c->moe_ws, &c->ws_bytes);
+        if (e != cudaSuccess) {
+            free_ctx(c);
+            return cuda_fail(e, "MoE workspace");
+        }
+    }
+    cudaMemset(c->d_err, 0, sizeof(int));
+    cudaMemset(c->d_flag, 0, sizeof(int));
+    c->layers.resize(cfg->L);
+    for (int n = 0; n < cfg->L; ++n) {
+        st = pack_layer(c, layers[n], c->layers[n], 0);
+        if (st != RM_OK) {
+            free_ctx(c);
+            return st;
+        }
+    }
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        free_ctx(c);
+        return cuda_fail(e, "rm_create");
+    }
+    *out = c;
+    return RM_OK;
+}
+
+rm_status rm_destroy(rm_ctx* ctx) {
+    if (!ctx) return RM_OK;
+    free_ctx(ctx);
+    return RM_OK;
+}
+
+rm_status rm_block_forward(rm_ctx* c, int layer, const void* X_in, void* X_out, void* S_out, int B, void* stream) {
+    rm_status st;
+    if ((st = check_ctx(c)) != RM_OK) return st;
+    if (layer < 0 || layer >= c->cfg.L) return fail(RM_ERR_INVALID_ARG, "layer %d out of range", layer);
+    if ((st = check_batch(c, B)) != RM_OK) return st;
+    if (!X_in || !X_out) return fail(RM_ERR_INVALID_ARG, "X_in / X_out is NULL");
+    if (!aligned16(X_in) || !aligned16(X_out) || (S_out && !aligned16(S_out)))
+        return fail(RM_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+    const size_t bytes = (size_t)B * c->cfg.T * c->cfg.D * c->esz;
+    const char* xi = (const char*)X_in;
+    const char* xo = (const char*)X_out;
+    if (xi < xo + bytes && xo < xi + bytes) return fail(RM_ERR_INVALID_ARG, "X_in and X_out overlap");
+    cudaSetDevice(c->device);
+    cudaStream_t s = as_stream(stream);
+    const rm_config& g = c->cfg;
+    MixLnArgs a = mix_args(c, layer, B);
+    a.X = X_in;
+    {
+        ProfScope ps(c, RM_K_MIX_LN1, s);
+        RM_CHECK_CUDA(launch_mix_ln1(c->act, false, a, c->num_sms, s), "mix+ln1");
+    }
+    if (S_out) {
+        ProfScope ps(c, RM_K_MISC, s);
+        RM_CHECK_CUDA(launch_token_to_sample(c->act, c->S, S_out, B, g.T, g.D, c->Bcap, s), "copy S");
+    }
+    if ((st = run_pffn(c, layer, B, s)) != RM_OK) return st;
+    ProfScope ps(c, RM_K_LN2_OUT, s);
+    RM_CHECK_CUDA(launch_ln2_out(c->act, c->Z, c->stats, c->layers[layer].g2, c->layers[layer].be2, X_out, B, g.T,
+                                 g.D, c->Bcap, layer_nchunk(c, layer), layer_cw(c, layer), g.ln_eps, c->num_sms, s),
+                  "ln2 out");
+    return RM_OK;
+}
+
+rm_status rm_stack_forward(rm_ctx* c, const void* X0, float* pooled, void* XL, int B, void* stream) {
+    rm_status st;
+    if ((st = check_ctx(c)) != RM_OK) return st;
+    if ((st = check_batch(c, B)) != RM_OK) return st;
+    if (!X0 || !pooled) return fail(RM_ERR_INVALID_ARG, "X0 / pooled is NULL");
+    if (!aligned16(X0) || !aligned16(pooled) || (XL && !aligned16(XL)))
+        return fail(RM_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+    cudaSetDevice(c->device);
+    return stack_device(c, X0, pooled, XL, B, as_stream(stream));
+}
+
+rm_status rm_stack_forward_host(rm_ctx* c, const void* X0_host, float* pooled_host, int B, void* stream) {
+    rm_status st;
+    if ((st = check_ctx(c)) != RM_OK) return st;
+    if ((st = check_batch(c, B)) != RM_OK) return st;
+    if (!X0_host || !pooled_host) return fail(RM_ERR_INVALID_ARG, "X0_host / pooled_host is NULL");
+    cudaSetDevice(c->device);
+    const rm_config& g = c->cfg;
+    if (!c->X0_dev) {
+        if ((st = dmalloc(c, &c->X0_dev, (size_t)c->Bcap * g.T * g.D * c->esz, &c->ws_bytes)) != RM_OK) return st;
+        if ((st = dmalloc(c, (void**)&c->pooled_dev, (size_t)c->Bcap * g.D * 4, &c->ws_bytes)) != RM_OK) return st;
+    }
+    cudaStream_t s = as_stream(stream);
+    const size_t in_bytes = (size_t)B * g.T * g.D * c->esz;
+    {
+        ProfScope ps(c, RM_K_MISC, s);
+        RM_CHECK_CUDA(cudaMemcpyAsync(c->X0_dev, X0_host, in_bytes, cudaMemcpyHostToDevice, s), "H2D X0");
+    }
+    if ((st = stack_device(c, c->X0_dev, c->pooled_dev, nullptr, B, s)) != RM_OK) return st;
+    {
+        ProfScope ps(c, RM_K_MISC, s);
+        RM_CHECK_CUDA(cudaMemcpyAsync(pooled_host, c->pooled_dev, (size_t)B * g.D * 4, cudaMemcpyDeviceToHost, s),
+                      "D2H pooled");
+    }
+    RM_CHECK_CUDA(cudaStreamSynchronize(s), "stream sync");
+    return RM_OK;
+}
+
+rm_status rm_moe_pffn_forward(rm_ctx* c, int layer, const void* S, float* V_out, float* gates, int B, void* stream) {
+    rm_status st;
+    if ((st = check_ctx(c)) != RM_OK) return st;
+    if (c->cfg.n_experts <= 0) return fail(RM_ERR_UNSUPPORTED, "context was created without experts");
+    if (layer < 0 || layer >= c->cfg.L) return fail(RM_ERR_INVALID_ARG, "layer %d out of range", layer);
+    if ((st = check_batch(c, B)) != RM_OK) return st;
+    if (!S || !V_out) return fail(RM_ERR_INVALID_ARG, "S / V_out is NULL");
+    if (!aligned16(S) || !aligned16(V_out) || (gates && !aligned16(gates)))
+        return fail(RM_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+    cudaSetDevice(c->device);
+    cudaStream_t s = as_stream(stream);
+    const rm_config& g = c->cfg;
+    MoeLaunch ml{c->act, S, /*S sample-major*/ true, g.T, g.D, g.n_experts, g.expert_hidden, B, c->Bcap, c->num_sms, c->d_err};
+    cudaError_t e = moe_forward(ml, c->layers[layer].moe, c->moe_ws, V_out, /*V token-major*/ false, gates, s,
+                                [&](int kind) { return (void*)new ProfScope(c, kind, s); },
+                                [](void* p) { delete (ProfScope*)p; });
+    if (e != cudaSuccess) return cuda_fail(e, "moe pffn");
+    return RM_OK;
+}
+
+rm_status rm_token_mix(const void* X, void* Y, int B, int T, int D, int H, rm_dtype dtype, void* stream) {
+    if (!X || !Y) return fail(RM_ERR_INVALID_ARG, "X / Y is NULL");
+    if (B < 1 || T < 1 || D < 1 || H < 1) return fail(RM_ERR_INVALID_ARG, "sizes must be positive");
+    if (D % H != 0) return fail(RM_ERR_INVALID_ARG, "D (%d) must be divisible by H (%d)", D, H);
+    if (dtype != RM_F32 && dtype != RM_BF16) return fail(RM_ERR_INVALID_ARG, "unknown dtype");
+    const int esz = dtype == RM_F32 ? 4 : 2;
+    const size_t bytes = (size_t)B * T * D * esz;
+    const char* x = (const char*)X;
+    const char* y = (const char*)Y;
+    if (x < y + bytes && y < x + bytes) return fail(RM_ERR_INVALID_ARG, "X and Y overlap");
+    RM_CHECK_CUDA(launch_token_mix(X, Y, B, T, D, H, esz, as_stream(stream)), "token mix");
+    return RM_OK;
+}
+
+rm_status rm_sync_status(rm_ctx* c, void* stream) {
+    rm_status st;
+    if ((st = check_ctx(c)) != RM_OK) return st;
+    cudaSetDevice(c->device);
+    RM_CHECK_CUDA(cudaStreamSynchronize(as_stream(stream)), "stream synchronize");
+    int code = 0;
+    RM_CHECK_CUDA(cudaMemcpy(&code, c->d_err, sizeof(int), cudaMemcpyDeviceToHost), "read error word");
+    if (code != 0) {
+        RM_CHECK_CUDA(cudaMemset(c->d_err, 0, sizeof(int)), "clear error word");
+        RM_CHECK_CUDA(cudaDeviceSynchronize(), "clear error word");
+        if (code == kDevErrTimeout) return fail(RM_ERR_TIMEOUT, "a device-side wait ran out of time");
+        return fail(RM_ERR_DEVICE, "device error code %d", code);
+    }
+    return RM_OK;
+}
+
+rm_status rm_get_info(const rm_ctx* c, rm_info* out) {
+    rm_status st;
+    if ((st = check_ctx(c)) != RM_OK) return st;
+    if (!out) return fail(RM_ERR_INVALID_ARG, "out is NULL");
+    const long long T = c->cfg.T, D = c->cfg.D, k = c->cfg.k, L = c->cfg.L;
+    out->params_per_layer = 2 * k * T * D * D + T * (k * D + D) + 4 * D;
+    out->flops_per_sample = 4 * k * L * T * D * D;
+    out->weight_bytes = c->weight_bytes;
+    out->workspace_bytes = c->ws_bytes;
+    out->gemm_path = c->use_tc ? RM_PATH_TCGEN05 : RM_PATH_SIMT;
+    out->num_sms = c->num_sms;
+    out->device = c->device;
+    return RM_OK;
+}
+
+rm_status rm_profile_enable(rm_ctx* c, int on) {
+    rm_status st;
+    if ((st = check_ctx(c)) != RM_OK) return st;
+    c->prof = on != 0;
+    return RM_OK;
+}
+
+rm_status rm_profile_read(rm_ctx* c, rm_kernel_stat* stats) {
+    rm_status st;
+    if ((st = check_ctx(c)) != RM_OK) return st;
+    if (!stats) return fail(RM_ERR_INVALID_ARG, "stats is NULL");
+    for (int k = 0; k < RM_K_COUNT; ++k) {
+        stats[k].launches = 0;
+        stats[k].total_ms = 0.0;
+    }
+    for (auto& u : c->ev_used) {
+        Event& e = c->ev_pool[u.second];
+        RM_CHECK_CUDA(cudaEventSynchronize(e.b), "event synchronize");
+        float ms = 0.f;
+        RM_CHECK_CUDA(cudaEventElapsedTime(&ms, e.a, e.b), "event elapsed");
+        stats[u.first].launches += 1;
+        stats[u.first].total_ms += ms;
+    }
+    c->ev_used.clear();
+    return RM_OK;
+}
+
+rm_status rm_debug_wait_timeout(rm_ctx* c, int timeout_us, void* stream) {
+    rm_status st;
+    if ((st = check_ctx(c)) != RM_OK) return st;
+    if (timeout_us < 1 || timeout_us > 10000000) return fail(RM_ERR_INVALID_ARG, "timeout_us out of range");
+    cudaSetDevice(c->device);
+    RM_CHECK_CUDA(launch_debug_wait(c->d_flag, c->d_err, (unsigned long long)timeout_us * 1000ull, as_stream(stream)),
+                  "debug wait");
+    return RM_OK;
+}
+
+}  // extern "C"

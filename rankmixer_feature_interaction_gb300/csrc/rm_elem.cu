@@ -1,0 +1,461 @@
+// Memory-bound kernels of the RankMixer block: TokenMixing fused with the
+// first residual and LayerNorm, the second LayerNorm's finalisation (into the
+// next layer's mixing, into a [B][T][D] output, or into mean pooling), and
+// the small layout/packing kernels used at context creation.
+//
+// "RankMixer: Scaling Up Ranking Models in Industrial Recommenders", section
+// 3.1 Eq. 1 and section 3.3.1 Eq. 3-5; "RankMixer 详解（1）" section 3.1 (the
+// element map of the mixing) and section 3.3 (LayerNorm).
+#include "rm_common.cuh"
+#include "rm_internal.h"
+
+namespace rm {
+namespace {
+
+constexpr int kMixThreads = 256;
+constexpr int kMixWarps = kMixThreads / 32;
+
+// LN affine applied to a finalised row element.  Every kernel that finalises
+// LN2 uses this exact expression so the stacked and block-by-block paths
+// agree bit for bit.
+__device__ __forceinline__ float ln_apply(float z, float mean, float rstd, float g, float b) {
+    const float n = (z - mean) * rstd;
+    return fmaf(n, g, b);
+}
+
+template <typename Tact> struct Vec2;
+template <> struct Vec2<float> {
+    using type = float2;
+    __device__ static float2 load(const float* p) { return *reinterpret_cast<const float2*>(p); }
+    __device__ static void store(float* p, float a, float b) { *reinterpret_cast<float2*>(p) = make_float2(a, b); }
+    __device__ static void split(float2 v, float& a, float& b) { a = v.x; b = v.y; }
+};
+template <> struct Vec2<__nv_bfloat16> {
+    __device__ static __nv_bfloat162 load(const __nv_bfloat16* p) {
+        return *reinterpret_cast<const __nv_bfloat162*>(p);
+    }
+    __device__ static void store(__nv_bfloat16* p, float a, float b) {
+        *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(a, b);
+    }
+    __device__ static void split(__nv_bfloat162 v, float& a, float& b) {
+        a = __low2float(v);
+        b = __high2float(v);
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Fused TokenMixing + residual + LN1.
+// One CTA per sample (grid-stride).  Phase 1 stages the sample's T x D
+// matrix X in shared memory (read from X, or finalised from the previous
+// layer's pre-LN2 rows Z).  Phase 2: one warp per output row h computes
+//   y[j] = X[t][h q + r] + X[h][j],  j = t q + r     (mix + residual)
+// keeps y in registers, reduces mean and biased variance with shuffles and
+// writes S[h] = LN1(y) token-major.
+// VEC = 2: each lane owns column pairs (needs q even, D % 64 == 0);
+// VEC = 1: each lane owns single columns (any q).  NI bounds D / (32 VEC).
+// ---------------------------------------------------------------------------
+template <typename Tact, bool FROM_Z, int VEC, int NI>
+__global__ void __launch_bounds__(kMixThreads)
+mix_ln1_kernel(const MixLnArgs a) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    Tact* xs = reinterpret_cast<Tact*>(smem_raw);   // [T][D]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int T = a.T, D = a.D, q = a.q;
+    const size_t TD = (size_t)T * D;
+    const Tact* X = reinterpret_cast<const Tact*>(a.X);
+    Tact* S = reinterpret_cast<Tact*>(a.S);
+    Tact* Xp = reinterpret_cast<Tact*>(a.Xprev_out);
+
+    for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
+        // ---- phase 1: stage X[b] ------------------------------------------
+        if (!FROM_Z) {
+            const Tact* src = X + (size_t)b * TD;
+            if (((TD * sizeof(Tact)) & 15) == 0) {
+                const uint4* s4 = reinterpret_cast<const uint4*>(src);
+                uint4* d4 = reinterpret_cast<uint4*>(xs);
+                const int n4 = (int)(TD * sizeof(Tact) / 16);
+                for (int i = threadIdx.x; i < n4; i += kMixThreads) d4[i] = __ldg(s4 + i);
+            } else {
+                for (int i = threadIdx.x; i < (int)TD; i += kMixThreads) xs[i] = src[i];
+            }
+        } else {
+            for (int t = warp; t < T; t += kMixWarps) {
+                const size_t row = (size_t)t * a.Bcap + b;
+                float mean, rstd;
+                merge_row_stats(a.stats + row * a.nchunk, a.nchunk, a.cw, D, a.eps, lane, mean, rstd);
+                const float* z = a.Z + row * D;
+                Tact* xd = xs + (size_t)t * D;
+                Tact* xo = Xp ? Xp + ((size_t)b * T + t) * D : nullptr;
+                for (int j = lane; j < D; j += 32) {
+                    const Tact v = from_f32<Tact>(ln_apply(z[j], mean, rstd, a.g2[j], a.be2[j]));
+                    xd[j] = v;
+                    if (xo) xo[j] = v;
+                }
+            }
+        }
+        __syncthreads();
+
+        // ---- phase 2: mix + residual + LN1, one warp per output row --------
+        for (int h = warp; h < T; h += kMixWarps) {
+            float y[NI * VEC];
+            const Tact* xh = xs + (size_t)h * D;
+            float sum = 0.f;
+            if (VEC == 2) {
+                const int ni = D >> 6;
+#pragma unroll
+                for (int i = 0; i < NI; ++i) {
+                    if (i < ni) {
+                        const int j = (i << 6) + (lane << 1);
+                        const int t = j / q;
+                        const int r = j - t * q;
+                        float m0, m1, x0, x1;
+                        Vec2<Tact>::split(Vec2<Tact>::load(xs + (size_t)t * D + h * q + r), m0, m1);
+                        Vec2<Tact>::split(Vec2<Tact>::load(xh + j), x0, x1);
+                        y[2 * i] = m0 + x0;
+                        y[2 * i + 1] = m1 + x1;
+                        sum += y[2 * i] + y[2 * i + 1];
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < NI; ++i) {
+                    const int j = (i << 5) + lane;
+                    if (j < D) {
+                        const int t = j / q;
+                        const int r = j - t * q;
+                        y[i] = to_f32(xs[(size_t)t * D + h * q + r]) + to_f32(xh[j]);
+                        sum += y[i];
+                    }
+                }
+            }
+            const float mean = warp_sum(sum) / (float)D;
+            float sq = 0.f;
+            if (VEC == 2) {
+                const int ni = D >> 6;
+#pragma unroll
+                for (int i = 0; i < NI; ++i)
+                    if (i < ni) {
+                        const float d0 = y[2 * i] - mean, d1 = y[2 * i + 1] - mean;
+                        sq += d0 * d0 + d1 * d1;
+                    }
+            } else {
+#pragma unroll
+                for (int i = 0; i < NI; ++i)
+                    if ((i << 5) + lane < D) {
+                        const float d = y[i] - mean;
+                        sq += d * d;
+                    }
+            }
+            const float rstd = rsqrtf(warp_sum(sq) / (float)D + a.eps);
+            Tact* srow = S + ((size_t)h * a.Bcap + b) * D;
+            if (VEC == 2) {
+                const int ni = D >> 6;
+#pragma unroll
+                for (int i = 0; i < NI; ++i)
+                    if (i < ni) {
+                        const int j = (i << 6) + (lane << 1);
+                        const float2 g = *reinterpret_cast<const float2*>(a.g1 + j);
+                        const float2 be = *reinterpret_cast<const float2*>(a.be1 + j);
+                        Vec2<Tact>::store(srow + j, ln_apply(y[2 * i], mean, rstd, g.x, be.x),
+                                          ln_apply(y[2 * i + 1], mean, rstd, g.y, be.y));
+                    }
+            } else {
+#pragma unroll
+                for (int i = 0; i < NI; ++i) {
+                    const int j = (i << 5) + lane;
+                    if (j < D) srow[j] = from_f32<Tact>(ln_apply(y[i], mean, rstd, a.g1[j], a.be1[j]));
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <typename Tact, bool FROM_Z, int VEC, int NI>
+cudaError_t launch_mix_inst(const MixLnArgs& a, int num_sms, cudaStream_t s) {
+    const size_t smem = (size_t)a.T * a.D * sizeof(Tact);
+    auto k = mix_ln1_kernel<Tact, FROM_Z, VEC, NI>;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    int per_sm = (int)((200 * 1024) / (smem + 1024));
+    if (per_sm < 1) per_sm = 1;
+    if (per_sm > 8) per_sm = 8;
+    int grid = num_sms * per_sm;
+    if (grid > a.B) grid = a.B;
+    k<<<grid, kMixThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename Tact, bool FROM_Z>
+cudaError_t launch_mix_dispatch(const MixLnArgs& a, int num_sms, cudaStream_t s) {
+    const bool vec2 = (a.q % 2 == 0) && (a.D % 64 == 0);
+    if (vec2) {
+        const int ni = a.D / 64;
+        if (ni <= 4) return launch_mix_inst<Tact, FROM_Z, 2, 4>(a, num_sms, s);
+        if (ni <= 12) return launch_mix_inst<Tact, FROM_Z, 2, 12>(a, num_sms, s);
+        if (ni <= 24) return launch_mix_inst<Tact, FROM_Z, 2, 24>(a, num_sms, s);
+        if (ni <= 48) return launch_mix_inst<Tact, FROM_Z, 2, 48>(a, num_sms, s);
+        return cudaErrorNotSupported;
+    }
+    const int ni = (a.D + 31) / 32;
+    if (ni <= 8) return launch_mix_inst<Tact, FROM_Z, 1, 8>(a, num_sms, s);
+    if (ni <= 48) return launch_mix_inst<Tact, FROM_Z, 1, 48>(a, num_sms, s);
+    return cudaErrorNotSupported;
+}
+
+// ---------------------------------------------------------------------------
+// LN2 finalisation into a sample-major output: one warp per (b, t) row.
+// ---------------------------------------------------------------------------
+template <typename Tact>
+__global__ void ln2_out_kernel(const float* __restrict__ Z, const float2* __restrict__ stats,
+                               const float* __restrict__ g2, const float* __restrict__ be2, Tact* __restrict__ X,
+                               int B, int T, int D, int Bcap, int nchunk, int cw, float eps) {
+    const int lane = threadIdx.x & 31;
+    const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+    for (long long r = wid; r < (long long)B * T; r += nw) {
+        const int b = (int)(r / T), t = (int)(r % T);
+        const size_t zr = (size_t)t * Bcap + b;
+        float mean, rstd;
+        merge_row_stats(stats + zr * nchunk, nchunk, cw, D, eps, lane, mean, rstd);
+        const float* z = Z + zr * D;
+        Tact* x = X + ((size_t)b * T + t) * D;
+        for (int j = lane; j < D; j += 32) x[j] = from_f32<Tact>(ln_apply(z[j], mean, rstd, g2[j], be2[j]));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Last LN2 finalisation + mean pooling over tokens, one CTA per sample.
+// ---------------------------------------------------------------------------
+constexpr int kPoolThreads = 256;
+constexpr int kPoolMaxT = 128;
+
+template <typename Tact>
+__global__ void __launch_bounds__(kPoolThreads)
+pool_kernel(const float* __restrict__ Z, const float2* __restrict__ stats, const float* __restrict__ g2,
+            const float* __restrict__ be2, float* __restrict__ pooled, Tact* __restrict__ XL, int B, int T, int D,
+            int Bcap, int nchunk, int cw, float eps) {
+    __shared__ float s_mean[kPoolMaxT], s_rstd[kPoolMaxT];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int b = blockIdx.x; b < B; b += gridDim.x) {
+        for (int t = warp; t < T; t += kPoolThreads / 32) {
+            float mean, rstd;
+            merge_row_stats(stats + ((size_t)t * Bcap + b) * nchunk, nchunk, cw, D, eps, lane, mean, rstd);
+            if (lane == 0) {
+                s_mean[t] = mean;
+                s_rstd[t] = rstd;
+            }
+        }
+        __syncthreads();
+        for (int j = threadIdx.x; j < D; j += kPoolThreads) {
+            const float g = g2[j], be = be2[j];
+            float acc = 0.f;
+            for (int t = 0; t < T; ++t) {
+                const Tact v = from_f32<Tact>(ln_apply(Z[((size_t)t * Bcap + b) * D + j], s_mean[t], s_rstd[t], g, be));
+                if (XL) XL[((size_t)b * T + t) * D + j] = v;
+                acc += to_f32(v);
+            }
+            pooled[(size_t)b * D + j] = acc / (float)T;
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Row statistics (mean, M2) of full Z rows, two passes, one warp per row.
+// ---------------------------------------------------------------------------
+__global__ void rowstats_kernel(const float* __restrict__ Z, float2* __restrict__ stats, int B, int T, int D,
+                                int Bcap) {
+    const int lane = threadIdx.x & 31;
+    const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+    for (long long r = wid; r < (long long)B * T; r += nw) {
+        const int t = (int)(r / B), b = (int)(r % B);
+        const size_t zr = (size_t)t * Bcap + b;
+        const float* z = Z + zr * D;
+        float s = 0.f;
+        for (int j = lane; j < D; j += 32) s += z[j];
+        const float mean = warp_sum(s) / (float)D;
+        float m2 = 0.f;
+        for (int j = lane; j < D; j += 32) {
+            const float d = z[j] - mean;
+            m2 += d * d;
+        }
+        m2 = warp_sum(m2);
+        if (lane == 0) stats[zr] = make_float2(mean, m2);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Layout helpers
+// ---------------------------------------------------------------------------
+template <typename E>
+__global__ void token_to_sample_kernel(const E* __restrict__ src, E* __restrict__ dst, int B, int T, int D,
+                                       int Bcap) {
+    const long long n = (long long)B * T * D;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        const int j = (int)(i % D);
+        const long long bt = i / D;
+        const int t = (int)(bt % T), b = (int)(bt / T);
+        dst[i] = src[((size_t)t * Bcap + b) * D + j];
+    }
+}
+
+// Standalone TokenMixing on element bits: Y[b][h][t q + r] = X[b][t][h q + r].
+template <typename E>
+__global__ void token_mix_kernel(const E* __restrict__ X, E* __restrict__ Y, int B, int T, int D, int H) {
+    const int q = D / H;
+    const long long TD = (long long)T * D;
+    const long long n = (long long)B * TD;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        const long long b = i / TD;
+        const long long o = i - b * TD;          // offset inside Y[b], row-major [H][T q]
+        const int h = (int)(o / ((long long)T * q));
+        const int c = (int)(o - (long long)h * T * q);
+        const int t = c / q, r = c - t * q;
+        Y[i] = X[b * TD + (long long)t * D + (long long)h * q + r];
+    }
+}
+
+template <typename E>
+__global__ void transpose_kernel(const E* __restrict__ in, E* __restrict__ out, int R, int C) {
+    __shared__ E tile[32][33];
+    const size_t g = blockIdx.z;
+    const E* src = in + g * (size_t)R * C;
+    E* dst = out + g * (size_t)R * C;
+    const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+    for (int i = threadIdx.y; i < 32; i += 8) {
+        const int r = r0 + i, c = c0 + threadIdx.x;
+        if (r < R && c < C) tile[i][threadIdx.x] = src[(size_t)r * C + c];
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += 8) {
+        const int c = c0 + i, r = r0 + threadIdx.x;
+        if (r < R && c < C) dst[(size_t)c * R + r] = tile[threadIdx.x][i];
+    }
+}
+
+template <typename Tin>
+__global__ void to_f32_kernel(const Tin* __restrict__ in, float* __restrict__ out, size_t n) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        out[i] = to_f32(in[i]);
+}
+
+__global__ void debug_wait_kernel(const int* flag, int* err, unsigned long long timeout_ns) {
+    if (threadIdx.x != 0) return;
+    const uint64_t t0 = globaltimer_ns();
+    while (*(volatile const int*)flag == 0) {
+        if (globaltimer_ns() - t0 > timeout_ns) {
+            latch_error(err, kDevErrTimeout);
+            return;
+        }
+        __nanosleep(1000);
+    }
+}
+
+inline int grid_for(long long n, int threads, int cap = 152 * 16) {
+    long long g = (n + threads - 1) / threads;
+    if (g < 1) g = 1;
+    if (g > cap) g = cap;
+    return (int)g;
+}
+
+}  // namespace
+
+cudaError_t launch_mix_ln1(Act act, bool from_z, const MixLnArgs& a, int num_sms, cudaStream_t s) {
+    if (a.B <= 0) return cudaSuccess;
+    if (act == Act::BF16)
+        return from_z ? launch_mix_dispatch<__nv_bfloat16, true>(a, num_sms, s)
+                      : launch_mix_dispatch<__nv_bfloat16, false>(a, num_sms, s);
+    return from_z ? launch_mix_dispatch<float, true>(a, num_sms, s) : launch_mix_dispatch<float, false>(a, num_sms, s);
+}
+
+cudaError_t launch_ln2_out(Act act, const float* Z, const float2* stats, const float* g2, const float* be2,
+                           void* X_out, int B, int T, int D, int Bcap, int nchunk, int cw, float eps, int num_sms,
+                           cudaStream_t s) {
+    if (B <= 0) return cudaSuccess;
+    const int grid = grid_for((long long)B * T * 32, 256, num_sms * 8);
+    if (act == Act::BF16)
+        ln2_out_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(Z, stats, g2, be2, (__nv_bfloat16*)X_out, B, T, D, Bcap,
+                                                            nchunk, cw, eps);
+    else
+        ln2_out_kernel<float><<<grid, 256, 0, s>>>(Z, stats, g2, be2, (float*)X_out, B, T, D, Bcap, nchunk, cw, eps);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pool(Act act, const float* Z, const float2* stats, const float* g2, const float* be2,
+                        float* pooled, void* XL, int B, int T, int D, int Bcap, int nchunk, int cw, float eps,
+                        int num_sms, cudaStream_t s) {
+    if (B <= 0) return cudaSuccess;
+    if (T > kPoolMaxT) return cudaErrorNotSupported;
+    const int grid = B < num_sms * 8 ? B : num_sms * 8;
+    if (act == Act::BF16)
+        pool_kernel<__nv_bfloat16><<<grid, kPoolThreads, 0, s>>>(Z, stats, g2, be2, pooled, (__nv_bfloat16*)XL, B, T,
+                                                                  D, Bcap, nchunk, cw, eps);
+    else
+        pool_kernel<float><<<grid, kPoolThreads, 0, s>>>(Z, stats, g2, be2, pooled, (float*)XL, B, T, D, Bcap, nchunk,
+                                                         cw, eps);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rowstats(const float* Z, float2* stats, int B, int T, int D, int Bcap, int num_sms,
+                            cudaStream_t s) {
+    if (B <= 0) return cudaSuccess;
+    const int grid = grid_for((long long)B * T * 32, 256, num_sms * 8);
+    rowstats_kernel<<<grid, 256, 0, s>>>(Z, stats, B, T, D, Bcap);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_token_to_sample(Act act, const void* src, void* dst, int B, int T, int D, int Bcap,
+                                   cudaStream_t s) {
+    if (B <= 0) return cudaSuccess;
+    const int grid = grid_for((long long)B * T * D, 256);
+    if (act == Act::BF16)
+        token_to_sample_kernel<uint16_t><<<grid, 256, 0, s>>>((const uint16_t*)src, (uint16_t*)dst, B, T, D, Bcap);
+    else
+        token_to_sample_kernel<uint32_t><<<grid, 256, 0, s>>>((const uint32_t*)src, (uint32_t*)dst, B, T, D, Bcap);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_token_mix(const void* X, void* Y, int B, int T, int D, int H, int esz, cudaStream_t s) {
+    if (B <= 0) return cudaSuccess;
+    const int grid = grid_for((long long)B * T * D, 256);
+    if (esz == 2)
+        token_mix_kernel<uint16_t><<<grid, 256, 0, s>>>((const uint16_t*)X, (uint16_t*)Y, B, T, D, H);
+    else if (esz == 4)
+        token_mix_kernel<uint32_t><<<grid, 256, 0, s>>>((const uint32_t*)X, (uint32_t*)Y, B, T, D, H);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose(const void* in, void* out, int G, int R, int C, int esz, cudaStream_t s) {
+    if (G <= 0 || R <= 0 || C <= 0) return cudaSuccess;
+    dim3 grid((C + 31) / 32, (R + 31) / 32, G), block(32, 8);
+    if (esz == 2)
+        transpose_kernel<uint16_t><<<grid, block, 0, s>>>((const uint16_t*)in, (uint16_t*)out, R, C);
+    else if (esz == 4)
+        transpose_kernel<uint32_t><<<grid, block, 0, s>>>((const uint32_t*)in, (uint32_t*)out, R, C);
+    else
+        return cudaErrorInvalidValue;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_to_f32(Act act, const void* in, float* out, size_t n, cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    const int grid = grid_for((long long)n, 256);
+    if (act == Act::BF16)
+        to_f32_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16*)in, out, n);
+    else
+        to_f32_kernel<float><<<grid, 256, 0, s>>>((const float*)in, out, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_debug_wait(const int* flag, int* err, unsigned long long timeout_ns, cudaStream_t s) {
+    debug_wait_kernel<<<1, 32, 0, s>>>(flag, err, timeout_ns);
+    return cudaGetLastError();
+}
+
+}  // namespace rm

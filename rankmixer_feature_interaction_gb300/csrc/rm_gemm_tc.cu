@@ -1,0 +1,576 @@
+// Grouped per-token FFN GEMMs on the 5th-generation tensor cores (sm_103a).
+//
+// "RankMixer: Scaling Up Ranking Models in Industrial Recommenders", section
+// 3.3.2 Eq. 6-9: token t owns W1_t (D x kD) and W2_t (kD x D).  The same-
+// position rows of a batch form a B x D matrix multiplied by that token's
+// weights ("RankMixer 详解（1）" section 4.3), so a layer's PFFN is T
+// independent GEMMs of equal shape -- one group per token.
+//
+//   GEMM1: Hid[t] = Gelu(S[t] W1_t + b1_t)            (M = B, N = kD, K = D)
+//   GEMM2: Z[t]   = Hid[t] W2_t + b2_t + S[t]         (M = B, N = D,  K = kD)
+//          plus per-row, per-chunk LayerNorm partials (mean, M2) of Z
+//
+// Kernel structure (one persistent CTA per SM, 12 warps):
+//   warp 0      TMA producer: 128x64 A and BNx64 B tiles (128-byte swizzle)
+//               into a STAGES-deep shared-memory ring, completion counted on
+//               "full" mbarriers
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=BN, K=16)
+//               into a double-buffered TMEM accumulator, frees ring slots with
+//               tcgen05.commit on the "empty" mbarriers
+//   warp 2      TMEM allocator
+//   warps 4-11  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM
+//               lanes 32*(w%4)..+31, i.e. tile rows; two warps per lane
+//               quadrant split the columns), fused bias + GELU (GEMM1) or
+//               bias + residual + row statistics (GEMM2), global stores
+// Every mbarrier wait is bounded in time; on expiry the CTA latches an error
+// word, the other roles see an abort flag and all of them unwind.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+#include <string>
+
+#include "rm_common.cuh"
+#include "rm_internal.h"
+
+namespace rm {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BK = 64;                 // one 128-byte swizzle row of bf16
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 128 + kEpiWarps * 32;
+
+enum { EPI_GELU = 1, EPI_RESID = 2, EPI_GATED = 3 };
+
+template <int BN>
+struct Cfg {
+    static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+    static constexpr int COLS_PER_WARP = BN / 2;        // two epilogue warps per lane quadrant
+    static constexpr int CHUNKS = COLS_PER_WARP / 32;
+    static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation must be a power of 2");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static_assert(CHUNKS >= 1, "BN >= 64");
+    static_assert(2 * STAGES * 8 + 4 * 8 + 8 <= BAR_BYTES, "barrier area");
+};
+
+struct Args {
+    int N, K;
+    int ngroups;              // groups in this launch
+    int group_base, group_stride;   // weight group of launch group j: group_base + j * group_stride
+    // uniform groups (dense PFFN): M rows each, A rows of group j start at j * a_group_rows
+    int M;
+    long long a_group_rows;
+    int m_tiles;              // ceil(M / BM), uniform groups only
+    int n_tiles;
+    long long tiles;          // uniform groups only
+    // variable groups (MoE experts), indexed by weight group: row count and first packed row;
+    // tile_prefix[j] = sum over launch groups i < j of ceil(count / BM)  (length ngroups + 1)
+    const int* g_count;
+    const int* g_off;
+    const int* tile_prefix;
+    const float* bias;        // [weight groups][N]
+    __nv_bfloat16* hid;       // EPI_GELU output rows (same row index as A)
+    const __nv_bfloat16* resid;  // EPI_RESID residual rows (same row index as A)
+    float* z;                 // EPI_RESID output rows
+    float2* stats;            // EPI_RESID row partials [row][nchunk]
+    int nchunk;
+    const int* row_sample;    // EPI_GATED: packed row -> sample index b
+    const float* gates;       // EPI_GATED: [B][T][E]
+    int gT, gE;
+    float* v;                 // EPI_GATED: V row (b, t) at b * v_sb + t * v_st
+    long long v_sb, v_st;
+    int* err;
+    unsigned long long timeout_ns;
+};
+
+struct TileCoord {
+    int j, mb, nb, wg, Mg;
+    long long row0;           // first A row of the group
+};
+
+__device__ __forceinline__ TileCoord decode_tile(long long tile, const Args& a) {
+    TileCoord c;
+    if (a.tile_prefix == nullptr) {
+        const long long per_group = (long long)a.m_tiles * a.n_tiles;
+        c.j = (int)(tile / per_group);
+        const int rem = (int)(tile - (long long)c.j * per_group);
+        c.nb = rem / a.m_tiles;   // m fastest: neighbouring CTAs share the weight tile
+        c.mb = rem - c.nb * a.m_tiles;
+        c.wg = a.group_base + c.j * a.group_stride;
+        c.Mg = a.M;
+        c.row0 = (long long)c.j * a.a_group_rows;
+    } else {
+        // largest j with tile_prefix[j] * n_tiles <= tile (skips empty groups)
+        int lo = 0, hi = a.ngroups - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if ((long long)__ldg(a.tile_prefix + mid) * a.n_tiles <= tile) lo = mid; else hi = mid - 1;
+        }
+        c.j = lo;
+        const int p0 = __ldg(a.tile_prefix + lo);
+        const int mt = __ldg(a.tile_prefix + lo + 1) - p0;
+        const int rem = (int)(tile - (long long)p0 * a.n_tiles);
+        c.nb = rem / mt;
+        c.mb = rem - c.nb * mt;
+        c.wg = a.group_base + c.j * a.group_stride;
+        c.Mg = __ldg(a.g_count + c.wg);
+        c.row0 = __ldg(a.g_off + c.wg);
+    }
+    return c;
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const Args args) {
+    using C = Cfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t* base_ptr = smem_raw + (base - raw_addr);
+    const uint32_t sA = base;
+    const uint32_t sB = base + C::STAGES * C::A_BYTES;
+    const uint32_t bar0 = base + C::STAGES * C::STAGE_BYTES;
+    // barrier addresses: full[s], empty[s], tfull[2], tempty[2]
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
+    uint32_t* tmem_holder =
+        reinterpret_cast<uint32_t*>(base_ptr + C::STAGES * C::STAGE_BYTES + 8 * (2 * C::STAGES + 4));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), kEpiWarps * 32);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
+
+    const int kblocks = args.K / BK;
+    const long long tiles =
+        args.tile_prefix ? (long long)__ldg(args.tile_prefix + args.ngroups) * args.n_tiles : args.tiles;
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (long long tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
+                const TileCoord tc = decode_tile(tile, args);
+                const int arow = (int)(tc.row0 + (long long)tc.mb * BM);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, args.err, args.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_bar(stage), (uint32_t)C::STAGE_BYTES);
+                    tma_load_3d(&tmA, sA + stage * C::A_BYTES, full_bar(stage), kb * BK, arow, 0);
+                    tma_load_3d(&tmB, sB + stage * C::B_BYTES, full_bar(stage), kb * BK, tc.nb * BN, tc.wg);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer --------------------------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc_bf16_f32(BM, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (long long tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
+                if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.err, args.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, args.err, args.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = sA + stage * C::A_BYTES;
+                    const uint32_t b0 = sB + stage * C::B_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        umma_bf16(d_tmem, make_sw128_desc(a0 + 32u * k), make_sw128_desc(b0 + 32u * k), idesc,
+                                  (kb > 0 || k > 0) ? 1u : 0u);
+                    }
+                    umma_commit(empty_bar(stage));
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(tfull_bar(acc));
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+        }
+    } else if (warp >= 4) {
+        // ------------------------------ epilogue ----------------------------------
+        const int ew = warp - 4;
+        const int quad = warp & 3;              // TMEM lanes this warp may read
+        const int half = ew >> 2;               // which BN/2 columns
+        const int row_in_tile = quad * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (long long tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+            const TileCoord tc = decode_tile(tile, args);
+            // one lane waits, the warp follows (keeps tcgen05.ld warp-converged)
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err, args.timeout_ns);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            __syncwarp();
+            tc_fence_after();
+            const int m = tc.mb * BM + row_in_tile;          // row inside the group
+            const bool valid = m < tc.Mg;
+            const long long arow = tc.row0 + m;             // row of A and of the row-aligned outputs
+            const uint32_t tbase =
+                tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN + half * C::COLS_PER_WARP);
+            const int n0 = tc.nb * BN + half * C::COLS_PER_WARP;
+            const size_t orow = (size_t)arow * (size_t)args.N + n0;
+            const float* bias = args.bias + (size_t)tc.wg * args.N + n0;
+
+            if (EPI == EPI_GELU) {
+#pragma unroll 1
+                for (int c = 0; c < C::CHUNKS; ++c) {
+                    float v[32];
+                    tmem_ld32(tbase + 32u * c, v);
+                    if (valid) {
+                        uint32_t p[16];
+                        const float4* b4 = reinterpret_cast<const float4*>(bias + 32 * c);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 bb = __ldg(b4 + j);
+                            p[2 * j] = pack_bf16x2(gelu_erf(v[4 * j] + bb.x), gelu_erf(v[4 * j + 1] + bb.y));
+                            p[2 * j + 1] = pack_bf16x2(gelu_erf(v[4 * j + 2] + bb.z), gelu_erf(v[4 * j + 3] + bb.w));
+                        }
+                        uint4* dst = reinterpret_cast<uint4*>(args.hid + orow + 32 * c);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+                    }
+                }
+            } else if (EPI == EPI_RESID) {
+                float shift = 0.f, s1 = 0.f, s2 = 0.f;
+#pragma unroll 1
+                for (int c = 0; c < C::CHUNKS; ++c) {
+                    float v[32];
+                    tmem_ld32(tbase + 32u * c, v);
+                    if (valid) {
+                        const float4* b4 = reinterpret_cast<const float4*>(bias + 32 * c);
+                        const uint4* r4 = reinterpret_cast<const uint4*>(args.resid + orow + 32 * c);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint4 rr = __ldg(r4 + j);
+                            const uint32_t w[4] = {rr.x, rr.y, rr.z, rr.w};
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162*>(&w[h]);
+                                v[8 * j + 2 * h] += __low2float(pr);
+                                v[8 * j + 2 * h + 1] += __high2float(pr);
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 bb = __ldg(b4 + j);
+                            v[4 * j] += bb.x;
+                            v[4 * j + 1] += bb.y;
+                            v[4 * j + 2] += bb.z;
+                            v[4 * j + 3] += bb.w;
+                        }
+                        if (c == 0) {
+                            float mm = 0.f;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) mm += v[j];
+                            shift = mm * (1.0f / 32.0f);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float d = v[j] - shift;
+                            s1 += d;
+                            s2 = fmaf(d, d, s2);
+                        }
+                        float4* dst = reinterpret_cast<float4*>(args.z + orow + 32 * c);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    }
+                }
+                if (valid) {
+                    const float n = (float)C::COLS_PER_WARP;
+                    const float mean = shift + s1 / n;
+                    const float m2 = fmaxf(s2 - s1 * s1 / n, 0.f);
+                    const int chunk = tc.nb * 2 + half;
+                    args.stats[(size_t)arow * args.nchunk + chunk] = make_float2(mean, m2);
+                }
+            } else {  // EPI_GATED: V[b, t] += gate * (acc + b2)
+                float gate = 0.f;
+                float* vrow = nullptr;
+                if (valid) {
+                    const int b = __ldg(args.row_sample + arow);
+                    const int t = tc.wg / args.gE, e = tc.wg - t * args.gE;
+                    gate = __ldg(args.gates + ((size_t)b * args.gT + t) * args.gE + e);
+                    vrow = args.v + (size_t)b * args.v_sb + (size_t)t * args.v_st + n0;
+                }
+#pragma unroll 1
+                for (int c = 0; c < C::CHUNKS; ++c) {
+                    float v[32];
+                    tmem_ld32(tbase + 32u * c, v);
+                    if (valid) {
+                        const float4* b4 = reinterpret_cast<const float4*>(bias + 32 * c);
+                        float4* dst = reinterpret_cast<float4*>(vrow + 32 * c);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 bb = __ldg(b4 + j);
+                            float4 o = dst[j];
+                            o.x = fmaf(gate, v[4 * j] + bb.x, o.x);
+                            o.y = fmaf(gate, v[4 * j + 1] + bb.y, o.y);
+                            o.z = fmaf(gate, v[4 * j + 2] + bb.z, o.z);
+                            o.w = fmaf(gate, v[4 * j + 3] + bb.w, o.w);
+                            dst[j] = o;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(tempty_bar(acc));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// ----------------------------------------------------------------------------
+// Host side
+// ----------------------------------------------------------------------------
+std::mutex g_mu;
+std::string g_err;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool get_encoder() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_encode) return true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+        g_err = "cuTensorMapEncodeTiled entry point not available";
+        return false;
+    }
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return true;
+}
+
+// 3-D bf16 tensor map over a [groups][rows][K] buffer (row pitch K elements,
+// group pitch group_rows * K), box = 64 (K) x box_rows x 1, 128-byte swizzle.
+// Rows past `rows` read as zeros.
+bool make_map(CUtensorMap* m, const void* ptr, int K, long long rows, int groups, long long group_rows,
+              int box_rows) {
+    if (!get_encoder()) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)groups};
+    cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)group_rows * (cuuint64_t)K * 2};
+    cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_err = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string((int)r);
+        return false;
+    }
+    return true;
+}
+
+int pick_bn(int N) {
+    if (N % 256 == 0) return 256;
+    if (N % 128 == 0) return 128;
+    if (N % 64 == 0) return 64;
+    return 0;
+}
+
+// A: rows_total x K activation rows (row r of launch group j at row0(j) + r);
+// W: n_wgroups x N x K weights.
+template <int BN, int EPI>
+cudaError_t run(const void* A, long long a_rows_total, const void* W, int n_wgroups, Args a, int num_sms,
+                cudaStream_t s) {
+    using C = Cfg<BN>;
+    a.n_tiles = a.N / BN;
+    if (a.tile_prefix == nullptr) {
+        a.m_tiles = (a.M + BM - 1) / BM;
+        a.tiles = (long long)a.ngroups * a.m_tiles * a.n_tiles;
+        if (a.tiles == 0) return cudaSuccess;
+    }
+    CUtensorMap mA, mB;
+    if (!make_map(&mA, A, a.K, a_rows_total, 1, a_rows_total, BM)) return cudaErrorInvalidValue;
+    if (!make_map(&mB, W, a.K, a.N, n_wgroups, a.N, BN)) return cudaErrorInvalidValue;
+    auto k = pffn_gemm_tc_kernel<BN, EPI>;
+    static bool attr_done = false;  // once per template instance
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    long long grid = num_sms;
+    if (a.tile_prefix == nullptr && a.tiles < grid) grid = a.tiles;
+    k<<<(int)grid, kThreads, C::SMEM_BYTES, s>>>(mA, mB, a);
+    return cudaGetLastError();
+}
+
+template <int EPI>
+cudaError_t run_bn(int bn, const void* A, long long a_rows_total, const void* W, int n_wgroups, const Args& a,
+                   int num_sms, cudaStream_t s) {
+    switch (bn) {
+        case 256: return run<256, EPI>(A, a_rows_total, W, n_wgroups, a, num_sms, s);
+        case 128: return run<128, EPI>(A, a_rows_total, W, n_wgroups, a, num_sms, s);
+        case 64: return run<64, EPI>(A, a_rows_total, W, n_wgroups, a, num_sms, s);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+}  // namespace tc
+
+bool tc_supported(int D, int F) {
+    return D % tc::BK == 0 && F % tc::BK == 0 && tc::pick_bn(F) != 0 && tc::pick_bn(D) != 0;
+}
+
+int tc_stats_chunk_width(int D) { return tc::pick_bn(D) / 2; }
+
+const char* tc_last_error() {
+    std::lock_guard<std::mutex> lk(tc::g_mu);
+    return tc::g_err.c_str();
+}
+
+cudaError_t launch_gemm1_tc(const void* S, const void* W1p, const float* b1, void* Hid, int B, int T, int D, int F,
+                            int Bcap, int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s) {
+    if (B <= 0) return cudaSuccess;
+    tc::Args a{};
+    a.N = F;
+    a.K = D;
+    a.ngroups = T;
+    a.group_base = 0;
+    a.group_stride = 1;
+    a.M = B;
+    a.a_group_rows = Bcap;
+    a.bias = b1;
+    a.hid = reinterpret_cast<__nv_bfloat16*>(Hid);
+    a.err = err;
+    a.timeout_ns = timeout_ns;
+    return tc::run_bn<tc::EPI_GELU>(tc::pick_bn(F), S, (long long)T * Bcap, W1p, T, a, num_sms, s);
+}
+
+cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, const void* S, float* Z,
+                            float2* stats, int B, int T, int D, int F, int Bcap, int num_sms, int* err,
+                            unsigned long long timeout_ns, cudaStream_t s) {
+    if (B <= 0) return cudaSuccess;
+    const int bn = tc::pick_bn(D);
+    if (bn == 0) return cudaErrorNotSupported;
+    tc::Args a{};
+    a.N = D;
+    a.K = F;
+    a.ngroups = T;
+    a.group_base = 0;
+    a.group_stride = 1;
+    a.M = B;
+    a.a_group_rows = Bcap;
+    a.bias = b2;
+    a.resid = reinterpret_cast<const __nv_bfloat16*>(S);
+    a.z = Z;
+    a.stats = stats;
+    a.nchunk = D / (bn / 2);
+    a.err = err;
+    a.timeout_ns = timeout_ns;
+    return tc::run_bn<tc::EPI_RESID>(bn, Hid, (long long)T * Bcap, W2p, T, a, num_sms, s);
+}
+
+cudaError_t launch_moe_gemm1_tc(const void* Sg, long long rows_total, const void* W1p, const float* b1, void* Hm,
+                                int groups, int D, int Fe, const int* g_count, const int* g_off,
+                                const int* tile_prefix, int num_sms, int* err, unsigned long long timeout_ns,
+                                cudaStream_t s) {
+    tc::Args a{};
+    a.N = Fe;
+    a.K = D;
+    a.ngroups = groups;
+    a.group_base = 0;
+    a.group_stride = 1;
+    a.g_count = g_count;
+    a.g_off = g_off;
+    a.tile_prefix = tile_prefix;
+    a.bias = b1;
+    a.hid = reinterpret_cast<__nv_bfloat16*>(Hm);
+    a.err = err;
+    a.timeout_ns = timeout_ns;
+    return tc::run_bn<tc::EPI_GELU>(tc::pick_bn(Fe), Sg, rows_total, W1p, groups, a, num_sms, s);
+}
+
+cudaError_t launch_moe_gemm2_tc(const void* Hm, long long rows_total, const void* W2p, const float* b2, int T, int E,
+                                int e, int D, int Fe, const int* g_count, const int* g_off, const int* tile_prefix_e,
+                                const int* row_sample, const float* gates, float* V, long long v_sb, long long v_st,
+                                int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s) {
+    tc::Args a{};
+    a.N = D;
+    a.K = Fe;
+    a.ngroups = T;
+    a.group_base = e;
+    a.group_stride = E;
+    a.g_count = g_count;
+    a.g_off = g_off;
+    a.tile_prefix = tile_prefix_e;
+    a.bias = b2;
+    a.row_sample = row_sample;
+    a.gates = gates;
+    a.gT = T;
+    a.gE = E;
+    a.v = V;
+    a.v_sb = v_sb;
+    a.v_st = v_st;
+    a.err = err;
+    a.timeout_ns = timeout_ns;
+    return tc::run_bn<tc::EPI_GATED>(tc::pick_bn(D), Hm, rows_total, W2p, T * E, a, num_sms, s);
+}
+
+}  // namespace rm

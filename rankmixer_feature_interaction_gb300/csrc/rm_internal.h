@@ -1,0 +1,94 @@
+// Internal launcher interface between the C-ABI layer (rm_api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rm {
+
+enum class Act { F32 = 0, BF16 = 1 };
+
+// Device error word values (latched with atomicCAS from 0).
+constexpr int kDevErrTimeout = 5;
+constexpr int kDevErrOther = 6;
+
+inline size_t act_size(Act a) { return a == Act::F32 ? 4 : 2; }
+
+// Token-major activation workspace: element (t, b, j) of a [T][Bcap][W] buffer
+// sits at (t * Bcap + b) * W + j.
+
+struct MixLnArgs {
+    // input: either X (sample-major [B][T][D], activation dtype) ...
+    const void* X;
+    // ... or the previous layer's pre-LN2 rows Z (token-major fp32) with
+    // per-row chunk statistics and that layer's LN2 affine.
+    const float* Z;
+    const float2* stats;
+    const float* g2;
+    const float* be2;
+    void* Xprev_out;        // optional sample-major copy of the finalised previous X
+    // output S (token-major) and this layer's LN1 affine
+    void* S;
+    const float* g1;
+    const float* be1;
+    int B, T, D, q, Bcap, nchunk, cw;
+    float eps;
+};
+
+// S = LN1(Mix(X) + X), X either given or finalised from (Z, stats).
+cudaError_t launch_mix_ln1(Act act, bool from_z, const MixLnArgs& a, int num_sms, cudaStream_t s);
+
+// X_out[b][t][:] = LN2(Z[t][b][:]) in the activation dtype.
+cudaError_t launch_ln2_out(Act act, const float* Z, const float2* stats, const float* g2, const float* be2,
+                           void* X_out, int B, int T, int D, int Bcap, int nchunk, int cw, float eps,
+                           int num_sms, cudaStream_t s);
+
+// pooled[b][:] = (1/T) sum_t X_L[b][t][:], X_L = LN2(Z) rounded to the activation
+// dtype; XL (optional) receives X_L sample-major.
+cudaError_t launch_pool(Act act, const float* Z, const float2* stats, const float* g2, const float* be2,
+                        float* pooled, void* XL, int B, int T, int D, int Bcap, int nchunk, int cw, float eps,
+                        int num_sms, cudaStream_t s);
+
+// (mean, M2) of each full row of Z (one chunk per row).
+cudaError_t launch_rowstats(const float* Z, float2* stats, int B, int T, int D, int Bcap, int num_sms,
+                            cudaStream_t s);
+
+// Token-major [T][Bcap][D] -> sample-major [B][T][D] copy (activation dtype).
+cudaError_t launch_token_to_sample(Act act, const void* src, void* dst, int B, int T, int D, int Bcap,
+                                   cudaStream_t s);
+
+// Y[b][h][t q + r] = X[b][t][h q + r] on raw element bits (esz 2 or 4).
+cudaError_t launch_token_mix(const void* X, void* Y, int B, int T, int D, int H, int esz, cudaStream_t s);
+
+// out[g][c][r] = in[g][r][c] for G matrices of R x C (element size esz, 2 or 4).
+cudaError_t launch_transpose(const void* in, void* out, int G, int R, int C, int esz, cudaStream_t s);
+
+// out[i] = float(in[i]) for n elements of the given dtype.
+cudaError_t launch_to_f32(Act act, const void* in, float* out, size_t n, cudaStream_t s);
+
+// Test hook: bounded wait on a flag nothing sets; latches kDevErrTimeout.
+cudaError_t launch_debug_wait(const int* flag, int* err, unsigned long long timeout_ns, cudaStream_t s);
+
+// ---- per-token FFN GEMMs -------------------------------------------------
+// GEMM1: Hid[t] = Gelu(S[t] W1_t + b1_t), GEMM2: Z[t] = Hid[t] W2_t + b2_t + S[t].
+// Activations token-major, weights packed K-major: W1p [T][N=kD][K=D], W2p [T][N=D][K=kD].
+
+cudaError_t launch_gemm1_simt(Act act, const void* S, const void* W1p, const float* b1, void* Hid, int B, int T,
+                              int D, int F, int Bcap, cudaStream_t s);
+cudaError_t launch_gemm2_simt(Act act, const void* Hid, const void* W2p, const float* b2, const void* S, float* Z,
+                              int B, int T, int D, int F, int Bcap, cudaStream_t s);
+
+// tcgen05 path (bf16 only).  Returns cudaErrorNotSupported for shapes it does not take.
+bool tc_supported(int D, int F);
+int tc_stats_chunk_width(int D);   // chunk width of the LN2 partial statistics written by GEMM2
+cudaError_t launch_gemm1_tc(const void* S, const void* W1p, const float* b1, void* Hid, int B, int T, int D, int F,
+                            int Bcap, int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s);
+cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, const void* S, float* Z,
+                            float2* stats, int B, int T, int D, int F, int Bcap, int num_sms, int* err,
+                            unsigned long long timeout_ns, cudaStream_t s);
+
+// Set by the tensor-map encoder when the driver call fails (host-side message).
+const char* tc_last_error();
+
+}  // namespace rm

@@ -1,0 +1,113 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+function include/rankmixer.h declares, and rejects bad arguments on the host
+before touching the device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from rankmixer_feature_interaction_gb300 import _lib
+from rankmixer_feature_interaction_gb300 import build as rm_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rankmixer.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(_lib.LIB_PATH):
+        rm_build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:RM_API\s+)?(?:rm_status\s+|const\s+char\s*\*\s*|int\s+)(rm_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ("rm_create", "rm_destroy", "rm_block_forward", "rm_stack_forward", "rm_moe_pffn_forward",
+                 "rm_token_mix", "rm_last_error"):
+        assert must in names
+    assert set(names) == set(_lib.EXPORTED), "binding and header disagree"
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} missing from librankmixer.so"
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\b(rm_\w+)\b", out))
+    assert set(declared_functions()) <= exported
+    assert exported <= set(declared_functions()), f"undeclared exports: {exported - set(declared_functions())}"
+
+
+def test_abi_version(lib):
+    assert _lib.rm_abi_version() == 1
+
+
+def _cfg(**kw):
+    base = dict(T=4, D=8, H=4, k=2, L=1, n_experts=0, expert_hidden=0, moe_layer_mask=0, dtype=_lib.RM_F32,
+                ln_eps=1e-5, max_batch=16, gemm_path=_lib.RM_PATH_AUTO)
+    base.update(kw)
+    return _lib.rm_config(**base)
+
+
+def _create_status(lib, cfg, layers=True):
+    out = ctypes.c_void_p()
+    arr = (_lib.rm_layer_params * max(cfg.L if cfg is not None else 1, 1))() if layers else None
+    return lib.rm_create(ctypes.byref(cfg) if cfg is not None else None, arr, 0, ctypes.byref(out)), out.value
+
+
+def test_create_rejects_bad_configs_on_host(lib):
+    st, ctx = _create_status(lib, None)
+    assert st == _lib.RM_ERR_INVALID_ARG and ctx is None
+    st, _ = _create_status(lib, _cfg(H=2))                     # H != T: needs the [T][D] shape for the residual
+    assert st == _lib.RM_ERR_UNSUPPORTED
+    assert "H (2) must equal T (4)" in _lib.rm_last_error()
+    st, _ = _create_status(lib, _cfg(D=9))                     # D % H != 0
+    assert st == _lib.RM_ERR_INVALID_ARG
+    st, _ = _create_status(lib, _cfg(max_batch=0))
+    assert st == _lib.RM_ERR_INVALID_ARG
+    st, _ = _create_status(lib, _cfg(dtype=7))
+    assert st == _lib.RM_ERR_INVALID_ARG
+    st, _ = _create_status(lib, _cfg(ln_eps=-1.0))
+    assert st == _lib.RM_ERR_INVALID_ARG
+    st, _ = _create_status(lib, _cfg(moe_layer_mask=1))        # MoE layer without experts
+    assert st == _lib.RM_ERR_INVALID_ARG
+    st, _ = _create_status(lib, _cfg(T=32, H=32, D=4096, dtype=_lib.RM_BF16))   # sample too big for one CTA
+    assert st == _lib.RM_ERR_UNSUPPORTED
+    st, _ = _create_status(lib, _cfg(), layers=False)
+    assert st == _lib.RM_ERR_INVALID_ARG
+
+
+def test_token_mix_rejects_bad_arguments_on_host(lib):
+    assert lib.rm_token_mix(None, None, 1, 4, 8, 4, _lib.RM_F32, None) == _lib.RM_ERR_INVALID_ARG
+    buf = ctypes.create_string_buffer(1024)
+    p = ctypes.addressof(buf)
+    assert lib.rm_token_mix(p, p + 512, 1, 4, 8, 3, _lib.RM_F32, None) == _lib.RM_ERR_INVALID_ARG   # D % H
+    assert lib.rm_token_mix(p, p + 64, 1, 4, 8, 4, _lib.RM_F32, None) == _lib.RM_ERR_INVALID_ARG    # overlap
+    assert lib.rm_token_mix(p, p + 512, 0, 4, 8, 4, _lib.RM_F32, None) == _lib.RM_ERR_INVALID_ARG   # B = 0
+    assert lib.rm_token_mix(p, p + 512, 1, 4, 8, 4, 9, None) == _lib.RM_ERR_INVALID_ARG             # dtype
+
+
+def test_null_context_calls(lib):
+    assert lib.rm_destroy(None) == _lib.RM_OK
+    info = _lib.rm_info()
+    assert lib.rm_get_info(None, ctypes.byref(info)) == _lib.RM_ERR_INVALID_ARG
+    assert lib.rm_block_forward(None, 0, None, None, None, 1, None) == _lib.RM_ERR_INVALID_ARG
+    assert lib.rm_stack_forward(None, None, None, None, 1, None) == _lib.RM_ERR_INVALID_ARG
+    assert lib.rm_moe_pffn_forward(None, 0, None, None, None, 1, None) == _lib.RM_ERR_INVALID_ARG
+    assert lib.rm_sync_status(None, None) == _lib.RM_ERR_INVALID_ARG
+    assert lib.rm_profile_enable(None, 1) == _lib.RM_ERR_INVALID_ARG
+    assert "ctx is NULL" in _lib.rm_last_error()
+
+
+def test_binding_raises_with_status_and_message(lib):
+    with pytest.raises(_lib.RankMixerError) as e:
+        _lib.rm_token_mix(0, 0, 1, 4, 8, 4, _lib.RM_F32, 0)
+    assert e.value.status == _lib.RM_ERR_INVALID_ARG
+    assert "NULL" in str(e.value)

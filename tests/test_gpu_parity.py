@@ -1,0 +1,335 @@
+"""GPU parity of the CUDA library against the CPU oracle (needs an sm_103a GPU).
+
+Every test feeds the same seeded values to both sides (the oracle receives the
+values as rounded to the library's dtype, in float64) and compares element by
+element: bit-exact for the mixing permutation, max relative error <= 1e-4 on
+the float32 path, max error <= 2e-2 * RMS on the bf16 path.  Full-size
+workloads run on the GPU in the benchmark's launch configuration and are
+compared on sampled samples the oracle computes one by one.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from rankmixer_feature_interaction_gb300 import _lib, synth
+from rankmixer_feature_interaction_gb300.api import RankMixer, token_mix
+from tests.helpers import check
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _build(T, D, k, L, B, seed, dtype, path="auto", max_batch=None, E=0, Fe=0, moe_mask=0, active=2.0):
+    layers = synth.make_stack(T, D, k, L, seed, dtype, DEV, E=E, Fe=Fe, active=active)
+    m = RankMixer(T, D, k, layers, dtype=dtype, max_batch=max_batch or B, n_experts=E, expert_hidden=Fe,
+                  moe_layer_mask=moe_mask, gemm_path=path)
+    X = synth.make_input(B, T, D, seed + 1, dtype, DEV)
+    return m, layers, X
+
+
+def _np(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+# ----------------------------------------------------------------------------
+# TokenMixing: bit-exact
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("B,T,D,H", [(3, 4, 8, 4), (5, 2, 6, 2), (7, 2, 6, 3), (2, 4, 12, 6), (2, 16, 768, 16),
+                                     (3, 32, 1536, 32), (1, 5, 15, 5)])
+def test_token_mix_bit_exact(dtype, B, T, D, H):
+    X = synth.make_input(B, T, D, 100 + B + T + D + H, dtype, DEV)
+    Y = token_mix(X, H)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(_np(Y), oracle.token_mix(_np(X), H))
+
+
+# ----------------------------------------------------------------------------
+# Tiny float32 configuration (T=4, D=8, H=4: the A1..D4 layout), 1e-4
+# ----------------------------------------------------------------------------
+
+def test_tiny_fp32_block_and_stack():
+    c = synth.CONFIGS["tiny_fp32"]
+    m, layers, X = _build(c["T"], c["D"], c["k"], c["L"], c["B"], 7, "f32")
+    assert m.path == "simt"
+    Xo, S = m.block_forward(0, X, return_S=True)
+    pooled, XL = m.stack_forward(X, return_XL=True)
+    torch.cuda.synchronize()
+    assert m.sync_status() == _lib.RM_OK
+    p64 = synth.to_f64(layers)
+    Xo_ref, S_ref = oracle.block_forward(_np(X), p64[0], return_S=True)
+    pooled_ref, XL_ref = oracle.stack_forward(_np(X), p64, return_XL=True)
+    check(_np(S), S_ref, "f32", "S (LN1)")
+    check(_np(Xo), Xo_ref, "f32", "block X_out")
+    check(_np(XL), XL_ref, "f32", "stack X_L")
+    check(_np(pooled), pooled_ref, "f32", "pooled")
+
+
+# ----------------------------------------------------------------------------
+# bf16 shapes that span several tiles and a ragged batch tail, both GEMM paths
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("path", ["tcgen05", "simt"])
+@pytest.mark.parametrize("T,D,k,L,B", [(4, 256, 2, 2, 300), (8, 512, 4, 1, 260), (2, 64, 1, 1, 129),
+                                       (16, 768, 4, 1, 77)])
+def test_bf16_block_and_stack(path, T, D, k, L, B):
+    m, layers, X = _build(T, D, k, L, B, 11 + T + D, "bf16", path=path)
+    assert m.path == path
+    Xo, S = m.block_forward(0, X, return_S=True)
+    pooled, XL = m.stack_forward(X, return_XL=True)
+    torch.cuda.synchronize()
+    assert m.sync_status() == _lib.RM_OK
+    p64 = synth.to_f64(layers)
+    Xo_ref, S_ref = oracle.block_forward(_np(X), p64[0], return_S=True)
+    check(_np(S), S_ref, "bf16", "S (LN1)")
+    check(_np(Xo), Xo_ref, "bf16", "block X_out")
+    pooled_ref, XL_ref = oracle.stack_forward(_np(X), p64, return_XL=True)
+    check(_np(XL), XL_ref, "bf16", "stack X_L")
+    check(_np(pooled), pooled_ref, "bf16", "pooled")
+
+
+@pytest.mark.parametrize("path", ["tcgen05", "simt"])
+def test_stack_equals_chained_blocks_bit_exact(path):
+    T, D, k, L, B = 4, 256, 2, 3, 200
+    m, layers, X = _build(T, D, k, L, B, 5, "bf16", path=path)
+    pooled, XL = m.stack_forward(X, return_XL=True)
+    Xn = X
+    for n in range(L):
+        Xn = m.block_forward(n, Xn)
+    torch.cuda.synchronize()
+    assert torch.equal(XL, Xn)
+    ref = Xn.float().sum(dim=1) / T
+    torch.testing.assert_close(pooled, ref, rtol=1e-6, atol=1e-6)
+
+
+def test_tcgen05_agrees_with_simt():
+    T, D, k, B = 8, 512, 4, 333
+    layers = synth.make_stack(T, D, k, 1, 9, "bf16", DEV)
+    X = synth.make_input(B, T, D, 10, "bf16", DEV)
+    a = RankMixer(T, D, k, layers, max_batch=B, gemm_path="tcgen05").block_forward(0, X)
+    b = RankMixer(T, D, k, layers, max_batch=B, gemm_path="simt").block_forward(0, X)
+    torch.cuda.synchronize()
+    check(_np(a), _np(b), "bf16", "tcgen05 vs simt", tol=1.5e-2)
+
+
+def test_deterministic_reruns():
+    T, D, k, L, B = 8, 512, 4, 2, 300
+    m, _, X = _build(T, D, k, L, B, 21, "bf16")
+    p1, x1 = m.stack_forward(X, return_XL=True)
+    p2, x2 = m.stack_forward(X, return_XL=True)
+    torch.cuda.synchronize()
+    assert torch.equal(p1, p2) and torch.equal(x1, x2)
+
+
+def test_host_entry_matches_device_entry():
+    T, D, k, L, B = 8, 512, 4, 2, 100
+    m, _, X = _build(T, D, k, L, B, 23, "bf16")
+    dev = m.stack_forward(X)
+    Xh = X.cpu().pin_memory()
+    host = m.stack_forward_host(Xh)
+    torch.cuda.synchronize()
+    assert torch.equal(dev.cpu(), host)
+
+
+# ----------------------------------------------------------------------------
+# Edge cases
+# ----------------------------------------------------------------------------
+
+def test_batch_of_one_and_full_capacity():
+    T, D, k, L = 4, 256, 2, 2
+    m, layers, X = _build(T, D, k, L, 257, 31, "bf16", max_batch=257)
+    p64 = synth.to_f64(layers)
+    for B in (1, 257):
+        pooled, XL = m.stack_forward(X[:B].contiguous(), return_XL=True)
+        torch.cuda.synchronize()
+        pr, xr = oracle.stack_forward(_np(X[:B]), p64, return_XL=True)
+        check(_np(XL), xr, "bf16", f"X_L B={B}")
+        check(_np(pooled), pr, "bf16", f"pooled B={B}")
+
+
+@pytest.mark.parametrize("dtype,T,D,k", [("bf16", 4, 12, 2), ("f32", 4, 12, 3), ("bf16", 6, 96, 2),
+                                         ("f32", 3, 48, 1), ("bf16", 32, 32, 1)])
+def test_odd_shapes_take_the_simt_path(dtype, T, D, k):
+    """q odd, D not a multiple of 64, q = 1 (plain transpose): CUDA-core GEMMs."""
+    B = 37
+    m, layers, X = _build(T, D, k, 2, B, 41 + D, dtype)
+    assert m.path == "simt"
+    pooled, XL = m.stack_forward(X, return_XL=True)
+    torch.cuda.synchronize()
+    pr, xr = oracle.stack_forward(_np(X), synth.to_f64(layers), return_XL=True)
+    check(_np(XL), xr, dtype, "X_L")
+    check(_np(pooled), pr, dtype, "pooled")
+
+
+def test_invalid_arguments_are_reported():
+    T, D, k = 4, 256, 2
+    m, layers, X = _build(T, D, k, 1, 16, 3, "bf16")
+    with pytest.raises(_lib.RankMixerError) as e:
+        m.block_forward(1, X)
+    assert e.value.status == _lib.RM_ERR_INVALID_ARG
+    with pytest.raises(_lib.RankMixerError) as e:
+        m.stack_forward(synth.make_input(17, T, D, 1, "bf16", DEV))
+    assert e.value.status == _lib.RM_ERR_INVALID_ARG
+    with pytest.raises(_lib.RankMixerError) as e:
+        _lib.rm_block_forward(m.ctx, 0, X.data_ptr(), X.data_ptr(), None, 16, 0)
+    assert e.value.status == _lib.RM_ERR_INVALID_ARG
+    with pytest.raises(_lib.RankMixerError) as e:
+        _lib.rm_stack_forward(m.ctx, X.data_ptr() + 2, m.stack_forward(X).data_ptr(), None, 16, 0)
+    assert e.value.status == _lib.RM_ERR_INVALID_ARG
+    with pytest.raises(_lib.RankMixerError) as e:
+        RankMixer(T, D, k, layers, gemm_path="tcgen05", dtype="f32")
+    assert e.value.status in (_lib.RM_ERR_UNSUPPORTED, _lib.RM_ERR_INVALID_ARG)
+    with pytest.raises(_lib.RankMixerError) as e:
+        m.moe_pffn_forward(0, X)
+    assert e.value.status == _lib.RM_ERR_UNSUPPORTED
+    # the context stays usable
+    m.stack_forward(X)
+    torch.cuda.synchronize()
+    assert m.sync_status() == _lib.RM_OK
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    T, D, k = 4, 256, 2
+    m, layers, X = _build(T, D, k, 1, 16, 3, "bf16")
+    m.debug_wait_timeout(2000)
+    assert m.sync_status() == _lib.RM_ERR_TIMEOUT
+    assert m.sync_status() == _lib.RM_OK      # cleared
+    out = m.block_forward(0, X)
+    torch.cuda.synchronize()
+    assert m.sync_status() == _lib.RM_OK
+    check(_np(out), oracle.block_forward(_np(X), synth.to_f64(layers)[0]), "bf16", "block after timeout")
+
+
+def test_profiler_counts_launches():
+    T, D, k, L, B = 4, 256, 2, 2, 64
+    m, _, X = _build(T, D, k, L, B, 3, "bf16")
+    m.profile(True)
+    m.stack_forward(X)
+    st = m.profile_read()
+    m.profile(False)
+    assert st["mix_ln1"][0] == L and st["gemm1"][0] == L and st["gemm2"][0] == L and st["pool"][0] == 1
+    assert all(ms >= 0 for _, ms in st.values())
+
+
+# ----------------------------------------------------------------------------
+# Full-size workloads, sampled parity
+# ----------------------------------------------------------------------------
+
+def _sampled_stack_parity(name, B, n_samples, seed, max_batch=None, model=None):
+    c = synth.CONFIGS[name]
+    T, D, k, L = c["T"], c["D"], c["k"], c["L"]
+    if model is None:
+        m, layers, _ = _build(T, D, k, L, 1, seed, "bf16", max_batch=max_batch or B)
+        p64 = synth.to_f64(layers)
+    else:
+        m, layers, p64 = model
+    X = synth.make_input(B, T, D, seed + B, "bf16", DEV)
+    pooled, XL = m.stack_forward(X, return_XL=True)
+    torch.cuda.synchronize()
+    assert m.sync_status() == _lib.RM_OK
+    rng = np.random.default_rng(seed + B)
+    idx = np.unique(np.concatenate([[0, B - 1], rng.choice(B, size=min(n_samples, B), replace=False)]))
+    pr, xr = oracle.stack_forward(_np(X[idx]), p64, return_XL=True)
+    check(_np(XL[idx]), xr, "bf16", f"{name} B={B} X_L")
+    check(_np(pooled[idx]), pr, "bf16", f"{name} B={B} pooled")
+    assert torch.isfinite(pooled).all()
+    return m
+
+
+def test_rankmixer_100m_full_size_sampled():
+    _sampled_stack_parity("rankmixer_100m", 2048, 24, 1000)
+
+
+@pytest.fixture(scope="module")
+def model_1b():
+    c = synth.CONFIGS["rankmixer_1b"]
+    layers = synth.make_stack(c["T"], c["D"], c["k"], c["L"], 2000, "bf16", DEV)
+    m = RankMixer(c["T"], c["D"], c["k"], layers, max_batch=8192)
+    assert m.path == "tcgen05"
+    p64 = synth.to_f64(layers)
+    yield m, layers, p64
+    m.close()
+
+
+def test_rankmixer_1b_full_size_sampled(model_1b):
+    _sampled_stack_parity("rankmixer_1b", 4096, 8, 2000, model=model_1b)
+
+
+@pytest.mark.parametrize("B", [1, 8, 64, 256, 1024, 8192])
+def test_rankmixer_1b_serving_sweep_sampled(model_1b, B):
+    _sampled_stack_parity("rankmixer_1b", B, 3, 2000, model=model_1b)
+
+
+# ----------------------------------------------------------------------------
+# Sparse-MoE PFFN
+# ----------------------------------------------------------------------------
+
+def _moe_oracle(S64, p64, t_slice=None):
+    return oracle.moe_pffn(S64, p64["Wg"], p64["bg"], p64["eW1"], p64["eb1"], p64["eW2"], p64["eb2"],
+                           return_gates=True)
+
+
+@pytest.mark.parametrize("dtype,path,T,D,E,Fe,B", [("bf16", "auto", 4, 256, 4, 256, 300),
+                                                   ("bf16", "simt", 4, 256, 4, 256, 300),
+                                                   ("bf16", "auto", 2, 128, 8, 384, 129),
+                                                   ("f32", "auto", 3, 16, 4, 24, 50)])
+def test_moe_pffn_small(dtype, path, T, D, E, Fe, B):
+    m, layers, _ = _build(T, D, 2, 1, B, 61 + D, dtype, path=path, E=E, Fe=Fe, active=E / 4)
+    S = synth.make_input(B, T, D, 62, dtype, DEV)
+    V, G = m.moe_pffn_forward(0, S, return_gates=True)
+    torch.cuda.synchronize()
+    assert m.sync_status() == _lib.RM_OK
+    p64 = synth.to_f64(layers[0])
+    V_ref, G_ref = _moe_oracle(_np(S), p64)
+    assert 0.1 < (G_ref > 0).mean() < 0.5, "router bias should open about a quarter of the experts"
+    np.testing.assert_allclose(_np(G), G_ref, atol=2e-4 if dtype == "bf16" else 1e-5, rtol=1e-3)
+    check(_np(V), V_ref, dtype, "MoE V")
+
+
+def test_moe_layer_inside_block():
+    T, D, E, Fe, B = 4, 256, 4, 256, 200
+    m, layers, X = _build(T, D, 2, 2, B, 71, "bf16", E=E, Fe=Fe, moe_mask=0b10, active=1.0)
+    p64 = synth.to_f64(layers)
+    X1 = m.block_forward(0, X)        # dense layer
+    X2, S2 = m.block_forward(1, X1, return_S=True)   # MoE layer
+    pooled, XL = m.stack_forward(X, return_XL=True)
+    torch.cuda.synchronize()
+    X1_ref = oracle.block_forward(_np(X), p64[0])
+    check(_np(X1), X1_ref, "bf16", "dense layer")
+    x1 = _np(X1)
+    S_ref = oracle.layernorm(oracle.token_mix(x1) + x1, p64[1]["ln1_g"], p64[1]["ln1_b"], 1e-5)
+    check(_np(S2), S_ref, "bf16", "MoE layer S")
+    V_ref = oracle.moe_pffn(_np(S2), p64[1]["Wg"], p64[1]["bg"], p64[1]["eW1"], p64[1]["eb1"], p64[1]["eW2"],
+                            p64[1]["eb2"])
+    s2 = _np(S2)
+    X2_ref = oracle.layernorm(V_ref + s2, p64[1]["ln2_g"], p64[1]["ln2_b"], 1e-5)
+    check(_np(X2), X2_ref, "bf16", "MoE layer X_out")
+    assert torch.equal(XL, X2)
+
+
+def test_moe_1b_full_size_sampled():
+    c = synth.CONFIGS["moe_1b"]
+    T, D, E, Fe, B = c["T"], c["D"], c["E"], c["Fe"], c["B"]
+    p = synth.make_experts(T, D, E, Fe, 3000, "bf16", DEV, active=c["active"])
+    dense = synth.make_layer(T, D, c["k"], 3001, "bf16", DEV)
+    dense.update(p)
+    m = RankMixer(T, D, c["k"], [dense], max_batch=B, n_experts=E, expert_hidden=Fe)
+    S = synth.make_input(B, T, D, 3002, "bf16", DEV)
+    V, G = m.moe_pffn_forward(0, S, return_gates=True)
+    torch.cuda.synchronize()
+    assert m.sync_status() == _lib.RM_OK
+    active = (G > 0).float().sum(-1).mean().item()
+    assert 1.7 < active < 2.3, f"mean active experts {active}"
+    rng = np.random.default_rng(5)
+    pairs = [(int(rng.integers(B)), int(rng.integers(T))) for _ in range(6)] + [(0, 0), (B - 1, T - 1)]
+    for b, t in pairs:
+        pt = {k: _np(v[t:t + 1]) for k, v in p.items()}
+        V_ref, G_ref = oracle.moe_pffn(_np(S[b:b + 1, t:t + 1]), pt["Wg"], pt["bg"], pt["eW1"], pt["eb1"],
+                                       pt["eW2"], pt["eb2"], return_gates=True)
+        np.testing.assert_allclose(_np(G[b:b + 1, t:t + 1]), G_ref, atol=2e-4, rtol=1e-3)
+        check(_np(V[b:b + 1, t:t + 1]), V_ref, "bf16", f"MoE V (b={b}, t={t})")
