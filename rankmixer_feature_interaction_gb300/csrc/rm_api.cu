@@ -78,6 +78,7 @@ struct rm_ctx {
     // workspace (token-major)
     int Bcap = 0;
     void* S = nullptr;
+    void* S_lo = nullptr;        // bf16 rounding remainder of S (bf16 contexts)
     void* Hid = nullptr;
     float* Z = nullptr;
     float2* stats = nullptr;
@@ -123,7 +124,7 @@ void free_ctx(rm_ctx* c) {
         moe_free_weights(l.moe);
     }
     moe_free_workspace(c->moe_ws);
-    cudaFree(c->S); cudaFree(c->Hid); cudaFree(c->Z); cudaFree(c->stats); cudaFree(c->V);
+    cudaFree(c->S); cudaFree(c->S_lo); cudaFree(c->Hid); cudaFree(c->Z); cudaFree(c->stats); cudaFree(c->V);
     cudaFree(c->X0_dev); cudaFree(c->pooled_dev);
     cudaFree(c->d_err); cudaFree(c->d_flag);
     for (auto& e : c->ev_pool) { cudaEventDestroy(e.a); cudaEventDestroy(e.b); }
@@ -164,9 +165,6 @@ rm_status validate_cfg(const rm_config* cfg) {
     if (!(cfg->ln_eps >= 0.f) || !std::isfinite(cfg->ln_eps)) return fail(RM_ERR_INVALID_ARG, "ln_eps must be >= 0");
     if (cfg->L > 32) return fail(RM_ERR_UNSUPPORTED, "at most 32 layers");
     if (cfg->T > 128) return fail(RM_ERR_UNSUPPORTED, "at most 128 tokens");
-    const size_t esz = cfg->dtype == RM_F32 ? 4 : 2;
-    if ((size_t)cfg->T * cfg->D * esz > 200 * 1024)
-        return fail(RM_ERR_UNSUPPORTED, "a sample (T*D elements) must fit 200 KB of shared memory");
     const int q = cfg->D / cfg->H;
     const bool vec2 = (q % 2 == 0) && (cfg->D % 64 == 0);
     if ((vec2 && cfg->D > 3072) || (!vec2 && cfg->D > 1536))
@@ -210,7 +208,7 @@ rm_status run_pffn(rm_ctx* c, int layer, int B, cudaStream_t s) {
         }
         if (st != RM_OK) return st;
         ProfScope ps(c, RM_K_GEMM2, s);
-        RM_CHECK_CUDA(moe_residual_z(c->act, c->V, c->S, c->Z, B, g.T, g.D, c->Bcap, s), "moe residual");
+        RM_CHECK_CUDA(moe_residual_z(c->act, c->V, c->S, c->S_lo, c->Z, B, g.T, g.D, c->Bcap, s), "moe residual");
         ProfScope ps2(c, RM_K_ROWSTATS, s);
         RM_CHECK_CUDA(launch_rowstats(c->Z, c->stats, B, g.T, g.D, c->Bcap, c->num_sms, s), "row stats");
         return RM_OK;
@@ -224,8 +222,8 @@ rm_status run_pffn(rm_ctx* c, int layer, int B, cudaStream_t s) {
         }
         {
             ProfScope ps(c, RM_K_GEMM2, s);
-            cudaError_t e = launch_gemm2_tc(c->Hid, w.W2p, w.b2, c->S, c->Z, c->stats, B, g.T, g.D, c->F, c->Bcap,
-                                            c->num_sms, c->d_err, kWaitTimeoutNs, s);
+            cudaError_t e = launch_gemm2_tc(c->Hid, w.W2p, w.b2, c->S, c->S_lo, c->Z, c->stats, B, g.T, g.D, c->F,
+                                            c->Bcap, c->num_sms, c->d_err, kWaitTimeoutNs, s);
             if (e != cudaSuccess) return cuda_fail(e, (std::string("gemm2 (tcgen05) ") + tc_last_error()).c_str());
         }
     } else {
@@ -236,7 +234,8 @@ rm_status run_pffn(rm_ctx* c, int layer, int B, cudaStream_t s) {
         }
         {
             ProfScope ps(c, RM_K_GEMM2, s);
-            RM_CHECK_CUDA(launch_gemm2_simt(c->act, c->Hid, w.W2p, w.b2, c->S, c->Z, B, g.T, g.D, c->F, c->Bcap, s),
+            RM_CHECK_CUDA(launch_gemm2_simt(c->act, c->Hid, w.W2p, w.b2, c->S, c->S_lo, c->Z, B, g.T, g.D, c->F,
+                                            c->Bcap, s),
                           "gemm2 (simt)");
         }
         ProfScope ps(c, RM_K_ROWSTATS, s);
@@ -258,6 +257,7 @@ MixLnArgs mix_args(const rm_ctx* c, int layer, int B) {
     MixLnArgs a{};
     const rm_config& g = c->cfg;
     a.S = c->S;
+    a.S_lo = c->S_lo;
     a.g1 = c->layers[layer].g1;
     a.be1 = c->layers[layer].be1;
     a.B = B;
@@ -376,6 +376,7 @@ rm_status rm_create(const rm_config* cfg, const rm_layer_params* layers, int dev
     const size_t T = cfg->T, D = cfg->D, F = c->F, Bc = c->Bcap;
     if ((st = dmalloc(c, &c->S, T * Bc * D * c->esz, &c->ws_bytes)) != RM_OK ||
         (st = dmalloc(c, &c->Hid, T * Bc * F * c->esz, &c->ws_bytes)) != RM_OK ||
+        (c->act == Act::BF16 && (st = dmalloc(c, &c->S_lo, T * Bc * D * 2, &c->ws_bytes)) != RM_OK) ||
         (st = dmalloc(c, (void**)&c->Z, T * Bc * D * 4, &c->ws_bytes)) != RM_OK ||
         (st = dmalloc(c, (void**)&c->stats, T * Bc * (size_t)c->nchunk * sizeof(float2), &c->ws_bytes)) != RM_OK ||
         (st = dmalloc(c, (void**)&c->d_err, sizeof(int), nullptr)) != RM_OK ||

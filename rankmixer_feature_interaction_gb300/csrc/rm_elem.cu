@@ -16,8 +16,8 @@ constexpr int kMixThreads = 256;
 constexpr int kMixWarps = kMixThreads / 32;
 
 // LN affine applied to a finalised row element.  Every kernel that finalises
-// LN2 uses this exact expression so the stacked and block-by-block paths
-// agree bit for bit.
+// LN2 (the next layer's mixing, the block output, the pool) uses this exact
+// expression, so they all see the same float32 value of X_n.
 __device__ __forceinline__ float ln_apply(float z, float mean, float rstd, float g, float b) {
     const float n = (z - mean) * rstd;
     return fmaf(n, g, b);
@@ -45,60 +45,86 @@ template <> struct Vec2<__nv_bfloat16> {
 
 // ---------------------------------------------------------------------------
 // Fused TokenMixing + residual + LN1.
-// One CTA per sample (grid-stride).  Phase 1 stages the sample's T x D
-// matrix X in shared memory (read from X, or finalised from the previous
-// layer's pre-LN2 rows Z).  Phase 2: one warp per output row h computes
-//   y[j] = X[t][h q + r] + X[h][j],  j = t q + r     (mix + residual)
-// keeps y in registers, reduces mean and biased variance with shuffles and
-// writes S[h] = LN1(y) token-major.
+// One CTA per sample (grid-stride), one warp per output row h:
+//   y[j] = X[t][h q + r] + X[h][j],  j = t q + r          (mix + residual)
+// with X read straight from global memory -- either the caller's X, or the
+// previous layer's pre-LN2 rows Z finalised on the fly in float32 (the row
+// statistics of the sample's T rows are merged once into shared memory).
+// y stays in registers; mean and biased variance come from two warp
+// reductions; S = LN1(y) is written token-major in the activation dtype,
+// plus (bf16) the rounding remainder S_lo used by the LN2 residual.
 // VEC = 2: each lane owns column pairs (needs q even, D % 64 == 0);
-// VEC = 1: each lane owns single columns (any q).  NI bounds D / (32 VEC).
+// VEC = 1: single columns (any q).  NI bounds D / (32 VEC).
 // ---------------------------------------------------------------------------
+constexpr int kMaxT = 128;
+
+template <typename Tact, bool FROM_Z>
+struct RowSrc {
+    const Tact* X;
+    const float* Z;
+    const float* g2;
+    const float* be2;
+    const float* mean;
+    const float* rstd;
+    size_t xrow_stride;   // elements between token rows of one sample
+    size_t zrow_stride;
+    __device__ __forceinline__ float load1(int t, int c) const {
+        if (FROM_Z) return ln_apply(Z[t * zrow_stride + c], mean[t], rstd[t], g2[c], be2[c]);
+        return to_f32(X[t * xrow_stride + c]);
+    }
+    __device__ __forceinline__ void load2(int t, int c, float& v0, float& v1) const {
+        if (FROM_Z) {
+            const float2 z = *reinterpret_cast<const float2*>(Z + t * zrow_stride + c);
+            const float2 g = *reinterpret_cast<const float2*>(g2 + c);
+            const float2 be = *reinterpret_cast<const float2*>(be2 + c);
+            v0 = ln_apply(z.x, mean[t], rstd[t], g.x, be.x);
+            v1 = ln_apply(z.y, mean[t], rstd[t], g.y, be.y);
+        } else {
+            Vec2<Tact>::split(Vec2<Tact>::load(X + t * xrow_stride + c), v0, v1);
+        }
+    }
+};
+
+template <typename Tact>
+__device__ __forceinline__ void store_s(Tact* s, __nv_bfloat16* s_lo, size_t o, float v) {
+    const Tact h = from_f32<Tact>(v);
+    s[o] = h;
+    if (s_lo) s_lo[o] = __float2bfloat16_rn(v - to_f32(h));
+}
+
 template <typename Tact, bool FROM_Z, int VEC, int NI>
 __global__ void __launch_bounds__(kMixThreads)
 mix_ln1_kernel(const MixLnArgs a) {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    Tact* xs = reinterpret_cast<Tact*>(smem_raw);   // [T][D]
+    __shared__ float s_mean[kMaxT], s_rstd[kMaxT];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int T = a.T, D = a.D, q = a.q;
-    const size_t TD = (size_t)T * D;
-    const Tact* X = reinterpret_cast<const Tact*>(a.X);
     Tact* S = reinterpret_cast<Tact*>(a.S);
-    Tact* Xp = reinterpret_cast<Tact*>(a.Xprev_out);
+    __nv_bfloat16* S_lo = reinterpret_cast<__nv_bfloat16*>(a.S_lo);
 
     for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
-        // ---- phase 1: stage X[b] ------------------------------------------
-        if (!FROM_Z) {
-            const Tact* src = X + (size_t)b * TD;
-            if (((TD * sizeof(Tact)) & 15) == 0) {
-                const uint4* s4 = reinterpret_cast<const uint4*>(src);
-                uint4* d4 = reinterpret_cast<uint4*>(xs);
-                const int n4 = (int)(TD * sizeof(Tact) / 16);
-                for (int i = threadIdx.x; i < n4; i += kMixThreads) d4[i] = __ldg(s4 + i);
-            } else {
-                for (int i = threadIdx.x; i < (int)TD; i += kMixThreads) xs[i] = src[i];
-            }
-        } else {
+        RowSrc<Tact, FROM_Z> src;
+        src.X = reinterpret_cast<const Tact*>(a.X) + (size_t)b * T * D;
+        src.Z = a.Z + (size_t)b * D;
+        src.g2 = a.g2;
+        src.be2 = a.be2;
+        src.mean = s_mean;
+        src.rstd = s_rstd;
+        src.xrow_stride = (size_t)D;
+        src.zrow_stride = (size_t)a.Bcap * D;
+        if (FROM_Z) {
             for (int t = warp; t < T; t += kMixWarps) {
-                const size_t row = (size_t)t * a.Bcap + b;
                 float mean, rstd;
-                merge_row_stats(a.stats + row * a.nchunk, a.nchunk, a.cw, D, a.eps, lane, mean, rstd);
-                const float* z = a.Z + row * D;
-                Tact* xd = xs + (size_t)t * D;
-                Tact* xo = Xp ? Xp + ((size_t)b * T + t) * D : nullptr;
-                for (int j = lane; j < D; j += 32) {
-                    const Tact v = from_f32<Tact>(ln_apply(z[j], mean, rstd, a.g2[j], a.be2[j]));
-                    xd[j] = v;
-                    if (xo) xo[j] = v;
+                merge_row_stats(a.stats + ((size_t)t * a.Bcap + b) * a.nchunk, a.nchunk, a.cw, D, a.eps, lane,
+                                mean, rstd);
+                if (lane == 0) {
+                    s_mean[t] = mean;
+                    s_rstd[t] = rstd;
                 }
             }
+            __syncthreads();
         }
-        __syncthreads();
-
-        // ---- phase 2: mix + residual + LN1, one warp per output row --------
         for (int h = warp; h < T; h += kMixWarps) {
             float y[NI * VEC];
-            const Tact* xh = xs + (size_t)h * D;
             float sum = 0.f;
             if (VEC == 2) {
                 const int ni = D >> 6;
@@ -109,8 +135,8 @@ mix_ln1_kernel(const MixLnArgs a) {
                         const int t = j / q;
                         const int r = j - t * q;
                         float m0, m1, x0, x1;
-                        Vec2<Tact>::split(Vec2<Tact>::load(xs + (size_t)t * D + h * q + r), m0, m1);
-                        Vec2<Tact>::split(Vec2<Tact>::load(xh + j), x0, x1);
+                        src.load2(t, h * q + r, m0, m1);
+                        src.load2(h, j, x0, x1);
                         y[2 * i] = m0 + x0;
                         y[2 * i + 1] = m1 + x1;
                         sum += y[2 * i] + y[2 * i + 1];
@@ -123,7 +149,7 @@ mix_ln1_kernel(const MixLnArgs a) {
                     if (j < D) {
                         const int t = j / q;
                         const int r = j - t * q;
-                        y[i] = to_f32(xs[(size_t)t * D + h * q + r]) + to_f32(xh[j]);
+                        y[i] = src.load1(t, h * q + r) + src.load1(h, j);
                         sum += y[i];
                     }
                 }
@@ -147,7 +173,7 @@ mix_ln1_kernel(const MixLnArgs a) {
                     }
             }
             const float rstd = rsqrtf(warp_sum(sq) / (float)D + a.eps);
-            Tact* srow = S + ((size_t)h * a.Bcap + b) * D;
+            const size_t srow = ((size_t)h * a.Bcap + b) * D;
             if (VEC == 2) {
                 const int ni = D >> 6;
 #pragma unroll
@@ -156,35 +182,30 @@ mix_ln1_kernel(const MixLnArgs a) {
                         const int j = (i << 6) + (lane << 1);
                         const float2 g = *reinterpret_cast<const float2*>(a.g1 + j);
                         const float2 be = *reinterpret_cast<const float2*>(a.be1 + j);
-                        Vec2<Tact>::store(srow + j, ln_apply(y[2 * i], mean, rstd, g.x, be.x),
-                                          ln_apply(y[2 * i + 1], mean, rstd, g.y, be.y));
+                        const float v0 = ln_apply(y[2 * i], mean, rstd, g.x, be.x);
+                        const float v1 = ln_apply(y[2 * i + 1], mean, rstd, g.y, be.y);
+                        Vec2<Tact>::store(S + srow + j, v0, v1);
+                        if (S_lo)
+                            Vec2<__nv_bfloat16>::store(S_lo + srow + j, v0 - to_f32(from_f32<Tact>(v0)),
+                                                       v1 - to_f32(from_f32<Tact>(v1)));
                     }
             } else {
 #pragma unroll
                 for (int i = 0; i < NI; ++i) {
                     const int j = (i << 5) + lane;
-                    if (j < D) srow[j] = from_f32<Tact>(ln_apply(y[i], mean, rstd, a.g1[j], a.be1[j]));
+                    if (j < D) store_s<Tact>(S, S_lo, srow + j, ln_apply(y[i], mean, rstd, a.g1[j], a.be1[j]));
                 }
             }
         }
-        __syncthreads();
+        if (FROM_Z) __syncthreads();   // s_mean / s_rstd are rewritten for the next sample
     }
 }
 
 template <typename Tact, bool FROM_Z, int VEC, int NI>
 cudaError_t launch_mix_inst(const MixLnArgs& a, int num_sms, cudaStream_t s) {
-    const size_t smem = (size_t)a.T * a.D * sizeof(Tact);
-    auto k = mix_ln1_kernel<Tact, FROM_Z, VEC, NI>;
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
-    int per_sm = (int)((200 * 1024) / (smem + 1024));
-    if (per_sm < 1) per_sm = 1;
-    if (per_sm > 8) per_sm = 8;
-    int grid = num_sms * per_sm;
+    int grid = num_sms * 8;
     if (grid > a.B) grid = a.B;
-    k<<<grid, kMixThreads, smem, s>>>(a);
+    mix_ln1_kernel<Tact, FROM_Z, VEC, NI><<<grid, kMixThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -227,7 +248,9 @@ __global__ void ln2_out_kernel(const float* __restrict__ Z, const float2* __rest
 }
 
 // ---------------------------------------------------------------------------
-// Last LN2 finalisation + mean pooling over tokens, one CTA per sample.
+// Last LN2 finalisation + mean pooling over tokens, one CTA per sample.  The
+// mean is taken over the float32 LN2 outputs in token order; XL (optional)
+// receives them rounded to the activation dtype.
 // ---------------------------------------------------------------------------
 constexpr int kPoolThreads = 256;
 constexpr int kPoolMaxT = 128;
@@ -253,9 +276,9 @@ pool_kernel(const float* __restrict__ Z, const float2* __restrict__ stats, const
             const float g = g2[j], be = be2[j];
             float acc = 0.f;
             for (int t = 0; t < T; ++t) {
-                const Tact v = from_f32<Tact>(ln_apply(Z[((size_t)t * Bcap + b) * D + j], s_mean[t], s_rstd[t], g, be));
-                if (XL) XL[((size_t)b * T + t) * D + j] = v;
-                acc += to_f32(v);
+                const float v = ln_apply(Z[((size_t)t * Bcap + b) * D + j], s_mean[t], s_rstd[t], g, be);
+                if (XL) XL[((size_t)b * T + t) * D + j] = from_f32<Tact>(v);
+                acc += v;
             }
             pooled[(size_t)b * D + j] = acc / (float)T;
         }

@@ -8,7 +8,8 @@
 //
 //   GEMM1: Hid[t] = Gelu(S[t] W1_t + b1_t)            (M = B, N = kD, K = D)
 //   GEMM2: Z[t]   = Hid[t] W2_t + b2_t + S[t]         (M = B, N = D,  K = kD)
-//          plus per-row, per-chunk LayerNorm partials (mean, M2) of Z
+//          plus per-row, per-chunk LayerNorm partials (mean, M2) of Z; the
+//          residual S is read as its bf16 value plus its bf16 rounding remainder
 //
 // Kernel structure (one persistent CTA per SM, 12 warps):
 //   warp 0      TMA producer: 128x64 A and BNx64 B tiles (128-byte swizzle)
@@ -77,6 +78,7 @@ struct Args {
     const float* bias;        // [weight groups][N]
     __nv_bfloat16* hid;       // EPI_GELU output rows (same row index as A)
     const __nv_bfloat16* resid;  // EPI_RESID residual rows (same row index as A)
+    const __nv_bfloat16* resid_lo;  // EPI_RESID rounding remainder of the residual (nullable)
     float* z;                 // EPI_RESID output rows
     float2* stats;            // EPI_RESID row partials [row][nchunk]
     int nchunk;
@@ -88,6 +90,22 @@ struct Args {
     int* err;
     unsigned long long timeout_ns;
 };
+
+// v[0..31] += 32 consecutive bf16 values at p (64-byte aligned).
+__device__ __forceinline__ void add_bf16x32(float (&v)[32], const __nv_bfloat16* p) {
+    const uint4* r4 = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint4 rr = __ldg(r4 + j);
+        const uint32_t w[4] = {rr.x, rr.y, rr.z, rr.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162*>(&w[h]);
+            v[8 * j + 2 * h] += __low2float(pr);
+            v[8 * j + 2 * h + 1] += __high2float(pr);
+        }
+    }
+}
 
 struct TileCoord {
     int j, mb, nb, wg, Mg;
@@ -295,18 +313,8 @@ pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     tmem_ld32(tbase + 32u * c, v);
                     if (valid) {
                         const float4* b4 = reinterpret_cast<const float4*>(bias + 32 * c);
-                        const uint4* r4 = reinterpret_cast<const uint4*>(args.resid + orow + 32 * c);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const uint4 rr = __ldg(r4 + j);
-                            const uint32_t w[4] = {rr.x, rr.y, rr.z, rr.w};
-#pragma unroll
-                            for (int h = 0; h < 4; ++h) {
-                                const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162*>(&w[h]);
-                                v[8 * j + 2 * h] += __low2float(pr);
-                                v[8 * j + 2 * h + 1] += __high2float(pr);
-                            }
-                        }
+                        add_bf16x32(v, args.resid + orow + 32 * c);
+                        if (args.resid_lo) add_bf16x32(v, args.resid_lo + orow + 32 * c);
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             const float4 bb = __ldg(b4 + j);
@@ -503,8 +511,8 @@ cudaError_t launch_gemm1_tc(const void* S, const void* W1p, const float* b1, voi
     return tc::run_bn<tc::EPI_GELU>(tc::pick_bn(F), S, (long long)T * Bcap, W1p, T, a, num_sms, s);
 }
 
-cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, const void* S, float* Z,
-                            float2* stats, int B, int T, int D, int F, int Bcap, int num_sms, int* err,
+cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, const void* S, const void* S_lo,
+                            float* Z, float2* stats, int B, int T, int D, int F, int Bcap, int num_sms, int* err,
                             unsigned long long timeout_ns, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     const int bn = tc::pick_bn(D);
@@ -519,6 +527,7 @@ cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, c
     a.a_group_rows = Bcap;
     a.bias = b2;
     a.resid = reinterpret_cast<const __nv_bfloat16*>(S);
+    a.resid_lo = reinterpret_cast<const __nv_bfloat16*>(S_lo);
     a.z = Z;
     a.stats = stats;
     a.nchunk = D / (bn / 2);

@@ -27,16 +27,17 @@ struct MixLnArgs {
     const float2* stats;
     const float* g2;
     const float* be2;
-    void* Xprev_out;        // optional sample-major copy of the finalised previous X
-    // output S (token-major) and this layer's LN1 affine
+    // output S (token-major) in the activation dtype and, for bf16, its rounding
+    // remainder S_lo = bf16(S - float(S)) so that S + S_lo carries ~16 mantissa bits
     void* S;
+    void* S_lo;
     const float* g1;
     const float* be1;
     int B, T, D, q, Bcap, nchunk, cw;
     float eps;
 };
 
-// S = LN1(Mix(X) + X), X either given or finalised from (Z, stats).
+// S = LN1(Mix(X) + X), X either given or finalised from (Z, stats) in float32.
 cudaError_t launch_mix_ln1(Act act, bool from_z, const MixLnArgs& a, int num_sms, cudaStream_t s);
 
 // X_out[b][t][:] = LN2(Z[t][b][:]) in the activation dtype.
@@ -44,8 +45,8 @@ cudaError_t launch_ln2_out(Act act, const float* Z, const float2* stats, const f
                            void* X_out, int B, int T, int D, int Bcap, int nchunk, int cw, float eps,
                            int num_sms, cudaStream_t s);
 
-// pooled[b][:] = (1/T) sum_t X_L[b][t][:], X_L = LN2(Z) rounded to the activation
-// dtype; XL (optional) receives X_L sample-major.
+// pooled[b][:] = (1/T) sum_t X_L[b][t][:] with X_L = LN2(Z) in float32; XL (optional)
+// receives X_L sample-major, rounded to the activation dtype.
 cudaError_t launch_pool(Act act, const float* Z, const float2* stats, const float* g2, const float* be2,
                         float* pooled, void* XL, int B, int T, int D, int Bcap, int nchunk, int cw, float eps,
                         int num_sms, cudaStream_t s);
@@ -76,16 +77,16 @@ cudaError_t launch_debug_wait(const int* flag, int* err, unsigned long long time
 
 cudaError_t launch_gemm1_simt(Act act, const void* S, const void* W1p, const float* b1, void* Hid, int B, int T,
                               int D, int F, int Bcap, cudaStream_t s);
-cudaError_t launch_gemm2_simt(Act act, const void* Hid, const void* W2p, const float* b2, const void* S, float* Z,
-                              int B, int T, int D, int F, int Bcap, cudaStream_t s);
+cudaError_t launch_gemm2_simt(Act act, const void* Hid, const void* W2p, const float* b2, const void* S,
+                              const void* S_lo, float* Z, int B, int T, int D, int F, int Bcap, cudaStream_t s);
 
 // tcgen05 path (bf16 only).  Returns cudaErrorNotSupported for shapes it does not take.
 bool tc_supported(int D, int F);
 int tc_stats_chunk_width(int D);   // chunk width of the LN2 partial statistics written by GEMM2
 cudaError_t launch_gemm1_tc(const void* S, const void* W1p, const float* b1, void* Hid, int B, int T, int D, int F,
                             int Bcap, int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s);
-cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, const void* S, float* Z,
-                            float2* stats, int B, int T, int D, int F, int Bcap, int num_sms, int* err,
+cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, const void* S, const void* S_lo,
+                            float* Z, float2* stats, int B, int T, int D, int F, int Bcap, int num_sms, int* err,
                             unsigned long long timeout_ns, cudaStream_t s);
 
 // Set by the tensor-map encoder when the driver call fails (host-side message).

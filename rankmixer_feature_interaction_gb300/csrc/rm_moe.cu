@@ -224,15 +224,16 @@ moe_gemm_simt_kernel(const Tin* __restrict__ A, const Tin* __restrict__ W, const
 }
 
 template <typename Tact>
-__global__ void residual_z_kernel(const float* __restrict__ V, const Tact* __restrict__ S, float* __restrict__ Z,
-                                  int B, int T, int D, int Bcap) {
+__global__ void residual_z_kernel(const float* __restrict__ V, const Tact* __restrict__ S,
+                                  const __nv_bfloat16* __restrict__ S_lo, float* __restrict__ Z, int B, int T, int D,
+                                  int Bcap) {
     const long long n = (long long)T * B * D;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
         const int j = (int)(i % D);
         const long long tb = i / D;
         const int b = (int)(tb % B), t = (int)(tb / B);
         const size_t o = ((size_t)t * Bcap + b) * D + j;
-        Z[o] = V[o] + to_f32(S[o]);
+        Z[o] = V[o] + (to_f32(S[o]) + (S_lo ? __bfloat162float(S_lo[o]) : 0.f));
     }
 }
 
@@ -413,15 +414,16 @@ cudaError_t moe_forward(const MoeLaunch& ml, const MoeWeights& w, MoeWorkspace& 
     return cudaSuccess;
 }
 
-cudaError_t moe_residual_z(Act act, const float* V, const void* S, float* Z, int B, int T, int D, int Bcap,
-                           cudaStream_t s) {
+cudaError_t moe_residual_z(Act act, const float* V, const void* S, const void* S_lo, float* Z, int B, int T, int D,
+                           int Bcap, cudaStream_t s) {
     const long long n = (long long)T * B * D;
     int grid = (int)((n + 255) / 256);
     if (grid > 152 * 16) grid = 152 * 16;
     if (act == Act::BF16)
-        residual_z_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(V, (const __nv_bfloat16*)S, Z, B, T, D, Bcap);
+        residual_z_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(V, (const __nv_bfloat16*)S,
+                                                               (const __nv_bfloat16*)S_lo, Z, B, T, D, Bcap);
     else
-        residual_z_kernel<float><<<grid, 256, 0, s>>>(V, (const float*)S, Z, B, T, D, Bcap);
+        residual_z_kernel<float><<<grid, 256, 0, s>>>(V, (const float*)S, nullptr, Z, B, T, D, Bcap);
     return cudaGetLastError();
 }
 

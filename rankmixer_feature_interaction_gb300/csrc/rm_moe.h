@@ -64,8 +64,9 @@ cudaError_t moe_forward(const MoeLaunch& ml, const MoeWeights& w, MoeWorkspace& 
                         float* gates_out, cudaStream_t s, const std::function<void*(int)>& prof_begin,
                         const std::function<void(void*)>& prof_end);
 
-// Z[t][b][:] = V[t][b][:] + S[t][b][:] (token-major, V and Z float32).
-cudaError_t moe_residual_z(Act act, const float* V, const void* S, float* Z, int B, int T, int D, int Bcap,
-                           cudaStream_t s);
+// Z[t][b][:] = V[t][b][:] + S[t][b][:] (+ S_lo, the bf16 rounding remainder of S, when given);
+// token-major, V and Z float32.
+cudaError_t moe_residual_z(Act act, const float* V, const void* S, const void* S_lo, float* Z, int B, int T, int D,
+                           int Bcap, cudaStream_t s);
 
 }  // namespace rm

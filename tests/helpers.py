@@ -34,5 +34,6 @@ def check(g, o, dtype: str, what: str, tol: float | None = None) -> float:
         err = rel_err_bf16(g, o)
         tol = TOL_BF16 if tol is None else tol
     assert np.all(np.isfinite(np.asarray(g, dtype=np.float64))), f"{what}: non-finite GPU values"
+    print(f"[parity] {what}: {err:.3e} (tol {tol:.1e})")
     assert err <= tol, f"{what}: error {err:.3e} > {tol:.1e}"
     return err

@@ -94,7 +94,10 @@ def test_bf16_block_and_stack(path, T, D, k, L, B):
 
 
 @pytest.mark.parametrize("path", ["tcgen05", "simt"])
-def test_stack_equals_chained_blocks_bit_exact(path):
+def test_stack_matches_chained_blocks(path):
+    """The stack keeps X_n in float32 between layers; chaining rm_block_forward rounds
+    each X_n to bf16.  Both must agree to within two bf16 roundings, and the pooled
+    output must be the token mean of X_L."""
     T, D, k, L, B = 4, 256, 2, 3, 200
     m, layers, X = _build(T, D, k, L, B, 5, "bf16", path=path)
     pooled, XL = m.stack_forward(X, return_XL=True)
@@ -102,9 +105,11 @@ def test_stack_equals_chained_blocks_bit_exact(path):
     for n in range(L):
         Xn = m.block_forward(n, Xn)
     torch.cuda.synchronize()
-    assert torch.equal(XL, Xn)
-    ref = Xn.float().sum(dim=1) / T
-    torch.testing.assert_close(pooled, ref, rtol=1e-6, atol=1e-6)
+    check(_np(XL), _np(Xn), "bf16", "stack vs chained blocks", tol=4e-2)
+    torch.testing.assert_close(pooled, XL.float().mean(dim=1), rtol=0, atol=2e-2)
+    pr, xr = oracle.stack_forward(_np(X), synth.to_f64(layers), return_XL=True)
+    check(_np(XL), xr, "bf16", "stack X_L (L=3)")
+    check(_np(pooled), pr, "bf16", "pooled (L=3)")
 
 
 def test_tcgen05_agrees_with_simt():
@@ -295,21 +300,25 @@ def test_moe_layer_inside_block():
     T, D, E, Fe, B = 4, 256, 4, 256, 200
     m, layers, X = _build(T, D, 2, 2, B, 71, "bf16", E=E, Fe=Fe, moe_mask=0b10, active=1.0)
     p64 = synth.to_f64(layers)
-    X1 = m.block_forward(0, X)        # dense layer
-    X2, S2 = m.block_forward(1, X1, return_S=True)   # MoE layer
-    pooled, XL = m.stack_forward(X, return_XL=True)
+    X1 = m.block_forward(0, X)                        # dense layer
+    X2, S2 = m.block_forward(1, X1, return_S=True)    # MoE layer, from the bf16 X1
+    pooled, XL = m.stack_forward(X, return_XL=True)   # both layers, float32 X1
     torch.cuda.synchronize()
+    assert m.sync_status() == _lib.RM_OK
+
+    def moe_block(x, p):
+        S = oracle.layernorm(oracle.token_mix(x) + x, p["ln1_g"], p["ln1_b"], 1e-5)
+        V = oracle.moe_pffn(S, p["Wg"], p["bg"], p["eW1"], p["eb1"], p["eW2"], p["eb2"])
+        return oracle.layernorm(V + S, p["ln2_g"], p["ln2_b"], 1e-5), S
+
     X1_ref = oracle.block_forward(_np(X), p64[0])
     check(_np(X1), X1_ref, "bf16", "dense layer")
-    x1 = _np(X1)
-    S_ref = oracle.layernorm(oracle.token_mix(x1) + x1, p64[1]["ln1_g"], p64[1]["ln1_b"], 1e-5)
-    check(_np(S2), S_ref, "bf16", "MoE layer S")
-    V_ref = oracle.moe_pffn(_np(S2), p64[1]["Wg"], p64[1]["bg"], p64[1]["eW1"], p64[1]["eb1"], p64[1]["eW2"],
-                            p64[1]["eb2"])
-    s2 = _np(S2)
-    X2_ref = oracle.layernorm(V_ref + s2, p64[1]["ln2_g"], p64[1]["ln2_b"], 1e-5)
+    X2_ref, S2_ref = moe_block(_np(X1), p64[1])
+    check(_np(S2), S2_ref, "bf16", "MoE layer S")
     check(_np(X2), X2_ref, "bf16", "MoE layer X_out")
-    assert torch.equal(XL, X2)
+    XL_ref, _ = moe_block(X1_ref, p64[1])
+    check(_np(XL), XL_ref, "bf16", "stack with a MoE layer, X_L")
+    check(_np(pooled), XL_ref.mean(axis=1), "bf16", "stack with a MoE layer, pooled")
 
 
 def test_moe_1b_full_size_sampled():
