@@ -77,9 +77,8 @@ struct rm_ctx {
     std::vector<LayerW> layers;
     // workspace (token-major)
     int Bcap = 0;
-    void* S = nullptr;
-    void* S_lo = nullptr;        // bf16 rounding remainder of S (bf16 contexts)
-    void* Hid = nullptr;
+    void* S = nullptr;           // operand type (fp16 for bf16 contexts)
+    void* Hid = nullptr;         // operand type
     float* Z = nullptr;
     float2* stats = nullptr;
     float* V = nullptr;          // MoE PFFN output inside the stack
@@ -124,7 +123,7 @@ void free_ctx(rm_ctx* c) {
         moe_free_weights(l.moe);
     }
     moe_free_workspace(c->moe_ws);
-    cudaFree(c->S); cudaFree(c->S_lo); cudaFree(c->Hid); cudaFree(c->Z); cudaFree(c->stats); cudaFree(c->V);
+    cudaFree(c->S); cudaFree(c->Hid); cudaFree(c->Z); cudaFree(c->stats); cudaFree(c->V);
     cudaFree(c->X0_dev); cudaFree(c->pooled_dev);
     cudaFree(c->d_err); cudaFree(c->d_flag);
     for (auto& e : c->ev_pool) { cudaEventDestroy(e.a); cudaEventDestroy(e.b); }
@@ -208,7 +207,7 @@ rm_status run_pffn(rm_ctx* c, int layer, int B, cudaStream_t s) {
         }
         if (st != RM_OK) return st;
         ProfScope ps(c, RM_K_GEMM2, s);
-        RM_CHECK_CUDA(moe_residual_z(c->act, c->V, c->S, c->S_lo, c->Z, B, g.T, g.D, c->Bcap, s), "moe residual");
+        RM_CHECK_CUDA(moe_residual_z(c->act, c->V, c->S, c->Z, B, g.T, g.D, c->Bcap, s), "moe residual");
         ProfScope ps2(c, RM_K_ROWSTATS, s);
         RM_CHECK_CUDA(launch_rowstats(c->Z, c->stats, B, g.T, g.D, c->Bcap, c->num_sms, s), "row stats");
         return RM_OK;
@@ -222,8 +221,8 @@ rm_status run_pffn(rm_ctx* c, int layer, int B, cudaStream_t s) {
         }
         {
             ProfScope ps(c, RM_K_GEMM2, s);
-            cudaError_t e = launch_gemm2_tc(c->Hid, w.W2p, w.b2, c->S, c->S_lo, c->Z, c->stats, B, g.T, g.D, c->F,
-                                            c->Bcap, c->num_sms, c->d_err, kWaitTimeoutNs, s);
+            cudaError_t e = launch_gemm2_tc(c->Hid, w.W2p, w.b2, c->S, c->Z, c->stats, B, g.T, g.D, c->F, c->Bcap,
+                                            c->num_sms, c->d_err, kWaitTimeoutNs, s);
             if (e != cudaSuccess) return cuda_fail(e, (std::string("gemm2 (tcgen05) ") + tc_last_error()).c_str());
         }
     } else {
@@ -234,8 +233,7 @@ rm_status run_pffn(rm_ctx* c, int layer, int B, cudaStream_t s) {
         }
         {
             ProfScope ps(c, RM_K_GEMM2, s);
-            RM_CHECK_CUDA(launch_gemm2_simt(c->act, c->Hid, w.W2p, w.b2, c->S, c->S_lo, c->Z, B, g.T, g.D, c->F,
-                                            c->Bcap, s),
+            RM_CHECK_CUDA(launch_gemm2_simt(c->act, c->Hid, w.W2p, w.b2, c->S, c->Z, B, g.T, g.D, c->F, c->Bcap, s),
                           "gemm2 (simt)");
         }
         ProfScope ps(c, RM_K_ROWSTATS, s);
@@ -257,7 +255,6 @@ MixLnArgs mix_args(const rm_ctx* c, int layer, int B) {
     MixLnArgs a{};
     const rm_config& g = c->cfg;
     a.S = c->S;
-    a.S_lo = c->S_lo;
     a.g1 = c->layers[layer].g1;
     a.be1 = c->layers[layer].be1;
     a.B = B;
@@ -313,8 +310,8 @@ rm_status pack_layer(rm_ctx* c, const rm_layer_params& p, LayerW& w, cudaStream_
     for (int i = 0; i < 4; ++i)
         if ((st = dmalloc(c, (void**)lnp[i], (size_t)D * 4, &c->weight_bytes)) != RM_OK) return st;
     // W1 [T][D][F] -> W1p [T][F][D];  W2 [T][F][D] -> W2p [T][D][F]
-    RM_CHECK_CUDA(launch_transpose(p.W1, w.W1p, T, D, F, (int)c->esz, s), "pack W1");
-    RM_CHECK_CUDA(launch_transpose(p.W2, w.W2p, T, F, D, (int)c->esz, s), "pack W2");
+    RM_CHECK_CUDA(launch_pack_transpose(c->act, p.W1, w.W1p, T, D, F, s), "pack W1");
+    RM_CHECK_CUDA(launch_pack_transpose(c->act, p.W2, w.W2p, T, F, D, s), "pack W2");
     RM_CHECK_CUDA(launch_to_f32(c->act, p.b1, w.b1, (size_t)T * F, s), "pack b1");
     RM_CHECK_CUDA(launch_to_f32(c->act, p.b2, w.b2, (size_t)T * D, s), "pack b2");
     for (int i = 0; i < 4; ++i) RM_CHECK_CUDA(launch_to_f32(c->act, lns[i], *lnp[i], (size_t)D, s), "pack LN");
@@ -376,7 +373,6 @@ rm_status rm_create(const rm_config* cfg, const rm_layer_params* layers, int dev
     const size_t T = cfg->T, D = cfg->D, F = c->F, Bc = c->Bcap;
     if ((st = dmalloc(c, &c->S, T * Bc * D * c->esz, &c->ws_bytes)) != RM_OK ||
         (st = dmalloc(c, &c->Hid, T * Bc * F * c->esz, &c->ws_bytes)) != RM_OK ||
-        (c->act == Act::BF16 && (st = dmalloc(c, &c->S_lo, T * Bc * D * 2, &c->ws_bytes)) != RM_OK) ||
         (st = dmalloc(c, (void**)&c->Z, T * Bc * D * 4, &c->ws_bytes)) != RM_OK ||
         (st = dmalloc(c, (void**)&c->stats, T * Bc * (size_t)c->nchunk * sizeof(float2), &c->ws_bytes)) != RM_OK ||
         (st = dmalloc(c, (void**)&c->d_err, sizeof(int), nullptr)) != RM_OK ||

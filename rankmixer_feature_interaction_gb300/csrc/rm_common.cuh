@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -17,12 +18,25 @@ namespace rm {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+
+// fp16 stores saturate finite overflow at +-65504 (NaN stays NaN).  The
+// tensor-core operands of the bf16 path are fp16: LN outputs are bounded by
+// sqrt(D) max|gamma| + max|beta| and GELU outputs by their input, far inside
+// fp16's range, and fp16 carries 3 more mantissa bits than bf16.
+__device__ __forceinline__ float sat_f16(float x) { return fabsf(x) > 65504.f ? copysignf(65504.f, x) : x; }
+
 template <typename T> __device__ __forceinline__ T from_f32(float x);
 template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+template <> __device__ __forceinline__ __half from_f32<__half>(float x) { return __float2half_rn(sat_f16(x)); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(sat_f16(lo), sat_f16(hi));
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
@@ -167,8 +181,8 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T, bf16 x bf16 -> f32, both operands K-major.
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+// D[tmem] (+)= A[smem] * B[smem]^T, 16-bit operands -> f32, both K-major.
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                           uint32_t accumulate) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
@@ -203,7 +217,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 }
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
-// with 128-byte swizzling: rows of 64 bf16 (128 B), 8-row swizzle atoms of
+// with 128-byte swizzling: rows of 64 16-bit elements (128 B), 8-row swizzle atoms of
 // 1024 B stacked along M/N (stride-byte-offset 1024), descriptor version 1,
 // layout type 2 (SWIZZLE_128B).  The tile base must be 1024-byte aligned;
 // stepping K by 16 elements inside the atom adds 32 B to the start address.
@@ -217,12 +231,12 @@ __device__ __forceinline__ uint64_t make_sw128_desc(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor for kind::f16: D f32, A and B bf16, both K-major,
-// N >> 3 at bit 17, M >> 4 at bit 24.
-__host__ __device__ constexpr uint32_t make_idesc_bf16_f32(int M, int N) {
+// Instruction descriptor for kind::f16: D f32, A and B fp16 (format 0), both
+// K-major, N >> 3 at bit 17, M >> 4 at bit 24.  A and B always share a type.
+__host__ __device__ constexpr uint32_t make_idesc_f16_f32(int M, int N) {
     return (1u << 4)                        // D format: f32
-         | (1u << 7)                        // A format: bf16
-         | (1u << 10)                       // B format: bf16
+         | (0u << 7)                        // A format: f16
+         | (0u << 10)                       // B format: f16
          | ((uint32_t)(N >> 3) << 17)
          | ((uint32_t)(M >> 4) << 24);
 }

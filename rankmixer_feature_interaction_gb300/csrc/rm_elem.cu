@@ -30,6 +30,16 @@ template <> struct Vec2<float> {
     __device__ static void store(float* p, float a, float b) { *reinterpret_cast<float2*>(p) = make_float2(a, b); }
     __device__ static void split(float2 v, float& a, float& b) { a = v.x; b = v.y; }
 };
+template <> struct Vec2<__half> {
+    __device__ static __half2 load(const __half* p) { return *reinterpret_cast<const __half2*>(p); }
+    __device__ static void store(__half* p, float a, float b) {
+        *reinterpret_cast<__half2*>(p) = __floats2half2_rn(sat_f16(a), sat_f16(b));
+    }
+    __device__ static void split(__half2 v, float& a, float& b) {
+        a = __low2float(v);
+        b = __high2float(v);
+    }
+};
 template <> struct Vec2<__nv_bfloat16> {
     __device__ static __nv_bfloat162 load(const __nv_bfloat16* p) {
         return *reinterpret_cast<const __nv_bfloat162*>(p);
@@ -51,16 +61,16 @@ template <> struct Vec2<__nv_bfloat16> {
 // previous layer's pre-LN2 rows Z finalised on the fly in float32 (the row
 // statistics of the sample's T rows are merged once into shared memory).
 // y stays in registers; mean and biased variance come from two warp
-// reductions; S = LN1(y) is written token-major in the activation dtype,
-// plus (bf16) the rounding remainder S_lo used by the LN2 residual.
+// reductions; S = LN1(y) is written token-major in the operand type Top
+// (fp16 for bf16 contexts, float for float32 contexts).
 // VEC = 2: each lane owns column pairs (needs q even, D % 64 == 0);
 // VEC = 1: single columns (any q).  NI bounds D / (32 VEC).
 // ---------------------------------------------------------------------------
 constexpr int kMaxT = 128;
 
-template <typename Tact, bool FROM_Z>
+template <typename Tin, bool FROM_Z>
 struct RowSrc {
-    const Tact* X;
+    const Tin* X;
     const float* Z;
     const float* g2;
     const float* be2;
@@ -80,30 +90,22 @@ struct RowSrc {
             v0 = ln_apply(z.x, mean[t], rstd[t], g.x, be.x);
             v1 = ln_apply(z.y, mean[t], rstd[t], g.y, be.y);
         } else {
-            Vec2<Tact>::split(Vec2<Tact>::load(X + t * xrow_stride + c), v0, v1);
+            Vec2<Tin>::split(Vec2<Tin>::load(X + t * xrow_stride + c), v0, v1);
         }
     }
 };
 
-template <typename Tact>
-__device__ __forceinline__ void store_s(Tact* s, __nv_bfloat16* s_lo, size_t o, float v) {
-    const Tact h = from_f32<Tact>(v);
-    s[o] = h;
-    if (s_lo) s_lo[o] = __float2bfloat16_rn(v - to_f32(h));
-}
-
-template <typename Tact, bool FROM_Z, int VEC, int NI>
+template <typename Tin, typename Top, bool FROM_Z, int VEC, int NI>
 __global__ void __launch_bounds__(kMixThreads)
 mix_ln1_kernel(const MixLnArgs a) {
     __shared__ float s_mean[kMaxT], s_rstd[kMaxT];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int T = a.T, D = a.D, q = a.q;
-    Tact* S = reinterpret_cast<Tact*>(a.S);
-    __nv_bfloat16* S_lo = reinterpret_cast<__nv_bfloat16*>(a.S_lo);
+    Top* S = reinterpret_cast<Top*>(a.S);
 
     for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
-        RowSrc<Tact, FROM_Z> src;
-        src.X = reinterpret_cast<const Tact*>(a.X) + (size_t)b * T * D;
+        RowSrc<Tin, FROM_Z> src;
+        src.X = reinterpret_cast<const Tin*>(a.X) + (size_t)b * T * D;
         src.Z = a.Z + (size_t)b * D;
         src.g2 = a.g2;
         src.be2 = a.be2;
@@ -184,16 +186,13 @@ mix_ln1_kernel(const MixLnArgs a) {
                         const float2 be = *reinterpret_cast<const float2*>(a.be1 + j);
                         const float v0 = ln_apply(y[2 * i], mean, rstd, g.x, be.x);
                         const float v1 = ln_apply(y[2 * i + 1], mean, rstd, g.y, be.y);
-                        Vec2<Tact>::store(S + srow + j, v0, v1);
-                        if (S_lo)
-                            Vec2<__nv_bfloat16>::store(S_lo + srow + j, v0 - to_f32(from_f32<Tact>(v0)),
-                                                       v1 - to_f32(from_f32<Tact>(v1)));
+                        Vec2<Top>::store(S + srow + j, v0, v1);
                     }
             } else {
 #pragma unroll
                 for (int i = 0; i < NI; ++i) {
                     const int j = (i << 5) + lane;
-                    if (j < D) store_s<Tact>(S, S_lo, srow + j, ln_apply(y[i], mean, rstd, a.g1[j], a.be1[j]));
+                    if (j < D) S[srow + j] = from_f32<Top>(ln_apply(y[i], mean, rstd, a.g1[j], a.be1[j]));
                 }
             }
         }
@@ -201,28 +200,28 @@ mix_ln1_kernel(const MixLnArgs a) {
     }
 }
 
-template <typename Tact, bool FROM_Z, int VEC, int NI>
+template <typename Tin, typename Top, bool FROM_Z, int VEC, int NI>
 cudaError_t launch_mix_inst(const MixLnArgs& a, int num_sms, cudaStream_t s) {
     int grid = num_sms * 8;
     if (grid > a.B) grid = a.B;
-    mix_ln1_kernel<Tact, FROM_Z, VEC, NI><<<grid, kMixThreads, 0, s>>>(a);
+    mix_ln1_kernel<Tin, Top, FROM_Z, VEC, NI><<<grid, kMixThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
-template <typename Tact, bool FROM_Z>
+template <typename Tin, typename Top, bool FROM_Z>
 cudaError_t launch_mix_dispatch(const MixLnArgs& a, int num_sms, cudaStream_t s) {
     const bool vec2 = (a.q % 2 == 0) && (a.D % 64 == 0);
     if (vec2) {
         const int ni = a.D / 64;
-        if (ni <= 4) return launch_mix_inst<Tact, FROM_Z, 2, 4>(a, num_sms, s);
-        if (ni <= 12) return launch_mix_inst<Tact, FROM_Z, 2, 12>(a, num_sms, s);
-        if (ni <= 24) return launch_mix_inst<Tact, FROM_Z, 2, 24>(a, num_sms, s);
-        if (ni <= 48) return launch_mix_inst<Tact, FROM_Z, 2, 48>(a, num_sms, s);
+        if (ni <= 4) return launch_mix_inst<Tin, Top, FROM_Z, 2, 4>(a, num_sms, s);
+        if (ni <= 12) return launch_mix_inst<Tin, Top, FROM_Z, 2, 12>(a, num_sms, s);
+        if (ni <= 24) return launch_mix_inst<Tin, Top, FROM_Z, 2, 24>(a, num_sms, s);
+        if (ni <= 48) return launch_mix_inst<Tin, Top, FROM_Z, 2, 48>(a, num_sms, s);
         return cudaErrorNotSupported;
     }
     const int ni = (a.D + 31) / 32;
-    if (ni <= 8) return launch_mix_inst<Tact, FROM_Z, 1, 8>(a, num_sms, s);
-    if (ni <= 48) return launch_mix_inst<Tact, FROM_Z, 1, 48>(a, num_sms, s);
+    if (ni <= 8) return launch_mix_inst<Tin, Top, FROM_Z, 1, 8>(a, num_sms, s);
+    if (ni <= 48) return launch_mix_inst<Tin, Top, FROM_Z, 1, 48>(a, num_sms, s);
     return cudaErrorNotSupported;
 }
 
@@ -314,15 +313,15 @@ __global__ void rowstats_kernel(const float* __restrict__ Z, float2* __restrict_
 // ---------------------------------------------------------------------------
 // Layout helpers
 // ---------------------------------------------------------------------------
-template <typename E>
-__global__ void token_to_sample_kernel(const E* __restrict__ src, E* __restrict__ dst, int B, int T, int D,
+template <typename Top, typename Tout>
+__global__ void token_to_sample_kernel(const Top* __restrict__ src, Tout* __restrict__ dst, int B, int T, int D,
                                        int Bcap) {
     const long long n = (long long)B * T * D;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
         const int j = (int)(i % D);
         const long long bt = i / D;
         const int t = (int)(bt % T), b = (int)(bt / T);
-        dst[i] = src[((size_t)t * Bcap + b) * D + j];
+        dst[i] = from_f32<Tout>(to_f32(src[((size_t)t * Bcap + b) * D + j]));
     }
 }
 
@@ -342,21 +341,22 @@ __global__ void token_mix_kernel(const E* __restrict__ X, E* __restrict__ Y, int
     }
 }
 
-template <typename E>
-__global__ void transpose_kernel(const E* __restrict__ in, E* __restrict__ out, int R, int C) {
-    __shared__ E tile[32][33];
+// out[g][c][r] = convert(in[g][r][c]), 32x32 tiles through shared memory.
+template <typename Ein, typename Eout>
+__global__ void transpose_kernel(const Ein* __restrict__ in, Eout* __restrict__ out, int R, int C) {
+    __shared__ float tile[32][33];
     const size_t g = blockIdx.z;
-    const E* src = in + g * (size_t)R * C;
-    E* dst = out + g * (size_t)R * C;
+    const Ein* src = in + g * (size_t)R * C;
+    Eout* dst = out + g * (size_t)R * C;
     const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
     for (int i = threadIdx.y; i < 32; i += 8) {
         const int r = r0 + i, c = c0 + threadIdx.x;
-        if (r < R && c < C) tile[i][threadIdx.x] = src[(size_t)r * C + c];
+        if (r < R && c < C) tile[i][threadIdx.x] = to_f32(src[(size_t)r * C + c]);
     }
     __syncthreads();
     for (int i = threadIdx.y; i < 32; i += 8) {
         const int c = c0 + i, r = r0 + threadIdx.x;
-        if (r < R && c < C) dst[(size_t)c * R + r] = tile[threadIdx.x][i];
+        if (r < R && c < C) dst[(size_t)c * R + r] = from_f32<Eout>(tile[threadIdx.x][i]);
     }
 }
 
@@ -390,9 +390,10 @@ inline int grid_for(long long n, int threads, int cap = 152 * 16) {
 cudaError_t launch_mix_ln1(Act act, bool from_z, const MixLnArgs& a, int num_sms, cudaStream_t s) {
     if (a.B <= 0) return cudaSuccess;
     if (act == Act::BF16)
-        return from_z ? launch_mix_dispatch<__nv_bfloat16, true>(a, num_sms, s)
-                      : launch_mix_dispatch<__nv_bfloat16, false>(a, num_sms, s);
-    return from_z ? launch_mix_dispatch<float, true>(a, num_sms, s) : launch_mix_dispatch<float, false>(a, num_sms, s);
+        return from_z ? launch_mix_dispatch<__nv_bfloat16, __half, true>(a, num_sms, s)
+                      : launch_mix_dispatch<__nv_bfloat16, __half, false>(a, num_sms, s);
+    return from_z ? launch_mix_dispatch<float, float, true>(a, num_sms, s)
+                  : launch_mix_dispatch<float, float, false>(a, num_sms, s);
 }
 
 cudaError_t launch_ln2_out(Act act, const float* Z, const float2* stats, const float* g2, const float* be2,
@@ -436,9 +437,10 @@ cudaError_t launch_token_to_sample(Act act, const void* src, void* dst, int B, i
     if (B <= 0) return cudaSuccess;
     const int grid = grid_for((long long)B * T * D, 256);
     if (act == Act::BF16)
-        token_to_sample_kernel<uint16_t><<<grid, 256, 0, s>>>((const uint16_t*)src, (uint16_t*)dst, B, T, D, Bcap);
+        token_to_sample_kernel<__half, __nv_bfloat16><<<grid, 256, 0, s>>>((const __half*)src, (__nv_bfloat16*)dst,
+                                                                           B, T, D, Bcap);
     else
-        token_to_sample_kernel<uint32_t><<<grid, 256, 0, s>>>((const uint32_t*)src, (uint32_t*)dst, B, T, D, Bcap);
+        token_to_sample_kernel<float, float><<<grid, 256, 0, s>>>((const float*)src, (float*)dst, B, T, D, Bcap);
     return cudaGetLastError();
 }
 
@@ -454,15 +456,20 @@ cudaError_t launch_token_mix(const void* X, void* Y, int B, int T, int D, int H,
     return cudaGetLastError();
 }
 
-cudaError_t launch_transpose(const void* in, void* out, int G, int R, int C, int esz, cudaStream_t s) {
+cudaError_t launch_pack_transpose(Act act, const void* in, void* out, int G, int R, int C, cudaStream_t s) {
     if (G <= 0 || R <= 0 || C <= 0) return cudaSuccess;
     dim3 grid((C + 31) / 32, (R + 31) / 32, G), block(32, 8);
-    if (esz == 2)
-        transpose_kernel<uint16_t><<<grid, block, 0, s>>>((const uint16_t*)in, (uint16_t*)out, R, C);
-    else if (esz == 4)
-        transpose_kernel<uint32_t><<<grid, block, 0, s>>>((const uint32_t*)in, (uint32_t*)out, R, C);
+    if (act == Act::BF16)
+        transpose_kernel<__nv_bfloat16, __half><<<grid, block, 0, s>>>((const __nv_bfloat16*)in, (__half*)out, R, C);
     else
-        return cudaErrorInvalidValue;
+        transpose_kernel<float, float><<<grid, block, 0, s>>>((const float*)in, (float*)out, R, C);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_f32(const float* in, float* out, int G, int R, int C, cudaStream_t s) {
+    if (G <= 0 || R <= 0 || C <= 0) return cudaSuccess;
+    dim3 grid((C + 31) / 32, (R + 31) / 32, G), block(32, 8);
+    transpose_kernel<float, float><<<grid, block, 0, s>>>(in, out, R, C);
     return cudaGetLastError();
 }
 

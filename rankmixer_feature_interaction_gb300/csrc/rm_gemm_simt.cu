@@ -1,6 +1,8 @@
 // CUDA-core per-token FFN GEMMs.  Used for the float32 path (the tensor
 // cores have no exact-fp32 MMA kind) and for shapes the tcgen05 kernels do
 // not tile.  Grouped: grid.z = token t, each token with its own weights.
+// Operands are float32 (float32 contexts) or fp16 (bf16 contexts), as on the
+// tensor-core path; accumulation is float32.
 //
 // "RankMixer: Scaling Up Ranking Models in Industrial Recommenders", section
 // 3.3.2 Eq. 6-7: u_t = s_t W1_t + b1_t, a_t = Gelu(u_t), v_t = a_t W2_t + b2_t.
@@ -19,8 +21,7 @@ enum { EPI_GELU = 1, EPI_RESID = 2 };
 template <typename Tin, int EPI>
 __global__ void __launch_bounds__(256)
 gemm_simt_kernel(const Tin* __restrict__ A, const Tin* __restrict__ W, const float* __restrict__ bias,
-                 void* __restrict__ out, const Tin* __restrict__ resid, const __nv_bfloat16* __restrict__ resid_lo,
-                 int M, int N, int K, int Bcap) {
+                 void* __restrict__ out, const Tin* __restrict__ resid, int M, int N, int K, int Bcap) {
     __shared__ float As[TK][TM + 4];
     __shared__ float Ws[TK][TN + 4];
     const int t = blockIdx.z;
@@ -72,19 +73,18 @@ gemm_simt_kernel(const Tin* __restrict__ A, const Tin* __restrict__ W, const flo
             if (EPI == EPI_GELU) {
                 reinterpret_cast<Tin*>(out)[o] = from_f32<Tin>(gelu_erf(u));
             } else {
-                const float r = to_f32(resid[o]) + (resid_lo ? __bfloat162float(resid_lo[o]) : 0.f);
-                reinterpret_cast<float*>(out)[o] = u + r;
+                reinterpret_cast<float*>(out)[o] = u + to_f32(resid[o]);
             }
         }
     }
 }
 
 template <typename Tin, int EPI>
-cudaError_t launch(const void* A, const void* W, const float* bias, void* out, const void* resid, const void* resid_lo,
-                   int M, int N, int K, int T, int Bcap, cudaStream_t s) {
+cudaError_t launch(const void* A, const void* W, const float* bias, void* out, const void* resid, int M, int N, int K,
+                   int T, int Bcap, cudaStream_t s) {
     dim3 grid((N + TN - 1) / TN, (M + TM - 1) / TM, T);
-    gemm_simt_kernel<Tin, EPI><<<grid, 256, 0, s>>>((const Tin*)A, (const Tin*)W, bias, out, (const Tin*)resid,
-                                                    (const __nv_bfloat16*)resid_lo, M, N, K, Bcap);
+    gemm_simt_kernel<Tin, EPI><<<grid, 256, 0, s>>>((const Tin*)A, (const Tin*)W, bias, out, (const Tin*)resid, M, N,
+                                                    K, Bcap);
     return cudaGetLastError();
 }
 
@@ -93,16 +93,15 @@ cudaError_t launch(const void* A, const void* W, const float* bias, void* out, c
 cudaError_t launch_gemm1_simt(Act act, const void* S, const void* W1p, const float* b1, void* Hid, int B, int T,
                               int D, int F, int Bcap, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
-    if (act == Act::BF16)
-        return launch<__nv_bfloat16, EPI_GELU>(S, W1p, b1, Hid, nullptr, nullptr, B, F, D, T, Bcap, s);
-    return launch<float, EPI_GELU>(S, W1p, b1, Hid, nullptr, nullptr, B, F, D, T, Bcap, s);
+    if (act == Act::BF16) return launch<__half, EPI_GELU>(S, W1p, b1, Hid, nullptr, B, F, D, T, Bcap, s);
+    return launch<float, EPI_GELU>(S, W1p, b1, Hid, nullptr, B, F, D, T, Bcap, s);
 }
 
-cudaError_t launch_gemm2_simt(Act act, const void* Hid, const void* W2p, const float* b2, const void* S,
-                              const void* S_lo, float* Z, int B, int T, int D, int F, int Bcap, cudaStream_t s) {
+cudaError_t launch_gemm2_simt(Act act, const void* Hid, const void* W2p, const float* b2, const void* S, float* Z,
+                              int B, int T, int D, int F, int Bcap, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
-    if (act == Act::BF16) return launch<__nv_bfloat16, EPI_RESID>(Hid, W2p, b2, Z, S, S_lo, B, D, F, T, Bcap, s);
-    return launch<float, EPI_RESID>(Hid, W2p, b2, Z, S, nullptr, B, D, F, T, Bcap, s);
+    if (act == Act::BF16) return launch<__half, EPI_RESID>(Hid, W2p, b2, Z, S, B, D, F, T, Bcap, s);
+    return launch<float, EPI_RESID>(Hid, W2p, b2, Z, S, B, D, F, T, Bcap, s);
 }
 
 }  // namespace rm

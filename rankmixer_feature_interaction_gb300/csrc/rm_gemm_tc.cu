@@ -8,8 +8,9 @@
 //
 //   GEMM1: Hid[t] = Gelu(S[t] W1_t + b1_t)            (M = B, N = kD, K = D)
 //   GEMM2: Z[t]   = Hid[t] W2_t + b2_t + S[t]         (M = B, N = D,  K = kD)
-//          plus per-row, per-chunk LayerNorm partials (mean, M2) of Z; the
-//          residual S is read as its bf16 value plus its bf16 rounding remainder
+//          plus per-row, per-chunk LayerNorm partials (mean, M2) of Z
+// Operands are fp16 (10-bit mantissa; the weights are converted exactly from
+// bf16 when the context is created), accumulation is fp32 in TMEM.
 //
 // Kernel structure (one persistent CTA per SM, 12 warps):
 //   warp 0      TMA producer: 128x64 A and BNx64 B tiles (128-byte swizzle)
@@ -37,7 +38,7 @@ namespace rm {
 namespace tc {
 
 constexpr int BM = 128;
-constexpr int BK = 64;                 // one 128-byte swizzle row of bf16
+constexpr int BK = 64;                 // one 128-byte swizzle row of fp16
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 128 + kEpiWarps * 32;
 
@@ -76,9 +77,8 @@ struct Args {
     const int* g_off;
     const int* tile_prefix;
     const float* bias;        // [weight groups][N]
-    __nv_bfloat16* hid;       // EPI_GELU output rows (same row index as A)
-    const __nv_bfloat16* resid;  // EPI_RESID residual rows (same row index as A)
-    const __nv_bfloat16* resid_lo;  // EPI_RESID rounding remainder of the residual (nullable)
+    __half* hid;              // EPI_GELU output rows (same row index as A), fp16
+    const __half* resid;      // EPI_RESID residual rows (same row index as A), fp16
     float* z;                 // EPI_RESID output rows
     float2* stats;            // EPI_RESID row partials [row][nchunk]
     int nchunk;
@@ -91,8 +91,8 @@ struct Args {
     unsigned long long timeout_ns;
 };
 
-// v[0..31] += 32 consecutive bf16 values at p (64-byte aligned).
-__device__ __forceinline__ void add_bf16x32(float (&v)[32], const __nv_bfloat16* p) {
+// v[0..31] += 32 consecutive fp16 values at p (64-byte aligned).
+__device__ __forceinline__ void add_f16x32(float (&v)[32], const __half* p) {
     const uint4* r4 = reinterpret_cast<const uint4*>(p);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -100,7 +100,7 @@ __device__ __forceinline__ void add_bf16x32(float (&v)[32], const __nv_bfloat16*
         const uint32_t w[4] = {rr.x, rr.y, rr.z, rr.w};
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-            const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162*>(&w[h]);
+            const __half2 pr = *reinterpret_cast<const __half2*>(&w[h]);
             v[8 * j + 2 * h] += __low2float(pr);
             v[8 * j + 2 * h + 1] += __high2float(pr);
         }
@@ -221,7 +221,7 @@ pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     } else if (warp == 1) {
         // ------------------------------ MMA issuer --------------------------------
         if (lane == 0) {
-            constexpr uint32_t idesc = make_idesc_bf16_f32(BM, BN);
+            constexpr uint32_t idesc = make_idesc_f16_f32(BM, BN);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -244,7 +244,7 @@ pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint32_t b0 = sB + stage * C::B_BYTES;
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
-                        umma_bf16(d_tmem, make_sw128_desc(a0 + 32u * k), make_sw128_desc(b0 + 32u * k), idesc,
+                        umma_f16(d_tmem, make_sw128_desc(a0 + 32u * k), make_sw128_desc(b0 + 32u * k), idesc,
                                   (kb > 0 || k > 0) ? 1u : 0u);
                     }
                     umma_commit(empty_bar(stage));
@@ -296,8 +296,8 @@ pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             const float4 bb = __ldg(b4 + j);
-                            p[2 * j] = pack_bf16x2(gelu_erf(v[4 * j] + bb.x), gelu_erf(v[4 * j + 1] + bb.y));
-                            p[2 * j + 1] = pack_bf16x2(gelu_erf(v[4 * j + 2] + bb.z), gelu_erf(v[4 * j + 3] + bb.w));
+                            p[2 * j] = pack_f16x2(gelu_erf(v[4 * j] + bb.x), gelu_erf(v[4 * j + 1] + bb.y));
+                            p[2 * j + 1] = pack_f16x2(gelu_erf(v[4 * j + 2] + bb.z), gelu_erf(v[4 * j + 3] + bb.w));
                         }
                         uint4* dst = reinterpret_cast<uint4*>(args.hid + orow + 32 * c);
 #pragma unroll
@@ -313,8 +313,7 @@ pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     tmem_ld32(tbase + 32u * c, v);
                     if (valid) {
                         const float4* b4 = reinterpret_cast<const float4*>(bias + 32 * c);
-                        add_bf16x32(v, args.resid + orow + 32 * c);
-                        if (args.resid_lo) add_bf16x32(v, args.resid_lo + orow + 32 * c);
+                        add_f16x32(v, args.resid + orow + 32 * c);
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             const float4 bb = __ldg(b4 + j);
@@ -413,7 +412,7 @@ bool get_encoder() {
     return true;
 }
 
-// 3-D bf16 tensor map over a [groups][rows][K] buffer (row pitch K elements,
+// 3-D fp16 tensor map over a [groups][rows][K] buffer (row pitch K elements,
 // group pitch group_rows * K), box = 64 (K) x box_rows x 1, 128-byte swizzle.
 // Rows past `rows` read as zeros.
 bool make_map(CUtensorMap* m, const void* ptr, int K, long long rows, int groups, long long group_rows,
@@ -423,7 +422,7 @@ bool make_map(CUtensorMap* m, const void* ptr, int K, long long rows, int groups
     cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)group_rows * (cuuint64_t)K * 2};
     cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
@@ -505,14 +504,14 @@ cudaError_t launch_gemm1_tc(const void* S, const void* W1p, const float* b1, voi
     a.M = B;
     a.a_group_rows = Bcap;
     a.bias = b1;
-    a.hid = reinterpret_cast<__nv_bfloat16*>(Hid);
+    a.hid = reinterpret_cast<__half*>(Hid);
     a.err = err;
     a.timeout_ns = timeout_ns;
     return tc::run_bn<tc::EPI_GELU>(tc::pick_bn(F), S, (long long)T * Bcap, W1p, T, a, num_sms, s);
 }
 
-cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, const void* S, const void* S_lo,
-                            float* Z, float2* stats, int B, int T, int D, int F, int Bcap, int num_sms, int* err,
+cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, const void* S, float* Z,
+                            float2* stats, int B, int T, int D, int F, int Bcap, int num_sms, int* err,
                             unsigned long long timeout_ns, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     const int bn = tc::pick_bn(D);
@@ -526,8 +525,7 @@ cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, c
     a.M = B;
     a.a_group_rows = Bcap;
     a.bias = b2;
-    a.resid = reinterpret_cast<const __nv_bfloat16*>(S);
-    a.resid_lo = reinterpret_cast<const __nv_bfloat16*>(S_lo);
+    a.resid = reinterpret_cast<const __half*>(S);
     a.z = Z;
     a.stats = stats;
     a.nchunk = D / (bn / 2);
@@ -550,7 +548,7 @@ cudaError_t launch_moe_gemm1_tc(const void* Sg, long long rows_total, const void
     a.g_off = g_off;
     a.tile_prefix = tile_prefix;
     a.bias = b1;
-    a.hid = reinterpret_cast<__nv_bfloat16*>(Hm);
+    a.hid = reinterpret_cast<__half*>(Hm);
     a.err = err;
     a.timeout_ns = timeout_ns;
     return tc::run_bn<tc::EPI_GELU>(tc::pick_bn(Fe), Sg, rows_total, W1p, groups, a, num_sms, s);

@@ -7,6 +7,9 @@
 
 namespace rm {
 
+// Caller-facing activation dtype of a context.  Internally a BF16 context
+// keeps its GEMM operands (S, hidden activations, packed weights) in fp16
+// ("operand" type); an F32 context keeps everything in float32.
 enum class Act { F32 = 0, BF16 = 1 };
 
 // Device error word values (latched with atomicCAS from 0).
@@ -14,39 +17,38 @@ constexpr int kDevErrTimeout = 5;
 constexpr int kDevErrOther = 6;
 
 inline size_t act_size(Act a) { return a == Act::F32 ? 4 : 2; }
+inline size_t op_size(Act a) { return a == Act::F32 ? 4 : 2; }
 
-// Token-major activation workspace: element (t, b, j) of a [T][Bcap][W] buffer
-// sits at (t * Bcap + b) * W + j.
+// Token-major workspace: element (t, b, j) of a [T][Bcap][W] buffer sits at
+// (t * Bcap + b) * W + j.
 
 struct MixLnArgs {
-    // input: either X (sample-major [B][T][D], activation dtype) ...
+    // input: either X (sample-major [B][T][D], caller dtype) ...
     const void* X;
     // ... or the previous layer's pre-LN2 rows Z (token-major fp32) with
-    // per-row chunk statistics and that layer's LN2 affine.
+    // per-row chunk statistics and that layer's LN2 affine, finalised in fp32.
     const float* Z;
     const float2* stats;
     const float* g2;
     const float* be2;
-    // output S (token-major) in the activation dtype and, for bf16, its rounding
-    // remainder S_lo = bf16(S - float(S)) so that S + S_lo carries ~16 mantissa bits
+    // output S (token-major, operand type) and this layer's LN1 affine
     void* S;
-    void* S_lo;
     const float* g1;
     const float* be1;
     int B, T, D, q, Bcap, nchunk, cw;
     float eps;
 };
 
-// S = LN1(Mix(X) + X), X either given or finalised from (Z, stats) in float32.
+// S = LN1(Mix(X) + X).
 cudaError_t launch_mix_ln1(Act act, bool from_z, const MixLnArgs& a, int num_sms, cudaStream_t s);
 
-// X_out[b][t][:] = LN2(Z[t][b][:]) in the activation dtype.
+// X_out[b][t][:] = LN2(Z[t][b][:]) in the caller dtype.
 cudaError_t launch_ln2_out(Act act, const float* Z, const float2* stats, const float* g2, const float* be2,
                            void* X_out, int B, int T, int D, int Bcap, int nchunk, int cw, float eps,
                            int num_sms, cudaStream_t s);
 
 // pooled[b][:] = (1/T) sum_t X_L[b][t][:] with X_L = LN2(Z) in float32; XL (optional)
-// receives X_L sample-major, rounded to the activation dtype.
+// receives X_L sample-major, rounded to the caller dtype.
 cudaError_t launch_pool(Act act, const float* Z, const float2* stats, const float* g2, const float* be2,
                         float* pooled, void* XL, int B, int T, int D, int Bcap, int nchunk, int cw, float eps,
                         int num_sms, cudaStream_t s);
@@ -55,17 +57,21 @@ cudaError_t launch_pool(Act act, const float* Z, const float2* stats, const floa
 cudaError_t launch_rowstats(const float* Z, float2* stats, int B, int T, int D, int Bcap, int num_sms,
                             cudaStream_t s);
 
-// Token-major [T][Bcap][D] -> sample-major [B][T][D] copy (activation dtype).
+// Token-major operand-type [T][Bcap][D] -> sample-major caller-dtype [B][T][D].
 cudaError_t launch_token_to_sample(Act act, const void* src, void* dst, int B, int T, int D, int Bcap,
                                    cudaStream_t s);
 
 // Y[b][h][t q + r] = X[b][t][h q + r] on raw element bits (esz 2 or 4).
 cudaError_t launch_token_mix(const void* X, void* Y, int B, int T, int D, int H, int esz, cudaStream_t s);
 
-// out[g][c][r] = in[g][r][c] for G matrices of R x C (element size esz, 2 or 4).
-cudaError_t launch_transpose(const void* in, void* out, int G, int R, int C, int esz, cudaStream_t s);
+// out[g][c][r] = op(in[g][r][c]) for G matrices of R x C: caller dtype in,
+// operand type out (bf16 -> fp16 conversion for BF16 contexts).
+cudaError_t launch_pack_transpose(Act act, const void* in, void* out, int G, int R, int C, cudaStream_t s);
 
-// out[i] = float(in[i]) for n elements of the given dtype.
+// out[g][c][r] = in[g][r][c], float32.
+cudaError_t launch_transpose_f32(const float* in, float* out, int G, int R, int C, cudaStream_t s);
+
+// out[i] = float(in[i]) for n elements of the caller dtype.
 cudaError_t launch_to_f32(Act act, const void* in, float* out, size_t n, cudaStream_t s);
 
 // Test hook: bounded wait on a flag nothing sets; latches kDevErrTimeout.
@@ -73,20 +79,21 @@ cudaError_t launch_debug_wait(const int* flag, int* err, unsigned long long time
 
 // ---- per-token FFN GEMMs -------------------------------------------------
 // GEMM1: Hid[t] = Gelu(S[t] W1_t + b1_t), GEMM2: Z[t] = Hid[t] W2_t + b2_t + S[t].
-// Activations token-major, weights packed K-major: W1p [T][N=kD][K=D], W2p [T][N=D][K=kD].
+// Activations token-major in the operand type, weights packed K-major:
+// W1p [T][N=kD][K=D], W2p [T][N=D][K=kD].
 
 cudaError_t launch_gemm1_simt(Act act, const void* S, const void* W1p, const float* b1, void* Hid, int B, int T,
                               int D, int F, int Bcap, cudaStream_t s);
-cudaError_t launch_gemm2_simt(Act act, const void* Hid, const void* W2p, const float* b2, const void* S,
-                              const void* S_lo, float* Z, int B, int T, int D, int F, int Bcap, cudaStream_t s);
+cudaError_t launch_gemm2_simt(Act act, const void* Hid, const void* W2p, const float* b2, const void* S, float* Z,
+                              int B, int T, int D, int F, int Bcap, cudaStream_t s);
 
-// tcgen05 path (bf16 only).  Returns cudaErrorNotSupported for shapes it does not take.
+// tcgen05 path (fp16 operands; BF16 contexts only).
 bool tc_supported(int D, int F);
 int tc_stats_chunk_width(int D);   // chunk width of the LN2 partial statistics written by GEMM2
 cudaError_t launch_gemm1_tc(const void* S, const void* W1p, const float* b1, void* Hid, int B, int T, int D, int F,
                             int Bcap, int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s);
-cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, const void* S, const void* S_lo,
-                            float* Z, float2* stats, int B, int T, int D, int F, int Bcap, int num_sms, int* err,
+cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, const void* S, float* Z,
+                            float2* stats, int B, int T, int D, int F, int Bcap, int num_sms, int* err,
                             unsigned long long timeout_ns, cudaStream_t s);
 
 // Set by the tensor-map encoder when the driver call fails (host-side message).

@@ -12,7 +12,7 @@
 //   2 count       one CTA per (t, e): number of samples with G > 0
 //   3 prefix      one thread: row offsets, 128-row tile prefixes per launch
 //   4 fill        one CTA per (t, e): ascending list of the active samples
-//   5 gather      packed rows Sg[off(t,e) + i] = S[b_i, t]
+//   5 gather      packed rows Sg[off(t,e) + i] = S[b_i, t]   (fp16 operands for bf16 contexts)
 //   6 expert L1   variable-size grouped GEMM + bias + GELU -> Hm (packed rows)
 //   7 expert L2   one launch per expert index e (fixed order e = 0..E-1):
 //                 V[b, t] += G * (Hm W2_{t,e} + b2_{t,e})
@@ -131,10 +131,10 @@ __global__ void __launch_bounds__(256) fill_kernel(const float* __restrict__ gat
 }
 
 // ---- 5: gather active rows ------------------------------------------------------------
-template <typename E>
-__global__ void gather_kernel(const E* __restrict__ S, long long s_sb, long long s_st, const int* __restrict__ counts,
-                              const int* __restrict__ offsets, const int* __restrict__ rows, E* __restrict__ Sg, int D,
-                              int NE) {
+template <typename Ein, typename Eout>
+__global__ void gather_kernel(const Ein* __restrict__ S, long long s_sb, long long s_st,
+                              const int* __restrict__ counts, const int* __restrict__ offsets,
+                              const int* __restrict__ rows, Eout* __restrict__ Sg, int D, int NE) {
     const int g = blockIdx.y;
     const int t = g / NE;
     const int cnt = counts[g], off = offsets[g];
@@ -142,9 +142,9 @@ __global__ void gather_kernel(const E* __restrict__ S, long long s_sb, long long
     const int wpb = blockDim.x >> 5;
     for (int i = blockIdx.x * wpb + (threadIdx.x >> 5); i < cnt; i += gridDim.x * wpb) {
         const int b = rows[off + i];
-        const E* src = S + b * s_sb + t * s_st;
-        E* dst = Sg + (size_t)(off + i) * D;
-        for (int j = lane; j < D; j += 32) dst[j] = src[j];
+        const Ein* src = S + b * s_sb + t * s_st;
+        Eout* dst = Sg + (size_t)(off + i) * D;
+        for (int j = lane; j < D; j += 32) dst[j] = from_f32<Eout>(to_f32(src[j]));
     }
 }
 
@@ -223,17 +223,16 @@ moe_gemm_simt_kernel(const Tin* __restrict__ A, const Tin* __restrict__ W, const
     }
 }
 
-template <typename Tact>
-__global__ void residual_z_kernel(const float* __restrict__ V, const Tact* __restrict__ S,
-                                  const __nv_bfloat16* __restrict__ S_lo, float* __restrict__ Z, int B, int T, int D,
-                                  int Bcap) {
+template <typename Top>
+__global__ void residual_z_kernel(const float* __restrict__ V, const Top* __restrict__ S, float* __restrict__ Z, int B,
+                                  int T, int D, int Bcap) {
     const long long n = (long long)T * B * D;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
         const int j = (int)(i % D);
         const long long tb = i / D;
         const int b = (int)(tb % B), t = (int)(tb / B);
         const size_t o = ((size_t)t * Bcap + b) * D + j;
-        Z[o] = V[o] + (to_f32(S[o]) + (S_lo ? __bfloat162float(S_lo[o]) : 0.f));
+        Z[o] = V[o] + to_f32(S[o]);
     }
 }
 
@@ -267,7 +266,7 @@ bool moe_use_tc(Act act, int D, int Fe) { return act == Act::BF16 && tc_supporte
 
 cudaError_t moe_pack_weights(const MoeShape& ms, const void* Wg, const void* bg, const void* eW1, const void* eb1,
                              const void* eW2, const void* eb2, MoeWeights& w, long long* bytes, cudaStream_t s) {
-    const size_t esz = act_size(ms.act);
+    const size_t esz = op_size(ms.act);
     const size_t G = (size_t)ms.T * ms.E;
     cudaError_t e;
     if ((e = dalloc_bytes(&w.W1p, G * ms.Fe * ms.D * esz, bytes)) != cudaSuccess) return e;
@@ -276,9 +275,9 @@ cudaError_t moe_pack_weights(const MoeShape& ms, const void* Wg, const void* bg,
     if ((e = dalloc(&w.b2, G * ms.D, bytes)) != cudaSuccess) return e;
     if ((e = dalloc(&w.Wg, (size_t)ms.T * ms.E * ms.D, bytes)) != cudaSuccess) return e;
     if ((e = dalloc(&w.bg, (size_t)ms.T * ms.E, bytes)) != cudaSuccess) return e;
-    // eW1 [T][E][D][Fe] -> [T*E][Fe][D];  eW2 [T][E][Fe][D] -> [T*E][D][Fe]
-    if ((e = launch_transpose(eW1, w.W1p, (int)G, ms.D, ms.Fe, (int)esz, s)) != cudaSuccess) return e;
-    if ((e = launch_transpose(eW2, w.W2p, (int)G, ms.Fe, ms.D, (int)esz, s)) != cudaSuccess) return e;
+    // eW1 [T][E][D][Fe] -> [T*E][Fe][D];  eW2 [T][E][Fe][D] -> [T*E][D][Fe]  (operand type)
+    if ((e = launch_pack_transpose(ms.act, eW1, w.W1p, (int)G, ms.D, ms.Fe, s)) != cudaSuccess) return e;
+    if ((e = launch_pack_transpose(ms.act, eW2, w.W2p, (int)G, ms.Fe, ms.D, s)) != cudaSuccess) return e;
     if ((e = launch_to_f32(ms.act, eb1, w.b1, G * ms.Fe, s)) != cudaSuccess) return e;
     if ((e = launch_to_f32(ms.act, eb2, w.b2, G * ms.D, s)) != cudaSuccess) return e;
     if ((e = launch_to_f32(ms.act, bg, w.bg, (size_t)ms.T * ms.E, s)) != cudaSuccess) return e;
@@ -286,7 +285,7 @@ cudaError_t moe_pack_weights(const MoeShape& ms, const void* Wg, const void* bg,
     float* tmp = nullptr;
     if ((e = dalloc(&tmp, (size_t)ms.T * ms.D * ms.E, nullptr)) != cudaSuccess) return e;
     e = launch_to_f32(ms.act, Wg, tmp, (size_t)ms.T * ms.D * ms.E, s);
-    if (e == cudaSuccess) e = launch_transpose(tmp, w.Wg, ms.T, ms.D, ms.E, 4, s);
+    if (e == cudaSuccess) e = launch_transpose_f32(tmp, w.Wg, ms.T, ms.D, ms.E, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     cudaFree(tmp);
     return e;
@@ -299,7 +298,7 @@ void moe_free_weights(MoeWeights& w) {
 
 cudaError_t moe_alloc_workspace(const MoeShape& ms, int Bcap, MoeWorkspace& ws, long long* bytes) {
     const size_t G = (size_t)ms.T * ms.E;
-    const size_t esz = act_size(ms.act);
+    const size_t esz = op_size(ms.act);
     ws.Bcap = Bcap;
     cudaError_t e;
     if ((e = dalloc(&ws.gates, (size_t)Bcap * G, bytes)) != cudaSuccess) return e;
@@ -340,21 +339,28 @@ cudaError_t moe_forward(const MoeLaunch& ml, const MoeWeights& w, MoeWorkspace& 
         const long long warps = (long long)B * T;
         int grid = (int)((warps * 32 + 255) / 256);
         if (grid > ml.num_sms * 16) grid = ml.num_sms * 16;
-        if (ml.act == Act::BF16)
+        if (ml.act == Act::F32)
+            router_kernel<float><<<grid, 256, 0, s>>>((const float*)ml.S, s_sb, s_st, w.Wg, w.bg, ws.gates, B, T, D, E);
+        else if (ml.S_sample_major)   // the caller's bf16 S
             router_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16*)ml.S, s_sb, s_st, w.Wg, w.bg,
                                                                ws.gates, B, T, D, E);
-        else
-            router_kernel<float><<<grid, 256, 0, s>>>((const float*)ml.S, s_sb, s_st, w.Wg, w.bg, ws.gates, B, T, D, E);
+        else                          // the stack's fp16 S
+            router_kernel<__half><<<grid, 256, 0, s>>>((const __half*)ml.S, s_sb, s_st, w.Wg, w.bg, ws.gates, B, T, D,
+                                                        E);
         count_kernel<<<G, 256, 0, s>>>(ws.gates, ws.counts, B, T, E);
         prefix_kernel<<<1, 32, 0, s>>>(ws.counts, ws.offsets, ws.tile_prefix, T, E);
         fill_kernel<<<G, 256, 0, s>>>(ws.gates, ws.offsets, ws.rows, B, T, E);
         dim3 gg((B + 7) / 8 < 64 ? (B + 7) / 8 : 64, G);
-        if (ml.act == Act::BF16)
-            gather_kernel<uint16_t><<<gg, 256, 0, s>>>((const uint16_t*)ml.S, s_sb, s_st, ws.counts, ws.offsets,
-                                                       ws.rows, (uint16_t*)ws.Sg, D, E);
+        if (ml.act == Act::F32)
+            gather_kernel<float, float><<<gg, 256, 0, s>>>((const float*)ml.S, s_sb, s_st, ws.counts, ws.offsets,
+                                                           ws.rows, (float*)ws.Sg, D, E);
+        else if (ml.S_sample_major)
+            gather_kernel<__nv_bfloat16, __half><<<gg, 256, 0, s>>>((const __nv_bfloat16*)ml.S, s_sb, s_st,
+                                                                     ws.counts, ws.offsets, ws.rows, (__half*)ws.Sg,
+                                                                     D, E);
         else
-            gather_kernel<uint32_t><<<gg, 256, 0, s>>>((const uint32_t*)ml.S, s_sb, s_st, ws.counts, ws.offsets,
-                                                       ws.rows, (uint32_t*)ws.Sg, D, E);
+            gather_kernel<__half, __half><<<gg, 256, 0, s>>>((const __half*)ml.S, s_sb, s_st, ws.counts, ws.offsets,
+                                                             ws.rows, (__half*)ws.Sg, D, E);
         if (gates_out) {
             cudaError_t r = cudaMemcpyAsync(gates_out, ws.gates, (size_t)B * G * sizeof(float),
                                             cudaMemcpyDeviceToDevice, s);
@@ -379,9 +385,9 @@ cudaError_t moe_forward(const MoeLaunch& ml, const MoeWeights& w, MoeWorkspace& 
                                        ws.tile_prefix, ml.num_sms, ml.err, kMoeWaitTimeoutNs, s);
         dim3 grid((Fe + TN - 1) / TN, (B + TM - 1) / TM, G);
         if (ml.act == Act::BF16)
-            moe_gemm_simt_kernel<__nv_bfloat16, 1><<<grid, 256, 0, s>>>(
-                (const __nv_bfloat16*)ws.Sg, (const __nv_bfloat16*)w.W1p, w.b1, (__nv_bfloat16*)ws.Hm, ws.counts,
-                ws.offsets, ws.rows, nullptr, nullptr, 0, 0, Fe, D, T, E, 0, 1);
+            moe_gemm_simt_kernel<__half, 1><<<grid, 256, 0, s>>>((const __half*)ws.Sg, (const __half*)w.W1p, w.b1,
+                                                                 (__half*)ws.Hm, ws.counts, ws.offsets, ws.rows,
+                                                                 nullptr, nullptr, 0, 0, Fe, D, T, E, 0, 1);
         else
             moe_gemm_simt_kernel<float, 1><<<grid, 256, 0, s>>>((const float*)ws.Sg, (const float*)w.W1p, w.b1,
                                                                 (float*)ws.Hm, ws.counts, ws.offsets, ws.rows, nullptr,
@@ -400,9 +406,9 @@ cudaError_t moe_forward(const MoeLaunch& ml, const MoeWeights& w, MoeWorkspace& 
                                            s);
             dim3 grid((D + TN - 1) / TN, (B + TM - 1) / TM, T);
             if (ml.act == Act::BF16)
-                moe_gemm_simt_kernel<__nv_bfloat16, 2><<<grid, 256, 0, s>>>(
-                    (const __nv_bfloat16*)ws.Hm, (const __nv_bfloat16*)w.W2p, w.b2, nullptr, ws.counts, ws.offsets,
-                    ws.rows, ws.gates, V, v_sb, v_st, D, Fe, T, E, ei, E);
+                moe_gemm_simt_kernel<__half, 2><<<grid, 256, 0, s>>>((const __half*)ws.Hm, (const __half*)w.W2p, w.b2,
+                                                                     nullptr, ws.counts, ws.offsets, ws.rows,
+                                                                     ws.gates, V, v_sb, v_st, D, Fe, T, E, ei, E);
             else
                 moe_gemm_simt_kernel<float, 2><<<grid, 256, 0, s>>>((const float*)ws.Hm, (const float*)w.W2p, w.b2,
                                                                     nullptr, ws.counts, ws.offsets, ws.rows, ws.gates,
@@ -414,16 +420,15 @@ cudaError_t moe_forward(const MoeLaunch& ml, const MoeWeights& w, MoeWorkspace& 
     return cudaSuccess;
 }
 
-cudaError_t moe_residual_z(Act act, const float* V, const void* S, const void* S_lo, float* Z, int B, int T, int D,
-                           int Bcap, cudaStream_t s) {
+cudaError_t moe_residual_z(Act act, const float* V, const void* S, float* Z, int B, int T, int D, int Bcap,
+                           cudaStream_t s) {
     const long long n = (long long)T * B * D;
     int grid = (int)((n + 255) / 256);
     if (grid > 152 * 16) grid = 152 * 16;
     if (act == Act::BF16)
-        residual_z_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(V, (const __nv_bfloat16*)S,
-                                                               (const __nv_bfloat16*)S_lo, Z, B, T, D, Bcap);
+        residual_z_kernel<__half><<<grid, 256, 0, s>>>(V, (const __half*)S, Z, B, T, D, Bcap);
     else
-        residual_z_kernel<float><<<grid, 256, 0, s>>>(V, (const float*)S, nullptr, Z, B, T, D, Bcap);
+        residual_z_kernel<float><<<grid, 256, 0, s>>>(V, (const float*)S, Z, B, T, D, Bcap);
     return cudaGetLastError();
 }
 

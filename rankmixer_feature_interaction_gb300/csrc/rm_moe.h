@@ -22,8 +22,8 @@ struct MoeShape {
 
 // Packed, device-resident expert parameters of one layer.
 struct MoeWeights {
-    void* W1p = nullptr;   // [T*E][Fe][D]   expert layer 1, K-major
-    void* W2p = nullptr;   // [T*E][D][Fe]   expert layer 2, K-major
+    void* W1p = nullptr;   // [T*E][Fe][D]   expert layer 1, K-major, operand type
+    void* W2p = nullptr;   // [T*E][D][Fe]   expert layer 2, K-major, operand type
     float* b1 = nullptr;   // [T*E][Fe]
     float* b2 = nullptr;   // [T*E][D]
     float* Wg = nullptr;   // [T][E][D]      router, transposed, fp32
@@ -39,14 +39,15 @@ struct MoeWorkspace {
     int* rows = nullptr;        // [T*E][Bcap] sample index of each gathered row, ascending
     int* tile_prefix = nullptr; // [T*E + 1] exclusive prefix of 128-row tiles per group
     int* pair_of_row = nullptr; // [T*E*Bcap] packed row -> group id (t*E + e)
-    void* Sg = nullptr;         // [T*E*Bcap][D]  gathered LN1 rows (activation dtype)
-    void* Hm = nullptr;         // [T*E*Bcap][Fe] expert hidden activations
+    void* Sg = nullptr;         // [T*E*Bcap][D]  gathered LN1 rows (operand type)
+    void* Hm = nullptr;         // [T*E*Bcap][Fe] expert hidden activations (operand type)
 };
 
 struct MoeLaunch {
     Act act;
     const void* S;
-    bool S_sample_major;       // S is [B][T][D] (true) or token-major [T][Bcap][D] (false)
+    bool S_sample_major;       // S is the caller's [B][T][D] (caller dtype) or the stack's
+                               // token-major [T][Bcap][D] (operand type)
     int T, D, E, Fe, B, Bcap, num_sms;
     int* err;                  // device error word for bounded waits (nullable)
 };
@@ -64,9 +65,8 @@ cudaError_t moe_forward(const MoeLaunch& ml, const MoeWeights& w, MoeWorkspace& 
                         float* gates_out, cudaStream_t s, const std::function<void*(int)>& prof_begin,
                         const std::function<void(void*)>& prof_end);
 
-// Z[t][b][:] = V[t][b][:] + S[t][b][:] (+ S_lo, the bf16 rounding remainder of S, when given);
-// token-major, V and Z float32.
-cudaError_t moe_residual_z(Act act, const float* V, const void* S, const void* S_lo, float* Z, int B, int T, int D,
-                           int Bcap, cudaStream_t s);
+// Z[t][b][:] = V[t][b][:] + S[t][b][:]; token-major, V and Z float32, S in the operand type.
+cudaError_t moe_residual_z(Act act, const float* V, const void* S, float* Z, int B, int T, int D, int Bcap,
+                           cudaStream_t s);
 
 }  // namespace rm

@@ -64,10 +64,10 @@ def test_tiny_fp32_block_and_stack():
     p64 = synth.to_f64(layers)
     Xo_ref, S_ref = oracle.block_forward(_np(X), p64[0], return_S=True)
     pooled_ref, XL_ref = oracle.stack_forward(_np(X), p64, return_XL=True)
-    check(_np(S), S_ref, "f32", "S (LN1)")
-    check(_np(Xo), Xo_ref, "f32", "block X_out")
-    check(_np(XL), XL_ref, "f32", "stack X_L")
-    check(_np(pooled), pooled_ref, "f32", "pooled")
+    check(S, S_ref, "f32", "S (LN1)")
+    check(Xo, Xo_ref, "f32", "block X_out")
+    check(XL, XL_ref, "f32", "stack X_L")
+    check(pooled, pooled_ref, "f32", "pooled")
 
 
 # ----------------------------------------------------------------------------
@@ -86,11 +86,11 @@ def test_bf16_block_and_stack(path, T, D, k, L, B):
     assert m.sync_status() == _lib.RM_OK
     p64 = synth.to_f64(layers)
     Xo_ref, S_ref = oracle.block_forward(_np(X), p64[0], return_S=True)
-    check(_np(S), S_ref, "bf16", "S (LN1)")
-    check(_np(Xo), Xo_ref, "bf16", "block X_out")
+    check(S, S_ref, "bf16", "S (LN1)")
+    check(Xo, Xo_ref, "bf16", "block X_out")
     pooled_ref, XL_ref = oracle.stack_forward(_np(X), p64, return_XL=True)
-    check(_np(XL), XL_ref, "bf16", "stack X_L")
-    check(_np(pooled), pooled_ref, "bf16", "pooled")
+    check(XL, XL_ref, "bf16", "stack X_L")
+    check(pooled, pooled_ref, "bf16", "pooled")
 
 
 @pytest.mark.parametrize("path", ["tcgen05", "simt"])
@@ -105,11 +105,11 @@ def test_stack_matches_chained_blocks(path):
     for n in range(L):
         Xn = m.block_forward(n, Xn)
     torch.cuda.synchronize()
-    check(_np(XL), _np(Xn), "bf16", "stack vs chained blocks", tol=4e-2)
+    check(XL, _np(Xn), "bf16", "stack vs chained blocks", tol=4e-2)
     torch.testing.assert_close(pooled, XL.float().mean(dim=1), rtol=0, atol=2e-2)
     pr, xr = oracle.stack_forward(_np(X), synth.to_f64(layers), return_XL=True)
-    check(_np(XL), xr, "bf16", "stack X_L (L=3)")
-    check(_np(pooled), pr, "bf16", "pooled (L=3)")
+    check(XL, xr, "bf16", "stack X_L (L=3)")
+    check(pooled, pr, "bf16", "pooled (L=3)")
 
 
 def test_tcgen05_agrees_with_simt():
@@ -119,7 +119,7 @@ def test_tcgen05_agrees_with_simt():
     a = RankMixer(T, D, k, layers, max_batch=B, gemm_path="tcgen05").block_forward(0, X)
     b = RankMixer(T, D, k, layers, max_batch=B, gemm_path="simt").block_forward(0, X)
     torch.cuda.synchronize()
-    check(_np(a), _np(b), "bf16", "tcgen05 vs simt", tol=1.5e-2)
+    check(a, _np(b), "bf16", "tcgen05 vs simt", tol=1.5e-2)
 
 
 def test_deterministic_reruns():
@@ -153,8 +153,8 @@ def test_batch_of_one_and_full_capacity():
         pooled, XL = m.stack_forward(X[:B].contiguous(), return_XL=True)
         torch.cuda.synchronize()
         pr, xr = oracle.stack_forward(_np(X[:B]), p64, return_XL=True)
-        check(_np(XL), xr, "bf16", f"X_L B={B}")
-        check(_np(pooled), pr, "bf16", f"pooled B={B}")
+        check(XL, xr, "bf16", f"X_L B={B}")
+        check(pooled, pr, "bf16", f"pooled B={B}")
 
 
 @pytest.mark.parametrize("dtype,T,D,k", [("bf16", 4, 12, 2), ("f32", 4, 12, 3), ("bf16", 6, 96, 2),
@@ -167,8 +167,8 @@ def test_odd_shapes_take_the_simt_path(dtype, T, D, k):
     pooled, XL = m.stack_forward(X, return_XL=True)
     torch.cuda.synchronize()
     pr, xr = oracle.stack_forward(_np(X), synth.to_f64(layers), return_XL=True)
-    check(_np(XL), xr, dtype, "X_L")
-    check(_np(pooled), pr, dtype, "pooled")
+    check(XL, xr, dtype, "X_L")
+    check(pooled, pr, dtype, "pooled")
 
 
 def test_invalid_arguments_are_reported():
@@ -207,7 +207,7 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     out = m.block_forward(0, X)
     torch.cuda.synchronize()
     assert m.sync_status() == _lib.RM_OK
-    check(_np(out), oracle.block_forward(_np(X), synth.to_f64(layers)[0]), "bf16", "block after timeout")
+    check(out, oracle.block_forward(_np(X), synth.to_f64(layers)[0]), "bf16", "block after timeout")
 
 
 def test_profiler_counts_launches():
@@ -240,8 +240,8 @@ def _sampled_stack_parity(name, B, n_samples, seed, max_batch=None, model=None):
     rng = np.random.default_rng(seed + B)
     idx = np.unique(np.concatenate([[0, B - 1], rng.choice(B, size=min(n_samples, B), replace=False)]))
     pr, xr = oracle.stack_forward(_np(X[idx]), p64, return_XL=True)
-    check(_np(XL[idx]), xr, "bf16", f"{name} B={B} X_L")
-    check(_np(pooled[idx]), pr, "bf16", f"{name} B={B} pooled")
+    check(XL[torch.as_tensor(idx, device=XL.device)], xr, "bf16", f"{name} B={B} X_L")
+    check(pooled[torch.as_tensor(idx, device=pooled.device)], pr, "bf16", f"{name} B={B} pooled")
     assert torch.isfinite(pooled).all()
     return m
 
@@ -293,7 +293,7 @@ def test_moe_pffn_small(dtype, path, T, D, E, Fe, B):
     V_ref, G_ref = _moe_oracle(_np(S), p64)
     assert 0.1 < (G_ref > 0).mean() < 0.5, "router bias should open about a quarter of the experts"
     np.testing.assert_allclose(_np(G), G_ref, atol=2e-4 if dtype == "bf16" else 1e-5, rtol=1e-3)
-    check(_np(V), V_ref, dtype, "MoE V")
+    check(V, V_ref, dtype, "MoE V")
 
 
 def test_moe_layer_inside_block():
@@ -312,13 +312,13 @@ def test_moe_layer_inside_block():
         return oracle.layernorm(V + S, p["ln2_g"], p["ln2_b"], 1e-5), S
 
     X1_ref = oracle.block_forward(_np(X), p64[0])
-    check(_np(X1), X1_ref, "bf16", "dense layer")
+    check(X1, X1_ref, "bf16", "dense layer")
     X2_ref, S2_ref = moe_block(_np(X1), p64[1])
-    check(_np(S2), S2_ref, "bf16", "MoE layer S")
-    check(_np(X2), X2_ref, "bf16", "MoE layer X_out")
+    check(S2, S2_ref, "bf16", "MoE layer S")
+    check(X2, X2_ref, "bf16", "MoE layer X_out")
     XL_ref, _ = moe_block(X1_ref, p64[1])
-    check(_np(XL), XL_ref, "bf16", "stack with a MoE layer, X_L")
-    check(_np(pooled), XL_ref.mean(axis=1), "bf16", "stack with a MoE layer, pooled")
+    check(XL, XL_ref, "bf16", "stack with a MoE layer, X_L")
+    check(pooled, XL_ref.mean(axis=1), "bf16", "stack with a MoE layer, pooled")
 
 
 def test_moe_1b_full_size_sampled():
@@ -341,4 +341,4 @@ def test_moe_1b_full_size_sampled():
         V_ref, G_ref = oracle.moe_pffn(_np(S[b:b + 1, t:t + 1]), pt["Wg"], pt["bg"], pt["eW1"], pt["eb1"],
                                        pt["eW2"], pt["eb2"], return_gates=True)
         np.testing.assert_allclose(_np(G[b:b + 1, t:t + 1]), G_ref, atol=2e-4, rtol=1e-3)
-        check(_np(V[b:b + 1, t:t + 1]), V_ref, "bf16", f"MoE V (b={b}, t={t})")
+        check(V[b:b + 1, t:t + 1], V_ref, "bf16", f"MoE V (b={b}, t={t})")
