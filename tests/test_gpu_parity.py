@@ -282,7 +282,7 @@ def _moe_oracle(S64, p64, t_slice=None):
 @pytest.mark.parametrize("dtype,path,T,D,E,Fe,B", [("bf16", "auto", 4, 256, 4, 256, 300),
                                                    ("bf16", "simt", 4, 256, 4, 256, 300),
                                                    ("bf16", "auto", 2, 128, 8, 384, 129),
-                                                   ("f32", "auto", 3, 16, 4, 24, 50)])
+                                                   ("f32", "auto", 3, 18, 4, 24, 50)])
 def test_moe_pffn_small(dtype, path, T, D, E, Fe, B):
     m, layers, _ = _build(T, D, 2, 1, B, 61 + D, dtype, path=path, E=E, Fe=Fe, active=E / 4)
     S = synth.make_input(B, T, D, 62, dtype, DEV)
