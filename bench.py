@@ -71,7 +71,11 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, t0: float, t1: float):
+        """Host wall-clock bounds of the timed region; samples outside it are dropped."""
+        self.window = (t0, t1)
 
     def stop(self) -> dict:
         if self.proc is None:
@@ -85,7 +89,10 @@ class ClockSampler:
             self.thread.join(timeout=2)
         sm, smax, power, reasons = [], None, [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        t0, t1 = getattr(self, "window", (0.0, float("inf")))
+        for ts, ln in self.lines:
+            if not (t0 <= ts <= t1 + 0.15):
+                continue
             parts = [x.strip() for x in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -141,7 +148,7 @@ def run_ours(args):
     B = args.batch or c["B"]
     T, D, k = c["T"], c["D"], c["k"]
     moe = args.config == "moe_1b"
-    L = c["L"]
+    L = args.layers or c["L"]
     E, Fe = c.get("E", 0), c.get("Fe", 0)
     seed = 20260101 + 17 * rank
     layers = synth.make_stack(T, D, k, L, 4242, "bf16", dev, E=E, Fe=Fe, active=c.get("active", 2.0))
@@ -168,17 +175,20 @@ def run_ours(args):
 
     clocks = ClockSampler(local)
     clocks.start()
-    time.sleep(0.3)
+    time.sleep(0.5)                  # let nvidia-smi come up
     m.profile(True)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
+    h0 = time.time()
     ev0.record(stream)
     for _ in range(args.steps):
         step()
     ev1.record(stream)
     torch.cuda.synchronize()
+    h1 = time.time()
+    clocks.mark(h0, h1)
     if world > 1:
         dist.barrier()
     ms_total = ev0.elapsed_time(ev1)
@@ -305,9 +315,10 @@ def cpu_baseline(config: str, B_full: int, seconds: float, n_steps: int = 1) -> 
         return time.perf_counter() - t0
 
     probe_n = max(1, cores)
+    run(probe_n)                     # first touch of the weights
     dt = run(probe_n)
     per_sample = dt / probe_n
-    nb = int(max(probe_n, min(4096, (seconds * 0.7) / max(per_sample, 1e-9))))
+    nb = int(max(probe_n, min(4096, seconds / max(per_sample, 1e-9))))
     nb = max(probe_n, (nb // probe_n) * probe_n)
     total_t, total_n = 0.0, 0
     for _ in range(n_steps):
@@ -346,11 +357,12 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", choices=["rankmixer_1b", "rankmixer_100m", "moe_1b"], default="rankmixer_1b")
     ap.add_argument("--batch", type=int, default=0, help="override the batch per GPU")
+    ap.add_argument("--layers", type=int, default=0, help="override the number of layers (profiling captures)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU oracle budget per measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
