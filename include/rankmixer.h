@@ -189,6 +189,33 @@ RM_API rm_status rm_stack_forward_host(rm_ctx *ctx, const void *X0_host, float *
 RM_API rm_status rm_moe_pffn_forward(rm_ctx *ctx, int layer, const void *S, float *V_out, float *gates,
                               int B, void *stream);
 
+/* Allocation-free variant of rm_block_forward (the paper has no counterpart;
+ * this is a deployment aid).  For callers that cannot allocate device memory
+ * where they run the model -- a serving loop whose memory belongs to a pool
+ * or framework allocator, a plugin with a fixed memory budget, code that must
+ * not risk the implicit synchronisation of cudaMalloc/cudaFree.  It computes
+ * exactly what rm_block_forward computes for a dense layer, with the same
+ * kernels, but keeps the intermediates (S, hidden activations, pre-LN2 rows
+ * and their statistics) in one static device array of 32 MiB compiled into
+ * the library instead of the context's workspace, and allocates nothing.
+ *   - The array exists on every GPU that loads the library until the process
+ *     exits.  B is limited by it: a call whose intermediates exceed 32 MiB
+ *     returns RM_ERR_INVALID_ARG and names the limit (about B <= 48 at
+ *     T=32, D=1536, k=4; about B <= 190 at T=16, D=768, k=4).  B is not
+ *     limited by cfg.max_batch.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before
+ *     any stream capture.
+ *   - All calls share the array and it keeps the last call's contents.  Every
+ *     element a call uses is written earlier in the same call, so nothing
+ *     needs clearing, but calls that overlap on the GPU (other streams, other
+ *     threads, other contexts) race on it: serialise them.
+ *   - Dense layers only (RM_ERR_UNSUPPORTED for a Sparse-MoE layer).
+ * X_in, X_out: device [B][T][D] in the context dtype, 16-byte aligned, not
+ * overlapping.  Asynchronous on `stream`. */
+RM_API rm_status rm_block_forward_noalloc(rm_ctx *ctx, int layer, const void *X_in, void *X_out, int B,
+                                          void *stream);
+
 /* Standalone TokenMixing ("RankMixer" Eq. 3-4): Y[b][h][t q + r] = X[b][t][h q + r],
  * q = D / H, for any H dividing D (Y is [B][H][T q]).  A pure permutation of
  * element bits, exact for both dtypes.  X, Y: device, non-overlapping. */

@@ -39,7 +39,8 @@ RM_K_COUNT = len(KERNEL_KINDS)
 
 EXPORTED = ["rm_create", "rm_destroy", "rm_block_forward", "rm_stack_forward", "rm_stack_forward_host",
             "rm_moe_pffn_forward", "rm_token_mix", "rm_sync_status", "rm_get_info", "rm_profile_enable",
-            "rm_profile_read", "rm_debug_wait_timeout", "rm_last_error", "rm_abi_version"]
+            "rm_profile_read", "rm_debug_wait_timeout", "rm_last_error", "rm_abi_version",
+            "rm_block_forward_noalloc"]
 
 
 class rm_config(ctypes.Structure):
@@ -98,6 +99,7 @@ def load() -> ctypes.CDLL:
         "rm_debug_wait_timeout": (st, [vp, i, vp]),
         "rm_last_error": (ctypes.c_char_p, []),
         "rm_abi_version": (i, []),
+        "rm_block_forward_noalloc": (st, [vp, i, vp, vp, i, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -128,6 +130,10 @@ def rm_destroy(ctx: int) -> None:
 
 def rm_block_forward(ctx: int, layer: int, X_in: int, X_out: int, S_out: int | None, B: int, stream: int) -> None:
     check(load().rm_block_forward(ctx, layer, X_in, X_out, S_out, B, stream), "rm_block_forward")
+
+
+def rm_block_forward_noalloc(ctx: int, layer: int, X_in: int, X_out: int, B: int, stream: int) -> None:
+    check(load().rm_block_forward_noalloc(ctx, layer, X_in, X_out, B, stream), "rm_block_forward_noalloc")
 
 
 def rm_stack_forward(ctx: int, X0: int, pooled: int, XL: int | None, B: int, stream: int) -> None:

@@ -7,6 +7,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -588,6 +589,119 @@ rm_status rm_debug_wait_timeout(rm_ctx* c, int timeout_us, void* stream) {
     cudaSetDevice(c->device);
     RM_CHECK_CUDA(launch_debug_wait(c->d_flag, c->d_err, (unsigned long long)timeout_us * 1000ull, as_stream(stream)),
                   "debug wait");
+    return RM_OK;
+}
+
+}  // extern "C"
+
+// =============================================================================
+// Allocation-free block forward
+//
+// Some callers cannot allocate device memory at the point where they run the
+// model: a serving loop whose memory is owned by a pool or a framework
+// allocator that forbids side allocations, a plugin with a fixed memory
+// budget, or code that must never trigger the implicit synchronisation a
+// cudaMalloc/cudaFree can cause.  rm_block_forward_noalloc serves them: it
+// runs the same kernels as rm_block_forward but keeps its intermediates (S,
+// the hidden activations, the pre-LN2 rows Z and their row statistics) in
+// the file-scope device array below instead of the context's workspace, and
+// allocates nothing.  The array is part of the library image, so every GPU
+// that loads the library holds it until the process exits.
+// =============================================================================
+namespace {
+constexpr size_t kNoAllocScratchBytes = 32ull << 20;   // 32 MiB
+constexpr int kNoAllocMaxDevices = 64;
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_base[kNoAllocMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on `device` (which must be current).
+// Looked up once per device; the host-side name of the array is not a
+// device address and must never be handed to a kernel.
+rm_status noalloc_scratch(int device, void** out) {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (device < 0 || device >= kNoAllocMaxDevices)
+        return fail(RM_ERR_UNSUPPORTED, "allocation-free entry point supports devices 0..%d", kNoAllocMaxDevices - 1);
+    if (!g_noalloc_base[device]) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+        g_noalloc_base[device] = p;
+    }
+    *out = g_noalloc_base[device];
+    return RM_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+extern "C" {
+
+rm_status rm_block_forward_noalloc(rm_ctx* c, int layer, const void* X_in, void* X_out, int B, void* stream) {
+    rm_status st;
+    if ((st = check_ctx(c)) != RM_OK) return st;
+    const rm_config& g = c->cfg;
+    if (layer < 0 || layer >= g.L) return fail(RM_ERR_INVALID_ARG, "layer %d out of range", layer);
+    if (g.moe_layer_mask & (1u << layer))
+        return fail(RM_ERR_UNSUPPORTED, "the allocation-free entry point runs dense layers only");
+    if (B < 1) return fail(RM_ERR_INVALID_ARG, "B must be >= 1");
+    if (!X_in || !X_out) return fail(RM_ERR_INVALID_ARG, "X_in / X_out is NULL");
+    if (!aligned16(X_in) || !aligned16(X_out)) return fail(RM_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+    const size_t T = g.T, D = g.D, F = c->F, Bs = (size_t)B;
+    const size_t io_bytes = Bs * T * D * c->esz;
+    const char* xi = (const char*)X_in;
+    const char* xo = (const char*)X_out;
+    if (xi < xo + io_bytes && xo < xi + io_bytes) return fail(RM_ERR_INVALID_ARG, "X_in and X_out overlap");
+    const int nchunk = layer_nchunk(c, layer), cw = layer_cw(c, layer);
+    // scratch layout (token-major, rows between tokens = B): S, Hid, Z, stats
+    const size_t bS = align256(T * Bs * D * op_size(c->act));
+    const size_t bH = align256(T * Bs * F * op_size(c->act));
+    const size_t bZ = align256(T * Bs * D * sizeof(float));
+    const size_t bT = align256(T * Bs * (size_t)nchunk * sizeof(float2));
+    const size_t need = bS + bH + bZ + bT;
+    if (need > kNoAllocScratchBytes) {
+        const size_t per = need / Bs + 1;
+        return fail(RM_ERR_INVALID_ARG,
+                    "B=%d needs %zu bytes of scratch; the static scratch holds %zu bytes (about B <= %zu here)", B,
+                    need, kNoAllocScratchBytes, kNoAllocScratchBytes / per);
+    }
+    RM_CHECK_CUDA(cudaSetDevice(c->device), "cudaSetDevice");
+    void* base = nullptr;
+    if ((st = noalloc_scratch(c->device, &base)) != RM_OK) return st;
+    char* p = static_cast<char*>(base);
+    void* S = p;
+    void* Hid = p + bS;
+    float* Z = reinterpret_cast<float*>(p + bS + bH);
+    float2* stats = reinterpret_cast<float2*>(p + bS + bH + bZ);
+
+    cudaStream_t s = as_stream(stream);
+    const LayerW& w = c->layers[layer];
+    MixLnArgs a = mix_args(c, layer, B);
+    a.X = X_in;
+    a.S = S;
+    a.Bcap = B;
+    RM_CHECK_CUDA(launch_mix_ln1(c->act, false, a, c->num_sms, s), "mix+ln1");
+    if (c->use_tc) {
+        cudaError_t e = launch_gemm1_tc(S, w.W1p, w.b1, Hid, B, g.T, g.D, c->F, B, c->num_sms, c->d_err,
+                                        kWaitTimeoutNs, s);
+        if (e != cudaSuccess) return cuda_fail(e, (std::string("gemm1 (tcgen05) ") + tc_last_error()).c_str());
+        e = launch_gemm2_tc(Hid, w.W2p, w.b2, S, Z, stats, B, g.T, g.D, c->F, B, c->num_sms, c->d_err,
+                            kWaitTimeoutNs, s);
+        if (e != cudaSuccess) return cuda_fail(e, (std::string("gemm2 (tcgen05) ") + tc_last_error()).c_str());
+    } else {
+        RM_CHECK_CUDA(launch_gemm1_simt(c->act, S, w.W1p, w.b1, Hid, B, g.T, g.D, c->F, B, s), "gemm1 (simt)");
+        RM_CHECK_CUDA(launch_gemm2_simt(c->act, Hid, w.W2p, w.b2, S, Z, B, g.T, g.D, c->F, B, s), "gemm2 (simt)");
+        RM_CHECK_CUDA(launch_rowstats(Z, stats, B, g.T, g.D, B, c->num_sms, s), "row stats");
+    }
+    RM_CHECK_CUDA(launch_ln2_out(c->act, Z, stats, w.g2, w.be2, X_out, B, g.T, g.D, B, nchunk, cw, g.ln_eps,
+                                 c->num_sms, s),
+                  "ln2 out");
     return RM_OK;
 }
 
