@@ -80,7 +80,7 @@ struct rm_ctx {
     int Bcap = 0;
     void* S = nullptr;           // operand type (fp16 for bf16 contexts)
     void* Hid = nullptr;         // operand type
-    float* Z = nullptr;
+    void* Z = nullptr;           // pre-LN2 rows, operand type
     float2* stats = nullptr;
     float* V = nullptr;          // MoE PFFN output inside the stack
     MoeWorkspace moe_ws;
@@ -210,7 +210,7 @@ rm_status run_pffn(rm_ctx* c, int layer, int B, cudaStream_t s) {
         ProfScope ps(c, RM_K_GEMM2, s);
         RM_CHECK_CUDA(moe_residual_z(c->act, c->V, c->S, c->Z, B, g.T, g.D, c->Bcap, s), "moe residual");
         ProfScope ps2(c, RM_K_ROWSTATS, s);
-        RM_CHECK_CUDA(launch_rowstats(c->Z, c->stats, B, g.T, g.D, c->Bcap, c->num_sms, s), "row stats");
+        RM_CHECK_CUDA(launch_rowstats(c->act, c->Z, c->stats, B, g.T, g.D, c->Bcap, c->num_sms, s), "row stats");
         return RM_OK;
     }
     if (c->use_tc) {
@@ -238,7 +238,7 @@ rm_status run_pffn(rm_ctx* c, int layer, int B, cudaStream_t s) {
                           "gemm2 (simt)");
         }
         ProfScope ps(c, RM_K_ROWSTATS, s);
-        RM_CHECK_CUDA(launch_rowstats(c->Z, c->stats, B, g.T, g.D, c->Bcap, c->num_sms, s), "row stats");
+        RM_CHECK_CUDA(launch_rowstats(c->act, c->Z, c->stats, B, g.T, g.D, c->Bcap, c->num_sms, s), "row stats");
     }
     return RM_OK;
 }
@@ -264,6 +264,8 @@ MixLnArgs mix_args(const rm_ctx* c, int layer, int B) {
     a.q = g.D / g.H;
     a.Bcap = c->Bcap;
     a.eps = g.ln_eps;
+    a.err = c->d_err;
+    a.timeout_ns = kWaitTimeoutNs;
     return a;
 }
 
@@ -374,7 +376,7 @@ rm_status rm_create(const rm_config* cfg, const rm_layer_params* layers, int dev
     const size_t T = cfg->T, D = cfg->D, F = c->F, Bc = c->Bcap;
     if ((st = dmalloc(c, &c->S, T * Bc * D * c->esz, &c->ws_bytes)) != RM_OK ||
         (st = dmalloc(c, &c->Hid, T * Bc * F * c->esz, &c->ws_bytes)) != RM_OK ||
-        (st = dmalloc(c, (void**)&c->Z, T * Bc * D * 4, &c->ws_bytes)) != RM_OK ||
+        (st = dmalloc(c, &c->Z, T * Bc * D * op_size(c->act), &c->ws_bytes)) != RM_OK ||
         (st = dmalloc(c, (void**)&c->stats, T * Bc * (size_t)c->nchunk * sizeof(float2), &c->ws_bytes)) != RM_OK ||
         (st = dmalloc(c, (void**)&c->d_err, sizeof(int), nullptr)) != RM_OK ||
         (st = dmalloc(c, (void**)&c->d_flag, sizeof(int), nullptr)) != RM_OK) {
@@ -662,7 +664,7 @@ rm_status rm_block_forward_noalloc(rm_ctx* c, int layer, const void* X_in, void*
     // scratch layout (token-major, rows between tokens = B): S, Hid, Z, stats
     const size_t bS = align256(T * Bs * D * op_size(c->act));
     const size_t bH = align256(T * Bs * F * op_size(c->act));
-    const size_t bZ = align256(T * Bs * D * sizeof(float));
+    const size_t bZ = align256(T * Bs * D * op_size(c->act));
     const size_t bT = align256(T * Bs * (size_t)nchunk * sizeof(float2));
     const size_t need = bS + bH + bZ + bT;
     if (need > kNoAllocScratchBytes) {
@@ -677,7 +679,7 @@ rm_status rm_block_forward_noalloc(rm_ctx* c, int layer, const void* X_in, void*
     char* p = static_cast<char*>(base);
     void* S = p;
     void* Hid = p + bS;
-    float* Z = reinterpret_cast<float*>(p + bS + bH);
+    void* Z = p + bS + bH;
     float2* stats = reinterpret_cast<float2*>(p + bS + bH + bZ);
 
     cudaStream_t s = as_stream(stream);
@@ -697,7 +699,7 @@ rm_status rm_block_forward_noalloc(rm_ctx* c, int layer, const void* X_in, void*
     } else {
         RM_CHECK_CUDA(launch_gemm1_simt(c->act, S, w.W1p, w.b1, Hid, B, g.T, g.D, c->F, B, s), "gemm1 (simt)");
         RM_CHECK_CUDA(launch_gemm2_simt(c->act, Hid, w.W2p, w.b2, S, Z, B, g.T, g.D, c->F, B, s), "gemm2 (simt)");
-        RM_CHECK_CUDA(launch_rowstats(Z, stats, B, g.T, g.D, B, c->num_sms, s), "row stats");
+        RM_CHECK_CUDA(launch_rowstats(c->act, Z, stats, B, g.T, g.D, B, c->num_sms, s), "row stats");
     }
     RM_CHECK_CUDA(launch_ln2_out(c->act, Z, stats, w.g2, w.be2, X_out, B, g.T, g.D, B, nchunk, cw, g.ln_eps,
                                  c->num_sms, s),

@@ -6,14 +6,17 @@
 // "RankMixer: Scaling Up Ranking Models in Industrial Recommenders", section
 // 3.1 Eq. 1 and section 3.3.1 Eq. 3-5; "RankMixer 详解（1）" section 3.1 (the
 // element map of the mixing) and section 3.3 (LayerNorm).
+//
+// Types: Tin is the caller's activation dtype (bf16 or float), Top the
+// operand type of the GEMMs (fp16 for bf16 contexts, float for float32
+// contexts).  The pre-LN2 rows Z are stored in Top as well.
 #include "rm_common.cuh"
 #include "rm_internal.h"
 
 namespace rm {
 namespace {
 
-constexpr int kMixThreads = 256;
-constexpr int kMixWarps = kMixThreads / 32;
+constexpr int kMaxT = 128;
 
 // LN affine applied to a finalised row element.  Every kernel that finalises
 // LN2 (the next layer's mixing, the block output, the pool) uses this exact
@@ -23,9 +26,8 @@ __device__ __forceinline__ float ln_apply(float z, float mean, float rstd, float
     return fmaf(n, g, b);
 }
 
-template <typename Tact> struct Vec2;
+template <typename T> struct Vec2;
 template <> struct Vec2<float> {
-    using type = float2;
     __device__ static float2 load(const float* p) { return *reinterpret_cast<const float2*>(p); }
     __device__ static void store(float* p, float a, float b) { *reinterpret_cast<float2*>(p) = make_float2(a, b); }
     __device__ static void split(float2 v, float& a, float& b) { a = v.x; b = v.y; }
@@ -53,147 +55,213 @@ template <> struct Vec2<__nv_bfloat16> {
     }
 };
 
-// ---------------------------------------------------------------------------
-// Fused TokenMixing + residual + LN1.
-// One CTA per sample (grid-stride), one warp per output row h:
-//   y[j] = X[t][h q + r] + X[h][j],  j = t q + r          (mix + residual)
-// with X read straight from global memory -- either the caller's X, or the
-// previous layer's pre-LN2 rows Z finalised on the fly in float32 (the row
-// statistics of the sample's T rows are merged once into shared memory).
-// y stays in registers; mean and biased variance come from two warp
-// reductions; S = LN1(y) is written token-major in the operand type Top
-// (fp16 for bf16 contexts, float for float32 contexts).
-// VEC = 2: each lane owns column pairs (needs q even, D % 64 == 0);
-// VEC = 1: single columns (any q).  NI bounds D / (32 VEC).
-// ---------------------------------------------------------------------------
-constexpr int kMaxT = 128;
+template <typename T>
+__device__ __forceinline__ void load_pair(const T* p, float& a, float& b) {
+    Vec2<T>::split(Vec2<T>::load(p), a, b);
+}
 
-template <typename Tin, bool FROM_Z>
-struct RowSrc {
-    const Tin* X;
-    const float* Z;
-    const float* g2;
-    const float* be2;
-    const float* mean;
-    const float* rstd;
-    size_t xrow_stride;   // elements between token rows of one sample
-    size_t zrow_stride;
-    __device__ __forceinline__ float load1(int t, int c) const {
-        if (FROM_Z) return ln_apply(Z[t * zrow_stride + c], mean[t], rstd[t], g2[c], be2[c]);
-        return to_f32(X[t * xrow_stride + c]);
-    }
-    __device__ __forceinline__ void load2(int t, int c, float& v0, float& v1) const {
-        if (FROM_Z) {
-            const float2 z = *reinterpret_cast<const float2*>(Z + t * zrow_stride + c);
-            const float2 g = *reinterpret_cast<const float2*>(g2 + c);
-            const float2 be = *reinterpret_cast<const float2*>(be2 + c);
-            v0 = ln_apply(z.x, mean[t], rstd[t], g.x, be.x);
-            v1 = ln_apply(z.y, mean[t], rstd[t], g.y, be.y);
-        } else {
-            Vec2<Tin>::split(Vec2<Tin>::load(X + t * xrow_stride + c), v0, v1);
+// Row statistics of the T rows of sample b into shared memory (one warp per row).
+__device__ __forceinline__ void sample_row_stats(const MixLnArgs& a, int b, float* s_mean, float* s_rstd, int warp,
+                                                 int nwarps, int lane) {
+    for (int t = warp; t < a.T; t += nwarps) {
+        float mean, rstd;
+        merge_row_stats(a.stats + ((size_t)t * a.Bcap + b) * a.nchunk, a.nchunk, a.cw, a.D, a.eps, lane, mean, rstd);
+        if (lane == 0) {
+            s_mean[t] = mean;
+            s_rstd[t] = rstd;
         }
     }
-};
+}
+
+// One output row h of the fused mix + residual + LN1, column pairs per lane:
+//   y[j] = X[t][h q + r] + X[h][j],  j = t q + r
+// X (T rows of length D at stride xrow) is read through `xs` (shared or global
+// memory) in its stored type Tx and, when FROM_Z, finalised from pre-LN2
+// values.  y stays in registers; S[h] = LN1(y) is stored at srow in the
+// operand type Top.  Needs q even and D % 64 == 0.
+template <typename Tx, typename Top, bool FROM_Z, int NI>
+__device__ __forceinline__ void mix_row_pairs(const MixLnArgs& a, const Tx* xs, size_t xrow, int h,
+                                              const float* s_mean, const float* s_rstd, Top* srow, int lane) {
+    const int D = a.D, q = a.q;
+    const int ni = D >> 6;
+    const Tx* xh = xs + (size_t)h * xrow;
+    float y[2 * NI];
+    float sum = 0.f;
+    int t = (2 * lane) / q;
+    int r = 2 * lane - t * q;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+        if (i < ni) {
+            const int j = (i << 6) + (lane << 1);
+            const int c = h * q + r;
+            float m0, m1, x0, x1;
+            load_pair(xs + (size_t)t * xrow + c, m0, m1);
+            load_pair(xh + j, x0, x1);
+            if (FROM_Z) {
+                const float2 gm = *reinterpret_cast<const float2*>(a.g2 + c);
+                const float2 bm = *reinterpret_cast<const float2*>(a.be2 + c);
+                const float2 gx = *reinterpret_cast<const float2*>(a.g2 + j);
+                const float2 bx = *reinterpret_cast<const float2*>(a.be2 + j);
+                const float mt = s_mean[t], rt = s_rstd[t], mh = s_mean[h], rh = s_rstd[h];
+                m0 = ln_apply(m0, mt, rt, gm.x, bm.x);
+                m1 = ln_apply(m1, mt, rt, gm.y, bm.y);
+                x0 = ln_apply(x0, mh, rh, gx.x, bx.x);
+                x1 = ln_apply(x1, mh, rh, gx.y, bx.y);
+            }
+            y[2 * i] = m0 + x0;
+            y[2 * i + 1] = m1 + x1;
+            sum += y[2 * i] + y[2 * i + 1];
+            r += 64;                      // next j is 64 columns further
+            while (r >= q) {
+                r -= q;
+                ++t;
+            }
+        }
+    }
+    const float mean = warp_sum(sum) / (float)D;
+    float sq = 0.f;
+#pragma unroll
+    for (int i = 0; i < NI; ++i)
+        if (i < ni) {
+            const float d0 = y[2 * i] - mean, d1 = y[2 * i + 1] - mean;
+            sq += d0 * d0 + d1 * d1;
+        }
+    const float rstd = rsqrtf(warp_sum(sq) / (float)D + a.eps);
+#pragma unroll
+    for (int i = 0; i < NI; ++i)
+        if (i < ni) {
+            const int j = (i << 6) + (lane << 1);
+            const float2 g = *reinterpret_cast<const float2*>(a.g1 + j);
+            const float2 be = *reinterpret_cast<const float2*>(a.be1 + j);
+            Vec2<Top>::store(srow + j, ln_apply(y[2 * i], mean, rstd, g.x, be.x),
+                             ln_apply(y[2 * i + 1], mean, rstd, g.y, be.y));
+        }
+}
+
+// ---------------------------------------------------------------------------
+// Staged mix + LN1 (bf16 contexts, q even, D % 64 == 0).  Persistent CTAs
+// walk samples b = blockIdx.x, + gridDim.x, ...; each sample's T x D source
+// rows (the caller's bf16 X, or the previous layer's fp16 pre-LN2 rows Z) are
+// brought into shared memory with 1-D bulk copies on an mbarrier, double
+// buffered so the next sample's copy overlaps this sample's arithmetic.
+// ---------------------------------------------------------------------------
+template <typename Tsrc, bool FROM_Z, int NI>
+__global__ void __launch_bounds__(512)
+mix_ln1_staged_kernel(const MixLnArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int T = a.T, D = a.D;
+    const uint32_t row_bytes = (uint32_t)D * 2u;
+    const uint32_t buf_bytes = (uint32_t)T * row_bytes;
+    Tsrc* buf = reinterpret_cast<Tsrc*>(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * (size_t)buf_bytes);
+    float* s_mean = reinterpret_cast<float*>(bars + 2);
+    float* s_rstd = s_mean + kMaxT;
+    volatile int* s_abort = reinterpret_cast<volatile int*>(s_rstd + kMaxT);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = blockDim.x >> 5;
+    const Tsrc* src = FROM_Z ? reinterpret_cast<const Tsrc*>(a.Z) : reinterpret_cast<const Tsrc*>(a.X);
+    __half* S = reinterpret_cast<__half*>(a.S);
+
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bars[0]), 1);
+        mbar_init(smem_u32(&bars[1]), 1);
+        *s_abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    auto issue = [&](int b, int slot) {   // thread 0 only
+        const uint32_t bar = smem_u32(&bars[slot]);
+        const uint32_t dst = smem_u32(buf) + (uint32_t)slot * buf_bytes;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, buf_bytes);
+        if (!FROM_Z) {
+            bulk_copy_g2s(dst, src + (size_t)b * T * D, buf_bytes, bar);
+        } else {
+            for (int t = 0; t < T; ++t)
+                bulk_copy_g2s(dst + (uint32_t)t * row_bytes, src + ((size_t)t * a.Bcap + b) * D, row_bytes, bar);
+        }
+    };
+
+    if (threadIdx.x == 0 && (int)blockIdx.x < a.B) issue(blockIdx.x, 0);
+    int it = 0;
+    for (int b = blockIdx.x; b < a.B; b += gridDim.x, ++it) {
+        const int slot = it & 1;
+        if (threadIdx.x == 0 && b + (int)gridDim.x < a.B) issue(b + gridDim.x, slot ^ 1);
+        if (FROM_Z) sample_row_stats(a, b, s_mean, s_rstd, warp, nwarps, lane);
+        mbar_wait_bounded(smem_u32(&bars[slot]), (uint32_t)(it >> 1) & 1u, s_abort, a.err, a.timeout_ns);
+        __syncthreads();
+        if (*s_abort) break;
+        const Tsrc* xs = buf + (size_t)slot * T * D;
+        for (int h = warp; h < T; h += nwarps)
+            mix_row_pairs<Tsrc, __half, FROM_Z, NI>(a, xs, (size_t)D, h, s_mean, s_rstd,
+                                                     S + ((size_t)h * a.Bcap + b) * D, lane);
+        __syncthreads();    // the slot and the row statistics are reused by later samples
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Direct mix + LN1 (float32 contexts and shapes the staged kernel does not
+// take): X read straight from global memory, one CTA per sample.
+// VEC = 2 uses mix_row_pairs (q even, D % 64 == 0); VEC = 1 handles any q.
+// ---------------------------------------------------------------------------
+constexpr int kMixThreads = 256;
+constexpr int kMixWarps = kMixThreads / 32;
 
 template <typename Tin, typename Top, bool FROM_Z, int VEC, int NI>
 __global__ void __launch_bounds__(kMixThreads)
-mix_ln1_kernel(const MixLnArgs a) {
+mix_ln1_direct_kernel(const MixLnArgs a) {
     __shared__ float s_mean[kMaxT], s_rstd[kMaxT];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int T = a.T, D = a.D, q = a.q;
     Top* S = reinterpret_cast<Top*>(a.S);
-
     for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
-        RowSrc<Tin, FROM_Z> src;
-        src.X = reinterpret_cast<const Tin*>(a.X) + (size_t)b * T * D;
-        src.Z = a.Z + (size_t)b * D;
-        src.g2 = a.g2;
-        src.be2 = a.be2;
-        src.mean = s_mean;
-        src.rstd = s_rstd;
-        src.xrow_stride = (size_t)D;
-        src.zrow_stride = (size_t)a.Bcap * D;
+        // source rows: X sample-major (row stride D) or Z token-major (row stride Bcap D)
+        const Tin* X = reinterpret_cast<const Tin*>(a.X) + (size_t)b * T * D;
+        const Top* Z = reinterpret_cast<const Top*>(a.Z) + (size_t)b * D;
+        const size_t zrow = (size_t)a.Bcap * D;
         if (FROM_Z) {
-            for (int t = warp; t < T; t += kMixWarps) {
-                float mean, rstd;
-                merge_row_stats(a.stats + ((size_t)t * a.Bcap + b) * a.nchunk, a.nchunk, a.cw, D, a.eps, lane,
-                                mean, rstd);
-                if (lane == 0) {
-                    s_mean[t] = mean;
-                    s_rstd[t] = rstd;
-                }
-            }
+            sample_row_stats(a, b, s_mean, s_rstd, warp, kMixWarps, lane);
             __syncthreads();
         }
         for (int h = warp; h < T; h += kMixWarps) {
-            float y[NI * VEC];
-            float sum = 0.f;
+            Top* srow = S + ((size_t)h * a.Bcap + b) * D;
             if (VEC == 2) {
-                const int ni = D >> 6;
+                if (FROM_Z)
+                    mix_row_pairs<Top, Top, true, NI>(a, Z, zrow, h, s_mean, s_rstd, srow, lane);
+                else
+                    mix_row_pairs<Tin, Top, false, NI>(a, X, (size_t)D, h, s_mean, s_rstd, srow, lane);
+                continue;
+            }
+            auto load1 = [&](int t, int c) -> float {
+                if (FROM_Z) return ln_apply(to_f32(Z[t * zrow + c]), s_mean[t], s_rstd[t], a.g2[c], a.be2[c]);
+                return to_f32(X[(size_t)t * D + c]);
+            };
+            float y[NI];
+            float sum = 0.f;
 #pragma unroll
-                for (int i = 0; i < NI; ++i) {
-                    if (i < ni) {
-                        const int j = (i << 6) + (lane << 1);
-                        const int t = j / q;
-                        const int r = j - t * q;
-                        float m0, m1, x0, x1;
-                        src.load2(t, h * q + r, m0, m1);
-                        src.load2(h, j, x0, x1);
-                        y[2 * i] = m0 + x0;
-                        y[2 * i + 1] = m1 + x1;
-                        sum += y[2 * i] + y[2 * i + 1];
-                    }
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < NI; ++i) {
-                    const int j = (i << 5) + lane;
-                    if (j < D) {
-                        const int t = j / q;
-                        const int r = j - t * q;
-                        y[i] = src.load1(t, h * q + r) + src.load1(h, j);
-                        sum += y[i];
-                    }
+            for (int i = 0; i < NI; ++i) {
+                const int j = (i << 5) + lane;
+                if (j < D) {
+                    const int t = j / q;
+                    const int r = j - t * q;
+                    y[i] = load1(t, h * q + r) + load1(h, j);
+                    sum += y[i];
                 }
             }
             const float mean = warp_sum(sum) / (float)D;
             float sq = 0.f;
-            if (VEC == 2) {
-                const int ni = D >> 6;
 #pragma unroll
-                for (int i = 0; i < NI; ++i)
-                    if (i < ni) {
-                        const float d0 = y[2 * i] - mean, d1 = y[2 * i + 1] - mean;
-                        sq += d0 * d0 + d1 * d1;
-                    }
-            } else {
-#pragma unroll
-                for (int i = 0; i < NI; ++i)
-                    if ((i << 5) + lane < D) {
-                        const float d = y[i] - mean;
-                        sq += d * d;
-                    }
-            }
-            const float rstd = rsqrtf(warp_sum(sq) / (float)D + a.eps);
-            const size_t srow = ((size_t)h * a.Bcap + b) * D;
-            if (VEC == 2) {
-                const int ni = D >> 6;
-#pragma unroll
-                for (int i = 0; i < NI; ++i)
-                    if (i < ni) {
-                        const int j = (i << 6) + (lane << 1);
-                        const float2 g = *reinterpret_cast<const float2*>(a.g1 + j);
-                        const float2 be = *reinterpret_cast<const float2*>(a.be1 + j);
-                        const float v0 = ln_apply(y[2 * i], mean, rstd, g.x, be.x);
-                        const float v1 = ln_apply(y[2 * i + 1], mean, rstd, g.y, be.y);
-                        Vec2<Top>::store(S + srow + j, v0, v1);
-                    }
-            } else {
-#pragma unroll
-                for (int i = 0; i < NI; ++i) {
-                    const int j = (i << 5) + lane;
-                    if (j < D) S[srow + j] = from_f32<Top>(ln_apply(y[i], mean, rstd, a.g1[j], a.be1[j]));
+            for (int i = 0; i < NI; ++i)
+                if ((i << 5) + lane < D) {
+                    const float d = y[i] - mean;
+                    sq += d * d;
                 }
+            const float rstd = rsqrtf(warp_sum(sq) / (float)D + a.eps);
+#pragma unroll
+            for (int i = 0; i < NI; ++i) {
+                const int j = (i << 5) + lane;
+                if (j < D) srow[j] = from_f32<Top>(ln_apply(y[i], mean, rstd, a.g1[j], a.be1[j]));
             }
         }
         if (FROM_Z) __syncthreads();   // s_mean / s_rstd are rewritten for the next sample
@@ -201,36 +269,70 @@ mix_ln1_kernel(const MixLnArgs a) {
 }
 
 template <typename Tin, typename Top, bool FROM_Z, int VEC, int NI>
-cudaError_t launch_mix_inst(const MixLnArgs& a, int num_sms, cudaStream_t s) {
+cudaError_t launch_direct(const MixLnArgs& a, int num_sms, cudaStream_t s) {
     int grid = num_sms * 8;
     if (grid > a.B) grid = a.B;
-    mix_ln1_kernel<Tin, Top, FROM_Z, VEC, NI><<<grid, kMixThreads, 0, s>>>(a);
+    mix_ln1_direct_kernel<Tin, Top, FROM_Z, VEC, NI><<<grid, kMixThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
 template <typename Tin, typename Top, bool FROM_Z>
-cudaError_t launch_mix_dispatch(const MixLnArgs& a, int num_sms, cudaStream_t s) {
+cudaError_t launch_direct_dispatch(const MixLnArgs& a, int num_sms, cudaStream_t s) {
     const bool vec2 = (a.q % 2 == 0) && (a.D % 64 == 0);
     if (vec2) {
         const int ni = a.D / 64;
-        if (ni <= 4) return launch_mix_inst<Tin, Top, FROM_Z, 2, 4>(a, num_sms, s);
-        if (ni <= 12) return launch_mix_inst<Tin, Top, FROM_Z, 2, 12>(a, num_sms, s);
-        if (ni <= 24) return launch_mix_inst<Tin, Top, FROM_Z, 2, 24>(a, num_sms, s);
-        if (ni <= 48) return launch_mix_inst<Tin, Top, FROM_Z, 2, 48>(a, num_sms, s);
+        if (ni <= 4) return launch_direct<Tin, Top, FROM_Z, 2, 4>(a, num_sms, s);
+        if (ni <= 12) return launch_direct<Tin, Top, FROM_Z, 2, 12>(a, num_sms, s);
+        if (ni <= 24) return launch_direct<Tin, Top, FROM_Z, 2, 24>(a, num_sms, s);
+        if (ni <= 48) return launch_direct<Tin, Top, FROM_Z, 2, 48>(a, num_sms, s);
         return cudaErrorNotSupported;
     }
     const int ni = (a.D + 31) / 32;
-    if (ni <= 8) return launch_mix_inst<Tin, Top, FROM_Z, 1, 8>(a, num_sms, s);
-    if (ni <= 48) return launch_mix_inst<Tin, Top, FROM_Z, 1, 48>(a, num_sms, s);
+    if (ni <= 8) return launch_direct<Tin, Top, FROM_Z, 1, 8>(a, num_sms, s);
+    if (ni <= 48) return launch_direct<Tin, Top, FROM_Z, 1, 48>(a, num_sms, s);
     return cudaErrorNotSupported;
+}
+
+size_t staged_smem_bytes(int T, int D) { return 2 * (size_t)T * D * 2 + 16 + 2 * kMaxT * 4 + 16; }
+
+template <typename Tsrc, bool FROM_Z, int NI>
+cudaError_t launch_staged(const MixLnArgs& a, int num_sms, cudaStream_t s) {
+    auto k = mix_ln1_staged_kernel<Tsrc, FROM_Z, NI>;
+    const size_t smem = staged_smem_bytes(a.T, a.D);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int threads = 32 * (a.T < 16 ? a.T : 16);
+    if (threads < 128) threads = 128;
+    int per_sm = 1;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    int grid = num_sms * per_sm;
+    if (grid > a.B) grid = a.B;
+    k<<<grid, threads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename Tsrc, bool FROM_Z>
+cudaError_t launch_staged_dispatch(const MixLnArgs& a, int num_sms, cudaStream_t s) {
+    const int ni = a.D / 64;
+    if (ni <= 4) return launch_staged<Tsrc, FROM_Z, 4>(a, num_sms, s);
+    if (ni <= 12) return launch_staged<Tsrc, FROM_Z, 12>(a, num_sms, s);
+    if (ni <= 24) return launch_staged<Tsrc, FROM_Z, 24>(a, num_sms, s);
+    return launch_staged<Tsrc, FROM_Z, 48>(a, num_sms, s);
+}
+
+bool staged_ok(const MixLnArgs& a) {
+    return a.q % 2 == 0 && a.D % 64 == 0 && a.D <= 3072 && a.T <= kMaxT &&
+           staged_smem_bytes(a.T, a.D) <= 220 * 1024;
 }
 
 // ---------------------------------------------------------------------------
 // LN2 finalisation into a sample-major output: one warp per (b, t) row.
 // ---------------------------------------------------------------------------
-template <typename Tact>
-__global__ void ln2_out_kernel(const float* __restrict__ Z, const float2* __restrict__ stats,
-                               const float* __restrict__ g2, const float* __restrict__ be2, Tact* __restrict__ X,
+template <typename Tz, typename Tout>
+__global__ void ln2_out_kernel(const Tz* __restrict__ Z, const float2* __restrict__ stats,
+                               const float* __restrict__ g2, const float* __restrict__ be2, Tout* __restrict__ X,
                                int B, int T, int D, int Bcap, int nchunk, int cw, float eps) {
     const int lane = threadIdx.x & 31;
     const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -240,26 +342,26 @@ __global__ void ln2_out_kernel(const float* __restrict__ Z, const float2* __rest
         const size_t zr = (size_t)t * Bcap + b;
         float mean, rstd;
         merge_row_stats(stats + zr * nchunk, nchunk, cw, D, eps, lane, mean, rstd);
-        const float* z = Z + zr * D;
-        Tact* x = X + ((size_t)b * T + t) * D;
-        for (int j = lane; j < D; j += 32) x[j] = from_f32<Tact>(ln_apply(z[j], mean, rstd, g2[j], be2[j]));
+        const Tz* z = Z + zr * D;
+        Tout* x = X + ((size_t)b * T + t) * D;
+        for (int j = lane; j < D; j += 32)
+            x[j] = from_f32<Tout>(ln_apply(to_f32(z[j]), mean, rstd, g2[j], be2[j]));
     }
 }
 
 // ---------------------------------------------------------------------------
 // Last LN2 finalisation + mean pooling over tokens, one CTA per sample.  The
 // mean is taken over the float32 LN2 outputs in token order; XL (optional)
-// receives them rounded to the activation dtype.
+// receives them rounded to the caller's dtype.
 // ---------------------------------------------------------------------------
 constexpr int kPoolThreads = 256;
-constexpr int kPoolMaxT = 128;
 
-template <typename Tact>
+template <typename Tz, typename Tout>
 __global__ void __launch_bounds__(kPoolThreads)
-pool_kernel(const float* __restrict__ Z, const float2* __restrict__ stats, const float* __restrict__ g2,
-            const float* __restrict__ be2, float* __restrict__ pooled, Tact* __restrict__ XL, int B, int T, int D,
+pool_kernel(const Tz* __restrict__ Z, const float2* __restrict__ stats, const float* __restrict__ g2,
+            const float* __restrict__ be2, float* __restrict__ pooled, Tout* __restrict__ XL, int B, int T, int D,
             int Bcap, int nchunk, int cw, float eps) {
-    __shared__ float s_mean[kPoolMaxT], s_rstd[kPoolMaxT];
+    __shared__ float s_mean[kMaxT], s_rstd[kMaxT];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int b = blockIdx.x; b < B; b += gridDim.x) {
         for (int t = warp; t < T; t += kPoolThreads / 32) {
@@ -271,15 +373,33 @@ pool_kernel(const float* __restrict__ Z, const float2* __restrict__ stats, const
             }
         }
         __syncthreads();
-        for (int j = threadIdx.x; j < D; j += kPoolThreads) {
-            const float g = g2[j], be = be2[j];
-            float acc = 0.f;
-            for (int t = 0; t < T; ++t) {
-                const float v = ln_apply(Z[((size_t)t * Bcap + b) * D + j], s_mean[t], s_rstd[t], g, be);
-                if (XL) XL[((size_t)b * T + t) * D + j] = from_f32<Tact>(v);
-                acc += v;
+        if ((D & 1) == 0) {
+            for (int j = 2 * threadIdx.x; j < D; j += 2 * kPoolThreads) {
+                const float2 g = *reinterpret_cast<const float2*>(g2 + j);
+                const float2 be = *reinterpret_cast<const float2*>(be2 + j);
+                float acc0 = 0.f, acc1 = 0.f;
+                for (int t = 0; t < T; ++t) {
+                    float z0, z1;
+                    load_pair(Z + ((size_t)t * Bcap + b) * D + j, z0, z1);
+                    const float v0 = ln_apply(z0, s_mean[t], s_rstd[t], g.x, be.x);
+                    const float v1 = ln_apply(z1, s_mean[t], s_rstd[t], g.y, be.y);
+                    if (XL) Vec2<Tout>::store(XL + ((size_t)b * T + t) * D + j, v0, v1);
+                    acc0 += v0;
+                    acc1 += v1;
+                }
+                *reinterpret_cast<float2*>(pooled + (size_t)b * D + j) = make_float2(acc0 / (float)T, acc1 / (float)T);
             }
-            pooled[(size_t)b * D + j] = acc / (float)T;
+        } else {
+            for (int j = threadIdx.x; j < D; j += kPoolThreads) {
+                const float g = g2[j], be = be2[j];
+                float acc = 0.f;
+                for (int t = 0; t < T; ++t) {
+                    const float v = ln_apply(to_f32(Z[((size_t)t * Bcap + b) * D + j]), s_mean[t], s_rstd[t], g, be);
+                    if (XL) XL[((size_t)b * T + t) * D + j] = from_f32<Tout>(v);
+                    acc += v;
+                }
+                pooled[(size_t)b * D + j] = acc / (float)T;
+            }
         }
         __syncthreads();
     }
@@ -288,21 +408,21 @@ pool_kernel(const float* __restrict__ Z, const float2* __restrict__ stats, const
 // ---------------------------------------------------------------------------
 // Row statistics (mean, M2) of full Z rows, two passes, one warp per row.
 // ---------------------------------------------------------------------------
-__global__ void rowstats_kernel(const float* __restrict__ Z, float2* __restrict__ stats, int B, int T, int D,
-                                int Bcap) {
+template <typename Tz>
+__global__ void rowstats_kernel(const Tz* __restrict__ Z, float2* __restrict__ stats, int B, int T, int D, int Bcap) {
     const int lane = threadIdx.x & 31;
     const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
     for (long long r = wid; r < (long long)B * T; r += nw) {
         const int t = (int)(r / B), b = (int)(r % B);
         const size_t zr = (size_t)t * Bcap + b;
-        const float* z = Z + zr * D;
+        const Tz* z = Z + zr * D;
         float s = 0.f;
-        for (int j = lane; j < D; j += 32) s += z[j];
+        for (int j = lane; j < D; j += 32) s += to_f32(z[j]);
         const float mean = warp_sum(s) / (float)D;
         float m2 = 0.f;
         for (int j = lane; j < D; j += 32) {
-            const float d = z[j] - mean;
+            const float d = to_f32(z[j]) - mean;
             m2 += d * d;
         }
         m2 = warp_sum(m2);
@@ -389,46 +509,56 @@ inline int grid_for(long long n, int threads, int cap = 152 * 16) {
 
 cudaError_t launch_mix_ln1(Act act, bool from_z, const MixLnArgs& a, int num_sms, cudaStream_t s) {
     if (a.B <= 0) return cudaSuccess;
-    if (act == Act::BF16)
-        return from_z ? launch_mix_dispatch<__nv_bfloat16, __half, true>(a, num_sms, s)
-                      : launch_mix_dispatch<__nv_bfloat16, __half, false>(a, num_sms, s);
-    return from_z ? launch_mix_dispatch<float, float, true>(a, num_sms, s)
-                  : launch_mix_dispatch<float, float, false>(a, num_sms, s);
+    if (act == Act::BF16) {
+        if (staged_ok(a))
+            return from_z ? launch_staged_dispatch<__half, true>(a, num_sms, s)
+                          : launch_staged_dispatch<__nv_bfloat16, false>(a, num_sms, s);
+        return from_z ? launch_direct_dispatch<__nv_bfloat16, __half, true>(a, num_sms, s)
+                      : launch_direct_dispatch<__nv_bfloat16, __half, false>(a, num_sms, s);
+    }
+    return from_z ? launch_direct_dispatch<float, float, true>(a, num_sms, s)
+                  : launch_direct_dispatch<float, float, false>(a, num_sms, s);
 }
 
-cudaError_t launch_ln2_out(Act act, const float* Z, const float2* stats, const float* g2, const float* be2,
+cudaError_t launch_ln2_out(Act act, const void* Z, const float2* stats, const float* g2, const float* be2,
                            void* X_out, int B, int T, int D, int Bcap, int nchunk, int cw, float eps, int num_sms,
                            cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     const int grid = grid_for((long long)B * T * 32, 256, num_sms * 8);
     if (act == Act::BF16)
-        ln2_out_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(Z, stats, g2, be2, (__nv_bfloat16*)X_out, B, T, D, Bcap,
-                                                            nchunk, cw, eps);
+        ln2_out_kernel<__half, __nv_bfloat16><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2,
+                                                                   (__nv_bfloat16*)X_out, B, T, D, Bcap, nchunk, cw,
+                                                                   eps);
     else
-        ln2_out_kernel<float><<<grid, 256, 0, s>>>(Z, stats, g2, be2, (float*)X_out, B, T, D, Bcap, nchunk, cw, eps);
+        ln2_out_kernel<float, float><<<grid, 256, 0, s>>>((const float*)Z, stats, g2, be2, (float*)X_out, B, T, D,
+                                                          Bcap, nchunk, cw, eps);
     return cudaGetLastError();
 }
 
-cudaError_t launch_pool(Act act, const float* Z, const float2* stats, const float* g2, const float* be2,
+cudaError_t launch_pool(Act act, const void* Z, const float2* stats, const float* g2, const float* be2,
                         float* pooled, void* XL, int B, int T, int D, int Bcap, int nchunk, int cw, float eps,
                         int num_sms, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
-    if (T > kPoolMaxT) return cudaErrorNotSupported;
+    if (T > kMaxT) return cudaErrorNotSupported;
     const int grid = B < num_sms * 8 ? B : num_sms * 8;
     if (act == Act::BF16)
-        pool_kernel<__nv_bfloat16><<<grid, kPoolThreads, 0, s>>>(Z, stats, g2, be2, pooled, (__nv_bfloat16*)XL, B, T,
-                                                                  D, Bcap, nchunk, cw, eps);
+        pool_kernel<__half, __nv_bfloat16><<<grid, kPoolThreads, 0, s>>>((const __half*)Z, stats, g2, be2, pooled,
+                                                                         (__nv_bfloat16*)XL, B, T, D, Bcap, nchunk,
+                                                                         cw, eps);
     else
-        pool_kernel<float><<<grid, kPoolThreads, 0, s>>>(Z, stats, g2, be2, pooled, (float*)XL, B, T, D, Bcap, nchunk,
-                                                         cw, eps);
+        pool_kernel<float, float><<<grid, kPoolThreads, 0, s>>>((const float*)Z, stats, g2, be2, pooled, (float*)XL,
+                                                                B, T, D, Bcap, nchunk, cw, eps);
     return cudaGetLastError();
 }
 
-cudaError_t launch_rowstats(const float* Z, float2* stats, int B, int T, int D, int Bcap, int num_sms,
+cudaError_t launch_rowstats(Act act, const void* Z, float2* stats, int B, int T, int D, int Bcap, int num_sms,
                             cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     const int grid = grid_for((long long)B * T * 32, 256, num_sms * 8);
-    rowstats_kernel<<<grid, 256, 0, s>>>(Z, stats, B, T, D, Bcap);
+    if (act == Act::BF16)
+        rowstats_kernel<__half><<<grid, 256, 0, s>>>((const __half*)Z, stats, B, T, D, Bcap);
+    else
+        rowstats_kernel<float><<<grid, 256, 0, s>>>((const float*)Z, stats, B, T, D, Bcap);
     return cudaGetLastError();
 }
 

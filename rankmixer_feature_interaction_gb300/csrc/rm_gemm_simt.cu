@@ -17,7 +17,8 @@ constexpr int TM = 64, TN = 64, TK = 16;
 enum { EPI_GELU = 1, EPI_RESID = 2 };
 
 // out[t][m][n] = epi(sum_k A[t][m][k] * W[t][n][k] + bias[t][n]).
-// A token-major [T][Bcap][K], W [T][N][K], outputs token-major [T][Bcap][N].
+// A token-major [T][Bcap][K], W [T][N][K], outputs token-major [T][Bcap][N] in
+// the operand type (EPI_GELU: hidden activations, EPI_RESID: Z = . + S).
 template <typename Tin, int EPI>
 __global__ void __launch_bounds__(256)
 gemm_simt_kernel(const Tin* __restrict__ A, const Tin* __restrict__ W, const float* __restrict__ bias,
@@ -73,7 +74,7 @@ gemm_simt_kernel(const Tin* __restrict__ A, const Tin* __restrict__ W, const flo
             if (EPI == EPI_GELU) {
                 reinterpret_cast<Tin*>(out)[o] = from_f32<Tin>(gelu_erf(u));
             } else {
-                reinterpret_cast<float*>(out)[o] = u + to_f32(resid[o]);
+                reinterpret_cast<Tin*>(out)[o] = from_f32<Tin>(u + to_f32(resid[o]));
             }
         }
     }
@@ -97,7 +98,7 @@ cudaError_t launch_gemm1_simt(Act act, const void* S, const void* W1p, const flo
     return launch<float, EPI_GELU>(S, W1p, b1, Hid, nullptr, B, F, D, T, Bcap, s);
 }
 
-cudaError_t launch_gemm2_simt(Act act, const void* Hid, const void* W2p, const float* b2, const void* S, float* Z,
+cudaError_t launch_gemm2_simt(Act act, const void* Hid, const void* W2p, const float* b2, const void* S, void* Z,
                               int B, int T, int D, int F, int Bcap, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     if (act == Act::BF16) return launch<__half, EPI_RESID>(Hid, W2p, b2, Z, S, B, D, F, T, Bcap, s);

@@ -8,7 +8,8 @@
 //
 //   GEMM1: Hid[t] = Gelu(S[t] W1_t + b1_t)            (M = B, N = kD, K = D)
 //   GEMM2: Z[t]   = Hid[t] W2_t + b2_t + S[t]         (M = B, N = D,  K = kD)
-//          plus per-row, per-chunk LayerNorm partials (mean, M2) of Z
+//          stored in fp16, plus per-row, per-chunk LayerNorm partials
+//          (mean, M2) of the float32 values
 // Operands are fp16 (10-bit mantissa; the weights are converted exactly from
 // bf16 when the context is created), accumulation is fp32 in TMEM.
 //
@@ -79,7 +80,7 @@ struct Args {
     const float* bias;        // [weight groups][N]
     __half* hid;              // EPI_GELU output rows (same row index as A), fp16
     const __half* resid;      // EPI_RESID residual rows (same row index as A), fp16
-    float* z;                 // EPI_RESID output rows
+    __half* z;                // EPI_RESID output rows (fp16)
     float2* stats;            // EPI_RESID row partials [row][nchunk]
     int nchunk;
     const int* row_sample;    // EPI_GATED: packed row -> sample index b
@@ -334,10 +335,12 @@ pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                             s1 += d;
                             s2 = fmaf(d, d, s2);
                         }
-                        float4* dst = reinterpret_cast<float4*>(args.z + orow + 32 * c);
+                        uint4* dst = reinterpret_cast<uint4*>(args.z + orow + 32 * c);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                        for (int j = 0; j < 4; ++j)
+                            dst[j] = make_uint4(pack_f16x2(v[8 * j], v[8 * j + 1]), pack_f16x2(v[8 * j + 2], v[8 * j + 3]),
+                                                pack_f16x2(v[8 * j + 4], v[8 * j + 5]),
+                                                pack_f16x2(v[8 * j + 6], v[8 * j + 7]));
                     }
                 }
                 if (valid) {
@@ -510,7 +513,7 @@ cudaError_t launch_gemm1_tc(const void* S, const void* W1p, const float* b1, voi
     return tc::run_bn<tc::EPI_GELU>(tc::pick_bn(F), S, (long long)T * Bcap, W1p, T, a, num_sms, s);
 }
 
-cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, const void* S, float* Z,
+cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, const void* S, void* Z,
                             float2* stats, int B, int T, int D, int F, int Bcap, int num_sms, int* err,
                             unsigned long long timeout_ns, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
@@ -526,7 +529,7 @@ cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, c
     a.a_group_rows = Bcap;
     a.bias = b2;
     a.resid = reinterpret_cast<const __half*>(S);
-    a.z = Z;
+    a.z = reinterpret_cast<__half*>(Z);
     a.stats = stats;
     a.nchunk = D / (bn / 2);
     a.err = err;

@@ -25,9 +25,9 @@ inline size_t op_size(Act a) { return a == Act::F32 ? 4 : 2; }
 struct MixLnArgs {
     // input: either X (sample-major [B][T][D], caller dtype) ...
     const void* X;
-    // ... or the previous layer's pre-LN2 rows Z (token-major fp32) with
-    // per-row chunk statistics and that layer's LN2 affine, finalised in fp32.
-    const float* Z;
+    // ... or the previous layer's pre-LN2 rows Z (token-major, operand type)
+    // with per-row chunk statistics and that layer's LN2 affine, finalised in fp32.
+    const void* Z;
     const float2* stats;
     const float* g2;
     const float* be2;
@@ -37,24 +37,26 @@ struct MixLnArgs {
     const float* be1;
     int B, T, D, q, Bcap, nchunk, cw;
     float eps;
+    int* err;                        // device error word for bounded waits (nullable)
+    unsigned long long timeout_ns;
 };
 
 // S = LN1(Mix(X) + X).
 cudaError_t launch_mix_ln1(Act act, bool from_z, const MixLnArgs& a, int num_sms, cudaStream_t s);
 
-// X_out[b][t][:] = LN2(Z[t][b][:]) in the caller dtype.
-cudaError_t launch_ln2_out(Act act, const float* Z, const float2* stats, const float* g2, const float* be2,
+// X_out[b][t][:] = LN2(Z[t][b][:]) in the caller dtype (Z in the operand type).
+cudaError_t launch_ln2_out(Act act, const void* Z, const float2* stats, const float* g2, const float* be2,
                            void* X_out, int B, int T, int D, int Bcap, int nchunk, int cw, float eps,
                            int num_sms, cudaStream_t s);
 
 // pooled[b][:] = (1/T) sum_t X_L[b][t][:] with X_L = LN2(Z) in float32; XL (optional)
 // receives X_L sample-major, rounded to the caller dtype.
-cudaError_t launch_pool(Act act, const float* Z, const float2* stats, const float* g2, const float* be2,
+cudaError_t launch_pool(Act act, const void* Z, const float2* stats, const float* g2, const float* be2,
                         float* pooled, void* XL, int B, int T, int D, int Bcap, int nchunk, int cw, float eps,
                         int num_sms, cudaStream_t s);
 
-// (mean, M2) of each full row of Z (one chunk per row).
-cudaError_t launch_rowstats(const float* Z, float2* stats, int B, int T, int D, int Bcap, int num_sms,
+// (mean, M2) of each full row of Z (operand type; one chunk per row).
+cudaError_t launch_rowstats(Act act, const void* Z, float2* stats, int B, int T, int D, int Bcap, int num_sms,
                             cudaStream_t s);
 
 // Token-major operand-type [T][Bcap][D] -> sample-major caller-dtype [B][T][D].
@@ -79,12 +81,12 @@ cudaError_t launch_debug_wait(const int* flag, int* err, unsigned long long time
 
 // ---- per-token FFN GEMMs -------------------------------------------------
 // GEMM1: Hid[t] = Gelu(S[t] W1_t + b1_t), GEMM2: Z[t] = Hid[t] W2_t + b2_t + S[t].
-// Activations token-major in the operand type, weights packed K-major:
+// Activations (and Z) token-major in the operand type, weights packed K-major:
 // W1p [T][N=kD][K=D], W2p [T][N=D][K=kD].
 
 cudaError_t launch_gemm1_simt(Act act, const void* S, const void* W1p, const float* b1, void* Hid, int B, int T,
                               int D, int F, int Bcap, cudaStream_t s);
-cudaError_t launch_gemm2_simt(Act act, const void* Hid, const void* W2p, const float* b2, const void* S, float* Z,
+cudaError_t launch_gemm2_simt(Act act, const void* Hid, const void* W2p, const float* b2, const void* S, void* Z,
                               int B, int T, int D, int F, int Bcap, cudaStream_t s);
 
 // tcgen05 path (fp16 operands; BF16 contexts only).
@@ -92,7 +94,7 @@ bool tc_supported(int D, int F);
 int tc_stats_chunk_width(int D);   // chunk width of the LN2 partial statistics written by GEMM2
 cudaError_t launch_gemm1_tc(const void* S, const void* W1p, const float* b1, void* Hid, int B, int T, int D, int F,
                             int Bcap, int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s);
-cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, const void* S, float* Z,
+cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, const void* S, void* Z,
                             float2* stats, int B, int T, int D, int F, int Bcap, int num_sms, int* err,
                             unsigned long long timeout_ns, cudaStream_t s);
 

@@ -224,7 +224,7 @@ moe_gemm_simt_kernel(const Tin* __restrict__ A, const Tin* __restrict__ W, const
 }
 
 template <typename Top>
-__global__ void residual_z_kernel(const float* __restrict__ V, const Top* __restrict__ S, float* __restrict__ Z, int B,
+__global__ void residual_z_kernel(const float* __restrict__ V, const Top* __restrict__ S, Top* __restrict__ Z, int B,
                                   int T, int D, int Bcap) {
     const long long n = (long long)T * B * D;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
@@ -232,7 +232,7 @@ __global__ void residual_z_kernel(const float* __restrict__ V, const Top* __rest
         const long long tb = i / D;
         const int b = (int)(tb % B), t = (int)(tb / B);
         const size_t o = ((size_t)t * Bcap + b) * D + j;
-        Z[o] = V[o] + to_f32(S[o]);
+        Z[o] = from_f32<Top>(V[o] + to_f32(S[o]));
     }
 }
 
@@ -420,15 +420,15 @@ cudaError_t moe_forward(const MoeLaunch& ml, const MoeWeights& w, MoeWorkspace& 
     return cudaSuccess;
 }
 
-cudaError_t moe_residual_z(Act act, const float* V, const void* S, float* Z, int B, int T, int D, int Bcap,
+cudaError_t moe_residual_z(Act act, const float* V, const void* S, void* Z, int B, int T, int D, int Bcap,
                            cudaStream_t s) {
     const long long n = (long long)T * B * D;
     int grid = (int)((n + 255) / 256);
     if (grid > 152 * 16) grid = 152 * 16;
     if (act == Act::BF16)
-        residual_z_kernel<__half><<<grid, 256, 0, s>>>(V, (const __half*)S, Z, B, T, D, Bcap);
+        residual_z_kernel<__half><<<grid, 256, 0, s>>>(V, (const __half*)S, (__half*)Z, B, T, D, Bcap);
     else
-        residual_z_kernel<float><<<grid, 256, 0, s>>>(V, (const float*)S, Z, B, T, D, Bcap);
+        residual_z_kernel<float><<<grid, 256, 0, s>>>(V, (const float*)S, (float*)Z, B, T, D, Bcap);
     return cudaGetLastError();
 }
 

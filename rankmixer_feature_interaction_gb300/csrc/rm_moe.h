@@ -65,8 +65,8 @@ cudaError_t moe_forward(const MoeLaunch& ml, const MoeWeights& w, MoeWorkspace& 
                         float* gates_out, cudaStream_t s, const std::function<void*(int)>& prof_begin,
                         const std::function<void(void*)>& prof_end);
 
-// Z[t][b][:] = V[t][b][:] + S[t][b][:]; token-major, V and Z float32, S in the operand type.
-cudaError_t moe_residual_z(Act act, const float* V, const void* S, float* Z, int B, int T, int D, int Bcap,
+// Z[t][b][:] = V[t][b][:] + S[t][b][:]; token-major, V float32, S and Z in the operand type.
+cudaError_t moe_residual_z(Act act, const float* V, const void* S, void* Z, int B, int T, int D, int Bcap,
                            cudaStream_t s);
 
 }  // namespace rm
