@@ -201,6 +201,204 @@ mix_ln1_staged_kernel(const MixLnArgs a) {
 }
 
 // ---------------------------------------------------------------------------
+// Staged mix + LN1, 8 columns per lane (bf16 contexts, q % 8 == 0,
+// D % 256 == 0).  Same pipeline as above, with:
+//   - 16-byte shared-memory loads and global stores (8 elements per lane);
+//     an 8-column group never crosses a head block because q % 8 == 0;
+//   - both LN affines staged in shared memory once per CTA;
+//   - (FROM_Z) LN2 finalised in place, once per element, before mixing.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void to_f32x8(const uint4 v, bool is_bf16, float (&o)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        float2 f;
+        if (is_bf16) f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+        else f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+        o[2 * k] = f.x;
+        o[2 * k + 1] = f.y;
+    }
+}
+
+template <bool FROM_Z, int NV>
+__global__ void __launch_bounds__(512)
+mix_ln1_v8_kernel(const MixLnArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int T = a.T, D = a.D, q = a.q;
+    const uint32_t row_bytes = (uint32_t)D * 2u;
+    const uint32_t buf_bytes = (uint32_t)T * row_bytes;
+    uint16_t* buf = reinterpret_cast<uint16_t*>(smem);                 // [2][T][D] 16-bit
+    float* sg1 = reinterpret_cast<float*>(smem + 2 * (size_t)buf_bytes);  // [D]
+    float* sb1 = sg1 + D;
+    float* sg2 = sb1 + D;                                               // FROM_Z only
+    float* sb2 = sg2 + D;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sb2 + D);
+    float* s_mean = reinterpret_cast<float*>(bars + 2);
+    float* s_rstd = s_mean + kMaxT;
+    volatile int* s_abort = reinterpret_cast<volatile int*>(s_rstd + kMaxT);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = blockDim.x >> 5;
+    const uint16_t* src = FROM_Z ? reinterpret_cast<const uint16_t*>(a.Z) : reinterpret_cast<const uint16_t*>(a.X);
+    __half* S = reinterpret_cast<__half*>(a.S);
+
+    for (int j = threadIdx.x; j < D; j += blockDim.x) {
+        sg1[j] = a.g1[j];
+        sb1[j] = a.be1[j];
+        if (FROM_Z) {
+            sg2[j] = a.g2[j];
+            sb2[j] = a.be2[j];
+        }
+    }
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bars[0]), 1);
+        mbar_init(smem_u32(&bars[1]), 1);
+        *s_abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    auto issue = [&](int b, int slot) {   // thread 0 only
+        const uint32_t bar = smem_u32(&bars[slot]);
+        const uint32_t dst = smem_u32(buf) + (uint32_t)slot * buf_bytes;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, buf_bytes);
+        if (!FROM_Z) {
+            bulk_copy_g2s(dst, src + (size_t)b * T * D, buf_bytes, bar);
+        } else {
+            for (int t = 0; t < T; ++t)
+                bulk_copy_g2s(dst + (uint32_t)t * row_bytes, src + ((size_t)t * a.Bcap + b) * D, row_bytes, bar);
+        }
+    };
+
+    if (threadIdx.x == 0 && (int)blockIdx.x < a.B) issue(blockIdx.x, 0);
+    int it = 0;
+    for (int b = blockIdx.x; b < a.B; b += gridDim.x, ++it) {
+        const int slot = it & 1;
+        if (threadIdx.x == 0 && b + (int)gridDim.x < a.B) issue(b + gridDim.x, slot ^ 1);
+        if (FROM_Z) sample_row_stats(a, b, s_mean, s_rstd, warp, nwarps, lane);
+        mbar_wait_bounded(smem_u32(&bars[slot]), (uint32_t)(it >> 1) & 1u, s_abort, a.err, a.timeout_ns);
+        __syncthreads();
+        if (*s_abort) break;
+        uint16_t* xs = buf + (size_t)slot * T * D;
+        if (FROM_Z) {
+            // X_{n-1} = LN2(Z) in place (fp16), 8 elements per lane
+            for (int t = warp; t < T; t += nwarps) {
+                const float mt = s_mean[t], rt = s_rstd[t];
+                uint16_t* row = xs + (size_t)t * D;
+                for (int c = lane * 8; c < D; c += 256) {
+                    float z[8];
+                    to_f32x8(*reinterpret_cast<const uint4*>(row + c), false, z);
+                    const float4 ga = *reinterpret_cast<const float4*>(sg2 + c);
+                    const float4 gb = *reinterpret_cast<const float4*>(sg2 + c + 4);
+                    const float4 ba = *reinterpret_cast<const float4*>(sb2 + c);
+                    const float4 bb = *reinterpret_cast<const float4*>(sb2 + c + 4);
+                    const float g[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+                    const float be[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        o[k] = pack_f16x2(ln_apply(z[2 * k], mt, rt, g[2 * k], be[2 * k]),
+                                          ln_apply(z[2 * k + 1], mt, rt, g[2 * k + 1], be[2 * k + 1]));
+                    *reinterpret_cast<uint4*>(row + c) = make_uint4(o[0], o[1], o[2], o[3]);
+                }
+            }
+            __syncthreads();
+        }
+        const int nv = D >> 8;
+        for (int h = warp; h < T; h += nwarps) {
+            const uint16_t* xh = xs + (size_t)h * D;
+            float y[8 * NV];
+            float sum = 0.f;
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                if (i < nv) {
+                    const int j0 = (i << 8) + (lane << 3);
+                    const int t = j0 / q;
+                    const int r = j0 - t * q;
+                    float m[8], x[8];
+                    to_f32x8(*reinterpret_cast<const uint4*>(xs + (size_t)t * D + h * q + r), !FROM_Z, m);
+                    to_f32x8(*reinterpret_cast<const uint4*>(xh + j0), !FROM_Z, x);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        y[8 * i + k] = m[k] + x[k];
+                        sum += y[8 * i + k];
+                    }
+                }
+            }
+            const float mean = warp_sum(sum) / (float)D;
+            float sq = 0.f;
+#pragma unroll
+            for (int i = 0; i < NV; ++i)
+                if (i < nv) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const float d = y[8 * i + k] - mean;
+                        sq += d * d;
+                    }
+                }
+            const float rstd = rsqrtf(warp_sum(sq) / (float)D + a.eps);
+            __half* srow = S + ((size_t)h * a.Bcap + b) * D;
+#pragma unroll
+            for (int i = 0; i < NV; ++i)
+                if (i < nv) {
+                    const int j0 = (i << 8) + (lane << 3);
+                    const float4 ga = *reinterpret_cast<const float4*>(sg1 + j0);
+                    const float4 gb = *reinterpret_cast<const float4*>(sg1 + j0 + 4);
+                    const float4 ba = *reinterpret_cast<const float4*>(sb1 + j0);
+                    const float4 bb = *reinterpret_cast<const float4*>(sb1 + j0 + 4);
+                    const float g[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+                    const float be[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        o[k] = pack_f16x2(ln_apply(y[8 * i + 2 * k], mean, rstd, g[2 * k], be[2 * k]),
+                                          ln_apply(y[8 * i + 2 * k + 1], mean, rstd, g[2 * k + 1], be[2 * k + 1]));
+                    *reinterpret_cast<uint4*>(srow + j0) = make_uint4(o[0], o[1], o[2], o[3]);
+                }
+        }
+        __syncthreads();    // the slot and the row statistics are reused by later samples
+    }
+}
+
+size_t v8_smem_bytes(int T, int D) {
+    return 2 * (size_t)T * D * 2 + 4 * (size_t)D * 4 + 16 + 2 * kMaxT * 4 + 16;
+}
+
+bool v8_ok(const MixLnArgs& a) {
+    return a.q % 8 == 0 && a.D % 256 == 0 && a.D <= 3072 && a.T <= kMaxT && v8_smem_bytes(a.T, a.D) <= 226 * 1024;
+}
+
+template <bool FROM_Z, int NV>
+cudaError_t launch_v8(const MixLnArgs& a, int num_sms, cudaStream_t s) {
+    auto k = mix_ln1_v8_kernel<FROM_Z, NV>;
+    const size_t smem = v8_smem_bytes(a.T, a.D);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int threads = 32 * (a.T < 16 ? a.T : 16);
+    if (threads < 128) threads = 128;
+    int per_sm = 1;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    int grid = num_sms * per_sm;
+    if (grid > a.B) grid = a.B;
+    k<<<grid, threads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <bool FROM_Z>
+cudaError_t launch_v8_dispatch(const MixLnArgs& a, int num_sms, cudaStream_t s) {
+    const int nv = a.D / 256;
+    if (nv <= 1) return launch_v8<FROM_Z, 1>(a, num_sms, s);
+    if (nv <= 2) return launch_v8<FROM_Z, 2>(a, num_sms, s);
+    if (nv <= 3) return launch_v8<FROM_Z, 3>(a, num_sms, s);
+    if (nv <= 4) return launch_v8<FROM_Z, 4>(a, num_sms, s);
+    if (nv <= 6) return launch_v8<FROM_Z, 6>(a, num_sms, s);
+    if (nv <= 8) return launch_v8<FROM_Z, 8>(a, num_sms, s);
+    return launch_v8<FROM_Z, 12>(a, num_sms, s);
+}
+
+// ---------------------------------------------------------------------------
 // Direct mix + LN1 (float32 contexts and shapes the staged kernel does not
 // take): X read straight from global memory, one CTA per sample.
 // VEC = 2 uses mix_row_pairs (q even, D % 64 == 0); VEC = 1 handles any q.
@@ -510,6 +708,7 @@ inline int grid_for(long long n, int threads, int cap = 152 * 16) {
 cudaError_t launch_mix_ln1(Act act, bool from_z, const MixLnArgs& a, int num_sms, cudaStream_t s) {
     if (a.B <= 0) return cudaSuccess;
     if (act == Act::BF16) {
+        if (v8_ok(a)) return from_z ? launch_v8_dispatch<true>(a, num_sms, s) : launch_v8_dispatch<false>(a, num_sms, s);
         if (staged_ok(a))
             return from_z ? launch_staged_dispatch<__half, true>(a, num_sms, s)
                           : launch_staged_dispatch<__nv_bfloat16, false>(a, num_sms, s);

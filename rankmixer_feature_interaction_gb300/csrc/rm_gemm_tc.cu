@@ -71,6 +71,7 @@ struct Args {
     long long a_group_rows;
     int m_tiles;              // ceil(M / BM), uniform groups only
     int n_tiles;
+    int n_fastest;            // uniform groups: walk N tiles fastest (A tile shared by neighbours)
     long long tiles;          // uniform groups only
     // variable groups (MoE experts), indexed by weight group: row count and first packed row;
     // tile_prefix[j] = sum over launch groups i < j of ceil(count / BM)  (length ngroups + 1)
@@ -119,8 +120,13 @@ __device__ __forceinline__ TileCoord decode_tile(long long tile, const Args& a) 
         const long long per_group = (long long)a.m_tiles * a.n_tiles;
         c.j = (int)(tile / per_group);
         const int rem = (int)(tile - (long long)c.j * per_group);
-        c.nb = rem / a.m_tiles;   // m fastest: neighbouring CTAs share the weight tile
-        c.mb = rem - c.nb * a.m_tiles;
+        if (a.n_fastest) {        // neighbouring CTAs share the activation tile
+            c.mb = rem / a.n_tiles;
+            c.nb = rem - c.mb * a.n_tiles;
+        } else {                  // neighbouring CTAs share the weight tile
+            c.nb = rem / a.m_tiles;
+            c.mb = rem - c.nb * a.m_tiles;
+        }
         c.wg = a.group_base + c.j * a.group_stride;
         c.Mg = a.M;
         c.row0 = (long long)c.j * a.a_group_rows;
@@ -453,6 +459,9 @@ cudaError_t run(const void* A, long long a_rows_total, const void* W, int n_wgro
     if (a.tile_prefix == nullptr) {
         a.m_tiles = (a.M + BM - 1) / BM;
         a.tiles = (long long)a.ngroups * a.m_tiles * a.n_tiles;
+        // Keep the larger operand of a group resident across neighbouring CTAs:
+        // walk N fastest when the activation rows (M x K) outweigh the weights (N x K).
+        a.n_fastest = a.M > a.N ? 1 : 0;
         if (a.tiles == 0) return cudaSuccess;
     }
     CUtensorMap mA, mB;
