@@ -29,6 +29,7 @@
 // word, the other roles see an abort flag and all of them unwind.
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 #include <string>
 
@@ -148,6 +149,110 @@ __device__ __forceinline__ TileCoord decode_tile(long long tile, const Args& a) 
         c.row0 = __ldg(a.g_off + c.wg);
     }
     return c;
+}
+
+// Epilogue of one accumulator tile for one warp: the warp owns 32 rows of the
+// tile (its TMEM lane quadrant) and COLS columns starting at n0; `tbase` is
+// the TMEM address of its first column.  Every lane takes part in the TMEM
+// loads; only rows inside the group (valid) are stored.
+template <int COLS, int EPI>
+__device__ __forceinline__ void epilogue_tile(const Args& args, const TileCoord& tc, bool valid, long long arow,
+                                              uint32_t tbase, int n0) {
+    const size_t orow = (size_t)arow * (size_t)args.N + n0;
+    const float* bias = args.bias + (size_t)tc.wg * args.N + n0;
+    if (EPI == EPI_GELU) {
+#pragma unroll 1
+        for (int c = 0; c < (COLS / 32); ++c) {
+            float v[32];
+            tmem_ld32(tbase + 32u * c, v);
+            if (valid) {
+                uint32_t p[16];
+                const float4* b4 = reinterpret_cast<const float4*>(bias + 32 * c);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 bb = __ldg(b4 + j);
+                    p[2 * j] = pack_f16x2(gelu_erf(v[4 * j] + bb.x), gelu_erf(v[4 * j + 1] + bb.y));
+                    p[2 * j + 1] = pack_f16x2(gelu_erf(v[4 * j + 2] + bb.z), gelu_erf(v[4 * j + 3] + bb.w));
+                }
+                uint4* dst = reinterpret_cast<uint4*>(args.hid + orow + 32 * c);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+            }
+        }
+    } else if (EPI == EPI_RESID) {
+        float shift = 0.f, s1 = 0.f, s2 = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < (COLS / 32); ++c) {
+            float v[32];
+            tmem_ld32(tbase + 32u * c, v);
+            if (valid) {
+                const float4* b4 = reinterpret_cast<const float4*>(bias + 32 * c);
+                add_f16x32(v, args.resid + orow + 32 * c);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 bb = __ldg(b4 + j);
+                    v[4 * j] += bb.x;
+                    v[4 * j + 1] += bb.y;
+                    v[4 * j + 2] += bb.z;
+                    v[4 * j + 3] += bb.w;
+                }
+                if (c == 0) {
+                    float mm = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) mm += v[j];
+                    shift = mm * (1.0f / 32.0f);
+                }
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float d = v[j] - shift;
+                    s1 += d;
+                    s2 = fmaf(d, d, s2);
+                }
+                uint4* dst = reinterpret_cast<uint4*>(args.z + orow + 32 * c);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    dst[j] = make_uint4(pack_f16x2(v[8 * j], v[8 * j + 1]), pack_f16x2(v[8 * j + 2], v[8 * j + 3]),
+                                        pack_f16x2(v[8 * j + 4], v[8 * j + 5]),
+                                        pack_f16x2(v[8 * j + 6], v[8 * j + 7]));
+            }
+        }
+        if (valid) {
+            const float n = (float)COLS;
+            const float mean = shift + s1 / n;
+            const float m2 = fmaxf(s2 - s1 * s1 / n, 0.f);
+            const int chunk = n0 / COLS;
+            args.stats[(size_t)arow * args.nchunk + chunk] = make_float2(mean, m2);
+        }
+    } else {  // EPI_GATED: V[b, t] += gate * (acc + b2)
+        float gate = 0.f;
+        float* vrow = nullptr;
+        if (valid) {
+            const int b = __ldg(args.row_sample + arow);
+            const int t = tc.wg / args.gE, e = tc.wg - t * args.gE;
+            gate = __ldg(args.gates + ((size_t)b * args.gT + t) * args.gE + e);
+            vrow = args.v + (size_t)b * args.v_sb + (size_t)t * args.v_st + n0;
+        }
+#pragma unroll 1
+        for (int c = 0; c < (COLS / 32); ++c) {
+            float v[32];
+            tmem_ld32(tbase + 32u * c, v);
+            if (valid) {
+                const float4* b4 = reinterpret_cast<const float4*>(bias + 32 * c);
+                float4* dst = reinterpret_cast<float4*>(vrow + 32 * c);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 bb = __ldg(b4 + j);
+                    float4 o = dst[j];
+                    o.x = fmaf(gate, v[4 * j] + bb.x, o.x);
+                    o.y = fmaf(gate, v[4 * j + 1] + bb.y, o.y);
+                    o.z = fmaf(gate, v[4 * j + 2] + bb.z, o.z);
+                    o.w = fmaf(gate, v[4 * j + 3] + bb.w, o.w);
+                    dst[j] = o;
+                }
+            }
+        }
+    }
 }
 
 template <int BN, int EPI>
@@ -289,102 +394,8 @@ pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const uint32_t tbase =
                 tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN + half * C::COLS_PER_WARP);
             const int n0 = tc.nb * BN + half * C::COLS_PER_WARP;
-            const size_t orow = (size_t)arow * (size_t)args.N + n0;
-            const float* bias = args.bias + (size_t)tc.wg * args.N + n0;
 
-            if (EPI == EPI_GELU) {
-#pragma unroll 1
-                for (int c = 0; c < C::CHUNKS; ++c) {
-                    float v[32];
-                    tmem_ld32(tbase + 32u * c, v);
-                    if (valid) {
-                        uint32_t p[16];
-                        const float4* b4 = reinterpret_cast<const float4*>(bias + 32 * c);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const float4 bb = __ldg(b4 + j);
-                            p[2 * j] = pack_f16x2(gelu_erf(v[4 * j] + bb.x), gelu_erf(v[4 * j + 1] + bb.y));
-                            p[2 * j + 1] = pack_f16x2(gelu_erf(v[4 * j + 2] + bb.z), gelu_erf(v[4 * j + 3] + bb.w));
-                        }
-                        uint4* dst = reinterpret_cast<uint4*>(args.hid + orow + 32 * c);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
-                    }
-                }
-            } else if (EPI == EPI_RESID) {
-                float shift = 0.f, s1 = 0.f, s2 = 0.f;
-#pragma unroll 1
-                for (int c = 0; c < C::CHUNKS; ++c) {
-                    float v[32];
-                    tmem_ld32(tbase + 32u * c, v);
-                    if (valid) {
-                        const float4* b4 = reinterpret_cast<const float4*>(bias + 32 * c);
-                        add_f16x32(v, args.resid + orow + 32 * c);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const float4 bb = __ldg(b4 + j);
-                            v[4 * j] += bb.x;
-                            v[4 * j + 1] += bb.y;
-                            v[4 * j + 2] += bb.z;
-                            v[4 * j + 3] += bb.w;
-                        }
-                        if (c == 0) {
-                            float mm = 0.f;
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) mm += v[j];
-                            shift = mm * (1.0f / 32.0f);
-                        }
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const float d = v[j] - shift;
-                            s1 += d;
-                            s2 = fmaf(d, d, s2);
-                        }
-                        uint4* dst = reinterpret_cast<uint4*>(args.z + orow + 32 * c);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            dst[j] = make_uint4(pack_f16x2(v[8 * j], v[8 * j + 1]), pack_f16x2(v[8 * j + 2], v[8 * j + 3]),
-                                                pack_f16x2(v[8 * j + 4], v[8 * j + 5]),
-                                                pack_f16x2(v[8 * j + 6], v[8 * j + 7]));
-                    }
-                }
-                if (valid) {
-                    const float n = (float)C::COLS_PER_WARP;
-                    const float mean = shift + s1 / n;
-                    const float m2 = fmaxf(s2 - s1 * s1 / n, 0.f);
-                    const int chunk = tc.nb * 2 + half;
-                    args.stats[(size_t)arow * args.nchunk + chunk] = make_float2(mean, m2);
-                }
-            } else {  // EPI_GATED: V[b, t] += gate * (acc + b2)
-                float gate = 0.f;
-                float* vrow = nullptr;
-                if (valid) {
-                    const int b = __ldg(args.row_sample + arow);
-                    const int t = tc.wg / args.gE, e = tc.wg - t * args.gE;
-                    gate = __ldg(args.gates + ((size_t)b * args.gT + t) * args.gE + e);
-                    vrow = args.v + (size_t)b * args.v_sb + (size_t)t * args.v_st + n0;
-                }
-#pragma unroll 1
-                for (int c = 0; c < C::CHUNKS; ++c) {
-                    float v[32];
-                    tmem_ld32(tbase + 32u * c, v);
-                    if (valid) {
-                        const float4* b4 = reinterpret_cast<const float4*>(bias + 32 * c);
-                        float4* dst = reinterpret_cast<float4*>(vrow + 32 * c);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const float4 bb = __ldg(b4 + j);
-                            float4 o = dst[j];
-                            o.x = fmaf(gate, v[4 * j] + bb.x, o.x);
-                            o.y = fmaf(gate, v[4 * j + 1] + bb.y, o.y);
-                            o.z = fmaf(gate, v[4 * j + 2] + bb.z, o.z);
-                            o.w = fmaf(gate, v[4 * j + 3] + bb.w, o.w);
-                            dst[j] = o;
-                        }
-                    }
-                }
-            }
+            epilogue_tile<C::COLS_PER_WARP, EPI>(args, tc, valid, arow, tbase, n0);
             tc_fence_before();
             mbar_arrive(tempty_bar(acc));
             acc ^= 1;
@@ -397,6 +408,200 @@ pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (warp == 2) {
         tc_fence_after();
         tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+
+// ----------------------------------------------------------------------------
+// CTA-pair variant for the dense PFFN (uniform groups): a cluster of 2 CTAs
+// on two SMs computes a 256 x BN tile with tcgen05.mma.cta_group::2.  CTA r
+// of the pair loads A rows [128 r, 128 r + 128) of the tile and B rows
+// [BN/2 r, BN/2 r + BN/2) into its own shared memory; the even CTA issues the
+// pair MMA (M = 256), which reads both CTAs' tiles and accumulates each CTA's
+// 128 rows x BN columns in that CTA's TMEM.  Per CTA a stage is 32 KB (A 16 KB
+// + half of B 16 KB), so 6 stages fit and each SM pulls a third less operand
+// data from L2 than the single-CTA kernel.
+//   full[s]   (even CTA)  1 arrival (its producer, expecting both CTAs' bytes)
+//                         + the TMA bytes of both CTAs
+//   empty[s]  (each CTA)  1 arrival: multicast commit from the even CTA
+//   tfull[a]  (each CTA)  1 arrival: multicast commit from the even CTA
+//   tempty[a] (even CTA)  16 arrivals: every epilogue warp of both CTAs
+// ----------------------------------------------------------------------------
+constexpr int BM2 = 256;                 // rows per CTA pair
+
+template <int BN>
+struct Cfg2 {
+    static constexpr int STAGES = 6;
+    static constexpr int A_BYTES = 128 * BK * 2;
+    static constexpr int B_BYTES = (BN / 2) * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int TMEM_COLS = 2 * BN;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+    static constexpr int COLS_PER_WARP = BN / 2;
+    static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation must be a power of 2");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "pair MMA N");
+    static_assert(2 * STAGES * 8 + 4 * 8 + 8 <= BAR_BYTES, "barrier area");
+};
+
+template <int BN, int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const Args args) {
+    using C = Cfg2<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t* base_ptr = smem_raw + (base - raw_addr);
+    const uint32_t sA = base;
+    const uint32_t sB = base + C::STAGES * C::A_BYTES;
+    const uint32_t bar0 = base + C::STAGES * C::STAGE_BYTES;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
+    uint32_t* tmem_holder =
+        reinterpret_cast<uint32_t*>(base_ptr + C::STAGES * C::STAGE_BYTES + 8 * (2 * C::STAGES + 4));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();          // 0: issues the pair MMAs
+    const long long pair = blockIdx.x >> 1;
+    const long long npairs = gridDim.x >> 1;
+
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 2 * kEpiWarps);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 2) {
+        tmem_alloc_pair(smem_u32(tmem_holder), C::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();               // reconverge before the aligned cluster barrier
+    cluster_sync_all();            // barriers and TMEM of both CTAs exist before any cross-CTA use
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
+
+    const int kblocks = args.K / BK;
+    const long long tiles = args.tiles;
+
+    if (warp == 0) {
+        // ---------------------------- TMA producer (both CTAs) ----------------------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (long long tile = pair; ok && tile < tiles; tile += npairs) {
+                const TileCoord tc = decode_tile(tile, args);
+                const int arow = (int)(tc.row0 + (long long)tc.mb * BM2 + 128 * (int)rank);
+                const int brow = tc.nb * BN + (BN / 2) * (int)rank;
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, args.err, args.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = mapa_shared(full_bar(stage), 0);
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), (uint32_t)(2 * C::STAGE_BYTES));
+                    tma_load_3d_pair(&tmA, sA + stage * C::A_BYTES, fb, kb * BK, arow, 0);
+                    tma_load_3d_pair(&tmB, sB + stage * C::B_BYTES, fb, kb * BK, brow, tc.wg);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------- pair MMA issuer (even CTA) --------------------------
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc = make_idesc_f16_f32(BM2, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (long long tile = pair; ok && tile < tiles; tile += npairs) {
+                if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.err, args.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, args.err, args.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = sA + stage * C::A_BYTES;
+                    const uint32_t b0 = sB + stage * C::B_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        umma_f16_pair(d_tmem, make_sw128_desc(a0 + 32u * k), make_sw128_desc(b0 + 32u * k), idesc,
+                                      (kb > 0 || k > 0) ? 1u : 0u);
+                    }
+                    umma_commit_pair_mc(empty_bar(stage), (uint16_t)0x3);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit_pair_mc(tfull_bar(acc), (uint16_t)0x3);
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+        }
+    } else if (warp >= 4) {
+        // ---------------------------- epilogue (both CTAs) --------------------------------
+        const int ew = warp - 4;
+        const int quad = warp & 3;
+        const int half = ew >> 2;
+        const int row_in_tile = quad * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (long long tile = pair; tile < tiles; tile += npairs) {
+            const TileCoord tc = decode_tile(tile, args);
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err, args.timeout_ns);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            __syncwarp();
+            tc_fence_after();
+            const int m = tc.mb * BM2 + 128 * (int)rank + row_in_tile;
+            const bool valid = m < tc.Mg;
+            const long long arow = tc.row0 + m;
+            const uint32_t tbase =
+                tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN + half * C::COLS_PER_WARP);
+            const int n0 = tc.nb * BN + half * C::COLS_PER_WARP;
+            epilogue_tile<C::COLS_PER_WARP, EPI>(args, tc, valid, arow, tbase, n0);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();            // no CTA leaves while its peer may still touch its memory
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
     }
 }
 
@@ -491,6 +696,75 @@ cudaError_t run_bn(int bn, const void* A, long long a_rows_total, const void* W,
     }
 }
 
+
+// CTA-pair launch for uniform groups (dense PFFN).  Grid = 2 x the number of
+// pairs that can be resident at once (persistent).
+template <int BN, int EPI>
+cudaError_t run_pair(const void* A, long long a_rows_total, const void* W, int n_wgroups, Args a, int num_sms,
+                     cudaStream_t s) {
+    using C = Cfg2<BN>;
+    a.n_tiles = a.N / BN;
+    a.m_tiles = (a.M + BM2 - 1) / BM2;
+    a.tiles = (long long)a.ngroups * a.m_tiles * a.n_tiles;
+    a.n_fastest = a.M > a.N ? 1 : 0;
+    if (a.tiles == 0) return cudaSuccess;
+    CUtensorMap mA, mB;
+    if (!make_map(&mA, A, a.K, a_rows_total, 1, a_rows_total, 128)) return cudaErrorInvalidValue;
+    if (!make_map(&mB, W, a.K, a.N, n_wgroups, a.N, BN / 2)) return cudaErrorInvalidValue;
+    auto k = pffn_gemm_tc2_kernel<BN, EPI>;
+    static int max_pairs = 0;   // once per template instance
+    if (max_pairs == 0) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(2 * (num_sms / 2)), 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = num_sms / 2;
+        }
+        max_pairs = n;
+    }
+    long long pairs = a.tiles < max_pairs ? a.tiles : max_pairs;
+    k<<<(int)(2 * pairs), kThreads, C::SMEM_BYTES, s>>>(mA, mB, a);
+    return cudaGetLastError();
+}
+
+// Pair tiles for the dense PFFN when every token group has at least 256 rows;
+// RM_GEMM_PAIR=0 in the environment selects the single-CTA kernel instead
+// (a tuning and diagnosis switch; both compute the same result).
+bool use_pair(int M) {
+    static int env = -1;
+    if (env < 0) {
+        const char* v = getenv("RM_GEMM_PAIR");
+        env = (v && v[0] == '0') ? 0 : 1;
+    }
+    return env == 1 && M >= BM2;
+}
+
+template <int EPI>
+cudaError_t run_dense(int bn, const void* A, long long a_rows_total, const void* W, int n_wgroups, const Args& a,
+                      int num_sms, cudaStream_t s) {
+    if (use_pair(a.M)) {
+        switch (bn) {
+            case 256: return run_pair<256, EPI>(A, a_rows_total, W, n_wgroups, a, num_sms, s);
+            case 128: return run_pair<128, EPI>(A, a_rows_total, W, n_wgroups, a, num_sms, s);
+            case 64: return run_pair<64, EPI>(A, a_rows_total, W, n_wgroups, a, num_sms, s);
+            default: return cudaErrorNotSupported;
+        }
+    }
+    return run_bn<EPI>(bn, A, a_rows_total, W, n_wgroups, a, num_sms, s);
+}
+
 }  // namespace tc
 
 bool tc_supported(int D, int F) {
@@ -519,7 +793,7 @@ cudaError_t launch_gemm1_tc(const void* S, const void* W1p, const float* b1, voi
     a.hid = reinterpret_cast<__half*>(Hid);
     a.err = err;
     a.timeout_ns = timeout_ns;
-    return tc::run_bn<tc::EPI_GELU>(tc::pick_bn(F), S, (long long)T * Bcap, W1p, T, a, num_sms, s);
+    return tc::run_dense<tc::EPI_GELU>(tc::pick_bn(F), S, (long long)T * Bcap, W1p, T, a, num_sms, s);
 }
 
 cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, const void* S, void* Z,
@@ -543,7 +817,7 @@ cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, c
     a.nchunk = D / (bn / 2);
     a.err = err;
     a.timeout_ns = timeout_ns;
-    return tc::run_bn<tc::EPI_RESID>(bn, Hid, (long long)T * Bcap, W2p, T, a, num_sms, s);
+    return tc::run_dense<tc::EPI_RESID>(bn, Hid, (long long)T * Bcap, W2p, T, a, num_sms, s);
 }
 
 cudaError_t launch_moe_gemm1_tc(const void* Sg, long long rows_total, const void* W1p, const float* b1, void* Hm,
