@@ -243,6 +243,12 @@ RM_API rm_status rm_profile_read(rm_ctx *ctx, rm_kernel_stat *stats);
  * error word and returns.  The next rm_sync_status() reports it. */
 RM_API rm_status rm_debug_wait_timeout(rm_ctx *ctx, int timeout_us, void *stream);
 
+/* Test hook: out[i] = the GELU the library's GEMM epilogues apply, for n
+ * float32 device values (u * Phi(u), "RankMixer 详解（1）" section 4.1, with
+ * erf from Abramowitz & Stegun formula 7.1.26, |error in erf| <= 1.5e-7).
+ * Asynchronous on `stream`. */
+RM_API rm_status rm_debug_gelu(const float *u, float *out, long long n, void *stream);
+
 /* Message of the last failing call on this host thread ("" if none). */
 RM_API const char *rm_last_error(void);
 

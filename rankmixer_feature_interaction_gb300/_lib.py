@@ -40,7 +40,7 @@ RM_K_COUNT = len(KERNEL_KINDS)
 EXPORTED = ["rm_create", "rm_destroy", "rm_block_forward", "rm_stack_forward", "rm_stack_forward_host",
             "rm_moe_pffn_forward", "rm_token_mix", "rm_sync_status", "rm_get_info", "rm_profile_enable",
             "rm_profile_read", "rm_debug_wait_timeout", "rm_last_error", "rm_abi_version",
-            "rm_block_forward_noalloc"]
+            "rm_block_forward_noalloc", "rm_debug_gelu"]
 
 
 class rm_config(ctypes.Structure):
@@ -100,6 +100,7 @@ def load() -> ctypes.CDLL:
         "rm_last_error": (ctypes.c_char_p, []),
         "rm_abi_version": (i, []),
         "rm_block_forward_noalloc": (st, [vp, i, vp, vp, i, vp]),
+        "rm_debug_gelu": (st, [vp, vp, ctypes.c_longlong, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -175,6 +176,10 @@ def rm_profile_read(ctx: int) -> dict:
 
 def rm_debug_wait_timeout(ctx: int, timeout_us: int, stream: int) -> None:
     check(load().rm_debug_wait_timeout(ctx, timeout_us, stream), "rm_debug_wait_timeout")
+
+
+def rm_debug_gelu(u: int, out: int, n: int, stream: int) -> None:
+    check(load().rm_debug_gelu(u, out, n, stream), "rm_debug_gelu")
 
 
 def rm_last_error() -> str:

@@ -584,6 +584,13 @@ rm_status rm_profile_read(rm_ctx* c, rm_kernel_stat* stats) {
     return RM_OK;
 }
 
+rm_status rm_debug_gelu(const float* u, float* out, long long n, void* stream) {
+    if (n < 0) return fail(RM_ERR_INVALID_ARG, "n must be >= 0");
+    if (n > 0 && (!u || !out)) return fail(RM_ERR_INVALID_ARG, "u / out is NULL");
+    RM_CHECK_CUDA(launch_debug_gelu(u, out, n, as_stream(stream)), "debug gelu");
+    return RM_OK;
+}
+
 rm_status rm_debug_wait_timeout(rm_ctx* c, int timeout_us, void* stream) {
     rm_status st;
     if ((st = check_ctx(c)) != RM_OK) return st;

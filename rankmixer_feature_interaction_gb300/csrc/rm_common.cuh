@@ -41,9 +41,24 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 }
 
 // GELU in its exact form u * Phi(u), Phi(u) = (1 + erf(u / sqrt 2)) / 2
-// ("RankMixer 详解（1）" section 4.1).
+// ("RankMixer 详解（1）" section 4.1), branch-free.  The complementary error
+// function of x = |u| / sqrt 2 >= 0 comes from Abramowitz & Stegun, Handbook
+// of Mathematical Functions (1964), formula 7.1.26 (after Hastings):
+//   1 - erf(x) = (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-x^2),
+//   t = 1 / (1 + p x),  |error in erf| <= 1.5e-7,
+// so 1 + erf(u / sqrt 2) is 2 - c for u >= 0 and c for u < 0 (no cancellation
+// for negative u).  The whole function costs two MUFU operations and a few
+// FMAs where erff branches on |x|.
 __device__ __forceinline__ float gelu_erf(float u) {
-    return 0.5f * u * (1.0f + erff(u * 0.70710678118654752f));
+    constexpr float p = 0.3275911f;
+    constexpr float a1 = 0.254829592f, a2 = -0.284496736f, a3 = 1.421413741f, a4 = -1.453152027f,
+                    a5 = 1.061405429f;
+    const float x = fabsf(u) * 0.70710678118654752f;
+    const float t = __fdividef(1.0f, fmaf(p, x, 1.0f));
+    const float poly = t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, a5, a4), a3), a2), a1);
+    const float c = poly * __expf(-x * x);            // 1 - erf(x)
+    const float phi2 = u >= 0.0f ? 2.0f - c : c;       // 1 + erf(u / sqrt 2)
+    return 0.5f * u * phi2;
 }
 
 // ---------------------------------------------------------------------------

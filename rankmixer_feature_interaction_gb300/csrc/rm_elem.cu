@@ -684,6 +684,11 @@ __global__ void to_f32_kernel(const Tin* __restrict__ in, float* __restrict__ ou
         out[i] = to_f32(in[i]);
 }
 
+__global__ void debug_gelu_kernel(const float* __restrict__ u, float* __restrict__ out, long long n) {
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+        out[i] = gelu_erf(u[i]);
+}
+
 __global__ void debug_wait_kernel(const int* flag, int* err, unsigned long long timeout_ns) {
     if (threadIdx.x != 0) return;
     const uint64_t t0 = globaltimer_ns();
@@ -809,6 +814,12 @@ cudaError_t launch_to_f32(Act act, const void* in, float* out, size_t n, cudaStr
         to_f32_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16*)in, out, n);
     else
         to_f32_kernel<float><<<grid, 256, 0, s>>>((const float*)in, out, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_debug_gelu(const float* u, float* out, long long n, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    debug_gelu_kernel<<<grid_for(n, 256), 256, 0, s>>>(u, out, n);
     return cudaGetLastError();
 }
 

@@ -49,6 +49,21 @@ def test_token_mix_bit_exact(dtype, B, T, D, H):
     np.testing.assert_array_equal(_np(Y), oracle.token_mix(_np(X), H))
 
 
+def test_device_gelu_matches_the_definition():
+    """The epilogue GELU (erf by Abramowitz & Stegun 7.1.26) against u * Phi(u) in float64."""
+    from scipy.special import ndtr
+    u = torch.cat([torch.linspace(-12, 12, 200001), torch.tensor([0.0, -0.0, 1.0, -1.0, 30.0, -30.0, 1e-8, -1e-8])])
+    out = torch.empty_like(u, device=DEV)
+    ud = u.to(DEV)
+    _lib.rm_debug_gelu(ud.data_ptr(), out.data_ptr(), u.numel(), torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    x = u.double().numpy()
+    ref = x * ndtr(x)
+    g = out.cpu().double().numpy()
+    err = np.abs(g - ref) / np.maximum(1.0, np.abs(x))
+    assert err.max() <= 4e-7, f"max scaled error {err.max():.3e}"
+
+
 # ----------------------------------------------------------------------------
 # Tiny float32 configuration (T=4, D=8, H=4: the A1..D4 layout), 1e-4
 # ----------------------------------------------------------------------------
