@@ -54,7 +54,8 @@ struct Cfg {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+    static constexpr int EPI_BYTES = kEpiWarps * 2 * 2048;   // per epilogue warp: two 32 x 32 fp16 blocks
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
     static constexpr int COLS_PER_WARP = BN / 2;        // two epilogue warps per lane quadrant
     static constexpr int CHUNKS = COLS_PER_WARP / 32;
     static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation must be a power of 2");
@@ -81,6 +82,7 @@ struct Args {
     const int* tile_prefix;
     const float* bias;        // [weight groups][N]
     __half* hid;              // EPI_GELU output rows (same row index as A), fp16
+    int hid_tma;              // EPI_GELU, uniform groups: store through shared memory with TMA (output map)
     const __half* resid;      // EPI_RESID residual rows (same row index as A), fp16
     __half* z;                // EPI_RESID output rows (fp16)
     float2* stats;            // EPI_RESID row partials [row][nchunk]
@@ -149,6 +151,50 @@ __device__ __forceinline__ TileCoord decode_tile(long long tile, const Args& a) 
         c.row0 = __ldg(a.g_off + c.wg);
     }
     return c;
+}
+
+// EPI_GELU epilogue through shared memory and TMA tensor stores (uniform
+// groups).  The warp's 32 rows x COLS columns are written in 32 x 32 blocks:
+// each lane packs its row's 32 GELU outputs (64 bytes) into a staging block
+// with the 64-byte swizzle (16-byte chunk k of row r at chunk k ^ ((r >> 1) & 3)),
+// and lane 0 hands the block to the TMA engine, which writes whole lines and
+// clips rows past the token group's batch.  Two staging blocks per warp
+// alternate; a block is refilled only after the store that read it has
+// finished reading (bulk wait_group.read 1).
+template <int COLS>
+__device__ __forceinline__ void epilogue_gelu_tma(const Args& args, const TileCoord& tc, const CUtensorMap* tmC,
+                                                  uint32_t tbase, int n0, int m_warp, uint32_t stage, int lane,
+                                                  int& sbuf) {
+    const float* bias = args.bias + (size_t)tc.wg * args.N + n0;
+    const bool any_valid = m_warp < tc.Mg;
+    const uint32_t sw = (uint32_t)((lane >> 1) & 3);
+#pragma unroll 1
+    for (int c = 0; c < COLS / 32; ++c) {
+        float v[32];
+        tmem_ld32(tbase + 32u * c, v);
+        uint32_t p[16];
+        const float4* b4 = reinterpret_cast<const float4*>(bias + 32 * c);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 bb = __ldg(b4 + j);
+            p[2 * j] = pack_f16x2(gelu_erf(v[4 * j] + bb.x), gelu_erf(v[4 * j + 1] + bb.y));
+            p[2 * j + 1] = pack_f16x2(gelu_erf(v[4 * j + 2] + bb.z), gelu_erf(v[4 * j + 3] + bb.w));
+        }
+        if (lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
+        const uint32_t buf = stage + (uint32_t)sbuf * 2048u;
+        const uint32_t row = buf + (uint32_t)lane * 64u;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            st_shared_v4(row + (((uint32_t)k ^ sw) << 4), p[4 * k], p[4 * k + 1], p[4 * k + 2], p[4 * k + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            if (any_valid) tma_store_3d(tmC, buf, n0 + 32 * c, m_warp, tc.j);
+            bulk_commit_group();
+        }
+        sbuf ^= 1;
+    }
 }
 
 // Epilogue of one accumulator tile for one warp: the warp owns 32 rows of the
@@ -258,7 +304,7 @@ __device__ __forceinline__ void epilogue_tile(const Args& args, const TileCoord&
 template <int BN, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
 pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const Args args) {
+                    const __grid_constant__ CUtensorMap tmC, const Args args) {
     using C = Cfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -266,14 +312,15 @@ pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     uint8_t* base_ptr = smem_raw + (base - raw_addr);
     const uint32_t sA = base;
     const uint32_t sB = base + C::STAGES * C::A_BYTES;
-    const uint32_t bar0 = base + C::STAGES * C::STAGE_BYTES;
+    const uint32_t sEpi = base + C::STAGES * C::STAGE_BYTES;           // epilogue staging, 1024-aligned
+    const uint32_t bar0 = sEpi + C::EPI_BYTES;
     // barrier addresses: full[s], empty[s], tfull[2], tempty[2]
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
     auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
     uint32_t* tmem_holder =
-        reinterpret_cast<uint32_t*>(base_ptr + C::STAGES * C::STAGE_BYTES + 8 * (2 * C::STAGES + 4));
+        reinterpret_cast<uint32_t*>(base_ptr + C::STAGES * C::STAGE_BYTES + C::EPI_BYTES + 8 * (2 * C::STAGES + 4));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -377,6 +424,8 @@ pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const int quad = warp & 3;              // TMEM lanes this warp may read
         const int half = ew >> 2;               // which BN/2 columns
         const int row_in_tile = quad * 32 + lane;
+        const uint32_t stage = sEpi + (uint32_t)ew * 4096u;
+        int sbuf = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (long long tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
@@ -394,13 +443,16 @@ pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const uint32_t tbase =
                 tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN + half * C::COLS_PER_WARP);
             const int n0 = tc.nb * BN + half * C::COLS_PER_WARP;
-
-            epilogue_tile<C::COLS_PER_WARP, EPI>(args, tc, valid, arow, tbase, n0);
+            if (EPI == EPI_GELU && args.hid_tma)
+                epilogue_gelu_tma<C::COLS_PER_WARP>(args, tc, &tmC, tbase, n0, m - lane, stage, lane, sbuf);
+            else
+                epilogue_tile<C::COLS_PER_WARP, EPI>(args, tc, valid, arow, tbase, n0);
             tc_fence_before();
             mbar_arrive(tempty_bar(acc));
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
+        if (lane == 0) bulk_wait_group<0>();   // this warp's tensor stores have landed
     }
 
     tc_fence_before();
@@ -437,7 +489,8 @@ struct Cfg2 {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+    static constexpr int EPI_BYTES = kEpiWarps * 2 * 2048;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
     static constexpr int COLS_PER_WARP = BN / 2;
     static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation must be a power of 2");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -448,7 +501,7 @@ struct Cfg2 {
 template <int BN, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const Args args) {
+                     const __grid_constant__ CUtensorMap tmC, const Args args) {
     using C = Cfg2<BN>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -456,13 +509,14 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     uint8_t* base_ptr = smem_raw + (base - raw_addr);
     const uint32_t sA = base;
     const uint32_t sB = base + C::STAGES * C::A_BYTES;
-    const uint32_t bar0 = base + C::STAGES * C::STAGE_BYTES;
+    const uint32_t sEpi = base + C::STAGES * C::STAGE_BYTES;           // epilogue staging, 1024-aligned
+    const uint32_t bar0 = sEpi + C::EPI_BYTES;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
     auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
     uint32_t* tmem_holder =
-        reinterpret_cast<uint32_t*>(base_ptr + C::STAGES * C::STAGE_BYTES + 8 * (2 * C::STAGES + 4));
+        reinterpret_cast<uint32_t*>(base_ptr + C::STAGES * C::STAGE_BYTES + C::EPI_BYTES + 8 * (2 * C::STAGES + 4));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -571,6 +625,8 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         const int quad = warp & 3;
         const int half = ew >> 2;
         const int row_in_tile = quad * 32 + lane;
+        const uint32_t stage = sEpi + (uint32_t)ew * 4096u;
+        int sbuf = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (long long tile = pair; tile < tiles; tile += npairs) {
@@ -587,13 +643,17 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             const uint32_t tbase =
                 tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN + half * C::COLS_PER_WARP);
             const int n0 = tc.nb * BN + half * C::COLS_PER_WARP;
-            epilogue_tile<C::COLS_PER_WARP, EPI>(args, tc, valid, arow, tbase, n0);
+            if (EPI == EPI_GELU && args.hid_tma)
+                epilogue_gelu_tma<C::COLS_PER_WARP>(args, tc, &tmC, tbase, n0, m - lane, stage, lane, sbuf);
+            else
+                epilogue_tile<C::COLS_PER_WARP, EPI>(args, tc, valid, arow, tbase, n0);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
+        if (lane == 0) bulk_wait_group<0>();   // this warp's tensor stores have landed
     }
 
     tc_fence_before();
@@ -647,6 +707,26 @@ bool make_map(CUtensorMap* m, const void* ptr, int K, long long rows, int groups
     return true;
 }
 
+// Output map for the hidden activations of uniform groups: fp16 [groups][rows][N]
+// (row pitch N, group pitch group_rows * N), box 32 x 32 x 1, 64-byte swizzle.
+// Rows at or past `rows` are clipped, so a tile never writes into the next group.
+bool make_map_out(CUtensorMap* m, const void* ptr, int N, int rows, int groups, long long group_rows) {
+    if (!get_encoder()) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)rows, (cuuint64_t)groups};
+    cuuint64_t strides[2] = {(cuuint64_t)N * 2, (cuuint64_t)group_rows * (cuuint64_t)N * 2};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        g_err = "cuTensorMapEncodeTiled (output) failed with CUresult " + std::to_string((int)r);
+        return false;
+    }
+    return true;
+}
+
 int pick_bn(int N) {
     if (N % 256 == 0) return 256;
     if (N % 128 == 0) return 128;
@@ -669,9 +749,15 @@ cudaError_t run(const void* A, long long a_rows_total, const void* W, int n_wgro
         a.n_fastest = a.M > a.N ? 1 : 0;
         if (a.tiles == 0) return cudaSuccess;
     }
-    CUtensorMap mA, mB;
+    CUtensorMap mA, mB, mC;
     if (!make_map(&mA, A, a.K, a_rows_total, 1, a_rows_total, BM)) return cudaErrorInvalidValue;
     if (!make_map(&mB, W, a.K, a.N, n_wgroups, a.N, BN)) return cudaErrorInvalidValue;
+    if (EPI == EPI_GELU && a.hid_tma && a.tile_prefix == nullptr) {
+        if (!make_map_out(&mC, a.hid, a.N, a.M, a.ngroups, a.a_group_rows)) return cudaErrorInvalidValue;
+    } else {
+        a.hid_tma = 0;
+        mC = mA;   // unused
+    }
     auto k = pffn_gemm_tc_kernel<BN, EPI>;
     static bool attr_done = false;  // once per template instance
     if (!attr_done) {
@@ -681,7 +767,7 @@ cudaError_t run(const void* A, long long a_rows_total, const void* W, int n_wgro
     }
     long long grid = num_sms;
     if (a.tile_prefix == nullptr && a.tiles < grid) grid = a.tiles;
-    k<<<(int)grid, kThreads, C::SMEM_BYTES, s>>>(mA, mB, a);
+    k<<<(int)grid, kThreads, C::SMEM_BYTES, s>>>(mA, mB, mC, a);
     return cudaGetLastError();
 }
 
@@ -708,9 +794,15 @@ cudaError_t run_pair(const void* A, long long a_rows_total, const void* W, int n
     a.tiles = (long long)a.ngroups * a.m_tiles * a.n_tiles;
     a.n_fastest = a.M > a.N ? 1 : 0;
     if (a.tiles == 0) return cudaSuccess;
-    CUtensorMap mA, mB;
+    CUtensorMap mA, mB, mC;
     if (!make_map(&mA, A, a.K, a_rows_total, 1, a_rows_total, 128)) return cudaErrorInvalidValue;
     if (!make_map(&mB, W, a.K, a.N, n_wgroups, a.N, BN / 2)) return cudaErrorInvalidValue;
+    if (EPI == EPI_GELU && a.hid_tma) {
+        if (!make_map_out(&mC, a.hid, a.N, a.M, a.ngroups, a.a_group_rows)) return cudaErrorInvalidValue;
+    } else {
+        a.hid_tma = 0;
+        mC = mA;   // unused
+    }
     auto k = pffn_gemm_tc2_kernel<BN, EPI>;
     static int max_pairs = 0;   // once per template instance
     if (max_pairs == 0) {
@@ -735,7 +827,7 @@ cudaError_t run_pair(const void* A, long long a_rows_total, const void* W, int n
         max_pairs = n;
     }
     long long pairs = a.tiles < max_pairs ? a.tiles : max_pairs;
-    k<<<(int)(2 * pairs), kThreads, C::SMEM_BYTES, s>>>(mA, mB, a);
+    k<<<(int)(2 * pairs), kThreads, C::SMEM_BYTES, s>>>(mA, mB, mC, a);
     return cudaGetLastError();
 }
 
@@ -791,6 +883,7 @@ cudaError_t launch_gemm1_tc(const void* S, const void* W1p, const float* b1, voi
     a.a_group_rows = Bcap;
     a.bias = b1;
     a.hid = reinterpret_cast<__half*>(Hid);
+    a.hid_tma = 1;
     a.err = err;
     a.timeout_ns = timeout_ns;
     return tc::run_dense<tc::EPI_GELU>(tc::pick_bn(F), S, (long long)T * Bcap, W1p, T, a, num_sms, s);
