@@ -35,9 +35,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
 }
+// Two floats -> packed fp16x2 (lo in the low half), round to nearest, finite
+// overflow saturated to +-65504 (NaN stays NaN): one cvt instruction.
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-    __half2 v = __floats2half2_rn(sat_f16(lo), sat_f16(hi));
-    return *reinterpret_cast<uint32_t*>(&v);
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
 // GELU in its exact form u * Phi(u), Phi(u) = (1 + erf(u / sqrt 2)) / 2
@@ -46,19 +49,33 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 // of Mathematical Functions (1964), formula 7.1.26 (after Hastings):
 //   1 - erf(x) = (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-x^2),
 //   t = 1 / (1 + p x),  |error in erf| <= 1.5e-7,
-// so 1 + erf(u / sqrt 2) is 2 - c for u >= 0 and c for u < 0 (no cancellation
-// for negative u).  The whole function costs two MUFU operations and a few
-// FMAs where erff branches on |x|.
+//   p = 0.3275911, a1..a5 = 0.254829592, -0.284496736, 1.421413741,
+//   -1.453152027, 1.061405429.
+// With c = 1 - erf(x): Gelu(u) = u - u c / 2 for u >= 0 and u c / 2 for u < 0
+// (no cancellation for negative u).  To save instructions the code works
+// with x' = |u| sqrt(log2(e) / 2), so exp(-x^2) = 2^(-x'^2) and t = 1 / (1 + p' x')
+// with p' = p / (sqrt 2 sqrt(log2(e) / 2)), and carries the 1/2 in the
+// coefficients (ah_i = a_i / 2).  Reciprocal and 2^y use the MUFU unit.
+__device__ __forceinline__ float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
 __device__ __forceinline__ float gelu_erf(float u) {
-    constexpr float p = 0.3275911f;
-    constexpr float a1 = 0.254829592f, a2 = -0.284496736f, a3 = 1.421413741f, a4 = -1.453152027f,
-                    a5 = 1.061405429f;
-    const float x = fabsf(u) * 0.70710678118654752f;
-    const float t = __fdividef(1.0f, fmaf(p, x, 1.0f));
-    const float poly = t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, a5, a4), a3), a2), a1);
-    const float c = poly * __expf(-x * x);            // 1 - erf(x)
-    const float phi2 = u >= 0.0f ? 2.0f - c : c;       // 1 + erf(u / sqrt 2)
-    return 0.5f * u * phi2;
+    constexpr float k1 = 0.8493218002880191f;     // sqrt(log2(e) / 2)
+    constexpr float pp = 0.27273748087922245f;    // p / (sqrt(2) k1)
+    constexpr float ah1 = 0.127414796f, ah2 = -0.142248368f, ah3 = 0.7107068705f, ah4 = -0.7265760135f,
+                    ah5 = 0.5307027145f;
+    const float xp = fabsf(u) * k1;
+    const float t = rcp_approx(fmaf(pp, xp, 1.0f));
+    const float poly = t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, ah5, ah4), ah3), ah2), ah1);
+    const float uc = u * (poly * ex2_approx(-xp * xp));   // u (1 - erf(|u| / sqrt 2)) / 2
+    return u >= 0.0f ? u - uc : uc;
 }
 
 // ---------------------------------------------------------------------------

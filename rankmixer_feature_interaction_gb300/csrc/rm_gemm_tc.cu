@@ -831,22 +831,27 @@ cudaError_t run_pair(const void* A, long long a_rows_total, const void* W, int n
     return cudaGetLastError();
 }
 
-// Pair tiles for the dense PFFN when every token group has at least 256 rows;
-// RM_GEMM_PAIR=0 in the environment selects the single-CTA kernel instead
-// (a tuning and diagnosis switch; both compute the same result).
-bool use_pair(int M) {
+// Pair tiles for the dense PFFN's second GEMM (K = kD) when every token group
+// has at least 256 rows.  Measured on GB300 at the 1B shape: pair tiles speed
+// up GEMM2 (3.14 -> 3.01 ms per step) but slow down GEMM1 (3.60 -> 3.87 ms),
+// whose short K (= D) leaves its heavier GELU epilogue on the critical path,
+// where the two CTAs of a pair wait for each other.  RM_GEMM_PAIR=0 (never) or
+// =1 (both GEMMs) in the environment overrides the choice (a tuning and
+// diagnosis switch; every choice computes the same result).
+bool use_pair(int M, int epi) {
     static int env = -1;
     if (env < 0) {
         const char* v = getenv("RM_GEMM_PAIR");
-        env = (v && v[0] == '0') ? 0 : 1;
+        env = !v ? 2 : (v[0] == '0' ? 0 : 1);
     }
-    return env == 1 && M >= BM2;
+    if (M < BM2 || env == 0) return false;
+    return env == 1 || epi == EPI_RESID;
 }
 
 template <int EPI>
 cudaError_t run_dense(int bn, const void* A, long long a_rows_total, const void* W, int n_wgroups, const Args& a,
                       int num_sms, cudaStream_t s) {
-    if (use_pair(a.M)) {
+    if (use_pair(a.M, EPI)) {
         switch (bn) {
             case 256: return run_pair<256, EPI>(A, a_rows_total, W, n_wgroups, a, num_sms, s);
             case 128: return run_pair<128, EPI>(A, a_rows_total, W, n_wgroups, a, num_sms, s);
