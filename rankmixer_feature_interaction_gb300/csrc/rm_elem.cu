@@ -220,18 +220,30 @@ __device__ __forceinline__ void to_f32x8(const uint4 v, bool is_bf16, float (&o)
     }
 }
 
+// Shared-memory layout of the 8-wide kernel.  Each staged row of D 16-bit
+// elements is padded to a stride RS with RS = q (mod 64): an 8-lane phase of a
+// 16-byte load covers 64 consecutive mixed columns, which may span two source
+// rows (head h of row t, then head h of row t + 1); with this stride the second
+// row's chunks continue the first row's bank sequence, so the phase touches 8
+// distinct 16-byte bank groups.  The LN affines are kept as fp16 (exact: they
+// arrive as bf16 values), so a lane's 8 affines are one 16-byte load.
+__host__ __device__ __forceinline__ int v8_row_stride(int D, int q) { return D + (q & 63); }
+
+__device__ __forceinline__ void f16x8_to_f32(const uint4 v, float (&o)[8]) { to_f32x8(v, false, o); }
+
 template <bool FROM_Z, int NV>
 __global__ void __launch_bounds__(512)
 mix_ln1_v8_kernel(const MixLnArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int T = a.T, D = a.D, q = a.q;
+    const int RS = v8_row_stride(D, q);
     const uint32_t row_bytes = (uint32_t)D * 2u;
-    const uint32_t buf_bytes = (uint32_t)T * row_bytes;
-    uint16_t* buf = reinterpret_cast<uint16_t*>(smem);                 // [2][T][D] 16-bit
-    float* sg1 = reinterpret_cast<float*>(smem + 2 * (size_t)buf_bytes);  // [D]
-    float* sb1 = sg1 + D;
-    float* sg2 = sb1 + D;                                               // FROM_Z only
-    float* sb2 = sg2 + D;
+    const uint32_t buf_elems = (uint32_t)T * RS;
+    uint16_t* buf = reinterpret_cast<uint16_t*>(smem);                       // [2][T][RS] 16-bit
+    __half* sg1 = reinterpret_cast<__half*>(smem + 4 * (size_t)buf_elems);    // [D] each
+    __half* sb1 = sg1 + D;
+    __half* sg2 = sb1 + D;                                                    // FROM_Z only
+    __half* sb2 = sg2 + D;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sb2 + D);
     float* s_mean = reinterpret_cast<float*>(bars + 2);
     float* s_rstd = s_mean + kMaxT;
@@ -242,11 +254,11 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
     __half* S = reinterpret_cast<__half*>(a.S);
 
     for (int j = threadIdx.x; j < D; j += blockDim.x) {
-        sg1[j] = a.g1[j];
-        sb1[j] = a.be1[j];
+        sg1[j] = __float2half_rn(a.g1[j]);
+        sb1[j] = __float2half_rn(a.be1[j]);
         if (FROM_Z) {
-            sg2[j] = a.g2[j];
-            sb2[j] = a.be2[j];
+            sg2[j] = __float2half_rn(a.g2[j]);
+            sb2[j] = __float2half_rn(a.be2[j]);
         }
     }
     if (threadIdx.x == 0) {
@@ -257,16 +269,14 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
     }
     __syncthreads();
 
-    auto issue = [&](int b, int slot) {   // thread 0 only
+    auto issue = [&](int b, int slot) {   // thread 0 only: T row copies into padded rows
         const uint32_t bar = smem_u32(&bars[slot]);
-        const uint32_t dst = smem_u32(buf) + (uint32_t)slot * buf_bytes;
+        const uint32_t dst = smem_u32(buf) + (uint32_t)slot * buf_elems * 2u;
         fence_proxy_async_smem();
-        mbar_arrive_expect_tx(bar, buf_bytes);
-        if (!FROM_Z) {
-            bulk_copy_g2s(dst, src + (size_t)b * T * D, buf_bytes, bar);
-        } else {
-            for (int t = 0; t < T; ++t)
-                bulk_copy_g2s(dst + (uint32_t)t * row_bytes, src + ((size_t)t * a.Bcap + b) * D, row_bytes, bar);
+        mbar_arrive_expect_tx(bar, (uint32_t)T * row_bytes);
+        for (int t = 0; t < T; ++t) {
+            const uint16_t* row = FROM_Z ? src + ((size_t)t * a.Bcap + b) * D : src + ((size_t)b * T + t) * D;
+            bulk_copy_g2s(dst + (uint32_t)t * (uint32_t)RS * 2u, row, row_bytes, bar);
         }
     };
 
@@ -279,21 +289,17 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
         mbar_wait_bounded(smem_u32(&bars[slot]), (uint32_t)(it >> 1) & 1u, s_abort, a.err, a.timeout_ns);
         __syncthreads();
         if (*s_abort) break;
-        uint16_t* xs = buf + (size_t)slot * T * D;
+        uint16_t* xs = buf + (size_t)slot * buf_elems;
         if (FROM_Z) {
             // X_{n-1} = LN2(Z) in place (fp16), 8 elements per lane
             for (int t = warp; t < T; t += nwarps) {
                 const float mt = s_mean[t], rt = s_rstd[t];
-                uint16_t* row = xs + (size_t)t * D;
+                uint16_t* row = xs + (size_t)t * RS;
                 for (int c = lane * 8; c < D; c += 256) {
-                    float z[8];
-                    to_f32x8(*reinterpret_cast<const uint4*>(row + c), false, z);
-                    const float4 ga = *reinterpret_cast<const float4*>(sg2 + c);
-                    const float4 gb = *reinterpret_cast<const float4*>(sg2 + c + 4);
-                    const float4 ba = *reinterpret_cast<const float4*>(sb2 + c);
-                    const float4 bb = *reinterpret_cast<const float4*>(sb2 + c + 4);
-                    const float g[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-                    const float be[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
+                    float z[8], g[8], be[8];
+                    f16x8_to_f32(*reinterpret_cast<const uint4*>(row + c), z);
+                    f16x8_to_f32(*reinterpret_cast<const uint4*>(sg2 + c), g);
+                    f16x8_to_f32(*reinterpret_cast<const uint4*>(sb2 + c), be);
                     uint32_t o[4];
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
@@ -306,7 +312,7 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
         }
         const int nv = D >> 8;
         for (int h = warp; h < T; h += nwarps) {
-            const uint16_t* xh = xs + (size_t)h * D;
+            const uint16_t* xh = xs + (size_t)h * RS;
             float y[8 * NV];
             float sum = 0.f;
 #pragma unroll
@@ -316,7 +322,7 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
                     const int t = j0 / q;
                     const int r = j0 - t * q;
                     float m[8], x[8];
-                    to_f32x8(*reinterpret_cast<const uint4*>(xs + (size_t)t * D + h * q + r), !FROM_Z, m);
+                    to_f32x8(*reinterpret_cast<const uint4*>(xs + (size_t)t * RS + h * q + r), !FROM_Z, m);
                     to_f32x8(*reinterpret_cast<const uint4*>(xh + j0), !FROM_Z, x);
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
@@ -342,12 +348,9 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
             for (int i = 0; i < NV; ++i)
                 if (i < nv) {
                     const int j0 = (i << 8) + (lane << 3);
-                    const float4 ga = *reinterpret_cast<const float4*>(sg1 + j0);
-                    const float4 gb = *reinterpret_cast<const float4*>(sg1 + j0 + 4);
-                    const float4 ba = *reinterpret_cast<const float4*>(sb1 + j0);
-                    const float4 bb = *reinterpret_cast<const float4*>(sb1 + j0 + 4);
-                    const float g[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-                    const float be[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
+                    float g[8], be[8];
+                    f16x8_to_f32(*reinterpret_cast<const uint4*>(sg1 + j0), g);
+                    f16x8_to_f32(*reinterpret_cast<const uint4*>(sb1 + j0), be);
                     uint32_t o[4];
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
@@ -360,18 +363,19 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
     }
 }
 
-size_t v8_smem_bytes(int T, int D) {
-    return 2 * (size_t)T * D * 2 + 4 * (size_t)D * 4 + 16 + 2 * kMaxT * 4 + 16;
+size_t v8_smem_bytes(int T, int D, int q) {
+    return 2 * (size_t)T * v8_row_stride(D, q) * 2 + 4 * (size_t)D * 2 + 16 + 2 * kMaxT * 4 + 16;
 }
 
 bool v8_ok(const MixLnArgs& a) {
-    return a.q % 8 == 0 && a.D % 256 == 0 && a.D <= 3072 && a.T <= kMaxT && v8_smem_bytes(a.T, a.D) <= 226 * 1024;
+    return a.q % 8 == 0 && a.D % 256 == 0 && a.D <= 3072 && a.T <= kMaxT &&
+           v8_smem_bytes(a.T, a.D, a.q) <= 226 * 1024;
 }
 
 template <bool FROM_Z, int NV>
 cudaError_t launch_v8(const MixLnArgs& a, int num_sms, cudaStream_t s) {
     auto k = mix_ln1_v8_kernel<FROM_Z, NV>;
-    const size_t smem = v8_smem_bytes(a.T, a.D);
+    const size_t smem = v8_smem_bytes(a.T, a.D, a.q);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int threads = 32 * (a.T < 16 ? a.T : 16);
