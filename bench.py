@@ -234,10 +234,15 @@ def run_ours(args):
     gemm_kinds = ["moe_gemm1", "moe_gemm2"] if moe else ["gemm1", "gemm2"]
     dom = max(gemm_kinds, key=lambda kk: kstats[kk][1])
     launches, tot_ms = kstats[dom]
+    active = None
     if moe:
-        # algorithmic flops of the launch class: active rows x 2 D Fe per expert layer
-        active_rows = None
-        flops_launch = None
+        # algorithmic flops: every open (sample, token, expert) runs 2 D Fe flops in each
+        # expert layer; expert layer 1 is one launch, layer 2 one launch per expert index
+        _, G = m.moe_pffn_forward(0, S_in, V, return_gates=True)
+        active = int((G > 0).sum().item())
+        per_layer = 2.0 * active * D * Fe
+        flops_launch = per_layer if dom == "moe_gemm1" else per_layer / E
+        flops_step = 2 * per_layer + 2.0 * B * T * D * E      # + router
     else:
         flops_launch = flops_gemm
     roofline = None
@@ -249,7 +254,8 @@ def run_ours(args):
                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
                     "peak_source": f"{peak_src} bf16_tflops_sustained",
                     "avg_launch_ms": round(avg_ms, 4)}
-    flops_step = 4.0 * k * L * T * D * D * B
+    if not moe:
+        flops_step = 4.0 * k * L * T * D * D * B
     gpu_launches = int(sum(v[0] for kk, v in kstats.items() if kk != "misc"))
 
     out = {
@@ -270,12 +276,13 @@ def run_ours(args):
                    "batch_per_gpu": B, "global_batch": B * world, "parallelism": f"replicas x{world} (batch sharded)",
                    "l2": "inputs larger than L2 (X0 %.0f MB, weights %.0f MB > 129 MB)" % (
                        X0.numel() * 2 / 1e6, m.info.weight_bytes / 1e6)},
-        "tflops": None if moe else round(flops_step * args.steps * world / (ms_max / 1e3) / 1e12, 1),
-        "frac_of_peak_step": None if moe else round(
+        "tflops": round(flops_step * args.steps * world / (ms_max / 1e3) / 1e12, 1),
+        "frac_of_peak_step": round(
             flops_step * args.steps / (ms_max / 1e3) / 1e12 / peaks.get("bf16_tflops_sustained", 1700.0), 4),
         "roofline": roofline,
         "kernels_ms_per_step": {kk: round(v[1] / args.steps, 4) for kk, v in kstats.items() if v[0]},
         "gpu_launches": gpu_launches,
+        "moe_mean_active_experts": round(active / (B * T), 3) if moe else None,
         "clocks": clk,
         "e2e": e2e,
     }
