@@ -128,6 +128,23 @@ def shard_batch(global_batch: int, world: int, rank: int) -> tuple[int, int]:
     return start, start + base + (1 if rank < rem else 0)
 
 
+def max_over_ranks(x: float, device="cpu") -> float:
+    """The largest of the ranks' values of x (each rank passes its own); x itself
+    when no process group is running."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(samples_per_rank: int, world: int, steps: int, seconds_max: float) -> float:
+    """Whole-job throughput: the samples all ranks processed over the slowest rank's time."""
+    return world * samples_per_rank * steps / seconds_max
+
+
 # ----------------------------------------------------------------------------
 # Our arm
 # ----------------------------------------------------------------------------
@@ -150,12 +167,13 @@ def run_ours(args):
     moe = args.config == "moe_1b"
     L = args.layers or c["L"]
     E, Fe = c.get("E", 0), c.get("Fe", 0)
-    seed = 20260101 + 17 * rank
+    # weak scaling: the job's batch is world * B samples, rank r owns shard r
+    start, stop = shard_batch(world * B, world, rank)
     layers = synth.make_stack(T, D, k, L, 4242, "bf16", dev, E=E, Fe=Fe, active=c.get("active", 2.0))
     m = RankMixer(T, D, k, layers, dtype="bf16", max_batch=B, n_experts=E, expert_hidden=Fe)
     del layers
     torch.cuda.empty_cache()
-    X0 = synth.make_input(B, T, D, seed, "bf16", dev)
+    X0 = synth.make_input_shard(world * B, start, stop, T, D, 20260101, "bf16", dev)
     pooled = torch.empty((B, D), dtype=torch.float32, device=dev)
     S_in = X0  # MoE PFFN input (an LN1 output in the model; same distribution class for timing)
     V = torch.empty((B, T, D), dtype=torch.float32, device=dev) if moe else None
@@ -199,13 +217,9 @@ def run_ours(args):
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
 
-    # max over ranks
-    t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max = max_over_ranks(ms_total, dev)
     ms_step = ms_max / args.steps
-    samples_per_s = world * B * args.steps / (ms_max / 1e3)
+    samples_per_s = job_rate(B, world, args.steps, ms_max / 1e3)
 
     # ---- e2e through the host-buffer entry point -----------------------------------
     e2e = None
@@ -221,10 +235,7 @@ def run_ours(args):
         for _ in range(args.steps):
             m.stack_forward_host(Xh, ph)
         t1 = time.perf_counter()
-        tt = torch.tensor([t1 - t0], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e = {"value": round(world * B * args.steps / float(tt.item()), 2), "unit": "samples/s",
+        e2e = {"value": round(job_rate(B, world, args.steps, max_over_ranks(t1 - t0, dev)), 2), "unit": "samples/s",
                "h2d_bytes_per_step": int(Xh.numel() * Xh.element_size()),
                "d2h_bytes_per_step": int(ph.numel() * ph.element_size())}
 

@@ -61,6 +61,29 @@ def make_input(B: int, T: int, D: int, seed: int, dtype: str = "bf16", device="c
     return _normal((B, T, D), 1.0, _gen(seed, device), device, TORCH_DTYPE[dtype])
 
 
+SHARD_BLOCK = 64
+
+
+def make_input_shard(global_B: int, start: int, stop: int, T: int, D: int, seed: int, dtype: str = "bf16",
+                     device="cpu") -> torch.Tensor:
+    """Samples [start, stop) of a seeded global batch of `global_B` inputs X0 ~ N(0, 1).
+
+    The global batch is drawn in blocks of SHARD_BLOCK samples, block j from its
+    own generator (seed, j), so a rank can draw its own shard without drawing the
+    rest, and the shards of any split concatenate to the same global batch."""
+    if not 0 <= start <= stop <= global_B:
+        raise ValueError(f"shard [{start}, {stop}) outside a batch of {global_B}")
+    parts = []
+    for j in range(start // SHARD_BLOCK, (stop + SHARD_BLOCK - 1) // SHARD_BLOCK):
+        b0 = j * SHARD_BLOCK
+        nb = min(SHARD_BLOCK, global_B - b0)
+        blk = _normal((nb, T, D), 1.0, _gen(seed * 1_000_003 + j, device), device, TORCH_DTYPE[dtype])
+        parts.append(blk[max(start - b0, 0):min(stop - b0, nb)])
+    if not parts:
+        return torch.empty((0, T, D), dtype=TORCH_DTYPE[dtype], device=device)
+    return torch.cat(parts, 0)
+
+
 def router_bias(active: float, E: int) -> float:
     """Router bias opening each expert with probability active / E (see the module docstring)."""
     p = active / E
