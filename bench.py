@@ -34,6 +34,32 @@ PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_BYTES = 129 * 1024 * 1024
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the
+# dominant kernel, from one ncu capture of this bench's own command line, keyed
+# by (config, batch per GPU, layers, kernel kind), with the SHA-256 of the
+# kernel sources the capture ran on.  Reported only while those sources are
+# unchanged; otherwise the traffic is unknown (null).
+KERNEL_SOURCES = ("rankmixer_feature_interaction_gb300/csrc/rm_gemm_tc.cu",
+                  "rankmixer_feature_interaction_gb300/csrc/rm_common.cuh",
+                  "rankmixer_feature_interaction_gb300/csrc/rm_internal.h")
+TRAFFIC = {}
+
+
+def kernel_source_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def captured_traffic(config: str, batch: int, layers: int, kind: str):
+    rec = TRAFFIC.get((config, batch, layers, kind))
+    if rec is None or rec[1] != kernel_source_digest():
+        return None
+    return rec[0]
+
 
 def load_peaks():
     try:
@@ -262,7 +288,8 @@ def run_ours(args):
         achieved = flops_launch / (avg_ms / 1e3) / 1e12
         peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
         roofline = {"kernel": f"pffn_{dom}_tcgen05", "bound": "tensor", "achieved": round(achieved, 1),
-                    "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                    "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                    "traffic": captured_traffic(args.config, B, L, dom),
                     "peak_source": f"{peak_src} bf16_tflops_sustained",
                     "avg_launch_ms": round(avg_ms, 4)}
     if not moe:

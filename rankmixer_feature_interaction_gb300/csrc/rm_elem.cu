@@ -231,6 +231,19 @@ __host__ __device__ __forceinline__ int v8_row_stride(int D, int q) { return D +
 
 __device__ __forceinline__ void f16x8_to_f32(const uint4 v, float (&o)[8]) { to_f32x8(v, false, o); }
 
+// The staged statistics rows are bulk copies: nchunk float2 must fill whole 16-byte units.
+__host__ __device__ __forceinline__ bool v8_stats_bulk(int nchunk) { return nchunk > 0 && nchunk % 2 == 0; }
+// Offset of the statistics staging area: after the two row buffers, the four
+// fp16 affines, two mbarriers, the row mean / rstd arrays and the abort flag
+// (every part a multiple of 16 bytes when q % 8 == 0 and D % 256 == 0).
+__host__ __device__ __forceinline__ size_t v8_stats_offset(int T, int D, int q) {
+    return 2 * (size_t)T * v8_row_stride(D, q) * 2 + 4 * (size_t)D * 2 + 16 + 2 * kMaxT * 4 + 16;
+}
+size_t v8_smem_bytes(bool from_z, int T, int D, int q, int nchunk) {
+    const size_t st = from_z && v8_stats_bulk(nchunk) ? 2 * (size_t)T * nchunk * 8 : 0;
+    return v8_stats_offset(T, D, q) + st;
+}
+
 template <bool FROM_Z, int NV>
 __global__ void __launch_bounds__(512)
 mix_ln1_v8_kernel(const MixLnArgs a) {
@@ -248,6 +261,10 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
     float* s_mean = reinterpret_cast<float*>(bars + 2);
     float* s_rstd = s_mean + kMaxT;
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_rstd + kMaxT);
+    // FROM_Z with an even chunk count: each sample's T rows of LN2 chunk
+    // statistics ride with its Z rows ([2][T][nchunk] float2, 16-byte aligned)
+    const bool stats_bulk = FROM_Z && v8_stats_bulk(a.nchunk);
+    float2* sst = reinterpret_cast<float2*>(smem + v8_stats_offset(T, D, q));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nwarps = blockDim.x >> 5;
     const uint16_t* src = FROM_Z ? reinterpret_cast<const uint16_t*>(a.Z) : reinterpret_cast<const uint16_t*>(a.X);
@@ -272,11 +289,18 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
     auto issue = [&](int b, int slot) {   // thread 0 only: T row copies into padded rows
         const uint32_t bar = smem_u32(&bars[slot]);
         const uint32_t dst = smem_u32(buf) + (uint32_t)slot * buf_elems * 2u;
+        const uint32_t st_bytes = stats_bulk ? (uint32_t)a.nchunk * 8u : 0u;
         fence_proxy_async_smem();
-        mbar_arrive_expect_tx(bar, (uint32_t)T * row_bytes);
+        mbar_arrive_expect_tx(bar, (uint32_t)T * (row_bytes + st_bytes));
         for (int t = 0; t < T; ++t) {
             const uint16_t* row = FROM_Z ? src + ((size_t)t * a.Bcap + b) * D : src + ((size_t)b * T + t) * D;
             bulk_copy_g2s(dst + (uint32_t)t * (uint32_t)RS * 2u, row, row_bytes, bar);
+        }
+        if (stats_bulk) {
+            const uint32_t sdst = smem_u32(sst) + (uint32_t)slot * (uint32_t)T * st_bytes;
+            for (int t = 0; t < T; ++t)
+                bulk_copy_g2s(sdst + (uint32_t)t * st_bytes, a.stats + ((size_t)t * a.Bcap + b) * a.nchunk, st_bytes,
+                              bar);
         }
     };
 
@@ -285,7 +309,7 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
     for (int b = blockIdx.x; b < a.B; b += gridDim.x, ++it) {
         const int slot = it & 1;
         if (threadIdx.x == 0 && b + (int)gridDim.x < a.B) issue(b + gridDim.x, slot ^ 1);
-        if (FROM_Z) sample_row_stats(a, b, s_mean, s_rstd, warp, nwarps, lane);
+        if (FROM_Z && !stats_bulk) sample_row_stats(a, b, s_mean, s_rstd, warp, nwarps, lane);
         mbar_wait_bounded(smem_u32(&bars[slot]), (uint32_t)(it >> 1) & 1u, s_abort, a.err, a.timeout_ns);
         __syncthreads();
         if (*s_abort) break;
@@ -293,7 +317,13 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
         if (FROM_Z) {
             // X_{n-1} = LN2(Z) in place (fp16), 8 elements per lane
             for (int t = warp; t < T; t += nwarps) {
-                const float mt = s_mean[t], rt = s_rstd[t];
+                float mt, rt;
+                if (stats_bulk) {
+                    merge_row_stats(sst + ((size_t)slot * T + t) * a.nchunk, a.nchunk, a.cw, D, a.eps, lane, mt, rt);
+                } else {
+                    mt = s_mean[t];
+                    rt = s_rstd[t];
+                }
                 uint16_t* row = xs + (size_t)t * RS;
                 for (int c = lane * 8; c < D; c += 256) {
                     float z[8], g[8], be[8];
@@ -363,19 +393,15 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
     }
 }
 
-size_t v8_smem_bytes(int T, int D, int q) {
-    return 2 * (size_t)T * v8_row_stride(D, q) * 2 + 4 * (size_t)D * 2 + 16 + 2 * kMaxT * 4 + 16;
-}
-
-bool v8_ok(const MixLnArgs& a) {
+bool v8_ok(bool from_z, const MixLnArgs& a) {
     return a.q % 8 == 0 && a.D % 256 == 0 && a.D <= 3072 && a.T <= kMaxT &&
-           v8_smem_bytes(a.T, a.D, a.q) <= 226 * 1024;
+           v8_smem_bytes(from_z, a.T, a.D, a.q, a.nchunk) <= 226 * 1024;
 }
 
 template <bool FROM_Z, int NV>
 cudaError_t launch_v8(const MixLnArgs& a, int num_sms, cudaStream_t s) {
     auto k = mix_ln1_v8_kernel<FROM_Z, NV>;
-    const size_t smem = v8_smem_bytes(a.T, a.D, a.q);
+    const size_t smem = v8_smem_bytes(FROM_Z, a.T, a.D, a.q, a.nchunk);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int threads = 32 * (a.T < 16 ? a.T : 16);
@@ -717,7 +743,7 @@ inline int grid_for(long long n, int threads, int cap = 152 * 16) {
 cudaError_t launch_mix_ln1(Act act, bool from_z, const MixLnArgs& a, int num_sms, cudaStream_t s) {
     if (a.B <= 0) return cudaSuccess;
     if (act == Act::BF16) {
-        if (v8_ok(a)) return from_z ? launch_v8_dispatch<true>(a, num_sms, s) : launch_v8_dispatch<false>(a, num_sms, s);
+        if (v8_ok(from_z, a)) return from_z ? launch_v8_dispatch<true>(a, num_sms, s) : launch_v8_dispatch<false>(a, num_sms, s);
         if (staged_ok(a))
             return from_z ? launch_staged_dispatch<__half, true>(a, num_sms, s)
                           : launch_staged_dispatch<__nv_bfloat16, false>(a, num_sms, s);

@@ -89,6 +89,7 @@ struct Args {
     int nchunk;
     const int* row_sample;    // EPI_GATED: packed row -> sample index b
     const float* gates;       // EPI_GATED: [B][T][E]
+    const int* first_e;       // EPI_GATED: [B][T] first open expert (it stores; later ones add)
     int gT, gE;
     float* v;                 // EPI_GATED: V row (b, t) at b * v_sb + t * v_st
     long long v_sb, v_st;
@@ -270,13 +271,15 @@ __device__ __forceinline__ void epilogue_tile(const Args& args, const TileCoord&
             const int chunk = n0 / COLS;
             args.stats[(size_t)arow * args.nchunk + chunk] = make_float2(mean, m2);
         }
-    } else {  // EPI_GATED: V[b, t] += gate * (acc + b2)
+    } else {  // EPI_GATED: V[b, t] (+)= gate * (acc + b2); the first open expert of (b, t) stores
         float gate = 0.f;
         float* vrow = nullptr;
+        bool first = true;
         if (valid) {
             const int b = __ldg(args.row_sample + arow);
             const int t = tc.wg / args.gE, e = tc.wg - t * args.gE;
             gate = __ldg(args.gates + ((size_t)b * args.gT + t) * args.gE + e);
+            first = __ldg(args.first_e + (size_t)b * args.gT + t) == e;
             vrow = args.v + (size_t)b * args.v_sb + (size_t)t * args.v_st + n0;
         }
 #pragma unroll 1
@@ -289,7 +292,7 @@ __device__ __forceinline__ void epilogue_tile(const Args& args, const TileCoord&
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const float4 bb = __ldg(b4 + j);
-                    float4 o = dst[j];
+                    float4 o = first ? make_float4(0.f, 0.f, 0.f, 0.f) : dst[j];
                     o.x = fmaf(gate, v[4 * j] + bb.x, o.x);
                     o.y = fmaf(gate, v[4 * j + 1] + bb.y, o.y);
                     o.z = fmaf(gate, v[4 * j + 2] + bb.z, o.z);
@@ -940,8 +943,9 @@ cudaError_t launch_moe_gemm1_tc(const void* Sg, long long rows_total, const void
 
 cudaError_t launch_moe_gemm2_tc(const void* Hm, long long rows_total, const void* W2p, const float* b2, int T, int E,
                                 int e, int D, int Fe, const int* g_count, const int* g_off, const int* tile_prefix_e,
-                                const int* row_sample, const float* gates, float* V, long long v_sb, long long v_st,
-                                int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s) {
+                                const int* row_sample, const float* gates, const int* first_e, float* V,
+                                long long v_sb, long long v_st, int num_sms, int* err, unsigned long long timeout_ns,
+                                cudaStream_t s) {
     tc::Args a{};
     a.N = D;
     a.K = Fe;
@@ -954,6 +958,7 @@ cudaError_t launch_moe_gemm2_tc(const void* Hm, long long rows_total, const void
     a.bias = b2;
     a.row_sample = row_sample;
     a.gates = gates;
+    a.first_e = first_e;
     a.gT = T;
     a.gE = E;
     a.v = V;

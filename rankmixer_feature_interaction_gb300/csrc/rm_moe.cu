@@ -8,15 +8,16 @@
 // zero and are skipped.
 //
 // Pipeline (all on the launch stream, no host synchronisation):
-//   1 router      one warp per (b, t): G = ReLU(s Wg_t + bg_t)
-//   2 count       one CTA per (t, e): number of samples with G > 0
-//   3 prefix      one thread: row offsets, 128-row tile prefixes per launch
-//   4 fill        one CTA per (t, e): ascending list of the active samples
-//   5 gather      packed rows Sg[off(t,e) + i] = S[b_i, t]   (fp16 operands for bf16 contexts)
-//   6 expert L1   variable-size grouped GEMM + bias + GELU -> Hm (packed rows)
-//   7 expert L2   one launch per expert index e (fixed order e = 0..E-1):
-//                 V[b, t] += G * (Hm W2_{t,e} + b2_{t,e})
-// The fixed order of step 7 makes the float32 sum over experts deterministic.
+//   1 route       one pass over S: G = ReLU(s Wg_t + bg_t); each open (b, t, e)
+//                 claims a slot of group t E + e and copies s into it (fp16
+//                 operands for bf16 contexts); V rows with no open expert are zeroed
+//   2 tiles       128-row tile prefix sums per launch
+//   3 expert L1   variable-size grouped GEMM + bias + GELU -> Hm (packed rows)
+//   4 expert L2   one launch per expert index e (fixed order e = 0..E-1):
+//                 V[b, t] (+)= G * (Hm W2_{t,e} + b2_{t,e}), the first open
+//                 expert of (b, t) storing and the later ones adding
+// The fixed order of step 4 makes the float32 sum over experts deterministic.
+#include <type_traits>
 #include <vector>
 
 #include "rm_common.cuh"
@@ -32,64 +33,214 @@ cudaError_t launch_moe_gemm1_tc(const void* Sg, long long rows_total, const void
                                 cudaStream_t s);
 cudaError_t launch_moe_gemm2_tc(const void* Hm, long long rows_total, const void* W2p, const float* b2, int T, int E,
                                 int e, int D, int Fe, const int* g_count, const int* g_off, const int* tile_prefix_e,
-                                const int* row_sample, const float* gates, float* V, long long v_sb, long long v_st,
-                                int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s);
+                                const int* row_sample, const float* gates, const int* first_e, float* V,
+                                long long v_sb, long long v_st, int num_sms, int* err, unsigned long long timeout_ns,
+                                cudaStream_t s);
 
 namespace {
 
 constexpr unsigned long long kMoeWaitTimeoutNs = 2000000000ull;
 
-// ---- 1: router -------------------------------------------------------------------
-template <typename Tact>
-__global__ void router_kernel(const Tact* __restrict__ S, long long s_sb, long long s_st, const float* __restrict__ Wg,
-                              const float* __restrict__ bg, float* __restrict__ gates, int B, int T, int D, int E) {
-    const int lane = threadIdx.x & 31;
-    const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
-    for (long long r = wid; r < (long long)B * T; r += nw) {
-        const int b = (int)(r / T), t = (int)(r % T);
-        const Tact* s = S + b * s_sb + t * s_st;
-        for (int e = 0; e < E; ++e) {
-            const float* w = Wg + ((size_t)t * E + e) * D;
-            float acc = 0.f;
-            for (int j = lane; j < D; j += 32) acc = fmaf(to_f32(s[j]), w[j], acc);
-            acc = warp_sum(acc);
-            if (lane == 0) gates[((size_t)b * T + t) * E + e] = fmaxf(acc + bg[(size_t)t * E + e], 0.f);
+// ---- 1: route (gates, slot claim, gather) ------------------------------------------
+// One warp takes RQ = 4 samples of one token t at a time.  Each lane walks its
+// columns of the 4 rows in chunks of CH elements (16-byte loads when the rows
+// allow), and accumulates the 4 x 8 partial dot products with an 8-expert slice
+// of Wg_t (fp32, read through L1: every warp of the CTA works on the same
+// token).  A transpose-reduction (31 shuffles) leaves lane l holding the full
+// sum for row l / 8 and expert l % 8 of the slice.  Each open (row, expert)
+// claims a slot of its group g = t E + e by an atomic on counts[g]; the slot's
+// packed row is g Bcap + slot, so the gathered rows of group g are the first
+// counts[g] rows of its fixed Bcap-row block.  The warp then copies each open
+// row into its slot, converted to the operand type.  A (sample, token) with
+// no open expert gets its V row zeroed here (the expert layer-2 launches write
+// the rows of the others; the first open expert stores, later ones add).
+//
+// The order of rows inside a group follows the atomics and may change from
+// run to run; no value does: each output row's arithmetic is independent of
+// its position in a tile, and the experts are combined in a fixed order.
+constexpr int kRouteRows = 4;       // samples per warp pass
+constexpr int kRouteExp = 8;        // experts per pass (kRouteRows * kRouteExp == 32)
+constexpr int kRouteWarps = 8;
+constexpr int kRouteSamplesPerCta = 128;
+
+template <typename Tin, int CH>
+__device__ __forceinline__ void load_chunk(const Tin* p, bool ok, float (&x)[CH]) {
+    if constexpr (CH == 1) {
+        x[0] = ok ? to_f32(p[0]) : 0.f;
+    } else if constexpr (sizeof(Tin) == 4) {
+        static_assert(CH == 4, "16-byte chunk of fp32");
+        const float4 v = ok ? __ldg(reinterpret_cast<const float4*>(p)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+    } else {
+        static_assert(CH == 8, "16-byte chunk of 16-bit values");
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (ok) v = __ldg(reinterpret_cast<const uint4*>(p));
+        const Tin* h = reinterpret_cast<const Tin*>(&v);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] = to_f32(h[k]);
+    }
+}
+
+// CH consecutive floats (16-byte loads when CH is a multiple of 4)
+template <int CH>
+__device__ __forceinline__ void load_wf(const float* p, float (&w)[CH]) {
+    if constexpr (CH % 4 == 0) {
+#pragma unroll
+        for (int q = 0; q < CH / 4; ++q) {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(p) + q);
+            w[4 * q] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < CH; ++k) w[k] = __ldg(p + k);
+    }
+}
+
+template <typename Tin, typename Tout, int CH>
+__device__ __forceinline__ void copy_row(const Tin* __restrict__ src, Tout* __restrict__ dst, int D, int lane) {
+    for (int c0 = CH * lane; c0 < D; c0 += 32 * CH) {
+        float x[CH];
+        load_chunk<Tin, CH>(src + c0, true, x);
+        if constexpr (CH == 8 && std::is_same_v<Tout, __half>) {
+            uint4 o;
+            uint32_t* w = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) w[k] = pack_f16x2(x[2 * k], x[2 * k + 1]);
+            *reinterpret_cast<uint4*>(dst + c0) = o;
+        } else if constexpr (CH == 4 && sizeof(Tout) == 4) {
+            *reinterpret_cast<float4*>(dst + c0) = make_float4(x[0], x[1], x[2], x[3]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < CH; ++k) dst[c0 + k] = from_f32<Tout>(x[k]);
         }
     }
 }
 
-// ---- 2: per-(t, e) active count -------------------------------------------------
-__global__ void count_kernel(const float* __restrict__ gates, int* __restrict__ counts, int B, int T, int E) {
-    __shared__ int s_cnt;
-    const int g = blockIdx.x;
-    const int t = g / E, e = g % E;
-    if (threadIdx.x == 0) s_cnt = 0;
-    __syncthreads();
-    int c = 0;
-    for (int b = threadIdx.x; b < B; b += blockDim.x) c += gates[((size_t)b * T + t) * E + e] > 0.f;
-    atomicAdd(&s_cnt, c);
-    __syncthreads();
-    if (threadIdx.x == 0) counts[g] = s_cnt;
+template <typename Tin, typename Tout, int CH>
+__global__ void __launch_bounds__(kRouteWarps * 32)
+route_kernel(const Tin* __restrict__ S, long long s_sb, long long s_st, const float* __restrict__ Wg,
+             const float* __restrict__ bg, float* __restrict__ gates, int* __restrict__ counts,
+             int* __restrict__ rows, int* __restrict__ first_e, Tout* __restrict__ Sg, float* __restrict__ V,
+             long long v_sb, long long v_st, int B, int T, int D, int E, int Bcap) {
+    const int t = blockIdx.y;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int my_r = lane / kRouteExp, my_e = lane % kRouteExp;
+    const int b_end = min(B, (int)(blockIdx.x + 1) * kRouteSamplesPerCta);
+    for (int b0 = blockIdx.x * kRouteSamplesPerCta + warp * kRouteRows; b0 < b_end; b0 += kRouteWarps * kRouteRows) {
+        const Tin* row[kRouteRows];
+        bool ok[kRouteRows];
+#pragma unroll
+        for (int r = 0; r < kRouteRows; ++r) {
+            ok[r] = b0 + r < b_end;
+            row[r] = S + (long long)(ok[r] ? b0 + r : b0) * s_sb + (long long)t * s_st;
+        }
+        int first = E;                               // first open expert of this lane's row (my_r)
+        for (int e0 = 0; e0 < E; e0 += kRouteExp) {
+            const int ne = min(kRouteExp, E - e0);
+            float acc[kRouteRows * kRouteExp];
+#pragma unroll
+            for (int i = 0; i < kRouteRows * kRouteExp; ++i) acc[i] = 0.f;
+            const float* wt = Wg + ((size_t)t * E + e0) * D;
+            for (int c0 = CH * lane; c0 < D; c0 += 32 * CH) {
+                float x[kRouteRows][CH];
+#pragma unroll
+                for (int r = 0; r < kRouteRows; ++r) load_chunk<Tin, CH>(row[r] + c0, ok[r], x[r]);
+#pragma unroll
+                for (int e = 0; e < kRouteExp; ++e) {
+                    if (e < ne) {
+                        float w[CH];
+                        load_wf<CH>(wt + (size_t)e * D + c0, w);
+#pragma unroll
+                        for (int r = 0; r < kRouteRows; ++r)
+#pragma unroll
+                            for (int k = 0; k < CH; ++k) acc[r * kRouteExp + e] = fmaf(x[r][k], w[k], acc[r * kRouteExp + e]);
+                    }
+                }
+            }
+            // transpose-reduction: after the step with offset o, a lane keeps the half of
+            // the remaining values selected by its bit o; lane l ends with value l's sum
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                const bool upper = (lane & o) != 0;
+#pragma unroll
+                for (int i = 0; i < o; ++i) {
+                    const float send = upper ? acc[i] : acc[i + o];
+                    const float keep = upper ? acc[i + o] : acc[i];
+                    acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+            }
+            const int b = b0 + my_r, e = e0 + my_e;
+            const bool mine = my_e < ne && ok[my_r];
+            const float g = mine ? fmaxf(acc[0] + __ldg(bg + (size_t)t * E + e), 0.f) : 0.f;
+            if (mine) gates[((size_t)b * T + t) * E + e] = g;
+            const bool open = mine && g > 0.f;
+            int slot = 0;
+            if (open) {
+                const int grp = t * E + e;
+                slot = atomicAdd(counts + grp, 1);
+                rows[(size_t)grp * Bcap + slot] = b;
+            }
+            unsigned m = __ballot_sync(0xffffffffu, open);
+            const unsigned row_bits = (m >> (my_r * kRouteExp)) & ((1u << kRouteExp) - 1u);
+            if (first == E && row_bits) first = e0 + __ffs(row_bits) - 1;
+            while (m) {
+                const int l = __ffs(m) - 1;
+                m &= m - 1;
+                const int sl = __shfl_sync(0xffffffffu, slot, l);
+                const int r = l / kRouteExp;
+                const int grp = t * E + e0 + l % kRouteExp;
+                copy_row<Tin, Tout, CH>(S + (long long)(b0 + r) * s_sb + (long long)t * s_st,
+                                        Sg + ((size_t)grp * Bcap + sl) * D, D, lane);
+            }
+        }
+        if (my_e == 0 && ok[my_r]) first_e[(size_t)(b0 + my_r) * T + t] = first;
+        // V rows of samples with no open expert are zero
+        const unsigned closed_rows = __ballot_sync(0xffffffffu, my_e == 0 && first == E);
+#pragma unroll
+        for (int r = 0; r < kRouteRows; ++r) {
+            if (ok[r] && (closed_rows >> (r * kRouteExp)) & 1u) {
+                float* vrow = V + (long long)(b0 + r) * v_sb + (long long)t * v_st;
+                for (int c = lane; c < D; c += 32) vrow[c] = 0.f;
+            }
+        }
+    }
 }
 
-// ---- 3: offsets and tile prefixes ---------------------------------------------------
-// offsets[g] over g = t E + e; tile_prefix[0 .. G] over the same order (expert layer 1);
-// tile_prefix[G + 1 + e (T + 1) + t] over t for fixed e (expert layer 2, one launch per e).
-__global__ void prefix_kernel(const int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ tile_prefix,
-                              int T, int E) {
-    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+// ---- 2: tile prefixes -------------------------------------------------------------
+// offsets[g] = g Bcap (fixed blocks); tile_prefix[0 .. G] over g = t E + e (expert
+// layer 1); tile_prefix[G + 1 + e (T + 1) + t] over t for fixed e (layer 2, one
+// launch per e).  One CTA, each thread a contiguous run of groups.
+constexpr int kTilesThreads = 1024;
+
+__global__ void __launch_bounds__(kTilesThreads)
+tiles_kernel(const int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ tile_prefix, int T, int E,
+             int Bcap) {
+    __shared__ int part[kTilesThreads];
     const int G = T * E;
-    int off = 0, tp = 0;
-    for (int g = 0; g < G; ++g) {
-        offsets[g] = off;
-        tile_prefix[g] = tp;
-        off += counts[g];
-        tp += (counts[g] + 127) / 128;
+    const int per = (G + kTilesThreads - 1) / kTilesThreads;
+    const int g0 = threadIdx.x * per, g1 = min(G, g0 + per);
+    int sum = 0;
+    for (int g = g0; g < g1; ++g) sum += (counts[g] + 127) / 128;
+    part[threadIdx.x] = sum;
+    __syncthreads();
+    // inclusive scan of the per-thread sums (Hillis-Steele)
+    for (int o = 1; o < kTilesThreads; o <<= 1) {
+        const int v = threadIdx.x >= o ? part[threadIdx.x - o] : 0;
+        __syncthreads();
+        part[threadIdx.x] += v;
+        __syncthreads();
     }
-    offsets[G] = off;
-    tile_prefix[G] = tp;
-    for (int e = 0; e < E; ++e) {
+    int run = part[threadIdx.x] - sum;
+    for (int g = g0; g < g1; ++g) {
+        offsets[g] = g * Bcap;
+        tile_prefix[g] = run;
+        run += (counts[g] + 127) / 128;
+    }
+    if (threadIdx.x == kTilesThreads - 1) {
+        tile_prefix[G] = part[kTilesThreads - 1];
+        offsets[G] = G * Bcap;
+    }
+    for (int e = threadIdx.x; e < E; e += kTilesThreads) {
         int* p = tile_prefix + G + 1 + e * (T + 1);
         int acc = 0;
         for (int t = 0; t < T; ++t) {
@@ -97,54 +248,6 @@ __global__ void prefix_kernel(const int* __restrict__ counts, int* __restrict__ 
             acc += (counts[t * E + e] + 127) / 128;
         }
         p[T] = acc;
-    }
-}
-
-// ---- 4: ordered compaction -------------------------------------------------------
-__global__ void __launch_bounds__(256) fill_kernel(const float* __restrict__ gates, const int* __restrict__ offsets,
-                                                   int* __restrict__ rows, int B, int T, int E) {
-    __shared__ int s_warp[8];
-    __shared__ int s_base;
-    const int g = blockIdx.x;
-    const int t = g / E, e = g % E;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (threadIdx.x == 0) s_base = 0;
-    __syncthreads();
-    int* out = rows + offsets[g];
-    for (int b0 = 0; b0 < B; b0 += 256) {
-        const int b = b0 + threadIdx.x;
-        const bool on = b < B && gates[((size_t)b * T + t) * E + e] > 0.f;
-        const unsigned m = __ballot_sync(0xffffffffu, on);
-        if (lane == 0) s_warp[warp] = __popc(m);
-        __syncthreads();
-        int before = s_base;
-        for (int w = 0; w < warp; ++w) before += s_warp[w];
-        if (on) out[before + __popc(m & ((1u << lane) - 1u))] = b;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            int tot = 0;
-            for (int w = 0; w < 8; ++w) tot += s_warp[w];
-            s_base += tot;
-        }
-        __syncthreads();
-    }
-}
-
-// ---- 5: gather active rows ------------------------------------------------------------
-template <typename Ein, typename Eout>
-__global__ void gather_kernel(const Ein* __restrict__ S, long long s_sb, long long s_st,
-                              const int* __restrict__ counts, const int* __restrict__ offsets,
-                              const int* __restrict__ rows, Eout* __restrict__ Sg, int D, int NE) {
-    const int g = blockIdx.y;
-    const int t = g / NE;
-    const int cnt = counts[g], off = offsets[g];
-    const int lane = threadIdx.x & 31;
-    const int wpb = blockDim.x >> 5;
-    for (int i = blockIdx.x * wpb + (threadIdx.x >> 5); i < cnt; i += gridDim.x * wpb) {
-        const int b = rows[off + i];
-        const Ein* src = S + b * s_sb + t * s_st;
-        Eout* dst = Sg + (size_t)(off + i) * D;
-        for (int j = lane; j < D; j += 32) dst[j] = from_f32<Eout>(to_f32(src[j]));
     }
 }
 
@@ -157,7 +260,8 @@ template <typename Tin, int EPI>
 __global__ void __launch_bounds__(256)
 moe_gemm_simt_kernel(const Tin* __restrict__ A, const Tin* __restrict__ W, const float* __restrict__ bias,
                      Tin* __restrict__ hout, const int* __restrict__ counts, const int* __restrict__ offsets,
-                     const int* __restrict__ rows, const float* __restrict__ gates, float* __restrict__ V,
+                     const int* __restrict__ rows, const float* __restrict__ gates, const int* __restrict__ first_e,
+                     float* __restrict__ V,
                      long long v_sb, long long v_st, int N, int K, int T, int NE, int base, int stride) {
     __shared__ float As[TK][TM + 4];
     __shared__ float Ws[TK][TN + 4];
@@ -213,11 +317,12 @@ moe_gemm_simt_kernel(const Tin* __restrict__ A, const Tin* __restrict__ W, const
         } else {
             const int b = rows[row0 + m];
             const float gate = gates[((size_t)b * T + t) * NE + ee];
+            const bool first = first_e[(size_t)b * T + t] == ee;   // the first open expert stores
             float* vrow = V + b * v_sb + t * v_st;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int n = n0 + tx + 16 * j;
-                if (n < N) vrow[n] = fmaf(gate, acc[i][j] + bias[(size_t)wg * N + n], vrow[n]);
+                if (n < N) vrow[n] = fmaf(gate, acc[i][j] + bias[(size_t)wg * N + n], first ? 0.f : vrow[n]);
             }
         }
     }
@@ -306,6 +411,7 @@ cudaError_t moe_alloc_workspace(const MoeShape& ms, int Bcap, MoeWorkspace& ws, 
     if ((e = dalloc(&ws.offsets, G + 1, bytes)) != cudaSuccess) return e;
     if ((e = dalloc(&ws.rows, G * Bcap, bytes)) != cudaSuccess) return e;
     if ((e = dalloc(&ws.tile_prefix, G + 1 + (size_t)ms.E * (ms.T + 1), bytes)) != cudaSuccess) return e;
+    if ((e = dalloc(&ws.first_e, (size_t)Bcap * ms.T, bytes)) != cudaSuccess) return e;
     if ((e = dalloc_bytes(&ws.Sg, G * Bcap * ms.D * esz, bytes)) != cudaSuccess) return e;
     if ((e = dalloc_bytes(&ws.Hm, G * Bcap * ms.Fe * esz, bytes)) != cudaSuccess) return e;
     return cudaSuccess;
@@ -313,7 +419,7 @@ cudaError_t moe_alloc_workspace(const MoeShape& ms, int Bcap, MoeWorkspace& ws, 
 
 void moe_free_workspace(MoeWorkspace& ws) {
     cudaFree(ws.gates); cudaFree(ws.counts); cudaFree(ws.offsets); cudaFree(ws.rows); cudaFree(ws.tile_prefix);
-    cudaFree(ws.pair_of_row); cudaFree(ws.Sg); cudaFree(ws.Hm);
+    cudaFree(ws.first_e); cudaFree(ws.Sg); cudaFree(ws.Hm);
     ws = MoeWorkspace{};
 }
 
@@ -334,47 +440,34 @@ cudaError_t moe_forward(const MoeLaunch& ml, const MoeWeights& w, MoeWorkspace& 
         prof_end(h);
         return r;
     };
-    // 1-5: route, compact, gather
+    // 1-2: route (gates, slots, gather, zero rows), tile prefixes
     e = scoped(6 /* RM_K_MOE_ROUTE */, [&]() -> cudaError_t {
-        const long long warps = (long long)B * T;
-        int grid = (int)((warps * 32 + 255) / 256);
-        if (grid > ml.num_sms * 16) grid = ml.num_sms * 16;
-        if (ml.act == Act::F32)
-            router_kernel<float><<<grid, 256, 0, s>>>((const float*)ml.S, s_sb, s_st, w.Wg, w.bg, ws.gates, B, T, D, E);
-        else if (ml.S_sample_major)   // the caller's bf16 S
-            router_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16*)ml.S, s_sb, s_st, w.Wg, w.bg,
-                                                               ws.gates, B, T, D, E);
-        else                          // the stack's fp16 S
-            router_kernel<__half><<<grid, 256, 0, s>>>((const __half*)ml.S, s_sb, s_st, w.Wg, w.bg, ws.gates, B, T, D,
-                                                        E);
-        count_kernel<<<G, 256, 0, s>>>(ws.gates, ws.counts, B, T, E);
-        prefix_kernel<<<1, 32, 0, s>>>(ws.counts, ws.offsets, ws.tile_prefix, T, E);
-        fill_kernel<<<G, 256, 0, s>>>(ws.gates, ws.offsets, ws.rows, B, T, E);
-        dim3 gg((B + 7) / 8 < 64 ? (B + 7) / 8 : 64, G);
-        if (ml.act == Act::F32)
-            gather_kernel<float, float><<<gg, 256, 0, s>>>((const float*)ml.S, s_sb, s_st, ws.counts, ws.offsets,
-                                                           ws.rows, (float*)ws.Sg, D, E);
-        else if (ml.S_sample_major)
-            gather_kernel<__nv_bfloat16, __half><<<gg, 256, 0, s>>>((const __nv_bfloat16*)ml.S, s_sb, s_st,
-                                                                     ws.counts, ws.offsets, ws.rows, (__half*)ws.Sg,
-                                                                     D, E);
-        else
-            gather_kernel<__half, __half><<<gg, 256, 0, s>>>((const __half*)ml.S, s_sb, s_st, ws.counts, ws.offsets,
-                                                             ws.rows, (__half*)ws.Sg, D, E);
+        cudaError_t r = cudaMemsetAsync(ws.counts, 0, (size_t)G * sizeof(int), s);
+        if (r != cudaSuccess) return r;
+        const dim3 grid((B + kRouteSamplesPerCta - 1) / kRouteSamplesPerCta, T);
+        const int esz = ml.act == Act::F32 ? 4 : 2;
+        const bool vec = ((uintptr_t)ml.S % 16 == 0) && (D % (16 / esz) == 0) && (s_sb * esz % 16 == 0) &&
+                         (s_st * esz % 16 == 0);
+#define RM_ROUTE(TIN, TOUT, CH)                                                                               \
+    route_kernel<TIN, TOUT, CH><<<grid, kRouteWarps * 32, 0, s>>>((const TIN*)ml.S, s_sb, s_st, w.Wg, w.bg,    \
+                                                                   ws.gates, ws.counts, ws.rows, ws.first_e,   \
+                                                                   (TOUT*)ws.Sg,                               \
+                                                                   V, v_sb, v_st, B, T, D, E, ws.Bcap)
+        if (ml.act == Act::F32) {
+            if (vec) RM_ROUTE(float, float, 4); else RM_ROUTE(float, float, 1);
+        } else if (ml.S_sample_major) {   // the caller's bf16 S
+            if (vec) RM_ROUTE(__nv_bfloat16, __half, 8); else RM_ROUTE(__nv_bfloat16, __half, 1);
+        } else {                          // the stack's fp16 S
+            if (vec) RM_ROUTE(__half, __half, 8); else RM_ROUTE(__half, __half, 1);
+        }
+#undef RM_ROUTE
+        tiles_kernel<<<1, kTilesThreads, 0, s>>>(ws.counts, ws.offsets, ws.tile_prefix, T, E, ws.Bcap);
         if (gates_out) {
-            cudaError_t r = cudaMemcpyAsync(gates_out, ws.gates, (size_t)B * G * sizeof(float),
-                                            cudaMemcpyDeviceToDevice, s);
+            r = cudaMemcpyAsync(gates_out, ws.gates, (size_t)B * G * sizeof(float), cudaMemcpyDeviceToDevice, s);
             if (r != cudaSuccess) return r;
         }
         return cudaGetLastError();
     });
-    if (e != cudaSuccess) return e;
-
-    // V = 0 on the B rows of every token
-    if (V_token_major)
-        e = cudaMemset2DAsync(V, (size_t)ml.Bcap * D * sizeof(float), 0, (size_t)B * D * sizeof(float), T, s);
-    else
-        e = cudaMemsetAsync(V, 0, (size_t)B * T * D * sizeof(float), s);
     if (e != cudaSuccess) return e;
 
     const bool tc = moe_use_tc(ml.act, D, Fe);
@@ -387,11 +480,11 @@ cudaError_t moe_forward(const MoeLaunch& ml, const MoeWeights& w, MoeWorkspace& 
         if (ml.act == Act::BF16)
             moe_gemm_simt_kernel<__half, 1><<<grid, 256, 0, s>>>((const __half*)ws.Sg, (const __half*)w.W1p, w.b1,
                                                                  (__half*)ws.Hm, ws.counts, ws.offsets, ws.rows,
-                                                                 nullptr, nullptr, 0, 0, Fe, D, T, E, 0, 1);
+                                                                 nullptr, nullptr, nullptr, 0, 0, Fe, D, T, E, 0, 1);
         else
             moe_gemm_simt_kernel<float, 1><<<grid, 256, 0, s>>>((const float*)ws.Sg, (const float*)w.W1p, w.b1,
                                                                 (float*)ws.Hm, ws.counts, ws.offsets, ws.rows, nullptr,
-                                                                nullptr, 0, 0, Fe, D, T, E, 0, 1);
+                                                                nullptr, nullptr, 0, 0, Fe, D, T, E, 0, 1);
         return cudaGetLastError();
     });
     if (e != cudaSuccess) return e;
@@ -402,17 +495,18 @@ cudaError_t moe_forward(const MoeLaunch& ml, const MoeWeights& w, MoeWorkspace& 
             const int* tp = ws.tile_prefix + G + 1 + ei * (T + 1);
             if (tc)
                 return launch_moe_gemm2_tc(ws.Hm, rows_cap, w.W2p, w.b2, T, E, ei, D, Fe, ws.counts, ws.offsets, tp,
-                                           ws.rows, ws.gates, V, v_sb, v_st, ml.num_sms, ml.err, kMoeWaitTimeoutNs,
-                                           s);
+                                           ws.rows, ws.gates, ws.first_e, V, v_sb, v_st, ml.num_sms, ml.err,
+                                           kMoeWaitTimeoutNs, s);
             dim3 grid((D + TN - 1) / TN, (B + TM - 1) / TM, T);
             if (ml.act == Act::BF16)
                 moe_gemm_simt_kernel<__half, 2><<<grid, 256, 0, s>>>((const __half*)ws.Hm, (const __half*)w.W2p, w.b2,
                                                                      nullptr, ws.counts, ws.offsets, ws.rows,
-                                                                     ws.gates, V, v_sb, v_st, D, Fe, T, E, ei, E);
+                                                                     ws.gates, ws.first_e, V, v_sb, v_st, D, Fe, T, E,
+                                                                     ei, E);
             else
                 moe_gemm_simt_kernel<float, 2><<<grid, 256, 0, s>>>((const float*)ws.Hm, (const float*)w.W2p, w.b2,
                                                                     nullptr, ws.counts, ws.offsets, ws.rows, ws.gates,
-                                                                    V, v_sb, v_st, D, Fe, T, E, ei, E);
+                                                                    ws.first_e, V, v_sb, v_st, D, Fe, T, E, ei, E);
             return cudaGetLastError();
         });
         if (e != cudaSuccess) return e;

@@ -34,11 +34,11 @@ struct MoeWeights {
 struct MoeWorkspace {
     int Bcap = 0;
     float* gates = nullptr;     // [B][T][E]
-    int* counts = nullptr;      // [T*E]
-    int* offsets = nullptr;     // [T*E + 1] exclusive prefix of counts (row offsets)
-    int* rows = nullptr;        // [T*E][Bcap] sample index of each gathered row, ascending
-    int* tile_prefix = nullptr; // [T*E + 1] exclusive prefix of 128-row tiles per group
-    int* pair_of_row = nullptr; // [T*E*Bcap] packed row -> group id (t*E + e)
+    int* counts = nullptr;      // [T*E] open samples per group g = t*E + e
+    int* offsets = nullptr;     // [T*E + 1] first packed row of each group: g * Bcap
+    int* rows = nullptr;        // [T*E][Bcap] sample index of each gathered row (first counts[g] used)
+    int* tile_prefix = nullptr; // [T*E + 1 + E*(T + 1)] exclusive prefixes of 128-row tiles per launch
+    int* first_e = nullptr;     // [Bcap][T] first open expert of (b, t) (E when none)
     void* Sg = nullptr;         // [T*E*Bcap][D]  gathered LN1 rows (operand type)
     void* Hm = nullptr;         // [T*E*Bcap][Fe] expert hidden activations (operand type)
 };

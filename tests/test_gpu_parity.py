@@ -311,6 +311,42 @@ def test_moe_pffn_small(dtype, path, T, D, E, Fe, B):
     check(V, V_ref, dtype, "MoE V")
 
 
+@pytest.mark.parametrize("dtype,T,D,E,Fe,B", [("bf16", 2, 128, 12, 128, 131),    # two 8-expert router slices
+                                               ("bf16", 4, 36, 4, 64, 37),       # rows not in 16-byte chunks
+                                               ("f32", 2, 8, 9, 16, 50)])        # fp32, E > 8, B % 4 != 0
+def test_moe_router_shapes_and_determinism(dtype, T, D, E, Fe, B):
+    m, layers, _ = _build(T, D, 2, 1, B, 90 + D + E, dtype, E=E, Fe=Fe, active=E / 4)
+    S = synth.make_input(B, T, D, 91, dtype, DEV)
+    V1 = torch.full(S.shape, float("nan"), dtype=torch.float32, device=DEV)   # every row must be written
+    V1, G = m.moe_pffn_forward(0, S, V1, return_gates=True)
+    V2 = torch.full(S.shape, float("nan"), dtype=torch.float32, device=DEV)
+    V2 = m.moe_pffn_forward(0, S, V2)
+    torch.cuda.synchronize()
+    assert m.sync_status() == _lib.RM_OK
+    p64 = synth.to_f64(layers[0])
+    V_ref, G_ref = _moe_oracle(_np(S), p64)
+    np.testing.assert_allclose(_np(G), G_ref, atol=2e-4 if dtype == "bf16" else 1e-5, rtol=1e-3)
+    check(V1, V_ref, dtype, f"MoE V (E={E}, D={D})")
+    # rows inside an expert group may be ordered differently from run to run; the values may not
+    assert torch.equal(V1, V2), "MoE PFFN is not deterministic"
+    closed = (G_ref > 0).sum(-1) == 0
+    assert closed.any(), "the case should have (sample, token) pairs with every expert closed"
+    assert (V1[torch.from_numpy(closed).to(DEV)] == 0).all()
+
+
+def test_moe_all_experts_closed_gives_exact_zero():
+    T, D, E, Fe, B = 4, 256, 4, 256, 70
+    layers = synth.make_stack(T, D, 2, 1, 93, "bf16", DEV, E=E, Fe=Fe)
+    layers[0]["bg"] = torch.full_like(layers[0]["bg"], -1e3)     # ReLU closes every gate
+    m = RankMixer(T, D, 2, layers, max_batch=B, n_experts=E, expert_hidden=Fe)
+    S = synth.make_input(B, T, D, 94, "bf16", DEV)
+    V = torch.full(S.shape, float("nan"), dtype=torch.float32, device=DEV)
+    V, G = m.moe_pffn_forward(0, S, V, return_gates=True)
+    torch.cuda.synchronize()
+    assert m.sync_status() == _lib.RM_OK
+    assert (G == 0).all() and (V == 0).all()
+
+
 def test_moe_layer_inside_block():
     T, D, E, Fe, B = 4, 256, 4, 256, 200
     m, layers, X = _build(T, D, 2, 2, B, 71, "bf16", E=E, Fe=Fe, moe_mask=0b10, active=1.0)
