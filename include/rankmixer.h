@@ -246,8 +246,10 @@ RM_API rm_status rm_debug_wait_timeout(rm_ctx *ctx, int timeout_us, void *stream
 /* Test hook: out[i] = the GELU the library's GEMM epilogues apply, for n
  * float32 device values (u * Phi(u), "RankMixer 详解（1）" section 4.1, with
  * erf from Abramowitz & Stegun formula 7.1.26, |error in erf| <= 1.5e-7).
- * Asynchronous on `stream`. */
-RM_API rm_status rm_debug_gelu(const float *u, float *out, long long n, void *stream);
+ * form 0: the scalar form of the CUDA-core GEMMs; form 1: the packed-pair
+ * (fp32x2) form of the tensor-core GEMM epilogues.  Asynchronous on `stream`;
+ * RM_ERR_INVALID_ARG for n < 0, NULL buffers or another form. */
+RM_API rm_status rm_debug_gelu(const float *u, float *out, long long n, int form, void *stream);
 
 /* Message of the last failing call on this host thread ("" if none). */
 RM_API const char *rm_last_error(void);

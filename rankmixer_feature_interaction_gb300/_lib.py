@@ -100,7 +100,7 @@ def load() -> ctypes.CDLL:
         "rm_last_error": (ctypes.c_char_p, []),
         "rm_abi_version": (i, []),
         "rm_block_forward_noalloc": (st, [vp, i, vp, vp, i, vp]),
-        "rm_debug_gelu": (st, [vp, vp, ctypes.c_longlong, vp]),
+        "rm_debug_gelu": (st, [vp, vp, ctypes.c_longlong, ctypes.c_int, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -178,8 +178,8 @@ def rm_debug_wait_timeout(ctx: int, timeout_us: int, stream: int) -> None:
     check(load().rm_debug_wait_timeout(ctx, timeout_us, stream), "rm_debug_wait_timeout")
 
 
-def rm_debug_gelu(u: int, out: int, n: int, stream: int) -> None:
-    check(load().rm_debug_gelu(u, out, n, stream), "rm_debug_gelu")
+def rm_debug_gelu(u: int, out: int, n: int, form: int, stream: int) -> None:
+    check(load().rm_debug_gelu(u, out, n, form, stream), "rm_debug_gelu")
 
 
 def rm_last_error() -> str:

@@ -584,10 +584,11 @@ rm_status rm_profile_read(rm_ctx* c, rm_kernel_stat* stats) {
     return RM_OK;
 }
 
-rm_status rm_debug_gelu(const float* u, float* out, long long n, void* stream) {
+rm_status rm_debug_gelu(const float* u, float* out, long long n, int form, void* stream) {
     if (n < 0) return fail(RM_ERR_INVALID_ARG, "n must be >= 0");
     if (n > 0 && (!u || !out)) return fail(RM_ERR_INVALID_ARG, "u / out is NULL");
-    RM_CHECK_CUDA(launch_debug_gelu(u, out, n, as_stream(stream)), "debug gelu");
+    if (form != 0 && form != 1) return fail(RM_ERR_INVALID_ARG, "form must be 0 (scalar) or 1 (packed)");
+    RM_CHECK_CUDA(launch_debug_gelu(u, out, n, form, as_stream(stream)), "debug gelu");
     return RM_OK;
 }
 

@@ -78,6 +78,72 @@ __device__ __forceinline__ float gelu_erf(float u) {
     return u >= 0.0f ? u - uc : uc;
 }
 
+// The same GELU for two values at once, with the packed fp32x2 arithmetic of
+// sm_100+ (one instruction per pair for add, multiply and fused multiply-add).
+// Written as Gelu(u) = relu(u) - |u| c / 2 with c = 1 - erf(|u| / sqrt 2),
+// which holds for both signs (u >= 0: u - u c / 2; u < 0: u c / 2), has no
+// branch and no cancellation for negative u; relu(u) = (u + |u|) / 2 is exact.
+// The coefficients carry the sign of -c / 2 so that the last step is one fma.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_splat(float x) { return f2_pack(x, x); }
+
+// (Gelu(u0 + b0), Gelu(u1 + b1)) as a packed pair
+__device__ __forceinline__ uint64_t gelu_erf_x2(uint64_t u, uint64_t b) {
+    constexpr float k1 = 0.8493218002880191f;     // sqrt(log2(e) / 2)
+    constexpr float pp = 0.27273748087922245f;    // p / (sqrt(2) k1)
+    // -a_i / 2 (Abramowitz & Stegun 7.1.26)
+    constexpr float nh1 = -0.127414796f, nh2 = 0.142248368f, nh3 = -0.7107068705f, nh4 = 0.7265760135f,
+                    nh5 = -0.5307027145f;
+    u = f2_add(u, b);
+    const uint64_t a = u & 0x7fffffff7fffffffull;                   // |u|
+    const uint64_t xp = f2_mul(a, f2_splat(k1));
+    const uint64_t den = f2_fma(f2_splat(pp), xp, f2_splat(1.0f));
+    float d0, d1;
+    f2_unpack(den, d0, d1);
+    const uint64_t t = f2_pack(rcp_approx(d0), rcp_approx(d1));
+    uint64_t q = f2_fma(t, f2_splat(nh5), f2_splat(nh4));
+    q = f2_fma(t, q, f2_splat(nh3));
+    q = f2_fma(t, q, f2_splat(nh2));
+    q = f2_fma(t, q, f2_splat(nh1));
+    q = f2_mul(q, t);                                               // -c / (2 e)
+    const uint64_t sq = f2_mul(xp, xp);
+    float s0, s1;
+    f2_unpack(sq, s0, s1);
+    const uint64_t e = f2_pack(ex2_approx(-s0), ex2_approx(-s1));   // exp(-u^2 / 2)
+    const uint64_t w = f2_mul(q, e);                                // -c / 2
+    const uint64_t relu = f2_mul(f2_add(u, a), f2_splat(0.5f));
+    return f2_fma(a, w, relu);
+}
+
+// Packed fp32 pair -> packed fp16 pair (saturating)
+__device__ __forceinline__ uint32_t pack_f16x2_from_f2(uint64_t v) {
+    float lo, hi;
+    f2_unpack(v, lo, hi);
+    return pack_f16x2(lo, hi);
+}
+
 // ---------------------------------------------------------------------------
 // Warp reductions
 // ---------------------------------------------------------------------------
@@ -284,6 +350,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+
+// The same load without the wait: the registers are valid only after
+// tmem_wait_ld(), so a caller can compute on the previous chunk meanwhile.
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
 // with 128-byte swizzling: rows of 64 16-bit elements (128 B), 8-row swizzle atoms of

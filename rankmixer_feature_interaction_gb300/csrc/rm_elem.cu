@@ -714,9 +714,17 @@ __global__ void to_f32_kernel(const Tin* __restrict__ in, float* __restrict__ ou
         out[i] = to_f32(in[i]);
 }
 
-__global__ void debug_gelu_kernel(const float* __restrict__ u, float* __restrict__ out, long long n) {
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
-        out[i] = gelu_erf(u[i]);
+__global__ void debug_gelu_kernel(const float* __restrict__ u, float* __restrict__ out, long long n, int form) {
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        if (form == 0) {
+            out[i] = gelu_erf(u[i]);
+        } else {     // the packed form, value in the low half, its neighbour in the high half
+            const float nb = i + 1 < n ? u[i + 1] : 0.f;
+            float lo, hi;
+            f2_unpack(gelu_erf_x2(f2_pack(u[i], nb), f2_pack(0.f, 0.f)), lo, hi);
+            out[i] = lo;
+        }
+    }
 }
 
 __global__ void debug_wait_kernel(const int* flag, int* err, unsigned long long timeout_ns) {
@@ -847,9 +855,9 @@ cudaError_t launch_to_f32(Act act, const void* in, float* out, size_t n, cudaStr
     return cudaGetLastError();
 }
 
-cudaError_t launch_debug_gelu(const float* u, float* out, long long n, cudaStream_t s) {
+cudaError_t launch_debug_gelu(const float* u, float* out, long long n, int form, cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
-    debug_gelu_kernel<<<grid_for(n, 256), 256, 0, s>>>(u, out, n);
+    debug_gelu_kernel<<<grid_for(n, 256), 256, 0, s>>>(u, out, n, form);
     return cudaGetLastError();
 }
 

@@ -166,20 +166,29 @@ template <int COLS>
 __device__ __forceinline__ void epilogue_gelu_tma(const Args& args, const TileCoord& tc, const CUtensorMap* tmC,
                                                   uint32_t tbase, int n0, int m_warp, uint32_t stage, int lane,
                                                   int& sbuf) {
+    constexpr int NC = COLS / 32;
     const float* bias = args.bias + (size_t)tc.wg * args.N + n0;
     const bool any_valid = m_warp < tc.Mg;
     const uint32_t sw = (uint32_t)((lane >> 1) & 3);
-#pragma unroll 1
-    for (int c = 0; c < COLS / 32; ++c) {
-        float v[32];
-        tmem_ld32(tbase + 32u * c, v);
+    // TMEM loads run one chunk ahead: chunk c + 1 is in flight while chunk c is
+    // turned into GELU outputs (the load registers alternate between two sets)
+    uint32_t r[2][32];
+    tmem_ld32_nowait(tbase, r[0]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        __syncwarp();
+        if (c + 1 < NC) tmem_ld32_nowait(tbase + 32u * (c + 1), r[(c + 1) & 1]);
+        const uint32_t* v = r[c & 1];
         uint32_t p[16];
         const float4* b4 = reinterpret_cast<const float4*>(bias + 32 * c);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const float4 bb = __ldg(b4 + j);
-            p[2 * j] = pack_f16x2(gelu_erf(v[4 * j] + bb.x), gelu_erf(v[4 * j + 1] + bb.y));
-            p[2 * j + 1] = pack_f16x2(gelu_erf(v[4 * j + 2] + bb.z), gelu_erf(v[4 * j + 3] + bb.w));
+            p[2 * j] = pack_f16x2_from_f2(gelu_erf_x2(f2_pack(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1])),
+                                                      f2_pack(bb.x, bb.y)));
+            p[2 * j + 1] = pack_f16x2_from_f2(
+                gelu_erf_x2(f2_pack(__uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])), f2_pack(bb.z, bb.w)));
         }
         if (lane == 0) bulk_wait_group_read<1>();
         __syncwarp();
@@ -195,6 +204,7 @@ __device__ __forceinline__ void epilogue_gelu_tma(const Args& args, const TileCo
             bulk_commit_group();
         }
         sbuf ^= 1;
+        if (c + 1 < NC) tmem_wait_ld();
     }
 }
 
@@ -218,8 +228,9 @@ __device__ __forceinline__ void epilogue_tile(const Args& args, const TileCoord&
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const float4 bb = __ldg(b4 + j);
-                    p[2 * j] = pack_f16x2(gelu_erf(v[4 * j] + bb.x), gelu_erf(v[4 * j + 1] + bb.y));
-                    p[2 * j + 1] = pack_f16x2(gelu_erf(v[4 * j + 2] + bb.z), gelu_erf(v[4 * j + 3] + bb.w));
+                    p[2 * j] = pack_f16x2_from_f2(gelu_erf_x2(f2_pack(v[4 * j], v[4 * j + 1]), f2_pack(bb.x, bb.y)));
+                    p[2 * j + 1] =
+                        pack_f16x2_from_f2(gelu_erf_x2(f2_pack(v[4 * j + 2], v[4 * j + 3]), f2_pack(bb.z, bb.w)));
                 }
                 uint4* dst = reinterpret_cast<uint4*>(args.hid + orow + 32 * c);
 #pragma unroll

@@ -77,7 +77,7 @@ cudaError_t launch_transpose_f32(const float* in, float* out, int G, int R, int 
 cudaError_t launch_to_f32(Act act, const void* in, float* out, size_t n, cudaStream_t s);
 
 // Test hook: out[i] = the GELU the GEMM epilogues use, applied to u[i].
-cudaError_t launch_debug_gelu(const float* u, float* out, long long n, cudaStream_t s);
+cudaError_t launch_debug_gelu(const float* u, float* out, long long n, int form, cudaStream_t s);
 
 // Test hook: bounded wait on a flag nothing sets; latches kDevErrTimeout.
 cudaError_t launch_debug_wait(const int* flag, int* err, unsigned long long timeout_ns, cudaStream_t s);

@@ -104,6 +104,9 @@ def test_null_context_calls(lib):
     assert lib.rm_sync_status(None, None) == _lib.RM_ERR_INVALID_ARG
     assert lib.rm_profile_enable(None, 1) == _lib.RM_ERR_INVALID_ARG
     assert "ctx is NULL" in _lib.rm_last_error()
+    assert lib.rm_debug_gelu(None, None, 0, 2, None) == _lib.RM_ERR_INVALID_ARG      # unknown form
+    assert lib.rm_debug_gelu(None, None, -1, 0, None) == _lib.RM_ERR_INVALID_ARG     # n < 0
+    assert lib.rm_debug_gelu(None, None, 5, 1, None) == _lib.RM_ERR_INVALID_ARG      # NULL buffers
 
 
 def test_binding_raises_with_status_and_message(lib):

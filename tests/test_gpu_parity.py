@@ -49,13 +49,16 @@ def test_token_mix_bit_exact(dtype, B, T, D, H):
     np.testing.assert_array_equal(_np(Y), oracle.token_mix(_np(X), H))
 
 
-def test_device_gelu_matches_the_definition():
-    """The epilogue GELU (erf by Abramowitz & Stegun 7.1.26) against u * Phi(u) in float64."""
+@pytest.mark.parametrize("form", [0, 1])
+def test_device_gelu_matches_the_definition(form):
+    """The epilogue GELU (erf by Abramowitz & Stegun 7.1.26) against u * Phi(u) in float64:
+    form 0 is the scalar form of the CUDA-core GEMMs, form 1 the packed form of the
+    tensor-core epilogues."""
     from scipy.special import ndtr
     u = torch.cat([torch.linspace(-12, 12, 200001), torch.tensor([0.0, -0.0, 1.0, -1.0, 30.0, -30.0, 1e-8, -1e-8])])
     out = torch.empty_like(u, device=DEV)
     ud = u.to(DEV)
-    _lib.rm_debug_gelu(ud.data_ptr(), out.data_ptr(), u.numel(), torch.cuda.current_stream().cuda_stream)
+    _lib.rm_debug_gelu(ud.data_ptr(), out.data_ptr(), u.numel(), form, torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     x = u.double().numpy()
     ref = x * ndtr(x)
