@@ -293,7 +293,8 @@ rm_status stack_device(rm_ctx* c, const void* X0, float* pooled, void* XL, int B
     const int last = g.L - 1;
     ProfScope ps(c, RM_K_POOL, s);
     RM_CHECK_CUDA(launch_pool(c->act, c->Z, c->stats, c->layers[last].g2, c->layers[last].be2, pooled, XL, B, g.T,
-                              g.D, c->Bcap, layer_nchunk(c, last), layer_cw(c, last), g.ln_eps, c->num_sms, s),
+                              g.D, c->Bcap, layer_nchunk(c, last), layer_cw(c, last), g.ln_eps, c->num_sms, c->d_err,
+                              kWaitTimeoutNs, s),
                   "ln2+pool");
     return RM_OK;
 }

@@ -286,29 +286,27 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
     }
     __syncthreads();
 
-    auto issue = [&](int b, int slot) {   // thread 0 only: T row copies into padded rows
+    auto issue = [&](int b, int slot) {   // warp 0: lane 0 arms the barrier, lane t copies row t
         const uint32_t bar = smem_u32(&bars[slot]);
         const uint32_t dst = smem_u32(buf) + (uint32_t)slot * buf_elems * 2u;
         const uint32_t st_bytes = stats_bulk ? (uint32_t)a.nchunk * 8u : 0u;
         fence_proxy_async_smem();
-        mbar_arrive_expect_tx(bar, (uint32_t)T * (row_bytes + st_bytes));
-        for (int t = 0; t < T; ++t) {
+        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)T * (row_bytes + st_bytes));
+        __syncwarp();
+        for (int t = lane; t < T; t += 32) {
             const uint16_t* row = FROM_Z ? src + ((size_t)t * a.Bcap + b) * D : src + ((size_t)b * T + t) * D;
             bulk_copy_g2s(dst + (uint32_t)t * (uint32_t)RS * 2u, row, row_bytes, bar);
-        }
-        if (stats_bulk) {
-            const uint32_t sdst = smem_u32(sst) + (uint32_t)slot * (uint32_t)T * st_bytes;
-            for (int t = 0; t < T; ++t)
-                bulk_copy_g2s(sdst + (uint32_t)t * st_bytes, a.stats + ((size_t)t * a.Bcap + b) * a.nchunk, st_bytes,
-                              bar);
+            if (stats_bulk)
+                bulk_copy_g2s(smem_u32(sst) + ((uint32_t)slot * (uint32_t)T + (uint32_t)t) * st_bytes,
+                              a.stats + ((size_t)t * a.Bcap + b) * a.nchunk, st_bytes, bar);
         }
     };
 
-    if (threadIdx.x == 0 && (int)blockIdx.x < a.B) issue(blockIdx.x, 0);
+    if (warp == 0 && (int)blockIdx.x < a.B) issue(blockIdx.x, 0);
     int it = 0;
     for (int b = blockIdx.x; b < a.B; b += gridDim.x, ++it) {
         const int slot = it & 1;
-        if (threadIdx.x == 0 && b + (int)gridDim.x < a.B) issue(b + gridDim.x, slot ^ 1);
+        if (warp == 0 && b + (int)gridDim.x < a.B) issue(b + gridDim.x, slot ^ 1);
         if (FROM_Z && !stats_bulk) sample_row_stats(a, b, s_mean, s_rstd, warp, nwarps, lane);
         mbar_wait_bounded(smem_u32(&bars[slot]), (uint32_t)(it >> 1) & 1u, s_abort, a.err, a.timeout_ns);
         __syncthreads();
@@ -325,17 +323,19 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
                     rt = s_rstd[t];
                 }
                 uint16_t* row = xs + (size_t)t * RS;
+                // (z - mean) (rstd gamma) + beta on fp16 pairs: the result is stored in
+                // fp16, and the row statistics themselves were merged in fp32
+                const __half2 m2 = __float2half2_rn(mt), r2 = __float2half2_rn(rt);
                 for (int c = lane * 8; c < D; c += 256) {
-                    float z[8], g[8], be[8];
-                    f16x8_to_f32(*reinterpret_cast<const uint4*>(row + c), z);
-                    f16x8_to_f32(*reinterpret_cast<const uint4*>(sg2 + c), g);
-                    f16x8_to_f32(*reinterpret_cast<const uint4*>(sb2 + c), be);
-                    uint32_t o[4];
+                    uint4 zv = *reinterpret_cast<const uint4*>(row + c);
+                    const uint4 gv = *reinterpret_cast<const uint4*>(sg2 + c);
+                    const uint4 bv = *reinterpret_cast<const uint4*>(sb2 + c);
+                    __half2* z2 = reinterpret_cast<__half2*>(&zv);
+                    const __half2* g2h = reinterpret_cast<const __half2*>(&gv);
+                    const __half2* b2h = reinterpret_cast<const __half2*>(&bv);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        o[k] = pack_f16x2(ln_apply(z[2 * k], mt, rt, g[2 * k], be[2 * k]),
-                                          ln_apply(z[2 * k + 1], mt, rt, g[2 * k + 1], be[2 * k + 1]));
-                    *reinterpret_cast<uint4*>(row + c) = make_uint4(o[0], o[1], o[2], o[3]);
+                    for (int k = 0; k < 4; ++k) z2[k] = __hfma2(__hsub2(z2[k], m2), __hmul2(r2, g2h[k]), b2h[k]);
+                    *reinterpret_cast<uint4*>(row + c) = zv;
                 }
             }
             __syncthreads();
@@ -779,7 +779,7 @@ cudaError_t launch_ln2_out(Act act, const void* Z, const float2* stats, const fl
 
 cudaError_t launch_pool(Act act, const void* Z, const float2* stats, const float* g2, const float* be2,
                         float* pooled, void* XL, int B, int T, int D, int Bcap, int nchunk, int cw, float eps,
-                        int num_sms, cudaStream_t s) {
+                        int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     if (T > kMaxT) return cudaErrorNotSupported;
     const int grid = B < num_sms * 8 ? B : num_sms * 8;

@@ -162,7 +162,7 @@ __device__ __forceinline__ TileCoord decode_tile(long long tile, const Args& a) 
 // clips rows past the token group's batch.  Two staging blocks per warp
 // alternate; a block is refilled only after the store that read it has
 // finished reading (bulk wait_group.read 1).
-template <int COLS>
+template <int COLS, bool PREFETCH>
 __device__ __forceinline__ void epilogue_gelu_tma(const Args& args, const TileCoord& tc, const CUtensorMap* tmC,
                                                   uint32_t tbase, int n0, int m_warp, uint32_t stage, int lane,
                                                   int& sbuf) {
@@ -170,16 +170,21 @@ __device__ __forceinline__ void epilogue_gelu_tma(const Args& args, const TileCo
     const float* bias = args.bias + (size_t)tc.wg * args.N + n0;
     const bool any_valid = m_warp < tc.Mg;
     const uint32_t sw = (uint32_t)((lane >> 1) & 3);
-    // TMEM loads run one chunk ahead: chunk c + 1 is in flight while chunk c is
-    // turned into GELU outputs (the load registers alternate between two sets)
-    uint32_t r[2][32];
+    // PREFETCH: TMEM loads run one chunk ahead, chunk c + 1 in flight while
+    // chunk c is turned into GELU outputs (two register sets).  Without it
+    // (more epilogue warps, fewer registers each) other warps hide the load.
+    uint32_t r[PREFETCH ? 2 : 1][32];
     tmem_ld32_nowait(tbase, r[0]);
     tmem_wait_ld();
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
         __syncwarp();
-        if (c + 1 < NC) tmem_ld32_nowait(tbase + 32u * (c + 1), r[(c + 1) & 1]);
-        const uint32_t* v = r[c & 1];
+        if (PREFETCH && c + 1 < NC) tmem_ld32_nowait(tbase + 32u * (c + 1), r[(c + 1) % (PREFETCH ? 2 : 1)]);
+        if (!PREFETCH && c > 0) {
+            tmem_ld32_nowait(tbase + 32u * c, r[0]);
+            tmem_wait_ld();
+        }
+        const uint32_t* v = r[c % (PREFETCH ? 2 : 1)];
         uint32_t p[16];
         const float4* b4 = reinterpret_cast<const float4*>(bias + 32 * c);
 #pragma unroll
@@ -204,7 +209,7 @@ __device__ __forceinline__ void epilogue_gelu_tma(const Args& args, const TileCo
             bulk_commit_group();
         }
         sbuf ^= 1;
-        if (c + 1 < NC) tmem_wait_ld();
+        if (PREFETCH && c + 1 < NC) tmem_wait_ld();
     }
 }
 
@@ -458,7 +463,7 @@ pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN + half * C::COLS_PER_WARP);
             const int n0 = tc.nb * BN + half * C::COLS_PER_WARP;
             if (EPI == EPI_GELU && args.hid_tma)
-                epilogue_gelu_tma<C::COLS_PER_WARP>(args, tc, &tmC, tbase, n0, m - lane, stage, lane, sbuf);
+                epilogue_gelu_tma<C::COLS_PER_WARP, true>(args, tc, &tmC, tbase, n0, m - lane, stage, lane, sbuf);
             else
                 epilogue_tile<C::COLS_PER_WARP, EPI>(args, tc, valid, arow, tbase, n0);
             tc_fence_before();
@@ -495,28 +500,33 @@ pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 // ----------------------------------------------------------------------------
 constexpr int BM2 = 256;                 // rows per CTA pair
 
-template <int BN>
+template <int BN, int EPW>
 struct Cfg2 {
-    static constexpr int STAGES = 6;
+    // 8 epilogue warps: 6 operand stages; 16 (for the GELU epilogue, which
+    // needs more warps to hide its latency): 5 stages, so the staging fits
+    static constexpr int STAGES = EPW == 16 ? 5 : 6;
+    static constexpr int THREADS = 128 + 32 * EPW;
     static constexpr int A_BYTES = 128 * BK * 2;
     static constexpr int B_BYTES = (BN / 2) * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int BAR_BYTES = 256;
-    static constexpr int EPI_BYTES = kEpiWarps * 2 * 2048;
+    static constexpr int EPI_BYTES = EPW * 2 * 2048;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
-    static constexpr int COLS_PER_WARP = BN / 2;
+    static constexpr int COLS_PER_WARP = BN / (EPW / 4);   // EPW / 4 warps share a TMEM lane quadrant
+    static_assert(EPW == 8 || EPW == 16, "epilogue warps");
+    static_assert(COLS_PER_WARP % 32 == 0, "whole 32-column chunks per warp");
     static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation must be a power of 2");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "pair MMA N");
     static_assert(2 * STAGES * 8 + 4 * 8 + 8 <= BAR_BYTES, "barrier area");
 };
 
-template <int BN, int EPI>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+template <int BN, int EPI, int EPW>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg2<BN, EPW>::THREADS, 1)
 pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const Args args) {
-    using C = Cfg2<BN>;
+    using C = Cfg2<BN, EPW>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -548,7 +558,7 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), 2 * kEpiWarps);
+            mbar_init(tempty_bar(a), 2 * EPW);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -637,7 +647,7 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         // ---------------------------- epilogue (both CTAs) --------------------------------
         const int ew = warp - 4;
         const int quad = warp & 3;
-        const int half = ew >> 2;
+        const int half = ew >> 2;               // which COLS_PER_WARP columns of the tile
         const int row_in_tile = quad * 32 + lane;
         const uint32_t stage = sEpi + (uint32_t)ew * 4096u;
         int sbuf = 0;
@@ -658,7 +668,8 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN + half * C::COLS_PER_WARP);
             const int n0 = tc.nb * BN + half * C::COLS_PER_WARP;
             if (EPI == EPI_GELU && args.hid_tma)
-                epilogue_gelu_tma<C::COLS_PER_WARP>(args, tc, &tmC, tbase, n0, m - lane, stage, lane, sbuf);
+                epilogue_gelu_tma<C::COLS_PER_WARP, EPW == 8>(args, tc, &tmC, tbase, n0, m - lane, stage, lane,
+                                                               sbuf);
             else
                 epilogue_tile<C::COLS_PER_WARP, EPI>(args, tc, valid, arow, tbase, n0);
             tc_fence_before();
@@ -799,10 +810,10 @@ cudaError_t run_bn(int bn, const void* A, long long a_rows_total, const void* W,
 
 // CTA-pair launch for uniform groups (dense PFFN).  Grid = 2 x the number of
 // pairs that can be resident at once (persistent).
-template <int BN, int EPI>
+template <int BN, int EPI, int EPW>
 cudaError_t run_pair(const void* A, long long a_rows_total, const void* W, int n_wgroups, Args a, int num_sms,
                      cudaStream_t s) {
-    using C = Cfg2<BN>;
+    using C = Cfg2<BN, EPW>;
     a.n_tiles = a.N / BN;
     a.m_tiles = (a.M + BM2 - 1) / BM2;
     a.tiles = (long long)a.ngroups * a.m_tiles * a.n_tiles;
@@ -817,14 +828,14 @@ cudaError_t run_pair(const void* A, long long a_rows_total, const void* W, int n
         a.hid_tma = 0;
         mC = mA;   // unused
     }
-    auto k = pffn_gemm_tc2_kernel<BN, EPI>;
+    auto k = pffn_gemm_tc2_kernel<BN, EPI, EPW>;
     static int max_pairs = 0;   // once per template instance
     if (max_pairs == 0) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(2 * (num_sms / 2)), 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.blockDim = dim3(C::THREADS, 1, 1);
         cfg.dynamicSmemBytes = C::SMEM_BYTES;
         cudaLaunchAttribute attr;
         attr.id = cudaLaunchAttributeClusterDimension;
@@ -841,22 +852,23 @@ cudaError_t run_pair(const void* A, long long a_rows_total, const void* W, int n
         max_pairs = n;
     }
     long long pairs = a.tiles < max_pairs ? a.tiles : max_pairs;
-    k<<<(int)(2 * pairs), kThreads, C::SMEM_BYTES, s>>>(mA, mB, mC, a);
+    k<<<(int)(2 * pairs), C::THREADS, C::SMEM_BYTES, s>>>(mA, mB, mC, a);
     return cudaGetLastError();
 }
 
-// Pair tiles for the dense PFFN's second GEMM (K = kD) when every token group
-// has at least 256 rows.  Measured on GB300 at the 1B shape: pair tiles speed
-// up GEMM2 (3.14 -> 3.01 ms per step) but slow down GEMM1 (3.60 -> 3.87 ms),
-// whose short K (= D) leaves its heavier GELU epilogue on the critical path,
-// where the two CTAs of a pair wait for each other.  RM_GEMM_PAIR=0 (never) or
-// =1 (both GEMMs) in the environment overrides the choice (a tuning and
-// diagnosis switch; every choice computes the same result).
+// Pair tiles (256 x BN per CTA pair) when every token group has at least 256
+// rows.  By default only the second GEMM (K = kD) takes them: measured on
+// GB300 at the 1B shape, pair tiles speed up that GEMM, while for the first
+// (K = D, GELU epilogue) neither pair tiles with 8 epilogue warps nor with 16
+// (5 operand stages) beat one CTA per tile (3.31 vs 3.37 ms and 3.21 vs 3.29
+// ms per step on two boxes).  RM_GEMM_PAIR in the environment overrides the
+// choice: 0 never, 1 both GEMMs (the first with 16 epilogue warps), 2 the
+// default (a tuning and diagnosis switch; every choice computes the same result).
 bool use_pair(int M, int epi) {
     static int env = -1;
     if (env < 0) {
         const char* v = getenv("RM_GEMM_PAIR");
-        env = !v ? 2 : (v[0] == '0' ? 0 : 1);
+        env = !v ? 2 : (v[0] == '0' ? 0 : (v[0] == '1' ? 1 : 2));
     }
     if (M < BM2 || env == 0) return false;
     return env == 1 || epi == EPI_RESID;
@@ -865,11 +877,12 @@ bool use_pair(int M, int epi) {
 template <int EPI>
 cudaError_t run_dense(int bn, const void* A, long long a_rows_total, const void* W, int n_wgroups, const Args& a,
                       int num_sms, cudaStream_t s) {
+    constexpr int EPW = EPI == EPI_GELU ? 16 : 8;
     if (use_pair(a.M, EPI)) {
         switch (bn) {
-            case 256: return run_pair<256, EPI>(A, a_rows_total, W, n_wgroups, a, num_sms, s);
-            case 128: return run_pair<128, EPI>(A, a_rows_total, W, n_wgroups, a, num_sms, s);
-            case 64: return run_pair<64, EPI>(A, a_rows_total, W, n_wgroups, a, num_sms, s);
+            case 256: return run_pair<256, EPI, EPW>(A, a_rows_total, W, n_wgroups, a, num_sms, s);
+            case 128: return run_pair<128, EPI, EPW>(A, a_rows_total, W, n_wgroups, a, num_sms, s);
+            case 64: return run_pair<64, EPI, 8>(A, a_rows_total, W, n_wgroups, a, num_sms, s);
             default: return cudaErrorNotSupported;
         }
     }

@@ -53,7 +53,7 @@ cudaError_t launch_ln2_out(Act act, const void* Z, const float2* stats, const fl
 // receives X_L sample-major, rounded to the caller dtype.
 cudaError_t launch_pool(Act act, const void* Z, const float2* stats, const float* g2, const float* be2,
                         float* pooled, void* XL, int B, int T, int D, int Bcap, int nchunk, int cw, float eps,
-                        int num_sms, cudaStream_t s);
+                        int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s);
 
 // (mean, M2) of each full row of Z (operand type; one chunk per row).
 cudaError_t launch_rowstats(Act act, const void* Z, float2* stats, int B, int T, int D, int Bcap, int num_sms,

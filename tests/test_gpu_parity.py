@@ -94,6 +94,7 @@ def test_tiny_fp32_block_and_stack():
 
 @pytest.mark.parametrize("path", ["tcgen05", "simt"])
 @pytest.mark.parametrize("T,D,k,L,B", [(4, 256, 2, 2, 300), (8, 512, 4, 1, 260), (2, 64, 1, 1, 129),
+                                       (2, 192, 2, 1, 300),    # pair tiles with BN = 128 (GEMM1) and 64 (GEMM2)
                                        (16, 768, 4, 1, 77)])
 def test_bf16_block_and_stack(path, T, D, k, L, B):
     m, layers, X = _build(T, D, k, L, B, 11 + T + D, "bf16", path=path)
@@ -396,3 +397,42 @@ def test_moe_1b_full_size_sampled():
                                        pt["eW2"], pt["eb2"], return_gates=True)
         np.testing.assert_allclose(_np(G[b:b + 1, t:t + 1]), G_ref, atol=2e-4, rtol=1e-3)
         check(V[b:b + 1, t:t + 1], V_ref, "bf16", f"MoE V (b={b}, t={t})")
+
+
+# ----------------------------------------------------------------------------
+# Every tile dispatch of the dense GEMMs (RM_GEMM_PAIR is read once per process)
+# ----------------------------------------------------------------------------
+
+_DISPATCH_CHILD = r"""
+import sys, numpy as np, torch
+sys.path.insert(0, {root!r})
+import oracle
+from rankmixer_feature_interaction_gb300 import synth
+from rankmixer_feature_interaction_gb300.api import RankMixer
+from tests.helpers import check
+T, D, k, L, B = {shape}
+layers = synth.make_stack(T, D, k, L, 123, "bf16", "cuda")
+m = RankMixer(T, D, k, layers, max_batch=B, gemm_path="tcgen05")
+X = synth.make_input(B, T, D, 124, "bf16", "cuda")
+pooled, XL = m.stack_forward(X, return_XL=True)
+torch.cuda.synchronize()
+assert m.sync_status() == 0
+p64 = synth.to_f64(layers)
+ref_pool, ref_XL = oracle.stack_forward(X.cpu().double().numpy(), p64, return_XL=True)
+check(XL, ref_XL, "bf16", "X_L")
+check(pooled, ref_pool, "bf16", "pooled")
+print("ok")
+"""
+
+
+@pytest.mark.parametrize("pair", ["0", "1", "2"])
+@pytest.mark.parametrize("shape", [(4, 256, 2, 2, 300), (2, 192, 2, 1, 300)])
+def test_every_gemm_tile_dispatch(pair, shape):
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, RM_GEMM_PAIR=pair)
+    r = subprocess.run([sys.executable, "-c", _DISPATCH_CHILD.format(root=root, shape=shape)], env=env, cwd=root,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
