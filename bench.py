@@ -274,11 +274,11 @@ def run_ours(args):
     active = None
     if moe:
         # algorithmic flops: every open (sample, token, expert) runs 2 D Fe flops in each
-        # expert layer; expert layer 1 is one launch, layer 2 one launch per expert index
+        # expert layer, each layer one launch over all (token, expert) groups
         _, G = m.moe_pffn_forward(0, S_in, V, return_gates=True)
         active = int((G > 0).sum().item())
         per_layer = 2.0 * active * D * Fe
-        flops_launch = per_layer if dom == "moe_gemm1" else per_layer / E
+        flops_launch = per_layer
         flops_step = 2 * per_layer + 2.0 * B * T * D * E      # + router
     else:
         flops_launch = flops_gemm

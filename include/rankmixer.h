@@ -138,9 +138,10 @@ typedef enum rm_kernel_kind {
     RM_K_ROWSTATS = 5,   /* LN2 row statistics (SIMT path only) */
     RM_K_MOE_ROUTE = 6,  /* router GEMV + ReLU + per-(token, expert) compaction */
     RM_K_MOE_GEMM1 = 7,  /* expert layer 1 + bias + GELU on gathered rows */
-    RM_K_MOE_GEMM2 = 8,  /* expert layer 2 + bias, gated scatter-add */
+    RM_K_MOE_GEMM2 = 8,  /* expert layer 2 + bias, gated, one packed row per (sample, token, open expert) */
     RM_K_MISC = 9,       /* copies, layout changes */
-    RM_K_COUNT = 10
+    RM_K_MOE_COMBINE = 10, /* sum of the open experts' gated rows per (sample, token), fixed expert order */
+    RM_K_COUNT = 11
 } rm_kernel_kind;
 
 typedef struct rm_kernel_stat {

@@ -87,12 +87,7 @@ struct Args {
     __half* z;                // EPI_RESID output rows (fp16)
     float2* stats;            // EPI_RESID row partials [row][nchunk]
     int nchunk;
-    const int* row_sample;    // EPI_GATED: packed row -> sample index b
-    const float* gates;       // EPI_GATED: [B][T][E]
-    const int* first_e;       // EPI_GATED: [B][T] first open expert (it stores; later ones add)
-    int gT, gE;
-    float* v;                 // EPI_GATED: V row (b, t) at b * v_sb + t * v_st
-    long long v_sb, v_st;
+    const float* row_gate;    // EPI_GATED: gate of each packed row (same row index as A)
     int* err;
     unsigned long long timeout_ns;
 };
@@ -287,34 +282,25 @@ __device__ __forceinline__ void epilogue_tile(const Args& args, const TileCoord&
             const int chunk = n0 / COLS;
             args.stats[(size_t)arow * args.nchunk + chunk] = make_float2(mean, m2);
         }
-    } else {  // EPI_GATED: V[b, t] (+)= gate * (acc + b2); the first open expert of (b, t) stores
-        float gate = 0.f;
-        float* vrow = nullptr;
-        bool first = true;
-        if (valid) {
-            const int b = __ldg(args.row_sample + arow);
-            const int t = tc.wg / args.gE, e = tc.wg - t * args.gE;
-            gate = __ldg(args.gates + ((size_t)b * args.gT + t) * args.gE + e);
-            first = __ldg(args.first_e + (size_t)b * args.gT + t) == e;
-            vrow = args.v + (size_t)b * args.v_sb + (size_t)t * args.v_st + n0;
-        }
+    } else {  // EPI_GATED: Y[row] = gate * (acc + b2) in fp16, row = the packed row of A
+        const float gate = valid ? __ldg(args.row_gate + arow) : 0.f;
 #pragma unroll 1
         for (int c = 0; c < (COLS / 32); ++c) {
             float v[32];
             tmem_ld32(tbase + 32u * c, v);
             if (valid) {
                 const float4* b4 = reinterpret_cast<const float4*>(bias + 32 * c);
-                float4* dst = reinterpret_cast<float4*>(vrow + 32 * c);
+                uint32_t p[16];
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const float4 bb = __ldg(b4 + j);
-                    float4 o = first ? make_float4(0.f, 0.f, 0.f, 0.f) : dst[j];
-                    o.x = fmaf(gate, v[4 * j] + bb.x, o.x);
-                    o.y = fmaf(gate, v[4 * j + 1] + bb.y, o.y);
-                    o.z = fmaf(gate, v[4 * j + 2] + bb.z, o.z);
-                    o.w = fmaf(gate, v[4 * j + 3] + bb.w, o.w);
-                    dst[j] = o;
+                    p[2 * j] = pack_f16x2(gate * (v[4 * j] + bb.x), gate * (v[4 * j + 1] + bb.y));
+                    p[2 * j + 1] = pack_f16x2(gate * (v[4 * j + 2] + bb.z), gate * (v[4 * j + 3] + bb.w));
                 }
+                uint4* dst = reinterpret_cast<uint4*>(args.hid + orow + 32 * c);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
             }
         }
     }
@@ -372,9 +358,12 @@ pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const long long tiles =
         args.tile_prefix ? (long long)__ldg(args.tile_prefix + args.ngroups) * args.n_tiles : args.tiles;
 
+    // The producer and MMA warps run their loops converged (every lane waits
+    // on the barriers); lane 0 issues the copies, the MMAs and their commits
+    // (a commit tracks the MMAs of the thread that issues it).
     if (warp == 0) {
         // ------------------------------ TMA producer ------------------------------
-        if (lane == 0) {
+        {
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -386,9 +375,12 @@ pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(full_bar(stage), (uint32_t)C::STAGE_BYTES);
-                    tma_load_3d(&tmA, sA + stage * C::A_BYTES, full_bar(stage), kb * BK, arow, 0);
-                    tma_load_3d(&tmB, sB + stage * C::B_BYTES, full_bar(stage), kb * BK, tc.nb * BN, tc.wg);
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(full_bar(stage), (uint32_t)C::STAGE_BYTES);
+                        tma_load_3d(&tmA, sA + stage * C::A_BYTES, full_bar(stage), kb * BK, arow, 0);
+                        tma_load_3d(&tmB, sB + stage * C::B_BYTES, full_bar(stage), kb * BK, tc.nb * BN, tc.wg);
+                    }
+                    __syncwarp();
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -398,7 +390,7 @@ pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer --------------------------------
-        if (lane == 0) {
+        {
             constexpr uint32_t idesc = make_idesc_f16_f32(BM, BN);
             int stage = 0;
             uint32_t phase = 0;
@@ -420,19 +412,23 @@ pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     tc_fence_after();
                     const uint32_t a0 = sA + stage * C::A_BYTES;
                     const uint32_t b0 = sB + stage * C::B_BYTES;
+                    if (lane == 0) {
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k) {
-                        umma_f16(d_tmem, make_sw128_desc(a0 + 32u * k), make_sw128_desc(b0 + 32u * k), idesc,
-                                  (kb > 0 || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < BK / 16; ++k) {
+                            umma_f16(d_tmem, make_sw128_desc(a0 + 32u * k), make_sw128_desc(b0 + 32u * k), idesc,
+                                     (kb > 0 || k > 0) ? 1u : 0u);
+                        }
+                        umma_commit(empty_bar(stage));
                     }
-                    umma_commit(empty_bar(stage));
+                    __syncwarp();
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                umma_commit(tfull_bar(acc));
+                if (lane == 0) umma_commit(tfull_bar(acc));
+                __syncwarp();
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
             }
@@ -449,12 +445,8 @@ pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         uint32_t acc_phase = 0;
         for (long long tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
             const TileCoord tc = decode_tile(tile, args);
-            // one lane waits, the warp follows (keeps tcgen05.ld warp-converged)
-            int ok = 1;
-            if (lane == 0) ok = mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err, args.timeout_ns);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            __syncwarp();
+            // every lane waits (the warp stays converged for tcgen05.ld)
+            if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err, args.timeout_ns)) break;
             tc_fence_after();
             const int m = tc.mb * BM + row_in_tile;          // row inside the group
             const bool valid = m < tc.Mg;
@@ -500,14 +492,18 @@ pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 // ----------------------------------------------------------------------------
 constexpr int BM2 = 256;                 // rows per CTA pair
 
-template <int BN, int EPW>
+template <int BN, int EPW, int KSUB>
 struct Cfg2 {
-    // 8 epilogue warps: 6 operand stages; 16 (for the GELU epilogue, which
-    // needs more warps to hide its latency): 5 stages, so the staging fits
-    static constexpr int STAGES = EPW == 16 ? 5 : 6;
+    // A stage holds KSUB 64-deep k-blocks (KSUB x 4 MMAs per barrier wait and
+    // commit).  8 epilogue warps: 6 stages of one k-block or 3 of two; 16
+    // (for the GELU epilogue, which needs more warps to hide its latency): 5
+    // or 2, so the epilogue staging fits.
+    static constexpr int STAGES = KSUB == 1 ? (EPW == 16 ? 5 : 6) : (EPW == 16 ? 2 : 3);
     static constexpr int THREADS = 128 + 32 * EPW;
-    static constexpr int A_BYTES = 128 * BK * 2;
-    static constexpr int B_BYTES = (BN / 2) * BK * 2;
+    static constexpr int A_SUB = 128 * BK * 2;           // one 64-deep k-block of A (this CTA's 128 rows)
+    static constexpr int B_SUB = (BN / 2) * BK * 2;      // ... and of this CTA's half of B
+    static constexpr int A_BYTES = KSUB * A_SUB;
+    static constexpr int B_BYTES = KSUB * B_SUB;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int BAR_BYTES = 256;
@@ -515,6 +511,7 @@ struct Cfg2 {
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
     static constexpr int COLS_PER_WARP = BN / (EPW / 4);   // EPW / 4 warps share a TMEM lane quadrant
     static_assert(EPW == 8 || EPW == 16, "epilogue warps");
+    static_assert(KSUB == 1 || KSUB == 2, "k-blocks per stage");
     static_assert(COLS_PER_WARP % 32 == 0, "whole 32-column chunks per warp");
     static_assert(TMEM_COLS <= 512 && (TMEM_COLS & (TMEM_COLS - 1)) == 0, "TMEM allocation must be a power of 2");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -522,11 +519,11 @@ struct Cfg2 {
     static_assert(2 * STAGES * 8 + 4 * 8 + 8 <= BAR_BYTES, "barrier area");
 };
 
-template <int BN, int EPI, int EPW>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg2<BN, EPW>::THREADS, 1)
+template <int BN, int EPI, int EPW, int KSUB>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg2<BN, EPW, KSUB>::THREADS, 1)
 pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const Args args) {
-    using C = Cfg2<BN, EPW>;
+    using C = Cfg2<BN, EPW, KSUB>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -573,12 +570,12 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
 
-    const int kblocks = args.K / BK;
+    const int kblocks = args.K / (BK * KSUB);
     const long long tiles = args.tiles;
 
     if (warp == 0) {
         // ---------------------------- TMA producer (both CTAs) ----------------------------
-        if (lane == 0) {
+        {
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -591,10 +588,17 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = mapa_shared(full_bar(stage), 0);
-                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), (uint32_t)(2 * C::STAGE_BYTES));
-                    tma_load_3d_pair(&tmA, sA + stage * C::A_BYTES, fb, kb * BK, arow, 0);
-                    tma_load_3d_pair(&tmB, sB + stage * C::B_BYTES, fb, kb * BK, brow, tc.wg);
+                    if (lane == 0) {
+                        const uint32_t fb = mapa_shared(full_bar(stage), 0);
+                        if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), (uint32_t)(2 * C::STAGE_BYTES));
+#pragma unroll
+                        for (int ks = 0; ks < KSUB; ++ks) {
+                            const int kx = (kb * KSUB + ks) * BK;
+                            tma_load_3d_pair(&tmA, sA + stage * C::A_BYTES + ks * C::A_SUB, fb, kx, arow, 0);
+                            tma_load_3d_pair(&tmB, sB + stage * C::B_BYTES + ks * C::B_SUB, fb, kx, brow, tc.wg);
+                        }
+                    }
+                    __syncwarp();
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -604,7 +608,7 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         }
     } else if (warp == 1) {
         // ---------------------------- pair MMA issuer (even CTA) --------------------------
-        if (lane == 0 && rank == 0) {
+        if (rank == 0) {
             constexpr uint32_t idesc = make_idesc_f16_f32(BM2, BN);
             int stage = 0;
             uint32_t phase = 0;
@@ -626,19 +630,25 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                     tc_fence_after();
                     const uint32_t a0 = sA + stage * C::A_BYTES;
                     const uint32_t b0 = sB + stage * C::B_BYTES;
+                    if (lane == 0) {
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k) {
-                        umma_f16_pair(d_tmem, make_sw128_desc(a0 + 32u * k), make_sw128_desc(b0 + 32u * k), idesc,
-                                      (kb > 0 || k > 0) ? 1u : 0u);
+                        for (int ks = 0; ks < KSUB; ++ks)
+#pragma unroll
+                            for (int k = 0; k < BK / 16; ++k)
+                                umma_f16_pair(d_tmem, make_sw128_desc(a0 + ks * C::A_SUB + 32u * k),
+                                              make_sw128_desc(b0 + ks * C::B_SUB + 32u * k), idesc,
+                                              (kb > 0 || ks > 0 || k > 0) ? 1u : 0u);
+                        umma_commit_pair_mc(empty_bar(stage), (uint16_t)0x3);
                     }
-                    umma_commit_pair_mc(empty_bar(stage), (uint16_t)0x3);
+                    __syncwarp();
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                umma_commit_pair_mc(tfull_bar(acc), (uint16_t)0x3);
+                if (lane == 0) umma_commit_pair_mc(tfull_bar(acc), (uint16_t)0x3);
+                __syncwarp();
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
             }
@@ -655,11 +665,8 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         uint32_t acc_phase = 0;
         for (long long tile = pair; tile < tiles; tile += npairs) {
             const TileCoord tc = decode_tile(tile, args);
-            int ok = 1;
-            if (lane == 0) ok = mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err, args.timeout_ns);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            __syncwarp();
+            // every lane waits (the warp stays converged for tcgen05.ld)
+            if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err, args.timeout_ns)) break;
             tc_fence_after();
             const int m = tc.mb * BM2 + 128 * (int)rank + row_in_tile;
             const bool valid = m < tc.Mg;
@@ -810,10 +817,11 @@ cudaError_t run_bn(int bn, const void* A, long long a_rows_total, const void* W,
 
 // CTA-pair launch for uniform groups (dense PFFN).  Grid = 2 x the number of
 // pairs that can be resident at once (persistent).
-template <int BN, int EPI, int EPW>
+template <int BN, int EPI, int EPW, int KSUB>
 cudaError_t run_pair(const void* A, long long a_rows_total, const void* W, int n_wgroups, Args a, int num_sms,
                      cudaStream_t s) {
-    using C = Cfg2<BN, EPW>;
+    using C = Cfg2<BN, EPW, KSUB>;
+    if (a.K % (BK * KSUB) != 0) return cudaErrorInvalidValue;
     a.n_tiles = a.N / BN;
     a.m_tiles = (a.M + BM2 - 1) / BM2;
     a.tiles = (long long)a.ngroups * a.m_tiles * a.n_tiles;
@@ -828,7 +836,7 @@ cudaError_t run_pair(const void* A, long long a_rows_total, const void* W, int n
         a.hid_tma = 0;
         mC = mA;   // unused
     }
-    auto k = pffn_gemm_tc2_kernel<BN, EPI, EPW>;
+    auto k = pffn_gemm_tc2_kernel<BN, EPI, EPW, KSUB>;
     static int max_pairs = 0;   // once per template instance
     if (max_pairs == 0) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
@@ -856,35 +864,73 @@ cudaError_t run_pair(const void* A, long long a_rows_total, const void* W, int n
     return cudaGetLastError();
 }
 
-// Pair tiles (256 x BN per CTA pair) when every token group has at least 256
-// rows.  By default only the second GEMM (K = kD) takes them: measured on
-// GB300 at the 1B shape, pair tiles speed up that GEMM, while for the first
-// (K = D, GELU epilogue) neither pair tiles with 8 epilogue warps nor with 16
-// (5 operand stages) beat one CTA per tile (3.31 vs 3.37 ms and 3.21 vs 3.29
-// ms per step on two boxes).  RM_GEMM_PAIR in the environment overrides the
-// choice: 0 never, 1 both GEMMs (the first with 16 epilogue warps), 2 the
-// default (a tuning and diagnosis switch; every choice computes the same result).
+// Pair tiles (256 x BN per CTA pair) for both GEMMs when every token group
+// has at least 256 rows.  RM_GEMM_PAIR in the environment overrides the
+// choice: 0 never, 2 the second GEMM only (a tuning and diagnosis switch;
+// every choice computes the same result).
 bool use_pair(int M, int epi) {
     static int env = -1;
     if (env < 0) {
         const char* v = getenv("RM_GEMM_PAIR");
-        env = !v ? 2 : (v[0] == '0' ? 0 : (v[0] == '1' ? 1 : 2));
+        env = !v ? 1 : (v[0] == '0' ? 0 : (v[0] == '2' ? 2 : 1));
     }
     if (M < BM2 || env == 0) return false;
     return env == 1 || epi == EPI_RESID;
 }
 
+// Two 64-deep k-blocks per pipeline stage (when K allows): half the barrier
+// waits and commits per MMA, 3 stages of 64 KB per CTA.  Measured on GB300
+// (ncu, B = 2048 at the 1B shape, tensor pipe busy): the first GEMM 91.8%
+// against 80.2% with 6 stages of one k-block (74.2% with one CTA per tile),
+// the second 88.6% against 86.8%.  RM_GEMM_KSUB=1 in the environment forces
+// one k-block per stage (a tuning switch; the same result either way).
+bool use_ksub2(int K, int epi) {
+    (void)epi;
+    static int env = -1;
+    if (env < 0) {
+        const char* v = getenv("RM_GEMM_KSUB");
+        env = (v && v[0] == '1') ? 1 : 2;
+    }
+    return env == 2 && K % (2 * BK) == 0;
+}
+
+// Epilogue warps of the GELU pair kernel: 8 by default (with two k-blocks per
+// stage, 3 stages fit beside their staging), RM_GEMM1_EPW=16 in the
+// environment for 16 (a tuning switch; the same result either way).
+bool gelu_pair_epw16() {
+    static int env = -1;
+    if (env < 0) {
+        const char* v = getenv("RM_GEMM1_EPW");
+        env = (v && v[0] == '1' && v[1] == '6') ? 16 : 8;
+    }
+    return env == 16;
+}
+
+template <int EPI, int EPW>
+cudaError_t run_pair_bn(int bn, bool k2, const void* A, long long a_rows_total, const void* W, int n_wgroups,
+                        const Args& a, int num_sms, cudaStream_t s) {
+    switch (bn) {
+        case 256:
+            return k2 ? run_pair<256, EPI, EPW, 2>(A, a_rows_total, W, n_wgroups, a, num_sms, s)
+                      : run_pair<256, EPI, EPW, 1>(A, a_rows_total, W, n_wgroups, a, num_sms, s);
+        case 128:
+            return k2 ? run_pair<128, EPI, EPW, 2>(A, a_rows_total, W, n_wgroups, a, num_sms, s)
+                      : run_pair<128, EPI, EPW, 1>(A, a_rows_total, W, n_wgroups, a, num_sms, s);
+        case 64:
+            return k2 ? run_pair<64, EPI, 8, 2>(A, a_rows_total, W, n_wgroups, a, num_sms, s)
+                      : run_pair<64, EPI, 8, 1>(A, a_rows_total, W, n_wgroups, a, num_sms, s);
+        default: return cudaErrorNotSupported;
+    }
+}
+
 template <int EPI>
 cudaError_t run_dense(int bn, const void* A, long long a_rows_total, const void* W, int n_wgroups, const Args& a,
                       int num_sms, cudaStream_t s) {
-    constexpr int EPW = EPI == EPI_GELU ? 16 : 8;
     if (use_pair(a.M, EPI)) {
-        switch (bn) {
-            case 256: return run_pair<256, EPI, EPW>(A, a_rows_total, W, n_wgroups, a, num_sms, s);
-            case 128: return run_pair<128, EPI, EPW>(A, a_rows_total, W, n_wgroups, a, num_sms, s);
-            case 64: return run_pair<64, EPI, 8>(A, a_rows_total, W, n_wgroups, a, num_sms, s);
-            default: return cudaErrorNotSupported;
-        }
+        const bool k2 = use_ksub2(a.K, EPI);
+        if (EPI == EPI_GELU && gelu_pair_epw16())
+            return run_pair_bn<EPI, 16>(bn, k2, A, a_rows_total, W, n_wgroups, a, num_sms, s);
+        return run_pair_bn<EPI, 8>(bn, k2, A, a_rows_total, W, n_wgroups, a, num_sms, s);
     }
     return run_bn<EPI>(bn, A, a_rows_total, W, n_wgroups, a, num_sms, s);
 }
@@ -965,32 +1011,25 @@ cudaError_t launch_moe_gemm1_tc(const void* Sg, long long rows_total, const void
     return tc::run_bn<tc::EPI_GELU>(tc::pick_bn(Fe), Sg, rows_total, W1p, groups, a, num_sms, s);
 }
 
-cudaError_t launch_moe_gemm2_tc(const void* Hm, long long rows_total, const void* W2p, const float* b2, int T, int E,
-                                int e, int D, int Fe, const int* g_count, const int* g_off, const int* tile_prefix_e,
-                                const int* row_sample, const float* gates, const int* first_e, float* V,
-                                long long v_sb, long long v_st, int num_sms, int* err, unsigned long long timeout_ns,
-                                cudaStream_t s) {
+cudaError_t launch_moe_gemm2_tc(const void* Hm, long long rows_total, const void* W2p, const float* b2, void* Y,
+                                int groups, int D, int Fe, const int* g_count, const int* g_off,
+                                const int* tile_prefix, const float* row_gate, int num_sms, int* err,
+                                unsigned long long timeout_ns, cudaStream_t s) {
     tc::Args a{};
     a.N = D;
     a.K = Fe;
-    a.ngroups = T;
-    a.group_base = e;
-    a.group_stride = E;
+    a.ngroups = groups;
+    a.group_base = 0;
+    a.group_stride = 1;
     a.g_count = g_count;
     a.g_off = g_off;
-    a.tile_prefix = tile_prefix_e;
+    a.tile_prefix = tile_prefix;
     a.bias = b2;
-    a.row_sample = row_sample;
-    a.gates = gates;
-    a.first_e = first_e;
-    a.gT = T;
-    a.gE = E;
-    a.v = V;
-    a.v_sb = v_sb;
-    a.v_st = v_st;
+    a.hid = reinterpret_cast<__half*>(Y);
+    a.row_gate = row_gate;
     a.err = err;
     a.timeout_ns = timeout_ns;
-    return tc::run_bn<tc::EPI_GATED>(tc::pick_bn(D), Hm, rows_total, W2p, T * E, a, num_sms, s);
+    return tc::run_bn<tc::EPI_GATED>(tc::pick_bn(D), Hm, rows_total, W2p, groups, a, num_sms, s);
 }
 
 }  // namespace rm

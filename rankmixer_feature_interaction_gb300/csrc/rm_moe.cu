@@ -10,13 +10,13 @@
 // Pipeline (all on the launch stream, no host synchronisation):
 //   1 route       one pass over S: G = ReLU(s Wg_t + bg_t); each open (b, t, e)
 //                 claims a slot of group t E + e and copies s into it (fp16
-//                 operands for bf16 contexts); V rows with no open expert are zeroed
-//   2 tiles       128-row tile prefix sums per launch
+//                 operands for bf16 contexts)
+//   2 tiles       128-row tile prefix sums over the groups
 //   3 expert L1   variable-size grouped GEMM + bias + GELU -> Hm (packed rows)
-//   4 expert L2   one launch per expert index e (fixed order e = 0..E-1):
-//                 V[b, t] (+)= G * (Hm W2_{t,e} + b2_{t,e}), the first open
-//                 expert of (b, t) storing and the later ones adding
-// The fixed order of step 4 makes the float32 sum over experts deterministic.
+//   4 expert L2   the same over all groups, + bias, times the row's gate -> Y
+//                 (packed rows, written over the gathered rows)
+//   5 combine     V[b, t] = sum of the open experts' Y rows in ascending e
+// The fixed order of step 5 makes the float32 sum over experts deterministic.
 #include <type_traits>
 #include <vector>
 
@@ -31,11 +31,10 @@ cudaError_t launch_moe_gemm1_tc(const void* Sg, long long rows_total, const void
                                 int groups, int D, int Fe, const int* g_count, const int* g_off,
                                 const int* tile_prefix, int num_sms, int* err, unsigned long long timeout_ns,
                                 cudaStream_t s);
-cudaError_t launch_moe_gemm2_tc(const void* Hm, long long rows_total, const void* W2p, const float* b2, int T, int E,
-                                int e, int D, int Fe, const int* g_count, const int* g_off, const int* tile_prefix_e,
-                                const int* row_sample, const float* gates, const int* first_e, float* V,
-                                long long v_sb, long long v_st, int num_sms, int* err, unsigned long long timeout_ns,
-                                cudaStream_t s);
+cudaError_t launch_moe_gemm2_tc(const void* Hm, long long rows_total, const void* W2p, const float* b2, void* Y,
+                                int groups, int D, int Fe, const int* g_count, const int* g_off,
+                                const int* tile_prefix, const float* row_gate, int num_sms, int* err,
+                                unsigned long long timeout_ns, cudaStream_t s);
 
 namespace {
 
@@ -51,9 +50,8 @@ constexpr unsigned long long kMoeWaitTimeoutNs = 2000000000ull;
 // claims a slot of its group g = t E + e by an atomic on counts[g]; the slot's
 // packed row is g Bcap + slot, so the gathered rows of group g are the first
 // counts[g] rows of its fixed Bcap-row block.  The warp then copies each open
-// row into its slot, converted to the operand type.  A (sample, token) with
-// no open expert gets its V row zeroed here (the expert layer-2 launches write
-// the rows of the others; the first open expert stores, later ones add).
+// row into its slot, converted to the operand type, and records the slot
+// (slot_of[b][t][e], -1 when closed) and the gate of the packed row.
 //
 // The order of rows inside a group follows the atomics and may change from
 // run to run; no value does: each output row's arithmetic is independent of
@@ -120,8 +118,8 @@ template <typename Tin, typename Tout, int CH>
 __global__ void __launch_bounds__(kRouteWarps * 32)
 route_kernel(const Tin* __restrict__ S, long long s_sb, long long s_st, const float* __restrict__ Wg,
              const float* __restrict__ bg, float* __restrict__ gates, int* __restrict__ counts,
-             int* __restrict__ rows, int* __restrict__ first_e, Tout* __restrict__ Sg, float* __restrict__ V,
-             long long v_sb, long long v_st, int B, int T, int D, int E, int Bcap) {
+             float* __restrict__ row_gate, int* __restrict__ slot_of, Tout* __restrict__ Sg, int B, int T, int D,
+             int E, int Bcap) {
     const int t = blockIdx.y;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int my_r = lane / kRouteExp, my_e = lane % kRouteExp;
@@ -134,7 +132,6 @@ route_kernel(const Tin* __restrict__ S, long long s_sb, long long s_st, const fl
             ok[r] = b0 + r < b_end;
             row[r] = S + (long long)(ok[r] ? b0 + r : b0) * s_sb + (long long)t * s_st;
         }
-        int first = E;                               // first open expert of this lane's row (my_r)
         for (int e0 = 0; e0 < E; e0 += kRouteExp) {
             const int ne = min(kRouteExp, E - e0);
             float acc[kRouteRows * kRouteExp];
@@ -174,15 +171,14 @@ route_kernel(const Tin* __restrict__ S, long long s_sb, long long s_st, const fl
             const float g = mine ? fmaxf(acc[0] + __ldg(bg + (size_t)t * E + e), 0.f) : 0.f;
             if (mine) gates[((size_t)b * T + t) * E + e] = g;
             const bool open = mine && g > 0.f;
-            int slot = 0;
+            int slot = -1;
             if (open) {
                 const int grp = t * E + e;
                 slot = atomicAdd(counts + grp, 1);
-                rows[(size_t)grp * Bcap + slot] = b;
+                row_gate[(size_t)grp * Bcap + slot] = g;
             }
+            if (mine) slot_of[((size_t)b * T + t) * E + e] = slot;      // -1: closed
             unsigned m = __ballot_sync(0xffffffffu, open);
-            const unsigned row_bits = (m >> (my_r * kRouteExp)) & ((1u << kRouteExp) - 1u);
-            if (first == E && row_bits) first = e0 + __ffs(row_bits) - 1;
             while (m) {
                 const int l = __ffs(m) - 1;
                 m &= m - 1;
@@ -193,23 +189,13 @@ route_kernel(const Tin* __restrict__ S, long long s_sb, long long s_st, const fl
                                         Sg + ((size_t)grp * Bcap + sl) * D, D, lane);
             }
         }
-        if (my_e == 0 && ok[my_r]) first_e[(size_t)(b0 + my_r) * T + t] = first;
-        // V rows of samples with no open expert are zero
-        const unsigned closed_rows = __ballot_sync(0xffffffffu, my_e == 0 && first == E);
-#pragma unroll
-        for (int r = 0; r < kRouteRows; ++r) {
-            if (ok[r] && (closed_rows >> (r * kRouteExp)) & 1u) {
-                float* vrow = V + (long long)(b0 + r) * v_sb + (long long)t * v_st;
-                for (int c = lane; c < D; c += 32) vrow[c] = 0.f;
-            }
-        }
     }
 }
 
 // ---- 2: tile prefixes -------------------------------------------------------------
-// offsets[g] = g Bcap (fixed blocks); tile_prefix[0 .. G] over g = t E + e (expert
-// layer 1); tile_prefix[G + 1 + e (T + 1) + t] over t for fixed e (layer 2, one
-// launch per e).  One CTA, each thread a contiguous run of groups.
+// offsets[g] = g Bcap (fixed blocks); tile_prefix[0 .. G] over g = t E + e, the
+// exclusive prefix of 128-row tiles (both expert layers tile their packed rows
+// alike).  One CTA, each thread a contiguous run of groups.
 constexpr int kTilesThreads = 1024;
 
 __global__ void __launch_bounds__(kTilesThreads)
@@ -240,32 +226,21 @@ tiles_kernel(const int* __restrict__ counts, int* __restrict__ offsets, int* __r
         tile_prefix[G] = part[kTilesThreads - 1];
         offsets[G] = G * Bcap;
     }
-    for (int e = threadIdx.x; e < E; e += kTilesThreads) {
-        int* p = tile_prefix + G + 1 + e * (T + 1);
-        int acc = 0;
-        for (int t = 0; t < T; ++t) {
-            p[t] = acc;
-            acc += (counts[t * E + e] + 127) / 128;
-        }
-        p[T] = acc;
-    }
 }
 
 // ---- 6/7 on CUDA cores (float32 path and shapes the tensor-core kernel does not tile) ----
 constexpr int TM = 64, TN = 64, TK = 16;
 
-// EPI 1: out[row][n] = Gelu(acc + b1) (activation dtype), rows packed;
-// EPI 2: V[b, t] += gate (acc + b2).  Launch group j -> weight group base + j stride.
+// Packed rows of group wg = blockIdx.z, out in the operand type, same row index as A:
+// EPI 1: out[row][n] = Gelu(acc + b1);  EPI 2: out[row][n] = row_gate[row] (acc + b2).
 template <typename Tin, int EPI>
 __global__ void __launch_bounds__(256)
 moe_gemm_simt_kernel(const Tin* __restrict__ A, const Tin* __restrict__ W, const float* __restrict__ bias,
                      Tin* __restrict__ hout, const int* __restrict__ counts, const int* __restrict__ offsets,
-                     const int* __restrict__ rows, const float* __restrict__ gates, const int* __restrict__ first_e,
-                     float* __restrict__ V,
-                     long long v_sb, long long v_st, int N, int K, int T, int NE, int base, int stride) {
+                     const float* __restrict__ row_gate, int N, int K) {
     __shared__ float As[TK][TM + 4];
     __shared__ float Ws[TK][TN + 4];
-    const int wg = base + blockIdx.z * stride;
+    const int wg = blockIdx.z;
     const int M = counts[wg];
     const int m0 = blockIdx.y * TM, n0 = blockIdx.x * TN;
     if (m0 >= M) return;
@@ -303,26 +278,56 @@ moe_gemm_simt_kernel(const Tin* __restrict__ A, const Tin* __restrict__ W, const
         }
         __syncthreads();
     }
-    const int t = wg / NE, ee = wg % NE;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int m = m0 + ty + 16 * i;
         if (m >= M) continue;
-        if (EPI == 1) {
+        const float gate = EPI == 2 ? row_gate[row0 + m] : 0.f;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int n = n0 + tx + 16 * j;
-                if (n < N) hout[(size_t)(row0 + m) * N + n] = from_f32<Tin>(gelu_erf(acc[i][j] + bias[(size_t)wg * N + n]));
+        for (int j = 0; j < 4; ++j) {
+            const int n = n0 + tx + 16 * j;
+            if (n >= N) continue;
+            const float u = acc[i][j] + bias[(size_t)wg * N + n];
+            hout[(size_t)(row0 + m) * N + n] = from_f32<Tin>(EPI == 1 ? gelu_erf(u) : gate * u);
+        }
+    }
+}
+
+// ---- 5: combine -----------------------------------------------------------------------
+// V[b, t] = sum over the open experts e of (b, t), ascending, of their gated rows
+// Y[slot_of[b][t][e] of group t E + e] (zero when none is open).  One warp per
+// (b, t); each lane sums CH-column chunks in float32.
+template <typename Ty, int CH>
+__global__ void __launch_bounds__(256)
+combine_kernel(const Ty* __restrict__ Y, const int* __restrict__ slot_of, float* __restrict__ V, long long v_sb,
+               long long v_st, int B, int T, int D, int E, int Bcap) {
+    const int lane = threadIdx.x & 31;
+    const long long w0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+    for (long long r = w0; r < (long long)B * T; r += nw) {
+        const int b = (int)(r / T), t = (int)(r % T);
+        const int* so = slot_of + r * E;
+        float* vrow = V + (long long)b * v_sb + (long long)t * v_st;
+        for (int c0 = CH * lane; c0 < D; c0 += 32 * CH) {
+            float acc[CH];
+#pragma unroll
+            for (int k = 0; k < CH; ++k) acc[k] = 0.f;
+            for (int e = 0; e < E; ++e) {
+                const int sl = __ldg(so + e);
+                if (sl < 0) continue;
+                float y[CH];
+                load_chunk<Ty, CH>(Y + ((size_t)(t * E + e) * Bcap + sl) * D + c0, true, y);
+#pragma unroll
+                for (int k = 0; k < CH; ++k) acc[k] += y[k];
             }
-        } else {
-            const int b = rows[row0 + m];
-            const float gate = gates[((size_t)b * T + t) * NE + ee];
-            const bool first = first_e[(size_t)b * T + t] == ee;   // the first open expert stores
-            float* vrow = V + b * v_sb + t * v_st;
+            if constexpr (CH % 4 == 0) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int n = n0 + tx + 16 * j;
-                if (n < N) vrow[n] = fmaf(gate, acc[i][j] + bias[(size_t)wg * N + n], first ? 0.f : vrow[n]);
+                for (int q = 0; q < CH / 4; ++q)
+                    reinterpret_cast<float4*>(vrow + c0)[q] =
+                        make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < CH; ++k) vrow[c0 + k] = acc[k];
             }
         }
     }
@@ -409,17 +414,17 @@ cudaError_t moe_alloc_workspace(const MoeShape& ms, int Bcap, MoeWorkspace& ws, 
     if ((e = dalloc(&ws.gates, (size_t)Bcap * G, bytes)) != cudaSuccess) return e;
     if ((e = dalloc(&ws.counts, G, bytes)) != cudaSuccess) return e;
     if ((e = dalloc(&ws.offsets, G + 1, bytes)) != cudaSuccess) return e;
-    if ((e = dalloc(&ws.rows, G * Bcap, bytes)) != cudaSuccess) return e;
-    if ((e = dalloc(&ws.tile_prefix, G + 1 + (size_t)ms.E * (ms.T + 1), bytes)) != cudaSuccess) return e;
-    if ((e = dalloc(&ws.first_e, (size_t)Bcap * ms.T, bytes)) != cudaSuccess) return e;
+    if ((e = dalloc(&ws.row_gate, G * Bcap, bytes)) != cudaSuccess) return e;
+    if ((e = dalloc(&ws.slot_of, (size_t)Bcap * G, bytes)) != cudaSuccess) return e;
+    if ((e = dalloc(&ws.tile_prefix, G + 1, bytes)) != cudaSuccess) return e;
     if ((e = dalloc_bytes(&ws.Sg, G * Bcap * ms.D * esz, bytes)) != cudaSuccess) return e;
     if ((e = dalloc_bytes(&ws.Hm, G * Bcap * ms.Fe * esz, bytes)) != cudaSuccess) return e;
     return cudaSuccess;
 }
 
 void moe_free_workspace(MoeWorkspace& ws) {
-    cudaFree(ws.gates); cudaFree(ws.counts); cudaFree(ws.offsets); cudaFree(ws.rows); cudaFree(ws.tile_prefix);
-    cudaFree(ws.first_e); cudaFree(ws.Sg); cudaFree(ws.Hm);
+    cudaFree(ws.gates); cudaFree(ws.counts); cudaFree(ws.offsets); cudaFree(ws.row_gate); cudaFree(ws.slot_of);
+    cudaFree(ws.tile_prefix); cudaFree(ws.Sg); cudaFree(ws.Hm);
     ws = MoeWorkspace{};
 }
 
@@ -440,7 +445,7 @@ cudaError_t moe_forward(const MoeLaunch& ml, const MoeWeights& w, MoeWorkspace& 
         prof_end(h);
         return r;
     };
-    // 1-2: route (gates, slots, gather, zero rows), tile prefixes
+    // 1-2: route (gates, slots, gather), tile prefixes
     e = scoped(6 /* RM_K_MOE_ROUTE */, [&]() -> cudaError_t {
         cudaError_t r = cudaMemsetAsync(ws.counts, 0, (size_t)G * sizeof(int), s);
         if (r != cudaSuccess) return r;
@@ -450,9 +455,8 @@ cudaError_t moe_forward(const MoeLaunch& ml, const MoeWeights& w, MoeWorkspace& 
                          (s_st * esz % 16 == 0);
 #define RM_ROUTE(TIN, TOUT, CH)                                                                               \
     route_kernel<TIN, TOUT, CH><<<grid, kRouteWarps * 32, 0, s>>>((const TIN*)ml.S, s_sb, s_st, w.Wg, w.bg,    \
-                                                                   ws.gates, ws.counts, ws.rows, ws.first_e,   \
-                                                                   (TOUT*)ws.Sg,                               \
-                                                                   V, v_sb, v_st, B, T, D, E, ws.Bcap)
+                                                                   ws.gates, ws.counts, ws.row_gate,           \
+                                                                   ws.slot_of, (TOUT*)ws.Sg, B, T, D, E, ws.Bcap)
         if (ml.act == Act::F32) {
             if (vec) RM_ROUTE(float, float, 4); else RM_ROUTE(float, float, 1);
         } else if (ml.S_sample_major) {   // the caller's bf16 S
@@ -471,47 +475,64 @@ cudaError_t moe_forward(const MoeLaunch& ml, const MoeWeights& w, MoeWorkspace& 
     if (e != cudaSuccess) return e;
 
     const bool tc = moe_use_tc(ml.act, D, Fe);
-    // 6: expert layer 1
+    const dim3 sgrid1((Fe + TN - 1) / TN, (B + TM - 1) / TM, G), sgrid2((D + TN - 1) / TN, (B + TM - 1) / TM, G);
+    // 3: expert layer 1 over all groups: Hm = Gelu(Sg W1 + b1)
     e = scoped(7 /* RM_K_MOE_GEMM1 */, [&]() -> cudaError_t {
         if (tc)
             return launch_moe_gemm1_tc(ws.Sg, rows_cap, w.W1p, w.b1, ws.Hm, G, D, Fe, ws.counts, ws.offsets,
                                        ws.tile_prefix, ml.num_sms, ml.err, kMoeWaitTimeoutNs, s);
-        dim3 grid((Fe + TN - 1) / TN, (B + TM - 1) / TM, G);
         if (ml.act == Act::BF16)
-            moe_gemm_simt_kernel<__half, 1><<<grid, 256, 0, s>>>((const __half*)ws.Sg, (const __half*)w.W1p, w.b1,
-                                                                 (__half*)ws.Hm, ws.counts, ws.offsets, ws.rows,
-                                                                 nullptr, nullptr, nullptr, 0, 0, Fe, D, T, E, 0, 1);
+            moe_gemm_simt_kernel<__half, 1><<<sgrid1, 256, 0, s>>>((const __half*)ws.Sg, (const __half*)w.W1p, w.b1,
+                                                                   (__half*)ws.Hm, ws.counts, ws.offsets, nullptr,
+                                                                   Fe, D);
         else
-            moe_gemm_simt_kernel<float, 1><<<grid, 256, 0, s>>>((const float*)ws.Sg, (const float*)w.W1p, w.b1,
-                                                                (float*)ws.Hm, ws.counts, ws.offsets, ws.rows, nullptr,
-                                                                nullptr, nullptr, 0, 0, Fe, D, T, E, 0, 1);
+            moe_gemm_simt_kernel<float, 1><<<sgrid1, 256, 0, s>>>((const float*)ws.Sg, (const float*)w.W1p, w.b1,
+                                                                  (float*)ws.Hm, ws.counts, ws.offsets, nullptr, Fe,
+                                                                  D);
         return cudaGetLastError();
     });
     if (e != cudaSuccess) return e;
 
-    // 7: expert layer 2, gated accumulation, one launch per expert index
-    for (int ei = 0; ei < E; ++ei) {
-        e = scoped(8 /* RM_K_MOE_GEMM2 */, [&]() -> cudaError_t {
-            const int* tp = ws.tile_prefix + G + 1 + ei * (T + 1);
-            if (tc)
-                return launch_moe_gemm2_tc(ws.Hm, rows_cap, w.W2p, w.b2, T, E, ei, D, Fe, ws.counts, ws.offsets, tp,
-                                           ws.rows, ws.gates, ws.first_e, V, v_sb, v_st, ml.num_sms, ml.err,
-                                           kMoeWaitTimeoutNs, s);
-            dim3 grid((D + TN - 1) / TN, (B + TM - 1) / TM, T);
-            if (ml.act == Act::BF16)
-                moe_gemm_simt_kernel<__half, 2><<<grid, 256, 0, s>>>((const __half*)ws.Hm, (const __half*)w.W2p, w.b2,
-                                                                     nullptr, ws.counts, ws.offsets, ws.rows,
-                                                                     ws.gates, ws.first_e, V, v_sb, v_st, D, Fe, T, E,
-                                                                     ei, E);
+    // 4: expert layer 2 over all groups: Y = gate (Hm W2 + b2), one packed row per open
+    //    (b, t, e), written over the gathered rows (no longer needed)
+    e = scoped(8 /* RM_K_MOE_GEMM2 */, [&]() -> cudaError_t {
+        if (tc)
+            return launch_moe_gemm2_tc(ws.Hm, rows_cap, w.W2p, w.b2, ws.Sg, G, D, Fe, ws.counts, ws.offsets,
+                                       ws.tile_prefix, ws.row_gate, ml.num_sms, ml.err, kMoeWaitTimeoutNs, s);
+        if (ml.act == Act::BF16)
+            moe_gemm_simt_kernel<__half, 2><<<sgrid2, 256, 0, s>>>((const __half*)ws.Hm, (const __half*)w.W2p, w.b2,
+                                                                   (__half*)ws.Sg, ws.counts, ws.offsets, ws.row_gate,
+                                                                   D, Fe);
+        else
+            moe_gemm_simt_kernel<float, 2><<<sgrid2, 256, 0, s>>>((const float*)ws.Hm, (const float*)w.W2p, w.b2,
+                                                                  (float*)ws.Sg, ws.counts, ws.offsets, ws.row_gate,
+                                                                  D, Fe);
+        return cudaGetLastError();
+    });
+    if (e != cudaSuccess) return e;
+
+    // 5: V[b, t] = sum of the open experts' rows, ascending e
+    return scoped(10 /* RM_K_MOE_COMBINE */, [&]() -> cudaError_t {
+        int grid = (int)(((long long)B * T * 32 + 255) / 256);
+        if (grid > ml.num_sms * 16) grid = ml.num_sms * 16;
+        const bool vec = D % 8 == 0 && (v_sb % 4 == 0) && (v_st % 4 == 0) && ((uintptr_t)V % 16 == 0);
+        if (ml.act == Act::BF16) {
+            if (vec)
+                combine_kernel<__half, 8><<<grid, 256, 0, s>>>((const __half*)ws.Sg, ws.slot_of, V, v_sb, v_st, B, T,
+                                                               D, E, ws.Bcap);
             else
-                moe_gemm_simt_kernel<float, 2><<<grid, 256, 0, s>>>((const float*)ws.Hm, (const float*)w.W2p, w.b2,
-                                                                    nullptr, ws.counts, ws.offsets, ws.rows, ws.gates,
-                                                                    ws.first_e, V, v_sb, v_st, D, Fe, T, E, ei, E);
-            return cudaGetLastError();
-        });
-        if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
+                combine_kernel<__half, 1><<<grid, 256, 0, s>>>((const __half*)ws.Sg, ws.slot_of, V, v_sb, v_st, B, T,
+                                                               D, E, ws.Bcap);
+        } else {
+            if (vec)
+                combine_kernel<float, 4><<<grid, 256, 0, s>>>((const float*)ws.Sg, ws.slot_of, V, v_sb, v_st, B, T,
+                                                              D, E, ws.Bcap);
+            else
+                combine_kernel<float, 1><<<grid, 256, 0, s>>>((const float*)ws.Sg, ws.slot_of, V, v_sb, v_st, B, T,
+                                                              D, E, ws.Bcap);
+        }
+        return cudaGetLastError();
+    });
 }
 
 cudaError_t moe_residual_z(Act act, const float* V, const void* S, void* Z, int B, int T, int D, int Bcap,

@@ -36,10 +36,11 @@ struct MoeWorkspace {
     float* gates = nullptr;     // [B][T][E]
     int* counts = nullptr;      // [T*E] open samples per group g = t*E + e
     int* offsets = nullptr;     // [T*E + 1] first packed row of each group: g * Bcap
-    int* rows = nullptr;        // [T*E][Bcap] sample index of each gathered row (first counts[g] used)
-    int* tile_prefix = nullptr; // [T*E + 1 + E*(T + 1)] exclusive prefixes of 128-row tiles per launch
-    int* first_e = nullptr;     // [Bcap][T] first open expert of (b, t) (E when none)
-    void* Sg = nullptr;         // [T*E*Bcap][D]  gathered LN1 rows (operand type)
+    float* row_gate = nullptr;  // [T*E][Bcap] gate of each packed row (first counts[g] used)
+    int* slot_of = nullptr;     // [Bcap][T][E] packed row of (b, t, e) inside group t*E + e, -1 when closed
+    int* tile_prefix = nullptr; // [T*E + 1] exclusive prefix of 128-row tiles over the groups
+    void* Sg = nullptr;         // [T*E*Bcap][D]  gathered LN1 rows (operand type); after expert
+                                //                 layer 1 it holds the gated expert outputs Y
     void* Hm = nullptr;         // [T*E*Bcap][Fe] expert hidden activations (operand type)
 };
 

@@ -425,14 +425,20 @@ print("ok")
 """
 
 
-@pytest.mark.parametrize("pair", ["0", "1", "2"])
+@pytest.mark.parametrize("tuning", [{},                                            # pairs, 2 k-blocks per stage
+                                    {"RM_GEMM_PAIR": "0"},                          # one CTA per tile
+                                    {"RM_GEMM_PAIR": "2"},                          # pairs for GEMM2 only
+                                    {"RM_GEMM_KSUB": "1"},                          # one k-block per stage
+                                    {"RM_GEMM1_EPW": "16"},                         # 16 GELU epilogue warps
+                                    {"RM_GEMM1_EPW": "16", "RM_GEMM_KSUB": "1"}])
 @pytest.mark.parametrize("shape", [(4, 256, 2, 2, 300), (2, 192, 2, 1, 300)])
-def test_every_gemm_tile_dispatch(pair, shape):
+def test_every_gemm_tile_dispatch(tuning, shape):
     import os
     import subprocess
     import sys
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    env = dict(os.environ, RM_GEMM_PAIR=pair)
+    env = {k: v for k, v in os.environ.items() if k not in ("RM_GEMM_PAIR", "RM_GEMM_KSUB", "RM_GEMM1_EPW")}
+    env.update(tuning)
     r = subprocess.run([sys.executable, "-c", _DISPATCH_CHILD.format(root=root, shape=shape)], env=env, cwd=root,
                        capture_output=True, text=True, timeout=600)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
