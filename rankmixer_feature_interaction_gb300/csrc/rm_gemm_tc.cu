@@ -571,7 +571,8 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
 
     const int kblocks = args.K / (BK * KSUB);
-    const long long tiles = args.tiles;
+    const long long tiles =
+        args.tile_prefix ? (long long)__ldg(args.tile_prefix + args.ngroups) * args.n_tiles : args.tiles;
 
     if (warp == 0) {
         // ---------------------------- TMA producer (both CTAs) ----------------------------
@@ -823,10 +824,15 @@ cudaError_t run_pair(const void* A, long long a_rows_total, const void* W, int n
     using C = Cfg2<BN, EPW, KSUB>;
     if (a.K % (BK * KSUB) != 0) return cudaErrorInvalidValue;
     a.n_tiles = a.N / BN;
-    a.m_tiles = (a.M + BM2 - 1) / BM2;
-    a.tiles = (long long)a.ngroups * a.m_tiles * a.n_tiles;
-    a.n_fastest = a.M > a.N ? 1 : 0;
-    if (a.tiles == 0) return cudaSuccess;
+    if (a.tile_prefix == nullptr) {        // uniform groups
+        a.m_tiles = (a.M + BM2 - 1) / BM2;
+        a.tiles = (long long)a.ngroups * a.m_tiles * a.n_tiles;
+        a.n_fastest = a.M > a.N ? 1 : 0;
+        if (a.tiles == 0) return cudaSuccess;
+    } else {                               // variable groups: a.tile_prefix counts 256-row tiles,
+        a.tiles = 0;                       // the kernel reads the total; persistent grid
+        a.hid_tma = 0;
+    }
     CUtensorMap mA, mB, mC;
     if (!make_map(&mA, A, a.K, a_rows_total, 1, a_rows_total, 128)) return cudaErrorInvalidValue;
     if (!make_map(&mB, W, a.K, a.N, n_wgroups, a.N, BN / 2)) return cudaErrorInvalidValue;
@@ -859,7 +865,7 @@ cudaError_t run_pair(const void* A, long long a_rows_total, const void* W, int n
         }
         max_pairs = n;
     }
-    long long pairs = a.tiles < max_pairs ? a.tiles : max_pairs;
+    long long pairs = (a.tile_prefix == nullptr && a.tiles < max_pairs) ? a.tiles : max_pairs;
     k<<<(int)(2 * pairs), C::THREADS, C::SMEM_BYTES, s>>>(mA, mB, mC, a);
     return cudaGetLastError();
 }
@@ -993,8 +999,8 @@ cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, c
 
 cudaError_t launch_moe_gemm1_tc(const void* Sg, long long rows_total, const void* W1p, const float* b1, void* Hm,
                                 int groups, int D, int Fe, const int* g_count, const int* g_off,
-                                const int* tile_prefix, int num_sms, int* err, unsigned long long timeout_ns,
-                                cudaStream_t s) {
+                                const int* tile_prefix, const int* tile_prefix256, int num_sms, int* err,
+                                unsigned long long timeout_ns, cudaStream_t s) {
     tc::Args a{};
     a.N = Fe;
     a.K = D;
@@ -1008,13 +1014,18 @@ cudaError_t launch_moe_gemm1_tc(const void* Sg, long long rows_total, const void
     a.hid = reinterpret_cast<__half*>(Hm);
     a.err = err;
     a.timeout_ns = timeout_ns;
+    if (tile_prefix256 && tc::pick_bn(Fe) >= 128) {     // CTA-pair tiles over 256-row tiles
+        a.tile_prefix = tile_prefix256;
+        return tc::run_pair_bn<tc::EPI_GELU, 8>(tc::pick_bn(Fe), tc::use_ksub2(D, tc::EPI_GELU), Sg, rows_total,
+                                                W1p, groups, a, num_sms, s);
+    }
     return tc::run_bn<tc::EPI_GELU>(tc::pick_bn(Fe), Sg, rows_total, W1p, groups, a, num_sms, s);
 }
 
 cudaError_t launch_moe_gemm2_tc(const void* Hm, long long rows_total, const void* W2p, const float* b2, void* Y,
                                 int groups, int D, int Fe, const int* g_count, const int* g_off,
-                                const int* tile_prefix, const float* row_gate, int num_sms, int* err,
-                                unsigned long long timeout_ns, cudaStream_t s) {
+                                const int* tile_prefix, const int* tile_prefix256, const float* row_gate,
+                                int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s) {
     tc::Args a{};
     a.N = D;
     a.K = Fe;
@@ -1029,6 +1040,11 @@ cudaError_t launch_moe_gemm2_tc(const void* Hm, long long rows_total, const void
     a.row_gate = row_gate;
     a.err = err;
     a.timeout_ns = timeout_ns;
+    if (tile_prefix256 && tc::pick_bn(D) >= 128) {      // CTA-pair tiles over 256-row tiles
+        a.tile_prefix = tile_prefix256;
+        return tc::run_pair_bn<tc::EPI_GATED, 8>(tc::pick_bn(D), tc::use_ksub2(Fe, tc::EPI_GATED), Hm, rows_total,
+                                                 W2p, groups, a, num_sms, s);
+    }
     return tc::run_bn<tc::EPI_GATED>(tc::pick_bn(D), Hm, rows_total, W2p, groups, a, num_sms, s);
 }
 

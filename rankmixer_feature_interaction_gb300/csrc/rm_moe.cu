@@ -29,16 +29,17 @@ namespace rm {
 // tcgen05 launchers (rm_gemm_tc.cu)
 cudaError_t launch_moe_gemm1_tc(const void* Sg, long long rows_total, const void* W1p, const float* b1, void* Hm,
                                 int groups, int D, int Fe, const int* g_count, const int* g_off,
-                                const int* tile_prefix, int num_sms, int* err, unsigned long long timeout_ns,
-                                cudaStream_t s);
+                                const int* tile_prefix, const int* tile_prefix256, int num_sms, int* err,
+                                unsigned long long timeout_ns, cudaStream_t s);
 cudaError_t launch_moe_gemm2_tc(const void* Hm, long long rows_total, const void* W2p, const float* b2, void* Y,
                                 int groups, int D, int Fe, const int* g_count, const int* g_off,
-                                const int* tile_prefix, const float* row_gate, int num_sms, int* err,
-                                unsigned long long timeout_ns, cudaStream_t s);
+                                const int* tile_prefix, const int* tile_prefix256, const float* row_gate,
+                                int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s);
 
 namespace {
 
 constexpr unsigned long long kMoeWaitTimeoutNs = 2000000000ull;
+constexpr int kMoePairMinBatch = 512;
 
 // ---- 1: route (gates, slot claim, gather) ------------------------------------------
 // One warp takes RQ = 4 samples of one token t at a time.  Each lane walks its
@@ -195,35 +196,45 @@ route_kernel(const Tin* __restrict__ S, long long s_sb, long long s_st, const fl
 // ---- 2: tile prefixes -------------------------------------------------------------
 // offsets[g] = g Bcap (fixed blocks); tile_prefix[0 .. G] over g = t E + e, the
 // exclusive prefix of 128-row tiles (both expert layers tile their packed rows
-// alike).  One CTA, each thread a contiguous run of groups.
+// alike), and tile_prefix256 the same over 256-row tiles (CTA-pair tiles).
+// One CTA, each thread a contiguous run of groups.
 constexpr int kTilesThreads = 1024;
 
 __global__ void __launch_bounds__(kTilesThreads)
-tiles_kernel(const int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ tile_prefix, int T, int E,
-             int Bcap) {
-    __shared__ int part[kTilesThreads];
+tiles_kernel(const int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ tile_prefix,
+             int* __restrict__ tile_prefix256, int T, int E, int Bcap) {
+    __shared__ int part[2][kTilesThreads];
     const int G = T * E;
     const int per = (G + kTilesThreads - 1) / kTilesThreads;
     const int g0 = threadIdx.x * per, g1 = min(G, g0 + per);
-    int sum = 0;
-    for (int g = g0; g < g1; ++g) sum += (counts[g] + 127) / 128;
-    part[threadIdx.x] = sum;
+    int sum = 0, sum2 = 0;
+    for (int g = g0; g < g1; ++g) {
+        sum += (counts[g] + 127) / 128;
+        sum2 += (counts[g] + 255) / 256;
+    }
+    part[0][threadIdx.x] = sum;
+    part[1][threadIdx.x] = sum2;
     __syncthreads();
-    // inclusive scan of the per-thread sums (Hillis-Steele)
+    // inclusive scans of the per-thread sums (Hillis-Steele)
     for (int o = 1; o < kTilesThreads; o <<= 1) {
-        const int v = threadIdx.x >= o ? part[threadIdx.x - o] : 0;
+        const int v = threadIdx.x >= o ? part[0][threadIdx.x - o] : 0;
+        const int v2 = threadIdx.x >= o ? part[1][threadIdx.x - o] : 0;
         __syncthreads();
-        part[threadIdx.x] += v;
+        part[0][threadIdx.x] += v;
+        part[1][threadIdx.x] += v2;
         __syncthreads();
     }
-    int run = part[threadIdx.x] - sum;
+    int run = part[0][threadIdx.x] - sum, run2 = part[1][threadIdx.x] - sum2;
     for (int g = g0; g < g1; ++g) {
         offsets[g] = g * Bcap;
         tile_prefix[g] = run;
+        tile_prefix256[g] = run2;
         run += (counts[g] + 127) / 128;
+        run2 += (counts[g] + 255) / 256;
     }
     if (threadIdx.x == kTilesThreads - 1) {
-        tile_prefix[G] = part[kTilesThreads - 1];
+        tile_prefix[G] = part[0][kTilesThreads - 1];
+        tile_prefix256[G] = part[1][kTilesThreads - 1];
         offsets[G] = G * Bcap;
     }
 }
@@ -417,6 +428,7 @@ cudaError_t moe_alloc_workspace(const MoeShape& ms, int Bcap, MoeWorkspace& ws, 
     if ((e = dalloc(&ws.row_gate, G * Bcap, bytes)) != cudaSuccess) return e;
     if ((e = dalloc(&ws.slot_of, (size_t)Bcap * G, bytes)) != cudaSuccess) return e;
     if ((e = dalloc(&ws.tile_prefix, G + 1, bytes)) != cudaSuccess) return e;
+    if ((e = dalloc(&ws.tile_prefix256, G + 1, bytes)) != cudaSuccess) return e;
     if ((e = dalloc_bytes(&ws.Sg, G * Bcap * ms.D * esz, bytes)) != cudaSuccess) return e;
     if ((e = dalloc_bytes(&ws.Hm, G * Bcap * ms.Fe * esz, bytes)) != cudaSuccess) return e;
     return cudaSuccess;
@@ -424,7 +436,7 @@ cudaError_t moe_alloc_workspace(const MoeShape& ms, int Bcap, MoeWorkspace& ws, 
 
 void moe_free_workspace(MoeWorkspace& ws) {
     cudaFree(ws.gates); cudaFree(ws.counts); cudaFree(ws.offsets); cudaFree(ws.row_gate); cudaFree(ws.slot_of);
-    cudaFree(ws.tile_prefix); cudaFree(ws.Sg); cudaFree(ws.Hm);
+    cudaFree(ws.tile_prefix); cudaFree(ws.tile_prefix256); cudaFree(ws.Sg); cudaFree(ws.Hm);
     ws = MoeWorkspace{};
 }
 
@@ -465,7 +477,8 @@ cudaError_t moe_forward(const MoeLaunch& ml, const MoeWeights& w, MoeWorkspace& 
             if (vec) RM_ROUTE(__half, __half, 8); else RM_ROUTE(__half, __half, 1);
         }
 #undef RM_ROUTE
-        tiles_kernel<<<1, kTilesThreads, 0, s>>>(ws.counts, ws.offsets, ws.tile_prefix, T, E, ws.Bcap);
+        tiles_kernel<<<1, kTilesThreads, 0, s>>>(ws.counts, ws.offsets, ws.tile_prefix, ws.tile_prefix256, T, E,
+                                                 ws.Bcap);
         if (gates_out) {
             r = cudaMemcpyAsync(gates_out, ws.gates, (size_t)B * G * sizeof(float), cudaMemcpyDeviceToDevice, s);
             if (r != cudaSuccess) return r;
@@ -475,12 +488,15 @@ cudaError_t moe_forward(const MoeLaunch& ml, const MoeWeights& w, MoeWorkspace& 
     if (e != cudaSuccess) return e;
 
     const bool tc = moe_use_tc(ml.act, D, Fe);
+    // CTA-pair tiles (256 rows) when the groups are large: each expert opens for
+    // about a quarter of the batch, so from B = 512 on a group holds ~128+ rows
+    const int* tp256 = B >= kMoePairMinBatch ? ws.tile_prefix256 : nullptr;
     const dim3 sgrid1((Fe + TN - 1) / TN, (B + TM - 1) / TM, G), sgrid2((D + TN - 1) / TN, (B + TM - 1) / TM, G);
     // 3: expert layer 1 over all groups: Hm = Gelu(Sg W1 + b1)
     e = scoped(7 /* RM_K_MOE_GEMM1 */, [&]() -> cudaError_t {
         if (tc)
             return launch_moe_gemm1_tc(ws.Sg, rows_cap, w.W1p, w.b1, ws.Hm, G, D, Fe, ws.counts, ws.offsets,
-                                       ws.tile_prefix, ml.num_sms, ml.err, kMoeWaitTimeoutNs, s);
+                                       ws.tile_prefix, tp256, ml.num_sms, ml.err, kMoeWaitTimeoutNs, s);
         if (ml.act == Act::BF16)
             moe_gemm_simt_kernel<__half, 1><<<sgrid1, 256, 0, s>>>((const __half*)ws.Sg, (const __half*)w.W1p, w.b1,
                                                                    (__half*)ws.Hm, ws.counts, ws.offsets, nullptr,
@@ -498,7 +514,7 @@ cudaError_t moe_forward(const MoeLaunch& ml, const MoeWeights& w, MoeWorkspace& 
     e = scoped(8 /* RM_K_MOE_GEMM2 */, [&]() -> cudaError_t {
         if (tc)
             return launch_moe_gemm2_tc(ws.Hm, rows_cap, w.W2p, w.b2, ws.Sg, G, D, Fe, ws.counts, ws.offsets,
-                                       ws.tile_prefix, ws.row_gate, ml.num_sms, ml.err, kMoeWaitTimeoutNs, s);
+                                       ws.tile_prefix, tp256, ws.row_gate, ml.num_sms, ml.err, kMoeWaitTimeoutNs, s);
         if (ml.act == Act::BF16)
             moe_gemm_simt_kernel<__half, 2><<<sgrid2, 256, 0, s>>>((const __half*)ws.Hm, (const __half*)w.W2p, w.b2,
                                                                    (__half*)ws.Sg, ws.counts, ws.offsets, ws.row_gate,

@@ -39,6 +39,7 @@ struct MoeWorkspace {
     float* row_gate = nullptr;  // [T*E][Bcap] gate of each packed row (first counts[g] used)
     int* slot_of = nullptr;     // [Bcap][T][E] packed row of (b, t, e) inside group t*E + e, -1 when closed
     int* tile_prefix = nullptr; // [T*E + 1] exclusive prefix of 128-row tiles over the groups
+    int* tile_prefix256 = nullptr; // [T*E + 1] the same over 256-row tiles
     void* Sg = nullptr;         // [T*E*Bcap][D]  gathered LN1 rows (operand type); after expert
                                 //                 layer 1 it holds the gated expert outputs Y
     void* Hm = nullptr;         // [T*E*Bcap][Fe] expert hidden activations (operand type)

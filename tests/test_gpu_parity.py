@@ -315,7 +315,8 @@ def test_moe_pffn_small(dtype, path, T, D, E, Fe, B):
     check(V, V_ref, dtype, "MoE V")
 
 
-@pytest.mark.parametrize("dtype,T,D,E,Fe,B", [("bf16", 2, 128, 12, 128, 131),    # two 8-expert router slices
+@pytest.mark.parametrize("dtype,T,D,E,Fe,B", [("bf16", 2, 256, 4, 256, 600),    # CTA-pair expert tiles (B >= 512)
+                                               ("bf16", 2, 128, 12, 128, 131),    # two 8-expert router slices
                                                ("bf16", 4, 36, 4, 64, 37),       # rows not in 16-byte chunks
                                                ("f32", 2, 8, 9, 16, 50)])        # fp32, E > 8, B % 4 != 0
 def test_moe_router_shapes_and_determinism(dtype, T, D, E, Fe, B):
