@@ -42,7 +42,14 @@ L2_BYTES = 129 * 1024 * 1024
 KERNEL_SOURCES = ("rankmixer_feature_interaction_gb300/csrc/rm_gemm_tc.cu",
                   "rankmixer_feature_interaction_gb300/csrc/rm_common.cuh",
                   "rankmixer_feature_interaction_gb300/csrc/rm_internal.h")
-TRAFFIC = {}
+TRAFFIC = {
+    # ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum on
+    # "bench.py --steps 3 --warmup 3" (and --config moe_1b), averaged over the captured launches
+    ("rankmixer_1b", 4096, 2, "gemm1"): (2571101696, "288a7442a01e56256ac6151f6a5a24d75b8ae3d5ff8f4047af256ca0585e93ce"),
+    ("rankmixer_1b", 4096, 2, "gemm2"): (3740605440, "288a7442a01e56256ac6151f6a5a24d75b8ae3d5ff8f4047af256ca0585e93ce"),
+    ("moe_1b", 4096, 1, "moe_gemm1"): (4680933888, "288a7442a01e56256ac6151f6a5a24d75b8ae3d5ff8f4047af256ca0585e93ce"),
+    ("moe_1b", 4096, 1, "moe_gemm2"): (4865119488, "288a7442a01e56256ac6151f6a5a24d75b8ae3d5ff8f4047af256ca0585e93ce"),
+}
 
 
 def kernel_source_digest() -> str:
