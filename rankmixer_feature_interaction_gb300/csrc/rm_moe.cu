@@ -80,6 +80,14 @@ __device__ __forceinline__ void load_chunk(const Tin* p, bool ok, float (&x)[CH]
     }
 }
 
+// 8 16-bit values (bf16 or fp16) of a 16-byte chunk -> float
+template <typename Tin>
+__device__ __forceinline__ void to_f32x8_any(const uint4 v, float (&x)[8]) {
+    const Tin* h = reinterpret_cast<const Tin*>(&v);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) x[k] = to_f32(h[k]);
+}
+
 // CH consecutive floats (16-byte loads when CH is a multiple of 4)
 template <int CH>
 __device__ __forceinline__ void load_wf(const float* p, float (&w)[CH]) {
@@ -188,6 +196,117 @@ route_kernel(const Tin* __restrict__ S, long long s_sb, long long s_st, const fl
                 const int grp = t * E + e0 + l % kRouteExp;
                 copy_row<Tin, Tout, CH>(S + (long long)(b0 + r) * s_sb + (long long)t * s_st,
                                         Sg + ((size_t)grp * Bcap + sl) * D, D, lane);
+            }
+        }
+    }
+}
+
+// Register-resident variant for 16-bit S with D = 256 NCH (NCH <= 8) and E <= 8
+// (one expert slice): a warp takes 2 samples of token t per pass and holds
+// both rows in registers (NCH 16-byte chunks per lane each), so the copies into
+// the expert groups are stores only.  The 2 x 8 dot products reduce in 16
+// shuffles; lane l then holds the sum for row (l >> 4) & 1, expert (l >> 1) & 7
+// (lanes 2v and 2v + 1 hold the same value; the even one acts).
+constexpr int kRoute2Rows = 2;
+
+template <typename Tin, int NCH>
+__global__ void __launch_bounds__(kRouteWarps * 32)
+route2_kernel(const Tin* __restrict__ S, long long s_sb, long long s_st, const float* __restrict__ Wg,
+              const float* __restrict__ bg, float* __restrict__ gates, int* __restrict__ counts,
+              float* __restrict__ row_gate, int* __restrict__ slot_of, __half* __restrict__ Sg, int B, int T,
+              int D, int E, int Bcap) {
+    static_assert(sizeof(Tin) == 2, "16-bit rows");
+    const int t = blockIdx.y;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int my_r = (lane >> 4) & 1, my_e = (lane >> 1) & 7;
+    const bool lead = (lane & 1) == 0;
+    const int b_end = min(B, (int)(blockIdx.x + 1) * kRouteSamplesPerCta);
+    for (int b0 = blockIdx.x * kRouteSamplesPerCta + warp * kRoute2Rows; b0 < b_end;
+         b0 += kRouteWarps * kRoute2Rows) {
+        const bool ok0 = b0 < b_end, ok1 = b0 + 1 < b_end;
+        const Tin* row0 = S + (long long)b0 * s_sb + (long long)t * s_st;
+        const Tin* row1 = S + (long long)(ok1 ? b0 + 1 : b0) * s_sb + (long long)t * s_st;
+        uint4 h0[NCH], h1[NCH];              // the rows: raw, then fp16
+#pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+            h0[i] = __ldg(reinterpret_cast<const uint4*>(row0 + 8 * lane + 256 * i));
+            h1[i] = ok1 ? __ldg(reinterpret_cast<const uint4*>(row1 + 8 * lane + 256 * i)) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        {
+            const int e0 = 0, ne = E;
+            float acc[2 * kRouteExp];
+#pragma unroll
+            for (int i = 0; i < 2 * kRouteExp; ++i) acc[i] = 0.f;
+            const float* wt = Wg + ((size_t)t * E + e0) * D + 8 * lane;
+#pragma unroll
+            for (int i = 0; i < NCH; ++i) {
+                float x0[8], x1[8];
+                to_f32x8_any<Tin>(h0[i], x0);
+                to_f32x8_any<Tin>(h1[i], x1);
+#pragma unroll
+                for (int e = 0; e < kRouteExp; ++e) {
+                    if (e < ne) {
+                        float w[8];
+                        load_wf<8>(wt + (size_t)e * D + 256 * i, w);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            acc[e] = fmaf(x0[k], w[k], acc[e]);
+                            acc[kRouteExp + e] = fmaf(x1[k], w[k], acc[kRouteExp + e]);
+                        }
+                    }
+                }
+            }
+            // 16 values: halve by lane bits 4, 3, 2, 1, then add the pair (bit 0)
+#pragma unroll
+            for (int o = 16; o >= 2; o >>= 1) {
+                const bool upper = (lane & o) != 0;
+                const int half = o / 2;
+#pragma unroll
+                for (int i = 0; i < half; ++i) {
+                    const float send = upper ? acc[i] : acc[i + half];
+                    const float keep = upper ? acc[i + half] : acc[i];
+                    acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+            }
+            acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 1);
+            const int b = b0 + my_r, e = e0 + my_e;
+            const bool mine = lead && my_e < ne && (my_r == 0 ? ok0 : ok1);
+            const float g = mine ? fmaxf(acc[0] + __ldg(bg + (size_t)t * E + e), 0.f) : 0.f;
+            if (mine) gates[((size_t)b * T + t) * E + e] = g;
+            const bool open = mine && g > 0.f;
+            int slot = -1;
+            if (open) {
+                const int grp = t * E + e;
+                slot = atomicAdd(counts + grp, 1);
+                row_gate[(size_t)grp * Bcap + slot] = g;
+            }
+            if (mine) slot_of[((size_t)b * T + t) * E + e] = slot;
+            if (!std::is_same_v<Tin, __half>) {     // rows to fp16 for the copies
+#pragma unroll
+                for (int i = 0; i < NCH; ++i) {
+                    float x[8];
+                    to_f32x8_any<Tin>(h0[i], x);
+                    h0[i] = make_uint4(pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]),
+                                       pack_f16x2(x[6], x[7]));
+                    to_f32x8_any<Tin>(h1[i], x);
+                    h1[i] = make_uint4(pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]),
+                                       pack_f16x2(x[6], x[7]));
+                }
+            }
+            unsigned m = __ballot_sync(0xffffffffu, open);
+            while (m) {
+                const int l = __ffs(m) - 1;
+                m &= m - 1;
+                const int sl = __shfl_sync(0xffffffffu, slot, l);
+                const int grp = t * E + e0 + ((l >> 1) & 7);
+                __half* dst = Sg + ((size_t)grp * Bcap + sl) * D + 8 * lane;
+                if (((l >> 4) & 1) == 0) {
+#pragma unroll
+                    for (int i = 0; i < NCH; ++i) *reinterpret_cast<uint4*>(dst + 256 * i) = h0[i];
+                } else {
+#pragma unroll
+                    for (int i = 0; i < NCH; ++i) *reinterpret_cast<uint4*>(dst + 256 * i) = h1[i];
+                }
             }
         }
     }
@@ -469,13 +588,36 @@ cudaError_t moe_forward(const MoeLaunch& ml, const MoeWeights& w, MoeWorkspace& 
     route_kernel<TIN, TOUT, CH><<<grid, kRouteWarps * 32, 0, s>>>((const TIN*)ml.S, s_sb, s_st, w.Wg, w.bg,    \
                                                                    ws.gates, ws.counts, ws.row_gate,           \
                                                                    ws.slot_of, (TOUT*)ws.Sg, B, T, D, E, ws.Bcap)
+        const int nch = D / 256;
+        const bool regs = ml.act != Act::F32 && vec && E <= kRouteExp && D % 256 == 0 && nch >= 1 && nch <= 8;
+#define RM_ROUTE2(TIN, NCH)                                                                                  \
+    route2_kernel<TIN, NCH><<<grid, kRouteWarps * 32, 0, s>>>((const TIN*)ml.S, s_sb, s_st, w.Wg, w.bg, ws.gates, \
+                                                              ws.counts, ws.row_gate, ws.slot_of, (__half*)ws.Sg,  \
+                                                              B, T, D, E, ws.Bcap)
+#define RM_ROUTE2_N(TIN)                                                                                     \
+    switch (nch) {                                                                                           \
+        case 1: RM_ROUTE2(TIN, 1); break;                                                                    \
+        case 2: RM_ROUTE2(TIN, 2); break;                                                                    \
+        case 3: RM_ROUTE2(TIN, 3); break;                                                                    \
+        case 4: RM_ROUTE2(TIN, 4); break;                                                                    \
+        case 5: RM_ROUTE2(TIN, 5); break;                                                                    \
+        case 6: RM_ROUTE2(TIN, 6); break;                                                                    \
+        case 7: RM_ROUTE2(TIN, 7); break;                                                                    \
+        default: RM_ROUTE2(TIN, 8); break;                                                                   \
+    }
         if (ml.act == Act::F32) {
             if (vec) RM_ROUTE(float, float, 4); else RM_ROUTE(float, float, 1);
         } else if (ml.S_sample_major) {   // the caller's bf16 S
-            if (vec) RM_ROUTE(__nv_bfloat16, __half, 8); else RM_ROUTE(__nv_bfloat16, __half, 1);
+            if (regs) { RM_ROUTE2_N(__nv_bfloat16) }
+            else if (vec) RM_ROUTE(__nv_bfloat16, __half, 8);
+            else RM_ROUTE(__nv_bfloat16, __half, 1);
         } else {                          // the stack's fp16 S
-            if (vec) RM_ROUTE(__half, __half, 8); else RM_ROUTE(__half, __half, 1);
+            if (regs) { RM_ROUTE2_N(__half) }
+            else if (vec) RM_ROUTE(__half, __half, 8);
+            else RM_ROUTE(__half, __half, 1);
         }
+#undef RM_ROUTE2_N
+#undef RM_ROUTE2
 #undef RM_ROUTE
         tiles_kernel<<<1, kTilesThreads, 0, s>>>(ws.counts, ws.offsets, ws.tile_prefix, ws.tile_prefix256, T, E,
                                                  ws.Bcap);
