@@ -369,7 +369,10 @@ pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             bool ok = true;
             for (long long tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
                 const TileCoord tc = decode_tile(tile, args);
-                const int arow = (int)(tc.row0 + (long long)tc.mb * BM);
+                // A: uniform groups through a [groups][M][K] map (rows past M of a group
+                // read as zeros without a memory access); variable groups as packed rows
+                const int arow = args.tile_prefix ? (int)(tc.row0 + (long long)tc.mb * BM) : tc.mb * BM;
+                const int agrp = args.tile_prefix ? 0 : tc.j;
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, args.err, args.timeout_ns)) {
                         ok = false;
@@ -377,7 +380,7 @@ pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
                     if (lane == 0) {
                         mbar_arrive_expect_tx(full_bar(stage), (uint32_t)C::STAGE_BYTES);
-                        tma_load_3d(&tmA, sA + stage * C::A_BYTES, full_bar(stage), kb * BK, arow, 0);
+                        tma_load_3d(&tmA, sA + stage * C::A_BYTES, full_bar(stage), kb * BK, arow, agrp);
                         tma_load_3d(&tmB, sB + stage * C::B_BYTES, full_bar(stage), kb * BK, tc.nb * BN, tc.wg);
                     }
                     __syncwarp();
@@ -582,7 +585,9 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             bool ok = true;
             for (long long tile = pair; ok && tile < tiles; tile += npairs) {
                 const TileCoord tc = decode_tile(tile, args);
-                const int arow = (int)(tc.row0 + (long long)tc.mb * BM2 + 128 * (int)rank);
+                const int arow = args.tile_prefix ? (int)(tc.row0 + (long long)tc.mb * BM2 + 128 * (int)rank)
+                                                  : tc.mb * BM2 + 128 * (int)rank;
+                const int agrp = args.tile_prefix ? 0 : tc.j;
                 const int brow = tc.nb * BN + (BN / 2) * (int)rank;
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, args.err, args.timeout_ns)) {
@@ -595,7 +600,7 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
 #pragma unroll
                         for (int ks = 0; ks < KSUB; ++ks) {
                             const int kx = (kb * KSUB + ks) * BK;
-                            tma_load_3d_pair(&tmA, sA + stage * C::A_BYTES + ks * C::A_SUB, fb, kx, arow, 0);
+                            tma_load_3d_pair(&tmA, sA + stage * C::A_BYTES + ks * C::A_SUB, fb, kx, arow, agrp);
                             tma_load_3d_pair(&tmB, sB + stage * C::B_BYTES + ks * C::B_SUB, fb, kx, brow, tc.wg);
                         }
                     }
@@ -783,7 +788,10 @@ cudaError_t run(const void* A, long long a_rows_total, const void* W, int n_wgro
         if (a.tiles == 0) return cudaSuccess;
     }
     CUtensorMap mA, mB, mC;
-    if (!make_map(&mA, A, a.K, a_rows_total, 1, a_rows_total, BM)) return cudaErrorInvalidValue;
+    const bool a_uniform = a.tile_prefix == nullptr;
+    if (!make_map(&mA, A, a.K, a_uniform ? a.M : a_rows_total, a_uniform ? a.ngroups : 1,
+                  a_uniform ? a.a_group_rows : a_rows_total, BM))
+        return cudaErrorInvalidValue;
     if (!make_map(&mB, W, a.K, a.N, n_wgroups, a.N, BN)) return cudaErrorInvalidValue;
     if (EPI == EPI_GELU && a.hid_tma && a.tile_prefix == nullptr) {
         if (!make_map_out(&mC, a.hid, a.N, a.M, a.ngroups, a.a_group_rows)) return cudaErrorInvalidValue;
@@ -834,7 +842,10 @@ cudaError_t run_pair(const void* A, long long a_rows_total, const void* W, int n
         a.hid_tma = 0;
     }
     CUtensorMap mA, mB, mC;
-    if (!make_map(&mA, A, a.K, a_rows_total, 1, a_rows_total, 128)) return cudaErrorInvalidValue;
+    const bool a_uniform = a.tile_prefix == nullptr;
+    if (!make_map(&mA, A, a.K, a_uniform ? a.M : a_rows_total, a_uniform ? a.ngroups : 1,
+                  a_uniform ? a.a_group_rows : a_rows_total, 128))
+        return cudaErrorInvalidValue;
     if (!make_map(&mB, W, a.K, a.N, n_wgroups, a.N, BN / 2)) return cudaErrorInvalidValue;
     if (EPI == EPI_GELU && a.hid_tma) {
         if (!make_map_out(&mC, a.hid, a.N, a.M, a.ngroups, a.a_group_rows)) return cudaErrorInvalidValue;
