@@ -231,6 +231,17 @@ __host__ __device__ __forceinline__ int v8_row_stride(int D, int q) { return D +
 
 __device__ __forceinline__ void f16x8_to_f32(const uint4 v, float (&o)[8]) { to_f32x8(v, false, o); }
 
+// A 32-bit word of two 16-bit values (bf16 or fp16, low half first) -> packed fp32 pair.
+template <bool BF16>
+__device__ __forceinline__ uint64_t pair16_to_f2(uint32_t w) {
+    if constexpr (BF16) {
+        return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    } else {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+        return f2_pack(f.x, f.y);
+    }
+}
+
 // The staged statistics rows are bulk copies: nchunk float2 must fill whole 16-byte units.
 __host__ __device__ __forceinline__ bool v8_stats_bulk(int nchunk) { return nchunk > 0 && nchunk % 2 == 0; }
 // Offset of the statistics staging area: after the two row buffers, the four
@@ -340,52 +351,64 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
             }
             __syncthreads();
         }
+        // mix + residual + LN1 on packed fp32 pairs: y = m + x and the row
+        // statistics in float32; the affine (y - mean) rstd gamma + beta as one
+        // float32 pair fma to (y - mean) rstd, then one fp16 pair fma with the fp16
+        // gamma, beta (S is stored in fp16)
         const int nv = D >> 8;
         for (int h = warp; h < T; h += nwarps) {
             const uint16_t* xh = xs + (size_t)h * RS;
-            float y[8 * NV];
-            float sum = 0.f;
+            uint64_t y[4 * NV];
+            uint64_t s2 = f2_splat(0.f);
 #pragma unroll
             for (int i = 0; i < NV; ++i) {
                 if (i < nv) {
                     const int j0 = (i << 8) + (lane << 3);
                     const int t = j0 / q;
                     const int r = j0 - t * q;
-                    float m[8], x[8];
-                    to_f32x8(*reinterpret_cast<const uint4*>(xs + (size_t)t * RS + h * q + r), !FROM_Z, m);
-                    to_f32x8(*reinterpret_cast<const uint4*>(xh + j0), !FROM_Z, x);
+                    const uint4 mv = *reinterpret_cast<const uint4*>(xs + (size_t)t * RS + h * q + r);
+                    const uint4 xv = *reinterpret_cast<const uint4*>(xh + j0);
+                    const uint32_t mw[4] = {mv.x, mv.y, mv.z, mv.w}, xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        y[8 * i + k] = m[k] + x[k];
-                        sum += y[8 * i + k];
+                    for (int k = 0; k < 4; ++k) {
+                        y[4 * i + k] = f2_add(pair16_to_f2<!FROM_Z>(mw[k]), pair16_to_f2<!FROM_Z>(xw[k]));
+                        s2 = f2_add(s2, y[4 * i + k]);
                     }
                 }
             }
-            const float mean = warp_sum(sum) / (float)D;
-            float sq = 0.f;
+            float lo, hi;
+            f2_unpack(s2, lo, hi);
+            const float mean = warp_sum(lo + hi) / (float)D;
+            const uint64_t nmean2 = f2_splat(-mean);
+            uint64_t q2 = f2_splat(0.f);
 #pragma unroll
             for (int i = 0; i < NV; ++i)
                 if (i < nv) {
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const float d = y[8 * i + k] - mean;
-                        sq += d * d;
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t d = f2_add(y[4 * i + k], nmean2);
+                        q2 = f2_fma(d, d, q2);
                     }
                 }
-            const float rstd = rsqrtf(warp_sum(sq) / (float)D + a.eps);
+            f2_unpack(q2, lo, hi);
+            const float rstd = rsqrtf(warp_sum(lo + hi) / (float)D + a.eps);
+            const uint64_t rstd2 = f2_splat(rstd), nmr2 = f2_splat(-mean * rstd);
             __half* srow = S + ((size_t)h * a.Bcap + b) * D;
 #pragma unroll
             for (int i = 0; i < NV; ++i)
                 if (i < nv) {
                     const int j0 = (i << 8) + (lane << 3);
-                    float g[8], be[8];
-                    f16x8_to_f32(*reinterpret_cast<const uint4*>(sg1 + j0), g);
-                    f16x8_to_f32(*reinterpret_cast<const uint4*>(sb1 + j0), be);
+                    const uint4 gv = *reinterpret_cast<const uint4*>(sg1 + j0);
+                    const uint4 bv = *reinterpret_cast<const uint4*>(sb1 + j0);
+                    const __half2* g2h = reinterpret_cast<const __half2*>(&gv);
+                    const __half2* b2h = reinterpret_cast<const __half2*>(&bv);
                     uint32_t o[4];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        o[k] = pack_f16x2(ln_apply(y[8 * i + 2 * k], mean, rstd, g[2 * k], be[2 * k]),
-                                          ln_apply(y[8 * i + 2 * k + 1], mean, rstd, g[2 * k + 1], be[2 * k + 1]));
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t nh = pack_f16x2_from_f2(f2_fma(y[4 * i + k], rstd2, nmr2));
+                        const __half2 v = __hfma2(*reinterpret_cast<const __half2*>(&nh), g2h[k], b2h[k]);
+                        o[k] = *reinterpret_cast<const uint32_t*>(&v);
+                    }
                     *reinterpret_cast<uint4*>(srow + j0) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
         }

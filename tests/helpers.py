@@ -34,13 +34,16 @@ def rel_err_f32(g: np.ndarray, o: np.ndarray) -> float:
     return float(np.max(np.abs(g - o) / np.maximum(np.abs(o), floor)))
 
 
-def rel_err_bf16(g: np.ndarray, o: np.ndarray, stored_bf16: bool = False) -> float:
+def rel_err_bf16(g: np.ndarray, o: np.ndarray, stored_bf16: bool = False, both_stored: bool = False) -> float:
+    """max |g - o| / rms(o); stored_bf16: g was rounded to bf16 by the library (half an
+    ulp allowed); both_stored: g and o are two such results (half an ulp each)."""
     g = np.asarray(g, dtype=np.float64)
     o = np.asarray(o, dtype=np.float64)
     d = np.abs(g - o)
-    if stored_bf16:
+    if stored_bf16 or both_stored:
         # (1 + 2^-14): the store rounds a float32 value, not the exact one
-        d = np.maximum(d - half_ulp_bf16(np.maximum(np.abs(o), np.abs(g))) * (1 + 2.0 ** -14), 0.0)
+        d = np.maximum(d - half_ulp_bf16(np.maximum(np.abs(o), np.abs(g))) * (1 + 2.0 ** -14) * (2 if both_stored else 1),
+                       0.0)
     return float(np.max(d) / max(rms(o), 1e-30))
 
 
@@ -54,14 +57,15 @@ def _as_np(g):
     return np.asarray(g, dtype=np.float64), False
 
 
-def check(g, o, dtype: str, what: str, tol: float | None = None) -> float:
-    """g: GPU result (torch tensor or array), o: oracle result; dtype: the path ("f32" or "bf16")."""
+def check(g, o, dtype: str, what: str, tol: float | None = None, both_stored: bool = False) -> float:
+    """g: GPU result (torch tensor or array), o: oracle result; dtype: the path ("f32" or "bf16").
+    both_stored: o is itself a bf16-stored GPU result (a comparison of two paths)."""
     g, stored_bf16 = _as_np(g)
     if dtype == "f32":
         err = rel_err_f32(g, o)
         tol = TOL_F32 if tol is None else tol
     else:
-        err = rel_err_bf16(g, o, stored_bf16)
+        err = rel_err_bf16(g, o, stored_bf16, both_stored=both_stored and stored_bf16)
         tol = TOL_BF16 if tol is None else tol
     assert np.all(np.isfinite(g)), f"{what}: non-finite GPU values"
     raw = rel_err_bf16(g, o) if dtype != "f32" else err

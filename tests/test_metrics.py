@@ -34,3 +34,15 @@ def test_f32_metric_floors_small_outputs_at_rms():
     o = np.array([1.0, -1.0, 1e-9])
     g = o + np.array([0.0, 0.0, 1e-6])
     assert rel_err_f32(g, o) < 2e-6
+
+
+def test_two_bf16_roundings_may_differ_by_one_ulp():
+    # two computations within 1e-3 rms of each other, each rounded to bf16, can land
+    # one ulp apart near a rounding boundary; comparing them allows half an ulp each
+    rng = np.random.default_rng(2)
+    x = rng.standard_normal(100000) * 3.0
+    a = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    b = torch.from_numpy(x + 1e-3 * rng.standard_normal(x.size)).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.max(np.abs(a - b) / (2 * half_ulp_bf16(np.maximum(np.abs(a), np.abs(b))))) >= 0.999   # some flip
+    assert rel_err_bf16(a, b, stored_bf16=True) > 1e-2        # one allowance is not enough
+    assert rel_err_bf16(a, b, both_stored=True) < 2e-3        # two are, and the 1e-3 difference remains
