@@ -135,7 +135,7 @@ typedef enum rm_kernel_kind {
     RM_K_GEMM2 = 2,      /* per-token FFN layer 2 + bias + residual + LN2 row statistics */
     RM_K_LN2_OUT = 3,    /* LN2 finalisation into a [B][T][D] output */
     RM_K_POOL = 4,       /* last LN2 finalisation + mean pooling */
-    RM_K_ROWSTATS = 5,   /* LN2 row statistics (SIMT path only) */
+    RM_K_ROWSTATS = 5,   /* LN2 row statistics: (mean, M2) of each full row, merged from the GEMM2 chunk partials */
     RM_K_MOE_ROUTE = 6,  /* router GEMV + ReLU + per-(token, expert) compaction */
     RM_K_MOE_GEMM1 = 7,  /* expert layer 1 + bias + GELU on gathered rows */
     RM_K_MOE_GEMM2 = 8,  /* expert layer 2 + bias, gated, one packed row per (sample, token, open expert) */

@@ -81,7 +81,8 @@ struct rm_ctx {
     void* S = nullptr;           // operand type (fp16 for bf16 contexts)
     void* Hid = nullptr;         // operand type
     void* Z = nullptr;           // pre-LN2 rows, operand type
-    float2* stats = nullptr;
+    float2* stats = nullptr;     // GEMM2 epilogue partials: [T][Bcap][nchunk] (mean, M2) per column chunk
+    float2* rows = nullptr;      // merged: [T][Bcap] (mean, M2) of each full pre-LN2 row
     float* V = nullptr;          // MoE PFFN output inside the stack
     MoeWorkspace moe_ws;
     // host-entry staging
@@ -124,7 +125,7 @@ void free_ctx(rm_ctx* c) {
         moe_free_weights(l.moe);
     }
     moe_free_workspace(c->moe_ws);
-    cudaFree(c->S); cudaFree(c->Hid); cudaFree(c->Z); cudaFree(c->stats); cudaFree(c->V);
+    cudaFree(c->S); cudaFree(c->Hid); cudaFree(c->Z); cudaFree(c->stats); cudaFree(c->rows); cudaFree(c->V);
     cudaFree(c->X0_dev); cudaFree(c->pooled_dev);
     cudaFree(c->d_err); cudaFree(c->d_flag);
     for (auto& e : c->ev_pool) { cudaEventDestroy(e.a); cudaEventDestroy(e.b); }
@@ -210,7 +211,7 @@ rm_status run_pffn(rm_ctx* c, int layer, int B, cudaStream_t s) {
         ProfScope ps(c, RM_K_GEMM2, s);
         RM_CHECK_CUDA(moe_residual_z(c->act, c->V, c->S, c->Z, B, g.T, g.D, c->Bcap, s), "moe residual");
         ProfScope ps2(c, RM_K_ROWSTATS, s);
-        RM_CHECK_CUDA(launch_rowstats(c->act, c->Z, c->stats, B, g.T, g.D, c->Bcap, c->num_sms, s), "row stats");
+        RM_CHECK_CUDA(launch_rowstats(c->act, c->Z, c->rows, B, g.T, g.D, c->Bcap, c->num_sms, s), "row stats");
         return RM_OK;
     }
     if (c->use_tc) {
@@ -226,6 +227,9 @@ rm_status run_pffn(rm_ctx* c, int layer, int B, cudaStream_t s) {
                                             c->num_sms, c->d_err, kWaitTimeoutNs, s);
             if (e != cudaSuccess) return cuda_fail(e, (std::string("gemm2 (tcgen05) ") + tc_last_error()).c_str());
         }
+        ProfScope ps(c, RM_K_ROWSTATS, s);
+        RM_CHECK_CUDA(launch_stats_finalize(c->stats, c->rows, B, g.T, c->Bcap, c->nchunk, c->cw, c->num_sms, s),
+                      "row statistics");
     } else {
         {
             ProfScope ps(c, RM_K_GEMM1, s);
@@ -238,19 +242,14 @@ rm_status run_pffn(rm_ctx* c, int layer, int B, cudaStream_t s) {
                           "gemm2 (simt)");
         }
         ProfScope ps(c, RM_K_ROWSTATS, s);
-        RM_CHECK_CUDA(launch_rowstats(c->act, c->Z, c->stats, B, g.T, g.D, c->Bcap, c->num_sms, s), "row stats");
+        RM_CHECK_CUDA(launch_rowstats(c->act, c->Z, c->rows, B, g.T, g.D, c->Bcap, c->num_sms, s), "row stats");
     }
     return RM_OK;
 }
 
-int layer_nchunk(const rm_ctx* c, int layer) {
-    const bool moe = (c->cfg.moe_layer_mask & (1u << layer)) != 0;
-    return (c->use_tc && !moe) ? c->nchunk : 1;
-}
-int layer_cw(const rm_ctx* c, int layer) {
-    const bool moe = (c->cfg.moe_layer_mask & (1u << layer)) != 0;
-    return (c->use_tc && !moe) ? c->cw : c->cfg.D;
-}
+// The LN2 consumers read c->rows: one merged (mean, M2) per row.
+int layer_nchunk(const rm_ctx*, int) { return 1; }
+int layer_cw(const rm_ctx* c, int) { return c->cfg.D; }
 
 MixLnArgs mix_args(const rm_ctx* c, int layer, int B) {
     MixLnArgs a{};
@@ -279,7 +278,7 @@ rm_status stack_device(rm_ctx* c, const void* X0, float* pooled, void* XL, int B
             RM_CHECK_CUDA(launch_mix_ln1(c->act, false, a, c->num_sms, s), "mix+ln1");
         } else {
             a.Z = c->Z;
-            a.stats = c->stats;
+            a.stats = c->rows;
             a.g2 = c->layers[n - 1].g2;
             a.be2 = c->layers[n - 1].be2;
             a.nchunk = layer_nchunk(c, n - 1);
@@ -292,7 +291,7 @@ rm_status stack_device(rm_ctx* c, const void* X0, float* pooled, void* XL, int B
     }
     const int last = g.L - 1;
     ProfScope ps(c, RM_K_POOL, s);
-    RM_CHECK_CUDA(launch_pool(c->act, c->Z, c->stats, c->layers[last].g2, c->layers[last].be2, pooled, XL, B, g.T,
+    RM_CHECK_CUDA(launch_pool(c->act, c->Z, c->rows, c->layers[last].g2, c->layers[last].be2, pooled, XL, B, g.T,
                               g.D, c->Bcap, layer_nchunk(c, last), layer_cw(c, last), g.ln_eps, c->num_sms, c->d_err,
                               kWaitTimeoutNs, s),
                   "ln2+pool");
@@ -379,6 +378,7 @@ rm_status rm_create(const rm_config* cfg, const rm_layer_params* layers, int dev
         (st = dmalloc(c, &c->Hid, T * Bc * F * c->esz, &c->ws_bytes)) != RM_OK ||
         (st = dmalloc(c, &c->Z, T * Bc * D * op_size(c->act), &c->ws_bytes)) != RM_OK ||
         (st = dmalloc(c, (void**)&c->stats, T * Bc * (size_t)c->nchunk * sizeof(float2), &c->ws_bytes)) != RM_OK ||
+        (st = dmalloc(c, (void**)&c->rows, T * Bc * sizeof(float2), &c->ws_bytes)) != RM_OK ||
         (st = dmalloc(c, (void**)&c->d_err, sizeof(int), nullptr)) != RM_OK ||
         (st = dmalloc(c, (void**)&c->d_flag, sizeof(int), nullptr)) != RM_OK) {
         free_ctx(c);
@@ -449,7 +449,7 @@ rm_status rm_block_forward(rm_ctx* c, int layer, const void* X_in, void* X_out, 
     }
     if ((st = run_pffn(c, layer, B, s)) != RM_OK) return st;
     ProfScope ps(c, RM_K_LN2_OUT, s);
-    RM_CHECK_CUDA(launch_ln2_out(c->act, c->Z, c->stats, c->layers[layer].g2, c->layers[layer].be2, X_out, B, g.T,
+    RM_CHECK_CUDA(launch_ln2_out(c->act, c->Z, c->rows, c->layers[layer].g2, c->layers[layer].be2, X_out, B, g.T,
                                  g.D, c->Bcap, layer_nchunk(c, layer), layer_cw(c, layer), g.ln_eps, c->num_sms, s),
                   "ln2 out");
     return RM_OK;
@@ -669,13 +669,13 @@ rm_status rm_block_forward_noalloc(rm_ctx* c, int layer, const void* X_in, void*
     const char* xi = (const char*)X_in;
     const char* xo = (const char*)X_out;
     if (xi < xo + io_bytes && xo < xi + io_bytes) return fail(RM_ERR_INVALID_ARG, "X_in and X_out overlap");
-    const int nchunk = layer_nchunk(c, layer), cw = layer_cw(c, layer);
-    // scratch layout (token-major, rows between tokens = B): S, Hid, Z, stats
+    // scratch layout (token-major, rows between tokens = B): S, Hid, Z, chunk statistics, row statistics
     const size_t bS = align256(T * Bs * D * op_size(c->act));
     const size_t bH = align256(T * Bs * F * op_size(c->act));
     const size_t bZ = align256(T * Bs * D * op_size(c->act));
-    const size_t bT = align256(T * Bs * (size_t)nchunk * sizeof(float2));
-    const size_t need = bS + bH + bZ + bT;
+    const size_t bT = align256(T * Bs * (size_t)c->nchunk * sizeof(float2));
+    const size_t bR = align256(T * Bs * sizeof(float2));
+    const size_t need = bS + bH + bZ + bT + bR;
     if (need > kNoAllocScratchBytes) {
         const size_t per = need / Bs + 1;
         return fail(RM_ERR_INVALID_ARG,
@@ -690,6 +690,7 @@ rm_status rm_block_forward_noalloc(rm_ctx* c, int layer, const void* X_in, void*
     void* Hid = p + bS;
     void* Z = p + bS + bH;
     float2* stats = reinterpret_cast<float2*>(p + bS + bH + bZ);
+    float2* rows = reinterpret_cast<float2*>(p + bS + bH + bZ + bT);
 
     cudaStream_t s = as_stream(stream);
     const LayerW& w = c->layers[layer];
@@ -705,13 +706,15 @@ rm_status rm_block_forward_noalloc(rm_ctx* c, int layer, const void* X_in, void*
         e = launch_gemm2_tc(Hid, w.W2p, w.b2, S, Z, stats, B, g.T, g.D, c->F, B, c->num_sms, c->d_err,
                             kWaitTimeoutNs, s);
         if (e != cudaSuccess) return cuda_fail(e, (std::string("gemm2 (tcgen05) ") + tc_last_error()).c_str());
+        RM_CHECK_CUDA(launch_stats_finalize(stats, rows, B, g.T, B, c->nchunk, c->cw, c->num_sms, s),
+                      "row statistics");
     } else {
         RM_CHECK_CUDA(launch_gemm1_simt(c->act, S, w.W1p, w.b1, Hid, B, g.T, g.D, c->F, B, s), "gemm1 (simt)");
         RM_CHECK_CUDA(launch_gemm2_simt(c->act, Hid, w.W2p, w.b2, S, Z, B, g.T, g.D, c->F, B, s), "gemm2 (simt)");
-        RM_CHECK_CUDA(launch_rowstats(c->act, Z, stats, B, g.T, g.D, B, c->num_sms, s), "row stats");
+        RM_CHECK_CUDA(launch_rowstats(c->act, Z, rows, B, g.T, g.D, B, c->num_sms, s), "row stats");
     }
-    RM_CHECK_CUDA(launch_ln2_out(c->act, Z, stats, w.g2, w.be2, X_out, B, g.T, g.D, B, nchunk, cw, g.ln_eps,
-                                 c->num_sms, s),
+    RM_CHECK_CUDA(launch_ln2_out(c->act, Z, rows, w.g2, w.be2, X_out, B, g.T, g.D, B, 1, g.D, g.ln_eps, c->num_sms,
+                                 s),
                   "ln2 out");
     return RM_OK;
 }

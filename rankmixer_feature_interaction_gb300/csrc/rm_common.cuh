@@ -162,6 +162,12 @@ __device__ __forceinline__ float warp_sum(float v) {
 // this for the same row gets bit-identical results.
 __device__ __forceinline__ void merge_row_stats(const float2* __restrict__ st, int nchunk, int cw, int D,
                                                 float eps, int lane, float& mean, float& rstd) {
+    if (nchunk == 1) {           // already merged: (mean, M2) of the whole row
+        const float2 v = st[0];
+        mean = v.x;
+        rstd = rsqrtf(v.y / (float)D + eps);
+        return;
+    }
     float s = 0.f;
     for (int c = lane; c < nchunk; c += 32) s += st[c].x;
     s = warp_sum(s);

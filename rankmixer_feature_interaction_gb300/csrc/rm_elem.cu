@@ -28,11 +28,13 @@ __device__ __forceinline__ float ln_apply(float z, float mean, float rstd, float
 
 template <typename T> struct Vec2;
 template <> struct Vec2<float> {
+    using type = float2;
     __device__ static float2 load(const float* p) { return *reinterpret_cast<const float2*>(p); }
     __device__ static void store(float* p, float a, float b) { *reinterpret_cast<float2*>(p) = make_float2(a, b); }
     __device__ static void split(float2 v, float& a, float& b) { a = v.x; b = v.y; }
 };
 template <> struct Vec2<__half> {
+    using type = __half2;
     __device__ static __half2 load(const __half* p) { return *reinterpret_cast<const __half2*>(p); }
     __device__ static void store(__half* p, float a, float b) {
         *reinterpret_cast<__half2*>(p) = __floats2half2_rn(sat_f16(a), sat_f16(b));
@@ -43,6 +45,7 @@ template <> struct Vec2<__half> {
     }
 };
 template <> struct Vec2<__nv_bfloat16> {
+    using type = __nv_bfloat162;
     __device__ static __nv_bfloat162 load(const __nv_bfloat16* p) {
         return *reinterpret_cast<const __nv_bfloat162*>(p);
     }
@@ -606,6 +609,7 @@ __global__ void ln2_out_kernel(const Tz* __restrict__ Z, const float2* __restric
 // receives them rounded to the caller's dtype.
 // ---------------------------------------------------------------------------
 constexpr int kPoolThreads = 256;
+constexpr int kPoolBatch = 8;
 
 template <typename Tz, typename Tout>
 __global__ void __launch_bounds__(kPoolThreads)
@@ -625,18 +629,32 @@ pool_kernel(const Tz* __restrict__ Z, const float2* __restrict__ stats, const fl
         }
         __syncthreads();
         if ((D & 1) == 0) {
+            const size_t tstride = (size_t)Bcap * D;
             for (int j = 2 * threadIdx.x; j < D; j += 2 * kPoolThreads) {
                 const float2 g = *reinterpret_cast<const float2*>(g2 + j);
                 const float2 be = *reinterpret_cast<const float2*>(be2 + j);
                 float acc0 = 0.f, acc1 = 0.f;
-                for (int t = 0; t < T; ++t) {
-                    float z0, z1;
-                    load_pair(Z + ((size_t)t * Bcap + b) * D + j, z0, z1);
-                    const float v0 = ln_apply(z0, s_mean[t], s_rstd[t], g.x, be.x);
-                    const float v1 = ln_apply(z1, s_mean[t], s_rstd[t], g.y, be.y);
-                    if (XL) Vec2<Tout>::store(XL + ((size_t)b * T + t) * D + j, v0, v1);
-                    acc0 += v0;
-                    acc1 += v1;
+                const Tz* zc = Z + (size_t)b * D + j;
+                // tokens in batches of kPoolBatch: the loads of a batch are issued before its
+                // arithmetic, so that several are in flight (the sum keeps token order)
+                for (int t0 = 0; t0 < T; t0 += kPoolBatch) {
+                    typename Vec2<Tz>::type zz[kPoolBatch];
+#pragma unroll
+                    for (int u = 0; u < kPoolBatch; ++u)
+                        if (t0 + u < T) zz[u] = Vec2<Tz>::load(zc + (size_t)(t0 + u) * tstride);
+#pragma unroll
+                    for (int u = 0; u < kPoolBatch; ++u) {
+                        if (t0 + u < T) {
+                            const int t = t0 + u;
+                            float z0, z1;
+                            Vec2<Tz>::split(zz[u], z0, z1);
+                            const float v0 = ln_apply(z0, s_mean[t], s_rstd[t], g.x, be.x);
+                            const float v1 = ln_apply(z1, s_mean[t], s_rstd[t], g.y, be.y);
+                            if (XL) Vec2<Tout>::store(XL + ((size_t)b * T + t) * D + j, v0, v1);
+                            acc0 += v0;
+                            acc1 += v1;
+                        }
+                    }
                 }
                 *reinterpret_cast<float2*>(pooled + (size_t)b * D + j) = make_float2(acc0 / (float)T, acc1 / (float)T);
             }
@@ -653,6 +671,29 @@ pool_kernel(const Tz* __restrict__ Z, const float2* __restrict__ stats, const fl
             }
         }
         __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// (mean, M2) of each full row from its nchunk chunk partials (mean, M2 over cw
+// columns each), merged by Chan's formula; one thread per row (the rows of the
+// first B samples of every token).  Consumers then read one value per row.
+// ---------------------------------------------------------------------------
+__global__ void stats_finalize_kernel(const float2* __restrict__ part, float2* __restrict__ out, int B, int T,
+                                      int Bcap, int nchunk, int cw) {
+    const long long n = (long long)T * B;
+    for (long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x; r < n; r += (long long)gridDim.x * blockDim.x) {
+        const int t = (int)(r / B), b = (int)(r % B);
+        const float2* p = part + ((size_t)t * Bcap + b) * nchunk;
+        float s = 0.f;
+        for (int c = 0; c < nchunk; ++c) s += p[c].x;
+        const float mean = s / (float)nchunk;
+        float m2 = 0.f;
+        for (int c = 0; c < nchunk; ++c) {
+            const float d = p[c].x - mean;
+            m2 += p[c].y + (float)cw * d * d;
+        }
+        out[(size_t)t * Bcap + b] = make_float2(mean, m2);
     }
 }
 
@@ -813,6 +854,14 @@ cudaError_t launch_pool(Act act, const void* Z, const float2* stats, const float
     else
         pool_kernel<float, float><<<grid, kPoolThreads, 0, s>>>((const float*)Z, stats, g2, be2, pooled, (float*)XL,
                                                                 B, T, D, Bcap, nchunk, cw, eps);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stats_finalize(const float2* part, float2* out, int B, int T, int Bcap, int nchunk, int cw,
+                                  int num_sms, cudaStream_t s) {
+    if (B <= 0) return cudaSuccess;
+    stats_finalize_kernel<<<grid_for((long long)B * T, 256, num_sms * 8), 256, 0, s>>>(part, out, B, T, Bcap, nchunk,
+                                                                                        cw);
     return cudaGetLastError();
 }
 

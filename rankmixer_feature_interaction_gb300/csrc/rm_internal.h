@@ -55,6 +55,10 @@ cudaError_t launch_pool(Act act, const void* Z, const float2* stats, const float
                         float* pooled, void* XL, int B, int T, int D, int Bcap, int nchunk, int cw, float eps,
                         int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s);
 
+// Merge each row's nchunk chunk partials (GEMM2 epilogue) into (mean, M2) of the row.
+cudaError_t launch_stats_finalize(const float2* part, float2* out, int B, int T, int Bcap, int nchunk, int cw,
+                                  int num_sms, cudaStream_t s);
+
 // (mean, M2) of each full row of Z (operand type; one chunk per row).
 cudaError_t launch_rowstats(Act act, const void* Z, float2* stats, int B, int T, int D, int Bcap, int num_sms,
                             cudaStream_t s);
