@@ -245,17 +245,10 @@ __device__ __forceinline__ uint64_t pair16_to_f2(uint32_t w) {
     }
 }
 
-// The staged statistics rows are bulk copies: nchunk float2 must fill whole 16-byte units.
-__host__ __device__ __forceinline__ bool v8_stats_bulk(int nchunk) { return nchunk > 0 && nchunk % 2 == 0; }
-// Offset of the statistics staging area: after the two row buffers, the four
-// fp16 affines, two mbarriers, the row mean / rstd arrays and the abort flag
-// (every part a multiple of 16 bytes when q % 8 == 0 and D % 256 == 0).
-__host__ __device__ __forceinline__ size_t v8_stats_offset(int T, int D, int q) {
+// Two row buffers, the four fp16 affines, two mbarriers, the row mean / rstd
+// arrays and the abort flag.
+size_t v8_smem_bytes(bool, int T, int D, int q, int) {
     return 2 * (size_t)T * v8_row_stride(D, q) * 2 + 4 * (size_t)D * 2 + 16 + 2 * kMaxT * 4 + 16;
-}
-size_t v8_smem_bytes(bool from_z, int T, int D, int q, int nchunk) {
-    const size_t st = from_z && v8_stats_bulk(nchunk) ? 2 * (size_t)T * nchunk * 8 : 0;
-    return v8_stats_offset(T, D, q) + st;
 }
 
 template <bool FROM_Z, int NV>
@@ -275,10 +268,6 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
     float* s_mean = reinterpret_cast<float*>(bars + 2);
     float* s_rstd = s_mean + kMaxT;
     volatile int* s_abort = reinterpret_cast<volatile int*>(s_rstd + kMaxT);
-    // FROM_Z with an even chunk count: each sample's T rows of LN2 chunk
-    // statistics ride with its Z rows ([2][T][nchunk] float2, 16-byte aligned)
-    const bool stats_bulk = FROM_Z && v8_stats_bulk(a.nchunk);
-    float2* sst = reinterpret_cast<float2*>(smem + v8_stats_offset(T, D, q));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nwarps = blockDim.x >> 5;
     const uint16_t* src = FROM_Z ? reinterpret_cast<const uint16_t*>(a.Z) : reinterpret_cast<const uint16_t*>(a.X);
@@ -303,25 +292,37 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
     auto issue = [&](int b, int slot) {   // warp 0: lane 0 arms the barrier, lane t copies row t
         const uint32_t bar = smem_u32(&bars[slot]);
         const uint32_t dst = smem_u32(buf) + (uint32_t)slot * buf_elems * 2u;
-        const uint32_t st_bytes = stats_bulk ? (uint32_t)a.nchunk * 8u : 0u;
         fence_proxy_async_smem();
-        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)T * (row_bytes + st_bytes));
+        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)T * row_bytes);
         __syncwarp();
         for (int t = lane; t < T; t += 32) {
             const uint16_t* row = FROM_Z ? src + ((size_t)t * a.Bcap + b) * D : src + ((size_t)b * T + t) * D;
             bulk_copy_g2s(dst + (uint32_t)t * (uint32_t)RS * 2u, row, row_bytes, bar);
-            if (stats_bulk)
-                bulk_copy_g2s(smem_u32(sst) + ((uint32_t)slot * (uint32_t)T + (uint32_t)t) * st_bytes,
-                              a.stats + ((size_t)t * a.Bcap + b) * a.nchunk, st_bytes, bar);
         }
     };
+
+    // FROM_Z with merged row statistics (one (mean, M2) per row): lane k of warp w
+    // holds row w + k nwarps of the next sample, loaded one sample ahead
+    const bool merged = FROM_Z && a.nchunk == 1;
+    const int pre_t = warp + lane * nwarps;
+    const bool pre_lane = merged && pre_t < T;
+    float2 pre = make_float2(0.f, 0.f);
+    if (pre_lane && (int)blockIdx.x < a.B) pre = __ldg(a.stats + (size_t)pre_t * a.Bcap + blockIdx.x);
 
     if (warp == 0 && (int)blockIdx.x < a.B) issue(blockIdx.x, 0);
     int it = 0;
     for (int b = blockIdx.x; b < a.B; b += gridDim.x, ++it) {
         const int slot = it & 1;
         if (warp == 0 && b + (int)gridDim.x < a.B) issue(b + gridDim.x, slot ^ 1);
-        if (FROM_Z && !stats_bulk) sample_row_stats(a, b, s_mean, s_rstd, warp, nwarps, lane);
+        if (merged) {
+            if (pre_lane) {
+                s_mean[pre_t] = pre.x;
+                s_rstd[pre_t] = rsqrtf(pre.y / (float)D + a.eps);
+                if (b + (int)gridDim.x < a.B) pre = __ldg(a.stats + (size_t)pre_t * a.Bcap + b + gridDim.x);
+            }
+        } else if (FROM_Z) {
+            sample_row_stats(a, b, s_mean, s_rstd, warp, nwarps, lane);
+        }
         mbar_wait_bounded(smem_u32(&bars[slot]), (uint32_t)(it >> 1) & 1u, s_abort, a.err, a.timeout_ns);
         __syncthreads();
         if (*s_abort) break;
@@ -329,13 +330,7 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
         if (FROM_Z) {
             // X_{n-1} = LN2(Z) in place (fp16), 8 elements per lane
             for (int t = warp; t < T; t += nwarps) {
-                float mt, rt;
-                if (stats_bulk) {
-                    merge_row_stats(sst + ((size_t)slot * T + t) * a.nchunk, a.nchunk, a.cw, D, a.eps, lane, mt, rt);
-                } else {
-                    mt = s_mean[t];
-                    rt = s_rstd[t];
-                }
+                const float mt = s_mean[t], rt = s_rstd[t];
                 uint16_t* row = xs + (size_t)t * RS;
                 // (z - mean) (rstd gamma) + beta on fp16 pairs: the result is stored in
                 // fp16, and the row statistics themselves were merged in fp32
@@ -374,7 +369,14 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
                     const uint32_t mw[4] = {mv.x, mv.y, mv.z, mv.w}, xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        y[4 * i + k] = f2_add(pair16_to_f2<!FROM_Z>(mw[k]), pair16_to_f2<!FROM_Z>(xw[k]));
+                        if constexpr (FROM_Z) {     // fp16 rows: add in fp16, convert once
+                            const __half2 yh = __hadd2(*reinterpret_cast<const __half2*>(&mw[k]),
+                                                       *reinterpret_cast<const __half2*>(&xw[k]));
+                            const float2 yf = __half22float2(yh);
+                            y[4 * i + k] = f2_pack(yf.x, yf.y);
+                        } else {
+                            y[4 * i + k] = f2_add(pair16_to_f2<true>(mw[k]), pair16_to_f2<true>(xw[k]));
+                        }
                         s2 = f2_add(s2, y[4 * i + k]);
                     }
                 }

@@ -124,7 +124,7 @@ def test_stack_matches_chained_blocks(path):
     for n in range(L):
         Xn = m.block_forward(n, Xn)
     torch.cuda.synchronize()
-    check(XL, _np(Xn), "bf16", "stack vs chained blocks", tol=4e-2)
+    check(XL, _np(Xn), "bf16", "stack vs chained blocks", tol=4e-2, both_stored=True)
     torch.testing.assert_close(pooled, XL.float().mean(dim=1), rtol=0, atol=2e-2)
     pr, xr = oracle.stack_forward(_np(X), synth.to_f64(layers), return_XL=True)
     check(XL, xr, "bf16", "stack X_L (L=3)")
