@@ -10,6 +10,8 @@
 // Types: Tin is the caller's activation dtype (bf16 or float), Top the
 // operand type of the GEMMs (fp16 for bf16 contexts, float for float32
 // contexts).  The pre-LN2 rows Z are stored in Top as well.
+#include <type_traits>
+
 #include "rm_common.cuh"
 #include "rm_internal.h"
 
@@ -614,11 +616,12 @@ constexpr int kPoolThreads = 256;
 constexpr int kPoolBatch = 8;
 
 template <typename Tz, typename Tout>
-__global__ void __launch_bounds__(kPoolThreads)
+__global__ void __launch_bounds__(kPoolThreads, 4)
 pool_kernel(const Tz* __restrict__ Z, const float2* __restrict__ stats, const float* __restrict__ g2,
             const float* __restrict__ be2, float* __restrict__ pooled, Tout* __restrict__ XL, int B, int T, int D,
             int Bcap, int nchunk, int cw, float eps) {
     __shared__ float s_mean[kMaxT], s_rstd[kMaxT];
+    __shared__ __half2 s_rh[kMaxT], s_nmrh[kMaxT];     // rstd and -mean rstd as fp16 pairs
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int b = blockIdx.x; b < B; b += gridDim.x) {
         for (int t = warp; t < T; t += kPoolThreads / 32) {
@@ -627,9 +630,42 @@ pool_kernel(const Tz* __restrict__ Z, const float2* __restrict__ stats, const fl
             if (lane == 0) {
                 s_mean[t] = mean;
                 s_rstd[t] = rstd;
+                s_rh[t] = __float2half2_rn(rstd);
+                s_nmrh[t] = __float2half2_rn(-mean * rstd);
             }
         }
         __syncthreads();
+        if constexpr (std::is_same_v<Tz, __half>) {
+            if (XL == nullptr && (D & 1) == 0) {
+                // pooled = gamma mean_t((z - mean_t) rstd_t) + beta: the centred, scaled values
+                // on fp16 pairs (one fma), summed over kPoolBatch tokens in fp16, each partial
+                // sum converted once and added in float32 (token order kept)
+                const size_t tstride = (size_t)Bcap * D;
+                for (int j = 2 * threadIdx.x; j < D; j += 2 * kPoolThreads) {
+                    const __half* zc = Z + (size_t)b * D + j;
+                    float acc0 = 0.f, acc1 = 0.f;
+                    for (int t0 = 0; t0 < T; t0 += kPoolBatch) {
+                        __half2 zz[kPoolBatch];
+#pragma unroll
+                        for (int u = 0; u < kPoolBatch; ++u)
+                            if (t0 + u < T) zz[u] = *reinterpret_cast<const __half2*>(zc + (size_t)(t0 + u) * tstride);
+                        __half2 part = __float2half2_rn(0.f);
+#pragma unroll
+                        for (int u = 0; u < kPoolBatch; ++u)
+                            if (t0 + u < T) part = __hadd2(part, __hfma2(zz[u], s_rh[t0 + u], s_nmrh[t0 + u]));
+                        const float2 pf = __half22float2(part);
+                        acc0 += pf.x;
+                        acc1 += pf.y;
+                    }
+                    const float2 g = *reinterpret_cast<const float2*>(g2 + j);
+                    const float2 be = *reinterpret_cast<const float2*>(be2 + j);
+                    *reinterpret_cast<float2*>(pooled + (size_t)b * D + j) =
+                        make_float2(fmaf(g.x, acc0 / (float)T, be.x), fmaf(g.y, acc1 / (float)T, be.y));
+                }
+                __syncthreads();
+                continue;
+            }
+        }
         if ((D & 1) == 0) {
             const size_t tstride = (size_t)Bcap * D;
             for (int j = 2 * threadIdx.x; j < D; j += 2 * kPoolThreads) {

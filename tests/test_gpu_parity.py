@@ -101,6 +101,7 @@ def test_bf16_block_and_stack(path, T, D, k, L, B):
     assert m.path == path
     Xo, S = m.block_forward(0, X, return_S=True)
     pooled, XL = m.stack_forward(X, return_XL=True)
+    pooled_only = m.stack_forward(X)          # the pool without X_L takes its own (fp16-pair) path
     torch.cuda.synchronize()
     assert m.sync_status() == _lib.RM_OK
     p64 = synth.to_f64(layers)
@@ -110,6 +111,7 @@ def test_bf16_block_and_stack(path, T, D, k, L, B):
     pooled_ref, XL_ref = oracle.stack_forward(_np(X), p64, return_XL=True)
     check(XL, XL_ref, "bf16", "stack X_L")
     check(pooled, pooled_ref, "bf16", "pooled")
+    check(pooled_only, pooled_ref, "bf16", "pooled (without X_L)")
 
 
 @pytest.mark.parametrize("path", ["tcgen05", "simt"])
@@ -254,6 +256,7 @@ def _sampled_stack_parity(name, B, n_samples, seed, max_batch=None, model=None):
         m, layers, p64 = model
     X = synth.make_input(B, T, D, seed + B, "bf16", DEV)
     pooled, XL = m.stack_forward(X, return_XL=True)
+    pooled_only = m.stack_forward(X)          # the serving call: no X_L
     torch.cuda.synchronize()
     assert m.sync_status() == _lib.RM_OK
     rng = np.random.default_rng(seed + B)
@@ -261,7 +264,8 @@ def _sampled_stack_parity(name, B, n_samples, seed, max_batch=None, model=None):
     pr, xr = oracle.stack_forward(_np(X[idx]), p64, return_XL=True)
     check(XL[torch.as_tensor(idx, device=XL.device)], xr, "bf16", f"{name} B={B} X_L")
     check(pooled[torch.as_tensor(idx, device=pooled.device)], pr, "bf16", f"{name} B={B} pooled")
-    assert torch.isfinite(pooled).all()
+    check(pooled_only[torch.as_tensor(idx, device=pooled.device)], pr, "bf16", f"{name} B={B} pooled (without X_L)")
+    assert torch.isfinite(pooled).all() and torch.isfinite(pooled_only).all()
     return m
 
 
