@@ -171,14 +171,18 @@ RM_API rm_status rm_block_forward(rm_ctx *ctx, int layer, const void *X_in, void
 
 /* The whole stack and the mean pooling ("RankMixer" section 3.1): pooled
  * (device float32 [B][D]) = mean_t X_L; XL (nullable, device [B][T][D]) receives
- * X_L.  X0: device [B][T][D].  Equal, bit for bit, to chaining rm_block_forward
- * over the layers and averaging the last output in float32 in token order. */
+ * X_L.  X0: device [B][T][D].  Agrees with chaining rm_block_forward over the
+ * layers up to the rounding of each intermediate X_n (the stack keeps them in
+ * fp16 on the device, the chained calls round them to the context dtype). */
 RM_API rm_status rm_stack_forward(rm_ctx *ctx, const void *X0, float *pooled, void *XL, int B, void *stream);
 
 /* rm_stack_forward from HOST buffers: copies X0_host ([B][T][D], context dtype)
  * to the device, runs the stack, copies the pooled float32 [B][D] result to
  * pooled_host.  Returns after the result is in pooled_host (synchronises the
- * stream).  Uses context-owned device staging buffers. */
+ * stream).  Uses context-owned device staging buffers.  From B = 2048 on, the
+ * batch runs as up to 4 chunks of at least 1024 samples, the copy of each chunk
+ * overlapping the computation of the previous one (two context-owned copy
+ * streams); pinned host buffers let the copies run asynchronously. */
 RM_API rm_status rm_stack_forward_host(rm_ctx *ctx, const void *X0_host, float *pooled_host, int B, void *stream);
 
 /* Sparse-MoE per-token FFN of layer `layer` ("RankMixer" Eq. 10, inference

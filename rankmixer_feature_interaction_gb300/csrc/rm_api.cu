@@ -47,6 +47,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // Default bound of every device-side wait (2 s of global time).
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
+// Pipelined host entry: at most this many chunks, each at least kHostChunkMin samples.
+constexpr int kHostChunksMax = 4;
+constexpr int kHostChunkMin = 1024;
 
 struct LayerW {
     void* W1p = nullptr;   // [T][F][D]  (K-major for GEMM1)
@@ -85,9 +88,12 @@ struct rm_ctx {
     float2* rows = nullptr;      // merged: [T][Bcap] (mean, M2) of each full pre-LN2 row
     float* V = nullptr;          // MoE PFFN output inside the stack
     MoeWorkspace moe_ws;
-    // host-entry staging
+    // host-entry staging: device copies of X0 and pooled, the copy streams and
+    // per-chunk events of the pipelined host entry
     void* X0_dev = nullptr;
     float* pooled_dev = nullptr;
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t ev_in[kHostChunksMax] = {}, ev_done[kHostChunksMax] = {};
     // error word and the debug flag nothing sets
     int* d_err = nullptr;
     int* d_flag = nullptr;
@@ -127,6 +133,12 @@ void free_ctx(rm_ctx* c) {
     moe_free_workspace(c->moe_ws);
     cudaFree(c->S); cudaFree(c->Hid); cudaFree(c->Z); cudaFree(c->stats); cudaFree(c->rows); cudaFree(c->V);
     cudaFree(c->X0_dev); cudaFree(c->pooled_dev);
+    for (int i = 0; i < kHostChunksMax; ++i) {
+        if (c->ev_in[i]) cudaEventDestroy(c->ev_in[i]);
+        if (c->ev_done[i]) cudaEventDestroy(c->ev_done[i]);
+    }
+    if (c->s_in) cudaStreamDestroy(c->s_in);
+    if (c->s_out) cudaStreamDestroy(c->s_out);
     cudaFree(c->d_err); cudaFree(c->d_flag);
     for (auto& e : c->ev_pool) { cudaEventDestroy(e.a); cudaEventDestroy(e.b); }
     delete c;
@@ -478,17 +490,64 @@ rm_status rm_stack_forward_host(rm_ctx* c, const void* X0_host, float* pooled_ho
         if ((st = dmalloc(c, (void**)&c->pooled_dev, (size_t)c->Bcap * g.D * 4, &c->ws_bytes)) != RM_OK) return st;
     }
     cudaStream_t s = as_stream(stream);
-    const size_t in_bytes = (size_t)B * g.T * g.D * c->esz;
-    {
-        ProfScope ps(c, RM_K_MISC, s);
-        RM_CHECK_CUDA(cudaMemcpyAsync(c->X0_dev, X0_host, in_bytes, cudaMemcpyHostToDevice, s), "H2D X0");
+    const size_t row_in = (size_t)g.T * g.D * c->esz, row_out = (size_t)g.D * 4;
+    char* x_dev = static_cast<char*>(c->X0_dev);
+    const char* x_host = static_cast<const char*>(X0_host);
+    // Large batches run as up to kHostChunksMax chunks (whole multiples of 256
+    // samples, the CTA-pair tile height): chunk i + 1 is copied in on one stream
+    // while chunk i computes on `stream`, and each chunk's pooled rows go back on
+    // a third; the workspace is reused chunk after chunk (the compute is serial).
+    int chunk = B;
+    if (B >= 2 * kHostChunkMin) {
+        chunk = ((B + kHostChunksMax - 1) / kHostChunksMax + 255) / 256 * 256;
+        if (chunk < kHostChunkMin) chunk = kHostChunkMin;
     }
-    if ((st = stack_device(c, c->X0_dev, c->pooled_dev, nullptr, B, s)) != RM_OK) return st;
-    {
-        ProfScope ps(c, RM_K_MISC, s);
-        RM_CHECK_CUDA(cudaMemcpyAsync(pooled_host, c->pooled_dev, (size_t)B * g.D * 4, cudaMemcpyDeviceToHost, s),
-                      "D2H pooled");
+    const int nchunks = (B + chunk - 1) / chunk;
+    if (nchunks == 1) {
+        {
+            ProfScope ps(c, RM_K_MISC, s);
+            RM_CHECK_CUDA(cudaMemcpyAsync(c->X0_dev, X0_host, (size_t)B * row_in, cudaMemcpyHostToDevice, s), "H2D X0");
+        }
+        if ((st = stack_device(c, c->X0_dev, c->pooled_dev, nullptr, B, s)) != RM_OK) return st;
+        {
+            ProfScope ps(c, RM_K_MISC, s);
+            RM_CHECK_CUDA(cudaMemcpyAsync(pooled_host, c->pooled_dev, (size_t)B * row_out, cudaMemcpyDeviceToHost, s),
+                          "D2H pooled");
+        }
+        RM_CHECK_CUDA(cudaStreamSynchronize(s), "stream sync");
+        return RM_OK;
     }
+    if (!c->s_in) {
+        RM_CHECK_CUDA(cudaStreamCreateWithFlags(&c->s_in, cudaStreamNonBlocking), "copy stream");
+        RM_CHECK_CUDA(cudaStreamCreateWithFlags(&c->s_out, cudaStreamNonBlocking), "copy stream");
+        for (int i = 0; i < kHostChunksMax; ++i) {
+            RM_CHECK_CUDA(cudaEventCreateWithFlags(&c->ev_in[i], cudaEventDisableTiming), "event");
+            RM_CHECK_CUDA(cudaEventCreateWithFlags(&c->ev_done[i], cudaEventDisableTiming), "event");
+        }
+    }
+    // the staging buffers may still be read by an earlier call's work on `stream`
+    RM_CHECK_CUDA(cudaEventRecord(c->ev_done[0], s), "event");
+    RM_CHECK_CUDA(cudaStreamWaitEvent(c->s_in, c->ev_done[0], 0), "wait");
+    for (int i = 0; i < nchunks; ++i) {
+        const int b0 = i * chunk, bn = B - b0 < chunk ? B - b0 : chunk;
+        RM_CHECK_CUDA(cudaMemcpyAsync(x_dev + (size_t)b0 * row_in, x_host + (size_t)b0 * row_in, (size_t)bn * row_in,
+                                      cudaMemcpyHostToDevice, c->s_in),
+                      "H2D X0 chunk");
+        RM_CHECK_CUDA(cudaEventRecord(c->ev_in[i], c->s_in), "event");
+    }
+    for (int i = 0; i < nchunks; ++i) {
+        const int b0 = i * chunk, bn = B - b0 < chunk ? B - b0 : chunk;
+        RM_CHECK_CUDA(cudaStreamWaitEvent(s, c->ev_in[i], 0), "wait");
+        if ((st = stack_device(c, x_dev + (size_t)b0 * row_in, c->pooled_dev + (size_t)b0 * g.D, nullptr, bn, s)) !=
+            RM_OK)
+            return st;
+        RM_CHECK_CUDA(cudaEventRecord(c->ev_done[i], s), "event");
+        RM_CHECK_CUDA(cudaStreamWaitEvent(c->s_out, c->ev_done[i], 0), "wait");
+        RM_CHECK_CUDA(cudaMemcpyAsync(pooled_host + (size_t)b0 * g.D, c->pooled_dev + (size_t)b0 * g.D,
+                                      (size_t)bn * row_out, cudaMemcpyDeviceToHost, c->s_out),
+                      "D2H pooled chunk");
+    }
+    RM_CHECK_CUDA(cudaStreamSynchronize(c->s_out), "stream sync");
     RM_CHECK_CUDA(cudaStreamSynchronize(s), "stream sync");
     return RM_OK;
 }
