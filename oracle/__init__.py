@@ -8,7 +8,7 @@ imports it.
 
 Sources: "RankMixer: Scaling Up Ranking Models in Industrial Recommenders",
 section 3.1 Eq. 1, section 3.3 Eq. 3-9, section 3.4 Eq. 10; "RankMixer 详解（1）",
-sections 3.1, 3.3, 4.1 and 5.1.  Every function below forwards to the C loop
+sections 3.1, 3.3, 4.1, 5.1 and 5.2 (the backward pass).  Every function below forwards to the C loop
 nest of the same name; the docstrings say which passage each follows.
 
 Parity status: every function is pinned by a test under ``tests/`` (printed
@@ -57,6 +57,10 @@ def _load():
             lib.oracle_mean_pool.argtypes = [dp, dp, i, i, i]
             lib.oracle_stack_forward.argtypes = [dp] * 11 + [ctypes.c_double, i, i, i, i, i]
             lib.oracle_moe_pffn.argtypes = [dp] * 9 + [i, i, i, i, i]
+            lib.oracle_gelu_grad.argtypes = [dp, dp, ctypes.c_size_t]
+            lib.oracle_layernorm_backward.argtypes = [dp, dp, dp, ctypes.c_double, dp, dp, dp, i, i]
+            lib.oracle_block_backward.argtypes = [dp] * 11 + [ctypes.c_double] + [dp] * 8 + [i, i, i, i]
+            lib.oracle_stack_backward.argtypes = [dp] * 11 + [ctypes.c_double] + [dp] * 8 + [i, i, i, i, i]
             lib.oracle_num_threads.restype = ctypes.c_int
             lib.oracle_set_num_threads.argtypes = [i]
             _lib = lib
@@ -181,3 +185,64 @@ def moe_pffn(S, Wg, bg, eW1, eb1, eW2, eb2, return_gates: bool = False):
     _load().oracle_moe_pffn(_p(S), _p(Wg), _p(bg), _p(eW1), _p(eb1), _p(eW2), _p(eb2), _p(V), _p(G),
                             B, T, D, E, Fe)
     return (V, G) if return_gates else V
+
+
+GRAD_KEYS = ("dW1", "db1", "dW2", "db2", "dln1_g", "dln1_b", "dln2_g", "dln2_b")
+_PARAM_KEYS = ("W1", "b1", "W2", "b2", "ln1_g", "ln1_b", "ln2_g", "ln2_b")
+
+
+def gelu_grad(u) -> np.ndarray:
+    """Gelu'(u) = Phi(u) + u phi(u) ("RankMixer 详解（1）" section 5.2)."""
+    u = _f64(u)
+    out = np.empty_like(u)
+    _load().oracle_gelu_grad(_p(u), _p(out), u.size)
+    return out
+
+
+def layernorm_backward(R, gamma, Gout, eps: float = 1e-5):
+    """Row LayerNorm backward ("RankMixer 详解（1）" section 5.2): returns (dR, dgamma, dbeta)
+    for LN input rows R and output gradient Gout (the affine gradients summed over rows)."""
+    R, Gout = _f64(R), _f64(Gout)
+    D = R.shape[-1]
+    g = _f64(gamma)
+    dR = np.empty_like(R)
+    dg = np.empty(D)
+    db = np.empty(D)
+    _load().oracle_layernorm_backward(_p(R), _p(g), _p(Gout), float(eps), _p(dR), _p(dg), _p(db), R.size // D, D)
+    return dR, dg, db
+
+
+def _grad_arrays(T, D, F, lead=()):
+    shapes = {"dW1": (T, D, F), "db1": (T, F), "dW2": (T, F, D), "db2": (T, D),
+              "dln1_g": (D,), "dln1_b": (D,), "dln2_g": (D,), "dln2_b": (D,)}
+    return {k: np.empty(tuple(lead) + shapes[k]) for k in GRAD_KEYS}
+
+
+def block_backward(X, G, p: dict, eps: float = 1e-5):
+    """Backward of one block ("RankMixer 详解（1）" section 5.2) for the loss whose gradient at the
+    block output is G.  Returns (dX, grads) with grads keyed by GRAD_KEYS, each summed over
+    the batch: dW1 [T,D,F], db1 [T,F], dW2 [T,F,D], db2 [T,D], dln*_g / dln*_b [D]."""
+    X, G = _f64(X), _f64(G)
+    B, T, D = X.shape
+    a = {k: _f64(p[k]) for k in _PARAM_KEYS}
+    F = a["W1"].shape[-1]
+    dX = np.empty_like(X)
+    g = _grad_arrays(T, D, F)
+    _load().oracle_block_backward(_p(X), _p(G), _p(dX), *[_p(a[k]) for k in _PARAM_KEYS], float(eps),
+                                  *[_p(g[k]) for k in GRAD_KEYS], B, T, D, F)
+    return dX, g
+
+
+def stack_backward(X0, dpooled, layers: list, eps: float = 1e-5):
+    """Backward of L stacked blocks and the mean pool ("RankMixer 详解（1）" section 5.2):
+    returns (dX0, [grads of layer 0, ..., grads of layer L-1])."""
+    X0, dpooled = _f64(X0), _f64(dpooled)
+    B, T, D = X0.shape
+    L = len(layers)
+    cat = {k: _f64(np.stack([np.asarray(l[k], dtype=np.float64) for l in layers])) for k in _PARAM_KEYS}
+    F = cat["W1"].shape[-1]
+    dX0 = np.empty_like(X0)
+    g = _grad_arrays(T, D, F, (L,))
+    _load().oracle_stack_backward(_p(X0), _p(dpooled), _p(dX0), *[_p(cat[k]) for k in _PARAM_KEYS], float(eps),
+                                  *[_p(g[k]) for k in GRAD_KEYS], B, T, D, F, L)
+    return dX0, [{k: g[k][n] for k in GRAD_KEYS} for n in range(L)]

@@ -27,6 +27,9 @@
  * concession to speed is an OpenMP loop over independent samples.
  */
 #include <math.h>
+#ifndef M_PI
+#define M_PI 3.14159265358979323846
+#endif
 #include <stddef.h>
 #include <stdlib.h>
 #include <string.h>
@@ -283,6 +286,222 @@ ORACLE_API void oracle_moe_pffn(const double *S, const double *Wg, const double 
             }
         free(a); free(v); free(g);
     }
+}
+
+/* ================================================================== */
+/* Backward pass of one block, "RankMixer 详解（1）" section 5.2.        */
+/* ================================================================== */
+
+/* Gelu'(u) = Phi(u) + u phi(u), phi the standard normal density        */
+/* ([WT] section 5.2, derivative of the exact GELU).                   */
+static double gelu_grad(double u)
+{
+    const double Phi = 0.5 * (1.0 + erf(u / sqrt(2.0)));
+    const double phi = exp(-0.5 * u * u) / sqrt(2.0 * M_PI);
+    return Phi + u * phi;
+}
+
+ORACLE_API void oracle_gelu_grad(const double *u, double *out, size_t n)
+{
+    for (size_t i = 0; i < n; ++i) out[i] = gelu_grad(u[i]);
+}
+
+/* LayerNorm backward on one row ([WT] section 5.2).  r is the LN input, */
+/* g the gradient arriving at the LN output:                          */
+/*   rhat_j = (r_j - mu) / sqrt(var + eps),  q_j = g_j gamma_j,         */
+/*   dr_j = (q_j - mean(q) - rhat_j mean(q rhat)) / sqrt(var + eps),    */
+/* and the affine parameters receive g_j rhat_j (gamma) and g_j (beta), */
+/* added into dgamma / dbeta when those are not NULL.                  */
+static void layernorm_row_backward(const double *r, const double *gamma, const double *g, double eps,
+                                   double *dr, double *dgamma, double *dbeta, int D)
+{
+    double mu = 0.0;
+    for (int j = 0; j < D; ++j) mu += r[j];
+    mu /= (double)D;
+    double var = 0.0;
+    for (int j = 0; j < D; ++j) var += (r[j] - mu) * (r[j] - mu);
+    var /= (double)D;
+    const double inv = 1.0 / sqrt(var + eps);
+    double mq = 0.0, mqr = 0.0;
+    for (int j = 0; j < D; ++j) {
+        const double rh = (r[j] - mu) * inv;
+        const double qj = g[j] * gamma[j];
+        mq += qj;
+        mqr += qj * rh;
+    }
+    mq /= (double)D;
+    mqr /= (double)D;
+    for (int j = 0; j < D; ++j) {
+        const double rh = (r[j] - mu) * inv;
+        dr[j] = (g[j] * gamma[j] - mq - rh * mqr) * inv;
+        if (dgamma) dgamma[j] += g[j] * rh;
+        if (dbeta) dbeta[j] += g[j];
+    }
+}
+
+ORACLE_API void oracle_layernorm_backward(const double *R, const double *gamma, const double *Gout, double eps,
+                                          double *dR, double *dgamma, double *dbeta, int rows, int D)
+{
+    for (int j = 0; j < D; ++j) dgamma[j] = dbeta[j] = 0.0;
+    for (int i = 0; i < rows; ++i)
+        layernorm_row_backward(R + (size_t)i * D, gamma, Gout + (size_t)i * D, eps, dR + (size_t)i * D,
+                               dgamma, dbeta, D);
+}
+
+/* ------------------------------------------------------------------ */
+/* Block backward.  Given the block input X and G = dl/dX' at its output */
+/* (X' = LN2(PFFN(S) + S), S = LN1(Mix(X) + X), [RM] Eq. 1), returns     */
+/* dX = dl/dX and the parameter gradients summed over the batch.        */
+/* For row (b, t), with u = s W1 + b1, a = Gelu(u), z = a W2 + b2 + s:  */
+/*   dz  = LN2 backward of G[b,t]          (also the residual's share)  */
+/*   dW2 += a^T dz,  db2 += dz,  da = dz W2^T                          */
+/*   du  = da * Gelu'(u)                                                */
+/*   dW1 += s^T du,  db1 += du,  ds = du W1^T + dz                      */
+/*   dy  = LN1 backward of ds              (y = Mix(X)[t] + X[t])       */
+/* and finally dX = P^T dY + dY with P the mixing permutation           */
+/* ([WT] section 5.2: the transpose routes each coordinate back).       */
+/* Rows of one token only touch that token's weights, so the loop runs  */
+/* tokens in parallel and samples in order: the sums over b do not      */
+/* depend on the thread count.  Requires H = T.                         */
+/* ------------------------------------------------------------------ */
+ORACLE_API void oracle_block_backward(const double *X, const double *G, double *dX,
+                                      const double *W1, const double *b1, const double *W2, const double *b2,
+                                      const double *g1, const double *be1, const double *g2, const double *be2,
+                                      double eps,
+                                      double *dW1, double *db1, double *dW2, double *db2,
+                                      double *dg1, double *dbe1, double *dg2, double *dbe2,
+                                      int B, int T, int D, int F)
+{
+    const int q = D / T;
+    const size_t TD = (size_t)T * D;
+    double *dY = (double *)malloc(sizeof(double) * (size_t)B * TD);
+    /* per-token partial sums of the LayerNorm affine gradients */
+    double *pg1 = (double *)calloc(TD, sizeof(double));
+    double *pbe1 = (double *)calloc(TD, sizeof(double));
+    double *pg2 = (double *)calloc(TD, sizeof(double));
+    double *pbe2 = (double *)calloc(TD, sizeof(double));
+    memset(dW1, 0, sizeof(double) * TD * F);
+    memset(db1, 0, sizeof(double) * (size_t)T * F);
+    memset(dW2, 0, sizeof(double) * TD * F);
+    memset(db2, 0, sizeof(double) * TD);
+
+#pragma omp parallel
+    {
+        double *y = (double *)malloc(sizeof(double) * (size_t)(6 * D + 4 * F));
+        double *s = y + D, *z = s + D, *dz = z + D, *ds = dz + D, *dy = ds + D;
+        double *u = dy + D, *a = u + F, *da = a + F, *du = da + F;
+#pragma omp for schedule(dynamic, 1)
+        for (int t = 0; t < T; ++t) {
+            const double *W1t = W1 + (size_t)t * D * F, *b1t = b1 + (size_t)t * F;
+            const double *W2t = W2 + (size_t)t * F * D, *b2t = b2 + (size_t)t * D;
+            double *dW1t = dW1 + (size_t)t * D * F, *db1t = db1 + (size_t)t * F;
+            double *dW2t = dW2 + (size_t)t * F * D, *db2t = db2 + (size_t)t * D;
+            for (int b = 0; b < B; ++b) {
+                const double *x = X + (size_t)b * TD;
+                /* forward of row (b, t): Mix(X)[t][c q + r] = X[c][t q + r] */
+                for (int c = 0; c < T; ++c)
+                    for (int r = 0; r < q; ++r)
+                        y[c * q + r] = x[(size_t)c * D + (size_t)t * q + r] + x[(size_t)t * D + (size_t)c * q + r];
+                layernorm_row(y, g1, be1, eps, s, D);
+                for (int j = 0; j < F; ++j) u[j] = b1t[j];
+                for (int i = 0; i < D; ++i)
+                    for (int j = 0; j < F; ++j) u[j] += s[i] * W1t[(size_t)i * F + j];
+                for (int j = 0; j < F; ++j) a[j] = gelu(u[j]);
+                for (int j = 0; j < D; ++j) z[j] = b2t[j] + s[j];
+                for (int i = 0; i < F; ++i)
+                    for (int j = 0; j < D; ++j) z[j] += a[i] * W2t[(size_t)i * D + j];
+                /* backward */
+                layernorm_row_backward(z, g2, G + (size_t)b * TD + (size_t)t * D, eps, dz,
+                                       pg2 + (size_t)t * D, pbe2 + (size_t)t * D, D);
+                for (int i = 0; i < F; ++i) {
+                    double acc = 0.0;
+                    for (int j = 0; j < D; ++j) {
+                        dW2t[(size_t)i * D + j] += a[i] * dz[j];
+                        acc += dz[j] * W2t[(size_t)i * D + j];
+                    }
+                    da[i] = acc;
+                }
+                for (int j = 0; j < D; ++j) db2t[j] += dz[j];
+                for (int j = 0; j < F; ++j) {
+                    du[j] = da[j] * gelu_grad(u[j]);
+                    db1t[j] += du[j];
+                }
+                for (int i = 0; i < D; ++i) {
+                    double acc = dz[i];
+                    for (int j = 0; j < F; ++j) {
+                        dW1t[(size_t)i * F + j] += s[i] * du[j];
+                        acc += du[j] * W1t[(size_t)i * F + j];
+                    }
+                    ds[i] = acc;
+                }
+                layernorm_row_backward(y, g1, ds, eps, dy, pg1 + (size_t)t * D, pbe1 + (size_t)t * D, D);
+                memcpy(dY + (size_t)b * TD + (size_t)t * D, dy, sizeof(double) * D);
+            }
+        }
+        free(y);
+    }
+    /* dX = dY + P^T dY:  dX[t][c q + r] = dY[t][c q + r] + dY[c][t q + r] */
+    for (int b = 0; b < B; ++b) {
+        const double *g = dY + (size_t)b * TD;
+        double *o = dX + (size_t)b * TD;
+        for (int t = 0; t < T; ++t)
+            for (int c = 0; c < T; ++c)
+                for (int r = 0; r < q; ++r)
+                    o[(size_t)t * D + c * q + r] = g[(size_t)t * D + c * q + r] + g[(size_t)c * D + (size_t)t * q + r];
+    }
+    for (int j = 0; j < D; ++j) {
+        double s1 = 0.0, s2 = 0.0, s3 = 0.0, s4 = 0.0;
+        for (int t = 0; t < T; ++t) {
+            s1 += pg1[(size_t)t * D + j];
+            s2 += pbe1[(size_t)t * D + j];
+            s3 += pg2[(size_t)t * D + j];
+            s4 += pbe2[(size_t)t * D + j];
+        }
+        dg1[j] = s1; dbe1[j] = s2; dg2[j] = s3; dbe2[j] = s4;
+    }
+    free(dY); free(pg1); free(pbe1); free(pg2); free(pbe2);
+}
+
+/* ------------------------------------------------------------------ */
+/* Backward of L stacked blocks and the mean pool.  The pool hands each */
+/* token row the same share, dl/dX_L[t] = g_o / T ([WT] section 5.2);   */
+/* the blocks then run in reverse order, each fed its saved input.      */
+/* Gradient arrays are concatenated along a leading layer axis.         */
+/* ------------------------------------------------------------------ */
+ORACLE_API void oracle_stack_backward(const double *X0, const double *dpooled, double *dX0,
+                                      const double *W1, const double *b1, const double *W2, const double *b2,
+                                      const double *g1, const double *be1, const double *g2, const double *be2,
+                                      double eps,
+                                      double *dW1, double *db1, double *dW2, double *db2,
+                                      double *dg1, double *dbe1, double *dg2, double *dbe2,
+                                      int B, int T, int D, int F, int L)
+{
+    const size_t TD = (size_t)T * D, BTD = (size_t)B * TD;
+    double *Xs = (double *)malloc(sizeof(double) * BTD * (size_t)L);   /* input of each layer */
+    double *Gc = (double *)malloc(sizeof(double) * BTD);
+    double *Gn = (double *)malloc(sizeof(double) * BTD);
+    memcpy(Xs, X0, sizeof(double) * BTD);
+    for (int n = 0; n + 1 < L; ++n)
+        oracle_block_forward(Xs + (size_t)n * BTD, Xs + (size_t)(n + 1) * BTD, NULL,
+                             W1 + (size_t)n * TD * F, b1 + (size_t)n * T * F,
+                             W2 + (size_t)n * TD * F, b2 + (size_t)n * TD,
+                             g1 + (size_t)n * D, be1 + (size_t)n * D, g2 + (size_t)n * D, be2 + (size_t)n * D,
+                             eps, B, T, D, F);
+    for (int b = 0; b < B; ++b)
+        for (int t = 0; t < T; ++t)
+            for (int j = 0; j < D; ++j) Gc[(size_t)b * TD + (size_t)t * D + j] = dpooled[(size_t)b * D + j] / (double)T;
+    for (int n = L - 1; n >= 0; --n) {
+        oracle_block_backward(Xs + (size_t)n * BTD, Gc, n == 0 ? dX0 : Gn,
+                              W1 + (size_t)n * TD * F, b1 + (size_t)n * T * F,
+                              W2 + (size_t)n * TD * F, b2 + (size_t)n * TD,
+                              g1 + (size_t)n * D, be1 + (size_t)n * D, g2 + (size_t)n * D, be2 + (size_t)n * D, eps,
+                              dW1 + (size_t)n * TD * F, db1 + (size_t)n * T * F,
+                              dW2 + (size_t)n * TD * F, db2 + (size_t)n * TD,
+                              dg1 + (size_t)n * D, dbe1 + (size_t)n * D, dg2 + (size_t)n * D, dbe2 + (size_t)n * D,
+                              B, T, D, F);
+        double *tmp = Gc; Gc = Gn; Gn = tmp;
+    }
+    free(Xs); free(Gc); free(Gn);
 }
 
 ORACLE_API int oracle_num_threads(void)

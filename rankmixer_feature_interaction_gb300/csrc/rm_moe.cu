@@ -210,7 +210,7 @@ route_kernel(const Tin* __restrict__ S, long long s_sb, long long s_st, const fl
 constexpr int kRoute2Rows = 2;
 
 template <typename Tin, int NCH>
-__global__ void __launch_bounds__(kRouteWarps * 32)
+__global__ void __launch_bounds__(kRouteWarps * 32, 2)
 route2_kernel(const Tin* __restrict__ S, long long s_sb, long long s_st, const float* __restrict__ Wg,
               const float* __restrict__ bg, float* __restrict__ gates, int* __restrict__ counts,
               float* __restrict__ row_gate, int* __restrict__ slot_of, __half* __restrict__ Sg, int B, int T,
@@ -255,6 +255,12 @@ route2_kernel(const Tin* __restrict__ S, long long s_sb, long long s_st, const f
                         }
                     }
                 }
+                if (!std::is_same_v<Tin, __half>) {     // the chunk to fp16 for the copies
+                    h0[i] = make_uint4(pack_f16x2(x0[0], x0[1]), pack_f16x2(x0[2], x0[3]), pack_f16x2(x0[4], x0[5]),
+                                       pack_f16x2(x0[6], x0[7]));
+                    h1[i] = make_uint4(pack_f16x2(x1[0], x1[1]), pack_f16x2(x1[2], x1[3]), pack_f16x2(x1[4], x1[5]),
+                                       pack_f16x2(x1[6], x1[7]));
+                }
             }
             // 16 values: halve by lane bits 4, 3, 2, 1, then add the pair (bit 0)
 #pragma unroll
@@ -281,18 +287,6 @@ route2_kernel(const Tin* __restrict__ S, long long s_sb, long long s_st, const f
                 row_gate[(size_t)grp * Bcap + slot] = g;
             }
             if (mine) slot_of[((size_t)b * T + t) * E + e] = slot;
-            if (!std::is_same_v<Tin, __half>) {     // rows to fp16 for the copies
-#pragma unroll
-                for (int i = 0; i < NCH; ++i) {
-                    float x[8];
-                    to_f32x8_any<Tin>(h0[i], x);
-                    h0[i] = make_uint4(pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]),
-                                       pack_f16x2(x[6], x[7]));
-                    to_f32x8_any<Tin>(h1[i], x);
-                    h1[i] = make_uint4(pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]),
-                                       pack_f16x2(x[6], x[7]));
-                }
-            }
             unsigned m = __ballot_sync(0xffffffffu, open);
             while (m) {
                 const int l = __ffs(m) - 1;
