@@ -198,22 +198,33 @@ def run_ours(args):
     B = args.batch or c["B"]
     T, D, k = c["T"], c["D"], c["k"]
     moe = args.config == "moe_1b"
+    train = args.pass_ == "train"
+    if moe and train:
+        raise SystemExit("--pass train covers the dense stack (rankmixer_1b / rankmixer_100m)")
     L = args.layers or c["L"]
     E, Fe = c.get("E", 0), c.get("Fe", 0)
     # weak scaling: the job's batch is world * B samples, rank r owns shard r
     start, stop = shard_batch(world * B, world, rank)
     layers = synth.make_stack(T, D, k, L, 4242, "bf16", dev, E=E, Fe=Fe, active=c.get("active", 2.0))
-    m = RankMixer(T, D, k, layers, dtype="bf16", max_batch=B, n_experts=E, expert_hidden=Fe)
+    m = RankMixer(T, D, k, layers, dtype="bf16", max_batch=B, n_experts=E, expert_hidden=Fe, training=train)
     del layers
     torch.cuda.empty_cache()
     X0 = synth.make_input_shard(world * B, start, stop, T, D, 20260101, "bf16", dev)
     pooled = torch.empty((B, D), dtype=torch.float32, device=dev)
     S_in = X0  # MoE PFFN input (an LN1 output in the model; same distribution class for timing)
     V = torch.empty((B, T, D), dtype=torch.float32, device=dev) if moe else None
+    if train:
+        # the gradient of a batch-mean loss at the pooled output
+        dP = synth.make_output_grad((B, D), 20260102 + rank, scale=1.0 / (B * world), device=dev)
+        dX0 = torch.empty((B, T, D), dtype=torch.float32, device=dev)
+        grads = m.alloc_grads(dev)
 
     def step():
         if moe:
             m.moe_pffn_forward(0, S_in, V)
+        elif train:
+            m.stack_forward(X0, pooled)
+            m.stack_backward(X0, dP, dX0, grads)
         else:
             m.stack_forward(X0, pooled)
 
@@ -256,7 +267,33 @@ def run_ours(args):
 
     # ---- e2e through the host-buffer entry point -----------------------------------
     e2e = None
-    if not moe:
+    if train:
+        # host X0 and pooled-output gradient in, pooled output back: copies on the
+        # compute stream around the same forward + backward calls
+        Xh = X0.cpu().pin_memory()
+        dPh = dP.cpu().pin_memory()
+        ph = torch.empty((B, D), dtype=torch.float32).pin_memory()
+
+        def step_host():
+            X0.copy_(Xh, non_blocking=True)
+            dP.copy_(dPh, non_blocking=True)
+            m.stack_forward(X0, pooled)
+            m.stack_backward(X0, dP, dX0, grads)
+            ph.copy_(pooled, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        for _ in range(2):
+            step_host()
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            step_host()
+        t1 = time.perf_counter()
+        e2e = {"value": round(job_rate(B, world, args.steps, max_over_ranks(t1 - t0, dev)), 2), "unit": "samples/s",
+               "h2d_bytes_per_step": int(Xh.numel() * Xh.element_size() + dPh.numel() * dPh.element_size()),
+               "d2h_bytes_per_step": int(ph.numel() * ph.element_size())}
+    elif not moe:
         Xh = X0.cpu().pin_memory()
         ph = torch.empty((B, D), dtype=torch.float32).pin_memory()
         for _ in range(2):
@@ -276,6 +313,11 @@ def run_ours(args):
     peaks, peak_src = load_peaks()
     flops_gemm = 2.0 * B * T * D * (k * D)          # one GEMM launch of the dense PFFN (either layer)
     gemm_kinds = ["moe_gemm1", "moe_gemm2"] if moe else ["gemm1", "gemm2"]
+    # flops per timed scope: one GEMM, or two (the backward's data-gradient pair and recompute pair)
+    scope_flops = {"gemm1": flops_gemm, "gemm2": flops_gemm, "bwd_wgrad": flops_gemm,
+                   "bwd_dgrad": 2 * flops_gemm, "bwd_recompute": 2 * flops_gemm}
+    if train:
+        gemm_kinds = ["gemm1", "gemm2", "bwd_wgrad", "bwd_dgrad", "bwd_recompute"]
     dom = max(gemm_kinds, key=lambda kk: kstats[kk][1])
     launches, tot_ms = kstats[dom]
     active = None
@@ -288,24 +330,33 @@ def run_ours(args):
         flops_launch = per_layer
         flops_step = 2 * per_layer + 2.0 * B * T * D * E      # + router
     else:
-        flops_launch = flops_gemm
+        flops_launch = scope_flops[dom]
     roofline = None
     if launches > 0 and flops_launch:
         avg_ms = tot_ms / launches
         achieved = flops_launch / (avg_ms / 1e3) / 1e12
         peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
-        roofline = {"kernel": f"pffn_{dom}_tcgen05", "bound": "tensor", "achieved": round(achieved, 1),
+        kname = {"bwd_wgrad": "train_gemm_wgrad_tcgen05", "bwd_dgrad": "train_gemm_dgrad_tcgen05 (x2 per scope)",
+                 "bwd_recompute": "train_gemm_recompute_tcgen05 (x2 per scope)"}.get(dom, f"pffn_{dom}_tcgen05")
+        roofline = {"kernel": kname, "bound": "tensor", "achieved": round(achieved, 1),
                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                     "traffic": captured_traffic(args.config, B, L, dom),
                     "peak_source": f"{peak_src} bf16_tflops_sustained",
                     "avg_launch_ms": round(avg_ms, 4)}
+    flops_executed = None
     if not moe:
         flops_step = 4.0 * k * L * T * D * D * B
+        if train:
+            # algorithmic: forward + backward = 3 x the forward GEMM flops; executed adds
+            # the recompute (L - 1 forward blocks and both FFN layers of every block)
+            flops_executed = flops_step + 2.0 * flops_gemm * (L - 1) + 6.0 * flops_gemm * L
+            flops_step = 3.0 * flops_step
     gpu_launches = int(sum(v[0] for kk, v in kstats.items() if kk != "misc"))
+    what = "train step: fwd + bwd" if train else "fwd"
 
     out = {
-        "metric": "samples/s (RankMixer-1B-shape block stack fwd)" if args.config == "rankmixer_1b"
-        else f"samples/s ({args.config} {'MoE PFFN' if moe else 'block stack'} fwd)",
+        "metric": f"samples/s (RankMixer-1B-shape block stack {what})" if args.config == "rankmixer_1b"
+        else f"samples/s ({args.config} {'MoE PFFN' if moe else 'block stack'} {what})",
         "value": round(samples_per_s, 2),
         "unit": "samples/s",
         "n_gpus": world,
@@ -322,6 +373,8 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (X0 %.0f MB, weights %.0f MB > 129 MB)" % (
                        X0.numel() * 2 / 1e6, m.info.weight_bytes / 1e6)},
         "tflops": round(flops_step * args.steps * world / (ms_max / 1e3) / 1e12, 1),
+        "tflops_executed": round(flops_executed * args.steps * world / (ms_max / 1e3) / 1e12, 1)
+        if flops_executed else None,
         "frac_of_peak_step": round(
             flops_step * args.steps / (ms_max / 1e3) / 1e12 / peaks.get("bf16_tflops_sustained", 1700.0), 4),
         "roofline": roofline,
@@ -332,7 +385,7 @@ def run_ours(args):
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(args.config, B, args.cpu_seconds)
+        out["cpu_baseline"] = cpu_baseline(args.config, B, args.cpu_seconds, train=train)
     if rank == 0:
         print(json.dumps(out), flush=True)
     m.close()
@@ -343,7 +396,7 @@ def run_ours(args):
 # ----------------------------------------------------------------------------
 # CPU oracle baseline (bounded sample)
 # ----------------------------------------------------------------------------
-def cpu_baseline(config: str, B_full: int, seconds: float, n_steps: int = 1) -> dict:
+def cpu_baseline(config: str, B_full: int, seconds: float, n_steps: int = 1, train: bool = False) -> dict:
     import numpy as np
 
     import oracle
@@ -362,6 +415,9 @@ def cpu_baseline(config: str, B_full: int, seconds: float, n_steps: int = 1) -> 
         if moe:
             p = layers[0]
             oracle.moe_pffn(X, p["Wg"], p["bg"], p["eW1"], p["eb1"], p["eW2"], p["eb2"])
+        elif train:
+            oracle.stack_forward(X, layers)
+            oracle.stack_backward(X, np.full((nb, D), 1.0 / nb), layers)
         else:
             oracle.stack_forward(X, layers)
         return time.perf_counter() - t0
@@ -377,7 +433,8 @@ def cpu_baseline(config: str, B_full: int, seconds: float, n_steps: int = 1) -> 
         total_t += run(nb)
         total_n += nb
     return {"value": round(total_n / total_t, 3), "unit": "samples/s", "cores": cores, "kind": "oracle",
-            "sample": f"{nb} samples of the {config} workload per step (of B={B_full}), float64 oracle, "
+            "sample": f"{nb} samples of the {config} workload per step (of B={B_full}), float64 oracle"
+                      f"{' forward + backward' if train else ''}, "
                       f"OpenMP over samples on {cores} host threads, {n_steps} step(s), {total_t:.1f} s"}
 
 
@@ -391,11 +448,13 @@ def run_reference(args):
     steps = max(1, args.steps)
     # each step is a bounded sample; the whole run is kept to a few minutes
     per_step_s = min(args.cpu_seconds, 150.0 / (steps + args.warmup))
-    cb = cpu_baseline(args.config, B, per_step_s, n_steps=steps)
+    train = args.pass_ == "train"
+    cb = cpu_baseline(args.config, B, per_step_s, n_steps=steps, train=train)
+    what = "train step: fwd + bwd" if train else "fwd"
     out = {
         "impl": "reference",
-        "metric": "samples/s (RankMixer-1B-shape block stack fwd)" if args.config == "rankmixer_1b"
-        else f"samples/s ({args.config})",
+        "metric": f"samples/s (RankMixer-1B-shape block stack {what})" if args.config == "rankmixer_1b"
+        else f"samples/s ({args.config}{' ' + what if train else ''})",
         "value": cb["value"], "unit": "samples/s", "n_gpus": world, "steps": steps, "warmup": args.warmup,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)",
@@ -417,6 +476,8 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=0, help="override the number of layers (profiling captures)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU oracle budget per measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "train"], default="fwd",
+                    help="fwd: the forward stack (the headline); train: forward + backward of the stack")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

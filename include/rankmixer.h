@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define RM_ABI_VERSION 1
+#define RM_ABI_VERSION 2
 
 /* Public symbols are the only ones the shared library exports. */
 #if defined(__GNUC__)
@@ -81,7 +81,10 @@ typedef enum rm_gemm_path {
  * moe_layer_mask bit n makes layer n's PFFN the MoE variant inside
  * rm_block_forward / rm_stack_forward.  ln_eps is the LayerNorm epsilon
  * (1e-5 in the pages' worked example).  max_batch bounds B for every call
- * and sizes the context's workspace. */
+ * and sizes the context's workspace.  training != 0 makes the context keep a
+ * second copy of the dense weights in the pages' layout (bf16 for RM_BF16,
+ * float for RM_F32) for rm_block_backward / rm_stack_backward; their
+ * workspace is allocated at the first backward call. */
 typedef struct rm_config {
     int T;
     int D;
@@ -95,6 +98,7 @@ typedef struct rm_config {
     float ln_eps;
     int max_batch;
     rm_gemm_path gemm_path;
+    int training;
 } rm_config;
 
 /* Parameters of one layer, as DEVICE pointers in the context's dtype, laid
@@ -114,6 +118,16 @@ typedef struct rm_layer_params {
     const void *Wg, *bg;
     const void *eW1, *eb1, *eW2, *eb2;
 } rm_layer_params;
+
+/* Gradients of one dense layer's parameters, DEVICE float32 buffers in the
+ * layout of rm_layer_params ("RankMixer 详解（1）" section 5.2): each is the
+ * sum over the batch of the per-sample gradients, and is overwritten.
+ *   dW1 [T][D][kD], db1 [T][kD], dW2 [T][kD][D], db2 [T][D],
+ *   dln1_gamma, dln1_beta, dln2_gamma, dln2_beta [D]. */
+typedef struct rm_layer_grads {
+    float *dW1, *db1, *dW2, *db2;
+    float *dln1_gamma, *dln1_beta, *dln2_gamma, *dln2_beta;
+} rm_layer_grads;
 
 typedef struct rm_ctx rm_ctx;
 
@@ -141,7 +155,11 @@ typedef enum rm_kernel_kind {
     RM_K_MOE_GEMM2 = 8,  /* expert layer 2 + bias, gated, one packed row per (sample, token, open expert) */
     RM_K_MISC = 9,       /* copies, layout changes */
     RM_K_MOE_COMBINE = 10, /* sum of the open experts' gated rows per (sample, token), fixed expert order */
-    RM_K_COUNT = 11
+    RM_K_BWD_RECOMPUTE = 11, /* backward: LN1 and per-token FFN recompute (U, Gelu(U), Gelu'(U), Z) */
+    RM_K_BWD_DGRAD = 12,   /* backward: dA = dZ W2^T (times Gelu'), dS = dU W1^T + dZ */
+    RM_K_BWD_WGRAD = 13,   /* backward: dW2 = A^T dZ, dW1 = S^T dU */
+    RM_K_BWD_ROWS = 14,    /* backward: LN2 and LN1 + mixing backward, bias / affine reductions */
+    RM_K_COUNT = 15
 } rm_kernel_kind;
 
 typedef struct rm_kernel_stat {
@@ -193,6 +211,41 @@ RM_API rm_status rm_stack_forward_host(rm_ctx *ctx, const void *X0_host, float *
  * cfg.n_experts > 0. */
 RM_API rm_status rm_moe_pffn_forward(rm_ctx *ctx, int layer, const void *S, float *V_out, float *gates,
                               int B, void *stream);
+
+/* Backward pass of one dense block ("RankMixer 详解（1）" section 5.2) for
+ * the loss whose gradient at the block output X' is dX_out:
+ *   dZ = LN2 backward of dX_out           (Z = PFFN(S) + S)
+ *   dW2 = A^T dZ, db2 = sum dZ, dA = dZ W2^T, dU = dA * Gelu'(U)
+ *   dW1 = S^T dU, db1 = sum dU, dS = dU W1^T + dZ
+ *   dY = LN1 backward of dS               (Y = Mix(X) + X)
+ *   dX_in = dY + P^T dY                   (P the mixing permutation, H = T)
+ * The call recomputes the forward intermediates (S, U, Gelu(U), Z) from X_in
+ * in its own workspace; nothing from an earlier forward call is needed.
+ *   X_in:   device [B][T][D], context dtype (the block's input)
+ *   dX_out: device float32 [B][T][D]
+ *   dX_in:  device float32 [B][T][D] (may not overlap dX_out)
+ *   grads:  host struct of device float32 buffers (see rm_layer_grads);
+ *           the sums over the B samples are written, not accumulated.
+ * Requires cfg.training != 0 (RM_ERR_UNSUPPORTED otherwise) and a dense layer
+ * (RM_ERR_UNSUPPORTED for a Sparse-MoE layer).  bf16 contexts run every
+ * product with fp16 operands and float32 accumulation, the gradient operands
+ * carrying an exact power-of-two scale per token so that gradients of any
+ * magnitude keep fp16's 11 significant bits; float32 contexts run in
+ * float32.  The first call allocates the backward workspace for max_batch
+ * samples (RM_ERR_OOM if that fails).  Asynchronous on `stream`. */
+RM_API rm_status rm_block_backward(rm_ctx *ctx, int layer, const void *X_in, const float *dX_out, float *dX_in,
+                                   const rm_layer_grads *grads, int B, void *stream);
+
+/* Backward pass of the whole stack and the mean pool for the loss whose
+ * gradient at the pooled output is dpooled (device float32 [B][D]): the pool
+ * hands each token row dpooled / T, then the blocks run backward from the last
+ * layer to the first, each from its input X_n.  The call recomputes X_1 ..
+ * X_{L-1} with the forward chain of rm_stack_forward and keeps them in
+ * float32 (a workspace of L x max_batch x T x D floats).  dX0: device
+ * float32 [B][T][D]; grads: host array of cfg.L structs (layer n at
+ * grads[n]).  Same requirements and asynchrony as rm_block_backward. */
+RM_API rm_status rm_stack_backward(rm_ctx *ctx, const void *X0, const float *dpooled, float *dX0,
+                                   const rm_layer_grads *grads, int B, void *stream);
 
 /* Allocation-free variant of rm_block_forward (the paper has no counterpart;
  * this is a deployment aid).  For callers that cannot allocate device memory
@@ -255,6 +308,12 @@ RM_API rm_status rm_debug_wait_timeout(rm_ctx *ctx, int timeout_us, void *stream
  * (fp32x2) form of the tensor-core GEMM epilogues.  Asynchronous on `stream`;
  * RM_ERR_INVALID_ARG for n < 0, NULL buffers or another form. */
 RM_API rm_status rm_debug_gelu(const float *u, float *out, long long n, int form, void *stream);
+
+/* Test hook: out[2i] = Gelu(u[i]) and out[2i+1] = Gelu'(u[i]) = Phi(u) + u phi(u)
+ * as the backward pass computes them ("RankMixer 详解（1）" section 5.2; Phi by
+ * Abramowitz & Stegun 7.1.26).  u: device float32 [n]; out: device float32
+ * [2n].  Asynchronous on `stream`; RM_ERR_INVALID_ARG for n < 0 or NULL buffers. */
+RM_API rm_status rm_debug_gelu_grad(const float *u, float *out, long long n, void *stream);
 
 /* Message of the last failing call on this host thread ("" if none). */
 RM_API const char *rm_last_error(void);

@@ -34,25 +34,33 @@ RM_PATH_TCGEN05 = 2
 
 # rm_kernel_kind
 KERNEL_KINDS = ["mix_ln1", "gemm1", "gemm2", "ln2_out", "pool", "rowstats", "moe_route", "moe_gemm1",
-                "moe_gemm2", "misc", "moe_combine"]
+                "moe_gemm2", "misc", "moe_combine", "bwd_recompute", "bwd_dgrad", "bwd_wgrad", "bwd_rows"]
 RM_K_COUNT = len(KERNEL_KINDS)
 
 EXPORTED = ["rm_create", "rm_destroy", "rm_block_forward", "rm_stack_forward", "rm_stack_forward_host",
             "rm_moe_pffn_forward", "rm_token_mix", "rm_sync_status", "rm_get_info", "rm_profile_enable",
             "rm_profile_read", "rm_debug_wait_timeout", "rm_last_error", "rm_abi_version",
-            "rm_block_forward_noalloc", "rm_debug_gelu"]
+            "rm_block_forward_noalloc", "rm_debug_gelu", "rm_block_backward", "rm_stack_backward",
+            "rm_debug_gelu_grad"]
 
 
 class rm_config(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int), ("D", ctypes.c_int), ("H", ctypes.c_int), ("k", ctypes.c_int),
                 ("L", ctypes.c_int), ("n_experts", ctypes.c_int), ("expert_hidden", ctypes.c_int),
                 ("moe_layer_mask", ctypes.c_uint), ("dtype", ctypes.c_int), ("ln_eps", ctypes.c_float),
-                ("max_batch", ctypes.c_int), ("gemm_path", ctypes.c_int)]
+                ("max_batch", ctypes.c_int), ("gemm_path", ctypes.c_int), ("training", ctypes.c_int)]
 
 
 class rm_layer_params(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("W1", "b1", "W2", "b2", "ln1_gamma", "ln1_beta", "ln2_gamma",
                                                "ln2_beta", "Wg", "bg", "eW1", "eb1", "eW2", "eb2")]
+
+
+GRAD_FIELDS = ("dW1", "db1", "dW2", "db2", "dln1_gamma", "dln1_beta", "dln2_gamma", "dln2_beta")
+
+
+class rm_layer_grads(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in GRAD_FIELDS]
 
 
 class rm_info(ctypes.Structure):
@@ -101,6 +109,9 @@ def load() -> ctypes.CDLL:
         "rm_abi_version": (i, []),
         "rm_block_forward_noalloc": (st, [vp, i, vp, vp, i, vp]),
         "rm_debug_gelu": (st, [vp, vp, ctypes.c_longlong, ctypes.c_int, vp]),
+        "rm_block_backward": (st, [vp, i, vp, vp, vp, ctypes.POINTER(rm_layer_grads), i, vp]),
+        "rm_stack_backward": (st, [vp, vp, vp, vp, ctypes.POINTER(rm_layer_grads), i, vp]),
+        "rm_debug_gelu_grad": (st, [vp, vp, ctypes.c_longlong, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -180,6 +191,21 @@ def rm_debug_wait_timeout(ctx: int, timeout_us: int, stream: int) -> None:
 
 def rm_debug_gelu(u: int, out: int, n: int, form: int, stream: int) -> None:
     check(load().rm_debug_gelu(u, out, n, form, stream), "rm_debug_gelu")
+
+
+def rm_block_backward(ctx: int, layer: int, X_in: int, dX_out: int, dX_in: int, grads: rm_layer_grads | None,
+                      B: int, stream: int) -> None:
+    gp = ctypes.byref(grads) if grads is not None else None
+    check(load().rm_block_backward(ctx, layer, X_in, dX_out, dX_in, gp, B, stream), "rm_block_backward")
+
+
+def rm_stack_backward(ctx: int, X0: int, dpooled: int, dX0: int, grads: list | None, B: int, stream: int) -> None:
+    arr = (rm_layer_grads * len(grads))(*grads) if grads else None
+    check(load().rm_stack_backward(ctx, X0, dpooled, dX0, arr, B, stream), "rm_stack_backward")
+
+
+def rm_debug_gelu_grad(u: int, out: int, n: int, stream: int) -> None:
+    check(load().rm_debug_gelu_grad(u, out, n, stream), "rm_debug_gelu_grad")
 
 
 def rm_last_error() -> str:

@@ -40,7 +40,7 @@ class RankMixer:
 
     def __init__(self, T: int, D: int, k: int, layers: list, dtype: str = "bf16", eps: float = 1e-5,
                  max_batch: int = 4096, n_experts: int = 0, expert_hidden: int = 0, moe_layer_mask: int = 0,
-                 gemm_path: str = "auto", device: int = 0):
+                 gemm_path: str = "auto", device: int = 0, training: bool = False):
         self.tdtype, cdtype = _DTYPES[dtype]
         self.T, self.D, self.k, self.L = T, D, k, len(layers)
         self.E = n_experts
@@ -48,7 +48,7 @@ class RankMixer:
         self.device = torch.device("cuda", device)
         cfg = _lib.rm_config(T=T, D=D, H=T, k=k, L=len(layers), n_experts=n_experts, expert_hidden=expert_hidden,
                              moe_layer_mask=moe_layer_mask, dtype=cdtype, ln_eps=eps, max_batch=max_batch,
-                             gemm_path=_PATHS[gemm_path])
+                             gemm_path=_PATHS[gemm_path], training=1 if training else 0)
         cl = []
         for p in layers:
             lp = _lib.rm_layer_params()
@@ -105,6 +105,42 @@ class RankMixer:
         G = torch.empty((B, self.T, self.E), dtype=torch.float32, device=S.device) if return_gates else None
         _lib.rm_moe_pffn_forward(self.ctx, layer, _ptr(S), _ptr(V), _ptr(G), B, _stream())
         return (V, G) if return_gates else V
+
+    # -- backward calls (contexts created with training=True) -------------------------
+    def _grad_tensors(self, dev) -> tuple[dict, _lib.rm_layer_grads]:
+        T, D, F = self.T, self.D, self.k * self.D
+        shapes = {"dW1": (T, D, F), "db1": (T, F), "dW2": (T, F, D), "db2": (T, D), "dln1_g": (D,),
+                  "dln1_b": (D,), "dln2_g": (D,), "dln2_b": (D,)}
+        g = {k_: torch.empty(v, dtype=torch.float32, device=dev) for k_, v in shapes.items()}
+        c = _lib.rm_layer_grads(dW1=_ptr(g["dW1"]), db1=_ptr(g["db1"]), dW2=_ptr(g["dW2"]), db2=_ptr(g["db2"]),
+                                dln1_gamma=_ptr(g["dln1_g"]), dln1_beta=_ptr(g["dln1_b"]),
+                                dln2_gamma=_ptr(g["dln2_g"]), dln2_beta=_ptr(g["dln2_b"]))
+        return g, c
+
+    def block_backward(self, layer: int, X: torch.Tensor, G: torch.Tensor, dX: torch.Tensor | None = None):
+        """Gradients of one block for the loss whose gradient at the block output is G
+        (float32 [B, T, D]): returns (dX float32 [B, T, D], dict of the parameter gradients
+        dW1, db1, dW2, db2, dln1_g, dln1_b, dln2_g, dln2_b, each summed over the batch)."""
+        B = X.shape[0]
+        dX = torch.empty(X.shape, dtype=torch.float32, device=X.device) if dX is None else dX
+        g, c = self._grad_tensors(X.device)
+        _lib.rm_block_backward(self.ctx, layer, _ptr(X), _ptr(G), _ptr(dX), c, B, _stream())
+        return dX, g
+
+    def alloc_grads(self, device=None) -> list:
+        """Gradient buffers for every layer: a list of (dict of tensors, rm_layer_grads)."""
+        return [self._grad_tensors(device or self.device) for _ in range(self.L)]
+
+    def stack_backward(self, X0: torch.Tensor, dpooled: torch.Tensor, dX0: torch.Tensor | None = None,
+                       grads: list | None = None):
+        """Gradients of the stack and the mean pool for the loss whose gradient at the pooled
+        output is dpooled (float32 [B, D]): returns (dX0, [grads of layer 0 .. L-1]).  grads:
+        buffers from alloc_grads() to write into (new ones when None)."""
+        B = X0.shape[0]
+        dX0 = torch.empty(X0.shape, dtype=torch.float32, device=X0.device) if dX0 is None else dX0
+        pairs = self.alloc_grads(X0.device) if grads is None else grads
+        _lib.rm_stack_backward(self.ctx, _ptr(X0), _ptr(dpooled), _ptr(dX0), [c for _, c in pairs], B, _stream())
+        return dX0, [g for g, _ in pairs]
 
     # -- status / profiling --------------------------------------------------------
     def sync_status(self) -> int:

@@ -14,6 +14,7 @@
 #include "../../include/rankmixer.h"
 #include "rm_internal.h"
 #include "rm_moe.h"
+#include "rm_train.h"
 
 using namespace rm;
 
@@ -61,6 +62,35 @@ struct LayerW {
     float* g2 = nullptr;
     float* be2 = nullptr;
     MoeWeights moe;
+    // training contexts: the dense weights again, in the pages' layout, as fp16
+    // (bf16 contexts) or float, for the backward products
+    void* W1t = nullptr;   // [T][D][F]
+    void* W2t = nullptr;   // [T][F][D]
+};
+
+// Workspace of the backward pass (token-major [T][Bcap][W] activations),
+// allocated at the first backward call for max_batch samples.
+struct TrainWS {
+    bool ready = false;
+    void* S = nullptr;        // LN1 output, operand type                 [T][Bcap][D]
+    void* A = nullptr;        // Gelu(U), operand type                    [T][Bcap][F]
+    void* Gp = nullptr;       // Gelu'(U); overwritten by s_t dU          [T][Bcap][F]
+    void* Z = nullptr;        // FFN output + S (pre-LN2)                 [T][Bcap][D]
+    float* dZ32 = nullptr;    // LN2 input gradient                       [T][Bcap][D]
+    void* dZ = nullptr;       // s_t dZ in fp16 (bf16 contexts)           [T][Bcap][D]
+    float* dS = nullptr;      // gradient at the LN1 output               [T][Bcap][D]
+    float* pmax = nullptr;    // largest |dZ| per (token, row block)      [T][nblk2]
+    float* inv_scale = nullptr;   // 1 / s_t                              [T]
+    float* part2 = nullptr;   // LN2 partials: db2, dgamma2, dbeta2       3 x [T][nblk2][D]
+    float* tmpTD = nullptr;   // per-token sums before the sum over tokens [T][D]
+    float* colpart = nullptr; // db1 partials                             [T][rows][F]
+    float* part1 = nullptr;   // LN1 partials: dgamma1, dbeta1            2 x [grid1][D]
+    float* scratch1 = nullptr;// LN1 backward dY when it does not fit in shared memory
+    // stack backward: each later layer's input (float32) and the two gradient buffers
+    float* Xs = nullptr;      // [L][Bcap][T][D] (slot 0 unused)
+    float* G0 = nullptr;      // [Bcap][T][D]
+    float* G1 = nullptr;
+    int nblk2 = 0, colrows = 0, grid1 = 0;
 };
 
 struct Event {
@@ -88,6 +118,7 @@ struct rm_ctx {
     float2* rows = nullptr;      // merged: [T][Bcap] (mean, M2) of each full pre-LN2 row
     float* V = nullptr;          // MoE PFFN output inside the stack
     MoeWorkspace moe_ws;
+    TrainWS tw;
     // host-entry staging: device copies of X0 and pooled, the copy streams and
     // per-chunk events of the pipelined host entry
     void* X0_dev = nullptr;
@@ -129,6 +160,14 @@ void free_ctx(rm_ctx* c) {
         cudaFree(l.W1p); cudaFree(l.W2p); cudaFree(l.b1); cudaFree(l.b2);
         cudaFree(l.g1); cudaFree(l.be1); cudaFree(l.g2); cudaFree(l.be2);
         moe_free_weights(l.moe);
+        cudaFree(l.W1t); cudaFree(l.W2t);
+    }
+    {
+        TrainWS& t = c->tw;
+        cudaFree(t.S); cudaFree(t.A); cudaFree(t.Gp); cudaFree(t.Z); cudaFree(t.dZ32); cudaFree(t.dZ);
+        cudaFree(t.dS); cudaFree(t.pmax); cudaFree(t.inv_scale);
+        cudaFree(t.part2); cudaFree(t.tmpTD); cudaFree(t.colpart); cudaFree(t.part1); cudaFree(t.scratch1);
+        cudaFree(t.Xs); cudaFree(t.G0); cudaFree(t.G1);
     }
     moe_free_workspace(c->moe_ws);
     cudaFree(c->S); cudaFree(c->Hid); cudaFree(c->Z); cudaFree(c->stats); cudaFree(c->rows); cudaFree(c->V);
@@ -330,6 +369,21 @@ rm_status pack_layer(rm_ctx* c, const rm_layer_params& p, LayerW& w, cudaStream_
     RM_CHECK_CUDA(launch_to_f32(c->act, p.b1, w.b1, (size_t)T * F, s), "pack b1");
     RM_CHECK_CUDA(launch_to_f32(c->act, p.b2, w.b2, (size_t)T * D, s), "pack b2");
     for (int i = 0; i < 4; ++i) RM_CHECK_CUDA(launch_to_f32(c->act, lns[i], *lnp[i], (size_t)D, s), "pack LN");
+    if (g.training) {
+        // the caller's W1 [T][D][F] and W2 [T][F][D] in their layout: float as
+        // they are, bf16 converted to fp16 (exact apart from |w| < 2^-14)
+        const long long n = (long long)T * D * F;
+        const size_t wb = (size_t)n * c->esz;
+        if ((st = dmalloc(c, &w.W1t, wb, &c->weight_bytes)) != RM_OK) return st;
+        if ((st = dmalloc(c, &w.W2t, wb, &c->weight_bytes)) != RM_OK) return st;
+        if (c->act == Act::F32) {
+            RM_CHECK_CUDA(cudaMemcpyAsync(w.W1t, p.W1, wb, cudaMemcpyDeviceToDevice, s), "copy W1");
+            RM_CHECK_CUDA(cudaMemcpyAsync(w.W2t, p.W2, wb, cudaMemcpyDeviceToDevice, s), "copy W2");
+        } else {
+            RM_CHECK_CUDA(launch_bf16_to_f16(p.W1, w.W1t, n, s), "copy W1");
+            RM_CHECK_CUDA(launch_bf16_to_f16(p.W2, w.W2t, n, s), "copy W2");
+        }
+    }
     if (g.n_experts > 0) {
         if (!p.Wg || !p.bg || !p.eW1 || !p.eb1 || !p.eW2 || !p.eb2)
             return fail(RM_ERR_INVALID_ARG, "a Sparse-MoE parameter pointer is NULL");
@@ -338,6 +392,181 @@ rm_status pack_layer(rm_ctx* c, const rm_layer_params& p, LayerW& w, cudaStream_
         if (e != cudaSuccess) return cuda_fail(e, "pack MoE weights");
     }
     return RM_OK;
+}
+
+// ---- backward pass ------------------------------------------------------------------
+rm_status train_ws_ready(rm_ctx* c, bool stack) {
+    TrainWS& t = c->tw;
+    const rm_config& g = c->cfg;
+    const size_t T = g.T, D = g.D, F = c->F, Bc = c->Bcap;
+    const size_t osz = op_size(c->act);                    // operands, Gelu'(U) and Z: fp16 or float
+    rm_status st;
+    if (!t.ready) {
+        t.nblk2 = (c->Bcap + ln2_bwd_row_block() - 1) / ln2_bwd_row_block();
+        t.colrows = (c->Bcap + 127) / 128 * (128 / kTrainColpartRows);
+        t.grid1 = ln1_bwd_grid(c->Bcap, c->num_sms);
+        if ((st = dmalloc(c, &t.S, T * Bc * D * osz, &c->ws_bytes)) != RM_OK ||
+            (st = dmalloc(c, &t.A, T * Bc * F * osz, &c->ws_bytes)) != RM_OK ||
+            (st = dmalloc(c, &t.Gp, T * Bc * F * osz, &c->ws_bytes)) != RM_OK ||
+            (st = dmalloc(c, &t.Z, T * Bc * D * osz, &c->ws_bytes)) != RM_OK ||
+            (st = dmalloc(c, (void**)&t.dZ32, T * Bc * D * 4, &c->ws_bytes)) != RM_OK ||
+            (c->act != Act::F32 && (st = dmalloc(c, &t.dZ, T * Bc * D * osz, &c->ws_bytes)) != RM_OK) ||
+            (st = dmalloc(c, (void**)&t.dS, T * Bc * D * 4, &c->ws_bytes)) != RM_OK ||
+            (st = dmalloc(c, (void**)&t.pmax, T * (size_t)t.nblk2 * 4, &c->ws_bytes)) != RM_OK ||
+            (st = dmalloc(c, (void**)&t.inv_scale, T * 4, &c->ws_bytes)) != RM_OK ||
+            (st = dmalloc(c, (void**)&t.part2, 3 * T * (size_t)t.nblk2 * D * 4, &c->ws_bytes)) != RM_OK ||
+            (st = dmalloc(c, (void**)&t.tmpTD, T * D * 4, &c->ws_bytes)) != RM_OK ||
+            (st = dmalloc(c, (void**)&t.colpart, T * (size_t)t.colrows * F * 4, &c->ws_bytes)) != RM_OK ||
+            (st = dmalloc(c, (void**)&t.part1, 2 * (size_t)t.grid1 * D * 4, &c->ws_bytes)) != RM_OK)
+            return st;
+        if (ln1_bwd_needs_scratch(g.T, g.D) &&
+            (st = dmalloc(c, (void**)&t.scratch1, (size_t)t.grid1 * T * D * 4, &c->ws_bytes)) != RM_OK)
+            return st;
+        t.ready = true;
+    }
+    if (stack && !t.Xs) {
+        if ((st = dmalloc(c, (void**)&t.Xs, (size_t)g.L * Bc * T * D * 4, &c->ws_bytes)) != RM_OK ||
+            (st = dmalloc(c, (void**)&t.G0, Bc * T * D * 4, &c->ws_bytes)) != RM_OK ||
+            (st = dmalloc(c, (void**)&t.G1, Bc * T * D * 4, &c->ws_bytes)) != RM_OK)
+            return st;
+    }
+    return RM_OK;
+}
+
+rm_status check_grads(const rm_layer_grads* gr) {
+    if (!gr) return fail(RM_ERR_INVALID_ARG, "grads is NULL");
+    const float* p[8] = {gr->dW1, gr->db1, gr->dW2, gr->db2, gr->dln1_gamma, gr->dln1_beta, gr->dln2_gamma,
+                         gr->dln2_beta};
+    for (const float* q : p) {
+        if (!q) return fail(RM_ERR_INVALID_ARG, "a gradient buffer is NULL");
+        if (!aligned16(q)) return fail(RM_ERR_INVALID_ARG, "gradient buffers must be 16-byte aligned");
+    }
+    return RM_OK;
+}
+
+// One dense block backward (the steps of rm_block_backward), on `s`.  X is the
+// block input, sample-major, in the context dtype or (x_f32) in float32.
+rm_status block_backward_impl(rm_ctx* c, int layer, const void* X, bool x_f32, const float* G, float* dX,
+                              const rm_layer_grads& gr, int B, cudaStream_t s) {
+    const rm_config& g = c->cfg;
+    const LayerW& w = c->layers[layer];
+    TrainWS& t = c->tw;
+    const int T = g.T, D = g.D, F = c->F, Bc = c->Bcap;
+    const long long BcD = (long long)Bc * D, BcF = (long long)Bc * F, DF = (long long)D * F;
+    auto base = [&]() {
+        TrainGemm m{};
+        m.G = T;
+        m.err = c->d_err;
+        m.timeout_ns = kWaitTimeoutNs;
+        return m;
+    };
+    auto run = [&](int epi, const TrainGemm& m, bool* used_tc, const char* what) -> rm_status {
+        const bool tc = c->use_tc && train_tc_supported(m);
+        if (used_tc) *used_tc = tc;
+        cudaError_t e = tc ? launch_train_gemm_tc(epi, m, c->num_sms, s) : launch_train_gemm_simt(c->act, epi, m, s);
+        if (e != cudaSuccess) return cuda_fail(e, what);
+        return RM_OK;
+    };
+    rm_status st;
+    {   // recompute S = LN1(Mix(X) + X), U = S W1 + b1 (A = Gelu(U), Gp = Gelu'(U)), Z = A W2 + b2 + S
+        ProfScope ps(c, RM_K_BWD_RECOMPUTE, s);
+        RM_CHECK_CUDA(launch_ln1_recompute(c->act, x_f32, X, t.S, w.g1, w.be1, B, T, D, Bc, g.ln_eps, c->num_sms,
+                                           s),
+                      "ln1 recompute");
+        TrainGemm m = base();
+        m.M = B; m.N = F; m.K = D; m.m_valid = B;
+        m.a = {t.S, D, B, BcD, false};
+        m.b = {w.W1t, F, D, DF, true};
+        m.c_gpitch = BcF; m.c0 = t.A; m.c1 = t.Gp; m.bias = w.b1;
+        if ((st = run(TE_GELU2, m, nullptr, "ffn layer 1 recompute")) != RM_OK) return st;
+        m = base();
+        m.M = B; m.N = D; m.K = F; m.m_valid = B;
+        m.a = {t.A, F, B, BcF, false};
+        m.b = {w.W2t, D, F, DF, true};
+        m.c_gpitch = BcD; m.c0 = t.Z; m.r = t.S; m.bias = w.b2;
+        if ((st = run(TE_RESID, m, nullptr, "ffn layer 2 recompute")) != RM_OK) return st;
+    }
+    const int nblk = (B + ln2_bwd_row_block() - 1) / ln2_bwd_row_block();
+    float* p_db2 = t.part2;
+    float* p_dg2 = t.part2 + (size_t)T * t.nblk2 * D;
+    float* p_dbe2 = t.part2 + 2 * (size_t)T * t.nblk2 * D;
+    // dZ as a GEMM operand: float for float32 contexts; s_t dZ in fp16 otherwise
+    const void* dZop = t.dZ32;
+    const float* inv = nullptr;
+    {
+        ProfScope ps(c, RM_K_BWD_ROWS, s);
+        RM_CHECK_CUDA(launch_ln2_backward(c->act, t.Z, G, w.g2, t.dZ32, p_db2, p_dg2, p_dbe2, t.pmax, B, T, D, Bc,
+                                          g.ln_eps, s),
+                      "ln2 backward");
+        if (c->act != Act::F32) {
+            RM_CHECK_CUDA(launch_grad_scale(t.dZ32, t.pmax, nblk, t.inv_scale, t.dZ, B, T, D, Bc, s), "grad scale");
+            dZop = t.dZ;
+            inv = t.inv_scale;
+        }
+    }
+    {   // dW2 = A^T dZ
+        ProfScope ps(c, RM_K_BWD_WGRAD, s);
+        TrainGemm m = base();
+        m.M = F; m.N = D; m.K = B; m.m_valid = F;
+        m.a = {t.A, F, B, BcF, true};
+        m.b = {dZop, D, B, BcD, true};
+        m.c_gpitch = DF; m.c0 = gr.dW2; m.inv_scale = inv;
+        if ((st = run(TE_F32, m, nullptr, "dW2")) != RM_OK) return st;
+    }
+    bool db1_partials = false;
+    void* dU = t.Gp;      // s_t dU = (s_t dZ W2^T) * Gelu'(U) replaces Gelu'(U) element by element
+    {
+        ProfScope ps(c, RM_K_BWD_DGRAD, s);
+        TrainGemm m = base();
+        m.M = B; m.N = F; m.K = D; m.m_valid = B;
+        m.a = {dZop, D, B, BcD, false};
+        m.b = {w.W2t, D, F, DF, false};
+        m.c_gpitch = BcF; m.c0 = dU; m.r = t.Gp; m.inv_scale = inv;
+        const bool tc = c->use_tc && train_tc_supported(m);
+        m.colpart = tc ? t.colpart : gr.db1;
+        if ((st = run(TE_DGELU, m, &db1_partials, "dU")) != RM_OK) return st;
+        m = base();
+        m.M = B; m.N = D; m.K = F; m.m_valid = B;
+        m.a = {dU, F, B, BcF, false};
+        m.b = {w.W1t, F, D, DF, false};
+        m.c_gpitch = BcD; m.c0 = t.dS; m.r = t.dZ32; m.inv_scale = inv;
+        if ((st = run(TE_DRESID, m, nullptr, "dS")) != RM_OK) return st;
+    }
+    {   // dW1 = S^T dU
+        ProfScope ps(c, RM_K_BWD_WGRAD, s);
+        TrainGemm m = base();
+        m.M = D; m.N = F; m.K = B; m.m_valid = D;
+        m.a = {t.S, D, B, BcD, true};
+        m.b = {dU, F, B, BcF, true};
+        m.c_gpitch = DF; m.c0 = gr.dW1; m.inv_scale = inv;
+        if ((st = run(TE_F32, m, nullptr, "dW1")) != RM_OK) return st;
+    }
+    {
+        ProfScope ps(c, RM_K_BWD_ROWS, s);
+        const int grid1 = ln1_bwd_grid(B, c->num_sms);
+        float* p_dg1 = t.part1;
+        float* p_dbe1 = t.part1 + (size_t)t.grid1 * D;
+        RM_CHECK_CUDA(launch_ln1_mix_backward(c->act, x_f32, X, t.dS, w.g1, dX, p_dg1, p_dbe1, t.scratch1, B, T, D,
+                                              Bc, g.ln_eps, grid1, s),
+                      "ln1 + mixing backward");
+        if (db1_partials) {
+            const int rows = (B + 127) / 128 * (128 / kTrainColpartRows);
+            RM_CHECK_CUDA(launch_sum_rows(t.colpart, gr.db1, nullptr, T, rows, F, s), "db1");
+        }
+        RM_CHECK_CUDA(launch_sum_rows(p_db2, gr.db2, nullptr, T, nblk, D, s), "db2");
+        RM_CHECK_CUDA(launch_sum_rows(p_dg2, t.tmpTD, gr.dln2_gamma, T, nblk, D, s), "dgamma2");
+        RM_CHECK_CUDA(launch_sum_rows(p_dbe2, t.tmpTD, gr.dln2_beta, T, nblk, D, s), "dbeta2");
+        RM_CHECK_CUDA(launch_sum_rows(p_dg1, gr.dln1_gamma, nullptr, 1, grid1, D, s), "dgamma1");
+        RM_CHECK_CUDA(launch_sum_rows(p_dbe1, gr.dln1_beta, nullptr, 1, grid1, D, s), "dbeta1");
+    }
+    return RM_OK;
+}
+
+rm_status check_backward(rm_ctx* c, int B) {
+    rm_status st;
+    if ((st = check_ctx(c)) != RM_OK) return st;
+    if (!c->cfg.training) return fail(RM_ERR_UNSUPPORTED, "the context was created without cfg.training");
+    return check_batch(c, B);
 }
 
 }  // namespace
@@ -569,6 +798,100 @@ rm_status rm_moe_pffn_forward(rm_ctx* c, int layer, const void* S, float* V_out,
                                 [&](int kind) { return (void*)new ProfScope(c, kind, s); },
                                 [](void* p) { delete (ProfScope*)p; });
     if (e != cudaSuccess) return cuda_fail(e, "moe pffn");
+    return RM_OK;
+}
+
+rm_status rm_block_backward(rm_ctx* c, int layer, const void* X_in, const float* dX_out, float* dX_in,
+                            const rm_layer_grads* grads, int B, void* stream) {
+    rm_status st;
+    if ((st = check_backward(c, B)) != RM_OK) return st;
+    const rm_config& g = c->cfg;
+    if (layer < 0 || layer >= g.L) return fail(RM_ERR_INVALID_ARG, "layer %d out of range", layer);
+    if (g.moe_layer_mask & (1u << layer)) return fail(RM_ERR_UNSUPPORTED, "the backward pass covers dense layers");
+    if (!X_in || !dX_out || !dX_in) return fail(RM_ERR_INVALID_ARG, "X_in / dX_out / dX_in is NULL");
+    if (!aligned16(X_in) || !aligned16(dX_out) || !aligned16(dX_in))
+        return fail(RM_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+    if ((st = check_grads(grads)) != RM_OK) return st;
+    const size_t gb = (size_t)B * g.T * g.D * 4;
+    const char* gi = (const char*)dX_out;
+    const char* go = (const char*)dX_in;
+    if (gi < go + gb && go < gi + gb) return fail(RM_ERR_INVALID_ARG, "dX_out and dX_in overlap");
+    cudaSetDevice(c->device);
+    if ((st = train_ws_ready(c, false)) != RM_OK) return st;
+    return block_backward_impl(c, layer, X_in, false, dX_out, dX_in, *grads, B, as_stream(stream));
+}
+
+rm_status rm_stack_backward(rm_ctx* c, const void* X0, const float* dpooled, float* dX0, const rm_layer_grads* grads,
+                            int B, void* stream) {
+    rm_status st;
+    if ((st = check_backward(c, B)) != RM_OK) return st;
+    const rm_config& g = c->cfg;
+    if (g.moe_layer_mask != 0) return fail(RM_ERR_UNSUPPORTED, "the backward pass covers dense layers");
+    if (!X0 || !dpooled || !dX0) return fail(RM_ERR_INVALID_ARG, "X0 / dpooled / dX0 is NULL");
+    if (!aligned16(X0) || !aligned16(dpooled) || !aligned16(dX0))
+        return fail(RM_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+    if (!grads) return fail(RM_ERR_INVALID_ARG, "grads is NULL");
+    for (int n = 0; n < g.L; ++n)
+        if ((st = check_grads(grads + n)) != RM_OK) return st;
+    cudaSetDevice(c->device);
+    if ((st = train_ws_ready(c, true)) != RM_OK) return st;
+    cudaStream_t s = as_stream(stream);
+    TrainWS& t = c->tw;
+    const size_t xelems = (size_t)c->Bcap * g.T * g.D;
+    auto layer_input = [&](int n) -> const void* {
+        return n == 0 ? X0 : static_cast<const void*>(t.Xs + (size_t)n * xelems);
+    };
+    // the forward chain of the stack (fp16 Z and row statistics from layer to
+    // layer, as rm_stack_forward), keeping each later layer's input X_n in float32
+    for (int n = 0; n + 1 < g.L; ++n) {
+        MixLnArgs a = mix_args(c, n, B);
+        if (n == 0) {
+            a.X = X0;
+        } else {
+            a.Z = c->Z;
+            a.stats = c->rows;
+            a.g2 = c->layers[n - 1].g2;
+            a.be2 = c->layers[n - 1].be2;
+            a.nchunk = layer_nchunk(c, n - 1);
+            a.cw = layer_cw(c, n - 1);
+        }
+        {
+            ProfScope ps(c, RM_K_MIX_LN1, s);
+            RM_CHECK_CUDA(launch_mix_ln1(c->act, n > 0, a, c->num_sms, s), "mix+ln1");
+        }
+        if ((st = run_pffn(c, n, B, s)) != RM_OK) return st;
+        ProfScope ps(c, RM_K_LN2_OUT, s);
+        if (c->act == Act::F32)
+            RM_CHECK_CUDA(launch_ln2_out(c->act, c->Z, c->rows, c->layers[n].g2, c->layers[n].be2,
+                                         t.Xs + (size_t)(n + 1) * xelems, B, g.T, g.D, c->Bcap, 1, g.D, g.ln_eps,
+                                         c->num_sms, s),
+                          "ln2 out");
+        else
+            RM_CHECK_CUDA(launch_ln2_out_f32(c->Z, c->rows, c->layers[n].g2, c->layers[n].be2,
+                                             t.Xs + (size_t)(n + 1) * xelems, B, g.T, g.D, c->Bcap, g.ln_eps,
+                                             c->num_sms, s),
+                          "ln2 out");
+    }
+    {
+        ProfScope ps(c, RM_K_BWD_ROWS, s);
+        RM_CHECK_CUDA(launch_pool_backward(dpooled, t.G0, B, g.T, g.D, s), "pool backward");
+    }
+    float* gcur = t.G0;
+    float* gnext = t.G1;
+    for (int n = g.L - 1; n >= 0; --n) {
+        float* out = n == 0 ? dX0 : gnext;
+        if ((st = block_backward_impl(c, n, layer_input(n), n > 0, gcur, out, grads[n], B, s)) != RM_OK) return st;
+        float* tmp = gcur;
+        gcur = gnext;
+        gnext = tmp;
+    }
+    return RM_OK;
+}
+
+rm_status rm_debug_gelu_grad(const float* u, float* out, long long n, void* stream) {
+    if (n < 0) return fail(RM_ERR_INVALID_ARG, "n must be >= 0");
+    if (n > 0 && (!u || !out)) return fail(RM_ERR_INVALID_ARG, "u / out is NULL");
+    RM_CHECK_CUDA(launch_debug_gelu_grad(u, out, n, as_stream(stream)), "debug gelu grad");
     return RM_OK;
 }
 

@@ -1,0 +1,132 @@
+// Internal launcher interface of the block backward pass ("RankMixer 详解（1）"
+// section 5.2).  Not part of the public ABI.
+//
+// Every GEMM of the backward pass, and the forward recompute it starts with,
+// is a set of G independent per-token products
+//     C_g[m][n] = sum_k A_g(m, k) B_g(n, k)      (fp32 accumulate)
+// whose operands are either K-major (element (r, k) at r * inner + k) or
+// MN-major (element (r, k) at k * inner + r), so weight gradients read the
+// token-major activations [T][Bcap][W] and the caller-layout weights in place.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "rm_internal.h"
+
+namespace rm {
+
+// One operand of a grouped product.  K-major: inner = K, outer = the M (or N)
+// rows; MN-major: inner = M (or N), outer = the K rows.  Rows at or past
+// `outer` (and columns at or past `inner`) read as zero.  Group g starts
+// gpitch elements after group g - 1.
+struct TOperand {
+    const void* ptr;
+    int inner;
+    int outer;
+    long long gpitch;
+    bool mn;
+};
+
+// Operand precision.  float32 contexts run every product in float32.  bf16
+// contexts run them on fp16 operands (11 significant bits) with float32
+// accumulation: the recomputed activations S, Gelu(U), Gelu'(U) and Z are
+// O(1) and the weights convert from bf16 exactly (apart from values below
+// 2^-14 in magnitude); the two gradient operands dZ and dU carry a per-token
+// power-of-two scale s_t that brings token t's largest |dZ| to 2^9, so
+// gradients of any magnitude keep fp16's relative precision.  Products with a
+// scaled operand multiply their accumulator by inv_scale[g] = 1 / s_g (exact).
+//
+// Epilogues.  Row m, column n of group g of C, and of the row-aligned inputs
+// R / Gp, sit at g * c_gpitch + m * N + n; rows m >= m_valid are not stored.
+// "acc" below is the accumulator times inv_scale[g] where inv_scale is given.
+enum TrainEpi {
+    TE_GELU2 = 1,    // C0 = Gelu(acc + bias)  (operand type), C1 = Gelu'(acc + bias)  (aux type)
+    TE_RESID = 2,    // C0 = acc + bias + R    (aux type; R operand type)
+    TE_DGELU = 3,    // C0 = raw accumulator * Gp (operand type, stays in the scaled domain; Gp aux
+                     //      type), plus column partial sums of acc * Gp
+    TE_DRESID = 4,   // C0 = acc + R           (float; R float)
+    TE_F32 = 5,      // C0 = acc               (float)
+};
+
+struct TrainGemm {
+    int G, M, N, K;
+    int m_valid;
+    TOperand a, b;
+    long long c_gpitch;
+    void* c0;
+    void* c1;
+    const void* r;          // TE_RESID / TE_DRESID: residual rows; TE_DGELU: Gp
+    const float* bias;      // [G][N]
+    const float* inv_scale; // [G] or null (1)
+    // TE_DGELU: column sums of C0 over each block of `colpart_rows` rows of a
+    // tile, [G][ceil(M / colpart_rows)][N] (tensor-core path: 32-row blocks;
+    // the SIMT path writes the finished sums instead, see launch_train_gemm_simt)
+    float* colpart;
+    int* err;
+    unsigned long long timeout_ns;
+};
+
+// Rows of C summed into one TE_DGELU partial on the tensor-core path.
+constexpr int kTrainColpartRows = 32;
+
+// tcgen05 path: fp16 operands (A and B), N a multiple of 256, K-major inner
+// extents multiples of 64, MN-major inner extents multiples of 128 (A) / 256 (B).
+bool train_tc_supported(const TrainGemm& g);
+cudaError_t launch_train_gemm_tc(int epi, const TrainGemm& g, int num_sms, cudaStream_t s);
+
+// SIMT path for any shape: operands and aux values are float for F32 contexts
+// and fp16 for BF16 contexts.  TE_DGELU writes the finished column sums (over
+// all m_valid rows, unscaled) into colpart [G][N].
+cudaError_t launch_train_gemm_simt(Act act, int epi, const TrainGemm& g, cudaStream_t s);
+
+// ---- row kernels ---------------------------------------------------------------
+// S[t][b][:] = LN1(Mix(X[b])[t] + X[b][t]) in the operand type (fp16 for BF16
+// contexts).  X is sample-major in the caller dtype, or float when x_f32.
+cudaError_t launch_ln1_recompute(Act act, bool x_f32, const void* X, void* S, const float* g1, const float* be1,
+                                 int B, int T, int D, int Bcap, float eps, int num_sms, cudaStream_t s);
+
+// X_out[b][t][:] = LN2(Z[t][b][:]) in float32 from fp16 Z and merged row
+// statistics (the stack backward keeps every layer input in float32).
+cudaError_t launch_ln2_out_f32(const void* Z, const float2* stats, const float* g2, const float* be2, float* X_out,
+                               int B, int T, int D, int Bcap, float eps, int num_sms, cudaStream_t s);
+
+// LN2 backward.  Z [T][Bcap][D] (aux type), G sample-major [B][T][D] float:
+// dZ = LN2 backward of G (float, token-major), per (token, block of rows)
+// partial sums [T][nblk][D] of dZ, G * zhat and G, and the largest |dZ| of
+// each (token, block) in part_max [T][nblk].
+int ln2_bwd_row_block();
+cudaError_t launch_ln2_backward(Act act, const void* Z, const float* G, const float* g2, float* dZ, float* part_db2,
+                                float* part_dg2, float* part_dbe2, float* part_max, int B, int T, int D, int Bcap,
+                                float eps, cudaStream_t s);
+
+// Per-token scale of the gradient operands: s_t = 2^(9 - e) with 2^e >= the
+// largest |dZ| of token t (1 when it is 0); inv_scale[t] = 1 / s_t and
+// dZh[t][b][:] = fp16(s_t dZ[t][b][:]) for b < B.
+cudaError_t launch_grad_scale(const float* dZ, const float* part_max, int nblk, float* inv_scale, void* dZh, int B,
+                              int T, int D, int Bcap, cudaStream_t s);
+
+// LN1 and mixing backward.  X sample-major (caller dtype, or float when x_f32), dS [T][Bcap][D]
+// float: dY = LN1 backward of dS (y = Mix(X) + X recomputed), dX = dY + P^T dY
+// sample-major float.  Per-CTA partial sums [grid][D] of dS * yhat and dS
+// (grid from ln1_bwd_grid).  scratch: [grid][T][D] floats, used when a
+// sample's dY does not fit in shared memory (may be null otherwise).
+int ln1_bwd_grid(int B, int num_sms);
+bool ln1_bwd_needs_scratch(int T, int D);
+cudaError_t launch_ln1_mix_backward(Act act, bool x_f32, const void* X, const float* dS, const float* g1, float* dX,
+                                    float* part_dg1, float* part_dbe1, float* scratch, int B, int T, int D, int Bcap,
+                                    float eps, int grid, cudaStream_t s);
+
+// out[g][n] = sum over r < R of in[g][r][n] (fixed order), and, when
+// out_all is not null, out_all[n] = sum over g of out[g][n].
+cudaError_t launch_sum_rows(const float* in, float* out, float* out_all, int G, int R, int N, cudaStream_t s);
+
+// out[i] = fp16(in[i]) for n bf16 values (saturating at +-65504).
+cudaError_t launch_bf16_to_f16(const void* in, void* out, long long n, cudaStream_t s);
+
+// G[b][t][:] = dpooled[b][:] / T  (the mean pool's backward).
+cudaError_t launch_pool_backward(const float* dpooled, float* G, int B, int T, int D, cudaStream_t s);
+
+// Test hook: out[2i] = Gelu(u[i]), out[2i+1] = Gelu'(u[i]) as the backward epilogues compute them.
+cudaError_t launch_debug_gelu_grad(const float* u, float* out, long long n, cudaStream_t s);
+
+}  // namespace rm

@@ -1,0 +1,513 @@
+// Grouped fp16 GEMMs of the block backward pass on the 5th-generation tensor
+// cores (sm_103a): the forward recompute of the per-token FFN, the two
+// data-gradient products and the two weight-gradient products of
+// "RankMixer 详解（1）" section 5.2, per token t:
+//   recompute  U = S W1 + b1 (Act = Gelu(U), Gp = Gelu'(U)),  Z = Act W2 + b2 + S
+//   dA = dZ W2^T  -> dU = dA * Gp                 (A = dZ, K-major; B = W2 [F][D], K-major)
+//   dS = dU W1^T + dZ                             (A = dU, K-major; B = W1 [D][F], K-major)
+//   dW2 = Act^T dZ,  dW1 = S^T dU                 (A and B MN-major: K is the batch)
+// The recompute reads W1 [D][F] and W2 [F][D] as MN-major B operands, so a
+// single fp16 copy of the weights in the pages' layout serves every product.
+// dZ and dU carry a per-token power-of-two scale (see rm_train.h); the
+// epilogues of the products that read them multiply by its inverse.
+//
+// Kernel structure (one persistent CTA per SM, 12 warps, 128 x 256 tiles):
+//   warp 0      TMA producer: A and B tiles of one 64-deep k-block per stage
+//               (K-major: one box of 64 x rows; MN-major: boxes of 64 x 64,
+//               64 rows of the M/N dimension each) with the 128-byte swizzle
+//   warp 1      MMA issuer: lane 0 issues tcgen05.mma (M = 128, N = 256, K = 16)
+//               into a double-buffered TMEM accumulator
+//   warp 2      TMEM allocator
+//   warps 4-11  epilogue (warp w reads TMEM lanes 32 (w % 4) .. + 31, i.e. 32
+//               rows; the two warps of a lane quadrant split the 256 columns)
+// Every mbarrier wait is bounded in time; on expiry the CTA latches an error
+// word and all roles unwind.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+#include <string>
+
+#include "rm_common.cuh"
+#include "rm_train.h"
+#include "rm_train_math.cuh"
+
+namespace rm {
+namespace ttc {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 128 + 32 * kEpiWarps;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int MN_BOX_BYTES = 64 * BK * 2;          // one 64 (M/N) x 64 (K) box of an MN-major operand
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+constexpr int COLS_PER_WARP = BN / 2;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+static_assert(2 * STAGES * 8 + 4 * 8 + 8 <= BAR_BYTES, "barrier area");
+
+struct KArgs {
+    int G, M, N, K;
+    int m_valid;
+    int m_tiles, n_tiles;
+    long long tiles;
+    long long c_gpitch;
+    void* c0;
+    void* c1;
+    const void* r;
+    const float* bias;
+    const float* inv_scale;
+    float* colpart;
+    int colpart_rows;      // partial rows per group: ceil(M / 32)
+    int* err;
+    unsigned long long timeout_ns;
+};
+
+// Shared-memory descriptors, 128-byte swizzle (layout type 2, descriptor version 1).
+// K-major: 8-row core groups 1024 bytes apart (stride byte offset); the
+// leading byte offset is unused.  MN-major: each 64-element run of M (or N)
+// is one 64 x 64 box (8192 bytes, leading byte offset between runs); the
+// 8-row groups along K are 1024 bytes apart (stride byte offset).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)2u << 61;
+    return d;
+}
+
+// kind::f16 instruction descriptor: D f32, A and B fp16 (format 0), majors
+// (bit 15: A MN-major, bit 16: B MN-major), N >> 3, M >> 4.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_f16_any(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tile_of(long long tile, const KArgs& a, int& g, int& mb, int& nb) {
+    const long long per_group = (long long)a.m_tiles * a.n_tiles;
+    g = (int)(tile / per_group);
+    const int rem = (int)(tile - (long long)g * per_group);
+    mb = rem / a.n_tiles;          // N tiles fastest: neighbouring CTAs share the A tile
+    nb = rem - mb * a.n_tiles;
+}
+
+// Two floats to an fp16 pair, saturating at +-65504 instead of overflowing.
+__device__ __forceinline__ uint32_t f16x2_bits(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(sat_f16(lo), sat_f16(hi));
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// v[0..31] from 32 consecutive 16-bit values at p (64-byte aligned).  RO: the
+// kernel never writes them (read through the non-coherent path); otherwise a
+// plain load (the values are overwritten in place later in the same thread).
+template <typename T16, bool RO = true>
+__device__ __forceinline__ void load16x32(const T16* p, float (&v)[32]) {
+    const uint4* r4 = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint4 rr = RO ? __ldg(r4 + j) : r4[j];
+        const uint32_t w[4] = {rr.x, rr.y, rr.z, rr.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            if constexpr (std::is_same_v<T16, __half>) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[h]));
+                v[8 * j + 2 * h] = f.x;
+                v[8 * j + 2 * h + 1] = f.y;
+            } else {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[h]));
+                v[8 * j + 2 * h] = f.x;
+                v[8 * j + 2 * h + 1] = f.y;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void store16x32(void* dst, const uint32_t (&p)[16]) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) d4[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+}
+
+// Sum of v[c] over the 32 lanes for every c, left in lane c: five exchange
+// rounds, each halving the values a lane holds (31 shuffles for 32 sums).
+__device__ __forceinline__ float column_sums32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < o; ++i) {
+            const float send = upper ? v[i] : v[i + o];
+            const float keep = upper ? v[i + o] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return v[0];
+}
+
+// Epilogue of one warp: 32 rows (TMEM lanes) x COLS_PER_WARP columns from n0.
+template <int EPI>
+__device__ __forceinline__ void epilogue(const KArgs& a, int g, int m, bool valid, uint32_t tbase, int n0, int lane,
+                                         int quad, int mb) {
+    const size_t row = (size_t)g * (size_t)a.c_gpitch + (size_t)m * (size_t)a.N + (size_t)n0;
+    const float inv_s = a.inv_scale ? __ldg(a.inv_scale + g) : 1.0f;
+#pragma unroll 1
+    for (int c = 0; c < COLS_PER_WARP / 32; ++c) {
+        float v[32];
+        tmem_ld32(tbase + 32u * c, v);
+        const size_t off = row + 32 * c;
+        if (EPI == TE_GELU2) {
+            if (valid) {
+                const float* bias = a.bias + (size_t)g * a.N + n0 + 32 * c;
+                uint32_t pa[16], pg[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const GeluPair x0 = gelu_with_grad(fmaf(v[2 * j], inv_s, __ldg(bias + 2 * j)));
+                    const GeluPair x1 = gelu_with_grad(fmaf(v[2 * j + 1], inv_s, __ldg(bias + 2 * j + 1)));
+                    pa[j] = f16x2_bits(x0.value, x1.value);
+                    pg[j] = f16x2_bits(x0.grad, x1.grad);
+                }
+                store16x32(reinterpret_cast<__half*>(a.c0) + off, pa);
+                store16x32(reinterpret_cast<__half*>(a.c1) + off, pg);
+            }
+        } else if (EPI == TE_RESID) {
+            if (valid) {
+                const float* bias = a.bias + (size_t)g * a.N + n0 + 32 * c;
+                float rr[32];
+                load16x32(reinterpret_cast<const __half*>(a.r) + off, rr);
+                uint32_t p[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    p[j] = f16x2_bits(fmaf(v[2 * j], inv_s, __ldg(bias + 2 * j)) + rr[2 * j],
+                                      fmaf(v[2 * j + 1], inv_s, __ldg(bias + 2 * j + 1)) + rr[2 * j + 1]);
+                store16x32(reinterpret_cast<__half*>(a.c0) + off, p);
+            }
+        } else if (EPI == TE_DGELU) {
+            if (valid) {
+                float gp[32];
+                load16x32<__half, false>(reinterpret_cast<const __half*>(a.r) + off, gp);
+                uint32_t p[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    p[j] = f16x2_bits(v[2 * j] * gp[2 * j], v[2 * j + 1] * gp[2 * j + 1]);
+                    // sum what the next products read (the stored fp16 value), unscaled
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&p[j]));
+                    v[2 * j] = f.x * inv_s;
+                    v[2 * j + 1] = f.y * inv_s;
+                }
+                store16x32(reinterpret_cast<__half*>(a.c0) + off, p);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            }
+            const float s = column_sums32(v, lane);
+            const int prow = mb * (BM / 32) + quad;
+            a.colpart[((size_t)g * a.colpart_rows + prow) * a.N + n0 + 32 * c + lane] = s;
+        } else if (EPI == TE_DRESID) {
+            if (valid) {
+                const float4* r4 = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(a.r) + off);
+                float4* d4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.c0) + off);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 rr = __ldg(r4 + j);
+                    d4[j] = make_float4(fmaf(v[4 * j], inv_s, rr.x), fmaf(v[4 * j + 1], inv_s, rr.y),
+                                        fmaf(v[4 * j + 2], inv_s, rr.z), fmaf(v[4 * j + 3], inv_s, rr.w));
+                }
+            }
+        } else {   // TE_F32
+            if (valid) {
+                float4* d4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.c0) + off);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    d4[j] = make_float4(v[4 * j] * inv_s, v[4 * j + 1] * inv_s, v[4 * j + 2] * inv_s,
+                                        v[4 * j + 3] * inv_s);
+            }
+        }
+    }
+}
+
+template <int EPI, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(kThreads, 1)
+train_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const KArgs args) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t* base_ptr = smem_raw + (base - raw_addr);
+    const uint32_t sA = base;
+    const uint32_t sB = base + STAGES * A_BYTES;
+    const uint32_t bar0 = base + STAGES * STAGE_BYTES;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull_bar = [&](int x) { return bar0 + 8u * (2 * STAGES + x); };
+    auto tempty_bar = [&](int x) { return bar0 + 8u * (2 * STAGES + 2 + x); };
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 4));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(tfull_bar(x), 1);
+            mbar_init(tempty_bar(x), kEpiWarps * 32);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
+    const int kblocks = (args.K + BK - 1) / BK;
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------------
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (long long tile = blockIdx.x; ok && tile < args.tiles; tile += gridDim.x) {
+            int g, mb, nb;
+            tile_of(tile, args, g, mb, nb);
+            for (int kb = 0; kb < kblocks; ++kb) {
+                if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, args.err, args.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    const uint32_t fb = full_bar(stage);
+                    mbar_arrive_expect_tx(fb, (uint32_t)STAGE_BYTES);
+                    const uint32_t a_dst = sA + stage * A_BYTES;
+                    const uint32_t b_dst = sB + stage * B_BYTES;
+                    if (A_MN) {
+#pragma unroll
+                        for (int i = 0; i < BM / 64; ++i)
+                            tma_load_3d(&tmA, a_dst + i * MN_BOX_BYTES, fb, mb * BM + 64 * i, kb * BK, g);
+                    } else {
+                        tma_load_3d(&tmA, a_dst, fb, kb * BK, mb * BM, g);
+                    }
+                    if (B_MN) {
+#pragma unroll
+                        for (int i = 0; i < BN / 64; ++i)
+                            tma_load_3d(&tmB, b_dst + i * MN_BOX_BYTES, fb, nb * BN + 64 * i, kb * BK, g);
+                    } else {
+                        tma_load_3d(&tmB, b_dst, fb, kb * BK, nb * BN, g);
+                    }
+                }
+                __syncwarp();
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer --------------------------------
+        constexpr uint32_t idesc = idesc_f16(BM, BN, A_MN, B_MN);
+        // per 16-deep step: K-major operands advance 32 bytes inside the swizzled
+        // row, MN-major operands 16 rows of 128 bytes
+        constexpr uint32_t a_step = A_MN ? 2048u : 32u, b_step = B_MN ? 2048u : 32u;
+        constexpr uint32_t a_lbo = A_MN ? (uint32_t)MN_BOX_BYTES : 16u, b_lbo = B_MN ? (uint32_t)MN_BOX_BYTES : 16u;
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (long long tile = blockIdx.x; ok && tile < args.tiles; tile += gridDim.x) {
+            if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.err, args.timeout_ns)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+            for (int kb = 0; kb < kblocks; ++kb) {
+                if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, args.err, args.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a0 = sA + stage * A_BYTES;
+                const uint32_t b0 = sB + stage * B_BYTES;
+                if (lane == 0) {
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        umma_f16_any(d_tmem, sw128_desc(a0 + a_step * k, a_lbo, 1024u),
+                                  sw128_desc(b0 + b_step * k, b_lbo, 1024u), idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                    umma_commit(empty_bar(stage));
+                }
+                __syncwarp();
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            if (lane == 0) umma_commit(tfull_bar(acc));
+            __syncwarp();
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    } else if (warp >= 4) {
+        // ------------------------------ epilogue ----------------------------------
+        const int ew = warp - 4;
+        const int quad = warp & 3;
+        const int half = ew >> 2;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (long long tile = blockIdx.x; tile < args.tiles; tile += gridDim.x) {
+            int g, mb, nb;
+            tile_of(tile, args, g, mb, nb);
+            if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err, args.timeout_ns)) break;
+            tc_fence_after();
+            const int m = mb * BM + quad * 32 + lane;
+            const uint32_t tbase =
+                tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN + half * COLS_PER_WARP);
+            epilogue<EPI>(args, g, m, m < args.m_valid, tbase, nb * BN + half * COLS_PER_WARP, lane, quad, mb);
+            tc_fence_before();
+            mbar_arrive(tempty_bar(acc));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ----------------------------------------------------------------------------
+// Host side
+// ----------------------------------------------------------------------------
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool get_encoder() {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_encode) return true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return false;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return true;
+}
+
+// 3-D fp16 map {inner, outer, G} with the given box (inner box 64 = 128 bytes).
+bool make_map(CUtensorMap* m, const TOperand& op, int G, int box_outer) {
+    if (!get_encoder()) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)op.inner, (cuuint64_t)op.outer, (cuuint64_t)G};
+    cuuint64_t strides[2] = {(cuuint64_t)op.inner * 2, (cuuint64_t)op.gpitch * 2};
+    cuuint32_t box[3] = {64u, (cuuint32_t)box_outer, 1u};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(op.ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int EPI, bool A_MN, bool B_MN>
+cudaError_t run(const TrainGemm& g, const KArgs& ka, int num_sms, cudaStream_t s) {
+    CUtensorMap mA, mB;
+    if (!make_map(&mA, g.a, g.G, A_MN ? BK : BM)) return cudaErrorInvalidValue;
+    if (!make_map(&mB, g.b, g.G, B_MN ? BK : BN)) return cudaErrorInvalidValue;
+    auto k = train_gemm_tc_kernel<EPI, A_MN, B_MN>;
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    const long long grid = ka.tiles < num_sms ? ka.tiles : num_sms;
+    k<<<(int)grid, kThreads, SMEM_BYTES, s>>>(mA, mB, ka);
+    return cudaGetLastError();
+}
+
+}  // namespace ttc
+
+bool train_tc_supported(const TrainGemm& g) {
+    auto aligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (g.N % ttc::BN != 0 || g.M < 1 || g.K < 1 || g.G < 1) return false;
+    if (!aligned(g.a.ptr) || !aligned(g.b.ptr)) return false;
+    // K-major operands: K is the inner extent and must fill whole 64-deep k-blocks
+    if (!g.a.mn && (g.a.inner != g.K || g.K % ttc::BK != 0)) return false;
+    if (!g.b.mn && (g.b.inner != g.K || g.K % ttc::BK != 0)) return false;
+    // MN-major operands: whole 128-row (A) / 256-column (B) tiles of the inner extent
+    if (g.a.mn && (g.a.inner != g.M || g.M % ttc::BM != 0)) return false;
+    if (g.b.mn && (g.b.inner != g.N)) return false;
+    if (g.a.gpitch % 8 != 0 || g.b.gpitch % 8 != 0) return false;
+    return true;
+}
+
+cudaError_t launch_train_gemm_tc(int epi, const TrainGemm& g, int num_sms, cudaStream_t s) {
+    if (!train_tc_supported(g)) return cudaErrorNotSupported;
+    ttc::KArgs ka{};
+    ka.G = g.G;
+    ka.M = g.M;
+    ka.N = g.N;
+    ka.K = g.K;
+    ka.m_valid = g.m_valid;
+    ka.m_tiles = (g.m_valid + ttc::BM - 1) / ttc::BM;
+    ka.n_tiles = g.N / ttc::BN;
+    ka.tiles = (long long)g.G * ka.m_tiles * ka.n_tiles;
+    ka.c_gpitch = g.c_gpitch;
+    ka.c0 = g.c0;
+    ka.c1 = g.c1;
+    ka.r = g.r;
+    ka.bias = g.bias;
+    ka.inv_scale = g.inv_scale;
+    ka.colpart = g.colpart;
+    ka.colpart_rows = ka.m_tiles * (ttc::BM / kTrainColpartRows);
+    ka.err = g.err;
+    ka.timeout_ns = g.timeout_ns;
+    if (ka.tiles == 0) return cudaSuccess;
+    const bool amn = g.a.mn, bmn = g.b.mn;
+    switch (epi) {
+        case TE_GELU2:
+            if (!amn && bmn) return ttc::run<TE_GELU2, false, true>(g, ka, num_sms, s);
+            break;
+        case TE_RESID:
+            if (!amn && bmn) return ttc::run<TE_RESID, false, true>(g, ka, num_sms, s);
+            break;
+        case TE_DGELU:
+            if (!amn && !bmn) return ttc::run<TE_DGELU, false, false>(g, ka, num_sms, s);
+            break;
+        case TE_DRESID:
+            if (!amn && !bmn) return ttc::run<TE_DRESID, false, false>(g, ka, num_sms, s);
+            break;
+        case TE_F32:
+            if (amn && bmn) return ttc::run<TE_F32, true, true>(g, ka, num_sms, s);
+            break;
+        default: break;
+    }
+    return cudaErrorNotSupported;
+}
+
+}  // namespace rm

@@ -61,6 +61,11 @@ def make_input(B: int, T: int, D: int, seed: int, dtype: str = "bf16", device="c
     return _normal((B, T, D), 1.0, _gen(seed, device), device, TORCH_DTYPE[dtype])
 
 
+def make_output_grad(shape: tuple, seed: int, scale: float = 1.0, device="cpu") -> torch.Tensor:
+    """A seeded loss gradient at a block or pooled output: scale * N(0, 1), float32."""
+    return _normal(tuple(shape), scale, _gen(seed, device), device, torch.float32)
+
+
 SHARD_BLOCK = 64
 
 

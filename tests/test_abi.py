@@ -46,12 +46,12 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert _lib.rm_abi_version() == 1
+    assert _lib.rm_abi_version() == 2
 
 
 def _cfg(**kw):
     base = dict(T=4, D=8, H=4, k=2, L=1, n_experts=0, expert_hidden=0, moe_layer_mask=0, dtype=_lib.RM_F32,
-                ln_eps=1e-5, max_batch=16, gemm_path=_lib.RM_PATH_AUTO)
+                ln_eps=1e-5, max_batch=16, gemm_path=_lib.RM_PATH_AUTO, training=0)
     base.update(kw)
     return _lib.rm_config(**base)
 
@@ -107,6 +107,22 @@ def test_null_context_calls(lib):
     assert lib.rm_debug_gelu(None, None, 0, 2, None) == _lib.RM_ERR_INVALID_ARG      # unknown form
     assert lib.rm_debug_gelu(None, None, -1, 0, None) == _lib.RM_ERR_INVALID_ARG     # n < 0
     assert lib.rm_debug_gelu(None, None, 5, 1, None) == _lib.RM_ERR_INVALID_ARG      # NULL buffers
+    grads = _lib.rm_layer_grads()
+    assert lib.rm_block_backward(None, 0, None, None, None, ctypes.byref(grads), 1, None) == _lib.RM_ERR_INVALID_ARG
+    assert lib.rm_stack_backward(None, None, None, None, ctypes.byref(grads), 1, None) == _lib.RM_ERR_INVALID_ARG
+    assert lib.rm_debug_gelu_grad(None, None, -1, None) == _lib.RM_ERR_INVALID_ARG   # n < 0
+    assert lib.rm_debug_gelu_grad(None, None, 3, None) == _lib.RM_ERR_INVALID_ARG    # NULL buffers
+
+
+def test_config_struct_matches_the_header(lib):
+    """The binding's rm_config / rm_layer_grads mirror the header field by field."""
+    text = open(HEADER, encoding="utf-8").read()
+    body = re.search(r"typedef struct rm_config \{(.*?)\} rm_config;", text, flags=re.S).group(1)
+    fields = re.findall(r"(\w+);", body)
+    assert fields == [f for f, _ in _lib.rm_config._fields_]
+    body = re.search(r"typedef struct rm_layer_grads \{(.*?)\} rm_layer_grads;", text, flags=re.S).group(1)
+    names = re.findall(r"\*(\w+)", body)
+    assert names == [f for f, _ in _lib.rm_layer_grads._fields_]
 
 
 def test_binding_raises_with_status_and_message(lib):
