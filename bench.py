@@ -223,8 +223,8 @@ def run_ours(args):
         if moe:
             m.moe_pffn_forward(0, S_in, V)
         elif train:
-            m.stack_forward(X0, pooled)
-            m.stack_backward(X0, dP, dX0, grads)
+            m.stack_forward_train(X0, pooled)
+            m.stack_backward_saved(dP, dX0, grads)
         else:
             m.stack_forward(X0, pooled)
 
@@ -277,8 +277,8 @@ def run_ours(args):
         def step_host():
             X0.copy_(Xh, non_blocking=True)
             dP.copy_(dPh, non_blocking=True)
-            m.stack_forward(X0, pooled)
-            m.stack_backward(X0, dP, dX0, grads)
+            m.stack_forward_train(X0, pooled)
+            m.stack_backward_saved(dP, dX0, grads)
             ph.copy_(pooled, non_blocking=True)
             torch.cuda.current_stream().synchronize()
 
@@ -316,6 +316,7 @@ def run_ours(args):
     # flops per timed scope: one GEMM, or two (the backward's data-gradient pair and recompute pair)
     scope_flops = {"gemm1": flops_gemm, "gemm2": flops_gemm, "bwd_wgrad": flops_gemm,
                    "bwd_dgrad": 2 * flops_gemm, "bwd_recompute": 2 * flops_gemm}
+    # (bwd_recompute times the training forward of a layer: LN1 and both FFN layers)
     if train:
         gemm_kinds = ["gemm1", "gemm2", "bwd_wgrad", "bwd_dgrad", "bwd_recompute"]
     dom = max(gemm_kinds, key=lambda kk: kstats[kk][1])
@@ -337,7 +338,7 @@ def run_ours(args):
         achieved = flops_launch / (avg_ms / 1e3) / 1e12
         peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
         kname = {"bwd_wgrad": "train_gemm_wgrad_tcgen05", "bwd_dgrad": "train_gemm_dgrad_tcgen05 (x2 per scope)",
-                 "bwd_recompute": "train_gemm_recompute_tcgen05 (x2 per scope)"}.get(dom, f"pffn_{dom}_tcgen05")
+                 "bwd_recompute": "train_gemm_forward_tcgen05 (x2 per scope)"}.get(dom, f"pffn_{dom}_tcgen05")
         roofline = {"kernel": kname, "bound": "tensor", "achieved": round(achieved, 1),
                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                     "traffic": captured_traffic(args.config, B, L, dom),
@@ -347,9 +348,9 @@ def run_ours(args):
     if not moe:
         flops_step = 4.0 * k * L * T * D * D * B
         if train:
-            # algorithmic: forward + backward = 3 x the forward GEMM flops; executed adds
-            # the recompute (L - 1 forward blocks and both FFN layers of every block)
-            flops_executed = flops_step + 2.0 * flops_gemm * (L - 1) + 6.0 * flops_gemm * L
+            # forward + backward = 3 x the forward GEMM flops (the training forward keeps the
+            # activations, so no GEMM runs twice)
+            flops_executed = 3.0 * flops_step
             flops_step = 3.0 * flops_step
     gpu_launches = int(sum(v[0] for kk, v in kstats.items() if kk != "misc"))
     what = "train step: fwd + bwd" if train else "fwd"

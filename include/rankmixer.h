@@ -155,7 +155,7 @@ typedef enum rm_kernel_kind {
     RM_K_MOE_GEMM2 = 8,  /* expert layer 2 + bias, gated, one packed row per (sample, token, open expert) */
     RM_K_MISC = 9,       /* copies, layout changes */
     RM_K_MOE_COMBINE = 10, /* sum of the open experts' gated rows per (sample, token), fixed expert order */
-    RM_K_BWD_RECOMPUTE = 11, /* backward: LN1 and per-token FFN recompute (U, Gelu(U), Gelu'(U), Z) */
+    RM_K_BWD_RECOMPUTE = 11, /* training forward of a layer: LN1 and the per-token FFN keeping S, yhat, Gelu(U), Gelu'(U), Z */
     RM_K_BWD_DGRAD = 12,   /* backward: dA = dZ W2^T (times Gelu'), dS = dU W1^T + dZ */
     RM_K_BWD_WGRAD = 13,   /* backward: dW2 = A^T dZ, dW1 = S^T dU */
     RM_K_BWD_ROWS = 14,    /* backward: LN2 and LN1 + mixing backward, bias / affine reductions */
@@ -219,8 +219,8 @@ RM_API rm_status rm_moe_pffn_forward(rm_ctx *ctx, int layer, const void *S, floa
  *   dW1 = S^T dU, db1 = sum dU, dS = dU W1^T + dZ
  *   dY = LN1 backward of dS               (Y = Mix(X) + X)
  *   dX_in = dY + P^T dY                   (P the mixing permutation, H = T)
- * The call recomputes the forward intermediates (S, U, Gelu(U), Z) from X_in
- * in its own workspace; nothing from an earlier forward call is needed.
+ * The call runs the block's training forward (S, U, Gelu(U), Gelu'(U), Z)
+ * from X_in in its own workspace; nothing from an earlier call is needed.
  *   X_in:   device [B][T][D], context dtype (the block's input)
  *   dX_out: device float32 [B][T][D]
  *   dX_in:  device float32 [B][T][D] (may not overlap dX_out)
@@ -236,14 +236,35 @@ RM_API rm_status rm_moe_pffn_forward(rm_ctx *ctx, int layer, const void *S, floa
 RM_API rm_status rm_block_backward(rm_ctx *ctx, int layer, const void *X_in, const float *dX_out, float *dX_in,
                                    const rm_layer_grads *grads, int B, void *stream);
 
-/* Backward pass of the whole stack and the mean pool for the loss whose
- * gradient at the pooled output is dpooled (device float32 [B][D]): the pool
- * hands each token row dpooled / T, then the blocks run backward from the last
- * layer to the first, each from its input X_n.  The call recomputes X_1 ..
- * X_{L-1} with the forward chain of rm_stack_forward and keeps them in
- * float32 (a workspace of L x max_batch x T x D floats).  dX0: device
- * float32 [B][T][D]; grads: host array of cfg.L structs (layer n at
- * grads[n]).  Same requirements and asynchrony as rm_block_backward. */
+/* Training forward of the whole stack: pooled (device float32 [B][D]) = the
+ * mean-pooled output of rm_stack_forward, computed by the training kernels
+ * (fp16 operands, the same precision as the backward), and every layer's
+ * activations that its backward reads (S, the normalised LN1 input and its
+ * rstd, Gelu(U), Gelu'(U) and the pre-LN2 rows Z) kept in the context's
+ * training workspace for the next rm_stack_backward_saved call.  The first
+ * call allocates that workspace: per layer (4 + 2k) x max_batch x T x D
+ * half-precision values (float for RM_F32), about 4.4 GB per layer at
+ * T = 32, D = 1536, k = 4, max_batch = 4096.  X0: device [B][T][D], context
+ * dtype.  Requires cfg.training != 0 and dense layers (RM_ERR_UNSUPPORTED
+ * otherwise).  Asynchronous on `stream`. */
+RM_API rm_status rm_stack_forward_train(rm_ctx *ctx, const void *X0, float *pooled, int B, void *stream);
+
+/* Backward of the stack and the mean pool from the activations the last
+ * rm_stack_forward_train left ("RankMixer 详解（1）" section 5.2), for the
+ * loss whose gradient at its pooled output is dpooled (device float32
+ * [B][D]): the pool hands each token row dpooled / T, then the layers run
+ * backward from the last to the first.  dX0: device float32 [B][T][D];
+ * grads: host array of cfg.L structs (layer n at grads[n]), sums over the
+ * batch written, not accumulated.  B must be the training forward's batch;
+ * the call consumes the saved activations (a second call without a new
+ * training forward returns RM_ERR_INVALID_ARG).  Asynchronous on `stream`. */
+RM_API rm_status rm_stack_backward_saved(rm_ctx *ctx, const float *dpooled, float *dX0, const rm_layer_grads *grads,
+                                         int B, void *stream);
+
+/* rm_stack_forward_train on X0 (into a context-owned pooled buffer) followed by
+ * rm_stack_backward_saved: the gradients of the stack for a pooled-output
+ * gradient dpooled, from X0 alone.  Same arguments, requirements, workspace
+ * and asynchrony as those two calls. */
 RM_API rm_status rm_stack_backward(rm_ctx *ctx, const void *X0, const float *dpooled, float *dX0,
                                    const rm_layer_grads *grads, int B, void *stream);
 

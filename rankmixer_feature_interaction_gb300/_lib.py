@@ -41,7 +41,7 @@ EXPORTED = ["rm_create", "rm_destroy", "rm_block_forward", "rm_stack_forward", "
             "rm_moe_pffn_forward", "rm_token_mix", "rm_sync_status", "rm_get_info", "rm_profile_enable",
             "rm_profile_read", "rm_debug_wait_timeout", "rm_last_error", "rm_abi_version",
             "rm_block_forward_noalloc", "rm_debug_gelu", "rm_block_backward", "rm_stack_backward",
-            "rm_debug_gelu_grad"]
+            "rm_debug_gelu_grad", "rm_stack_forward_train", "rm_stack_backward_saved"]
 
 
 class rm_config(ctypes.Structure):
@@ -112,6 +112,8 @@ def load() -> ctypes.CDLL:
         "rm_block_backward": (st, [vp, i, vp, vp, vp, ctypes.POINTER(rm_layer_grads), i, vp]),
         "rm_stack_backward": (st, [vp, vp, vp, vp, ctypes.POINTER(rm_layer_grads), i, vp]),
         "rm_debug_gelu_grad": (st, [vp, vp, ctypes.c_longlong, vp]),
+        "rm_stack_forward_train": (st, [vp, vp, vp, i, vp]),
+        "rm_stack_backward_saved": (st, [vp, vp, vp, ctypes.POINTER(rm_layer_grads), i, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -202,6 +204,15 @@ def rm_block_backward(ctx: int, layer: int, X_in: int, dX_out: int, dX_in: int, 
 def rm_stack_backward(ctx: int, X0: int, dpooled: int, dX0: int, grads: list | None, B: int, stream: int) -> None:
     arr = (rm_layer_grads * len(grads))(*grads) if grads else None
     check(load().rm_stack_backward(ctx, X0, dpooled, dX0, arr, B, stream), "rm_stack_backward")
+
+
+def rm_stack_forward_train(ctx: int, X0: int, pooled: int, B: int, stream: int) -> None:
+    check(load().rm_stack_forward_train(ctx, X0, pooled, B, stream), "rm_stack_forward_train")
+
+
+def rm_stack_backward_saved(ctx: int, dpooled: int, dX0: int, grads: list | None, B: int, stream: int) -> None:
+    arr = (rm_layer_grads * len(grads))(*grads) if grads else None
+    check(load().rm_stack_backward_saved(ctx, dpooled, dX0, arr, B, stream), "rm_stack_backward_saved")
 
 
 def rm_debug_gelu_grad(u: int, out: int, n: int, stream: int) -> None:

@@ -142,6 +142,23 @@ class RankMixer:
         _lib.rm_stack_backward(self.ctx, _ptr(X0), _ptr(dpooled), _ptr(dX0), [c for _, c in pairs], B, _stream())
         return dX0, [g for g, _ in pairs]
 
+    def stack_forward_train(self, X0: torch.Tensor, pooled: torch.Tensor | None = None) -> torch.Tensor:
+        """Training forward of the stack: returns pooled (float32 [B, D]) and keeps every
+        layer's activations for the next stack_backward_saved call."""
+        B = X0.shape[0]
+        pooled = torch.empty((B, self.D), dtype=torch.float32, device=X0.device) if pooled is None else pooled
+        _lib.rm_stack_forward_train(self.ctx, _ptr(X0), _ptr(pooled), B, _stream())
+        return pooled
+
+    def stack_backward_saved(self, dpooled: torch.Tensor, dX0: torch.Tensor | None = None, grads: list | None = None):
+        """Backward from the last stack_forward_train's activations for the pooled-output
+        gradient dpooled: returns (dX0, [grads of layer 0 .. L-1])."""
+        B = dpooled.shape[0]
+        dX0 = torch.empty((B, self.T, self.D), dtype=torch.float32, device=dpooled.device) if dX0 is None else dX0
+        pairs = self.alloc_grads(dpooled.device) if grads is None else grads
+        _lib.rm_stack_backward_saved(self.ctx, _ptr(dpooled), _ptr(dX0), [c for _, c in pairs], B, _stream())
+        return dX0, [g for g, _ in pairs]
+
     # -- status / profiling --------------------------------------------------------
     def sync_status(self) -> int:
         return _lib.rm_sync_status(self.ctx, _stream())

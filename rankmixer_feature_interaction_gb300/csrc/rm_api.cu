@@ -68,14 +68,24 @@ struct LayerW {
     void* W2t = nullptr;   // [T][F][D]
 };
 
-// Workspace of the backward pass (token-major [T][Bcap][W] activations),
-// allocated at the first backward call for max_batch samples.
-struct TrainWS {
-    bool ready = false;
+// Activations one layer's backward reads (token-major [T][Bcap][W]): the
+// LN1 output and its normalised input, the FFN's Gelu(U) and Gelu'(U), and
+// the pre-LN2 rows.
+struct TrainSlot {
     void* S = nullptr;        // LN1 output, operand type                 [T][Bcap][D]
+    void* Yh = nullptr;       // normalised LN1 input yhat, fp16 / float  [T][Bcap][D]
+    float* rstd1 = nullptr;   // LN1 1 / sqrt(var + eps) per row          [T][Bcap]
     void* A = nullptr;        // Gelu(U), operand type                    [T][Bcap][F]
     void* Gp = nullptr;       // Gelu'(U); overwritten by s_t dU          [T][Bcap][F]
     void* Z = nullptr;        // FFN output + S (pre-LN2)                 [T][Bcap][D]
+};
+
+// Workspace of the backward pass, allocated at the first training call for
+// max_batch samples: slot 0 for rm_block_backward, one slot per layer for
+// the stack's training forward, and the buffers every layer's backward shares.
+struct TrainWS {
+    bool ready = false;
+    std::vector<TrainSlot> slots;
     float* dZ32 = nullptr;    // LN2 input gradient                       [T][Bcap][D]
     void* dZ = nullptr;       // s_t dZ in fp16 (bf16 contexts)           [T][Bcap][D]
     float* dS = nullptr;      // gradient at the LN1 output               [T][Bcap][D]
@@ -85,12 +95,13 @@ struct TrainWS {
     float* tmpTD = nullptr;   // per-token sums before the sum over tokens [T][D]
     float* colpart = nullptr; // db1 partials                             [T][rows][F]
     float* part1 = nullptr;   // LN1 partials: dgamma1, dbeta1            2 x [grid1][D]
-    float* scratch1 = nullptr;// LN1 backward dY when it does not fit in shared memory
-    // stack backward: each later layer's input (float32) and the two gradient buffers
-    float* Xs = nullptr;      // [L][Bcap][T][D] (slot 0 unused)
+    // the stack: the next layer's input (float32), the two gradient buffers, pooled scratch
+    float* Xn = nullptr;      // [Bcap][T][D]
     float* G0 = nullptr;      // [Bcap][T][D]
     float* G1 = nullptr;
+    float* pooled = nullptr;  // [Bcap][D]
     int nblk2 = 0, colrows = 0, grid1 = 0;
+    int saved_B = 0;          // batch of the activations rm_stack_forward_train left in the slots (0: none)
 };
 
 struct Event {
@@ -164,10 +175,12 @@ void free_ctx(rm_ctx* c) {
     }
     {
         TrainWS& t = c->tw;
-        cudaFree(t.S); cudaFree(t.A); cudaFree(t.Gp); cudaFree(t.Z); cudaFree(t.dZ32); cudaFree(t.dZ);
-        cudaFree(t.dS); cudaFree(t.pmax); cudaFree(t.inv_scale);
-        cudaFree(t.part2); cudaFree(t.tmpTD); cudaFree(t.colpart); cudaFree(t.part1); cudaFree(t.scratch1);
-        cudaFree(t.Xs); cudaFree(t.G0); cudaFree(t.G1);
+        for (auto& sl : t.slots) {
+            cudaFree(sl.S); cudaFree(sl.Yh); cudaFree(sl.rstd1); cudaFree(sl.A); cudaFree(sl.Gp); cudaFree(sl.Z);
+        }
+        cudaFree(t.dZ32); cudaFree(t.dZ); cudaFree(t.dS); cudaFree(t.pmax); cudaFree(t.inv_scale);
+        cudaFree(t.part2); cudaFree(t.tmpTD); cudaFree(t.colpart); cudaFree(t.part1);
+        cudaFree(t.Xn); cudaFree(t.G0); cudaFree(t.G1); cudaFree(t.pooled);
     }
     moe_free_workspace(c->moe_ws);
     cudaFree(c->S); cudaFree(c->Hid); cudaFree(c->Z); cudaFree(c->stats); cudaFree(c->rows); cudaFree(c->V);
@@ -395,21 +408,18 @@ rm_status pack_layer(rm_ctx* c, const rm_layer_params& p, LayerW& w, cudaStream_
 }
 
 // ---- backward pass ------------------------------------------------------------------
-rm_status train_ws_ready(rm_ctx* c, bool stack) {
+// nslots: how many activation slots the call needs (1 for a block, L for the stack).
+rm_status train_ws_ready(rm_ctx* c, int nslots, bool stack) {
     TrainWS& t = c->tw;
     const rm_config& g = c->cfg;
     const size_t T = g.T, D = g.D, F = c->F, Bc = c->Bcap;
-    const size_t osz = op_size(c->act);                    // operands, Gelu'(U) and Z: fp16 or float
+    const size_t osz = op_size(c->act);                    // operands, yhat, Gelu'(U) and Z: fp16 or float
     rm_status st;
     if (!t.ready) {
-        t.nblk2 = (c->Bcap + ln2_bwd_row_block() - 1) / ln2_bwd_row_block();
+        t.nblk2 = ln2_bwd_blocks(c->Bcap, g.T, c->num_sms);
         t.colrows = (c->Bcap + 127) / 128 * (128 / kTrainColpartRows);
         t.grid1 = ln1_bwd_grid(c->Bcap, c->num_sms);
-        if ((st = dmalloc(c, &t.S, T * Bc * D * osz, &c->ws_bytes)) != RM_OK ||
-            (st = dmalloc(c, &t.A, T * Bc * F * osz, &c->ws_bytes)) != RM_OK ||
-            (st = dmalloc(c, &t.Gp, T * Bc * F * osz, &c->ws_bytes)) != RM_OK ||
-            (st = dmalloc(c, &t.Z, T * Bc * D * osz, &c->ws_bytes)) != RM_OK ||
-            (st = dmalloc(c, (void**)&t.dZ32, T * Bc * D * 4, &c->ws_bytes)) != RM_OK ||
+        if ((st = dmalloc(c, (void**)&t.dZ32, T * Bc * D * 4, &c->ws_bytes)) != RM_OK ||
             (c->act != Act::F32 && (st = dmalloc(c, &t.dZ, T * Bc * D * osz, &c->ws_bytes)) != RM_OK) ||
             (st = dmalloc(c, (void**)&t.dS, T * Bc * D * 4, &c->ws_bytes)) != RM_OK ||
             (st = dmalloc(c, (void**)&t.pmax, T * (size_t)t.nblk2 * 4, &c->ws_bytes)) != RM_OK ||
@@ -419,15 +429,24 @@ rm_status train_ws_ready(rm_ctx* c, bool stack) {
             (st = dmalloc(c, (void**)&t.colpart, T * (size_t)t.colrows * F * 4, &c->ws_bytes)) != RM_OK ||
             (st = dmalloc(c, (void**)&t.part1, 2 * (size_t)t.grid1 * D * 4, &c->ws_bytes)) != RM_OK)
             return st;
-        if (ln1_bwd_needs_scratch(g.T, g.D) &&
-            (st = dmalloc(c, (void**)&t.scratch1, (size_t)t.grid1 * T * D * 4, &c->ws_bytes)) != RM_OK)
-            return st;
         t.ready = true;
     }
-    if (stack && !t.Xs) {
-        if ((st = dmalloc(c, (void**)&t.Xs, (size_t)g.L * Bc * T * D * 4, &c->ws_bytes)) != RM_OK ||
+    while ((int)t.slots.size() < nslots) {
+        t.slots.emplace_back();
+        TrainSlot& sl = t.slots.back();
+        if ((st = dmalloc(c, &sl.S, T * Bc * D * osz, &c->ws_bytes)) != RM_OK ||
+            (st = dmalloc(c, &sl.Yh, T * Bc * D * osz, &c->ws_bytes)) != RM_OK ||
+            (st = dmalloc(c, (void**)&sl.rstd1, T * Bc * 4, &c->ws_bytes)) != RM_OK ||
+            (st = dmalloc(c, &sl.A, T * Bc * F * osz, &c->ws_bytes)) != RM_OK ||
+            (st = dmalloc(c, &sl.Gp, T * Bc * F * osz, &c->ws_bytes)) != RM_OK ||
+            (st = dmalloc(c, &sl.Z, T * Bc * D * osz, &c->ws_bytes)) != RM_OK)
+            return st;
+    }
+    if (stack && !t.Xn) {
+        if ((st = dmalloc(c, (void**)&t.Xn, Bc * T * D * 4, &c->ws_bytes)) != RM_OK ||
             (st = dmalloc(c, (void**)&t.G0, Bc * T * D * 4, &c->ws_bytes)) != RM_OK ||
-            (st = dmalloc(c, (void**)&t.G1, Bc * T * D * 4, &c->ws_bytes)) != RM_OK)
+            (st = dmalloc(c, (void**)&t.G1, Bc * T * D * 4, &c->ws_bytes)) != RM_OK ||
+            (st = dmalloc(c, (void**)&t.pooled, Bc * D * 4, &c->ws_bytes)) != RM_OK)
             return st;
     }
     return RM_OK;
@@ -444,49 +463,65 @@ rm_status check_grads(const rm_layer_grads* gr) {
     return RM_OK;
 }
 
-// One dense block backward (the steps of rm_block_backward), on `s`.  X is the
-// block input, sample-major, in the context dtype or (x_f32) in float32.
-rm_status block_backward_impl(rm_ctx* c, int layer, const void* X, bool x_f32, const float* G, float* dX,
-                              const rm_layer_grads& gr, int B, cudaStream_t s) {
+TrainGemm train_gemm_base(rm_ctx* c) {
+    TrainGemm m{};
+    m.G = c->cfg.T;
+    m.err = c->d_err;
+    m.timeout_ns = kWaitTimeoutNs;
+    return m;
+}
+
+rm_status run_train_gemm(rm_ctx* c, int epi, const TrainGemm& m, bool* used_tc, const char* what, cudaStream_t s) {
+    const bool tc = c->use_tc && train_tc_supported(m);
+    if (used_tc) *used_tc = tc;
+    cudaError_t e = tc ? launch_train_gemm_tc(epi, m, c->num_sms, s) : launch_train_gemm_simt(c->act, epi, m, s);
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    return RM_OK;
+}
+
+// The forward of dense layer `layer` into activation slot `slot`, keeping
+// what its backward reads: S = LN1(Mix(X) + X) with yhat and rstd,
+// A = Gelu(U) and Gp = Gelu'(U) for U = S W1 + b1, and Z = A W2 + b2 + S.
+// X is the layer input, sample-major, in the context dtype or (x_f32) float32.
+rm_status train_layer_forward(rm_ctx* c, int layer, int slot, const void* X, bool x_f32, int B, cudaStream_t s) {
+    const rm_config& g = c->cfg;
+    const LayerW& w = c->layers[layer];
+    TrainSlot& sl = c->tw.slots[slot];
+    const int T = g.T, D = g.D, F = c->F, Bc = c->Bcap;
+    const long long BcD = (long long)Bc * D, BcF = (long long)Bc * F, DF = (long long)D * F;
+    ProfScope ps(c, RM_K_BWD_RECOMPUTE, s);
+    RM_CHECK_CUDA(launch_ln1_recompute(c->act, x_f32, X, sl.S, sl.Yh, sl.rstd1, w.g1, w.be1, B, T, D, Bc, g.ln_eps,
+                                       c->num_sms, s),
+                  "ln1 (training forward)");
+    rm_status st;
+    TrainGemm m = train_gemm_base(c);
+    m.M = B; m.N = F; m.K = D; m.m_valid = B;
+    m.a = {sl.S, D, B, BcD, false};
+    m.b = {w.W1t, F, D, DF, true};
+    m.c_gpitch = BcF; m.c0 = sl.A; m.c1 = sl.Gp; m.bias = w.b1;
+    if ((st = run_train_gemm(c, TE_GELU2, m, nullptr, "ffn layer 1 (training forward)", s)) != RM_OK) return st;
+    m = train_gemm_base(c);
+    m.M = B; m.N = D; m.K = F; m.m_valid = B;
+    m.a = {sl.A, F, B, BcF, false};
+    m.b = {w.W2t, D, F, DF, true};
+    m.c_gpitch = BcD; m.c0 = sl.Z; m.r = sl.S; m.bias = w.b2;
+    return run_train_gemm(c, TE_RESID, m, nullptr, "ffn layer 2 (training forward)", s);
+}
+
+// The backward of dense layer `layer` from the activations in slot `slot`
+// (written by train_layer_forward for the same batch): G = dl/dX' at the
+// layer output (float32 [B][T][D]) -> dX (float32 [B][T][D]) and the
+// parameter gradients.  Consumes the slot's Gelu'(U) (replaced by s_t dU).
+rm_status train_layer_backward(rm_ctx* c, int layer, int slot, const float* G, float* dX, const rm_layer_grads& gr,
+                               int B, cudaStream_t s) {
     const rm_config& g = c->cfg;
     const LayerW& w = c->layers[layer];
     TrainWS& t = c->tw;
+    TrainSlot& sl = t.slots[slot];
     const int T = g.T, D = g.D, F = c->F, Bc = c->Bcap;
     const long long BcD = (long long)Bc * D, BcF = (long long)Bc * F, DF = (long long)D * F;
-    auto base = [&]() {
-        TrainGemm m{};
-        m.G = T;
-        m.err = c->d_err;
-        m.timeout_ns = kWaitTimeoutNs;
-        return m;
-    };
-    auto run = [&](int epi, const TrainGemm& m, bool* used_tc, const char* what) -> rm_status {
-        const bool tc = c->use_tc && train_tc_supported(m);
-        if (used_tc) *used_tc = tc;
-        cudaError_t e = tc ? launch_train_gemm_tc(epi, m, c->num_sms, s) : launch_train_gemm_simt(c->act, epi, m, s);
-        if (e != cudaSuccess) return cuda_fail(e, what);
-        return RM_OK;
-    };
     rm_status st;
-    {   // recompute S = LN1(Mix(X) + X), U = S W1 + b1 (A = Gelu(U), Gp = Gelu'(U)), Z = A W2 + b2 + S
-        ProfScope ps(c, RM_K_BWD_RECOMPUTE, s);
-        RM_CHECK_CUDA(launch_ln1_recompute(c->act, x_f32, X, t.S, w.g1, w.be1, B, T, D, Bc, g.ln_eps, c->num_sms,
-                                           s),
-                      "ln1 recompute");
-        TrainGemm m = base();
-        m.M = B; m.N = F; m.K = D; m.m_valid = B;
-        m.a = {t.S, D, B, BcD, false};
-        m.b = {w.W1t, F, D, DF, true};
-        m.c_gpitch = BcF; m.c0 = t.A; m.c1 = t.Gp; m.bias = w.b1;
-        if ((st = run(TE_GELU2, m, nullptr, "ffn layer 1 recompute")) != RM_OK) return st;
-        m = base();
-        m.M = B; m.N = D; m.K = F; m.m_valid = B;
-        m.a = {t.A, F, B, BcF, false};
-        m.b = {w.W2t, D, F, DF, true};
-        m.c_gpitch = BcD; m.c0 = t.Z; m.r = t.S; m.bias = w.b2;
-        if ((st = run(TE_RESID, m, nullptr, "ffn layer 2 recompute")) != RM_OK) return st;
-    }
-    const int nblk = (B + ln2_bwd_row_block() - 1) / ln2_bwd_row_block();
+    const int nblk = ln2_bwd_blocks(B, T, c->num_sms);
     float* p_db2 = t.part2;
     float* p_dg2 = t.part2 + (size_t)T * t.nblk2 * D;
     float* p_dbe2 = t.part2 + 2 * (size_t)T * t.nblk2 * D;
@@ -495,8 +530,8 @@ rm_status block_backward_impl(rm_ctx* c, int layer, const void* X, bool x_f32, c
     const float* inv = nullptr;
     {
         ProfScope ps(c, RM_K_BWD_ROWS, s);
-        RM_CHECK_CUDA(launch_ln2_backward(c->act, t.Z, G, w.g2, t.dZ32, p_db2, p_dg2, p_dbe2, t.pmax, B, T, D, Bc,
-                                          g.ln_eps, s),
+        RM_CHECK_CUDA(launch_ln2_backward(c->act, sl.Z, G, w.g2, t.dZ32, p_db2, p_dg2, p_dbe2, t.pmax, B, T, D, Bc,
+                                          g.ln_eps, c->num_sms, s),
                       "ln2 backward");
         if (c->act != Act::F32) {
             RM_CHECK_CUDA(launch_grad_scale(t.dZ32, t.pmax, nblk, t.inv_scale, t.dZ, B, T, D, Bc, s), "grad scale");
@@ -506,48 +541,48 @@ rm_status block_backward_impl(rm_ctx* c, int layer, const void* X, bool x_f32, c
     }
     {   // dW2 = A^T dZ
         ProfScope ps(c, RM_K_BWD_WGRAD, s);
-        TrainGemm m = base();
+        TrainGemm m = train_gemm_base(c);
         m.M = F; m.N = D; m.K = B; m.m_valid = F;
-        m.a = {t.A, F, B, BcF, true};
+        m.a = {sl.A, F, B, BcF, true};
         m.b = {dZop, D, B, BcD, true};
         m.c_gpitch = DF; m.c0 = gr.dW2; m.inv_scale = inv;
-        if ((st = run(TE_F32, m, nullptr, "dW2")) != RM_OK) return st;
+        if ((st = run_train_gemm(c, TE_F32, m, nullptr, "dW2", s)) != RM_OK) return st;
     }
     bool db1_partials = false;
-    void* dU = t.Gp;      // s_t dU = (s_t dZ W2^T) * Gelu'(U) replaces Gelu'(U) element by element
+    void* dU = sl.Gp;     // s_t dU = (s_t dZ W2^T) * Gelu'(U) replaces Gelu'(U) element by element
     {
         ProfScope ps(c, RM_K_BWD_DGRAD, s);
-        TrainGemm m = base();
+        TrainGemm m = train_gemm_base(c);
         m.M = B; m.N = F; m.K = D; m.m_valid = B;
         m.a = {dZop, D, B, BcD, false};
         m.b = {w.W2t, D, F, DF, false};
-        m.c_gpitch = BcF; m.c0 = dU; m.r = t.Gp; m.inv_scale = inv;
+        m.c_gpitch = BcF; m.c0 = dU; m.r = sl.Gp; m.inv_scale = inv;
         const bool tc = c->use_tc && train_tc_supported(m);
         m.colpart = tc ? t.colpart : gr.db1;
-        if ((st = run(TE_DGELU, m, &db1_partials, "dU")) != RM_OK) return st;
-        m = base();
+        if ((st = run_train_gemm(c, TE_DGELU, m, &db1_partials, "dU", s)) != RM_OK) return st;
+        m = train_gemm_base(c);
         m.M = B; m.N = D; m.K = F; m.m_valid = B;
         m.a = {dU, F, B, BcF, false};
         m.b = {w.W1t, F, D, DF, false};
         m.c_gpitch = BcD; m.c0 = t.dS; m.r = t.dZ32; m.inv_scale = inv;
-        if ((st = run(TE_DRESID, m, nullptr, "dS")) != RM_OK) return st;
+        if ((st = run_train_gemm(c, TE_DRESID, m, nullptr, "dS", s)) != RM_OK) return st;
     }
     {   // dW1 = S^T dU
         ProfScope ps(c, RM_K_BWD_WGRAD, s);
-        TrainGemm m = base();
+        TrainGemm m = train_gemm_base(c);
         m.M = D; m.N = F; m.K = B; m.m_valid = D;
-        m.a = {t.S, D, B, BcD, true};
+        m.a = {sl.S, D, B, BcD, true};
         m.b = {dU, F, B, BcF, true};
         m.c_gpitch = DF; m.c0 = gr.dW1; m.inv_scale = inv;
-        if ((st = run(TE_F32, m, nullptr, "dW1")) != RM_OK) return st;
+        if ((st = run_train_gemm(c, TE_F32, m, nullptr, "dW1", s)) != RM_OK) return st;
     }
     {
         ProfScope ps(c, RM_K_BWD_ROWS, s);
         const int grid1 = ln1_bwd_grid(B, c->num_sms);
         float* p_dg1 = t.part1;
         float* p_dbe1 = t.part1 + (size_t)t.grid1 * D;
-        RM_CHECK_CUDA(launch_ln1_mix_backward(c->act, x_f32, X, t.dS, w.g1, dX, p_dg1, p_dbe1, t.scratch1, B, T, D,
-                                              Bc, g.ln_eps, grid1, s),
+        RM_CHECK_CUDA(launch_ln1_mix_backward(c->act, sl.Yh, sl.rstd1, t.dS, w.g1, dX, p_dg1, p_dbe1, B, T, D, Bc,
+                                              grid1, s),
                       "ln1 + mixing backward");
         if (db1_partials) {
             const int rows = (B + 127) / 128 * (128 / kTrainColpartRows);
@@ -558,6 +593,64 @@ rm_status block_backward_impl(rm_ctx* c, int layer, const void* X, bool x_f32, c
         RM_CHECK_CUDA(launch_sum_rows(p_dbe2, t.tmpTD, gr.dln2_beta, T, nblk, D, s), "dbeta2");
         RM_CHECK_CUDA(launch_sum_rows(p_dg1, gr.dln1_gamma, nullptr, 1, grid1, D, s), "dgamma1");
         RM_CHECK_CUDA(launch_sum_rows(p_dbe1, gr.dln1_beta, nullptr, 1, grid1, D, s), "dbeta1");
+    }
+    return RM_OK;
+}
+
+// The stack's training forward: every layer's activations into its slot; the
+// next layer's input X_{n+1} = LN2(Z_n) in float32; pooled from the last Z.
+rm_status stack_forward_train_impl(rm_ctx* c, const void* X0, float* pooled, int B, cudaStream_t s) {
+    const rm_config& g = c->cfg;
+    TrainWS& t = c->tw;
+    rm_status st;
+    t.saved_B = 0;
+    for (int n = 0; n < g.L; ++n) {
+        if ((st = train_layer_forward(c, n, n, n == 0 ? X0 : t.Xn, n > 0, B, s)) != RM_OK) return st;
+        const TrainSlot& sl = t.slots[n];
+        {
+            ProfScope ps(c, RM_K_ROWSTATS, s);
+            RM_CHECK_CUDA(launch_rowstats(c->act, sl.Z, c->rows, B, g.T, g.D, c->Bcap, c->num_sms, s), "row stats");
+        }
+        if (n + 1 < g.L) {
+            ProfScope ps(c, RM_K_LN2_OUT, s);
+            if (c->act == Act::F32)
+                RM_CHECK_CUDA(launch_ln2_out(c->act, sl.Z, c->rows, c->layers[n].g2, c->layers[n].be2, t.Xn, B, g.T,
+                                             g.D, c->Bcap, 1, g.D, g.ln_eps, c->num_sms, s),
+                              "ln2 out");
+            else
+                RM_CHECK_CUDA(launch_ln2_out_f32(sl.Z, c->rows, c->layers[n].g2, c->layers[n].be2, t.Xn, B, g.T, g.D,
+                                                 c->Bcap, g.ln_eps, c->num_sms, s),
+                              "ln2 out");
+        } else {
+            ProfScope ps(c, RM_K_POOL, s);
+            RM_CHECK_CUDA(launch_pool(c->act, sl.Z, c->rows, c->layers[n].g2, c->layers[n].be2, pooled, nullptr, B,
+                                      g.T, g.D, c->Bcap, 1, g.D, g.ln_eps, c->num_sms, c->d_err, kWaitTimeoutNs, s),
+                          "ln2 + pool");
+        }
+    }
+    t.saved_B = B;
+    return RM_OK;
+}
+
+// The stack's backward from the slots rm_stack_forward_train filled.
+rm_status stack_backward_saved_impl(rm_ctx* c, const float* dpooled, float* dX0, const rm_layer_grads* grads, int B,
+                                    cudaStream_t s) {
+    const rm_config& g = c->cfg;
+    TrainWS& t = c->tw;
+    rm_status st;
+    {
+        ProfScope ps(c, RM_K_BWD_ROWS, s);
+        RM_CHECK_CUDA(launch_pool_backward(dpooled, t.G0, B, g.T, g.D, s), "pool backward");
+    }
+    float* gcur = t.G0;
+    float* gnext = t.G1;
+    t.saved_B = 0;            // the backward consumes Gelu'(U) of every slot
+    for (int n = g.L - 1; n >= 0; --n) {
+        float* out = n == 0 ? dX0 : gnext;
+        if ((st = train_layer_backward(c, n, n, gcur, out, grads[n], B, s)) != RM_OK) return st;
+        float* tmp = gcur;
+        gcur = gnext;
+        gnext = tmp;
     }
     return RM_OK;
 }
@@ -817,8 +910,40 @@ rm_status rm_block_backward(rm_ctx* c, int layer, const void* X_in, const float*
     const char* go = (const char*)dX_in;
     if (gi < go + gb && go < gi + gb) return fail(RM_ERR_INVALID_ARG, "dX_out and dX_in overlap");
     cudaSetDevice(c->device);
-    if ((st = train_ws_ready(c, false)) != RM_OK) return st;
-    return block_backward_impl(c, layer, X_in, false, dX_out, dX_in, *grads, B, as_stream(stream));
+    if ((st = train_ws_ready(c, 1, false)) != RM_OK) return st;
+    cudaStream_t s = as_stream(stream);
+    c->tw.saved_B = 0;        // slot 0 is reused
+    if ((st = train_layer_forward(c, layer, 0, X_in, false, B, s)) != RM_OK) return st;
+    return train_layer_backward(c, layer, 0, dX_out, dX_in, *grads, B, s);
+}
+
+rm_status rm_stack_forward_train(rm_ctx* c, const void* X0, float* pooled, int B, void* stream) {
+    rm_status st;
+    if ((st = check_backward(c, B)) != RM_OK) return st;
+    if (c->cfg.moe_layer_mask != 0) return fail(RM_ERR_UNSUPPORTED, "the training path covers dense layers");
+    if (!X0 || !pooled) return fail(RM_ERR_INVALID_ARG, "X0 / pooled is NULL");
+    if (!aligned16(X0) || !aligned16(pooled)) return fail(RM_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+    cudaSetDevice(c->device);
+    if ((st = train_ws_ready(c, c->cfg.L, true)) != RM_OK) return st;
+    return stack_forward_train_impl(c, X0, pooled, B, as_stream(stream));
+}
+
+rm_status rm_stack_backward_saved(rm_ctx* c, const float* dpooled, float* dX0, const rm_layer_grads* grads, int B,
+                                  void* stream) {
+    rm_status st;
+    if ((st = check_backward(c, B)) != RM_OK) return st;
+    const rm_config& g = c->cfg;
+    if (!dpooled || !dX0) return fail(RM_ERR_INVALID_ARG, "dpooled / dX0 is NULL");
+    if (!aligned16(dpooled) || !aligned16(dX0)) return fail(RM_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+    if (!grads) return fail(RM_ERR_INVALID_ARG, "grads is NULL");
+    for (int n = 0; n < g.L; ++n)
+        if ((st = check_grads(grads + n)) != RM_OK) return st;
+    if (c->tw.saved_B == 0)
+        return fail(RM_ERR_INVALID_ARG, "no saved activations: call rm_stack_forward_train first (once per backward)");
+    if (c->tw.saved_B != B)
+        return fail(RM_ERR_INVALID_ARG, "B (%d) differs from the training forward's batch (%d)", B, c->tw.saved_B);
+    cudaSetDevice(c->device);
+    return stack_backward_saved_impl(c, dpooled, dX0, grads, B, as_stream(stream));
 }
 
 rm_status rm_stack_backward(rm_ctx* c, const void* X0, const float* dpooled, float* dX0, const rm_layer_grads* grads,
@@ -834,58 +959,10 @@ rm_status rm_stack_backward(rm_ctx* c, const void* X0, const float* dpooled, flo
     for (int n = 0; n < g.L; ++n)
         if ((st = check_grads(grads + n)) != RM_OK) return st;
     cudaSetDevice(c->device);
-    if ((st = train_ws_ready(c, true)) != RM_OK) return st;
+    if ((st = train_ws_ready(c, g.L, true)) != RM_OK) return st;
     cudaStream_t s = as_stream(stream);
-    TrainWS& t = c->tw;
-    const size_t xelems = (size_t)c->Bcap * g.T * g.D;
-    auto layer_input = [&](int n) -> const void* {
-        return n == 0 ? X0 : static_cast<const void*>(t.Xs + (size_t)n * xelems);
-    };
-    // the forward chain of the stack (fp16 Z and row statistics from layer to
-    // layer, as rm_stack_forward), keeping each later layer's input X_n in float32
-    for (int n = 0; n + 1 < g.L; ++n) {
-        MixLnArgs a = mix_args(c, n, B);
-        if (n == 0) {
-            a.X = X0;
-        } else {
-            a.Z = c->Z;
-            a.stats = c->rows;
-            a.g2 = c->layers[n - 1].g2;
-            a.be2 = c->layers[n - 1].be2;
-            a.nchunk = layer_nchunk(c, n - 1);
-            a.cw = layer_cw(c, n - 1);
-        }
-        {
-            ProfScope ps(c, RM_K_MIX_LN1, s);
-            RM_CHECK_CUDA(launch_mix_ln1(c->act, n > 0, a, c->num_sms, s), "mix+ln1");
-        }
-        if ((st = run_pffn(c, n, B, s)) != RM_OK) return st;
-        ProfScope ps(c, RM_K_LN2_OUT, s);
-        if (c->act == Act::F32)
-            RM_CHECK_CUDA(launch_ln2_out(c->act, c->Z, c->rows, c->layers[n].g2, c->layers[n].be2,
-                                         t.Xs + (size_t)(n + 1) * xelems, B, g.T, g.D, c->Bcap, 1, g.D, g.ln_eps,
-                                         c->num_sms, s),
-                          "ln2 out");
-        else
-            RM_CHECK_CUDA(launch_ln2_out_f32(c->Z, c->rows, c->layers[n].g2, c->layers[n].be2,
-                                             t.Xs + (size_t)(n + 1) * xelems, B, g.T, g.D, c->Bcap, g.ln_eps,
-                                             c->num_sms, s),
-                          "ln2 out");
-    }
-    {
-        ProfScope ps(c, RM_K_BWD_ROWS, s);
-        RM_CHECK_CUDA(launch_pool_backward(dpooled, t.G0, B, g.T, g.D, s), "pool backward");
-    }
-    float* gcur = t.G0;
-    float* gnext = t.G1;
-    for (int n = g.L - 1; n >= 0; --n) {
-        float* out = n == 0 ? dX0 : gnext;
-        if ((st = block_backward_impl(c, n, layer_input(n), n > 0, gcur, out, grads[n], B, s)) != RM_OK) return st;
-        float* tmp = gcur;
-        gcur = gnext;
-        gnext = tmp;
-    }
-    return RM_OK;
+    if ((st = stack_forward_train_impl(c, X0, c->tw.pooled, B, s)) != RM_OK) return st;
+    return stack_backward_saved_impl(c, dpooled, dX0, grads, B, s);
 }
 
 rm_status rm_debug_gelu_grad(const float* u, float* out, long long n, void* stream) {

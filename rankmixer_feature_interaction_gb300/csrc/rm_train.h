@@ -81,9 +81,12 @@ cudaError_t launch_train_gemm_simt(Act act, int epi, const TrainGemm& g, cudaStr
 
 // ---- row kernels ---------------------------------------------------------------
 // S[t][b][:] = LN1(Mix(X[b])[t] + X[b][t]) in the operand type (fp16 for BF16
-// contexts).  X is sample-major in the caller dtype, or float when x_f32.
-cudaError_t launch_ln1_recompute(Act act, bool x_f32, const void* X, void* S, const float* g1, const float* be1,
-                                 int B, int T, int D, int Bcap, float eps, int num_sms, cudaStream_t s);
+// contexts), with the normalised row yhat (fp16, or float for F32 contexts)
+// in Yh [T][Bcap][D] and 1 / sqrt(var + eps) in rstd [T][Bcap].  X is
+// sample-major in the caller dtype, or float when x_f32.
+cudaError_t launch_ln1_recompute(Act act, bool x_f32, const void* X, void* S, void* Yh, float* rstd, const float* g1,
+                                 const float* be1, int B, int T, int D, int Bcap, float eps, int num_sms,
+                                 cudaStream_t s);
 
 // X_out[b][t][:] = LN2(Z[t][b][:]) in float32 from fp16 Z and merged row
 // statistics (the stack backward keeps every layer input in float32).
@@ -91,13 +94,14 @@ cudaError_t launch_ln2_out_f32(const void* Z, const float2* stats, const float* 
                                int B, int T, int D, int Bcap, float eps, int num_sms, cudaStream_t s);
 
 // LN2 backward.  Z [T][Bcap][D] (aux type), G sample-major [B][T][D] float:
-// dZ = LN2 backward of G (float, token-major), per (token, block of rows)
-// partial sums [T][nblk][D] of dZ, G * zhat and G, and the largest |dZ| of
-// each (token, block) in part_max [T][nblk].
-int ln2_bwd_row_block();
+// dZ = LN2 backward of G (float, token-major); per (token, CTA) partial sums
+// [T][nblk][D] of dZ, G * zhat and G, and the largest |dZ| of each (token,
+// CTA) in part_max [T][nblk], nblk = ln2_bwd_blocks(B, T, num_sms) (which
+// never exceeds ln2_bwd_blocks(max_batch, T, num_sms)).
+int ln2_bwd_blocks(int B, int T, int num_sms);
 cudaError_t launch_ln2_backward(Act act, const void* Z, const float* G, const float* g2, float* dZ, float* part_db2,
                                 float* part_dg2, float* part_dbe2, float* part_max, int B, int T, int D, int Bcap,
-                                float eps, cudaStream_t s);
+                                float eps, int num_sms, cudaStream_t s);
 
 // Per-token scale of the gradient operands: s_t = 2^(9 - e) with 2^e >= the
 // largest |dZ| of token t (1 when it is 0); inv_scale[t] = 1 / s_t and
@@ -105,16 +109,14 @@ cudaError_t launch_ln2_backward(Act act, const void* Z, const float* G, const fl
 cudaError_t launch_grad_scale(const float* dZ, const float* part_max, int nblk, float* inv_scale, void* dZh, int B,
                               int T, int D, int Bcap, cudaStream_t s);
 
-// LN1 and mixing backward.  X sample-major (caller dtype, or float when x_f32), dS [T][Bcap][D]
-// float: dY = LN1 backward of dS (y = Mix(X) + X recomputed), dX = dY + P^T dY
-// sample-major float.  Per-CTA partial sums [grid][D] of dS * yhat and dS
-// (grid from ln1_bwd_grid).  scratch: [grid][T][D] floats, used when a
-// sample's dY does not fit in shared memory (may be null otherwise).
+// LN1 and mixing backward from the recompute's yhat and rstd: dS [T][Bcap][D]
+// float, dX = dY + P^T dY sample-major float with dY the LN1 backward of dS.
+// Per-CTA partial sums [grid][D] of dS * yhat and dS, grid from ln1_bwd_grid
+// (which never exceeds ln1_bwd_grid(max_batch, num_sms)).
 int ln1_bwd_grid(int B, int num_sms);
-bool ln1_bwd_needs_scratch(int T, int D);
-cudaError_t launch_ln1_mix_backward(Act act, bool x_f32, const void* X, const float* dS, const float* g1, float* dX,
-                                    float* part_dg1, float* part_dbe1, float* scratch, int B, int T, int D, int Bcap,
-                                    float eps, int grid, cudaStream_t s);
+cudaError_t launch_ln1_mix_backward(Act act, const void* Yh, const float* rstd, const float* dS, const float* g1,
+                                    float* dX, float* part_dg1, float* part_dbe1, int B, int T, int D, int Bcap,
+                                    int grid, cudaStream_t s);
 
 // out[g][n] = sum over r < R of in[g][r][n] (fixed order), and, when
 // out_all is not null, out_all[n] = sum over g of out[g][n].

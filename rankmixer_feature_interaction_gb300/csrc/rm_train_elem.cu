@@ -22,78 +22,54 @@ namespace rm {
 namespace {
 
 constexpr int kLn2Threads = 256;
-constexpr int kLn2Rows = 32;                 // rows (samples) of one token per CTA
+constexpr int kLn2Chunk = 8;                 // rows staged in shared memory per step (one per warp)
 constexpr int kLn2MaxCols = 3072 / kLn2Threads;
-constexpr int kLn1Threads = 512;
+constexpr int kLn1Threads = 256;
 constexpr int kLn1MaxCols = 3072 / kLn1Threads;
-constexpr int kLn1SmemLimit = 200 * 1024;    // bytes of dY a CTA may hold in shared memory
+constexpr int kRowMaxT = 128;
+
+// k / q for 0 <= k < 2^16 by a multiply-high: with m = ceil(2^32 / q) the
+// error of k m / 2^32 against k / q stays below 2^-16 < 1 / q, so the floor
+// is exact for 2 <= q < 2^16 (checked exhaustively on the host for q <= 3072);
+// q = 1 is the identity (m = 0 marks it).
+struct QDiv {
+    uint32_t q, m;
+    __device__ __forceinline__ int div(int k) const { return m == 0 ? k : (int)__umulhi((uint32_t)k, m); }
+};
+
+QDiv make_qdiv(int q) {
+    QDiv d;
+    d.q = (uint32_t)q;
+    d.m = q == 1 ? 0u : (uint32_t)((((uint64_t)1 << 32) + (uint64_t)q - 1) / (uint64_t)q);
+    return d;
+}
 
 // Element k of the residual row y = Mix(X)[t] + X[t] of one sample:
 // Mix(X)[t][c q + r] = X[c][t q + r].
 template <typename Tx>
-__device__ __forceinline__ float mixed_row_elem(const Tx* __restrict__ Xb, int t, int k, int q, int D) {
-    const int c = k / q, r = k - (k / q) * q;
-    return to_f32(Xb[(size_t)c * D + (size_t)t * q + r]) + to_f32(Xb[(size_t)t * D + k]);
-}
-
-// Mean and 1 / sqrt(var + eps) of y = Mix(X)[t] + X[t] (called by a full warp).
-template <typename Tx>
-__device__ __forceinline__ void mixed_row_stats(const Tx* __restrict__ Xb, int t, int q, int D, float eps, int lane,
-                                                float& mean, float& rstd) {
-    const float shift = mixed_row_elem(Xb, t, 0, q, D);     // shifted sums keep the variance accurate
-    float s1 = 0.f, s2 = 0.f;
-    for (int k = lane; k < D; k += 32) {
-        const float d = mixed_row_elem(Xb, t, k, q, D) - shift;
-        s1 += d;
-        s2 = fmaf(d, d, s2);
-    }
-    s1 = warp_sum(s1);
-    s2 = warp_sum(s2);
-    const float dm = s1 / (float)D;
-    mean = shift + dm;
-    rstd = rsqrtf(fmaxf(s2 / (float)D - dm * dm, 0.f) + eps);
+__device__ __forceinline__ float mixed_row_elem(const Tx* __restrict__ Xb, int t, int k, QDiv qd, int D) {
+    const int c = qd.div(k), r = k - c * (int)qd.q;
+    return to_f32(Xb[(size_t)c * D + (size_t)t * qd.q + r]) + to_f32(Xb[(size_t)t * D + k]);
 }
 
 // ---- LN1 recompute ---------------------------------------------------------------
-template <typename Tx, typename Top>
+// One warp per row (b, t): y = Mix(X)[t] + X[t] (two loads per element, no
+// division), its mean and rstd with shifted sums, then S = gamma1 yhat + beta1
+// (operand type), yhat itself (Tyh) and rstd for the LN1 backward.
+template <typename Tx, typename Top, typename Tyh>
 __global__ void __launch_bounds__(256)
-ln1_recompute_kernel(const Tx* __restrict__ X, Top* __restrict__ S, const float* __restrict__ g1,
-                     const float* __restrict__ be1, int B, int T, int D, int Bcap, float eps) {
+ln1_recompute_kernel(const Tx* __restrict__ X, Top* __restrict__ S, Tyh* __restrict__ Yh, float* __restrict__ rstd_out,
+                     const float* __restrict__ g1, const float* __restrict__ be1, int B, int T, int D, int Bcap,
+                     float eps, QDiv qd) {
     const int lane = threadIdx.x & 31;
-    const int q = D / T;
     const long long rows = (long long)B * T;
     for (long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5); row < rows; row += (long long)gridDim.x * 8) {
         const int b = (int)(row / T), t = (int)(row - (long long)b * T);
         const Tx* Xb = X + (size_t)b * T * D;
-        float mean, rstd;
-        mixed_row_stats(Xb, t, q, D, eps, lane, mean, rstd);
-        Top* out = S + ((size_t)t * Bcap + b) * D;
-        for (int k = lane; k < D; k += 32)
-            out[k] = from_f32<Top>(fmaf(g1[k], (mixed_row_elem(Xb, t, k, q, D) - mean) * rstd, be1[k]));
-    }
-}
-
-// ---- LN2 backward ----------------------------------------------------------------
-template <typename Tz>
-__global__ void __launch_bounds__(kLn2Threads)
-ln2_backward_kernel(const Tz* __restrict__ Z, const float* __restrict__ G, const float* __restrict__ g2,
-                    float* __restrict__ dZ, float* __restrict__ part_db2, float* __restrict__ part_dg2,
-                    float* __restrict__ part_dbe2, float* __restrict__ part_max, int B, int T, int D, int Bcap,
-                    float eps) {
-    __shared__ float4 st[kLn2Rows];          // (mean, rstd, mean(q), mean(q zhat)) per row
-    __shared__ float wmax[kLn2Threads / 32];
-    const int t = blockIdx.y, blk = blockIdx.x, nblk = gridDim.x;
-    const int b0 = blk * kLn2Rows;
-    const int nrows = min(kLn2Rows, B - b0);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int i = warp; i < nrows; i += kLn2Threads / 32) {
-        const int b = b0 + i;
-        const Tz* z = Z + ((size_t)t * Bcap + b) * D;
-        const float* gr = G + ((size_t)b * T + t) * D;
-        const float shift = to_f32(z[0]);
+        const float shift = mixed_row_elem(Xb, t, 0, qd, D);
         float s1 = 0.f, s2 = 0.f;
         for (int k = lane; k < D; k += 32) {
-            const float d = to_f32(z[k]) - shift;
+            const float d = mixed_row_elem(Xb, t, k, qd, D) - shift;
             s1 += d;
             s2 = fmaf(d, d, s2);
         }
@@ -102,43 +78,176 @@ ln2_backward_kernel(const Tz* __restrict__ Z, const float* __restrict__ G, const
         const float dm = s1 / (float)D;
         const float mean = shift + dm;
         const float rstd = rsqrtf(fmaxf(s2 / (float)D - dm * dm, 0.f) + eps);
-        float mq = 0.f, mqz = 0.f;
+        const size_t o = ((size_t)t * Bcap + b) * D;
         for (int k = lane; k < D; k += 32) {
-            const float qk = gr[k] * g2[k];
-            mq += qk;
-            mqz = fmaf(qk, (to_f32(z[k]) - mean) * rstd, mqz);
+            const float yh = (mixed_row_elem(Xb, t, k, qd, D) - mean) * rstd;
+            S[o + k] = from_f32<Top>(fmaf(g1[k], yh, be1[k]));
+            Yh[o + k] = from_f32<Tyh>(yh);
         }
-        mq = warp_sum(mq);
-        mqz = warp_sum(mqz);
-        if (lane == 0) st[i] = make_float4(mean, rstd, mq / (float)D, mqz / (float)D);
+        if (lane == 0) rstd_out[(size_t)t * Bcap + b] = rstd;
     }
-    __syncthreads();
+}
+
+// The same on column pairs (q even): lane l takes k = 2 l + 64 i, both
+// elements of a pair in the same head chunk, so each load and store moves two.
+template <typename T>
+__device__ __forceinline__ float2 ld_pair(const T* p);
+template <>
+__device__ __forceinline__ float2 ld_pair<__nv_bfloat16>(const __nv_bfloat16* p) {
+    return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+template <>
+__device__ __forceinline__ float2 ld_pair<float>(const float* p) {
+    return *reinterpret_cast<const float2*>(p);
+}
+template <typename T>
+__device__ __forceinline__ void st_pair(T* p, float a, float b);
+template <>
+__device__ __forceinline__ void st_pair<__half>(__half* p, float a, float b) {
+    *reinterpret_cast<__half2*>(p) = __floats2half2_rn(sat_f16(a), sat_f16(b));
+}
+template <>
+__device__ __forceinline__ void st_pair<float>(float* p, float a, float b) {
+    *reinterpret_cast<float2*>(p) = make_float2(a, b);
+}
+
+template <typename Tx, typename Top, typename Tyh>
+__global__ void __launch_bounds__(256)
+ln1_recompute_pair_kernel(const Tx* __restrict__ X, Top* __restrict__ S, Tyh* __restrict__ Yh,
+                          float* __restrict__ rstd_out, const float* __restrict__ g1, const float* __restrict__ be1,
+                          int B, int T, int D, int Bcap, float eps, QDiv qd) {
+    const int lane = threadIdx.x & 31;
+    const int q = (int)qd.q;
+    const long long rows = (long long)B * T;
+    for (long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5); row < rows; row += (long long)gridDim.x * 8) {
+        const int b = (int)(row / T), t = (int)(row - (long long)b * T);
+        const Tx* Xb = X + (size_t)b * T * D;
+        const Tx* Xt = Xb + (size_t)t * D;
+        const float shift = to_f32(Xb[(size_t)t * q]) + to_f32(Xt[0]);
+        float s1 = 0.f, s2 = 0.f;
+        for (int k = 2 * lane; k < D; k += 64) {
+            const int c = qd.div(k), r = k - c * q;
+            const float2 m = ld_pair<Tx>(Xb + (size_t)c * D + (size_t)t * q + r);
+            const float2 x = ld_pair<Tx>(Xt + k);
+            const float d0 = m.x + x.x - shift, d1 = m.y + x.y - shift;
+            s1 += d0 + d1;
+            s2 = fmaf(d0, d0, fmaf(d1, d1, s2));
+        }
+        s1 = warp_sum(s1);
+        s2 = warp_sum(s2);
+        const float dm = s1 / (float)D;
+        const float mean = shift + dm;
+        const float rstd = rsqrtf(fmaxf(s2 / (float)D - dm * dm, 0.f) + eps);
+        const size_t o = ((size_t)t * Bcap + b) * D;
+        for (int k = 2 * lane; k < D; k += 64) {
+            const int c = qd.div(k), r = k - c * q;
+            const float2 m = ld_pair<Tx>(Xb + (size_t)c * D + (size_t)t * q + r);
+            const float2 x = ld_pair<Tx>(Xt + k);
+            const float2 ga = *reinterpret_cast<const float2*>(g1 + k);
+            const float2 be = *reinterpret_cast<const float2*>(be1 + k);
+            const float y0 = (m.x + x.x - mean) * rstd, y1 = (m.y + x.y - mean) * rstd;
+            st_pair<Top>(S + o + k, fmaf(ga.x, y0, be.x), fmaf(ga.y, y1, be.y));
+            st_pair<Tyh>(Yh + o + k, y0, y1);
+        }
+        if (lane == 0) rstd_out[(size_t)t * Bcap + b] = rstd;
+    }
+}
+
+// ---- LN2 backward ----------------------------------------------------------------
+// Grid (nbx, T): CTA (x, t) walks its share of token t's rows in chunks of 8,
+// each chunk staged in shared memory (Z and G rows) so both passes read it
+// from there: a warp per row for the statistics (mean, rstd, mean(q),
+// mean(q zhat), q = G gamma2), then a thread per column for dZ and the
+// column sums of dZ, G zhat and G, kept in registers across the CTA's rows.
+template <typename Tz>
+__global__ void __launch_bounds__(kLn2Threads)
+ln2_backward_kernel(const Tz* __restrict__ Z, const float* __restrict__ G, const float* __restrict__ g2,
+                    float* __restrict__ dZ, float* __restrict__ part_db2, float* __restrict__ part_dg2,
+                    float* __restrict__ part_dbe2, float* __restrict__ part_max, int B, int T, int D, int Bcap,
+                    float eps, int rows_per_cta) {
+    extern __shared__ float4 smem4[];
+    float4* st = smem4;                                            // [kLn2Chunk]
+    float* gs = reinterpret_cast<float*>(smem4 + kLn2Chunk);       // [kLn2Chunk][D]
+    Tz* zs = reinterpret_cast<Tz*>(gs + (size_t)kLn2Chunk * D);    // [kLn2Chunk][D]
+    __shared__ float wmax[kLn2Threads / 32];
+    const int t = blockIdx.y, bx = blockIdx.x, nbx = gridDim.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b_begin = bx * rows_per_cta;
+    const int b_end = min(B, b_begin + rows_per_cta);
     float adb[kLn2MaxCols], adg[kLn2MaxCols], adbe[kLn2MaxCols];
 #pragma unroll
     for (int c = 0; c < kLn2MaxCols; ++c) adb[c] = adg[c] = adbe[c] = 0.f;
     float amax = 0.f;
-    for (int i = 0; i < nrows; ++i) {
-        const float4 s = st[i];
-        const int b = b0 + i;
-        const Tz* z = Z + ((size_t)t * Bcap + b) * D;
-        const float* gr = G + ((size_t)b * T + t) * D;
-        float* dz = dZ + ((size_t)t * Bcap + b) * D;
+    const bool vec = (D * sizeof(Tz)) % 16 == 0;
+    for (int b0 = b_begin; b0 < b_end; b0 += kLn2Chunk) {
+        const int nrows = min(kLn2Chunk, b_end - b0);
+        __syncthreads();                       // the previous chunk is done with the staged rows
+        if (vec) {
+            const int zq = D * (int)sizeof(Tz) / 16, gq = D / 4;
+            for (int i = threadIdx.x; i < nrows * zq; i += kLn2Threads) {
+                const int rr = i / zq, j = i - rr * zq;
+                reinterpret_cast<uint4*>(zs + (size_t)rr * D)[j] =
+                    __ldg(reinterpret_cast<const uint4*>(Z + ((size_t)t * Bcap + b0 + rr) * D) + j);
+            }
+            for (int i = threadIdx.x; i < nrows * gq; i += kLn2Threads) {
+                const int rr = i / gq, j = i - rr * gq;
+                reinterpret_cast<float4*>(gs + (size_t)rr * D)[j] =
+                    __ldg(reinterpret_cast<const float4*>(G + ((size_t)(b0 + rr) * T + t) * D) + j);
+            }
+        } else {
+            for (int i = threadIdx.x; i < nrows * D; i += kLn2Threads) {
+                const int rr = i / D, k = i - rr * D;
+                zs[(size_t)rr * D + k] = Z[((size_t)t * Bcap + b0 + rr) * D + k];
+                gs[(size_t)rr * D + k] = G[((size_t)(b0 + rr) * T + t) * D + k];
+            }
+        }
+        __syncthreads();
+        if (warp < nrows) {
+            const Tz* z = zs + (size_t)warp * D;
+            const float* gr = gs + (size_t)warp * D;
+            const float shift = to_f32(z[0]);
+            float s1 = 0.f, s2 = 0.f;
+            for (int k = lane; k < D; k += 32) {
+                const float d = to_f32(z[k]) - shift;
+                s1 += d;
+                s2 = fmaf(d, d, s2);
+            }
+            s1 = warp_sum(s1);
+            s2 = warp_sum(s2);
+            const float dm = s1 / (float)D;
+            const float mean = shift + dm;
+            const float rstd = rsqrtf(fmaxf(s2 / (float)D - dm * dm, 0.f) + eps);
+            float mq = 0.f, mqz = 0.f;
+            for (int k = lane; k < D; k += 32) {
+                const float qk = gr[k] * g2[k];
+                mq += qk;
+                mqz = fmaf(qk, (to_f32(z[k]) - mean) * rstd, mqz);
+            }
+            mq = warp_sum(mq);
+            mqz = warp_sum(mqz);
+            if (lane == 0) st[warp] = make_float4(mean, rstd, mq / (float)D, mqz / (float)D);
+        }
+        __syncthreads();
+        for (int i = 0; i < nrows; ++i) {
+            const float4 s = st[i];
+            float* dz = dZ + ((size_t)t * Bcap + b0 + i) * D;
 #pragma unroll
-        for (int c = 0; c < kLn2MaxCols; ++c) {
-            const int k = threadIdx.x + c * kLn2Threads;
-            if (k < D) {
-                const float zh = (to_f32(z[k]) - s.x) * s.y;
-                const float gk = gr[k];
-                const float d = (gk * g2[k] - s.z - zh * s.w) * s.y;
-                dz[k] = d;
-                amax = fmaxf(amax, fabsf(d));
-                adb[c] += d;
-                adg[c] = fmaf(gk, zh, adg[c]);
-                adbe[c] += gk;
+            for (int c = 0; c < kLn2MaxCols; ++c) {
+                const int k = threadIdx.x + c * kLn2Threads;
+                if (k < D) {
+                    const float zh = (to_f32(zs[(size_t)i * D + k]) - s.x) * s.y;
+                    const float gk = gs[(size_t)i * D + k];
+                    const float d = (gk * g2[k] - s.z - zh * s.w) * s.y;
+                    dz[k] = d;
+                    amax = fmaxf(amax, fabsf(d));
+                    adb[c] += d;
+                    adg[c] = fmaf(gk, zh, adg[c]);
+                    adbe[c] += gk;
+                }
             }
         }
     }
-    const size_t prow = ((size_t)t * nblk + blk) * D;
+    const size_t prow = ((size_t)t * nbx + bx) * D;
 #pragma unroll
     for (int c = 0; c < kLn2MaxCols; ++c) {
         const int k = threadIdx.x + c * kLn2Threads;
@@ -155,7 +264,146 @@ ln2_backward_kernel(const Tz* __restrict__ Z, const float* __restrict__ G, const
     if (threadIdx.x == 0) {
         float m = 0.f;
         for (int w = 0; w < kLn2Threads / 32; ++w) m = fmaxf(m, wmax[w]);
-        part_max[(size_t)t * nblk + blk] = m;
+        part_max[(size_t)t * nbx + bx] = m;
+    }
+}
+
+// The same for D a multiple of 4: one pass per row for the statistics (4
+// columns per lane step; mean(q zhat) = rstd (sum q (z - shift) - (mean -
+// shift) sum q) / D with the row's first value as the shift), and column
+// pairs per thread in the second phase.
+template <typename Tz>
+__device__ __forceinline__ float4 ld4_any(const Tz* p);
+template <>
+__device__ __forceinline__ float4 ld4_any<__half>(const __half* p) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+template <>
+__device__ __forceinline__ float4 ld4_any<float>(const float* p) {
+    return *reinterpret_cast<const float4*>(p);
+}
+template <typename Tz>
+__device__ __forceinline__ float2 ld2_any(const Tz* p);
+template <>
+__device__ __forceinline__ float2 ld2_any<__half>(const __half* p) {
+    return __half22float2(*reinterpret_cast<const __half2*>(p));
+}
+template <>
+__device__ __forceinline__ float2 ld2_any<float>(const float* p) {
+    return *reinterpret_cast<const float2*>(p);
+}
+
+constexpr int kLn2MaxPairs = 3072 / 2 / kLn2Threads;
+
+template <typename Tz>
+__global__ void __launch_bounds__(kLn2Threads, 3)
+ln2_backward_vec_kernel(const Tz* __restrict__ Z, const float* __restrict__ G, const float* __restrict__ g2,
+                        float* __restrict__ dZ, float* __restrict__ part_db2, float* __restrict__ part_dg2,
+                        float* __restrict__ part_dbe2, float* __restrict__ part_max, int B, int T, int D, int Bcap,
+                        float eps, int rows_per_cta) {
+    extern __shared__ float4 smem4[];
+    float4* st = smem4;                                            // [kLn2Chunk]
+    float* gs = reinterpret_cast<float*>(smem4 + kLn2Chunk);       // [kLn2Chunk][D]
+    Tz* zs = reinterpret_cast<Tz*>(gs + (size_t)kLn2Chunk * D);    // [kLn2Chunk][D]
+    __shared__ float wmax[kLn2Threads / 32];
+    const int t = blockIdx.y, bx = blockIdx.x, nbx = gridDim.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b_begin = bx * rows_per_cta;
+    const int b_end = min(B, b_begin + rows_per_cta);
+    const int npairs = D / 2;
+    float2 adb[kLn2MaxPairs], adg[kLn2MaxPairs], adbe[kLn2MaxPairs];
+#pragma unroll
+    for (int j = 0; j < kLn2MaxPairs; ++j) adb[j] = adg[j] = adbe[j] = make_float2(0.f, 0.f);
+    float amax = 0.f;
+    const int zq = D * (int)sizeof(Tz) / 16, gq = D / 4;
+    for (int b0 = b_begin; b0 < b_end; b0 += kLn2Chunk) {
+        const int nrows = min(kLn2Chunk, b_end - b0);
+        __syncthreads();                       // the previous chunk is done with the staged rows
+        for (int i = threadIdx.x; i < nrows * zq; i += kLn2Threads) {
+            const int rr = i / zq, j = i - rr * zq;
+            reinterpret_cast<uint4*>(zs + (size_t)rr * D)[j] =
+                __ldg(reinterpret_cast<const uint4*>(Z + ((size_t)t * Bcap + b0 + rr) * D) + j);
+        }
+        for (int i = threadIdx.x; i < nrows * gq; i += kLn2Threads) {
+            const int rr = i / gq, j = i - rr * gq;
+            reinterpret_cast<float4*>(gs + (size_t)rr * D)[j] =
+                __ldg(reinterpret_cast<const float4*>(G + ((size_t)(b0 + rr) * T + t) * D) + j);
+        }
+        __syncthreads();
+        if (warp < nrows) {
+            const Tz* z = zs + (size_t)warp * D;
+            const float* gr = gs + (size_t)warp * D;
+            const float shift = to_f32(z[0]);
+            float s1 = 0.f, s2 = 0.f, sq = 0.f, sqz = 0.f;
+            for (int k = 4 * lane; k < D; k += 128) {
+                const float4 zz = ld4_any<Tz>(z + k);
+                const float4 gg = *reinterpret_cast<const float4*>(gr + k);
+                const float4 ga = __ldg(reinterpret_cast<const float4*>(g2 + k));
+                const float d0 = zz.x - shift, d1 = zz.y - shift, d2 = zz.z - shift, d3 = zz.w - shift;
+                const float q0 = gg.x * ga.x, q1 = gg.y * ga.y, q2 = gg.z * ga.z, q3 = gg.w * ga.w;
+                s1 += (d0 + d1) + (d2 + d3);
+                s2 = fmaf(d0, d0, fmaf(d1, d1, fmaf(d2, d2, fmaf(d3, d3, s2))));
+                sq += (q0 + q1) + (q2 + q3);
+                sqz = fmaf(q0, d0, fmaf(q1, d1, fmaf(q2, d2, fmaf(q3, d3, sqz))));
+            }
+            s1 = warp_sum(s1);
+            s2 = warp_sum(s2);
+            sq = warp_sum(sq);
+            sqz = warp_sum(sqz);
+            const float dm = s1 / (float)D;
+            const float rstd = rsqrtf(fmaxf(s2 / (float)D - dm * dm, 0.f) + eps);
+            if (lane == 0)
+                st[warp] = make_float4(shift + dm, rstd, sq / (float)D, rstd * (sqz - dm * sq) / (float)D);
+        }
+        __syncthreads();
+        for (int i = 0; i < nrows; ++i) {
+            const float4 s = st[i];
+            float* dz = dZ + ((size_t)t * Bcap + b0 + i) * D;
+#pragma unroll
+            for (int j = 0; j < kLn2MaxPairs; ++j) {
+                const int pidx = threadIdx.x + j * kLn2Threads;
+                if (pidx < npairs) {
+                    const int k = 2 * pidx;
+                    const float2 zz = ld2_any<Tz>(zs + (size_t)i * D + k);
+                    const float2 gk = *reinterpret_cast<const float2*>(gs + (size_t)i * D + k);
+                    const float2 ga = __ldg(reinterpret_cast<const float2*>(g2 + k));
+                    const float zh0 = (zz.x - s.x) * s.y, zh1 = (zz.y - s.x) * s.y;
+                    float2 d;
+                    d.x = (gk.x * ga.x - s.z - zh0 * s.w) * s.y;
+                    d.y = (gk.y * ga.y - s.z - zh1 * s.w) * s.y;
+                    *reinterpret_cast<float2*>(dz + k) = d;
+                    amax = fmaxf(amax, fmaxf(fabsf(d.x), fabsf(d.y)));
+                    adb[j].x += d.x;
+                    adb[j].y += d.y;
+                    adg[j].x = fmaf(gk.x, zh0, adg[j].x);
+                    adg[j].y = fmaf(gk.y, zh1, adg[j].y);
+                    adbe[j].x += gk.x;
+                    adbe[j].y += gk.y;
+                }
+            }
+        }
+    }
+    const size_t prow = ((size_t)t * nbx + bx) * D;
+#pragma unroll
+    for (int j = 0; j < kLn2MaxPairs; ++j) {
+        const int pidx = threadIdx.x + j * kLn2Threads;
+        if (pidx < npairs) {
+            *reinterpret_cast<float2*>(part_db2 + prow + 2 * pidx) = adb[j];
+            *reinterpret_cast<float2*>(part_dg2 + prow + 2 * pidx) = adg[j];
+            *reinterpret_cast<float2*>(part_dbe2 + prow + 2 * pidx) = adbe[j];
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) wmax[warp] = amax;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float m = 0.f;
+        for (int w = 0; w < kLn2Threads / 32; ++w) m = fmaxf(m, wmax[w]);
+        part_max[(size_t)t * nbx + bx] = m;
     }
 }
 
@@ -195,68 +443,186 @@ __global__ void bf16_to_f16_kernel(const __nv_bfloat16* __restrict__ in, __half*
 }
 
 // ---- LN1 + mixing backward ---------------------------------------------------------
-template <typename Tx, bool SMEM_DY>
+// One CTA per sample at a time (persistent over samples), from yhat and rstd
+// of the LN1 recompute:
+//   1. per row t (a warp): mean(q) and mean(q yhat), q = dS[t] gamma1;
+//   2. per element (a thread per column k = c q + r, rows t in turn):
+//        dX[t][k] = F(t, k) + F(c, t q + r),
+//      F(u, j) = rstd_u (dS[u][j] gamma1[j] - mean(q)_u - yhat[u][j] mean(q yhat)_u),
+//      i.e. dY + P^T dY with dY = F never stored: the transposed partner of
+//      element (t, c q + r) is (c, t q + r).  A thread's columns (and so c
+//      and r) are fixed, so no division runs per element.
+// The thread owning column k also sums dS[t][k] yhat[t][k] and dS[t][k] over
+// the rows of its samples (the CTA's dgamma1, dbeta1 partials).
+template <typename Tyh>
 __global__ void __launch_bounds__(kLn1Threads)
-ln1_mix_backward_kernel(const Tx* __restrict__ X, const float* __restrict__ dS, const float* __restrict__ g1,
-                        float* __restrict__ dX, float* __restrict__ part_dg1, float* __restrict__ part_dbe1,
-                        float* __restrict__ scratch, int B, int T, int D, int Bcap, float eps) {
-    extern __shared__ float4 smem4[];
-    float4* st = smem4;                                      // [T] (mean, rstd, mean(q), mean(q yhat))
-    float* dY = SMEM_DY ? reinterpret_cast<float*>(smem4 + T) : scratch + (size_t)blockIdx.x * T * D;
+ln1_mix_backward_kernel(const Tyh* __restrict__ Yh, const float* __restrict__ rstdv, const float* __restrict__ dS,
+                        const float* __restrict__ g1, float* __restrict__ dX, float* __restrict__ part_dg1,
+                        float* __restrict__ part_dbe1, int B, int T, int D, int Bcap, QDiv qd) {
+    __shared__ float4 st[kRowMaxT];                   // (rstd, mean(q), mean(q yhat)) per row
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int q = D / T;
+    const int q = (int)qd.q;
+    int cc_[kLn1MaxCols], rr_[kLn1MaxCols];
+#pragma unroll
+    for (int j = 0; j < kLn1MaxCols; ++j) {
+        const int k = threadIdx.x + j * kLn1Threads;
+        cc_[j] = k < D ? qd.div(k) : 0;
+        rr_[j] = k - cc_[j] * q;
+    }
     float adg[kLn1MaxCols], adbe[kLn1MaxCols];
 #pragma unroll
-    for (int c = 0; c < kLn1MaxCols; ++c) adg[c] = adbe[c] = 0.f;
+    for (int j = 0; j < kLn1MaxCols; ++j) adg[j] = adbe[j] = 0.f;
     for (int b = blockIdx.x; b < B; b += gridDim.x) {
-        const Tx* Xb = X + (size_t)b * T * D;
+        __syncthreads();                              // the previous sample is done with st
         for (int t = warp; t < T; t += kLn1Threads / 32) {
-            float mean, rstd;
-            mixed_row_stats(Xb, t, q, D, eps, lane, mean, rstd);
-            const float* ds = dS + ((size_t)t * Bcap + b) * D;
+            const size_t o = ((size_t)t * Bcap + b) * D;
             float mq = 0.f, mqy = 0.f;
             for (int k = lane; k < D; k += 32) {
-                const float qk = ds[k] * g1[k];
+                const float qk = dS[o + k] * g1[k];
                 mq += qk;
-                mqy = fmaf(qk, (mixed_row_elem(Xb, t, k, q, D) - mean) * rstd, mqy);
+                mqy = fmaf(qk, to_f32(Yh[o + k]), mqy);
             }
             mq = warp_sum(mq);
             mqy = warp_sum(mqy);
-            if (lane == 0) st[t] = make_float4(mean, rstd, mq / (float)D, mqy / (float)D);
+            if (lane == 0) st[t] = make_float4(rstdv[(size_t)t * Bcap + b], mq / (float)D, mqy / (float)D, 0.f);
         }
         __syncthreads();
+        float* out = dX + (size_t)b * T * D;
         for (int t = 0; t < T; ++t) {
-            const float4 s = st[t];
-            const float* ds = dS + ((size_t)t * Bcap + b) * D;
+            const float4 s1 = st[t];
+            const size_t o1 = ((size_t)t * Bcap + b) * D;
 #pragma unroll
-            for (int c = 0; c < kLn1MaxCols; ++c) {
-                const int k = threadIdx.x + c * kLn1Threads;
+            for (int j = 0; j < kLn1MaxCols; ++j) {
+                const int k = threadIdx.x + j * kLn1Threads;
                 if (k < D) {
-                    const float yh = (mixed_row_elem(Xb, t, k, q, D) - s.x) * s.y;
-                    const float dk = ds[k];
-                    dY[(size_t)t * D + k] = (dk * g1[k] - s.z - yh * s.w) * s.y;
-                    adg[c] = fmaf(dk, yh, adg[c]);
-                    adbe[c] += dk;
+                    const int c = cc_[j];
+                    const int k2 = t * q + rr_[j];            // the partner element (c, t q + r)
+                    const float4 s2 = st[c];
+                    const size_t o2 = ((size_t)c * Bcap + b) * D + k2;
+                    const float yh1 = to_f32(Yh[o1 + k]);
+                    const float yh2 = to_f32(Yh[o2]);
+                    const float d1 = dS[o1 + k];
+                    const float d2 = dS[o2];
+                    const float f1 = (d1 * g1[k] - s1.y - yh1 * s1.z) * s1.x;
+                    const float f2 = (d2 * g1[k2] - s2.y - yh2 * s2.z) * s2.x;
+                    out[(size_t)t * D + k] = f1 + f2;
+                    adg[j] = fmaf(d1, yh1, adg[j]);
+                    adbe[j] += d1;
                 }
             }
         }
-        __syncthreads();
-        // dX[t][c q + r] = dY[t][c q + r] + dY[c][t q + r]
-        float* out = dX + (size_t)b * T * D;
-        const int n = T * D;
-        for (int i = threadIdx.x; i < n; i += kLn1Threads) {
-            const int t = i / D, k = i - (i / D) * D;
-            const int c = k / q, r = k - (k / q) * q;
-            out[i] = dY[i] + dY[(size_t)c * D + (size_t)t * q + r];
-        }
-        __syncthreads();
     }
 #pragma unroll
-    for (int c = 0; c < kLn1MaxCols; ++c) {
-        const int k = threadIdx.x + c * kLn1Threads;
+    for (int j = 0; j < kLn1MaxCols; ++j) {
+        const int k = threadIdx.x + j * kLn1Threads;
         if (k < D) {
-            part_dg1[(size_t)blockIdx.x * D + k] = adg[c];
-            part_dbe1[(size_t)blockIdx.x * D + k] = adbe[c];
+            part_dg1[(size_t)blockIdx.x * D + k] = adg[j];
+            part_dbe1[(size_t)blockIdx.x * D + k] = adbe[j];
+        }
+    }
+}
+
+// The same with two adjacent columns per thread step (q and D even, D a
+// multiple of 4): column pairs (k, k + 1) with k even have their partners at
+// (c, t q + r) and (c, t q + r + 1), so every load and store moves a pair, and
+// the row statistics read 4 columns per lane step.
+template <typename Tyh>
+struct Pair2;
+template <>
+struct Pair2<__half> {
+    static __device__ __forceinline__ float2 ld(const __half* p) {
+        return __half22float2(*reinterpret_cast<const __half2*>(p));
+    }
+    static __device__ __forceinline__ float4 ld4(const __half* p) {
+        const uint2 v = *reinterpret_cast<const uint2*>(p);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+        return make_float4(a.x, a.y, b.x, b.y);
+    }
+};
+template <>
+struct Pair2<float> {
+    static __device__ __forceinline__ float2 ld(const float* p) { return *reinterpret_cast<const float2*>(p); }
+    static __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+};
+
+constexpr int kLn1MaxPairs = 3072 / 2 / kLn1Threads;
+
+template <typename Tyh>
+__global__ void __launch_bounds__(kLn1Threads, 3)
+ln1_mix_backward_pair_kernel(const Tyh* __restrict__ Yh, const float* __restrict__ rstdv,
+                             const float* __restrict__ dS, const float* __restrict__ g1, float* __restrict__ dX,
+                             float* __restrict__ part_dg1, float* __restrict__ part_dbe1, int B, int T, int D, int Bcap,
+                             QDiv qd) {
+    __shared__ float4 st[kRowMaxT];                   // (rstd, mean(q), mean(q yhat)) per row
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = (int)qd.q;
+    const int npairs = D / 2;
+    int cc_[kLn1MaxPairs], rr_[kLn1MaxPairs];
+#pragma unroll
+    for (int j = 0; j < kLn1MaxPairs; ++j) {
+        const int k = 2 * (threadIdx.x + j * kLn1Threads);
+        cc_[j] = k < D ? qd.div(k) : 0;
+        rr_[j] = k - cc_[j] * q;
+    }
+    float2 adg[kLn1MaxPairs], adbe[kLn1MaxPairs];
+#pragma unroll
+    for (int j = 0; j < kLn1MaxPairs; ++j) adg[j] = adbe[j] = make_float2(0.f, 0.f);
+    for (int b = blockIdx.x; b < B; b += gridDim.x) {
+        __syncthreads();                              // the previous sample is done with st
+        for (int t = warp; t < T; t += kLn1Threads / 32) {
+            const size_t o = ((size_t)t * Bcap + b) * D;
+            float mq = 0.f, mqy = 0.f;
+            for (int k = 4 * lane; k < D; k += 128) {
+                const float4 d = *reinterpret_cast<const float4*>(dS + o + k);
+                const float4 gg = *reinterpret_cast<const float4*>(g1 + k);
+                const float4 y = Pair2<Tyh>::ld4(Yh + o + k);
+                const float q0 = d.x * gg.x, q1 = d.y * gg.y, q2 = d.z * gg.z, q3 = d.w * gg.w;
+                mq += (q0 + q1) + (q2 + q3);
+                mqy = fmaf(q0, y.x, fmaf(q1, y.y, fmaf(q2, y.z, fmaf(q3, y.w, mqy))));
+            }
+            mq = warp_sum(mq);
+            mqy = warp_sum(mqy);
+            if (lane == 0) st[t] = make_float4(rstdv[(size_t)t * Bcap + b], mq / (float)D, mqy / (float)D, 0.f);
+        }
+        __syncthreads();
+        float* out = dX + (size_t)b * T * D;
+        for (int t = 0; t < T; ++t) {
+            const float4 s1 = st[t];
+            const size_t o1 = ((size_t)t * Bcap + b) * D;
+#pragma unroll
+            for (int j = 0; j < kLn1MaxPairs; ++j) {
+                const int pidx = threadIdx.x + j * kLn1Threads;
+                if (pidx < npairs) {
+                    const int k = 2 * pidx;
+                    const int c = cc_[j];
+                    const int k2 = t * q + rr_[j];            // partners (c, k2) and (c, k2 + 1)
+                    const float4 s2 = st[c];
+                    const size_t o2 = ((size_t)c * Bcap + b) * D + k2;
+                    const float2 y1 = Pair2<Tyh>::ld(Yh + o1 + k);
+                    const float2 y2 = Pair2<Tyh>::ld(Yh + o2);
+                    const float2 d1 = *reinterpret_cast<const float2*>(dS + o1 + k);
+                    const float2 d2 = *reinterpret_cast<const float2*>(dS + o2);
+                    const float2 ga = *reinterpret_cast<const float2*>(g1 + k);
+                    const float2 gb = *reinterpret_cast<const float2*>(g1 + k2);
+                    float2 r;
+                    r.x = (d1.x * ga.x - s1.y - y1.x * s1.z) * s1.x + (d2.x * gb.x - s2.y - y2.x * s2.z) * s2.x;
+                    r.y = (d1.y * ga.y - s1.y - y1.y * s1.z) * s1.x + (d2.y * gb.y - s2.y - y2.y * s2.z) * s2.x;
+                    *reinterpret_cast<float2*>(out + (size_t)t * D + k) = r;
+                    adg[j].x = fmaf(d1.x, y1.x, adg[j].x);
+                    adg[j].y = fmaf(d1.y, y1.y, adg[j].y);
+                    adbe[j].x += d1.x;
+                    adbe[j].y += d1.y;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < kLn1MaxPairs; ++j) {
+        const int pidx = threadIdx.x + j * kLn1Threads;
+        if (pidx < npairs) {
+            *reinterpret_cast<float2*>(part_dg1 + (size_t)blockIdx.x * D + 2 * pidx) = adg[j];
+            *reinterpret_cast<float2*>(part_dbe1 + (size_t)blockIdx.x * D + 2 * pidx) = adbe[j];
         }
     }
 }
@@ -280,13 +646,28 @@ __global__ void sum_groups_kernel(const float* __restrict__ in, float* __restric
     out[n] = s;
 }
 
+// G[b][t][k] = dP[b][k] / T: a thread per (sample, 4 columns) writes its float4 to every token row.
 __global__ void pool_backward_kernel(const float* __restrict__ dP, float* __restrict__ G, int B, int T, int D) {
-    const long long n = (long long)B * T * D;
+    const int d4 = D / 4;
+    const long long n = (long long)B * d4;
     const float inv = 1.0f / (float)T;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
-        const long long b = i / ((long long)T * D);
-        const int k = (int)(i % D);
-        G[i] = dP[b * D + k] * inv;
+        const int b = (int)(i / d4), j = (int)(i - (long long)b * d4);
+        float4 v = reinterpret_cast<const float4*>(dP + (size_t)b * D)[j];
+        v.x *= inv; v.y *= inv; v.z *= inv; v.w *= inv;
+        float4* o = reinterpret_cast<float4*>(G + (size_t)b * T * D) + j;
+        for (int t = 0; t < T; ++t) o[(size_t)t * d4] = v;
+    }
+}
+
+// The same for D not a multiple of 4.
+__global__ void pool_backward_scalar_kernel(const float* __restrict__ dP, float* __restrict__ G, int B, int T, int D) {
+    const long long n = (long long)B * D;
+    const float inv = 1.0f / (float)T;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        const int b = (int)(i / D), k = (int)(i - (long long)b * D);
+        const float v = dP[i] * inv;
+        for (int t = 0; t < T; ++t) G[((size_t)b * T + t) * D + k] = v;
     }
 }
 
@@ -304,40 +685,86 @@ int grid_for(long long n, int threads, int cap) {
     return (int)(g < 1 ? 1 : g);
 }
 
-size_t ln1_smem_bytes(int T, int D) { return (size_t)T * sizeof(float4) + (size_t)T * D * sizeof(float); }
 
 }  // namespace
 
-cudaError_t launch_ln1_recompute(Act act, bool x_f32, const void* X, void* S, const float* g1, const float* be1,
-                                 int B, int T, int D, int Bcap, float eps, int num_sms, cudaStream_t s) {
+cudaError_t launch_ln1_recompute(Act act, bool x_f32, const void* X, void* S, void* Yh, float* rstd, const float* g1,
+                                 const float* be1, int B, int T, int D, int Bcap, float eps, int num_sms,
+                                 cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     const int grid = grid_for((long long)B * T, 8, num_sms * 8);
+    const QDiv qd = make_qdiv(D / T);
+    if ((D / T) % 2 == 0) {
+        if (act == Act::F32)
+            ln1_recompute_pair_kernel<float, float, float><<<grid, 256, 0, s>>>(
+                (const float*)X, (float*)S, (float*)Yh, rstd, g1, be1, B, T, D, Bcap, eps, qd);
+        else if (x_f32)
+            ln1_recompute_pair_kernel<float, __half, __half><<<grid, 256, 0, s>>>(
+                (const float*)X, (__half*)S, (__half*)Yh, rstd, g1, be1, B, T, D, Bcap, eps, qd);
+        else
+            ln1_recompute_pair_kernel<__nv_bfloat16, __half, __half><<<grid, 256, 0, s>>>(
+                (const __nv_bfloat16*)X, (__half*)S, (__half*)Yh, rstd, g1, be1, B, T, D, Bcap, eps, qd);
+        return cudaGetLastError();
+    }
     if (act == Act::F32)
-        ln1_recompute_kernel<float, float><<<grid, 256, 0, s>>>((const float*)X, (float*)S, g1, be1, B, T, D, Bcap,
-                                                                 eps);
+        ln1_recompute_kernel<float, float, float><<<grid, 256, 0, s>>>((const float*)X, (float*)S, (float*)Yh, rstd,
+                                                                        g1, be1, B, T, D, Bcap, eps, qd);
     else if (x_f32)
-        ln1_recompute_kernel<float, __half><<<grid, 256, 0, s>>>((const float*)X, (__half*)S, g1, be1, B, T, D,
-                                                                  Bcap, eps);
+        ln1_recompute_kernel<float, __half, __half><<<grid, 256, 0, s>>>((const float*)X, (__half*)S, (__half*)Yh,
+                                                                          rstd, g1, be1, B, T, D, Bcap, eps, qd);
     else
-        ln1_recompute_kernel<__nv_bfloat16, __half><<<grid, 256, 0, s>>>((const __nv_bfloat16*)X, (__half*)S, g1,
-                                                                          be1, B, T, D, Bcap, eps);
+        ln1_recompute_kernel<__nv_bfloat16, __half, __half><<<grid, 256, 0, s>>>(
+            (const __nv_bfloat16*)X, (__half*)S, (__half*)Yh, rstd, g1, be1, B, T, D, Bcap, eps, qd);
     return cudaGetLastError();
 }
 
-int ln2_bwd_row_block() { return kLn2Rows; }
+int ln2_bwd_blocks(int B, int T, int num_sms) {
+    const int want = (3 * num_sms + T - 1) / T;
+    const int most = (B + kLn2Chunk - 1) / kLn2Chunk;
+    const int n = want < most ? want : most;
+    return n < 1 ? 1 : n;
+}
 
 cudaError_t launch_ln2_backward(Act act, const void* Z, const float* G, const float* g2, float* dZ, float* part_db2,
                                 float* part_dg2, float* part_dbe2, float* part_max, int B, int T, int D, int Bcap,
-                                float eps, cudaStream_t s) {
+                                float eps, int num_sms, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     if (D > kLn2MaxCols * kLn2Threads) return cudaErrorNotSupported;
-    const dim3 grid((B + kLn2Rows - 1) / kLn2Rows, T);
-    if (act == Act::F32)
-        ln2_backward_kernel<float><<<grid, kLn2Threads, 0, s>>>((const float*)Z, G, g2, dZ, part_db2, part_dg2,
-                                                                 part_dbe2, part_max, B, T, D, Bcap, eps);
-    else
-        ln2_backward_kernel<__half><<<grid, kLn2Threads, 0, s>>>((const __half*)Z, G, g2, dZ, part_db2, part_dg2,
-                                                                  part_dbe2, part_max, B, T, D, Bcap, eps);
+    const int nbx = ln2_bwd_blocks(B, T, num_sms);
+    const int per = ((B + nbx - 1) / nbx + kLn2Chunk - 1) / kLn2Chunk * kLn2Chunk;
+    const dim3 grid(nbx, T);
+    const size_t zsz = act == Act::F32 ? 4 : 2;
+    const size_t bytes = kLn2Chunk * sizeof(float4) + (size_t)kLn2Chunk * D * (4 + zsz);
+    const bool vec = D % 8 == 0;               // whole 16-byte lines of fp16 rows and float4 of float rows
+    if (vec) {
+        if (act == Act::F32) {
+            auto k = ln2_backward_vec_kernel<float>;
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+            if (e != cudaSuccess) return e;
+            k<<<grid, kLn2Threads, bytes, s>>>((const float*)Z, G, g2, dZ, part_db2, part_dg2, part_dbe2, part_max,
+                                               B, T, D, Bcap, eps, per);
+        } else {
+            auto k = ln2_backward_vec_kernel<__half>;
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+            if (e != cudaSuccess) return e;
+            k<<<grid, kLn2Threads, bytes, s>>>((const __half*)Z, G, g2, dZ, part_db2, part_dg2, part_dbe2, part_max,
+                                               B, T, D, Bcap, eps, per);
+        }
+        return cudaGetLastError();
+    }
+    if (act == Act::F32) {
+        auto k = ln2_backward_kernel<float>;
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        if (e != cudaSuccess) return e;
+        k<<<grid, kLn2Threads, bytes, s>>>((const float*)Z, G, g2, dZ, part_db2, part_dg2, part_dbe2, part_max, B, T,
+                                           D, Bcap, eps, per);
+    } else {
+        auto k = ln2_backward_kernel<__half>;
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        if (e != cudaSuccess) return e;
+        k<<<grid, kLn2Threads, bytes, s>>>((const __half*)Z, G, g2, dZ, part_db2, part_dg2, part_dbe2, part_max, B,
+                                           T, D, Bcap, eps, per);
+    }
     return cudaGetLastError();
 }
 
@@ -355,32 +782,33 @@ cudaError_t launch_bf16_to_f16(const void* in, void* out, long long n, cudaStrea
     return cudaGetLastError();
 }
 
-int ln1_bwd_grid(int B, int num_sms) { return B < num_sms ? (B < 1 ? 1 : B) : num_sms; }
+int ln1_bwd_grid(int B, int num_sms) {
+    const int cap = num_sms * 4;
+    return B < cap ? (B < 1 ? 1 : B) : cap;
+}
 
-bool ln1_bwd_needs_scratch(int T, int D) { return ln1_smem_bytes(T, D) > (size_t)kLn1SmemLimit; }
-
-cudaError_t launch_ln1_mix_backward(Act act, bool x_f32, const void* X, const float* dS, const float* g1, float* dX,
-                                    float* part_dg1, float* part_dbe1, float* scratch, int B, int T, int D, int Bcap,
-                                    float eps, int grid, cudaStream_t s) {
+cudaError_t launch_ln1_mix_backward(Act act, const void* Yh, const float* rstd, const float* dS, const float* g1,
+                                    float* dX, float* part_dg1, float* part_dbe1, int B, int T, int D, int Bcap,
+                                    int grid, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
-    if (D > kLn1MaxCols * kLn1Threads) return cudaErrorNotSupported;
-    const bool smem = !ln1_bwd_needs_scratch(T, D);
-    if (!smem && scratch == nullptr) return cudaErrorInvalidValue;
-    const size_t bytes = smem ? ln1_smem_bytes(T, D) : (size_t)T * sizeof(float4);
-#define RM_LN1B(TX, SM)                                                                                        \
-    do {                                                                                                       \
-        auto k = ln1_mix_backward_kernel<TX, SM>;                                                              \
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);      \
-        if (e != cudaSuccess) return e;                                                                        \
-        k<<<grid, kLn1Threads, bytes, s>>>((const TX*)X, dS, g1, dX, part_dg1, part_dbe1, scratch, B, T, D,    \
-                                           Bcap, eps);                                                         \
-    } while (0)
-    if (act == Act::F32 || x_f32) {
-        if (smem) RM_LN1B(float, true); else RM_LN1B(float, false);
+    if (D > kLn1MaxCols * kLn1Threads || T > kRowMaxT) return cudaErrorNotSupported;
+    const QDiv qd = make_qdiv(D / T);
+    const bool pairs = (D / T) % 2 == 0 && D % 4 == 0;
+    if (act == Act::F32) {
+        if (pairs)
+            ln1_mix_backward_pair_kernel<float><<<grid, kLn1Threads, 0, s>>>((const float*)Yh, rstd, dS, g1, dX,
+                                                                             part_dg1, part_dbe1, B, T, D, Bcap, qd);
+        else
+            ln1_mix_backward_kernel<float><<<grid, kLn1Threads, 0, s>>>((const float*)Yh, rstd, dS, g1, dX, part_dg1,
+                                                                        part_dbe1, B, T, D, Bcap, qd);
     } else {
-        if (smem) RM_LN1B(__nv_bfloat16, true); else RM_LN1B(__nv_bfloat16, false);
+        if (pairs)
+            ln1_mix_backward_pair_kernel<__half><<<grid, kLn1Threads, 0, s>>>((const __half*)Yh, rstd, dS, g1, dX,
+                                                                              part_dg1, part_dbe1, B, T, D, Bcap, qd);
+        else
+            ln1_mix_backward_kernel<__half><<<grid, kLn1Threads, 0, s>>>((const __half*)Yh, rstd, dS, g1, dX,
+                                                                         part_dg1, part_dbe1, B, T, D, Bcap, qd);
     }
-#undef RM_LN1B
     return cudaGetLastError();
 }
 
@@ -395,7 +823,12 @@ cudaError_t launch_sum_rows(const float* in, float* out, float* out_all, int G, 
 
 cudaError_t launch_pool_backward(const float* dpooled, float* G, int B, int T, int D, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
-    pool_backward_kernel<<<grid_for((long long)B * T * D, 256, 4096), 256, 0, s>>>(dpooled, G, B, T, D);
+    const bool vec = D % 4 == 0 && (reinterpret_cast<uintptr_t>(dpooled) & 15u) == 0 &&
+                     (reinterpret_cast<uintptr_t>(G) & 15u) == 0;
+    if (vec)
+        pool_backward_kernel<<<grid_for((long long)B * (D / 4), 256, 4096), 256, 0, s>>>(dpooled, G, B, T, D);
+    else
+        pool_backward_scalar_kernel<<<grid_for((long long)B * D, 256, 4096), 256, 0, s>>>(dpooled, G, B, T, D);
     return cudaGetLastError();
 }
 

@@ -4,10 +4,14 @@
 // Phi comes from the upper tail Q(x) = erfc(x / sqrt 2) / 2 for x = |u|,
 // with erfc by Abramowitz & Stegun 7.1.26 (|error of erf| <= 1.5e-7):
 //   erfc(y) ~= t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-y^2),  t = 1 / (1 + p y).
-// exp(-y^2) with y = |u| / sqrt 2 is exp(-u^2 / 2), which phi(u) shares.
+// exp(-y^2) with y = |u| / sqrt 2 is exp(-u^2 / 2), which phi(u) shares; it and
+// the reciprocal run on the special-function unit (ex2.approx, rcp.approx,
+// relative error about 2^-22), far inside the approximation's own 1.5e-7.
 #pragma once
 
 #include <cuda_runtime.h>
+
+#include "rm_common.cuh"
 
 namespace rm {
 
@@ -22,9 +26,10 @@ __device__ __forceinline__ GeluPair gelu_with_grad(float u) {
                     a5 = 1.061405429f;
     constexpr float inv_sqrt2 = 0.70710678118654752f;
     constexpr float inv_sqrt_2pi = 0.39894228040143268f;
+    constexpr float half_log2e = 0.72134752044448170f;     // log2(e) / 2
     const float y = fabsf(u) * inv_sqrt2;
-    const float e = __expf(-0.5f * u * u);                 // exp(-u^2 / 2)
-    const float t = __frcp_rn(fmaf(p, y, 1.0f));
+    const float e = ex2_approx(-half_log2e * u * u);       // exp(-u^2 / 2) on the MUFU unit
+    const float t = rcp_approx(fmaf(p, y, 1.0f));
     const float poly = t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, a5, a4), a3), a2), a1);
     const float q = 0.5f * poly * e;                       // Q(|u|) = P(N(0,1) > |u|)
     const float Phi = u >= 0.0f ? 1.0f - q : q;

@@ -174,28 +174,37 @@ __device__ __forceinline__ void epilogue(const KArgs& a, int g, int m, bool vali
         const size_t off = row + 32 * c;
         if (EPI == TE_GELU2) {
             if (valid) {
-                const float* bias = a.bias + (size_t)g * a.N + n0 + 32 * c;
+                const float4* b4 = reinterpret_cast<const float4*>(a.bias + (size_t)g * a.N + n0 + 32 * c);
                 uint32_t pa[16], pg[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const GeluPair x0 = gelu_with_grad(fmaf(v[2 * j], inv_s, __ldg(bias + 2 * j)));
-                    const GeluPair x1 = gelu_with_grad(fmaf(v[2 * j + 1], inv_s, __ldg(bias + 2 * j + 1)));
-                    pa[j] = f16x2_bits(x0.value, x1.value);
-                    pg[j] = f16x2_bits(x0.grad, x1.grad);
+                for (int j = 0; j < 8; ++j) {
+                    const float4 bb = __ldg(b4 + j);
+                    const GeluPair x0 = gelu_with_grad(fmaf(v[4 * j], inv_s, bb.x));
+                    const GeluPair x1 = gelu_with_grad(fmaf(v[4 * j + 1], inv_s, bb.y));
+                    const GeluPair x2 = gelu_with_grad(fmaf(v[4 * j + 2], inv_s, bb.z));
+                    const GeluPair x3 = gelu_with_grad(fmaf(v[4 * j + 3], inv_s, bb.w));
+                    pa[2 * j] = f16x2_bits(x0.value, x1.value);
+                    pa[2 * j + 1] = f16x2_bits(x2.value, x3.value);
+                    pg[2 * j] = f16x2_bits(x0.grad, x1.grad);
+                    pg[2 * j + 1] = f16x2_bits(x2.grad, x3.grad);
                 }
                 store16x32(reinterpret_cast<__half*>(a.c0) + off, pa);
                 store16x32(reinterpret_cast<__half*>(a.c1) + off, pg);
             }
         } else if (EPI == TE_RESID) {
             if (valid) {
-                const float* bias = a.bias + (size_t)g * a.N + n0 + 32 * c;
+                const float4* b4 = reinterpret_cast<const float4*>(a.bias + (size_t)g * a.N + n0 + 32 * c);
                 float rr[32];
                 load16x32(reinterpret_cast<const __half*>(a.r) + off, rr);
                 uint32_t p[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    p[j] = f16x2_bits(fmaf(v[2 * j], inv_s, __ldg(bias + 2 * j)) + rr[2 * j],
-                                      fmaf(v[2 * j + 1], inv_s, __ldg(bias + 2 * j + 1)) + rr[2 * j + 1]);
+                for (int j = 0; j < 8; ++j) {
+                    const float4 bb = __ldg(b4 + j);
+                    p[2 * j] = f16x2_bits(fmaf(v[4 * j], inv_s, bb.x) + rr[4 * j],
+                                          fmaf(v[4 * j + 1], inv_s, bb.y) + rr[4 * j + 1]);
+                    p[2 * j + 1] = f16x2_bits(fmaf(v[4 * j + 2], inv_s, bb.z) + rr[4 * j + 2],
+                                              fmaf(v[4 * j + 3], inv_s, bb.w) + rr[4 * j + 3]);
+                }
                 store16x32(reinterpret_cast<__half*>(a.c0) + off, p);
             }
         } else if (EPI == TE_DGELU) {

@@ -110,6 +110,8 @@ def test_null_context_calls(lib):
     grads = _lib.rm_layer_grads()
     assert lib.rm_block_backward(None, 0, None, None, None, ctypes.byref(grads), 1, None) == _lib.RM_ERR_INVALID_ARG
     assert lib.rm_stack_backward(None, None, None, None, ctypes.byref(grads), 1, None) == _lib.RM_ERR_INVALID_ARG
+    assert lib.rm_stack_forward_train(None, None, None, 1, None) == _lib.RM_ERR_INVALID_ARG
+    assert lib.rm_stack_backward_saved(None, None, None, ctypes.byref(grads), 1, None) == _lib.RM_ERR_INVALID_ARG
     assert lib.rm_debug_gelu_grad(None, None, -1, None) == _lib.RM_ERR_INVALID_ARG   # n < 0
     assert lib.rm_debug_gelu_grad(None, None, 3, None) == _lib.RM_ERR_INVALID_ARG    # NULL buffers
 

@@ -185,3 +185,50 @@ def test_backward_needs_a_training_context():
     assert e.value.status == _lib.RM_ERR_INVALID_ARG
     with pytest.raises(_lib.RankMixerError):
         mt.block_backward(0, torch.cat([X, X]), torch.cat([G, G]))   # B above max_batch
+
+
+@pytest.mark.parametrize("dtype,T,D,k,B,L", [("f32", 4, 8, 2, 64, 2), ("bf16", 4, 256, 4, 130, 2),
+                                             ("bf16", 16, 768, 4, 40, 2)])
+def test_training_forward_pooled_matches_oracle(dtype, T, D, k, B, L):
+    m, layers = _model(T, D, k, L, B, 81 + D, dtype)
+    X0 = synth.make_input(B, T, D, 82, dtype, DEV)
+    pooled = m.stack_forward_train(X0)
+    torch.cuda.synchronize()
+    assert m.sync_status() == _lib.RM_OK
+    check(pooled, oracle.stack_forward(_np(X0), synth.to_f64(layers)), dtype, f"training forward {dtype} pooled")
+
+
+def test_saved_backward_equals_the_one_call_backward():
+    """stack_forward_train + stack_backward_saved gives the one-call stack_backward's
+    gradients bit for bit (the same kernels on the same inputs)."""
+    T, D, k, B, L = 4, 256, 4, 150, 2
+    m, layers = _model(T, D, k, L, B, 91, "bf16")
+    X0 = synth.make_input(B, T, D, 92, "bf16", DEV)
+    dP = synth.make_output_grad((B, D), 93, device=DEV)
+    dX_a, g_a = m.stack_backward(X0, dP)
+    m.stack_forward_train(X0)
+    dX_b, g_b = m.stack_backward_saved(dP)
+    torch.cuda.synchronize()
+    assert torch.equal(dX_a, dX_b)
+    for n in range(L):
+        for k_ in NAMES:
+            assert torch.equal(g_a[n][k_], g_b[n][k_]), (n, k_)
+
+
+def test_saved_backward_needs_its_training_forward():
+    T, D, k, B = 4, 8, 2, 8
+    m, _ = _model(T, D, k, 2, B, 95, "f32")
+    X0 = synth.make_input(B, T, D, 96, "f32", DEV)
+    dP = synth.make_output_grad((B, D), 97, device=DEV)
+    with pytest.raises(_lib.RankMixerError) as e:          # nothing saved yet
+        m.stack_backward_saved(dP)
+    assert e.value.status == _lib.RM_ERR_INVALID_ARG
+    m.stack_forward_train(X0)
+    with pytest.raises(_lib.RankMixerError) as e:          # another batch size
+        m.stack_backward_saved(dP[:4].contiguous())
+    assert e.value.status == _lib.RM_ERR_INVALID_ARG
+    m.stack_backward_saved(dP)
+    torch.cuda.synchronize()
+    with pytest.raises(_lib.RankMixerError) as e:          # the activations were consumed
+        m.stack_backward_saved(dP)
+    assert e.value.status == _lib.RM_ERR_INVALID_ARG
