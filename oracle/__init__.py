@@ -61,6 +61,9 @@ def _load():
             lib.oracle_layernorm_backward.argtypes = [dp, dp, dp, ctypes.c_double, dp, dp, dp, i, i]
             lib.oracle_block_backward.argtypes = [dp] * 11 + [ctypes.c_double] + [dp] * 8 + [i, i, i, i]
             lib.oracle_stack_backward.argtypes = [dp] * 11 + [ctypes.c_double] + [dp] * 8 + [i, i, i, i, i]
+            lib.oracle_head.argtypes = [dp, dp, ctypes.c_double, dp, dp, dp, dp, dp, dp, i, i]
+            lib.oracle_tokenize.argtypes = [dp, dp, dp, dp, i, i, i, i]
+            lib.oracle_tokenize_backward.argtypes = [dp] * 6 + [i, i, i, i]
             lib.oracle_num_threads.restype = ctypes.c_int
             lib.oracle_set_num_threads.argtypes = [i]
             _lib = lib
@@ -246,3 +249,42 @@ def stack_backward(X0, dpooled, layers: list, eps: float = 1e-5):
     _load().oracle_stack_backward(_p(X0), _p(dpooled), _p(dX0), *[_p(cat[k]) for k in _PARAM_KEYS], float(eps),
                                   *[_p(g[k]) for k in GRAD_KEYS], B, T, D, F, L)
     return dX0, [{k: g[k][n] for k in GRAD_KEYS} for n in range(L)]
+
+
+def head(O, w, b: float, y=None):
+    """Prediction head ("RankMixer 详解（1）" sections 5.1-5.2): z = o w + b, p = sigmoid(z),
+    and with labels y the per-sample BCE loss, dl/dz = p - y and dl/do = (p - y) w.
+    Returns a dict with z, p (and loss, dz, dO when y is given)."""
+    O, w = _f64(O), _f64(w)
+    B, D = O.shape
+    out = {"z": np.empty(B), "p": np.empty(B)}
+    null = ctypes.POINTER(ctypes.c_double)()
+    if y is None:
+        _load().oracle_head(_p(O), _p(w), float(b), null, _p(out["z"]), _p(out["p"]), null, null, null, B, D)
+        return out
+    y = _f64(y)
+    out.update(loss=np.empty(B), dz=np.empty(B), dO=np.empty_like(O))
+    _load().oracle_head(_p(O), _p(w), float(b), _p(y), _p(out["z"]), _p(out["p"]), _p(out["loss"]), _p(out["dz"]),
+                        _p(out["dO"]), B, D)
+    return out
+
+
+def tokenize(E, W, bias) -> np.ndarray:
+    """Feature tokenization ("RankMixer" Eq. 2; "RankMixer 详解（1）" section 2.4): X0[b, t] =
+    E[b, t d:(t + 1) d] W[t] + bias[t].  E [B, T d], W [T, d, D], bias [T, D] -> X0 [B, T, D]."""
+    E, W, bias = _f64(E), _f64(W), _f64(bias)
+    T, d, D = W.shape
+    B = E.shape[0]
+    X0 = np.empty((B, T, D))
+    _load().oracle_tokenize(_p(E), _p(W), _p(bias), _p(X0), B, T, d, D)
+    return X0
+
+
+def tokenize_backward(E, W, dX0):
+    """Gradients of the tokenization for dX0 [B, T, D]: returns (dE [B, T d], dW [T, d, D], db [T, D])."""
+    E, W, dX0 = _f64(E), _f64(W), _f64(dX0)
+    T, d, D = W.shape
+    B = E.shape[0]
+    dE, dW, db = np.empty_like(E), np.empty_like(W), np.empty((T, D))
+    _load().oracle_tokenize_backward(_p(E), _p(W), _p(dX0), _p(dE), _p(dW), _p(db), B, T, d, D)
+    return dE, dW, db

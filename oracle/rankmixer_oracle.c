@@ -504,6 +504,81 @@ ORACLE_API void oracle_stack_backward(const double *X0, const double *dpooled, d
     free(Xs); free(Gc); free(Gn);
 }
 
+/* ------------------------------------------------------------------ */
+/* Prediction head on the pooled output, [WT] sections 5.1-5.2:         */
+/*   z = o w + b,  p = sigmoid(z) = 1 / (1 + e^-z),                     */
+/*   l = -y log p - (1 - y) log(1 - p),  dl/dz = p - y,                 */
+/*   dl/do = (p - y) w.                                                 */
+/* log p = -softplus(-z) and log(1 - p) = -softplus(z) with             */
+/* softplus(x) = log(1 + e^x), written so neither overflows.            */
+/* y, loss, dz and dO may be NULL (no label: z and p only).             */
+/* ------------------------------------------------------------------ */
+static double softplus(double x)
+{
+    return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x));
+}
+
+ORACLE_API void oracle_head(const double *O, const double *w, double b, const double *y,
+                            double *z, double *p, double *loss, double *dz, double *dO, int B, int D)
+{
+    for (int i = 0; i < B; ++i) {
+        double zi = b;
+        for (int j = 0; j < D; ++j) zi += O[(size_t)i * D + j] * w[j];
+        const double pi = 1.0 / (1.0 + exp(-zi));
+        if (z) z[i] = zi;
+        if (p) p[i] = pi;
+        if (!y) continue;
+        if (loss) loss[i] = y[i] * softplus(-zi) + (1.0 - y[i]) * softplus(zi);
+        if (dz) dz[i] = pi - y[i];
+        if (dO)
+            for (int j = 0; j < D; ++j) dO[(size_t)i * D + j] = (pi - y[i]) * w[j];
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Feature tokenization, [RM] Eq. 2 / [WT] section 2.4: token i is the  */
+/* i-th slice of d coordinates of the concatenated embedding, projected */
+/* to D by its own linear layer,                                        */
+/*   x_i = e[d (i-1) : d i] W_i + b_i,  W_i [d][D], b_i [D]             */
+/* (0-based here: slice t is e[t d : (t + 1) d]).  E [B][T d] -> X0     */
+/* [B][T][D].  Backward: dW_i = sum_b e_slice^T dX0[b][i],              */
+/* db_i = sum_b dX0[b][i], dE slice = dX0[b][i] W_i^T.                  */
+/* ------------------------------------------------------------------ */
+ORACLE_API void oracle_tokenize(const double *E, const double *W, const double *bias, double *X0,
+                                int B, int T, int d, int D)
+{
+    for (int b = 0; b < B; ++b)
+        for (int t = 0; t < T; ++t) {
+            const double *e = E + (size_t)b * T * d + (size_t)t * d;
+            double *x = X0 + ((size_t)b * T + t) * D;
+            for (int j = 0; j < D; ++j) x[j] = bias[(size_t)t * D + j];
+            for (int i = 0; i < d; ++i)
+                for (int j = 0; j < D; ++j) x[j] += e[i] * W[((size_t)t * d + i) * D + j];
+        }
+}
+
+ORACLE_API void oracle_tokenize_backward(const double *E, const double *W, const double *dX0, double *dE,
+                                         double *dW, double *db, int B, int T, int d, int D)
+{
+    memset(dW, 0, sizeof(double) * (size_t)T * d * D);
+    memset(db, 0, sizeof(double) * (size_t)T * D);
+    for (int b = 0; b < B; ++b)
+        for (int t = 0; t < T; ++t) {
+            const double *e = E + (size_t)b * T * d + (size_t)t * d;
+            const double *g = dX0 + ((size_t)b * T + t) * D;
+            double *de = dE + (size_t)b * T * d + (size_t)t * d;
+            for (int j = 0; j < D; ++j) db[(size_t)t * D + j] += g[j];
+            for (int i = 0; i < d; ++i) {
+                double acc = 0.0;
+                for (int j = 0; j < D; ++j) {
+                    dW[((size_t)t * d + i) * D + j] += e[i] * g[j];
+                    acc += g[j] * W[((size_t)t * d + i) * D + j];
+                }
+                de[i] = acc;
+            }
+        }
+}
+
 ORACLE_API int oracle_num_threads(void)
 {
 #if defined(_OPENMP)
