@@ -416,9 +416,9 @@ rm_status train_ws_ready(rm_ctx* c, int nslots, bool stack) {
     const size_t osz = op_size(c->act);                    // operands, yhat, Gelu'(U) and Z: fp16 or float
     rm_status st;
     if (!t.ready) {
-        t.nblk2 = ln2_bwd_blocks(c->Bcap, g.T, c->num_sms);
+        t.nblk2 = ln2_bwd_blocks(c->act, c->Bcap, g.T, g.D, c->num_sms);
         t.colrows = (c->Bcap + 127) / 128 * (128 / kTrainColpartRows);
-        t.grid1 = ln1_bwd_grid(c->Bcap, c->num_sms);
+        t.grid1 = ln1_bwd_grid(c->Bcap, g.T, g.D, c->num_sms);
         if ((st = dmalloc(c, (void**)&t.dZ32, T * Bc * D * 4, &c->ws_bytes)) != RM_OK ||
             (c->act != Act::F32 && (st = dmalloc(c, &t.dZ, T * Bc * D * osz, &c->ws_bytes)) != RM_OK) ||
             (st = dmalloc(c, (void**)&t.dS, T * Bc * D * 4, &c->ws_bytes)) != RM_OK ||
@@ -521,7 +521,7 @@ rm_status train_layer_backward(rm_ctx* c, int layer, int slot, const float* G, f
     const int T = g.T, D = g.D, F = c->F, Bc = c->Bcap;
     const long long BcD = (long long)Bc * D, BcF = (long long)Bc * F, DF = (long long)D * F;
     rm_status st;
-    const int nblk = ln2_bwd_blocks(B, T, c->num_sms);
+    const int nblk = ln2_bwd_blocks(c->act, B, T, D, c->num_sms);
     float* p_db2 = t.part2;
     float* p_dg2 = t.part2 + (size_t)T * t.nblk2 * D;
     float* p_dbe2 = t.part2 + 2 * (size_t)T * t.nblk2 * D;
@@ -531,7 +531,7 @@ rm_status train_layer_backward(rm_ctx* c, int layer, int slot, const float* G, f
     {
         ProfScope ps(c, RM_K_BWD_ROWS, s);
         RM_CHECK_CUDA(launch_ln2_backward(c->act, sl.Z, G, w.g2, t.dZ32, p_db2, p_dg2, p_dbe2, t.pmax, B, T, D, Bc,
-                                          g.ln_eps, c->num_sms, s),
+                                          g.ln_eps, c->num_sms, c->d_err, kWaitTimeoutNs, s),
                       "ln2 backward");
         if (c->act != Act::F32) {
             RM_CHECK_CUDA(launch_grad_scale(t.dZ32, t.pmax, nblk, t.inv_scale, t.dZ, B, T, D, Bc, s), "grad scale");
@@ -578,11 +578,11 @@ rm_status train_layer_backward(rm_ctx* c, int layer, int slot, const float* G, f
     }
     {
         ProfScope ps(c, RM_K_BWD_ROWS, s);
-        const int grid1 = ln1_bwd_grid(B, c->num_sms);
+        const int grid1 = ln1_bwd_grid(B, T, D, c->num_sms);
         float* p_dg1 = t.part1;
         float* p_dbe1 = t.part1 + (size_t)t.grid1 * D;
         RM_CHECK_CUDA(launch_ln1_mix_backward(c->act, sl.Yh, sl.rstd1, t.dS, w.g1, dX, p_dg1, p_dbe1, B, T, D, Bc,
-                                              grid1, s),
+                                              grid1, c->d_err, kWaitTimeoutNs, s),
                       "ln1 + mixing backward");
         if (db1_partials) {
             const int rows = (B + 127) / 128 * (128 / kTrainColpartRows);

@@ -96,12 +96,13 @@ cudaError_t launch_ln2_out_f32(const void* Z, const float2* stats, const float* 
 // LN2 backward.  Z [T][Bcap][D] (aux type), G sample-major [B][T][D] float:
 // dZ = LN2 backward of G (float, token-major); per (token, CTA) partial sums
 // [T][nblk][D] of dZ, G * zhat and G, and the largest |dZ| of each (token,
-// CTA) in part_max [T][nblk], nblk = ln2_bwd_blocks(B, T, num_sms) (which
-// never exceeds ln2_bwd_blocks(max_batch, T, num_sms)).
-int ln2_bwd_blocks(int B, int T, int num_sms);
+// CTA) in part_max [T][nblk], nblk = ln2_bwd_blocks(act, B, T, D, num_sms)
+// (never above its value at max_batch).  Bulk-copy waits are bounded
+// (timeout_ns, error word err).
+int ln2_bwd_blocks(Act act, int B, int T, int D, int num_sms);
 cudaError_t launch_ln2_backward(Act act, const void* Z, const float* G, const float* g2, float* dZ, float* part_db2,
                                 float* part_dg2, float* part_dbe2, float* part_max, int B, int T, int D, int Bcap,
-                                float eps, int num_sms, cudaStream_t s);
+                                float eps, int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s);
 
 // Per-token scale of the gradient operands: s_t = 2^(9 - e) with 2^e >= the
 // largest |dZ| of token t (1 when it is 0); inv_scale[t] = 1 / s_t and
@@ -112,11 +113,13 @@ cudaError_t launch_grad_scale(const float* dZ, const float* part_max, int nblk, 
 // LN1 and mixing backward from the recompute's yhat and rstd: dS [T][Bcap][D]
 // float, dX = dY + P^T dY sample-major float with dY the LN1 backward of dS.
 // Per-CTA partial sums [grid][D] of dS * yhat and dS, grid from ln1_bwd_grid
-// (which never exceeds ln1_bwd_grid(max_batch, num_sms)).
-int ln1_bwd_grid(int B, int num_sms);
+// (which never exceeds ln1_bwd_grid(max_batch, T, D, num_sms)).
+// When the sample's dS rows fit in shared memory the kernel stages them with
+// bulk copies; its wait on them is bounded (timeout_ns, error word err).
+int ln1_bwd_grid(int B, int T, int D, int num_sms);
 cudaError_t launch_ln1_mix_backward(Act act, const void* Yh, const float* rstd, const float* dS, const float* g1,
                                     float* dX, float* part_dg1, float* part_dbe1, int B, int T, int D, int Bcap,
-                                    int grid, cudaStream_t s);
+                                    int grid, int* err, unsigned long long timeout_ns, cudaStream_t s);
 
 // out[g][n] = sum over r < R of in[g][r][n] (fixed order), and, when
 // out_all is not null, out_all[n] = sum over g of out[g][n].

@@ -44,6 +44,16 @@ QDiv make_qdiv(int q) {
     return d;
 }
 
+// After a bounded wait gave up: wait (again bounded, ignoring the abort flag)
+// for the bulk copies still counted on `bar`, so that none lands in shared
+// memory after the CTA has exited.
+__device__ __forceinline__ void drain_copies(uint32_t bar, uint32_t parity, unsigned long long timeout_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > timeout_ns) return;
+    }
+}
+
 // Element k of the residual row y = Mix(X)[t] + X[t] of one sample:
 // Mix(X)[t][c q + r] = X[c][t q + r].
 template <typename Tx>
@@ -359,6 +369,7 @@ ln2_backward_vec_kernel(const Tz* __restrict__ Z, const float* __restrict__ G, c
                 st[warp] = make_float4(shift + dm, rstd, sq / (float)D, rstd * (sqz - dm * sq) / (float)D);
         }
         __syncthreads();
+#pragma unroll 4
         for (int i = 0; i < nrows; ++i) {
             const float4 s = st[i];
             float* dz = dZ + ((size_t)t * Bcap + b0 + i) * D;
@@ -385,6 +396,144 @@ ln2_backward_vec_kernel(const Tz* __restrict__ Z, const float* __restrict__ G, c
                 }
             }
         }
+    }
+    const size_t prow = ((size_t)t * nbx + bx) * D;
+#pragma unroll
+    for (int j = 0; j < kLn2MaxPairs; ++j) {
+        const int pidx = threadIdx.x + j * kLn2Threads;
+        if (pidx < npairs) {
+            *reinterpret_cast<float2*>(part_db2 + prow + 2 * pidx) = adb[j];
+            *reinterpret_cast<float2*>(part_dg2 + prow + 2 * pidx) = adg[j];
+            *reinterpret_cast<float2*>(part_dbe2 + prow + 2 * pidx) = adbe[j];
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    if (lane == 0) wmax[warp] = amax;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float m = 0.f;
+        for (int w = 0; w < kLn2Threads / 32; ++w) m = fmaxf(m, wmax[w]);
+        part_max[(size_t)t * nbx + bx] = m;
+    }
+}
+
+// Double-buffered variant (D a multiple of 8, two chunks fit in shared
+// memory): a chunk is 8 rows of one token; while the CTA computes chunk i from
+// one buffer, chunk i + 1 arrives in the other by bulk copies (the 8 Z rows
+// are one contiguous block; the 8 G rows are T D floats apart), completion
+// counted on that buffer's mbarrier with a bounded wait.
+template <typename Tz>
+__global__ void __launch_bounds__(kLn2Threads, 1)
+ln2_backward_db_kernel(const Tz* __restrict__ Z, const float* __restrict__ G, const float* __restrict__ g2,
+                       float* __restrict__ dZ, float* __restrict__ part_db2, float* __restrict__ part_dg2,
+                       float* __restrict__ part_dbe2, float* __restrict__ part_max, int B, int T, int D, int Bcap,
+                       float eps, int rows_per_cta, int* err, unsigned long long timeout_ns) {
+    extern __shared__ float4 smem4[];
+    float4* st = smem4;                                            // [kLn2Chunk]
+    float* gbuf = reinterpret_cast<float*>(smem4 + kLn2Chunk);     // 2 x [kLn2Chunk][D]
+    Tz* zbuf = reinterpret_cast<Tz*>(gbuf + 2 * (size_t)kLn2Chunk * D);   // 2 x [kLn2Chunk][D]
+    __shared__ __align__(8) uint64_t bars[2];
+    __shared__ int s_abort;
+    __shared__ float wmax[kLn2Threads / 32];
+    const int t = blockIdx.y, bx = blockIdx.x, nbx = gridDim.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b_begin = bx * rows_per_cta;
+    const int b_end = min(B, b_begin + rows_per_cta);
+    const int npairs = D / 2;
+    float2 adb[kLn2MaxPairs], adg[kLn2MaxPairs], adbe[kLn2MaxPairs];
+#pragma unroll
+    for (int j = 0; j < kLn2MaxPairs; ++j) adb[j] = adg[j] = adbe[j] = make_float2(0.f, 0.f);
+    float amax = 0.f;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bars[0]), 1);
+        mbar_init(smem_u32(&bars[1]), 1);
+        s_abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    auto issue = [&](int chunk, int buf) {     // thread 0: chunk `chunk` of this CTA into buffer `buf`
+        const int b0 = b_begin + chunk * kLn2Chunk;
+        const int nrows = min(kLn2Chunk, b_end - b0);
+        const uint32_t bar = smem_u32(&bars[buf]);
+        const uint32_t zbytes = (uint32_t)(nrows * D * sizeof(Tz)), gbytes = (uint32_t)(D * sizeof(float));
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, zbytes + gbytes * (uint32_t)nrows);
+        bulk_copy_g2s(smem_u32(zbuf + (size_t)buf * kLn2Chunk * D), Z + ((size_t)t * Bcap + b0) * D, zbytes, bar);
+        for (int r = 0; r < nrows; ++r)
+            bulk_copy_g2s(smem_u32(gbuf + ((size_t)buf * kLn2Chunk + r) * D), G + ((size_t)(b0 + r) * T + t) * D,
+                          gbytes, bar);
+    };
+    const int nchunks = b_end > b_begin ? (b_end - b_begin + kLn2Chunk - 1) / kLn2Chunk : 0;
+    if (threadIdx.x == 0 && nchunks > 0) issue(0, 0);
+    for (int i = 0; i < nchunks; ++i) {
+        const int buf = i & 1;
+        if (threadIdx.x == 0 && i + 1 < nchunks) issue(i + 1, buf ^ 1);   // its buffer was released by the last sync
+        const bool ok = mbar_wait_bounded(smem_u32(&bars[buf]), (uint32_t)(i >> 1) & 1u, &s_abort, err, timeout_ns);
+        if (__syncthreads_or(!ok)) {           // every thread leaves together; the copies in flight land first
+            if (threadIdx.x == 0) {
+                drain_copies(smem_u32(&bars[buf]), (uint32_t)(i >> 1) & 1u, timeout_ns);
+                if (i + 1 < nchunks) drain_copies(smem_u32(&bars[buf ^ 1]), (uint32_t)((i + 1) >> 1) & 1u, timeout_ns);
+            }
+            break;
+        }
+        const int b0 = b_begin + i * kLn2Chunk;
+        const int nrows = min(kLn2Chunk, b_end - b0);
+        const Tz* zs = zbuf + (size_t)buf * kLn2Chunk * D;
+        const float* gs = gbuf + (size_t)buf * kLn2Chunk * D;
+        if (warp < nrows) {
+            const Tz* z = zs + (size_t)warp * D;
+            const float* gr = gs + (size_t)warp * D;
+            const float shift = to_f32(z[0]);
+            float s1 = 0.f, s2 = 0.f, sq = 0.f, sqz = 0.f;
+            for (int k = 4 * lane; k < D; k += 128) {
+                const float4 zz = ld4_any<Tz>(z + k);
+                const float4 gg = *reinterpret_cast<const float4*>(gr + k);
+                const float4 ga = __ldg(reinterpret_cast<const float4*>(g2 + k));
+                const float d0 = zz.x - shift, d1 = zz.y - shift, d2 = zz.z - shift, d3 = zz.w - shift;
+                const float q0 = gg.x * ga.x, q1 = gg.y * ga.y, q2 = gg.z * ga.z, q3 = gg.w * ga.w;
+                s1 += (d0 + d1) + (d2 + d3);
+                s2 = fmaf(d0, d0, fmaf(d1, d1, fmaf(d2, d2, fmaf(d3, d3, s2))));
+                sq += (q0 + q1) + (q2 + q3);
+                sqz = fmaf(q0, d0, fmaf(q1, d1, fmaf(q2, d2, fmaf(q3, d3, sqz))));
+            }
+            s1 = warp_sum(s1);
+            s2 = warp_sum(s2);
+            sq = warp_sum(sq);
+            sqz = warp_sum(sqz);
+            const float dm = s1 / (float)D;
+            const float rstd = rsqrtf(fmaxf(s2 / (float)D - dm * dm, 0.f) + eps);
+            if (lane == 0)
+                st[warp] = make_float4(shift + dm, rstd, sq / (float)D, rstd * (sqz - dm * sq) / (float)D);
+        }
+        __syncthreads();
+        for (int r = 0; r < nrows; ++r) {
+            const float4 s = st[r];
+            float* dz = dZ + ((size_t)t * Bcap + b0 + r) * D;
+#pragma unroll
+            for (int j = 0; j < kLn2MaxPairs; ++j) {
+                const int pidx = threadIdx.x + j * kLn2Threads;
+                if (pidx < npairs) {
+                    const int k = 2 * pidx;
+                    const float2 zz = ld2_any<Tz>(zs + (size_t)r * D + k);
+                    const float2 gk = *reinterpret_cast<const float2*>(gs + (size_t)r * D + k);
+                    const float2 ga = __ldg(reinterpret_cast<const float2*>(g2 + k));
+                    const float zh0 = (zz.x - s.x) * s.y, zh1 = (zz.y - s.x) * s.y;
+                    float2 d;
+                    d.x = (gk.x * ga.x - s.z - zh0 * s.w) * s.y;
+                    d.y = (gk.y * ga.y - s.z - zh1 * s.w) * s.y;
+                    *reinterpret_cast<float2*>(dz + k) = d;
+                    amax = fmaxf(amax, fmaxf(fabsf(d.x), fabsf(d.y)));
+                    adb[j].x += d.x;
+                    adb[j].y += d.y;
+                    adg[j].x = fmaf(gk.x, zh0, adg[j].x);
+                    adg[j].y = fmaf(gk.y, zh1, adg[j].y);
+                    adbe[j].x += gk.x;
+                    adbe[j].y += gk.y;
+                }
+            }
+        }
+        __syncthreads();                       // buffer `buf` is free for chunk i + 2
     }
     const size_t prow = ((size_t)t * nbx + bx) * D;
 #pragma unroll
@@ -587,6 +736,7 @@ ln1_mix_backward_pair_kernel(const Tyh* __restrict__ Yh, const float* __restrict
         }
         __syncthreads();
         float* out = dX + (size_t)b * T * D;
+#pragma unroll 4
         for (int t = 0; t < T; ++t) {
             const float4 s1 = st[t];
             const size_t o1 = ((size_t)t * Bcap + b) * D;
@@ -620,6 +770,119 @@ ln1_mix_backward_pair_kernel(const Tyh* __restrict__ Yh, const float* __restrict
 #pragma unroll
     for (int j = 0; j < kLn1MaxPairs; ++j) {
         const int pidx = threadIdx.x + j * kLn1Threads;
+        if (pidx < npairs) {
+            *reinterpret_cast<float2*>(part_dg1 + (size_t)blockIdx.x * D + 2 * pidx) = adg[j];
+            *reinterpret_cast<float2*>(part_dbe1 + (size_t)blockIdx.x * D + 2 * pidx) = adbe[j];
+        }
+    }
+}
+
+// Staged variant (T D floats fit in shared memory, q even, D a multiple of 4):
+// one 1024-thread CTA per SM walks the samples; a sample's dS rows arrive in
+// shared memory by bulk copies (one per token row, completion counted on an
+// mbarrier with a bounded wait), so dS is read from HBM once and both the
+// row statistics and the transposed partners read it from shared memory.
+// yhat stays in global memory: with one sample per SM in flight its rows stay
+// in L2 between the two phases.
+constexpr int kLn1StThreads = 1024;
+constexpr int kLn1StMaxPairs = 3072 / 2 / kLn1StThreads + 1;
+
+template <typename Tyh>
+__global__ void __launch_bounds__(kLn1StThreads, 1)
+ln1_mix_backward_staged_kernel(const Tyh* __restrict__ Yh, const float* __restrict__ rstdv,
+                               const float* __restrict__ dS, const float* __restrict__ g1, float* __restrict__ dX,
+                               float* __restrict__ part_dg1, float* __restrict__ part_dbe1, int B, int T, int D,
+                               int Bcap, QDiv qd, int* err, unsigned long long timeout_ns) {
+    extern __shared__ float4 smem4[];
+    float4* st = smem4;                                      // [T] (rstd, mean(q), mean(q yhat))
+    float* ds = reinterpret_cast<float*>(smem4 + T);         // [T][D] the sample's dS rows
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int s_abort;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = (int)qd.q;
+    const int npairs = D / 2;
+    int cc_[kLn1StMaxPairs], rr_[kLn1StMaxPairs];
+#pragma unroll
+    for (int j = 0; j < kLn1StMaxPairs; ++j) {
+        const int k = 2 * (threadIdx.x + j * kLn1StThreads);
+        cc_[j] = k < D ? qd.div(k) : 0;
+        rr_[j] = k - cc_[j] * q;
+    }
+    float2 adg[kLn1StMaxPairs], adbe[kLn1StMaxPairs];
+#pragma unroll
+    for (int j = 0; j < kLn1StMaxPairs; ++j) adg[j] = adbe[j] = make_float2(0.f, 0.f);
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        s_abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const uint32_t row_bytes = (uint32_t)D * 4u;
+    uint32_t phase = 0;
+    for (int b = blockIdx.x; b < B; b += gridDim.x) {
+        __syncthreads();                                     // the previous sample is done with ds and st
+        if (threadIdx.x == 0) {
+            fence_proxy_async_smem();                        // generic reads of ds before the async writes
+            mbar_arrive_expect_tx(smem_u32(&bar), row_bytes * (uint32_t)T);
+            for (int t = 0; t < T; ++t)
+                bulk_copy_g2s(smem_u32(ds + (size_t)t * D), dS + ((size_t)t * Bcap + b) * D, row_bytes,
+                              smem_u32(&bar));
+        }
+        const bool ok = mbar_wait_bounded(smem_u32(&bar), phase, &s_abort, err, timeout_ns);
+        if (__syncthreads_or(!ok)) {                         // every thread leaves together on a timeout
+            if (threadIdx.x == 0) drain_copies(smem_u32(&bar), phase, timeout_ns);
+            break;
+        }
+        phase ^= 1u;
+        for (int t = warp; t < T; t += kLn1StThreads / 32) {
+            const size_t o = ((size_t)t * Bcap + b) * D;
+            const float* dr = ds + (size_t)t * D;
+            float mq = 0.f, mqy = 0.f;
+            for (int k = 4 * lane; k < D; k += 128) {
+                const float4 d = *reinterpret_cast<const float4*>(dr + k);
+                const float4 gg = __ldg(reinterpret_cast<const float4*>(g1 + k));
+                const float4 y = Pair2<Tyh>::ld4(Yh + o + k);
+                const float q0 = d.x * gg.x, q1 = d.y * gg.y, q2 = d.z * gg.z, q3 = d.w * gg.w;
+                mq += (q0 + q1) + (q2 + q3);
+                mqy = fmaf(q0, y.x, fmaf(q1, y.y, fmaf(q2, y.z, fmaf(q3, y.w, mqy))));
+            }
+            mq = warp_sum(mq);
+            mqy = warp_sum(mqy);
+            if (lane == 0) st[t] = make_float4(rstdv[(size_t)t * Bcap + b], mq / (float)D, mqy / (float)D, 0.f);
+        }
+        __syncthreads();
+        float* out = dX + (size_t)b * T * D;
+#pragma unroll
+        for (int j = 0; j < kLn1StMaxPairs; ++j) {
+            const int pidx = threadIdx.x + j * kLn1StThreads;
+            if (pidx < npairs) {
+                const int k = 2 * pidx;
+                const int c = cc_[j];
+                const float4 s2 = st[c];
+                const float2 ga = __ldg(reinterpret_cast<const float2*>(g1 + k));
+                for (int t = 0; t < T; ++t) {
+                    const float4 s1 = st[t];
+                    const int k2 = t * q + rr_[j];           // partners (c, k2) and (c, k2 + 1)
+                    const float2 gb = __ldg(reinterpret_cast<const float2*>(g1 + k2));
+                    const float2 y1 = Pair2<Tyh>::ld(Yh + ((size_t)t * Bcap + b) * D + k);
+                    const float2 y2 = Pair2<Tyh>::ld(Yh + ((size_t)c * Bcap + b) * D + k2);
+                    const float2 d1 = *reinterpret_cast<const float2*>(ds + (size_t)t * D + k);
+                    const float2 d2 = *reinterpret_cast<const float2*>(ds + (size_t)c * D + k2);
+                    float2 r;
+                    r.x = (d1.x * ga.x - s1.y - y1.x * s1.z) * s1.x + (d2.x * gb.x - s2.y - y2.x * s2.z) * s2.x;
+                    r.y = (d1.y * ga.y - s1.y - y1.y * s1.z) * s1.x + (d2.y * gb.y - s2.y - y2.y * s2.z) * s2.x;
+                    *reinterpret_cast<float2*>(out + (size_t)t * D + k) = r;
+                    adg[j].x = fmaf(d1.x, y1.x, adg[j].x);
+                    adg[j].y = fmaf(d1.y, y1.y, adg[j].y);
+                    adbe[j].x += d1.x;
+                    adbe[j].y += d1.y;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < kLn1StMaxPairs; ++j) {
+        const int pidx = threadIdx.x + j * kLn1StThreads;
         if (pidx < npairs) {
             *reinterpret_cast<float2*>(part_dg1 + (size_t)blockIdx.x * D + 2 * pidx) = adg[j];
             *reinterpret_cast<float2*>(part_dbe1 + (size_t)blockIdx.x * D + 2 * pidx) = adbe[j];
@@ -718,8 +981,16 @@ cudaError_t launch_ln1_recompute(Act act, bool x_f32, const void* X, void* S, vo
     return cudaGetLastError();
 }
 
-int ln2_bwd_blocks(int B, int T, int num_sms) {
-    const int want = (3 * num_sms + T - 1) / T;
+constexpr int kLn2DbSmemLimit = 220 * 1024;
+
+bool ln2_bwd_double_buffered(Act act, int D) {
+    const size_t zsz = act == Act::F32 ? 4 : 2;
+    return D % 8 == 0 && kLn2Chunk * sizeof(float4) + 2 * (size_t)kLn2Chunk * D * (4 + zsz) <= (size_t)kLn2DbSmemLimit;
+}
+
+int ln2_bwd_blocks(Act act, int B, int T, int D, int num_sms) {
+    const int per_sm = ln2_bwd_double_buffered(act, D) ? 1 : 3;
+    const int want = (per_sm * num_sms + T - 1) / T;
     const int most = (B + kLn2Chunk - 1) / kLn2Chunk;
     const int n = want < most ? want : most;
     return n < 1 ? 1 : n;
@@ -727,13 +998,30 @@ int ln2_bwd_blocks(int B, int T, int num_sms) {
 
 cudaError_t launch_ln2_backward(Act act, const void* Z, const float* G, const float* g2, float* dZ, float* part_db2,
                                 float* part_dg2, float* part_dbe2, float* part_max, int B, int T, int D, int Bcap,
-                                float eps, int num_sms, cudaStream_t s) {
+                                float eps, int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     if (D > kLn2MaxCols * kLn2Threads) return cudaErrorNotSupported;
-    const int nbx = ln2_bwd_blocks(B, T, num_sms);
+    const int nbx = ln2_bwd_blocks(act, B, T, D, num_sms);
     const int per = ((B + nbx - 1) / nbx + kLn2Chunk - 1) / kLn2Chunk * kLn2Chunk;
     const dim3 grid(nbx, T);
     const size_t zsz = act == Act::F32 ? 4 : 2;
+    if (ln2_bwd_double_buffered(act, D)) {
+        const size_t dbytes = kLn2Chunk * sizeof(float4) + 2 * (size_t)kLn2Chunk * D * (4 + zsz);
+        if (act == Act::F32) {
+            auto k = ln2_backward_db_kernel<float>;
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dbytes);
+            if (e != cudaSuccess) return e;
+            k<<<grid, kLn2Threads, dbytes, s>>>((const float*)Z, G, g2, dZ, part_db2, part_dg2, part_dbe2, part_max,
+                                                B, T, D, Bcap, eps, per, err, timeout_ns);
+        } else {
+            auto k = ln2_backward_db_kernel<__half>;
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dbytes);
+            if (e != cudaSuccess) return e;
+            k<<<grid, kLn2Threads, dbytes, s>>>((const __half*)Z, G, g2, dZ, part_db2, part_dg2, part_dbe2, part_max,
+                                                B, T, D, Bcap, eps, per, err, timeout_ns);
+        }
+        return cudaGetLastError();
+    }
     const size_t bytes = kLn2Chunk * sizeof(float4) + (size_t)kLn2Chunk * D * (4 + zsz);
     const bool vec = D % 8 == 0;               // whole 16-byte lines of fp16 rows and float4 of float rows
     if (vec) {
@@ -782,17 +1070,42 @@ cudaError_t launch_bf16_to_f16(const void* in, void* out, long long n, cudaStrea
     return cudaGetLastError();
 }
 
-int ln1_bwd_grid(int B, int num_sms) {
-    const int cap = num_sms * 4;
+constexpr int kLn1StagedSmemLimit = 220 * 1024;
+bool ln1_bwd_staged(int T, int D);
+
+int ln1_bwd_grid(int B, int T, int D, int num_sms) {
+    const int cap = ln1_bwd_staged(T, D) ? num_sms : num_sms * 4;
     return B < cap ? (B < 1 ? 1 : B) : cap;
+}
+
+bool ln1_bwd_staged(int T, int D) {
+    return (D / T) % 2 == 0 && D % 4 == 0 &&
+           (size_t)T * sizeof(float4) + (size_t)T * D * sizeof(float) <= (size_t)kLn1StagedSmemLimit;
 }
 
 cudaError_t launch_ln1_mix_backward(Act act, const void* Yh, const float* rstd, const float* dS, const float* g1,
                                     float* dX, float* part_dg1, float* part_dbe1, int B, int T, int D, int Bcap,
-                                    int grid, cudaStream_t s) {
+                                    int grid, int* err, unsigned long long timeout_ns, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     if (D > kLn1MaxCols * kLn1Threads || T > kRowMaxT) return cudaErrorNotSupported;
     const QDiv qd = make_qdiv(D / T);
+    if (ln1_bwd_staged(T, D)) {
+        const size_t bytes = (size_t)T * sizeof(float4) + (size_t)T * D * sizeof(float);
+        if (act == Act::F32) {
+            auto k = ln1_mix_backward_staged_kernel<float>;
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+            if (e != cudaSuccess) return e;
+            k<<<grid, kLn1StThreads, bytes, s>>>((const float*)Yh, rstd, dS, g1, dX, part_dg1, part_dbe1, B, T, D,
+                                                 Bcap, qd, err, timeout_ns);
+        } else {
+            auto k = ln1_mix_backward_staged_kernel<__half>;
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+            if (e != cudaSuccess) return e;
+            k<<<grid, kLn1StThreads, bytes, s>>>((const __half*)Yh, rstd, dS, g1, dX, part_dg1, part_dbe1, B, T, D,
+                                                 Bcap, qd, err, timeout_ns);
+        }
+        return cudaGetLastError();
+    }
     const bool pairs = (D / T) % 2 == 0 && D % 4 == 0;
     if (act == Act::F32) {
         if (pairs)
