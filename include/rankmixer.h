@@ -159,7 +159,9 @@ typedef enum rm_kernel_kind {
     RM_K_BWD_DGRAD = 12,   /* backward: dA = dZ W2^T (times Gelu'), dS = dU W1^T + dZ */
     RM_K_BWD_WGRAD = 13,   /* backward: dW2 = A^T dZ, dW1 = S^T dU */
     RM_K_BWD_ROWS = 14,    /* backward: LN2 and LN1 + mixing backward, bias / affine reductions */
-    RM_K_COUNT = 15
+    RM_K_TOKENIZE = 15,    /* feature tokenization: per-token projection of the embedding slices */
+    RM_K_HEAD = 16,        /* prediction head on the pooled output */
+    RM_K_COUNT = 17
 } rm_kernel_kind;
 
 typedef struct rm_kernel_stat {
@@ -267,6 +269,38 @@ RM_API rm_status rm_stack_backward_saved(rm_ctx *ctx, const float *dpooled, floa
  * and asynchrony as those two calls. */
 RM_API rm_status rm_stack_backward(rm_ctx *ctx, const void *X0, const float *dpooled, float *dX0,
                                    const rm_layer_grads *grads, int B, void *stream);
+
+/* Prediction head on the pooled output ("RankMixer 详解（1）" sections 5.1-5.2):
+ *   z = pooled[i] . w + b,  p[i] = sigmoid(z),
+ *   loss[i] = -y log p - (1 - y) log(1 - p),  dpooled[i] = s (p - y) w,
+ * with s = 1 / B when mean_loss (the gradient of the batch-mean loss), else 1.
+ * pooled: device float32 [B][D]; w: device float32 [D]; y (nullable): device
+ * float32 labels [B]; p, loss (nullable): device float32 [B]; dpooled
+ * (nullable): device float32 [B][D].  loss and dpooled need y.  The loss is
+ * computed as y softplus(-z) + (1 - y) softplus(z), finite for any z.  Needs
+ * no context.  Asynchronous on `stream`. */
+RM_API rm_status rm_head_forward(const float *pooled, const float *w, float b, const float *y, float *p,
+                                 float *loss, float *dpooled, int B, int D, int mean_loss, void *stream);
+
+/* Feature tokenization ("RankMixer" section 3.2 Eq. 2; "RankMixer 详解（1）"
+ * section 2.4): token t of a sample is the t-th slice of d coordinates of its
+ * concatenated embedding, projected to D by token t's own linear layer,
+ *   X0[b][t] = E[b][t d : (t + 1) d] W_t + b_t,  W [T][d][D], bias [T][D].
+ * rm_set_tokenizer copies W and bias (device, context dtype) into the context
+ * (synchronous; replaces an earlier tokenizer).  rm_tokenize: E device
+ * [B][T d] in the context dtype -> X0 device [B][T][D] in the context dtype
+ * (bf16 contexts: fp16 operands on the tensor cores when d is a multiple of
+ * 64 and D of 256, float32 accumulation, one bf16 rounding of X0). */
+RM_API rm_status rm_set_tokenizer(rm_ctx *ctx, const void *W, const void *bias, int d);
+RM_API rm_status rm_tokenize(rm_ctx *ctx, const void *E, void *X0, int B, void *stream);
+
+/* End-to-end scoring: p[b] = sigmoid(head(pool(stack(tokenize(E[b]))))) with
+ * the head's w (device float32 [D]) and b.  E: device [B][T d] (context dtype);
+ * p: device float32 [B].  Runs rm_tokenize, rm_stack_forward and
+ * rm_head_forward on context-owned buffers (allocated at the first call).
+ * Dense stacks only. */
+RM_API rm_status rm_score(rm_ctx *ctx, const void *E, const float *head_w, float head_b, float *p, int B,
+                          void *stream);
 
 /* Allocation-free variant of rm_block_forward (the paper has no counterpart;
  * this is a deployment aid).  For callers that cannot allocate device memory

@@ -34,14 +34,16 @@ RM_PATH_TCGEN05 = 2
 
 # rm_kernel_kind
 KERNEL_KINDS = ["mix_ln1", "gemm1", "gemm2", "ln2_out", "pool", "rowstats", "moe_route", "moe_gemm1",
-                "moe_gemm2", "misc", "moe_combine", "bwd_recompute", "bwd_dgrad", "bwd_wgrad", "bwd_rows"]
+                "moe_gemm2", "misc", "moe_combine", "bwd_recompute", "bwd_dgrad", "bwd_wgrad", "bwd_rows",
+                "tokenize", "head"]
 RM_K_COUNT = len(KERNEL_KINDS)
 
 EXPORTED = ["rm_create", "rm_destroy", "rm_block_forward", "rm_stack_forward", "rm_stack_forward_host",
             "rm_moe_pffn_forward", "rm_token_mix", "rm_sync_status", "rm_get_info", "rm_profile_enable",
             "rm_profile_read", "rm_debug_wait_timeout", "rm_last_error", "rm_abi_version",
             "rm_block_forward_noalloc", "rm_debug_gelu", "rm_block_backward", "rm_stack_backward",
-            "rm_debug_gelu_grad", "rm_stack_forward_train", "rm_stack_backward_saved"]
+            "rm_debug_gelu_grad", "rm_stack_forward_train", "rm_stack_backward_saved", "rm_head_forward",
+            "rm_set_tokenizer", "rm_tokenize", "rm_score"]
 
 
 class rm_config(ctypes.Structure):
@@ -113,6 +115,10 @@ def load() -> ctypes.CDLL:
         "rm_stack_backward": (st, [vp, vp, vp, vp, ctypes.POINTER(rm_layer_grads), i, vp]),
         "rm_debug_gelu_grad": (st, [vp, vp, ctypes.c_longlong, vp]),
         "rm_stack_forward_train": (st, [vp, vp, vp, i, vp]),
+        "rm_head_forward": (st, [vp, vp, ctypes.c_float, vp, vp, vp, vp, i, i, i, vp]),
+        "rm_set_tokenizer": (st, [vp, vp, vp, i]),
+        "rm_tokenize": (st, [vp, vp, vp, i, vp]),
+        "rm_score": (st, [vp, vp, vp, ctypes.c_float, vp, i, vp]),
         "rm_stack_backward_saved": (st, [vp, vp, vp, ctypes.POINTER(rm_layer_grads), i, vp]),
     }
     for name, (res, args) in sig.items():
@@ -213,6 +219,24 @@ def rm_stack_forward_train(ctx: int, X0: int, pooled: int, B: int, stream: int) 
 def rm_stack_backward_saved(ctx: int, dpooled: int, dX0: int, grads: list | None, B: int, stream: int) -> None:
     arr = (rm_layer_grads * len(grads))(*grads) if grads else None
     check(load().rm_stack_backward_saved(ctx, dpooled, dX0, arr, B, stream), "rm_stack_backward_saved")
+
+
+def rm_head_forward(pooled: int, w: int, b: float, y: int | None, p: int | None, loss: int | None,
+                    dpooled: int | None, B: int, D: int, mean_loss: bool, stream: int) -> None:
+    check(load().rm_head_forward(pooled, w, b, y, p, loss, dpooled, B, D, 1 if mean_loss else 0, stream),
+          "rm_head_forward")
+
+
+def rm_set_tokenizer(ctx: int, W: int, bias: int, d: int) -> None:
+    check(load().rm_set_tokenizer(ctx, W, bias, d), "rm_set_tokenizer")
+
+
+def rm_tokenize(ctx: int, E: int, X0: int, B: int, stream: int) -> None:
+    check(load().rm_tokenize(ctx, E, X0, B, stream), "rm_tokenize")
+
+
+def rm_score(ctx: int, E: int, head_w: int, head_b: float, p: int, B: int, stream: int) -> None:
+    check(load().rm_score(ctx, E, head_w, head_b, p, B, stream), "rm_score")
 
 
 def rm_debug_gelu_grad(u: int, out: int, n: int, stream: int) -> None:

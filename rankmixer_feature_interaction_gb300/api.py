@@ -159,6 +159,27 @@ class RankMixer:
         _lib.rm_stack_backward_saved(self.ctx, _ptr(dpooled), _ptr(dX0), [c for _, c in pairs], B, _stream())
         return dX0, [g for g, _ in pairs]
 
+    # -- tokenization, head and scoring ------------------------------------------------
+    def set_tokenizer(self, W: torch.Tensor, bias: torch.Tensor) -> None:
+        """W [T, d, D], bias [T, D] in the context dtype (token t's projection of its slice)."""
+        self.tok_d = int(W.shape[1])
+        torch.cuda.synchronize(self.device)
+        _lib.rm_set_tokenizer(self.ctx, _ptr(W), _ptr(bias), self.tok_d)
+
+    def tokenize(self, E: torch.Tensor, X0: torch.Tensor | None = None) -> torch.Tensor:
+        """E [B, T d] -> X0 [B, T, D] (context dtype)."""
+        B = E.shape[0]
+        X0 = torch.empty((B, self.T, self.D), dtype=E.dtype, device=E.device) if X0 is None else X0
+        _lib.rm_tokenize(self.ctx, _ptr(E), _ptr(X0), B, _stream())
+        return X0
+
+    def score(self, E: torch.Tensor, head_w: torch.Tensor, head_b: float, p: torch.Tensor | None = None):
+        """E [B, T d] -> p [B] = sigmoid(head(pool(stack(tokenize(E)))))."""
+        B = E.shape[0]
+        p = torch.empty(B, dtype=torch.float32, device=E.device) if p is None else p
+        _lib.rm_score(self.ctx, _ptr(E), _ptr(head_w), float(head_b), _ptr(p), B, _stream())
+        return p
+
     # -- status / profiling --------------------------------------------------------
     def sync_status(self) -> int:
         return _lib.rm_sync_status(self.ctx, _stream())
@@ -181,3 +202,20 @@ def token_mix(X: torch.Tensor, H: int | None = None) -> torch.Tensor:
     dt = _lib.RM_BF16 if X.dtype == torch.bfloat16 else _lib.RM_F32
     _lib.rm_token_mix(_ptr(X), _ptr(Y), B, T, D, H, dt, _stream())
     return Y
+
+
+def head_forward(pooled: torch.Tensor, w: torch.Tensor, b: float, y: torch.Tensor | None = None,
+                 mean_loss: bool = True) -> dict:
+    """The prediction head on the GPU: returns p, and with labels y the per-sample loss
+    and dpooled (the gradient of the batch-mean loss when mean_loss, else of the sum)."""
+    B, D = pooled.shape
+    p = torch.empty(B, dtype=torch.float32, device=pooled.device)
+    out = {"p": p}
+    loss = dp = None
+    if y is not None:
+        loss = torch.empty(B, dtype=torch.float32, device=pooled.device)
+        dp = torch.empty_like(pooled)
+        out.update(loss=loss, dpooled=dp)
+    _lib.rm_head_forward(_ptr(pooled), _ptr(w), float(b), _ptr(y), _ptr(p), _ptr(loss), _ptr(dp), B, D, mean_loss,
+                         _stream())
+    return out

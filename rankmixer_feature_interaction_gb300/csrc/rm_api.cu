@@ -130,6 +130,13 @@ struct rm_ctx {
     float* V = nullptr;          // MoE PFFN output inside the stack
     MoeWorkspace moe_ws;
     TrainWS tw;
+    // feature tokenization ("RankMixer" Eq. 2), set by rm_set_tokenizer
+    int tok_d = 0;
+    void* Wtok = nullptr;        // [T][d][D], fp16 (bf16 contexts) or float
+    float* btok = nullptr;       // [T][D]
+    void* Etok = nullptr;        // fp16 copy of the embeddings [Bcap][T d] (bf16 contexts)
+    void* X0ws = nullptr;        // tokens for rm_score [Bcap][T][D], context dtype
+    float* pooled_ws = nullptr;  // [Bcap][D]
     // host-entry staging: device copies of X0 and pooled, the copy streams and
     // per-chunk events of the pipelined host entry
     void* X0_dev = nullptr;
@@ -182,6 +189,7 @@ void free_ctx(rm_ctx* c) {
         cudaFree(t.part2); cudaFree(t.tmpTD); cudaFree(t.colpart); cudaFree(t.part1);
         cudaFree(t.Xn); cudaFree(t.G0); cudaFree(t.G1); cudaFree(t.pooled);
     }
+    cudaFree(c->Wtok); cudaFree(c->btok); cudaFree(c->Etok); cudaFree(c->X0ws); cudaFree(c->pooled_ws);
     moe_free_workspace(c->moe_ws);
     cudaFree(c->S); cudaFree(c->Hid); cudaFree(c->Z); cudaFree(c->stats); cudaFree(c->rows); cudaFree(c->V);
     cudaFree(c->X0_dev); cudaFree(c->pooled_dev);
@@ -963,6 +971,97 @@ rm_status rm_stack_backward(rm_ctx* c, const void* X0, const float* dpooled, flo
     cudaStream_t s = as_stream(stream);
     if ((st = stack_forward_train_impl(c, X0, c->tw.pooled, B, s)) != RM_OK) return st;
     return stack_backward_saved_impl(c, dpooled, dX0, grads, B, s);
+}
+
+rm_status rm_head_forward(const float* pooled, const float* w, float b, const float* y, float* p, float* loss,
+                          float* dpooled, int B, int D, int mean_loss, void* stream) {
+    if (B < 1 || D < 1) return fail(RM_ERR_INVALID_ARG, "B and D must be positive");
+    if (!pooled || !w) return fail(RM_ERR_INVALID_ARG, "pooled / w is NULL");
+    if (!y && (loss || dpooled)) return fail(RM_ERR_INVALID_ARG, "loss and dpooled need the labels y");
+    if (!p && !loss && !dpooled) return fail(RM_ERR_INVALID_ARG, "no output requested");
+    if (!aligned16(pooled) || !aligned16(w) || (dpooled && !aligned16(dpooled)))
+        return fail(RM_ERR_INVALID_ARG, "pooled, w and dpooled must be 16-byte aligned");
+    if (!std::isfinite(b)) return fail(RM_ERR_INVALID_ARG, "b must be finite");
+    const float gscale = mean_loss ? 1.0f / (float)B : 1.0f;
+    RM_CHECK_CUDA(launch_head(pooled, w, b, y, p, loss, dpooled, gscale, B, D, as_stream(stream)), "head");
+    return RM_OK;
+}
+
+rm_status rm_set_tokenizer(rm_ctx* c, const void* W, const void* bias, int d) {
+    rm_status st;
+    if ((st = check_ctx(c)) != RM_OK) return st;
+    if (!W || !bias) return fail(RM_ERR_INVALID_ARG, "W / bias is NULL");
+    if (d < 1) return fail(RM_ERR_INVALID_ARG, "d must be positive");
+    const rm_config& g = c->cfg;
+    cudaSetDevice(c->device);
+    cudaFree(c->Wtok); cudaFree(c->btok); cudaFree(c->Etok);
+    c->Wtok = nullptr; c->btok = nullptr; c->Etok = nullptr; c->tok_d = 0;
+    const long long n = (long long)g.T * d * g.D;
+    if ((st = dmalloc(c, &c->Wtok, (size_t)n * c->esz, &c->weight_bytes)) != RM_OK) return st;
+    if ((st = dmalloc(c, (void**)&c->btok, (size_t)g.T * g.D * 4, &c->weight_bytes)) != RM_OK) return st;
+    if (c->act == Act::F32)
+        RM_CHECK_CUDA(cudaMemcpy(c->Wtok, W, (size_t)n * 4, cudaMemcpyDeviceToDevice), "copy tokenizer W");
+    else {
+        RM_CHECK_CUDA(launch_bf16_to_f16(W, c->Wtok, n, 0), "copy tokenizer W");
+        if ((st = dmalloc(c, &c->Etok, (size_t)c->Bcap * g.T * d * 2, &c->ws_bytes)) != RM_OK) return st;
+    }
+    RM_CHECK_CUDA(launch_to_f32(c->act, bias, c->btok, (size_t)g.T * g.D, 0), "copy tokenizer bias");
+    RM_CHECK_CUDA(cudaDeviceSynchronize(), "rm_set_tokenizer");
+    c->tok_d = d;
+    return RM_OK;
+}
+
+namespace {
+rm_status tokenize_impl(rm_ctx* c, const void* E, void* X0, int B, cudaStream_t s) {
+    const rm_config& g = c->cfg;
+    const int T = g.T, D = g.D, d = c->tok_d;
+    ProfScope ps(c, RM_K_TOKENIZE, s);
+    const void* Eop = E;
+    if (c->act != Act::F32) {
+        RM_CHECK_CUDA(launch_bf16_to_f16(E, c->Etok, (long long)B * T * d, s), "embeddings to fp16");
+        Eop = c->Etok;
+    }
+    TrainGemm m = train_gemm_base(c);
+    m.M = B; m.N = D; m.K = d; m.m_valid = B;
+    m.a = {Eop, d, B, d, false, (long long)T * d};        // slice t of row b: E[b][t d .. t d + d)
+    m.b = {c->Wtok, D, d, (long long)d * D, true};        // W_t [d][D]
+    m.c_gpitch = D; m.c_ld = (long long)T * D;            // X0[b][t][:]
+    m.c0 = X0; m.bias = c->btok;
+    return run_train_gemm(c, TE_BIAS_IO, m, nullptr, "tokenize", s);
+}
+}  // namespace
+
+rm_status rm_tokenize(rm_ctx* c, const void* E, void* X0, int B, void* stream) {
+    rm_status st;
+    if ((st = check_ctx(c)) != RM_OK) return st;
+    if (c->tok_d == 0) return fail(RM_ERR_INVALID_ARG, "no tokenizer: call rm_set_tokenizer first");
+    if ((st = check_batch(c, B)) != RM_OK) return st;
+    if (!E || !X0) return fail(RM_ERR_INVALID_ARG, "E / X0 is NULL");
+    if (!aligned16(E) || !aligned16(X0)) return fail(RM_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+    cudaSetDevice(c->device);
+    return tokenize_impl(c, E, X0, B, as_stream(stream));
+}
+
+rm_status rm_score(rm_ctx* c, const void* E, const float* head_w, float head_b, float* p, int B, void* stream) {
+    rm_status st;
+    if ((st = check_ctx(c)) != RM_OK) return st;
+    if (c->tok_d == 0) return fail(RM_ERR_INVALID_ARG, "no tokenizer: call rm_set_tokenizer first");
+    if ((st = check_batch(c, B)) != RM_OK) return st;
+    if (!E || !head_w || !p) return fail(RM_ERR_INVALID_ARG, "E / head_w / p is NULL");
+    if (!aligned16(E) || !aligned16(head_w)) return fail(RM_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+    if (c->cfg.moe_layer_mask != 0) return fail(RM_ERR_UNSUPPORTED, "rm_score runs dense stacks");
+    cudaSetDevice(c->device);
+    const rm_config& g = c->cfg;
+    if (!c->X0ws) {
+        if ((st = dmalloc(c, &c->X0ws, (size_t)c->Bcap * g.T * g.D * c->esz, &c->ws_bytes)) != RM_OK) return st;
+        if ((st = dmalloc(c, (void**)&c->pooled_ws, (size_t)c->Bcap * g.D * 4, &c->ws_bytes)) != RM_OK) return st;
+    }
+    cudaStream_t s = as_stream(stream);
+    if ((st = tokenize_impl(c, E, c->X0ws, B, s)) != RM_OK) return st;
+    if ((st = stack_device(c, c->X0ws, c->pooled_ws, nullptr, B, s)) != RM_OK) return st;
+    ProfScope ps(c, RM_K_HEAD, s);
+    RM_CHECK_CUDA(launch_head(c->pooled_ws, head_w, head_b, nullptr, p, nullptr, nullptr, 1.0f, B, g.D, s), "head");
+    return RM_OK;
 }
 
 rm_status rm_debug_gelu_grad(const float* u, float* out, long long n, void* stream) {

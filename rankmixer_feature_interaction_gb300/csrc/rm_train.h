@@ -25,6 +25,7 @@ struct TOperand {
     int outer;
     long long gpitch;
     bool mn;
+    long long ld = 0;       // elements between consecutive outer rows (0: inner)
 };
 
 // Operand precision.  float32 contexts run every product in float32.  bf16
@@ -37,7 +38,8 @@ struct TOperand {
 // scaled operand multiply their accumulator by inv_scale[g] = 1 / s_g (exact).
 //
 // Epilogues.  Row m, column n of group g of C, and of the row-aligned inputs
-// R / Gp, sit at g * c_gpitch + m * N + n; rows m >= m_valid are not stored.
+// R / Gp, sit at g * c_gpitch + m * c_ld + n (c_ld = N unless set); rows
+// m >= m_valid are not stored.
 // "acc" below is the accumulator times inv_scale[g] where inv_scale is given.
 enum TrainEpi {
     TE_GELU2 = 1,    // C0 = Gelu(acc + bias)  (operand type), C1 = Gelu'(acc + bias)  (aux type)
@@ -46,6 +48,7 @@ enum TrainEpi {
                      //      type), plus column partial sums of acc * Gp
     TE_DRESID = 4,   // C0 = acc + R           (float; R float)
     TE_F32 = 5,      // C0 = acc               (float)
+    TE_BIAS_IO = 6,  // C0 = acc + bias        (the context's caller dtype: bf16 or float)
 };
 
 struct TrainGemm {
@@ -53,6 +56,7 @@ struct TrainGemm {
     int m_valid;
     TOperand a, b;
     long long c_gpitch;
+    long long c_ld;         // elements between consecutive rows of C (0: N)
     void* c0;
     void* c1;
     const void* r;          // TE_RESID / TE_DRESID: residual rows; TE_DGELU: Gp
@@ -130,6 +134,11 @@ cudaError_t launch_bf16_to_f16(const void* in, void* out, long long n, cudaStrea
 
 // G[b][t][:] = dpooled[b][:] / T  (the mean pool's backward).
 cudaError_t launch_pool_backward(const float* dpooled, float* G, int B, int T, int D, cudaStream_t s);
+
+// Prediction head: p[i] = sigmoid(pooled[i] . w + b); with labels y also the
+// per-sample loss and dO[i] = gscale (p[i] - y[i]) w (any output may be null).
+cudaError_t launch_head(const float* pooled, const float* w, float b, const float* y, float* p, float* loss, float* dO,
+                        float gscale, int B, int D, cudaStream_t s);
 
 // Test hook: out[2i] = Gelu(u[i]), out[2i+1] = Gelu'(u[i]) as the backward epilogues compute them.
 cudaError_t launch_debug_gelu_grad(const float* u, float* out, long long n, cudaStream_t s);

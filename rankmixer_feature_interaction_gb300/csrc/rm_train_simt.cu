@@ -20,12 +20,13 @@ template <typename Top>
 __device__ __forceinline__ float op_at(const TOperand& o, int g, int r, int k, int r_lim, int k_lim) {
     if (r >= r_lim || k >= k_lim) return 0.f;
     const Top* p = reinterpret_cast<const Top*>(o.ptr) + (size_t)g * (size_t)o.gpitch;
+    const size_t ld = o.ld ? (size_t)o.ld : (size_t)o.inner;
     if (o.mn) {
         if (k >= o.outer || r >= o.inner) return 0.f;
-        return to_f32(p[(size_t)k * o.inner + r]);
+        return to_f32(p[(size_t)k * ld + r]);
     }
     if (r >= o.outer || k >= o.inner) return 0.f;
-    return to_f32(p[(size_t)r * o.inner + k]);
+    return to_f32(p[(size_t)r * ld + k]);
 }
 
 template <typename Top, typename Taux, int EPI>
@@ -68,7 +69,7 @@ train_gemm_simt_kernel(const TrainGemm g) {
         for (int j = 0; j < 4; ++j) {
             const int n = n0 + tx + 16 * j;
             if (n >= g.N) continue;
-            const size_t off = (size_t)grp * (size_t)g.c_gpitch + (size_t)m * g.N + n;
+            const size_t off = (size_t)grp * (size_t)g.c_gpitch + (size_t)m * (g.c_ld ? (size_t)g.c_ld : (size_t)g.N) + n;
             const float raw = acc[i][j];
             const float v = raw * inv_s;
             if (EPI == TE_GELU2) {
@@ -83,6 +84,12 @@ train_gemm_simt_kernel(const TrainGemm g) {
                 reinterpret_cast<Top*>(g.c0)[off] = from_f32<Top>(raw * gp);
             } else if (EPI == TE_DRESID) {
                 reinterpret_cast<float*>(g.c0)[off] = v + reinterpret_cast<const float*>(g.r)[off];
+            } else if (EPI == TE_BIAS_IO) {      // the caller dtype: float, or bf16 for fp16-operand contexts
+                const float o = v + g.bias[(size_t)grp * g.N + n];
+                if constexpr (std::is_same_v<Top, float>)
+                    reinterpret_cast<float*>(g.c0)[off] = o;
+                else
+                    reinterpret_cast<__nv_bfloat16*>(g.c0)[off] = __float2bfloat16_rn(o);
             } else {
                 reinterpret_cast<float*>(g.c0)[off] = v;
             }
@@ -97,7 +104,7 @@ __global__ void colsum_kernel(const T* __restrict__ C, long long gpitch, int row
     const int grp = blockIdx.y;
     const int n = blockIdx.x * blockDim.x + threadIdx.x;
     if (n >= N) return;
-    const T* p = C + (size_t)grp * (size_t)gpitch + n;
+    const T* p = C + (size_t)grp * (size_t)gpitch + n;   // rows N apart (TE_DGELU outputs are dense)
     const float inv_s = inv_scale ? inv_scale[grp] : 1.0f;
     float s = 0.f;
     for (int m = 0; m < rows; ++m) s = fmaf(to_f32(p[(size_t)m * N]), inv_s, s);
@@ -113,6 +120,7 @@ cudaError_t run_simt(int epi, const TrainGemm& g, cudaStream_t s) {
         case TE_DGELU: train_gemm_simt_kernel<Top, Taux, TE_DGELU><<<grid, 256, 0, s>>>(g); break;
         case TE_DRESID: train_gemm_simt_kernel<Top, Taux, TE_DRESID><<<grid, 256, 0, s>>>(g); break;
         case TE_F32: train_gemm_simt_kernel<Top, Taux, TE_F32><<<grid, 256, 0, s>>>(g); break;
+        case TE_BIAS_IO: train_gemm_simt_kernel<Top, Taux, TE_BIAS_IO><<<grid, 256, 0, s>>>(g); break;
         default: return cudaErrorInvalidValue;
     }
     cudaError_t e = cudaGetLastError();

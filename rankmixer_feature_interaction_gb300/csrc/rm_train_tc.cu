@@ -64,6 +64,7 @@ struct KArgs {
     int m_tiles, n_tiles;
     long long tiles;
     long long c_gpitch;
+    long long c_ld;
     void* c0;
     void* c1;
     const void* r;
@@ -172,7 +173,7 @@ __device__ __forceinline__ float column_sums32(float (&v)[32], int lane) {
 template <int EPI>
 __device__ __forceinline__ void epilogue(const KArgs& a, int g, int m, bool valid, uint32_t tbase, int n0, int lane,
                                          int quad, int mb) {
-    const size_t row = (size_t)g * (size_t)a.c_gpitch + (size_t)m * (size_t)a.N + (size_t)n0;
+    const size_t row = (size_t)g * (size_t)a.c_gpitch + (size_t)m * (size_t)a.c_ld + (size_t)n0;
     const float inv_s = a.inv_scale ? __ldg(a.inv_scale + g) : 1.0f;
     constexpr int NC = EpiCfg<EPI>::COLS / 32;
     // chunk c + 1 loads from TMEM while chunk c is processed (two register sets)
@@ -252,6 +253,20 @@ __device__ __forceinline__ void epilogue(const KArgs& a, int g, int m, bool vali
                     d4[j] = make_float4(fmaf(v[4 * j], inv_s, rr.x), fmaf(v[4 * j + 1], inv_s, rr.y),
                                         fmaf(v[4 * j + 2], inv_s, rr.z), fmaf(v[4 * j + 3], inv_s, rr.w));
                 }
+            }
+        } else if (EPI == TE_BIAS_IO) {       // bf16 output (tensor-core path: bf16 contexts)
+            if (valid) {
+                const float4* b4 = reinterpret_cast<const float4*>(a.bias + (size_t)g * a.N + n0 + 32 * c);
+                uint32_t p[16];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float4 bb = __ldg(b4 + j);
+                    const __nv_bfloat162 h0 = __floats2bfloat162_rn(v[4 * j] + bb.x, v[4 * j + 1] + bb.y);
+                    const __nv_bfloat162 h1 = __floats2bfloat162_rn(v[4 * j + 2] + bb.z, v[4 * j + 3] + bb.w);
+                    p[2 * j] = *reinterpret_cast<const uint32_t*>(&h0);
+                    p[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&h1);
+                }
+                store16x32(reinterpret_cast<__nv_bfloat16*>(a.c0) + off, p);
             }
         } else {   // TE_F32
             if (valid) {
@@ -449,7 +464,7 @@ bool get_encoder() {
 bool make_map(CUtensorMap* m, const TOperand& op, int G, int box_outer) {
     if (!get_encoder()) return false;
     cuuint64_t dims[3] = {(cuuint64_t)op.inner, (cuuint64_t)op.outer, (cuuint64_t)G};
-    cuuint64_t strides[2] = {(cuuint64_t)op.inner * 2, (cuuint64_t)op.gpitch * 2};
+    cuuint64_t strides[2] = {(cuuint64_t)(op.ld ? op.ld : op.inner) * 2, (cuuint64_t)op.gpitch * 2};
     cuuint32_t box[3] = {64u, (cuuint32_t)box_outer, 1u};
     cuuint32_t estr[3] = {1, 1, 1};
     return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(op.ptr), dims, strides, box, estr,
@@ -487,6 +502,8 @@ bool train_tc_supported(const TrainGemm& g) {
     if (g.a.mn && (g.a.inner != g.M || g.M % ttc::BM != 0)) return false;
     if (g.b.mn && (g.b.inner != g.N)) return false;
     if (g.a.gpitch % 8 != 0 || g.b.gpitch % 8 != 0) return false;
+    if (g.a.ld % 8 != 0 || g.b.ld % 8 != 0) return false;         // 16-byte row pitches for TMA
+    if ((g.c_ld ? g.c_ld : g.N) % 8 != 0 || g.c_gpitch % 8 != 0) return false;   // 16-byte vector stores
     return true;
 }
 
@@ -502,6 +519,7 @@ cudaError_t launch_train_gemm_tc(int epi, const TrainGemm& g, int num_sms, cudaS
     ka.n_tiles = g.N / ttc::BN;
     ka.tiles = (long long)g.G * ka.m_tiles * ka.n_tiles;
     ka.c_gpitch = g.c_gpitch;
+    ka.c_ld = g.c_ld ? g.c_ld : g.N;
     ka.c0 = g.c0;
     ka.c1 = g.c1;
     ka.r = g.r;
@@ -528,6 +546,9 @@ cudaError_t launch_train_gemm_tc(int epi, const TrainGemm& g, int num_sms, cudaS
             break;
         case TE_F32:
             if (amn && bmn) return ttc::run<TE_F32, true, true>(g, ka, num_sms, s);
+            break;
+        case TE_BIAS_IO:
+            if (!amn && bmn) return ttc::run<TE_BIAS_IO, false, true>(g, ka, num_sms, s);
             break;
         default: break;
     }
