@@ -64,6 +64,7 @@ def _load():
             lib.oracle_head.argtypes = [dp, dp, ctypes.c_double, dp, dp, dp, dp, dp, dp, i, i]
             lib.oracle_tokenize.argtypes = [dp, dp, dp, dp, i, i, i, i]
             lib.oracle_tokenize_backward.argtypes = [dp] * 6 + [i, i, i, i]
+            lib.oracle_moe_pffn_train.argtypes = [dp] * 14 + [i, i, i, i, i]
             lib.oracle_num_threads.restype = ctypes.c_int
             lib.oracle_set_num_threads.argtypes = [i]
             _lib = lib
@@ -288,3 +289,21 @@ def tokenize_backward(E, W, dX0):
     dE, dW, db = np.empty_like(E), np.empty_like(W), np.empty((T, D))
     _load().oracle_tokenize_backward(_p(E), _p(W), _p(dX0), _p(dE), _p(dW), _p(db), B, T, d, D)
     return dE, dW, db
+
+
+def moe_pffn_train(S, Wt, bt, Wi, bi, eW1, eb1, eW2, eb2) -> dict:
+    """Training forward of the Sparse-MoE PFFN with dense-training / sparse-inference routers
+    ("RankMixer" section 3.4 Eq. 10-11; "6.4 Rankmixer: 硬件效率优化" section 6.4.4): V from the
+    training router's gates G_train; the inference router's gates G_infer, the per-sample
+    regulariser lreg = sum over tokens and experts of G_infer, and the per-expert activation
+    A = sum over samples and tokens of G_infer."""
+    S, Wt, bt, Wi, bi, eW1, eb1, eW2, eb2 = map(_f64, (S, Wt, bt, Wi, bi, eW1, eb1, eW2, eb2))
+    B, T, D = S.shape
+    E = Wt.shape[-1]
+    Fe = eW1.shape[-1]
+    out = {"V": np.empty_like(S), "G_train": np.empty((B, T, E)), "G_infer": np.empty((B, T, E)),
+           "lreg": np.empty(B), "A": np.empty(E)}
+    _load().oracle_moe_pffn_train(_p(S), _p(Wt), _p(bt), _p(Wi), _p(bi), _p(eW1), _p(eb1), _p(eW2), _p(eb2),
+                                  _p(out["V"]), _p(out["G_train"]), _p(out["G_infer"]), _p(out["lreg"]),
+                                  _p(out["A"]), B, T, D, E, Fe)
+    return out

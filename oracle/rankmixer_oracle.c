@@ -10,6 +10,7 @@
  *   [RM]  "RankMixer: Scaling Up Ranking Models in Industrial Recommenders"
  *         (Zhu et al., ByteDance), section 3.1 Eq. 1, section 3.3.1 Eq. 3-5,
  *         section 3.3.2 Eq. 6-9, section 3.4 Eq. 10, section 3.5 Eq. 12.
+ *   [TU]  "6.4 Rankmixer: 硬件效率优化", section 6.4.4 (DTSI-MoE routers).
  *   [WT]  "RankMixer 详解（1）：特征分组与完整计算流程", section 3.1 (the
  *         element map of TokenMixing), section 3.3 (LayerNorm definition),
  *         section 4.1 (GELU = u*Phi(u), row-vector FFN), section 5.1 (mean
@@ -577,6 +578,42 @@ ORACLE_API void oracle_tokenize_backward(const double *E, const double *W, const
                 de[i] = acc;
             }
         }
+}
+
+/* ------------------------------------------------------------------ */
+/* Training forward of the Sparse-MoE PFFN, dense-training / sparse-    */
+/* inference ([RM] section 3.4 Eq. 10-11; [TU] section 6.4.4 Eq. 6.4.7):*/
+/* two linear routers per token, h_train and h_infer; the forward uses  */
+/*   G_train = ReLU(s Wt_t + bt_t),  v = sum_e G_train[e] FFN_{t,e}(s), */
+/* and alongside it G_infer = ReLU(s Wi_t + bi_t), whose sum is the     */
+/* sparsity regulariser: L_reg[b] = sum_{t,e} G_infer[b,t,e] per sample */
+/* (Eq. 11 sums over tokens i and experts j) and the per-expert         */
+/* activation A[e] = sum_{b,t} G_infer[b,t,e] over the batch.           */
+/* G_train, G_infer [B][T][E]; lreg [B]; A [E].                         */
+/* ------------------------------------------------------------------ */
+ORACLE_API void oracle_moe_pffn_train(const double *S, const double *Wt, const double *bt,
+                                      const double *Wi, const double *bi,
+                                      const double *eW1, const double *eb1, const double *eW2, const double *eb2,
+                                      double *V, double *Gtrain, double *Ginfer, double *lreg, double *A,
+                                      int B, int T, int D, int E, int Fe)
+{
+    oracle_moe_pffn(S, Wt, bt, eW1, eb1, eW2, eb2, V, Gtrain, B, T, D, E, Fe);
+    for (int e = 0; e < E; ++e) A[e] = 0.0;
+    for (int b = 0; b < B; ++b) {
+        double l = 0.0;
+        for (int t = 0; t < T; ++t) {
+            const double *s = S + ((size_t)b * T + t) * D;
+            for (int e = 0; e < E; ++e) {
+                double h = bi[(size_t)t * E + e];
+                for (int i = 0; i < D; ++i) h += s[i] * Wi[((size_t)t * D + i) * E + e];
+                const double g = h > 0.0 ? h : 0.0;
+                Ginfer[((size_t)b * T + t) * E + e] = g;
+                l += g;
+                A[e] += g;
+            }
+        }
+        lreg[b] = l;
+    }
 }
 
 ORACLE_API int oracle_num_threads(void)

@@ -348,3 +348,42 @@ def test_moe_single_open_expert_is_a_dense_pffn():
     W2 = rng.standard_normal((T, 1, Fe, D)); b2 = rng.standard_normal((T, 1, D))
     V = oracle.moe_pffn(S, np.zeros((T, D, 1)), np.ones((T, 1)), W1, b1, W2, b2)
     np.testing.assert_allclose(V, oracle.pffn(S, W1[:, 0], b1[:, 0], W2[:, 0], b2[:, 0]), atol=1e-12)
+
+
+# ----------------------------------------------------------------------------
+# DTSI-MoE training forward ("RankMixer" section 3.4 Eq. 10-11; "6.4 Rankmixer:
+# 硬件效率优化" section 6.4.4): V from h_train's gates, the regulariser from
+# h_infer's.  Pinned against the (separately pinned) inference MoE oracle run
+# with each router, and against the definition of L_reg and A_j as sums of the
+# inference gates that oracle returns.
+# ----------------------------------------------------------------------------
+
+def _moe_case(B, T, D, E, Fe, seed):
+    r = np.random.default_rng(seed)
+    S = r.standard_normal((B, T, D))
+    Wt = r.standard_normal((T, D, E)) / np.sqrt(D)
+    Wi = r.standard_normal((T, D, E)) / np.sqrt(D)
+    bt = 0.2 * r.standard_normal((T, E))
+    bi = -0.5 + 0.1 * r.standard_normal((T, E))
+    eW1 = r.standard_normal((T, E, D, Fe)) / np.sqrt(D)
+    eb1 = 0.1 * r.standard_normal((T, E, Fe))
+    eW2 = r.standard_normal((T, E, Fe, D)) / np.sqrt(Fe)
+    eb2 = 0.1 * r.standard_normal((T, E, D))
+    return S, Wt, bt, Wi, bi, eW1, eb1, eW2, eb2
+
+
+def test_moe_train_forward_uses_the_training_router_and_regularises_the_inference_one():
+    S, Wt, bt, Wi, bi, eW1, eb1, eW2, eb2 = _moe_case(5, 3, 8, 4, 6, 71)
+    r = oracle.moe_pffn_train(S, Wt, bt, Wi, bi, eW1, eb1, eW2, eb2)
+    V_train, G_train = oracle.moe_pffn(S, Wt, bt, eW1, eb1, eW2, eb2, return_gates=True)
+    V_infer, G_infer = oracle.moe_pffn(S, Wi, bi, eW1, eb1, eW2, eb2, return_gates=True)
+    np.testing.assert_array_equal(r["V"], V_train)
+    np.testing.assert_array_equal(r["G_train"], G_train)
+    np.testing.assert_allclose(r["G_infer"], G_infer, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(r["lreg"], G_infer.sum(axis=(1, 2)), rtol=1e-14)
+    np.testing.assert_allclose(r["A"], G_infer.sum(axis=(0, 1)), rtol=1e-14)
+    assert not np.allclose(r["V"], V_infer)            # the forward does not follow h_infer
+    # the regulariser is a sum of ReLU outputs: zero exactly when every inference gate is closed
+    z = oracle.moe_pffn_train(S, Wt, bt, Wi, bi - 100.0, eW1, eb1, eW2, eb2)
+    assert np.all(z["lreg"] == 0.0) and np.all(z["A"] == 0.0)
+    np.testing.assert_array_equal(z["V"], r["V"])
