@@ -39,6 +39,9 @@ L2_BYTES = 129 * 1024 * 1024
 # by (config, batch per GPU, layers, kernel kind), with the SHA-256 of the
 # kernel sources the capture ran on.  Reported only while those sources are
 # unchanged; otherwise the traffic is unknown (null).
+# embedding coordinates per token for --pass score (the tokenizer's slice length d)
+SCORE_SLICE = {"rankmixer_1b": 512, "rankmixer_100m": 256}
+
 KERNEL_SOURCES = ("rankmixer_feature_interaction_gb300/csrc/rm_gemm_tc.cu",
                   "rankmixer_feature_interaction_gb300/csrc/rm_common.cuh",
                   "rankmixer_feature_interaction_gb300/csrc/rm_internal.h")
@@ -185,7 +188,7 @@ def run_ours(args):
     import torch
     import torch.distributed as dist
 
-    from rankmixer_feature_interaction_gb300 import synth
+    from rankmixer_feature_interaction_gb300 import _lib, synth
     from rankmixer_feature_interaction_gb300.api import RankMixer
 
     world, rank, local = dist_env()
@@ -193,42 +196,67 @@ def run_ours(args):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
 
     c = dict(synth.CONFIGS[args.config])
     B = args.batch or c["B"]
     T, D, k = c["T"], c["D"], c["k"]
     moe = args.config == "moe_1b"
     train = args.pass_ == "train"
-    if moe and train:
-        raise SystemExit("--pass train covers the dense stack (rankmixer_1b / rankmixer_100m)")
+    score = args.pass_ == "score"
+    if moe and score:
+        raise SystemExit("--pass score runs the dense stack (rankmixer_1b / rankmixer_100m)")
     L = args.layers or c["L"]
     E, Fe = c.get("E", 0), c.get("Fe", 0)
     # weak scaling: the job's batch is world * B samples, rank r owns shard r
     start, stop = shard_batch(world * B, world, rank)
     layers = synth.make_stack(T, D, k, L, 4242, "bf16", dev, E=E, Fe=Fe, active=c.get("active", 2.0))
-    m = RankMixer(T, D, k, layers, dtype="bf16", max_batch=B, n_experts=E, expert_hidden=Fe, training=train)
+    if moe and train:    # the dense-training router: about 6 of 8 experts open
+        layers[0].update(synth.make_train_router(T, D, E, 4243, "bf16", dev, active=0.75 * E))
+    m = RankMixer(T, D, k, layers, dtype="bf16", max_batch=B, n_experts=E, expert_hidden=Fe,
+                  training=train and not moe)
     del layers
     torch.cuda.empty_cache()
     X0 = synth.make_input_shard(world * B, start, stop, T, D, 20260101, "bf16", dev)
     pooled = torch.empty((B, D), dtype=torch.float32, device=dev)
     S_in = X0  # MoE PFFN input (an LN1 output in the model; same distribution class for timing)
     V = torch.empty((B, T, D), dtype=torch.float32, device=dev) if moe else None
-    if train:
+    if train and not moe:
         # the gradient of a batch-mean loss at the pooled output
         dP = synth.make_output_grad((B, D), 20260102 + rank, scale=1.0 / (B * world), device=dev)
         dX0 = torch.empty((B, T, D), dtype=torch.float32, device=dev)
         grads = m.alloc_grads(dev)
+    if moe and train:
+        Gt = torch.empty((B, T, E), dtype=torch.float32, device=dev)
+        Gi = torch.empty_like(Gt)
+        lreg = torch.empty(B, dtype=torch.float32, device=dev)
+        Aexp = torch.empty(E, dtype=torch.float32, device=dev)
+    d_tok = SCORE_SLICE[args.config] if score else 0
+    if score:
+        # tokenizer (token t projects its d-coordinate slice) and head, random-init; embeddings N(0, 1)
+        gtok = torch.Generator(device=dev).manual_seed(4244)
+        Wtok = (torch.randn((T, d_tok, D), generator=gtok, device=dev) / d_tok ** 0.5).to(torch.bfloat16)
+        btok = (0.1 * torch.randn((T, D), generator=gtok, device=dev)).to(torch.bfloat16)
+        m.set_tokenizer(Wtok, btok)
+        del Wtok, btok
+        Emb = synth.make_input_shard(world * B, start, stop, T, d_tok, 20260103, "bf16", dev).reshape(B, T * d_tok)
+        hw = torch.randn(D, generator=gtok, device=dev) / D ** 0.5
+        p_out = torch.empty(B, dtype=torch.float32, device=dev)
 
     def step():
-        if moe:
+        if moe and train:
+            _lib.rm_moe_pffn_forward_train(m.ctx, 0, S_in.data_ptr(), V.data_ptr(), Gt.data_ptr(), Gi.data_ptr(),
+                                           lreg.data_ptr(), Aexp.data_ptr(), B, stream.cuda_stream)
+        elif moe:
             m.moe_pffn_forward(0, S_in, V)
+        elif score:
+            m.score(Emb, hw, 0.1, p_out)
         elif train:
             m.stack_forward_train(X0, pooled)
             m.stack_backward_saved(dP, dX0, grads)
         else:
             m.stack_forward(X0, pooled)
 
-    stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -267,7 +295,28 @@ def run_ours(args):
 
     # ---- e2e through the host-buffer entry point -----------------------------------
     e2e = None
-    if train:
+    if score:
+        Eh = Emb.cpu().pin_memory()
+        ph_ = torch.empty(B, dtype=torch.float32).pin_memory()
+
+        def step_host():
+            Emb.copy_(Eh, non_blocking=True)
+            m.score(Emb, hw, 0.1, p_out)
+            ph_.copy_(p_out, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        for _ in range(2):
+            step_host()
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            step_host()
+        t1 = time.perf_counter()
+        e2e = {"value": round(job_rate(B, world, args.steps, max_over_ranks(t1 - t0, dev)), 2), "unit": "samples/s",
+               "h2d_bytes_per_step": int(Eh.numel() * Eh.element_size()),
+               "d2h_bytes_per_step": int(ph_.numel() * ph_.element_size())}
+    elif train and not moe:
         # host X0 and pooled-output gradient in, pooled output back: copies on the
         # compute stream around the same forward + backward calls
         Xh = X0.cpu().pin_memory()
@@ -325,11 +374,14 @@ def run_ours(args):
     if moe:
         # algorithmic flops: every open (sample, token, expert) runs 2 D Fe flops in each
         # expert layer, each layer one launch over all (token, expert) groups
-        _, G = m.moe_pffn_forward(0, S_in, V, return_gates=True)
-        active = int((G > 0).sum().item())
+        if train:
+            active = int((Gt > 0).sum().item())
+        else:
+            _, G = m.moe_pffn_forward(0, S_in, V, return_gates=True)
+            active = int((G > 0).sum().item())
         per_layer = 2.0 * active * D * Fe
         flops_launch = per_layer
-        flops_step = 2 * per_layer + 2.0 * B * T * D * E      # + router
+        flops_step = 2 * per_layer + 2.0 * B * T * D * E * (2 if train else 1)      # + router(s)
     else:
         flops_launch = scope_flops[dom]
     roofline = None
@@ -341,19 +393,22 @@ def run_ours(args):
                  "bwd_recompute": "train_gemm_forward_tcgen05 (x2 per scope)"}.get(dom, f"pffn_{dom}_tcgen05")
         roofline = {"kernel": kname, "bound": "tensor", "achieved": round(achieved, 1),
                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                    "traffic": captured_traffic(args.config, B, L, dom),
+                    "traffic": captured_traffic(args.config, B, L, dom) if not (moe and train) else None,
                     "peak_source": f"{peak_src} bf16_tflops_sustained",
                     "avg_launch_ms": round(avg_ms, 4)}
     flops_executed = None
     if not moe:
         flops_step = 4.0 * k * L * T * D * D * B
+        if score:
+            flops_step += 2.0 * T * d_tok * D * B + 2.0 * D * B      # tokenizer + head
         if train:
             # forward + backward = 3 x the forward GEMM flops (the training forward keeps the
             # activations, so no GEMM runs twice)
             flops_executed = 3.0 * flops_step
             flops_step = 3.0 * flops_step
     gpu_launches = int(sum(v[0] for kk, v in kstats.items() if kk != "misc"))
-    what = "train step: fwd + bwd" if train else "fwd"
+    what = ("DTSI train forward" if moe else "train step: fwd + bwd") if train else (
+        "score: tokenize + fwd + head" if score else "fwd")
 
     out = {
         "metric": f"samples/s (RankMixer-1B-shape block stack {what})" if args.config == "rankmixer_1b"
@@ -369,7 +424,8 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) inputs, N(0,1/fan_in) weights; random-init)",
-        "config": {"workload": f"{args.config} B={B} T={T} D={D} k={k} L={L}" + (f" E={E} Fe={Fe}" if moe else ""),
+        "config": {"workload": f"{args.config} B={B} T={T} D={D} k={k} L={L}" + (f" E={E} Fe={Fe}" if moe else "")
+                   + (f" d={d_tok}" if score else ""),
                    "batch_per_gpu": B, "global_batch": B * world, "parallelism": f"replicas x{world} (batch sharded)",
                    "l2": "inputs larger than L2 (X0 %.0f MB, weights %.0f MB > 129 MB)" % (
                        X0.numel() * 2 / 1e6, m.info.weight_bytes / 1e6)},
@@ -386,7 +442,7 @@ def run_ours(args):
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(args.config, B, args.cpu_seconds, train=train)
+        out["cpu_baseline"] = cpu_baseline(args.config, B, args.cpu_seconds, train=train, score=score)
     if rank == 0:
         print(json.dumps(out), flush=True)
     m.close()
@@ -397,7 +453,8 @@ def run_ours(args):
 # ----------------------------------------------------------------------------
 # CPU oracle baseline (bounded sample)
 # ----------------------------------------------------------------------------
-def cpu_baseline(config: str, B_full: int, seconds: float, n_steps: int = 1, train: bool = False) -> dict:
+def cpu_baseline(config: str, B_full: int, seconds: float, n_steps: int = 1, train: bool = False,
+                 score: bool = False) -> dict:
     import numpy as np
 
     import oracle
@@ -408,14 +465,29 @@ def cpu_baseline(config: str, B_full: int, seconds: float, n_steps: int = 1, tra
     moe = config == "moe_1b"
     layers = synth.to_f64(synth.make_stack(T, D, k, L, 4242, "bf16", "cpu", E=c.get("E", 0), Fe=c.get("Fe", 0),
                                            active=c.get("active", 2.0)))
+    if moe and train:
+        layers[0].update(synth.to_f64(synth.make_train_router(T, D, c["E"], 4243, "bf16", "cpu", active=0.75 * c["E"])))
+    d_tok = SCORE_SLICE.get(config, 0)
+    if score:
+        r = np.random.default_rng(4244)
+        Wtok = r.standard_normal((T, d_tok, D)) / d_tok ** 0.5
+        btok = 0.1 * r.standard_normal((T, D))
+        hw = r.standard_normal(D) / D ** 0.5
     cores = oracle.num_threads()
 
     def run(nb):
         X = synth.to_f64(synth.make_input(nb, T, D, 99, "bf16", "cpu"))
         t0 = time.perf_counter()
-        if moe:
+        if moe and train:
+            p = layers[0]
+            oracle.moe_pffn_train(X, p["Wg_train"], p["bg_train"], p["Wg"], p["bg"], p["eW1"], p["eb1"], p["eW2"],
+                                  p["eb2"])
+        elif moe:
             p = layers[0]
             oracle.moe_pffn(X, p["Wg"], p["bg"], p["eW1"], p["eb1"], p["eW2"], p["eb2"])
+        elif score:
+            E_ = np.random.default_rng(99).standard_normal((nb, T * d_tok))
+            oracle.head(oracle.stack_forward(oracle.tokenize(E_, Wtok, btok), layers), hw, 0.1)
         elif train:
             oracle.stack_forward(X, layers)
             oracle.stack_backward(X, np.full((nb, D), 1.0 / nb), layers)
@@ -450,12 +522,15 @@ def run_reference(args):
     # each step is a bounded sample; the whole run is kept to a few minutes
     per_step_s = min(args.cpu_seconds, 150.0 / (steps + args.warmup))
     train = args.pass_ == "train"
-    cb = cpu_baseline(args.config, B, per_step_s, n_steps=steps, train=train)
-    what = "train step: fwd + bwd" if train else "fwd"
+    score = args.pass_ == "score"
+    moe = args.config == "moe_1b"
+    cb = cpu_baseline(args.config, B, per_step_s, n_steps=steps, train=train, score=score)
+    what = ("DTSI train forward" if moe else "train step: fwd + bwd") if train else (
+        "score: tokenize + fwd + head" if score else "fwd")
     out = {
         "impl": "reference",
         "metric": f"samples/s (RankMixer-1B-shape block stack {what})" if args.config == "rankmixer_1b"
-        else f"samples/s ({args.config}{' ' + what if train else ''})",
+        else f"samples/s ({args.config}{' ' + what if (train or score) else ''})",
         "value": cb["value"], "unit": "samples/s", "n_gpus": world, "steps": steps, "warmup": args.warmup,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)",
@@ -477,8 +552,9 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=0, help="override the number of layers (profiling captures)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU oracle budget per measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--pass", dest="pass_", choices=["fwd", "train"], default="fwd",
-                    help="fwd: the forward stack (the headline); train: forward + backward of the stack")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "train", "score"], default="fwd",
+                    help="fwd: the forward stack (the headline); train: forward + backward of the stack (with "
+                         "moe_1b: the dense-training MoE forward); score: tokenization + stack + head")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

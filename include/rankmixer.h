@@ -110,6 +110,10 @@ typedef struct rm_config {
  *   Wg [T][D][E], bg [T][E]              router h_t(s) = s Wg_t + bg_t, gate ReLU(h)
  *   eW1 [T][E][D][Fe], eb1 [T][E][Fe]    expert first layer (Fe = expert_hidden)
  *   eW2 [T][E][Fe][D], eb2 [T][E][D]     expert second layer
+ * Dense-training / sparse-inference MoE ("RankMixer" section 3.4; "6.4
+ * Rankmixer: 硬件效率优化" section 6.4.4), optional (NULL: not set):
+ *   Wg_train [T][D][E], bg_train [T][E]  the training router h_train; Wg / bg
+ *                                        above are h_infer
  * rm_create copies and repacks everything it needs; the caller may free
  * these buffers once rm_create has returned. */
 typedef struct rm_layer_params {
@@ -117,6 +121,7 @@ typedef struct rm_layer_params {
     const void *ln1_gamma, *ln1_beta, *ln2_gamma, *ln2_beta;
     const void *Wg, *bg;
     const void *eW1, *eb1, *eW2, *eb2;
+    const void *Wg_train, *bg_train;
 } rm_layer_params;
 
 /* Gradients of one dense layer's parameters, DEVICE float32 buffers in the
@@ -213,6 +218,23 @@ RM_API rm_status rm_stack_forward_host(rm_ctx *ctx, const void *X0_host, float *
  * cfg.n_experts > 0. */
 RM_API rm_status rm_moe_pffn_forward(rm_ctx *ctx, int layer, const void *S, float *V_out, float *gates,
                               int B, void *stream);
+
+/* Training forward of the Sparse-MoE PFFN of layer `layer` with the dense-
+ * training / sparse-inference routers ("RankMixer" section 3.4 Eq. 10-11;
+ * "6.4 Rankmixer: 硬件效率优化" section 6.4.4):
+ *   G_train = ReLU(S Wg_train_t + bg_train_t),  V = sum_e G_train[e] FFN_{t,e}(S)
+ *   (the experts with G_train > 0 are computed, as rm_moe_pffn_forward does
+ *   for its router), and alongside it
+ *   G_infer = ReLU(S Wg_t + bg_t),  lreg[b] = sum_{t,e} G_infer[b][t][e],
+ *   A[e] = sum_{b,t} G_infer[b][t][e]  (the regulariser of Eq. 11 per sample,
+ *   and each expert's activation over the batch).
+ * S: device [B][T][D] (context dtype); V_out: device float32 [B][T][D];
+ * gates_train, gates_infer (nullable): device float32 [B][T][E]; lreg
+ * (nullable): device float32 [B]; A (nullable): device float32 [E].  Requires
+ * cfg.n_experts > 0 and the layer's training router (RM_ERR_UNSUPPORTED
+ * otherwise).  Asynchronous on `stream`. */
+RM_API rm_status rm_moe_pffn_forward_train(rm_ctx *ctx, int layer, const void *S, float *V_out, float *gates_train,
+                                           float *gates_infer, float *lreg, float *A, int B, void *stream);
 
 /* Backward pass of one dense block ("RankMixer 详解（1）" section 5.2) for
  * the loss whose gradient at the block output X' is dX_out:

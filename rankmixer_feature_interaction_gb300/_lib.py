@@ -43,7 +43,7 @@ EXPORTED = ["rm_create", "rm_destroy", "rm_block_forward", "rm_stack_forward", "
             "rm_profile_read", "rm_debug_wait_timeout", "rm_last_error", "rm_abi_version",
             "rm_block_forward_noalloc", "rm_debug_gelu", "rm_block_backward", "rm_stack_backward",
             "rm_debug_gelu_grad", "rm_stack_forward_train", "rm_stack_backward_saved", "rm_head_forward",
-            "rm_set_tokenizer", "rm_tokenize", "rm_score"]
+            "rm_set_tokenizer", "rm_tokenize", "rm_score", "rm_moe_pffn_forward_train"]
 
 
 class rm_config(ctypes.Structure):
@@ -55,7 +55,8 @@ class rm_config(ctypes.Structure):
 
 class rm_layer_params(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("W1", "b1", "W2", "b2", "ln1_gamma", "ln1_beta", "ln2_gamma",
-                                               "ln2_beta", "Wg", "bg", "eW1", "eb1", "eW2", "eb2")]
+                                               "ln2_beta", "Wg", "bg", "eW1", "eb1", "eW2", "eb2", "Wg_train",
+                                               "bg_train")]
 
 
 GRAD_FIELDS = ("dW1", "db1", "dW2", "db2", "dln1_gamma", "dln1_beta", "dln2_gamma", "dln2_beta")
@@ -119,6 +120,7 @@ def load() -> ctypes.CDLL:
         "rm_set_tokenizer": (st, [vp, vp, vp, i]),
         "rm_tokenize": (st, [vp, vp, vp, i, vp]),
         "rm_score": (st, [vp, vp, vp, ctypes.c_float, vp, i, vp]),
+        "rm_moe_pffn_forward_train": (st, [vp, i, vp, vp, vp, vp, vp, vp, i, vp]),
         "rm_stack_backward_saved": (st, [vp, vp, vp, ctypes.POINTER(rm_layer_grads), i, vp]),
     }
     for name, (res, args) in sig.items():
@@ -225,6 +227,12 @@ def rm_head_forward(pooled: int, w: int, b: float, y: int | None, p: int | None,
                     dpooled: int | None, B: int, D: int, mean_loss: bool, stream: int) -> None:
     check(load().rm_head_forward(pooled, w, b, y, p, loss, dpooled, B, D, 1 if mean_loss else 0, stream),
           "rm_head_forward")
+
+
+def rm_moe_pffn_forward_train(ctx: int, layer: int, S: int, V: int, gates_train: int | None, gates_infer: int | None,
+                              lreg: int | None, A: int | None, B: int, stream: int) -> None:
+    check(load().rm_moe_pffn_forward_train(ctx, layer, S, V, gates_train, gates_infer, lreg, A, B, stream),
+          "rm_moe_pffn_forward_train")
 
 
 def rm_set_tokenizer(ctx: int, W: int, bias: int, d: int) -> None:

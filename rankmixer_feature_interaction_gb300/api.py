@@ -10,9 +10,10 @@ from . import _lib
 
 _DENSE_KEYS = ("W1", "b1", "W2", "b2", "ln1_g", "ln1_b", "ln2_g", "ln2_b")
 _MOE_KEYS = ("Wg", "bg", "eW1", "eb1", "eW2", "eb2")
+_MOE_TRAIN_KEYS = ("Wg_train", "bg_train")
 _C_NAMES = {"W1": "W1", "b1": "b1", "W2": "W2", "b2": "b2", "ln1_g": "ln1_gamma", "ln1_b": "ln1_beta",
             "ln2_g": "ln2_gamma", "ln2_b": "ln2_beta", "Wg": "Wg", "bg": "bg", "eW1": "eW1", "eb1": "eb1",
-            "eW2": "eW2", "eb2": "eb2"}
+            "eW2": "eW2", "eb2": "eb2", "Wg_train": "Wg_train", "bg_train": "bg_train"}
 _DTYPES = {"bf16": (torch.bfloat16, _lib.RM_BF16), "f32": (torch.float32, _lib.RM_F32)}
 _PATHS = {"auto": _lib.RM_PATH_AUTO, "simt": _lib.RM_PATH_SIMT, "tcgen05": _lib.RM_PATH_TCGEN05}
 
@@ -54,6 +55,9 @@ class RankMixer:
             lp = _lib.rm_layer_params()
             for k_ in _DENSE_KEYS + (_MOE_KEYS if n_experts > 0 else ()):
                 setattr(lp, _C_NAMES[k_], _ptr(p[k_]))
+            if n_experts > 0 and "Wg_train" in p:
+                for k_ in _MOE_TRAIN_KEYS:
+                    setattr(lp, _C_NAMES[k_], _ptr(p[k_]))
             cl.append(lp)
         torch.cuda.synchronize(self.device)
         self.ctx = _lib.rm_create(cfg, cl, device)
@@ -105,6 +109,20 @@ class RankMixer:
         G = torch.empty((B, self.T, self.E), dtype=torch.float32, device=S.device) if return_gates else None
         _lib.rm_moe_pffn_forward(self.ctx, layer, _ptr(S), _ptr(V), _ptr(G), B, _stream())
         return (V, G) if return_gates else V
+
+    def moe_pffn_forward_train(self, layer: int, S: torch.Tensor, V: torch.Tensor | None = None) -> dict:
+        """Dense-training / sparse-inference MoE PFFN forward: V on the training router's
+        gates, plus both routers' gates, the per-sample regulariser lreg and the per-expert
+        activation A of the inference router."""
+        B = S.shape[0]
+        V = torch.empty(S.shape, dtype=torch.float32, device=S.device) if V is None else V
+        gt = torch.empty((B, self.T, self.E), dtype=torch.float32, device=S.device)
+        gi = torch.empty_like(gt)
+        lreg = torch.empty(B, dtype=torch.float32, device=S.device)
+        A = torch.empty(self.E, dtype=torch.float32, device=S.device)
+        _lib.rm_moe_pffn_forward_train(self.ctx, layer, _ptr(S), _ptr(V), _ptr(gt), _ptr(gi), _ptr(lreg), _ptr(A), B,
+                                       _stream())
+        return {"V": V, "G_train": gt, "G_infer": gi, "lreg": lreg, "A": A}
 
     # -- backward calls (contexts created with training=True) -------------------------
     def _grad_tensors(self, dev) -> tuple[dict, _lib.rm_layer_grads]:

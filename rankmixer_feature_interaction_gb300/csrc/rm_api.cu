@@ -66,6 +66,9 @@ struct LayerW {
     // (bf16 contexts) or float, for the backward products
     void* W1t = nullptr;   // [T][D][F]
     void* W2t = nullptr;   // [T][F][D]
+    // the training router of a dense-training / sparse-inference MoE layer
+    float* Wg_train = nullptr;   // [T][E][D]
+    float* bg_train = nullptr;   // [T][E]
 };
 
 // Activations one layer's backward reads (token-major [T][Bcap][W]): the
@@ -137,6 +140,7 @@ struct rm_ctx {
     void* Etok = nullptr;        // fp16 copy of the embeddings [Bcap][T d] (bf16 contexts)
     void* X0ws = nullptr;        // tokens for rm_score [Bcap][T][D], context dtype
     float* pooled_ws = nullptr;  // [Bcap][D]
+    float* ginfer = nullptr;     // inference-router gates of the MoE training forward [Bcap][T][E]
     // host-entry staging: device copies of X0 and pooled, the copy streams and
     // per-chunk events of the pipelined host entry
     void* X0_dev = nullptr;
@@ -178,7 +182,7 @@ void free_ctx(rm_ctx* c) {
         cudaFree(l.W1p); cudaFree(l.W2p); cudaFree(l.b1); cudaFree(l.b2);
         cudaFree(l.g1); cudaFree(l.be1); cudaFree(l.g2); cudaFree(l.be2);
         moe_free_weights(l.moe);
-        cudaFree(l.W1t); cudaFree(l.W2t);
+        cudaFree(l.W1t); cudaFree(l.W2t); cudaFree(l.Wg_train); cudaFree(l.bg_train);
     }
     {
         TrainWS& t = c->tw;
@@ -190,6 +194,7 @@ void free_ctx(rm_ctx* c) {
         cudaFree(t.Xn); cudaFree(t.G0); cudaFree(t.G1); cudaFree(t.pooled);
     }
     cudaFree(c->Wtok); cudaFree(c->btok); cudaFree(c->Etok); cudaFree(c->X0ws); cudaFree(c->pooled_ws);
+    cudaFree(c->ginfer);
     moe_free_workspace(c->moe_ws);
     cudaFree(c->S); cudaFree(c->Hid); cudaFree(c->Z); cudaFree(c->stats); cudaFree(c->rows); cudaFree(c->V);
     cudaFree(c->X0_dev); cudaFree(c->pooled_dev);
@@ -411,6 +416,12 @@ rm_status pack_layer(rm_ctx* c, const rm_layer_params& p, LayerW& w, cudaStream_
         MoeShape ms{c->act, T, D, g.n_experts, g.expert_hidden};
         cudaError_t e = moe_pack_weights(ms, p.Wg, p.bg, p.eW1, p.eb1, p.eW2, p.eb2, w.moe, &c->weight_bytes, s);
         if (e != cudaSuccess) return cuda_fail(e, "pack MoE weights");
+        if ((p.Wg_train == nullptr) != (p.bg_train == nullptr))
+            return fail(RM_ERR_INVALID_ARG, "Wg_train and bg_train must both be set or both be NULL");
+        if (p.Wg_train) {
+            e = moe_pack_router(ms, p.Wg_train, p.bg_train, &w.Wg_train, &w.bg_train, &c->weight_bytes, s);
+            if (e != cudaSuccess) return cuda_fail(e, "pack the training router");
+        }
     }
     return RM_OK;
 }
@@ -1068,6 +1079,47 @@ rm_status rm_debug_gelu_grad(const float* u, float* out, long long n, void* stre
     if (n < 0) return fail(RM_ERR_INVALID_ARG, "n must be >= 0");
     if (n > 0 && (!u || !out)) return fail(RM_ERR_INVALID_ARG, "u / out is NULL");
     RM_CHECK_CUDA(launch_debug_gelu_grad(u, out, n, as_stream(stream)), "debug gelu grad");
+    return RM_OK;
+}
+
+rm_status rm_moe_pffn_forward_train(rm_ctx* c, int layer, const void* S, float* V_out, float* gates_train,
+                                    float* gates_infer, float* lreg, float* A, int B, void* stream) {
+    rm_status st;
+    if ((st = check_ctx(c)) != RM_OK) return st;
+    if (c->cfg.n_experts <= 0) return fail(RM_ERR_UNSUPPORTED, "context was created without experts");
+    if (layer < 0 || layer >= c->cfg.L) return fail(RM_ERR_INVALID_ARG, "layer %d out of range", layer);
+    const LayerW& w = c->layers[layer];
+    if (!w.Wg_train) return fail(RM_ERR_UNSUPPORTED, "layer %d has no training router (Wg_train)", layer);
+    if ((st = check_batch(c, B)) != RM_OK) return st;
+    if (!S || !V_out) return fail(RM_ERR_INVALID_ARG, "S / V_out is NULL");
+    if (!aligned16(S) || !aligned16(V_out) || (gates_train && !aligned16(gates_train)) ||
+        (gates_infer && !aligned16(gates_infer)))
+        return fail(RM_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+    cudaSetDevice(c->device);
+    cudaStream_t s = as_stream(stream);
+    const rm_config& g = c->cfg;
+    // the forward on the training router: the layer's experts with h_train's weights in the router slots
+    MoeWeights wt = w.moe;
+    wt.Wg = w.Wg_train;
+    wt.bg = w.bg_train;
+    MoeLaunch ml{c->act, S, /*S sample-major*/ true, g.T, g.D, g.n_experts, g.expert_hidden, B, c->Bcap, c->num_sms,
+                 c->d_err};
+    cudaError_t e = moe_forward(ml, wt, c->moe_ws, V_out, /*V token-major*/ false, gates_train, s,
+                                [&](int kind) { return (void*)new ProfScope(c, kind, s); },
+                                [](void* p) { delete (ProfScope*)p; });
+    if (e != cudaSuccess) return cuda_fail(e, "moe pffn (training router)");
+    if (!gates_infer && !lreg && !A) return RM_OK;
+    float* gi = gates_infer;
+    if (!gi) {
+        if (!c->ginfer &&
+            (st = dmalloc(c, (void**)&c->ginfer, (size_t)c->Bcap * g.T * g.n_experts * 4, &c->ws_bytes)) != RM_OK)
+            return st;
+        gi = c->ginfer;
+    }
+    ProfScope ps(c, RM_K_MOE_ROUTE, s);
+    RM_CHECK_CUDA(moe_router_gates(c->act, S, w.moe.Wg, w.moe.bg, gi, B, g.T, g.D, g.n_experts, s),
+                  "inference-router gates");
+    RM_CHECK_CUDA(moe_gate_sums(gi, lreg, A, B, g.T, g.n_experts, s), "gate sums");
     return RM_OK;
 }
 

@@ -525,6 +525,21 @@ cudaError_t moe_pack_weights(const MoeShape& ms, const void* Wg, const void* bg,
     return e;
 }
 
+cudaError_t moe_pack_router(const MoeShape& ms, const void* Wg, const void* bg, float** Wg_out, float** bg_out,
+                            long long* bytes, cudaStream_t s) {
+    cudaError_t e;
+    if ((e = dalloc(Wg_out, (size_t)ms.T * ms.E * ms.D, bytes)) != cudaSuccess) return e;
+    if ((e = dalloc(bg_out, (size_t)ms.T * ms.E, bytes)) != cudaSuccess) return e;
+    if ((e = launch_to_f32(ms.act, bg, *bg_out, (size_t)ms.T * ms.E, s)) != cudaSuccess) return e;
+    float* tmp = nullptr;
+    if ((e = dalloc(&tmp, (size_t)ms.T * ms.D * ms.E, nullptr)) != cudaSuccess) return e;
+    e = launch_to_f32(ms.act, Wg, tmp, (size_t)ms.T * ms.D * ms.E, s);
+    if (e == cudaSuccess) e = launch_transpose_f32(tmp, *Wg_out, ms.T, ms.D, ms.E, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    cudaFree(tmp);
+    return e;
+}
+
 void moe_free_weights(MoeWeights& w) {
     cudaFree(w.W1p); cudaFree(w.W2p); cudaFree(w.b1); cudaFree(w.b2); cudaFree(w.Wg); cudaFree(w.bg);
     w = MoeWeights{};
@@ -697,6 +712,91 @@ cudaError_t moe_residual_z(Act act, const float* V, const void* S, void* Z, int 
     else
         residual_z_kernel<float><<<grid, 256, 0, s>>>(V, (const float*)S, (float*)Z, B, T, D, Bcap);
     return cudaGetLastError();
+}
+
+
+// ---- gates of a second router (the inference router during DTSI training) ----------
+// One warp per (b, t) row, experts in groups of 8: lane-strided dot products
+// over D, then a butterfly sum per expert; lane 0 writes ReLU(. + bg).
+namespace {
+template <typename Tin>
+__global__ void __launch_bounds__(256)
+router_gates_kernel(const Tin* __restrict__ S, const float* __restrict__ Wg, const float* __restrict__ bg,
+                    float* __restrict__ G, int B, int T, int D, int E) {
+    const int lane = threadIdx.x & 31;
+    const long long rows = (long long)B * T;
+    for (long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5); row < rows; row += (long long)gridDim.x * 8) {
+        const int t = (int)(row % T);
+        const Tin* s = S + (size_t)row * D;
+        for (int e0 = 0; e0 < E; e0 += 8) {
+            const int ne = min(8, E - e0);
+            float acc[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+            for (int k = lane; k < D; k += 32) {
+                const float x = to_f32(s[k]);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j < ne) acc[j] = fmaf(x, __ldg(Wg + ((size_t)t * E + e0 + j) * D + k), acc[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = warp_sum(acc[j]);
+            if (lane == 0)
+                for (int j = 0; j < ne; ++j)
+                    G[(size_t)row * E + e0 + j] = fmaxf(acc[j] + __ldg(bg + (size_t)t * E + e0 + j), 0.f);
+        }
+    }
+}
+
+__global__ void gate_lreg_kernel(const float* __restrict__ G, float* __restrict__ lreg, int B, int TE) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    const float* g = G + (size_t)b * TE;
+    float s = 0.f;
+    for (int i = 0; i < TE; ++i) s += g[i];
+    lreg[b] = s;
+}
+
+__global__ void __launch_bounds__(256)
+gate_activation_kernel(const float* __restrict__ G, float* __restrict__ A, long long rows, int E) {
+    __shared__ float red[256];
+    const int e = blockIdx.x;
+    float s = 0.f;
+    for (long long r = threadIdx.x; r < rows; r += 256) s += G[(size_t)r * E + e];
+    red[threadIdx.x] = s;
+    __syncthreads();
+    for (int o = 128; o > 0; o >>= 1) {
+        if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) A[e] = red[0];
+}
+}  // namespace
+
+cudaError_t moe_router_gates(Act act, const void* S, const float* Wg, const float* bg, float* G, int B, int T,
+                             int D, int E, cudaStream_t s) {
+    if (B <= 0) return cudaSuccess;
+    long long g = ((long long)B * T + 7) / 8;
+    const int grid = (int)(g > 8192 ? 8192 : g);
+    if (act == Act::F32)
+        router_gates_kernel<float><<<grid, 256, 0, s>>>((const float*)S, Wg, bg, G, B, T, D, E);
+    else
+        router_gates_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>((const __nv_bfloat16*)S, Wg, bg, G, B, T, D, E);
+    return cudaGetLastError();
+}
+
+cudaError_t moe_gate_sums(const float* G, float* lreg, float* A, int B, int T, int E, cudaStream_t s) {
+    if (B <= 0) return cudaSuccess;
+    if (lreg) {
+        gate_lreg_kernel<<<(B + 255) / 256, 256, 0, s>>>(G, lreg, B, T * E);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (A) {
+        gate_activation_kernel<<<E, 256, 0, s>>>(G, A, (long long)B * T, E);
+        return cudaGetLastError();
+    }
+    return cudaSuccess;
 }
 
 }  // namespace rm

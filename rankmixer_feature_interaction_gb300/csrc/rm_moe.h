@@ -67,6 +67,20 @@ cudaError_t moe_forward(const MoeLaunch& ml, const MoeWeights& w, MoeWorkspace& 
                         float* gates_out, cudaStream_t s, const std::function<void*(int)>& prof_begin,
                         const std::function<void(void*)>& prof_end);
 
+// A router alone ([T][D][E] in the caller dtype, bias [T][E]) packed as the
+// expert weights' router is: float32, transposed to [T][E][D].
+cudaError_t moe_pack_router(const MoeShape& ms, const void* Wg, const void* bg, float** Wg_out, float** bg_out,
+                            long long* bytes, cudaStream_t s);
+
+// G[b][t][e] = ReLU(S[b][t] . Wg[t][e] + bg[t][e]) for a packed router; S is
+// sample-major [B][T][D] in the caller dtype.
+cudaError_t moe_router_gates(Act act, const void* S, const float* Wg, const float* bg, float* G, int B, int T,
+                             int D, int E, cudaStream_t s);
+
+// lreg[b] = sum over t, e of G[b][t][e] and A[e] = sum over b, t of G[b][t][e]
+// (either may be null), in a fixed order.
+cudaError_t moe_gate_sums(const float* G, float* lreg, float* A, int B, int T, int E, cudaStream_t s);
+
 // Z[t][b][:] = V[t][b][:] + S[t][b][:]; token-major, V float32, S and Z in the operand type.
 cudaError_t moe_residual_z(Act act, const float* V, const void* S, void* Z, int B, int T, int D, int Bcap,
                            cudaStream_t s);

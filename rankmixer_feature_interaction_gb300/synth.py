@@ -130,6 +130,16 @@ def make_experts(T: int, D: int, E: int, Fe: int, seed: int, dtype: str = "bf16"
     }
 
 
+def make_train_router(T: int, D: int, E: int, seed: int, dtype: str = "bf16", device="cpu",
+                      active: float = 6.0) -> dict:
+    """A second (training) router for the dense-training / sparse-inference MoE: Wg_train
+    [T, D, E] ~ N(0, 1/D), its bias set so that about `active` of E experts open."""
+    td = TORCH_DTYPE[dtype]
+    g = _gen(seed, device)
+    return {"Wg_train": _normal((T, D, E), 1.0 / math.sqrt(D), g, device, td),
+            "bg_train": torch.full((T, E), router_bias(active, E), device=device, dtype=torch.float32).to(td)}
+
+
 def make_stack(T: int, D: int, k: int, L: int, seed: int, dtype: str = "bf16", device="cpu", E: int = 0,
                Fe: int = 0, active: float = 2.0) -> list:
     return [make_layer(T, D, k, seed * 131 + n, dtype, device, E, Fe, active) for n in range(L)]
