@@ -1,6 +1,8 @@
 /*
  * rankmixer.h -- C ABI of librankmixer.so, a GB300 (sm_103a) implementation of
- * the RankMixer block forward.
+ * the RankMixer block forward, its backward (training), the dense-training /
+ * sparse-inference MoE forward, and the tokenization and prediction head on
+ * either side of the stack.
  *
  * What is computed (per sample, X_n in R^{T x D}, H = T heads of q = D/H):
  *   S_{n-1} = LN1(TokenMixing(X_{n-1}) + X_{n-1})
