@@ -366,7 +366,7 @@ def run_ours(args):
     scope_flops = {"gemm1": flops_gemm, "gemm2": flops_gemm, "bwd_wgrad": flops_gemm,
                    "bwd_dgrad": 2 * flops_gemm, "bwd_recompute": 2 * flops_gemm}
     # (bwd_recompute times the training forward of a layer: LN1 and both FFN layers)
-    if train:
+    if train and not moe:
         gemm_kinds = ["gemm1", "gemm2", "bwd_wgrad", "bwd_dgrad", "bwd_recompute"]
     dom = max(gemm_kinds, key=lambda kk: kstats[kk][1])
     launches, tot_ms = kstats[dom]

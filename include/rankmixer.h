@@ -318,6 +318,16 @@ RM_API rm_status rm_head_forward(const float *pooled, const float *w, float b, c
 RM_API rm_status rm_set_tokenizer(rm_ctx *ctx, const void *W, const void *bias, int d);
 RM_API rm_status rm_tokenize(rm_ctx *ctx, const void *E, void *X0, int B, void *stream);
 
+/* Backward of rm_tokenize for the gradient dX0 (device float32 [B][T][D]) at
+ * its output: dW (device float32 [T][d][D]) = sum_b E_slice^T dX0[b][t],
+ * db (device float32 [T][D]) = sum_b dX0[b][t], and, when dE is not NULL,
+ * dE (device float32 [B][T d]) slice t = dX0[b][t] W_t^T.  E: the forward's
+ * input, device [B][T d] (context dtype).  bf16 contexts run the products on
+ * fp16 operands with an exact power-of-two scale per token on dX0.  Sums over
+ * the batch are written, not accumulated.  Asynchronous on `stream`. */
+RM_API rm_status rm_tokenize_backward(rm_ctx *ctx, const void *E, const float *dX0, float *dE, float *dW, float *db,
+                                      int B, void *stream);
+
 /* End-to-end scoring: p[b] = sigmoid(head(pool(stack(tokenize(E[b]))))) with
  * the head's w (device float32 [D]) and b.  E: device [B][T d] (context dtype);
  * p: device float32 [B].  Runs rm_tokenize, rm_stack_forward and

@@ -43,7 +43,7 @@ EXPORTED = ["rm_create", "rm_destroy", "rm_block_forward", "rm_stack_forward", "
             "rm_profile_read", "rm_debug_wait_timeout", "rm_last_error", "rm_abi_version",
             "rm_block_forward_noalloc", "rm_debug_gelu", "rm_block_backward", "rm_stack_backward",
             "rm_debug_gelu_grad", "rm_stack_forward_train", "rm_stack_backward_saved", "rm_head_forward",
-            "rm_set_tokenizer", "rm_tokenize", "rm_score", "rm_moe_pffn_forward_train"]
+            "rm_set_tokenizer", "rm_tokenize", "rm_score", "rm_moe_pffn_forward_train", "rm_tokenize_backward"]
 
 
 class rm_config(ctypes.Structure):
@@ -119,6 +119,7 @@ def load() -> ctypes.CDLL:
         "rm_head_forward": (st, [vp, vp, ctypes.c_float, vp, vp, vp, vp, i, i, i, vp]),
         "rm_set_tokenizer": (st, [vp, vp, vp, i]),
         "rm_tokenize": (st, [vp, vp, vp, i, vp]),
+        "rm_tokenize_backward": (st, [vp, vp, vp, vp, vp, vp, i, vp]),
         "rm_score": (st, [vp, vp, vp, ctypes.c_float, vp, i, vp]),
         "rm_moe_pffn_forward_train": (st, [vp, i, vp, vp, vp, vp, vp, vp, i, vp]),
         "rm_stack_backward_saved": (st, [vp, vp, vp, ctypes.POINTER(rm_layer_grads), i, vp]),
@@ -241,6 +242,10 @@ def rm_set_tokenizer(ctx: int, W: int, bias: int, d: int) -> None:
 
 def rm_tokenize(ctx: int, E: int, X0: int, B: int, stream: int) -> None:
     check(load().rm_tokenize(ctx, E, X0, B, stream), "rm_tokenize")
+
+
+def rm_tokenize_backward(ctx: int, E: int, dX0: int, dE: int | None, dW: int, db: int, B: int, stream: int) -> None:
+    check(load().rm_tokenize_backward(ctx, E, dX0, dE, dW, db, B, stream), "rm_tokenize_backward")
 
 
 def rm_score(ctx: int, E: int, head_w: int, head_b: float, p: int, B: int, stream: int) -> None:

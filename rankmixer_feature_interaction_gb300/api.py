@@ -191,6 +191,17 @@ class RankMixer:
         _lib.rm_tokenize(self.ctx, _ptr(E), _ptr(X0), B, _stream())
         return X0
 
+    def tokenize_backward(self, E: torch.Tensor, dX0: torch.Tensor, with_dE: bool = True) -> dict:
+        """Gradients of tokenize(E) for dX0 [B, T, D] (float32): dW [T, d, D], db [T, D] and
+        (with_dE) dE [B, T d], all float32."""
+        B = E.shape[0]
+        d = self.tok_d
+        dW = torch.empty((self.T, d, self.D), dtype=torch.float32, device=E.device)
+        db = torch.empty((self.T, self.D), dtype=torch.float32, device=E.device)
+        dE = torch.empty((B, self.T * d), dtype=torch.float32, device=E.device) if with_dE else None
+        _lib.rm_tokenize_backward(self.ctx, _ptr(E), _ptr(dX0), _ptr(dE), _ptr(dW), _ptr(db), B, _stream())
+        return {"dE": dE, "dW": dW, "db": db}
+
     def score(self, E: torch.Tensor, head_w: torch.Tensor, head_b: float, p: torch.Tensor | None = None):
         """E [B, T d] -> p [B] = sigmoid(head(pool(stack(tokenize(E)))))."""
         B = E.shape[0]

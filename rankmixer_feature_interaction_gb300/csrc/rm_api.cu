@@ -141,6 +141,9 @@ struct rm_ctx {
     void* X0ws = nullptr;        // tokens for rm_score [Bcap][T][D], context dtype
     float* pooled_ws = nullptr;  // [Bcap][D]
     float* ginfer = nullptr;     // inference-router gates of the MoE training forward [Bcap][T][E]
+    void* dX0h = nullptr;        // tokenization backward: s_t dX0 in fp16 [Bcap][T][D] (bf16 contexts)
+    float* tok_part = nullptr;   // [T][kTokParts] per-token maxima
+    float* tok_inv = nullptr;    // [T] 1 / s_t
     // host-entry staging: device copies of X0 and pooled, the copy streams and
     // per-chunk events of the pipelined host entry
     void* X0_dev = nullptr;
@@ -194,7 +197,7 @@ void free_ctx(rm_ctx* c) {
         cudaFree(t.Xn); cudaFree(t.G0); cudaFree(t.G1); cudaFree(t.pooled);
     }
     cudaFree(c->Wtok); cudaFree(c->btok); cudaFree(c->Etok); cudaFree(c->X0ws); cudaFree(c->pooled_ws);
-    cudaFree(c->ginfer);
+    cudaFree(c->ginfer); cudaFree(c->dX0h); cudaFree(c->tok_part); cudaFree(c->tok_inv);
     moe_free_workspace(c->moe_ws);
     cudaFree(c->S); cudaFree(c->Hid); cudaFree(c->Z); cudaFree(c->stats); cudaFree(c->rows); cudaFree(c->V);
     cudaFree(c->X0_dev); cudaFree(c->pooled_dev);
@@ -1051,6 +1054,56 @@ rm_status rm_tokenize(rm_ctx* c, const void* E, void* X0, int B, void* stream) {
     if (!aligned16(E) || !aligned16(X0)) return fail(RM_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
     cudaSetDevice(c->device);
     return tokenize_impl(c, E, X0, B, as_stream(stream));
+}
+
+rm_status rm_tokenize_backward(rm_ctx* c, const void* E, const float* dX0, float* dE, float* dW, float* db, int B,
+                               void* stream) {
+    rm_status st;
+    if ((st = check_ctx(c)) != RM_OK) return st;
+    if (c->tok_d == 0) return fail(RM_ERR_INVALID_ARG, "no tokenizer: call rm_set_tokenizer first");
+    if ((st = check_batch(c, B)) != RM_OK) return st;
+    if (!E || !dX0 || !dW || !db) return fail(RM_ERR_INVALID_ARG, "E / dX0 / dW / db is NULL");
+    if (!aligned16(E) || !aligned16(dX0) || !aligned16(dW) || !aligned16(db) || (dE && !aligned16(dE)))
+        return fail(RM_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+    cudaSetDevice(c->device);
+    const rm_config& g = c->cfg;
+    const int T = g.T, D = g.D, d = c->tok_d;
+    constexpr int kTokParts = 16;
+    cudaStream_t s = as_stream(stream);
+    ProfScope ps(c, RM_K_TOKENIZE, s);
+    const void* Eop = E;
+    const void* Gop = dX0;
+    const float* inv = nullptr;
+    if (c->act != Act::F32) {
+        if (!c->dX0h) {
+            if ((st = dmalloc(c, &c->dX0h, (size_t)c->Bcap * T * D * 2, &c->ws_bytes)) != RM_OK) return st;
+            if ((st = dmalloc(c, (void**)&c->tok_part, (size_t)T * kTokParts * 4, &c->ws_bytes)) != RM_OK) return st;
+            if ((st = dmalloc(c, (void**)&c->tok_inv, (size_t)T * 4, &c->ws_bytes)) != RM_OK) return st;
+        }
+        RM_CHECK_CUDA(launch_bf16_to_f16(E, c->Etok, (long long)B * T * d, s), "embeddings to fp16");
+        RM_CHECK_CUDA(launch_token_grad_scale(dX0, c->tok_part, kTokParts, c->tok_inv, c->dX0h, B, T, D, s),
+                      "token gradient scale");
+        Eop = c->Etok;
+        Gop = c->dX0h;
+        inv = c->tok_inv;
+    }
+    // dW_t = E_t^T dX0_t: both operands MN-major, K = the batch
+    TrainGemm m = train_gemm_base(c);
+    m.M = d; m.N = D; m.K = B; m.m_valid = d;
+    m.a = {Eop, d, B, d, true, (long long)T * d};
+    m.b = {Gop, D, B, D, true, (long long)T * D};
+    m.c_gpitch = (long long)d * D; m.c0 = dW; m.inv_scale = inv;
+    if ((st = run_train_gemm(c, TE_F32, m, nullptr, "tokenizer dW", s)) != RM_OK) return st;
+    if (dE) {   // dE slice t = dX0_t W_t^T
+        m = train_gemm_base(c);
+        m.M = B; m.N = d; m.K = D; m.m_valid = B;
+        m.a = {Gop, D, B, D, false, (long long)T * D};
+        m.b = {c->Wtok, D, d, (long long)d * D, false};
+        m.c_gpitch = d; m.c_ld = (long long)T * d; m.c0 = dE; m.inv_scale = inv;
+        if ((st = run_train_gemm(c, TE_F32, m, nullptr, "tokenizer dE", s)) != RM_OK) return st;
+    }
+    RM_CHECK_CUDA(launch_token_colsum(dX0, db, B, T, D, s), "tokenizer db");
+    return RM_OK;
 }
 
 rm_status rm_score(rm_ctx* c, const void* E, const float* head_w, float head_b, float* p, int B, void* stream) {

@@ -140,6 +140,13 @@ cudaError_t launch_pool_backward(const float* dpooled, float* G, int B, int T, i
 cudaError_t launch_head(const float* pooled, const float* w, float b, const float* y, float* p, float* loss, float* dO,
                         float gscale, int B, int D, cudaStream_t s);
 
+// Tokenization backward helpers.  For a sample-major gradient G [B][T][D]:
+// the per-token power-of-two scale (part: [T][nparts] scratch) with
+// Gh = fp16(s_t G) and inv_scale[t] = 1 / s_t; and db[t][k] = sum_b G[b][t][k].
+cudaError_t launch_token_grad_scale(const float* G, float* part, int nparts, float* inv_scale, void* Gh, int B, int T,
+                                    int D, cudaStream_t s);
+cudaError_t launch_token_colsum(const float* G, float* db, int B, int T, int D, cudaStream_t s);
+
 // Test hook: out[2i] = Gelu(u[i]), out[2i+1] = Gelu'(u[i]) as the backward epilogues compute them.
 cudaError_t launch_debug_gelu_grad(const float* u, float* out, long long n, cudaStream_t s);
 

@@ -546,6 +546,7 @@ cudaError_t launch_train_gemm_tc(int epi, const TrainGemm& g, int num_sms, cudaS
             break;
         case TE_F32:
             if (amn && bmn) return ttc::run<TE_F32, true, true>(g, ka, num_sms, s);
+            if (!amn && !bmn) return ttc::run<TE_F32, false, false>(g, ka, num_sms, s);
             break;
         case TE_BIAS_IO:
             if (!amn && bmn) return ttc::run<TE_BIAS_IO, false, true>(g, ka, num_sms, s);

@@ -103,3 +103,27 @@ def test_score_needs_a_tokenizer():
     with pytest.raises(_lib.RankMixerError) as e:
         m.score(E, torch.zeros(D, device=DEV), 0.0)
     assert e.value.status == _lib.RM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("dtype,path,T,d,D,B,gscale", [
+    ("bf16", "auto", 4, 256, 256, 300, 1.0),      # tensor cores: dW (MN x MN, K = B ragged), dE (N = d)
+    ("bf16", "auto", 4, 256, 256, 120, 1e-6),     # a small gradient keeps its precision (per-token scale)
+    ("bf16", "auto", 32, 512, 1536, 64, 1.0),     # the 1B width with the bench's slice length
+    ("bf16", "simt", 4, 40, 256, 70, 1.0),        # d not a multiple of 64
+    ("f32", "auto", 4, 6, 8, 64, 1.0),
+])
+def test_tokenize_backward_matches_oracle(dtype, path, T, d, D, B, gscale):
+    layers = synth.make_stack(T, D, 2, 1, 17, dtype, DEV)
+    m = RankMixer(T, D, 2, layers, dtype=dtype, max_batch=B, gemm_path=path)
+    W, b = _tokenizer(T, d, D, 18 + d, dtype)
+    m.set_tokenizer(W, b)
+    E = synth.make_input(B, T, d, 19, dtype, DEV).reshape(B, T * d).contiguous()
+    G = synth.make_output_grad((B, T, D), 20, scale=gscale, device=DEV)
+    out = m.tokenize_backward(E, G)
+    torch.cuda.synchronize()
+    assert m.sync_status() == _lib.RM_OK
+    dE, dW, db = oracle.tokenize_backward(_np(E), _np(W), _np(G))
+    tag = f"tokenize backward {dtype}/{path} T={T} d={d} D={D} B={B} scale={gscale:g}"
+    check(out["dE"], dE, dtype, tag + " dE")
+    check(out["dW"], dW, dtype, tag + " dW")
+    check(out["db"], db, dtype, tag + " db")
