@@ -176,6 +176,14 @@ def max_over_ranks(x: float, device="cpu") -> float:
     return float(t.item())
 
 
+def allreduce_grads(flat) -> None:
+    """Data-parallel training's one exchange: sum every rank's parameter gradients
+    (one flat float32 buffer) over the ranks, in place; nothing without a process group."""
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(flat, op=dist.ReduceOp.SUM)
+
+
 def job_rate(samples_per_rank: int, world: int, steps: int, seconds_max: float) -> float:
     """Whole-job throughput: the samples all ranks processed over the slowest rank's time."""
     return world * samples_per_rank * steps / seconds_max
@@ -225,7 +233,8 @@ def run_ours(args):
         # the gradient of a batch-mean loss at the pooled output
         dP = synth.make_output_grad((B, D), 20260102 + rank, scale=1.0 / (B * world), device=dev)
         dX0 = torch.empty((B, T, D), dtype=torch.float32, device=dev)
-        grads = m.alloc_grads(dev)
+        gflat = torch.empty(m.flat_grad_numel(), dtype=torch.float32, device=dev)
+        grads = m.alloc_grads(dev, flat=gflat)
     if moe and train:
         Gt = torch.empty((B, T, E), dtype=torch.float32, device=dev)
         Gi = torch.empty_like(Gt)
@@ -254,6 +263,7 @@ def run_ours(args):
         elif train:
             m.stack_forward_train(X0, pooled)
             m.stack_backward_saved(dP, dX0, grads)
+            allreduce_grads(gflat)          # the replicas' gradient sum (N > 1)
         else:
             m.stack_forward(X0, pooled)
 
@@ -328,6 +338,7 @@ def run_ours(args):
             dP.copy_(dPh, non_blocking=True)
             m.stack_forward_train(X0, pooled)
             m.stack_backward_saved(dP, dX0, grads)
+            allreduce_grads(gflat)
             ph.copy_(pooled, non_blocking=True)
             torch.cuda.current_stream().synchronize()
 
@@ -426,7 +437,8 @@ def run_ours(args):
         "data": "synthetic (seeded N(0,1) inputs, N(0,1/fan_in) weights; random-init)",
         "config": {"workload": f"{args.config} B={B} T={T} D={D} k={k} L={L}" + (f" E={E} Fe={Fe}" if moe else "")
                    + (f" d={d_tok}" if score else ""),
-                   "batch_per_gpu": B, "global_batch": B * world, "parallelism": f"replicas x{world} (batch sharded)",
+                   "batch_per_gpu": B, "global_batch": B * world, "parallelism": f"replicas x{world} (batch sharded" + (", gradients all-reduced)" if train and not moe and world > 1
+                                                                        else ")"),
                    "l2": "inputs larger than L2 (X0 %.0f MB, weights %.0f MB > 129 MB)" % (
                        X0.numel() * 2 / 1e6, m.info.weight_bytes / 1e6)},
         "tflops": round(flops_step * args.steps * world / (ms_max / 1e3) / 1e12, 1),

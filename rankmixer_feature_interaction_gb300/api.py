@@ -125,11 +125,25 @@ class RankMixer:
         return {"V": V, "G_train": gt, "G_infer": gi, "lreg": lreg, "A": A}
 
     # -- backward calls (contexts created with training=True) -------------------------
-    def _grad_tensors(self, dev) -> tuple[dict, _lib.rm_layer_grads]:
+    def grad_numel(self) -> int:
+        """Float32 values of one layer's parameter gradients."""
+        T, D, F = self.T, self.D, self.k * self.D
+        return 2 * T * D * F + T * F + T * D + 4 * D
+
+    def _grad_tensors(self, dev, flat: torch.Tensor | None = None) -> tuple[dict, _lib.rm_layer_grads]:
         T, D, F = self.T, self.D, self.k * self.D
         shapes = {"dW1": (T, D, F), "db1": (T, F), "dW2": (T, F, D), "db2": (T, D), "dln1_g": (D,),
                   "dln1_b": (D,), "dln2_g": (D,), "dln2_b": (D,)}
-        g = {k_: torch.empty(v, dtype=torch.float32, device=dev) for k_, v in shapes.items()}
+        if flat is None:
+            g = {k_: torch.empty(v, dtype=torch.float32, device=dev) for k_, v in shapes.items()}
+        else:   # views into one buffer (16-byte aligned pieces), e.g. for a single all-reduce
+            g, off = {}, 0
+            for k_, v in shapes.items():
+                n = 1
+                for x in v:
+                    n *= x
+                g[k_] = flat[off:off + n].view(v)
+                off += (n + 3) // 4 * 4
         c = _lib.rm_layer_grads(dW1=_ptr(g["dW1"]), db1=_ptr(g["db1"]), dW2=_ptr(g["dW2"]), db2=_ptr(g["db2"]),
                                 dln1_gamma=_ptr(g["dln1_g"]), dln1_beta=_ptr(g["dln1_b"]),
                                 dln2_gamma=_ptr(g["dln2_g"]), dln2_beta=_ptr(g["dln2_b"]))
@@ -145,9 +159,20 @@ class RankMixer:
         _lib.rm_block_backward(self.ctx, layer, _ptr(X), _ptr(G), _ptr(dX), c, B, _stream())
         return dX, g
 
-    def alloc_grads(self, device=None) -> list:
-        """Gradient buffers for every layer: a list of (dict of tensors, rm_layer_grads)."""
-        return [self._grad_tensors(device or self.device) for _ in range(self.L)]
+    def alloc_grads(self, device=None, flat: torch.Tensor | None = None) -> list:
+        """Gradient buffers for every layer: a list of (dict of tensors, rm_layer_grads).
+        With `flat` (float32, at least L * padded grad_numel() values, see flat_grad_numel)
+        the tensors are views into it, layer after layer."""
+        if flat is None:
+            return [self._grad_tensors(device or self.device) for _ in range(self.L)]
+        per = self.flat_grad_numel() // self.L
+        return [self._grad_tensors(flat.device, flat[n * per:(n + 1) * per]) for n in range(self.L)]
+
+    def flat_grad_numel(self) -> int:
+        """Values of a flat buffer holding every layer's gradients (each piece padded to 4)."""
+        T, D, F = self.T, self.D, self.k * self.D
+        pieces = [T * D * F, T * F, T * F * D, T * D, D, D, D, D]
+        return self.L * sum((n + 3) // 4 * 4 for n in pieces)
 
     def stack_backward(self, X0: torch.Tensor, dpooled: torch.Tensor, dX0: torch.Tensor | None = None,
                        grads: list | None = None):

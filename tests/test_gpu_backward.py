@@ -232,3 +232,19 @@ def test_saved_backward_needs_its_training_forward():
     with pytest.raises(_lib.RankMixerError) as e:          # the activations were consumed
         m.stack_backward_saved(dP)
     assert e.value.status == _lib.RM_ERR_INVALID_ARG
+
+
+def test_gradients_into_one_flat_buffer_equal_separate_buffers():
+    """The benchmark's replicas write all gradients into one flat buffer (one all-reduce);
+    the views get the same values as separate tensors."""
+    T, D, k, B, L = 4, 256, 4, 100, 2
+    m, _ = _model(T, D, k, L, B, 401, "bf16")
+    X0 = synth.make_input(B, T, D, 402, "bf16", DEV)
+    dP = synth.make_output_grad((B, D), 403, device=DEV)
+    _, g_sep = m.stack_backward(X0, dP)
+    flat = torch.full((m.flat_grad_numel(),), float("nan"), dtype=torch.float32, device=DEV)
+    _, g_flat = m.stack_backward(X0, dP, grads=m.alloc_grads(flat=flat))
+    torch.cuda.synchronize()
+    for n in range(L):
+        for k_ in NAMES:
+            assert torch.equal(g_sep[n][k_], g_flat[n][k_]), (n, k_)

@@ -109,3 +109,52 @@ def test_two_gloo_ranks_shard_the_batch_and_take_the_max_time(tmp_path):
     sharded = np.load(tmp_path / "pooled_sharded.npy")
     assert sharded.shape == whole.shape
     assert np.array_equal(sharded, whole)
+
+
+def _train_rank_main(rank: int, world: int, port: int, out_dir: str):
+    """Data-parallel training on gloo ranks: each rank's oracle gradients on its shard,
+    summed over the ranks by bench.allreduce_grads."""
+    import torch.distributed as dist
+
+    import oracle
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        T, D, k, L = 2, 4, 2, 2
+        global_B = 2 * synth.SHARD_BLOCK + 3
+        start, stop = bench.shard_batch(global_B, world, rank)
+        layers = synth.to_f64(synth.make_stack(T, D, k, L, 6, "f32", "cpu"))
+        X = synth.to_f64(synth.make_input_shard(global_B, start, stop, T, D, 20260101, "f32"))
+        dP = np.random.default_rng(7).standard_normal((global_B, D))[start:stop] / global_B
+        oracle.set_num_threads(1)
+        _, grads = oracle.stack_backward(X, dP, layers)
+        flat = torch.from_numpy(np.concatenate([g[key].reshape(-1) for g in grads for key in oracle.GRAD_KEYS]))
+        bench.allreduce_grads(flat)
+        if rank == 0:
+            np.save(os.path.join(out_dir, "grads_allreduced.npy"), flat.numpy())
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_all_reduce_their_shard_gradients(tmp_path):
+    """The sum over ranks of the shard gradients is the whole batch's gradient ("RankMixer 详解（1）"
+    section 5.2: batch gradients add up over samples), so a replica step needs exactly this one
+    exchange."""
+    import oracle
+
+    world = 2
+    mp.start_processes(_train_rank_main, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True,
+                       start_method="spawn")
+    T, D, k, L = 2, 4, 2, 2
+    global_B = 2 * synth.SHARD_BLOCK + 3
+    layers = synth.to_f64(synth.make_stack(T, D, k, L, 6, "f32", "cpu"))
+    X = synth.to_f64(synth.make_input_shard(global_B, 0, global_B, T, D, 20260101, "f32"))
+    dP = np.random.default_rng(7).standard_normal((global_B, D)) / global_B
+    _, grads = oracle.stack_backward(X, dP, layers)
+    whole = np.concatenate([g[key].reshape(-1) for g in grads for key in oracle.GRAD_KEYS])
+    summed = np.load(tmp_path / "grads_allreduced.npy")
+    np.testing.assert_allclose(summed, whole, rtol=1e-11, atol=1e-13)
+    # without a process group the call leaves the buffer alone
+    t = torch.ones(3, dtype=torch.float64)
+    bench.allreduce_grads(t)
+    assert torch.equal(t, torch.ones(3, dtype=torch.float64))
