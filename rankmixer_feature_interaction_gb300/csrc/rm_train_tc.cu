@@ -37,26 +37,35 @@ namespace ttc {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
-// Epilogue warps: 8 (two per TMEM lane quadrant).  16 warps for the heavy
-// epilogues measured the same (2.03 against 2.05 ms for the Gelu and Gelu'
-// epilogue at the 1B shape): the wait on each TMEM load was the cost, which
-// loading the next 32 columns during the current ones removes.
-template <int EPI>
-struct EpiCfg {
-    static constexpr int WARPS = 8;
-    static constexpr int THREADS = 128 + 32 * WARPS;
-    static constexpr int COLS = 256 / (WARPS / 4);      // columns of the tile per epilogue warp
-};
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int MN_BOX_BYTES = 64 * BK * 2;          // one 64 (M/N) x 64 (K) box of an MN-major operand
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-static_assert(2 * STAGES * 8 + 4 * 8 + 8 <= BAR_BYTES, "barrier area");
+// Epilogue warps: 8 (two per TMEM lane quadrant).  16 warps for the heavy
+// epilogues measured the same (2.03 against 2.05 ms for the Gelu and Gelu'
+// epilogue at the 1B shape): the wait on each TMEM load was the cost, which
+// loading the next 32 columns during the current ones removes.
+//
+// The epilogue with Gelu and Gelu' outputs stores through shared memory and
+// TMA tensor stores (32 x 32 fp16 blocks, two outputs, two buffers each per
+// warp, 8 KB per warp): a lane's row of 64 bytes is one 16-byte store per
+// quarter instead of 32 rows' scattered 16-byte pieces per warp store, which
+// kept that product at half the tensor rate.  Its staging takes the room of
+// one pipeline stage (3 stages of 48 KB instead of 4).
+template <int EPI>
+struct EpiCfg {
+    static constexpr int WARPS = 8;
+    static constexpr int THREADS = 128 + 32 * WARPS;
+    static constexpr int COLS = 256 / (WARPS / 4);      // columns of the tile per epilogue warp
+    static constexpr bool TMA_OUT = EPI == TE_GELU2;
+    static constexpr int STAGES = TMA_OUT ? 3 : 4;
+    static constexpr int EPI_BYTES = TMA_OUT ? WARPS * 4 * 2048 : 0;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static_assert(2 * STAGES * 8 + 4 * 8 + 8 <= BAR_BYTES, "barrier area");
+};
 
 struct KArgs {
     int G, M, N, K;
@@ -170,6 +179,62 @@ __device__ __forceinline__ float column_sums32(float (&v)[32], int lane) {
 }
 
 // Epilogue of one warp: 32 rows (TMEM lanes) x EpiCfg<EPI>::COLS columns from n0.
+// Gelu / Gelu' epilogue through shared memory: per 32-column chunk each lane
+// packs its row's 32 values of each output (64 bytes) into a staging block
+// with the 64-byte swizzle (16-byte piece k of row r at piece k ^ ((r >> 1) & 3)),
+// and lane 0 hands both blocks to the TMA engine, which clips the rows past
+// the batch.  Two pairs of blocks alternate; a pair is refilled only after the
+// stores that read it have finished reading (bulk wait_group.read 1).
+__device__ __forceinline__ void epilogue_gelu2_tma(const KArgs& a, const CUtensorMap* tmC0, const CUtensorMap* tmC1,
+                                                   int g, int m_warp, uint32_t tbase, int n0, int lane,
+                                                   uint32_t stage, int& sbuf) {
+    constexpr int NC = EpiCfg<TE_GELU2>::COLS / 32;
+    const float inv_s = a.inv_scale ? __ldg(a.inv_scale + g) : 1.0f;
+    const uint32_t sw = (uint32_t)((lane >> 1) & 3);
+    uint32_t rbuf[2][32];
+    tmem_ld32_nowait(tbase, rbuf[0]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+        if (c + 1 < NC) tmem_ld32_nowait(tbase + 32u * (c + 1), rbuf[(c + 1) & 1]);
+        const float4* b4 = reinterpret_cast<const float4*>(a.bias + (size_t)g * a.N + n0 + 32 * c);
+        uint32_t pa[16], pg[16];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float4 bb = __ldg(b4 + j);
+            const uint32_t* r = rbuf[c & 1];
+            const GeluPair x0 = gelu_with_grad(fmaf(__uint_as_float(r[4 * j]), inv_s, bb.x));
+            const GeluPair x1 = gelu_with_grad(fmaf(__uint_as_float(r[4 * j + 1]), inv_s, bb.y));
+            const GeluPair x2 = gelu_with_grad(fmaf(__uint_as_float(r[4 * j + 2]), inv_s, bb.z));
+            const GeluPair x3 = gelu_with_grad(fmaf(__uint_as_float(r[4 * j + 3]), inv_s, bb.w));
+            pa[2 * j] = f16x2_bits(x0.value, x1.value);
+            pa[2 * j + 1] = f16x2_bits(x2.value, x3.value);
+            pg[2 * j] = f16x2_bits(x0.grad, x1.grad);
+            pg[2 * j + 1] = f16x2_bits(x2.grad, x3.grad);
+        }
+        if (lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
+        const uint32_t buf0 = stage + (uint32_t)sbuf * 4096u, buf1 = buf0 + 2048u;
+        const uint32_t row0 = buf0 + (uint32_t)lane * 64u, row1 = buf1 + (uint32_t)lane * 64u;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            st_shared_v4(row0 + (((uint32_t)k ^ sw) << 4), pa[4 * k], pa[4 * k + 1], pa[4 * k + 2], pa[4 * k + 3]);
+            st_shared_v4(row1 + (((uint32_t)k ^ sw) << 4), pg[4 * k], pg[4 * k + 1], pg[4 * k + 2], pg[4 * k + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            if (m_warp < a.m_valid) {
+                tma_store_3d(tmC0, buf0, n0 + 32 * c, m_warp, g);
+                tma_store_3d(tmC1, buf1, n0 + 32 * c, m_warp, g);
+            }
+            bulk_commit_group();
+        }
+        sbuf ^= 1;
+        if (c + 1 < NC) tmem_wait_ld();
+    }
+}
+
 template <int EPI>
 __device__ __forceinline__ void epilogue(const KArgs& a, int g, int m, bool valid, uint32_t tbase, int n0, int lane,
                                          int quad, int mb) {
@@ -284,19 +349,23 @@ __device__ __forceinline__ void epilogue(const KArgs& a, int g, int m, bool vali
 template <int EPI, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(EpiCfg<EPI>::THREADS, 1)
 train_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
                      const KArgs args) {
+    constexpr int STAGES = EpiCfg<EPI>::STAGES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - raw_addr);
     const uint32_t sA = base;
     const uint32_t sB = base + STAGES * A_BYTES;
-    const uint32_t bar0 = base + STAGES * STAGE_BYTES;
+    const uint32_t sEpi = base + STAGES * STAGE_BYTES;                 // TMA-store staging (1024-aligned)
+    const uint32_t bar0 = sEpi + EpiCfg<EPI>::EPI_BYTES;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto tfull_bar = [&](int x) { return bar0 + 8u * (2 * STAGES + x); };
     auto tempty_bar = [&](int x) { return bar0 + 8u * (2 * STAGES + 2 + x); };
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + STAGES * STAGE_BYTES + 8 * (2 * STAGES + 4));
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + STAGES * STAGE_BYTES + EpiCfg<EPI>::EPI_BYTES +
+                                                        8 * (2 * STAGES + 4));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -417,6 +486,8 @@ train_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         const int ew = warp - 4;
         const int quad = warp & 3;
         const int half = ew >> 2;               // which group of EpiCfg<EPI>::COLS columns
+        const uint32_t stage = sEpi + (uint32_t)ew * 8192u;
+        int sbuf = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
         for (long long tile = blockIdx.x; tile < args.tiles; tile += gridDim.x) {
@@ -427,12 +498,18 @@ train_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             const int m = mb * BM + quad * 32 + lane;
             const uint32_t tbase =
                 tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN + half * EpiCfg<EPI>::COLS);
-            epilogue<EPI>(args, g, m, m < args.m_valid, tbase, nb * BN + half * EpiCfg<EPI>::COLS, lane, quad, mb);
+            if constexpr (EpiCfg<EPI>::TMA_OUT)
+                epilogue_gelu2_tma(args, &tmC0, &tmC1, g, m - lane, tbase, nb * BN + half * EpiCfg<EPI>::COLS, lane,
+                                   stage, sbuf);
+            else
+                epilogue<EPI>(args, g, m, m < args.m_valid, tbase, nb * BN + half * EpiCfg<EPI>::COLS, lane, quad,
+                              mb);
             tc_fence_before();
             mbar_arrive(tempty_bar(acc));
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
+        if (EpiCfg<EPI>::TMA_OUT && lane == 0) bulk_wait_group<0>();   // this warp's tensor stores have landed
     }
 
     tc_fence_before();
@@ -472,20 +549,41 @@ bool make_map(CUtensorMap* m, const TOperand& op, int G, int box_outer) {
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp16 output map over [G][rows][N] (row pitch ld, group pitch gpitch): box
+// 32 x 32 x 1 with the 64-byte swizzle; rows at or past `rows` are clipped.
+bool make_map_out(CUtensorMap* m, void* ptr, int N, int rows, int G, long long ld, long long gpitch) {
+    if (!get_encoder()) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)rows, (cuuint64_t)G};
+    cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)gpitch * 2};
+    cuuint32_t box[3] = {32u, 32u, 1u};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, ptr, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int EPI, bool A_MN, bool B_MN>
 cudaError_t run(const TrainGemm& g, const KArgs& ka, int num_sms, cudaStream_t s) {
-    CUtensorMap mA, mB;
+    CUtensorMap mA, mB, mC0, mC1;
     if (!make_map(&mA, g.a, g.G, A_MN ? BK : BM)) return cudaErrorInvalidValue;
     if (!make_map(&mB, g.b, g.G, B_MN ? BK : BN)) return cudaErrorInvalidValue;
+    if constexpr (EpiCfg<EPI>::TMA_OUT) {
+        if (!make_map_out(&mC0, g.c0, g.N, g.m_valid, g.G, ka.c_ld, g.c_gpitch)) return cudaErrorInvalidValue;
+        if (!make_map_out(&mC1, g.c1, g.N, g.m_valid, g.G, ka.c_ld, g.c_gpitch)) return cudaErrorInvalidValue;
+    } else {
+        mC0 = mA;   // unused
+        mC1 = mA;
+    }
     auto k = train_gemm_tc_kernel<EPI, A_MN, B_MN>;
+    constexpr int smem = EpiCfg<EPI>::SMEM_BYTES;
     static bool attr_done = false;
     if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
     const long long grid = ka.tiles < num_sms ? ka.tiles : num_sms;
-    k<<<(int)grid, EpiCfg<EPI>::THREADS, SMEM_BYTES, s>>>(mA, mB, ka);
+    k<<<(int)grid, EpiCfg<EPI>::THREADS, smem, s>>>(mA, mB, mC0, mC1, ka);
     return cudaGetLastError();
 }
 
@@ -495,6 +593,7 @@ bool train_tc_supported(const TrainGemm& g) {
     auto aligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     if (g.N % ttc::BN != 0 || g.M < 1 || g.K < 1 || g.G < 1) return false;
     if (!aligned(g.a.ptr) || !aligned(g.b.ptr)) return false;
+    if ((g.c0 && !aligned(g.c0)) || (g.c1 && !aligned(g.c1))) return false;   // TMA stores, 16-byte vectors
     // K-major operands: K is the inner extent and must fill whole 64-deep k-blocks
     if (!g.a.mn && (g.a.inner != g.K || g.K % ttc::BK != 0)) return false;
     if (!g.b.mn && (g.b.inner != g.K || g.K % ttc::BK != 0)) return false;
