@@ -439,7 +439,7 @@ rm_status train_ws_ready(rm_ctx* c, int nslots, bool stack) {
     rm_status st;
     if (!t.ready) {
         t.nblk2 = ln2_bwd_blocks(c->act, c->Bcap, g.T, g.D, c->num_sms);
-        t.colrows = (c->Bcap + 127) / 128 * (128 / kTrainColpartRows);
+        t.colrows = (c->Bcap + 255) / 256 * (256 / kTrainColpartRows);   // covers 128- and 256-row tiles
         t.grid1 = ln1_bwd_grid(c->Bcap, g.T, g.D, c->num_sms);
         if ((st = dmalloc(c, (void**)&t.dZ32, T * Bc * D * 4, &c->ws_bytes)) != RM_OK ||
             (c->act != Act::F32 && (st = dmalloc(c, &t.dZ, T * Bc * D * osz, &c->ws_bytes)) != RM_OK) ||
@@ -571,6 +571,7 @@ rm_status train_layer_backward(rm_ctx* c, int layer, int slot, const float* G, f
         if ((st = run_train_gemm(c, TE_F32, m, nullptr, "dW2", s)) != RM_OK) return st;
     }
     bool db1_partials = false;
+    int colrows = 0;
     void* dU = sl.Gp;     // s_t dU = (s_t dZ W2^T) * Gelu'(U) replaces Gelu'(U) element by element
     {
         ProfScope ps(c, RM_K_BWD_DGRAD, s);
@@ -581,6 +582,7 @@ rm_status train_layer_backward(rm_ctx* c, int layer, int slot, const float* G, f
         m.c_gpitch = BcF; m.c0 = dU; m.r = sl.Gp; m.inv_scale = inv;
         const bool tc = c->use_tc && train_tc_supported(m);
         m.colpart = tc ? t.colpart : gr.db1;
+        colrows = tc ? train_colpart_rows(m, c->num_sms) : 0;
         if ((st = run_train_gemm(c, TE_DGELU, m, &db1_partials, "dU", s)) != RM_OK) return st;
         m = train_gemm_base(c);
         m.M = B; m.N = D; m.K = F; m.m_valid = B;
@@ -606,10 +608,8 @@ rm_status train_layer_backward(rm_ctx* c, int layer, int slot, const float* G, f
         RM_CHECK_CUDA(launch_ln1_mix_backward(c->act, sl.Yh, sl.rstd1, t.dS, w.g1, dX, p_dg1, p_dbe1, B, T, D, Bc,
                                               grid1, c->d_err, kWaitTimeoutNs, s),
                       "ln1 + mixing backward");
-        if (db1_partials) {
-            const int rows = (B + 127) / 128 * (128 / kTrainColpartRows);
-            RM_CHECK_CUDA(launch_sum_rows(t.colpart, gr.db1, nullptr, T, rows, F, s), "db1");
-        }
+        if (db1_partials)
+            RM_CHECK_CUDA(launch_sum_rows(t.colpart, gr.db1, nullptr, T, colrows, F, s), "db1");
         RM_CHECK_CUDA(launch_sum_rows(p_db2, gr.db2, nullptr, T, nblk, D, s), "db2");
         RM_CHECK_CUDA(launch_sum_rows(p_dg2, t.tmpTD, gr.dln2_gamma, T, nblk, D, s), "dgamma2");
         RM_CHECK_CUDA(launch_sum_rows(p_dbe2, t.tmpTD, gr.dln2_beta, T, nblk, D, s), "dbeta2");

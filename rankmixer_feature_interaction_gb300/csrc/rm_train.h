@@ -62,9 +62,9 @@ struct TrainGemm {
     const void* r;          // TE_RESID / TE_DRESID: residual rows; TE_DGELU: Gp
     const float* bias;      // [G][N]
     const float* inv_scale; // [G] or null (1)
-    // TE_DGELU: column sums of C0 over each block of `colpart_rows` rows of a
-    // tile, [G][ceil(M / colpart_rows)][N] (tensor-core path: 32-row blocks;
-    // the SIMT path writes the finished sums instead, see launch_train_gemm_simt)
+    // TE_DGELU: column sums of C0 over each 32-row block of a tile,
+    // [G][train_colpart_rows(g)][N] (tensor-core path; the SIMT path writes the
+    // finished sums instead, see launch_train_gemm_simt)
     float* colpart;
     int* err;
     unsigned long long timeout_ns;
@@ -72,6 +72,11 @@ struct TrainGemm {
 
 // Rows of C summed into one TE_DGELU partial on the tensor-core path.
 constexpr int kTrainColpartRows = 32;
+
+// Partial rows per group that the tensor-core path writes for g: whole tiles
+// of 128 rows (one CTA) or 256 rows (a CTA pair) in 32-row blocks; never more
+// than ceil(m_valid / 256) * 8.
+int train_colpart_rows(const TrainGemm& g, int num_sms);
 
 // tcgen05 path: fp16 operands (A and B), N a multiple of 256, K-major inner
 // extents multiples of 64, MN-major inner extents multiples of 128 (A) / 256 (B).

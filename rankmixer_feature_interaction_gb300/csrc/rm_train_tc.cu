@@ -37,12 +37,11 @@ namespace ttc {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int A_BYTES = BM * BK * 2;               // one 64-deep k-block of this CTA's 128 rows of A
 constexpr int MN_BOX_BYTES = 64 * BK * 2;          // one 64 (M/N) x 64 (K) box of an MN-major operand
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int BAR_BYTES = 256;
+constexpr int SMEM_LIMIT = 227 * 1024;
 // Epilogue warps: 8 (two per TMEM lane quadrant).  16 warps for the heavy
 // epilogues measured the same (2.03 against 2.05 ms for the Gelu and Gelu'
 // epilogue at the 1B shape): the wait on each TMEM load was the cost, which
@@ -50,21 +49,38 @@ constexpr int BAR_BYTES = 256;
 //
 // The epilogue with Gelu and Gelu' outputs stores through shared memory and
 // TMA tensor stores (32 x 32 fp16 blocks, two outputs, two buffers each per
-// warp, 8 KB per warp): a lane's row of 64 bytes is one 16-byte store per
-// quarter instead of 32 rows' scattered 16-byte pieces per warp store, which
-// kept that product at half the tensor rate.  Its staging takes the room of
-// one pipeline stage (3 stages of 48 KB instead of 4).
-template <int EPI>
-struct EpiCfg {
+// warp, 8 KB per warp, plus the warp's 128 bias values): a lane's row of 64
+// bytes is one 16-byte store per quarter instead of 32 rows' scattered
+// 16-byte pieces per warp store.
+//
+// PAIR: a cluster of two CTAs on two SMs computes a 256 x 256 tile with
+// tcgen05.mma.cta_group::2.  CTA r loads A rows [128 r, 128 r + 128) of the
+// tile and B rows (N) [128 r, 128 r + 128); the even CTA issues the MMAs
+// (M = 256), which accumulate each CTA's 128 rows in its own TMEM.  A stage
+// is then 32 KB per CTA instead of 48 KB, so each SM pulls a third less
+// operand data from L2 per flop and more stages fit (more loads in flight).
+//   full[s]   (even CTA)  1 arrival (its producer, expecting both CTAs' bytes)
+//   empty[s]  (each CTA)  1 arrival: multicast commit from the even CTA
+//   tfull[a]  (each CTA)  1 arrival: multicast commit from the even CTA
+//   tempty[a] (even CTA)  2 x 8 arrivals: every epilogue warp of both CTAs
+template <int EPI, bool PAIR>
+struct KCfg {
     static constexpr int WARPS = 8;
     static constexpr int THREADS = 128 + 32 * WARPS;
     static constexpr int COLS = 256 / (WARPS / 4);      // columns of the tile per epilogue warp
     static constexpr bool TMA_OUT = EPI == TE_GELU2;
-    static constexpr int STAGES = TMA_OUT ? 3 : 4;
-    static constexpr int EPI_BYTES = TMA_OUT ? WARPS * 4 * 2048 : 0;
+    static constexpr int TM = PAIR ? 256 : BM;          // rows of C per tile
+    static constexpr int BROWS = PAIR ? BN / 2 : BN;    // rows (N) of B this CTA loads
+    static constexpr int B_BYTES = BROWS * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int EPI_BYTES = TMA_OUT ? WARPS * (4 * 2048 + 4 * COLS) : 0;
+    static constexpr int FIT = (SMEM_LIMIT - 1024 - EPI_BYTES - BAR_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES = FIT < 7 ? FIT : 7;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
-    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static_assert(STAGES >= 3, "pipeline depth");
+    static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
     static_assert(2 * STAGES * 8 + 4 * 8 + 8 <= BAR_BYTES, "barrier area");
+    static_assert(COLS == 128, "one float4 of bias per lane in the staged epilogue");
 };
 
 struct KArgs {
@@ -126,6 +142,12 @@ __device__ __forceinline__ void tile_of(long long tile, const KArgs& a, int& g, 
 }
 
 // Two floats to an fp16 pair, saturating at +-65504 instead of overflowing.
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ uint32_t f16x2_bits(float lo, float hi) {
     const __half2 h = __floats2half2_rn(sat_f16(lo), sat_f16(hi));
     return *reinterpret_cast<const uint32_t*>(&h);
@@ -178,7 +200,7 @@ __device__ __forceinline__ float column_sums32(float (&v)[32], int lane) {
     return v[0];
 }
 
-// Epilogue of one warp: 32 rows (TMEM lanes) x EpiCfg<EPI>::COLS columns from n0.
+// Epilogue of one warp: 32 rows (TMEM lanes) x 128 columns from n0.
 // Gelu / Gelu' epilogue through shared memory: per 32-column chunk each lane
 // packs its row's 32 values of each output (64 bytes) into a staging block
 // with the 64-byte swizzle (16-byte piece k of row r at piece k ^ ((r >> 1) & 3)),
@@ -187,9 +209,9 @@ __device__ __forceinline__ float column_sums32(float (&v)[32], int lane) {
 // stores that read it have finished reading (bulk wait_group.read 1).
 __device__ __forceinline__ void epilogue_gelu2_tma(const KArgs& a, const CUtensorMap* tmC0, const CUtensorMap* tmC1,
                                                    int g, int m_warp, uint32_t tbase, int n0, int lane,
-                                                   uint32_t stage, int& sbuf) {
-    constexpr int NC = EpiCfg<TE_GELU2>::COLS / 32;
-    const float inv_s = a.inv_scale ? __ldg(a.inv_scale + g) : 1.0f;
+                                                   uint32_t stage, uint32_t sbias, int& sbuf) {
+    constexpr int NC = KCfg<TE_GELU2, false>::COLS / 32;
+    const uint64_t s2 = f2_splat(a.inv_scale ? __ldg(a.inv_scale + g) : 1.0f);
     const uint32_t sw = (uint32_t)((lane >> 1) & 3);
     uint32_t rbuf[2][32];
     tmem_ld32_nowait(tbase, rbuf[0]);
@@ -197,20 +219,20 @@ __device__ __forceinline__ void epilogue_gelu2_tma(const KArgs& a, const CUtenso
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
         if (c + 1 < NC) tmem_ld32_nowait(tbase + 32u * (c + 1), rbuf[(c + 1) & 1]);
-        const float4* b4 = reinterpret_cast<const float4*>(a.bias + (size_t)g * a.N + n0 + 32 * c);
+        const uint32_t* r = rbuf[c & 1];
         uint32_t pa[16], pg[16];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const float4 bb = __ldg(b4 + j);
-            const uint32_t* r = rbuf[c & 1];
-            const GeluPair x0 = gelu_with_grad(fmaf(__uint_as_float(r[4 * j]), inv_s, bb.x));
-            const GeluPair x1 = gelu_with_grad(fmaf(__uint_as_float(r[4 * j + 1]), inv_s, bb.y));
-            const GeluPair x2 = gelu_with_grad(fmaf(__uint_as_float(r[4 * j + 2]), inv_s, bb.z));
-            const GeluPair x3 = gelu_with_grad(fmaf(__uint_as_float(r[4 * j + 3]), inv_s, bb.w));
-            pa[2 * j] = f16x2_bits(x0.value, x1.value);
-            pa[2 * j + 1] = f16x2_bits(x2.value, x3.value);
-            pg[2 * j] = f16x2_bits(x0.grad, x1.grad);
-            pg[2 * j + 1] = f16x2_bits(x2.grad, x3.grad);
+            const float4 bb = ld_shared_f4(sbias + 128u * c + 16u * j);
+            uint64_t v0, g0, v1, g1;
+            gelu_with_grad_x2(f2_pack(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1])), s2,
+                              f2_pack(bb.x, bb.y), v0, g0);
+            gelu_with_grad_x2(f2_pack(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])), s2,
+                              f2_pack(bb.z, bb.w), v1, g1);
+            pa[2 * j] = pack_f16x2_from_f2(v0);
+            pa[2 * j + 1] = pack_f16x2_from_f2(v1);
+            pg[2 * j] = pack_f16x2_from_f2(g0);
+            pg[2 * j + 1] = pack_f16x2_from_f2(g1);
         }
         if (lane == 0) bulk_wait_group_read<1>();
         __syncwarp();
@@ -237,10 +259,10 @@ __device__ __forceinline__ void epilogue_gelu2_tma(const KArgs& a, const CUtenso
 
 template <int EPI>
 __device__ __forceinline__ void epilogue(const KArgs& a, int g, int m, bool valid, uint32_t tbase, int n0, int lane,
-                                         int quad, int mb) {
+                                         int prow) {
     const size_t row = (size_t)g * (size_t)a.c_gpitch + (size_t)m * (size_t)a.c_ld + (size_t)n0;
     const float inv_s = a.inv_scale ? __ldg(a.inv_scale + g) : 1.0f;
-    constexpr int NC = EpiCfg<EPI>::COLS / 32;
+    constexpr int NC = KCfg<EPI, false>::COLS / 32;
     // chunk c + 1 loads from TMEM while chunk c is processed (two register sets)
     uint32_t rbuf[2][32];
     tmem_ld32_nowait(tbase, rbuf[0]);
@@ -252,26 +274,7 @@ __device__ __forceinline__ void epilogue(const KArgs& a, int g, int m, bool vali
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(rbuf[c & 1][i]);
         const size_t off = row + 32 * c;
-        if (EPI == TE_GELU2) {
-            if (valid) {
-                const float4* b4 = reinterpret_cast<const float4*>(a.bias + (size_t)g * a.N + n0 + 32 * c);
-                uint32_t pa[16], pg[16];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float4 bb = __ldg(b4 + j);
-                    const GeluPair x0 = gelu_with_grad(fmaf(v[4 * j], inv_s, bb.x));
-                    const GeluPair x1 = gelu_with_grad(fmaf(v[4 * j + 1], inv_s, bb.y));
-                    const GeluPair x2 = gelu_with_grad(fmaf(v[4 * j + 2], inv_s, bb.z));
-                    const GeluPair x3 = gelu_with_grad(fmaf(v[4 * j + 3], inv_s, bb.w));
-                    pa[2 * j] = f16x2_bits(x0.value, x1.value);
-                    pa[2 * j + 1] = f16x2_bits(x2.value, x3.value);
-                    pg[2 * j] = f16x2_bits(x0.grad, x1.grad);
-                    pg[2 * j + 1] = f16x2_bits(x2.grad, x3.grad);
-                }
-                store16x32(reinterpret_cast<__half*>(a.c0) + off, pa);
-                store16x32(reinterpret_cast<__half*>(a.c1) + off, pg);
-            }
-        } else if (EPI == TE_RESID) {
+        if (EPI == TE_RESID) {
             if (valid) {
                 const float4* b4 = reinterpret_cast<const float4*>(a.bias + (size_t)g * a.N + n0 + 32 * c);
                 float rr[32];
@@ -306,7 +309,6 @@ __device__ __forceinline__ void epilogue(const KArgs& a, int g, int m, bool vali
                 for (int j = 0; j < 32; ++j) v[j] = 0.f;
             }
             const float s = column_sums32(v, lane);
-            const int prow = mb * (BM / 32) + quad;
             a.colpart[((size_t)g * a.colpart_rows + prow) * a.N + n0 + 32 * c + lane] = s;
         } else if (EPI == TE_DRESID) {
             if (valid) {
@@ -346,12 +348,14 @@ __device__ __forceinline__ void epilogue(const KArgs& a, int g, int m, bool vali
     }
 }
 
-template <int EPI, bool A_MN, bool B_MN>
-__global__ void __launch_bounds__(EpiCfg<EPI>::THREADS, 1)
+template <int EPI, bool A_MN, bool B_MN, bool PAIR>
+__global__ void __launch_bounds__(KCfg<EPI, PAIR>::THREADS, 1)
 train_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC0, const __grid_constant__ CUtensorMap tmC1,
                      const KArgs args) {
-    constexpr int STAGES = EpiCfg<EPI>::STAGES;
+    using C = KCfg<EPI, PAIR>;
+    constexpr int STAGES = C::STAGES;
+    constexpr int STAGE_BYTES = C::STAGE_BYTES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -359,17 +363,20 @@ train_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     const uint32_t sA = base;
     const uint32_t sB = base + STAGES * A_BYTES;
     const uint32_t sEpi = base + STAGES * STAGE_BYTES;                 // TMA-store staging (1024-aligned)
-    const uint32_t bar0 = sEpi + EpiCfg<EPI>::EPI_BYTES;
+    const uint32_t bar0 = sEpi + C::EPI_BYTES;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto tfull_bar = [&](int x) { return bar0 + 8u * (2 * STAGES + x); };
     auto tempty_bar = [&](int x) { return bar0 + 8u * (2 * STAGES + 2 + x); };
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + STAGES * STAGE_BYTES + EpiCfg<EPI>::EPI_BYTES +
-                                                        8 * (2 * STAGES + 4));
+    uint32_t* tmem_holder =
+        reinterpret_cast<uint32_t*>(base_ptr + STAGES * STAGE_BYTES + C::EPI_BYTES + 8 * (2 * STAGES + 4));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;    // 0: issues the MMAs
+    const long long unit = PAIR ? (long long)(blockIdx.x >> 1) : (long long)blockIdx.x;
+    const long long nunits = PAIR ? (long long)(gridDim.x >> 1) : (long long)gridDim.x;
 
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
@@ -380,17 +387,23 @@ train_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(tfull_bar(x), 1);
-            mbar_init(tempty_bar(x), EpiCfg<EPI>::WARPS * 32);
+            mbar_init(tempty_bar(x), PAIR ? 2 * C::WARPS : C::WARPS * 32);
         }
         *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 2) {
-        tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(smem_u32(tmem_holder), TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync_all();    // both CTAs' barriers and TMEM exist before any cross-CTA use
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
     const int kblocks = (args.K + BK - 1) / BK;
@@ -400,32 +413,40 @@ train_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        for (long long tile = blockIdx.x; ok && tile < args.tiles; tile += gridDim.x) {
+        for (long long tile = unit; ok && tile < args.tiles; tile += nunits) {
             int g, mb, nb;
             tile_of(tile, args, g, mb, nb);
+            const int arow = mb * C::TM + BM * (int)rank;
+            const int brow = nb * BN + C::BROWS * (int)rank;
             for (int kb = 0; kb < kblocks; ++kb) {
                 if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, args.err, args.timeout_ns)) {
                     ok = false;
                     break;
                 }
                 if (lane == 0) {
-                    const uint32_t fb = full_bar(stage);
-                    mbar_arrive_expect_tx(fb, (uint32_t)STAGE_BYTES);
+                    // the even CTA's full barrier counts both CTAs' bytes
+                    const uint32_t fb = PAIR ? mapa_shared(full_bar(stage), 0) : full_bar(stage);
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), (uint32_t)((PAIR ? 2 : 1) * STAGE_BYTES));
                     const uint32_t a_dst = sA + stage * A_BYTES;
-                    const uint32_t b_dst = sB + stage * B_BYTES;
+                    const uint32_t b_dst = sB + stage * C::B_BYTES;
+                    auto load = [&](const CUtensorMap* m, uint32_t dst, int x, int y) {
+                        if constexpr (PAIR)
+                            tma_load_3d_pair(m, dst, fb, x, y, g);
+                        else
+                            tma_load_3d(m, dst, fb, x, y, g);
+                    };
                     if (A_MN) {
 #pragma unroll
-                        for (int i = 0; i < BM / 64; ++i)
-                            tma_load_3d(&tmA, a_dst + i * MN_BOX_BYTES, fb, mb * BM + 64 * i, kb * BK, g);
+                        for (int i = 0; i < BM / 64; ++i) load(&tmA, a_dst + i * MN_BOX_BYTES, arow + 64 * i, kb * BK);
                     } else {
-                        tma_load_3d(&tmA, a_dst, fb, kb * BK, mb * BM, g);
+                        load(&tmA, a_dst, kb * BK, arow);
                     }
                     if (B_MN) {
 #pragma unroll
-                        for (int i = 0; i < BN / 64; ++i)
-                            tma_load_3d(&tmB, b_dst + i * MN_BOX_BYTES, fb, nb * BN + 64 * i, kb * BK, g);
+                        for (int i = 0; i < C::BROWS / 64; ++i)
+                            load(&tmB, b_dst + i * MN_BOX_BYTES, brow + 64 * i, kb * BK);
                     } else {
-                        tma_load_3d(&tmB, b_dst, fb, kb * BK, nb * BN, g);
+                        load(&tmB, b_dst, kb * BK, brow);
                     }
                 }
                 __syncwarp();
@@ -435,9 +456,9 @@ train_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 }
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 && rank == 0) {
         // ------------------------------ MMA issuer --------------------------------
-        constexpr uint32_t idesc = idesc_f16(BM, BN, A_MN, B_MN);
+        constexpr uint32_t idesc = idesc_f16(C::TM, BN, A_MN, B_MN);
         // per 16-deep step: K-major operands advance 32 bytes inside the swizzled
         // row, MN-major operands 16 rows of 128 bytes
         constexpr uint32_t a_step = A_MN ? 2048u : 32u, b_step = B_MN ? 2048u : 32u;
@@ -447,7 +468,7 @@ train_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
-        for (long long tile = blockIdx.x; ok && tile < args.tiles; tile += gridDim.x) {
+        for (long long tile = unit; ok && tile < args.tiles; tile += nunits) {
             if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.err, args.timeout_ns)) {
                 ok = false;
                 break;
@@ -461,13 +482,21 @@ train_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 }
                 tc_fence_after();
                 const uint32_t a0 = sA + stage * A_BYTES;
-                const uint32_t b0 = sB + stage * B_BYTES;
+                const uint32_t b0 = sB + stage * C::B_BYTES;
                 if (lane == 0) {
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)
-                        umma_f16_any(d_tmem, sw128_desc(a0 + a_step * k, a_lbo, 1024u),
-                                  sw128_desc(b0 + b_step * k, b_lbo, 1024u), idesc, (kb > 0 || k > 0) ? 1u : 0u);
-                    umma_commit(empty_bar(stage));
+                    for (int k = 0; k < BK / 16; ++k) {
+                        const uint64_t ad = sw128_desc(a0 + a_step * k, a_lbo, 1024u);
+                        const uint64_t bd = sw128_desc(b0 + b_step * k, b_lbo, 1024u);
+                        if constexpr (PAIR)
+                            umma_f16_pair(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                        else
+                            umma_f16_any(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                    }
+                    if constexpr (PAIR)
+                        umma_commit_pair_mc(empty_bar(stage), (uint16_t)0x3);
+                    else
+                        umma_commit(empty_bar(stage));
                 }
                 __syncwarp();
                 if (++stage == STAGES) {
@@ -476,7 +505,12 @@ train_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 }
             }
             if (!ok) break;
-            if (lane == 0) umma_commit(tfull_bar(acc));
+            if (lane == 0) {
+                if constexpr (PAIR)
+                    umma_commit_pair_mc(tfull_bar(acc), (uint16_t)0x3);
+                else
+                    umma_commit(tfull_bar(acc));
+            }
             __syncwarp();
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
@@ -485,38 +519,58 @@ train_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         // ------------------------------ epilogue ----------------------------------
         const int ew = warp - 4;
         const int quad = warp & 3;
-        const int half = ew >> 2;               // which group of EpiCfg<EPI>::COLS columns
+        const int half = ew >> 2;               // which group of C::COLS columns
         const uint32_t stage = sEpi + (uint32_t)ew * 8192u;
+        const uint32_t sbias = sEpi + (uint32_t)C::WARPS * 8192u + (uint32_t)ew * (4u * C::COLS);
         int sbuf = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (long long tile = blockIdx.x; tile < args.tiles; tile += gridDim.x) {
+        for (long long tile = unit; tile < args.tiles; tile += nunits) {
             int g, mb, nb;
             tile_of(tile, args, g, mb, nb);
+            float4 bias4;
+            if constexpr (C::TMA_OUT)     // this warp's bias slice, loaded during the wait
+                bias4 = __ldg(reinterpret_cast<const float4*>(args.bias + (size_t)g * args.N + nb * BN +
+                                                              half * C::COLS) + lane);
             if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err, args.timeout_ns)) break;
             tc_fence_after();
-            const int m = mb * BM + quad * 32 + lane;
+            if constexpr (C::TMA_OUT) {
+                __syncwarp();                           // the previous tile's reads of the slice are done
+                st_shared_v4(sbias + 16u * lane, __float_as_uint(bias4.x), __float_as_uint(bias4.y),
+                             __float_as_uint(bias4.z), __float_as_uint(bias4.w));
+                __syncwarp();
+            }
+            const int m = mb * C::TM + BM * (int)rank + quad * 32 + lane;
             const uint32_t tbase =
-                tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN + half * EpiCfg<EPI>::COLS);
-            if constexpr (EpiCfg<EPI>::TMA_OUT)
-                epilogue_gelu2_tma(args, &tmC0, &tmC1, g, m - lane, tbase, nb * BN + half * EpiCfg<EPI>::COLS, lane,
-                                   stage, sbuf);
+                tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN + half * C::COLS);
+            if constexpr (C::TMA_OUT)
+                epilogue_gelu2_tma(args, &tmC0, &tmC1, g, m - lane, tbase, nb * BN + half * C::COLS, lane, stage,
+                                   sbias, sbuf);
             else
-                epilogue<EPI>(args, g, m, m < args.m_valid, tbase, nb * BN + half * EpiCfg<EPI>::COLS, lane, quad,
-                              mb);
+                epilogue<EPI>(args, g, m, m < args.m_valid, tbase, nb * BN + half * C::COLS, lane,
+                              (mb * C::TM + BM * (int)rank) / kTrainColpartRows + quad);
             tc_fence_before();
-            mbar_arrive(tempty_bar(acc));
+            if constexpr (PAIR) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+            } else {
+                mbar_arrive(tempty_bar(acc));
+            }
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
-        if (EpiCfg<EPI>::TMA_OUT && lane == 0) bulk_wait_group<0>();   // this warp's tensor stores have landed
+        if (C::TMA_OUT && lane == 0) bulk_wait_group<0>();   // this warp's tensor stores have landed
     }
 
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync_all();    // no CTA leaves while its peer may still touch its memory
     if (warp == 2) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        if constexpr (PAIR)
+            tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, TMEM_COLS);
     }
 }
 
@@ -562,29 +616,56 @@ bool make_map_out(CUtensorMap* m, void* ptr, int N, int rows, int G, long long l
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int EPI, bool A_MN, bool B_MN>
+template <int EPI, bool A_MN, bool B_MN, bool PAIR>
 cudaError_t run(const TrainGemm& g, const KArgs& ka, int num_sms, cudaStream_t s) {
+    using C = KCfg<EPI, PAIR>;
     CUtensorMap mA, mB, mC0, mC1;
     if (!make_map(&mA, g.a, g.G, A_MN ? BK : BM)) return cudaErrorInvalidValue;
-    if (!make_map(&mB, g.b, g.G, B_MN ? BK : BN)) return cudaErrorInvalidValue;
-    if constexpr (EpiCfg<EPI>::TMA_OUT) {
+    if (!make_map(&mB, g.b, g.G, B_MN ? BK : C::BROWS)) return cudaErrorInvalidValue;
+    if constexpr (C::TMA_OUT) {
         if (!make_map_out(&mC0, g.c0, g.N, g.m_valid, g.G, ka.c_ld, g.c_gpitch)) return cudaErrorInvalidValue;
         if (!make_map_out(&mC1, g.c1, g.N, g.m_valid, g.G, ka.c_ld, g.c_gpitch)) return cudaErrorInvalidValue;
     } else {
         mC0 = mA;   // unused
         mC1 = mA;
     }
-    auto k = train_gemm_tc_kernel<EPI, A_MN, B_MN>;
-    constexpr int smem = EpiCfg<EPI>::SMEM_BYTES;
+    auto k = train_gemm_tc_kernel<EPI, A_MN, B_MN, PAIR>;
+    constexpr int smem = C::SMEM_BYTES;
     static bool attr_done = false;
     if (!attr_done) {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    const long long grid = ka.tiles < num_sms ? ka.tiles : num_sms;
-    k<<<(int)grid, EpiCfg<EPI>::THREADS, smem, s>>>(mA, mB, mC0, mC1, ka);
-    return cudaGetLastError();
+    // persistent: one CTA (or CTA pair) per SM (pair of SMs), at most one per tile
+    const long long units = PAIR ? num_sms / 2 : num_sms;
+    const long long grid = (ka.tiles < units ? ka.tiles : units) * (PAIR ? 2 : 1);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = PAIR ? 2 : 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = PAIR ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k, mA, mB, mC0, mC1, ka);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// CTA pairs where they measured faster at the 1B shape (B = 4096, per-launch
+// device time): the weight gradients, both operands MN-major with six TMA
+// boxes per single-CTA stage (1658 -> 1595 us), and the Gelu / Gelu' product,
+// whose epilogue staging leaves a single CTA only 3 stages (about 1.84 ->
+// 1.71 ms).  The other products ran slower as pairs (Z 1406 -> 1539 us, dU
+// 1756 -> 1815, dS 1529 -> 1606) and keep one CTA per tile.  Pairs need at
+// least two 128-row blocks (and whole 256-row tiles of an MN-major A).
+bool use_pair(int epi, const TrainGemm& g, int num_sms) {
+    const bool wanted = epi == TE_GELU2 || (epi == TE_F32 && g.a.mn && g.b.mn);
+    return wanted && num_sms >= 2 && g.m_valid > BM && (!g.a.mn || g.M % (2 * BM) == 0);
 }
 
 }  // namespace ttc
@@ -606,15 +687,22 @@ bool train_tc_supported(const TrainGemm& g) {
     return true;
 }
 
+int train_colpart_rows(const TrainGemm& g, int num_sms) {
+    const int tm = ttc::use_pair(TE_DGELU, g, num_sms) ? 2 * ttc::BM : ttc::BM;
+    return (g.m_valid + tm - 1) / tm * (tm / kTrainColpartRows);
+}
+
 cudaError_t launch_train_gemm_tc(int epi, const TrainGemm& g, int num_sms, cudaStream_t s) {
     if (!train_tc_supported(g)) return cudaErrorNotSupported;
+    const bool pair = ttc::use_pair(epi, g, num_sms);
+    const int tm = pair ? 2 * ttc::BM : ttc::BM;
     ttc::KArgs ka{};
     ka.G = g.G;
     ka.M = g.M;
     ka.N = g.N;
     ka.K = g.K;
     ka.m_valid = g.m_valid;
-    ka.m_tiles = (g.m_valid + ttc::BM - 1) / ttc::BM;
+    ka.m_tiles = (g.m_valid + tm - 1) / tm;
     ka.n_tiles = g.N / ttc::BN;
     ka.tiles = (long long)g.G * ka.m_tiles * ka.n_tiles;
     ka.c_gpitch = g.c_gpitch;
@@ -625,33 +713,36 @@ cudaError_t launch_train_gemm_tc(int epi, const TrainGemm& g, int num_sms, cudaS
     ka.bias = g.bias;
     ka.inv_scale = g.inv_scale;
     ka.colpart = g.colpart;
-    ka.colpart_rows = ka.m_tiles * (ttc::BM / kTrainColpartRows);
+    ka.colpart_rows = train_colpart_rows(g, num_sms);
     ka.err = g.err;
     ka.timeout_ns = g.timeout_ns;
     if (ka.tiles == 0) return cudaSuccess;
     const bool amn = g.a.mn, bmn = g.b.mn;
+#define RM_TRAIN_RUN(E, AMN, BMN) \
+    return pair ? ttc::run<E, AMN, BMN, true>(g, ka, num_sms, s) : ttc::run<E, AMN, BMN, false>(g, ka, num_sms, s)
     switch (epi) {
         case TE_GELU2:
-            if (!amn && bmn) return ttc::run<TE_GELU2, false, true>(g, ka, num_sms, s);
+            if (!amn && bmn) RM_TRAIN_RUN(TE_GELU2, false, true);
             break;
         case TE_RESID:
-            if (!amn && bmn) return ttc::run<TE_RESID, false, true>(g, ka, num_sms, s);
+            if (!amn && bmn) RM_TRAIN_RUN(TE_RESID, false, true);
             break;
         case TE_DGELU:
-            if (!amn && !bmn) return ttc::run<TE_DGELU, false, false>(g, ka, num_sms, s);
+            if (!amn && !bmn) RM_TRAIN_RUN(TE_DGELU, false, false);
             break;
         case TE_DRESID:
-            if (!amn && !bmn) return ttc::run<TE_DRESID, false, false>(g, ka, num_sms, s);
+            if (!amn && !bmn) RM_TRAIN_RUN(TE_DRESID, false, false);
             break;
         case TE_F32:
-            if (amn && bmn) return ttc::run<TE_F32, true, true>(g, ka, num_sms, s);
-            if (!amn && !bmn) return ttc::run<TE_F32, false, false>(g, ka, num_sms, s);
+            if (amn && bmn) RM_TRAIN_RUN(TE_F32, true, true);
+            if (!amn && !bmn) RM_TRAIN_RUN(TE_F32, false, false);
             break;
         case TE_BIAS_IO:
-            if (!amn && bmn) return ttc::run<TE_BIAS_IO, false, true>(g, ka, num_sms, s);
+            if (!amn && bmn) RM_TRAIN_RUN(TE_BIAS_IO, false, true);
             break;
         default: break;
     }
+#undef RM_TRAIN_RUN
     return cudaErrorNotSupported;
 }
 
