@@ -7,7 +7,9 @@ import this package.  It shares no code with the CUDA library and never
 imports it.
 
 Sources: "RankMixer: Scaling Up Ranking Models in Industrial Recommenders",
-section 3.1 Eq. 1, section 3.3 Eq. 3-9, section 3.4 Eq. 10; "RankMixer 详解（1）",
+section 3.1 Eq. 1, section 3.3 Eq. 3-9, section 3.4 Eq. 10; "UniMixer: A Unified
+Architecture for Scaling Laws in Recommendation Systems", section 4.3 Eq. 11-15
+and Appendices A-B (UniMixing); "RankMixer 详解（1）",
 sections 3.1, 3.3, 4.1, 5.1 and 5.2 (the backward pass).  Every function below forwards to the C loop
 nest of the same name; the docstrings say which passage each follows.
 
@@ -65,6 +67,9 @@ def _load():
             lib.oracle_tokenize.argtypes = [dp, dp, dp, dp, i, i, i, i]
             lib.oracle_tokenize_backward.argtypes = [dp] * 6 + [i, i, i, i]
             lib.oracle_moe_pffn_train.argtypes = [dp] * 14 + [i, i, i, i, i]
+            lib.oracle_sinkhorn.argtypes = [dp, dp, i, i, ctypes.c_double, i]
+            lib.oracle_unimixing.argtypes = [dp, dp, dp, dp, i, i, i]
+            lib.oracle_stack_forward_unimix.argtypes = [dp] * 13 + [i, ctypes.c_double, i, i, i, i, i]
             lib.oracle_num_threads.restype = ctypes.c_int
             lib.oracle_set_num_threads.argtypes = [i]
             _lib = lib
@@ -173,6 +178,60 @@ def stack_forward(X0, layers: list, eps: float = 1e-5, return_XL: bool = False):
     _load().oracle_stack_forward(_p(X0), _p(pooled), xl_ptr, _p(cat["W1"]), _p(cat["b1"]), _p(cat["W2"]),
                                  _p(cat["b2"]), _p(cat["ln1_g"]), _p(cat["ln1_b"]), _p(cat["ln2_g"]),
                                  _p(cat["ln2_b"]), float(eps), B, T, D, F, L)
+    return (pooled, XL) if return_XL else pooled
+
+
+def sinkhorn(W, tau: float, iters: int) -> np.ndarray:
+    """Constrained UniMixing weights ("UniMixer", section 4.3 Eq. 15): for each
+    n x n matrix in ``W`` ([..., n, n]), Sinkhorn-Knopp of (W + W^T) / (2 tau):
+    elementwise exp, then ``iters`` rounds of row then column normalisation."""
+    W = _f64(W)
+    n = W.shape[-1]
+    if W.shape[-2] != n:
+        raise ValueError("square matrices expected")
+    count = W.size // (n * n)
+    out = np.empty_like(W)
+    _load().oracle_sinkhorn(_p(W), _p(out), count, n, float(tau), int(iters))
+    return out
+
+
+def unimixing(X, WG, WB) -> np.ndarray:
+    """UniMixing ("UniMixer", section 4.3 Eq. 12-14): flatten each sample of X
+    ([B, ...], L values), cut it into nb = L / bs blocks x_j, h_j = x_j WB[j],
+    out_i = sum_j WG[i, j] h_j.  WG [nb, nb], WB [nb, bs, bs] (constrained
+    weights); returns X's shape."""
+    X = _f64(X)
+    WG, WB = _f64(WG), _f64(WB)
+    B = X.shape[0]
+    L = X.size // B
+    nb, bs = WB.shape[0], WB.shape[-1]
+    if nb * bs != L or WG.shape != (nb, nb) or WB.shape != (nb, bs, bs):
+        raise ValueError("UniMixing shapes: WG [nb, nb], WB [nb, bs, bs] with nb * bs = L")
+    Y = np.empty_like(X)
+    _load().oracle_unimixing(_p(X), _p(Y), _p(WG), _p(WB), B, L, bs)
+    return Y
+
+
+def stack_forward_unimix(X0, layers: list, eps: float = 1e-5, return_XL: bool = False):
+    """``stack_forward`` with UniMixing ("UniMixer", section 4.3 Eq. 14) in place of
+    TokenMixing in every layer: each layer dict also holds the constrained
+    weights WG [nb, nb] and WB [nb, bs, bs] (nb * bs = T * D)."""
+    X0 = _f64(X0)
+    B, T, D = X0.shape
+    L = len(layers)
+    keys = ("W1", "b1", "W2", "b2", "ln1_g", "ln1_b", "ln2_g", "ln2_b", "WG", "WB")
+    cat = {k: _f64(np.stack([np.asarray(l[k], dtype=np.float64) for l in layers])) for k in keys}
+    F = cat["W1"].shape[-1]
+    nb, bs = cat["WB"].shape[1], cat["WB"].shape[-1]
+    if nb * bs != T * D or cat["WG"].shape[1:] != (nb, nb):
+        raise ValueError("UniMixing shapes: WG [nb, nb], WB [nb, bs, bs] with nb * bs = T * D")
+    pooled = np.empty((B, D), dtype=np.float64)
+    XL = np.empty_like(X0) if return_XL else None
+    xl_ptr = _p(XL) if return_XL else ctypes.POINTER(ctypes.c_double)()
+    _load().oracle_stack_forward_unimix(_p(X0), _p(pooled), xl_ptr, _p(cat["W1"]), _p(cat["b1"]), _p(cat["W2"]),
+                                        _p(cat["b2"]), _p(cat["ln1_g"]), _p(cat["ln1_b"]), _p(cat["ln2_g"]),
+                                        _p(cat["ln2_b"]), _p(cat["WG"]), _p(cat["WB"]), bs, float(eps), B, T, D,
+                                        F, L)
     return (pooled, XL) if return_XL else pooled
 
 

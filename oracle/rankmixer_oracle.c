@@ -11,6 +11,10 @@
  *         (Zhu et al., ByteDance), section 3.1 Eq. 1, section 3.3.1 Eq. 3-5,
  *         section 3.3.2 Eq. 6-9, section 3.4 Eq. 10, section 3.5 Eq. 12.
  *   [TU]  "6.4 Rankmixer: 硬件效率优化", section 6.4.4 (DTSI-MoE routers).
+ *   [UM]  "UniMixer: A Unified Architecture for Scaling Laws in
+ *         Recommendation Systems", section 4.3 Eq. 11-15 (UniMixing and its
+ *         constrained weights), Appendix A (the TokenMixer as a Kronecker
+ *         product), Appendix B (the computation flow, Eq. 24-29).
  *   [WT]  "RankMixer 详解（1）：特征分组与完整计算流程", section 3.1 (the
  *         element map of TokenMixing), section 3.3 (LayerNorm definition),
  *         section 4.1 (GELU = u*Phi(u), row-vector FFN), section 5.1 (mean
@@ -144,24 +148,105 @@ ORACLE_API void oracle_pffn(const double *S, const double *W1, const double *b1,
 }
 
 /* ------------------------------------------------------------------ */
+/* UniMixing, [UM] section 4.3.                                        */
+/*                                                                    */
+/* Constrained weights, Eq. 15: each n x n matrix W is symmetrised,     */
+/* W~ = (W + W^T) / 2, and handed to Sinkhorn-Knopp at temperature tau: */
+/* every element becomes exp(W~ / tau) (positive), then `iters` rounds  */
+/* each divide every row by its sum and then every column by its sum.   */
+/* The pages fix neither the round count nor which axis goes first;     */
+/* here a round is rows, then columns.                                  */
+/* ------------------------------------------------------------------ */
+ORACLE_API void oracle_sinkhorn(const double *W, double *out, int count, int n, double tau, int iters)
+{
+    const size_t nn = (size_t)n * n;
+    for (int c = 0; c < count; ++c) {
+        const double *w = W + (size_t)c * nn;
+        double *o = out + (size_t)c * nn;
+        for (int i = 0; i < n; ++i)
+            for (int j = 0; j < n; ++j)
+                o[(size_t)i * n + j] = exp(0.5 * (w[(size_t)i * n + j] + w[(size_t)j * n + i]) / tau);
+        for (int it = 0; it < iters; ++it) {
+            for (int i = 0; i < n; ++i) {
+                double sum = 0.0;
+                for (int j = 0; j < n; ++j) sum += o[(size_t)i * n + j];
+                for (int j = 0; j < n; ++j) o[(size_t)i * n + j] /= sum;
+            }
+            for (int j = 0; j < n; ++j) {
+                double sum = 0.0;
+                for (int i = 0; i < n; ++i) sum += o[(size_t)i * n + j];
+                for (int i = 0; i < n; ++i) o[(size_t)i * n + j] /= sum;
+            }
+        }
+    }
+}
+
+/* UniMixing of one flattened sample, [UM] Eq. 12-14 (the optimised flow,  */
+/* Appendix B Eq. 29): flatten(X) (length L) is cut into nb = L / bs row   */
+/* vectors x_j; the local step is h_j = x_j WB_j (bs x bs, one per block); */
+/* the global step is out_i = sum_j WG[i][j] h_j; the output is            */
+/* out_0 | out_1 | ... | out_{nb-1}, reshaped back to X's shape.           */
+/* WG [nb][nb], WB [nb][bs][bs] (row s, column r), h: nb * bs scratch.     */
+static void unimix_sample(const double *x, double *y, const double *WG, const double *WB, int L, int bs,
+                          double *h)
+{
+    const int nb = L / bs;
+    for (int j = 0; j < nb; ++j)
+        for (int r = 0; r < bs; ++r) {
+            double acc = 0.0;
+            for (int s = 0; s < bs; ++s)
+                acc += x[(size_t)j * bs + s] * WB[((size_t)j * bs + s) * bs + r];
+            h[(size_t)j * bs + r] = acc;
+        }
+    for (int i = 0; i < nb; ++i)
+        for (int r = 0; r < bs; ++r) {
+            double acc = 0.0;
+            for (int j = 0; j < nb; ++j) acc += WG[(size_t)i * nb + j] * h[(size_t)j * bs + r];
+            y[(size_t)i * bs + r] = acc;
+        }
+}
+
+/* Y[b] = UniMixing(X[b]) for B samples of length L (block size bs). */
+ORACLE_API void oracle_unimixing(const double *X, double *Y, const double *WG, const double *WB, int B, int L,
+                                 int bs)
+{
+#pragma omp parallel
+    {
+        double *h = (double *)malloc(sizeof(double) * (size_t)L);
+#pragma omp for schedule(static)
+        for (int b = 0; b < B; ++b)
+            unimix_sample(X + (size_t)b * L, Y + (size_t)b * L, WG, WB, L, bs, h);
+        free(h);
+    }
+}
+
+/* ------------------------------------------------------------------ */
 /* One RankMixer block on one sample, [RM] Eq. 1:                       */
 /*   S  = LN1(TokenMixing(X) + X)                                       */
 /*   X' = LN2(PFFN(S) + S)                                              */
 /* S_out may be NULL.  Requires H = T (the residual needs equal shape). */
+/* With WG non-NULL the mixing is UniMixing with constrained weights    */
+/* WG, WB and block size bs ([UM] Eq. 14) in place of TokenMixing; the  */
+/* rest of the block is unchanged.                                      */
 /* ------------------------------------------------------------------ */
 static void block_sample(const double *X, double *Xout, double *S_keep,
                          const double *W1, const double *b1, const double *W2, const double *b2,
                          const double *g1, const double *be1, const double *g2, const double *be2,
+                         const double *WG, const double *WB, int bs,
                          double eps, int T, int D, int F, double *work)
 {
     const size_t TD = (size_t)T * D;
     double *M = work;            /* [T][D] mixed   */
     double *S = M + TD;          /* [T][D] LN1 out */
     double *Y = S + TD;          /* [T][D] residual sums */
-    double *a = Y + TD;          /* [F]   hidden   */
+    double *hb = Y + TD;         /* [T*D] UniMixing local outputs */
+    double *a = hb + TD;         /* [F]   hidden   */
     double *v = a + F;           /* [D]   FFN out  */
 
-    mix_sample(X, M, T, D, T);
+    if (WG)
+        unimix_sample(X, M, WG, WB, (int)TD, bs, hb);
+    else
+        mix_sample(X, M, T, D, T);
     for (size_t i = 0; i < TD; ++i) Y[i] = M[i] + X[i];
     for (int t = 0; t < T; ++t) layernorm_row(Y + (size_t)t * D, g1, be1, eps, S + (size_t)t * D, D);
 
@@ -184,11 +269,11 @@ ORACLE_API void oracle_block_forward(const double *X, double *Xout, double *S_ou
     const size_t TD = (size_t)T * D;
 #pragma omp parallel
     {
-        double *work = (double *)malloc(sizeof(double) * (3 * TD + (size_t)F + (size_t)D));
+        double *work = (double *)malloc(sizeof(double) * (4 * TD + (size_t)F + (size_t)D));
 #pragma omp for schedule(static)
         for (int b = 0; b < B; ++b)
             block_sample(X + b * TD, Xout + b * TD, S_out ? S_out + b * TD : NULL,
-                         W1, b1, W2, b2, g1, be1, g2, be2, eps, T, D, F, work);
+                         W1, b1, W2, b2, g1, be1, g2, be2, NULL, NULL, 0, eps, T, D, F, work);
         free(work);
     }
 }
@@ -209,17 +294,18 @@ ORACLE_API void oracle_mean_pool(const double *X, double *o, int B, int T, int D
 /* the factor L in Eq. 12), then mean pooling.  Per-layer parameter     */
 /* arrays are concatenated along a leading layer axis.  XL may be NULL. */
 /* ------------------------------------------------------------------ */
-ORACLE_API void oracle_stack_forward(const double *X0, double *pooled, double *XL,
-                                     const double *W1, const double *b1,
-                                     const double *W2, const double *b2,
-                                     const double *g1, const double *be1,
-                                     const double *g2, const double *be2,
-                                     double eps, int B, int T, int D, int F, int L)
+static void stack_forward(const double *X0, double *pooled, double *XL,
+                          const double *W1, const double *b1,
+                          const double *W2, const double *b2,
+                          const double *g1, const double *be1,
+                          const double *g2, const double *be2,
+                          const double *WG, const double *WB, int bs,
+                          double eps, int B, int T, int D, int F, int L)
 {
     const size_t TD = (size_t)T * D;
 #pragma omp parallel
     {
-        double *work = (double *)malloc(sizeof(double) * (3 * TD + (size_t)F + (size_t)D));
+        double *work = (double *)malloc(sizeof(double) * (4 * TD + (size_t)F + (size_t)D));
         double *cur = (double *)malloc(sizeof(double) * TD);
         double *nxt = (double *)malloc(sizeof(double) * TD);
 #pragma omp for schedule(static)
@@ -231,7 +317,8 @@ ORACLE_API void oracle_stack_forward(const double *X0, double *pooled, double *X
                              W2 + (size_t)n * T * F * D, b2 + (size_t)n * T * D,
                              g1 + (size_t)n * D, be1 + (size_t)n * D,
                              g2 + (size_t)n * D, be2 + (size_t)n * D,
-                             eps, T, D, F, work);
+                             WG ? WG + (size_t)n * (T * D / bs) * (T * D / bs) : NULL,
+                             WB ? WB + (size_t)n * T * D * bs : NULL, bs, eps, T, D, F, work);
                 double *tmp = cur; cur = nxt; nxt = tmp;
             }
             for (int j = 0; j < D; ++j) {
@@ -243,6 +330,30 @@ ORACLE_API void oracle_stack_forward(const double *X0, double *pooled, double *X
         }
         free(work); free(cur); free(nxt);
     }
+}
+
+ORACLE_API void oracle_stack_forward(const double *X0, double *pooled, double *XL,
+                                     const double *W1, const double *b1,
+                                     const double *W2, const double *b2,
+                                     const double *g1, const double *be1,
+                                     const double *g2, const double *be2,
+                                     double eps, int B, int T, int D, int F, int L)
+{
+    stack_forward(X0, pooled, XL, W1, b1, W2, b2, g1, be1, g2, be2, NULL, NULL, 0, eps, B, T, D, F, L);
+}
+
+/* The stack with UniMixing in every layer ([UM] Eq. 14 in place of [RM]   */
+/* Eq. 3-4): WG [L][nb][nb] and WB [L][nb][bs][bs] are the constrained      */
+/* weights (see oracle_sinkhorn), nb = T * D / bs.                          */
+ORACLE_API void oracle_stack_forward_unimix(const double *X0, double *pooled, double *XL,
+                                            const double *W1, const double *b1,
+                                            const double *W2, const double *b2,
+                                            const double *g1, const double *be1,
+                                            const double *g2, const double *be2,
+                                            const double *WG, const double *WB, int bs,
+                                            double eps, int B, int T, int D, int F, int L)
+{
+    stack_forward(X0, pooled, XL, W1, b1, W2, b2, g1, be1, g2, be2, WG, WB, bs, eps, B, T, D, F, L);
 }
 
 /* ------------------------------------------------------------------ */
