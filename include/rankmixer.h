@@ -168,7 +168,8 @@ typedef enum rm_kernel_kind {
     RM_K_BWD_ROWS = 14,    /* backward: LN2 and LN1 + mixing backward, bias / affine reductions */
     RM_K_TOKENIZE = 15,    /* feature tokenization: per-token projection of the embedding slices */
     RM_K_HEAD = 16,        /* prediction head on the pooled output */
-    RM_K_COUNT = 17
+    RM_K_UNIMIX = 17,      /* UniMixing: local block products, global product, residual + LN1 */
+    RM_K_COUNT = 18
 } rm_kernel_kind;
 
 typedef struct rm_kernel_stat {
@@ -305,6 +306,37 @@ RM_API rm_status rm_stack_backward(rm_ctx *ctx, const void *X0, const float *dpo
  * no context.  Asynchronous on `stream`. */
 RM_API rm_status rm_head_forward(const float *pooled, const float *w, float b, const float *y, float *p,
                                  float *loss, float *dpooled, int B, int D, int mean_loss, void *stream);
+
+/* UniMixing ("UniMixer: A Unified Architecture for Scaling Laws in
+ * Recommendation Systems", section 4.3 Eq. 11-15): a learned block-Kronecker
+ * mixing in place of a layer's TokenMixing.  Per sample, flatten(X) (L = T D
+ * values) is cut into nb = L / bs blocks x_j of bs values and
+ *   h_j = x_j WB_j,   out_i = sum_j WG[i][j] h_j,   UniMixing(X) = out_0 | ... | out_{nb-1}
+ * with the constrained weights of Eq. 15: each raw matrix W (WG, and every WB_j)
+ * is symmetrised, (W + W^T) / 2, divided by the temperature tau and passed to
+ * Sinkhorn-Knopp: elementwise exp, then `iters` rounds of dividing every row by
+ * its sum and then every column by its sum.  With bs = D / T, WG the block
+ * permutation of TokenMixing and WB_j = I it reproduces TokenMixing exactly
+ * (the same page, Appendix A).  The layer then runs S = LN1(X + UniMixing(X))
+ * and the rest of the block unchanged.
+ *
+ * rm_set_unimixing: WG device float32 [nb][nb], WB device float32 [nb][bs][bs]
+ * (row s, column r of WB_j at WB[j][s][r]), raw (unconstrained); bs must
+ * divide T D; tau > 0; iters >= 0; D <= 1536.  Computes the constrained
+ * weights on the device (float32, in the log domain: P = exp(C + f_i + g_j)
+ * with C = (W + W^T) / (2 tau) and f, g the row and column log-scalings, the
+ * same values as the alternating normalisation) and keeps them in the context;
+ * the global product runs on fp16 copies in bf16 contexts.  Synchronous: drains
+ * `stream` first, returns when done.  Replaces an earlier setting of the layer.
+ * Training calls return RM_ERR_UNSUPPORTED on contexts with UniMixing layers.
+ * rm_unimixing_weights: copies the constrained weights (device float32, same
+ * layouts; either output may be NULL).  rm_unimixing: Y = UniMixing(X) of
+ * layer `layer`, X and Y device [B][T][D] in the context dtype.  Asynchronous
+ * on `stream`. */
+RM_API rm_status rm_set_unimixing(rm_ctx *ctx, int layer, const float *WG, const float *WB, int bs, float tau,
+                                  int iters, void *stream);
+RM_API rm_status rm_unimixing_weights(rm_ctx *ctx, int layer, float *WG_out, float *WB_out, void *stream);
+RM_API rm_status rm_unimixing(rm_ctx *ctx, int layer, const void *X, void *Y, int B, void *stream);
 
 /* Feature tokenization ("RankMixer" section 3.2 Eq. 2; "RankMixer 详解（1）"
  * section 2.4): token t of a sample is the t-th slice of d coordinates of its

@@ -35,7 +35,7 @@ RM_PATH_TCGEN05 = 2
 # rm_kernel_kind
 KERNEL_KINDS = ["mix_ln1", "gemm1", "gemm2", "ln2_out", "pool", "rowstats", "moe_route", "moe_gemm1",
                 "moe_gemm2", "misc", "moe_combine", "bwd_recompute", "bwd_dgrad", "bwd_wgrad", "bwd_rows",
-                "tokenize", "head"]
+                "tokenize", "head", "unimix"]
 RM_K_COUNT = len(KERNEL_KINDS)
 
 EXPORTED = ["rm_create", "rm_destroy", "rm_block_forward", "rm_stack_forward", "rm_stack_forward_host",
@@ -43,7 +43,8 @@ EXPORTED = ["rm_create", "rm_destroy", "rm_block_forward", "rm_stack_forward", "
             "rm_profile_read", "rm_debug_wait_timeout", "rm_last_error", "rm_abi_version",
             "rm_block_forward_noalloc", "rm_debug_gelu", "rm_block_backward", "rm_stack_backward",
             "rm_debug_gelu_grad", "rm_stack_forward_train", "rm_stack_backward_saved", "rm_head_forward",
-            "rm_set_tokenizer", "rm_tokenize", "rm_score", "rm_moe_pffn_forward_train", "rm_tokenize_backward"]
+            "rm_set_tokenizer", "rm_tokenize", "rm_score", "rm_moe_pffn_forward_train", "rm_tokenize_backward",
+            "rm_set_unimixing", "rm_unimixing_weights", "rm_unimixing"]
 
 
 class rm_config(ctypes.Structure):
@@ -123,6 +124,9 @@ def load() -> ctypes.CDLL:
         "rm_score": (st, [vp, vp, vp, ctypes.c_float, vp, i, vp]),
         "rm_moe_pffn_forward_train": (st, [vp, i, vp, vp, vp, vp, vp, vp, i, vp]),
         "rm_stack_backward_saved": (st, [vp, vp, vp, ctypes.POINTER(rm_layer_grads), i, vp]),
+        "rm_set_unimixing": (st, [vp, i, vp, vp, i, ctypes.c_float, i, vp]),
+        "rm_unimixing_weights": (st, [vp, i, vp, vp, vp]),
+        "rm_unimixing": (st, [vp, i, vp, vp, i, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -250,6 +254,18 @@ def rm_tokenize_backward(ctx: int, E: int, dX0: int, dE: int | None, dW: int, db
 
 def rm_score(ctx: int, E: int, head_w: int, head_b: float, p: int, B: int, stream: int) -> None:
     check(load().rm_score(ctx, E, head_w, head_b, p, B, stream), "rm_score")
+
+
+def rm_set_unimixing(ctx: int, layer: int, WG: int, WB: int, bs: int, tau: float, iters: int, stream: int) -> None:
+    check(load().rm_set_unimixing(ctx, layer, WG, WB, bs, tau, iters, stream), "rm_set_unimixing")
+
+
+def rm_unimixing_weights(ctx: int, layer: int, WG_out: int | None, WB_out: int | None, stream: int) -> None:
+    check(load().rm_unimixing_weights(ctx, layer, WG_out, WB_out, stream), "rm_unimixing_weights")
+
+
+def rm_unimixing(ctx: int, layer: int, X: int, Y: int, B: int, stream: int) -> None:
+    check(load().rm_unimixing(ctx, layer, X, Y, B, stream), "rm_unimixing")
 
 
 def rm_debug_gelu_grad(u: int, out: int, n: int, stream: int) -> None:

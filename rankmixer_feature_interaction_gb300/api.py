@@ -203,6 +203,33 @@ class RankMixer:
         return dX0, [g for g, _ in pairs]
 
     # -- tokenization, head and scoring ------------------------------------------------
+    def set_unimixing(self, layer: int, WG: torch.Tensor, WB: torch.Tensor, tau: float = 1.0,
+                      iters: int = 20) -> None:
+        """UniMixing ("UniMixer", section 4.3) in place of layer ``layer``'s TokenMixing.
+        WG [nb, nb] and WB [nb, bs, bs] are the raw float32 weights (nb * bs = T * D);
+        the context keeps their Sinkhorn-Knopp constrained form (Eq. 15)."""
+        WG = WG.to(device=self.device, dtype=torch.float32).contiguous()
+        WB = WB.to(device=self.device, dtype=torch.float32).contiguous()
+        bs = int(WB.shape[-1])
+        _lib.rm_set_unimixing(self.ctx, layer, _ptr(WG), _ptr(WB), bs, float(tau), int(iters), _stream())
+        self._um_bs = getattr(self, "_um_bs", {})
+        self._um_bs[layer] = bs
+
+    def unimixing_weights(self, layer: int) -> tuple[torch.Tensor, torch.Tensor]:
+        """The constrained weights (WG [nb, nb], WB [nb, bs, bs], float32) of a UniMixing layer."""
+        bs = self._um_bs[layer]
+        nb = self.T * self.D // bs
+        WG = torch.empty((nb, nb), dtype=torch.float32, device=self.device)
+        WB = torch.empty((nb, bs, bs), dtype=torch.float32, device=self.device)
+        _lib.rm_unimixing_weights(self.ctx, layer, _ptr(WG), _ptr(WB), _stream())
+        return WG, WB
+
+    def unimixing(self, layer: int, X: torch.Tensor, Y: torch.Tensor | None = None) -> torch.Tensor:
+        """Y = UniMixing(X) of layer ``layer``: X [B, T, D] in the context dtype."""
+        Y = torch.empty_like(X) if Y is None else Y
+        _lib.rm_unimixing(self.ctx, layer, _ptr(X), _ptr(Y), X.shape[0], _stream())
+        return Y
+
     def set_tokenizer(self, W: torch.Tensor, bias: torch.Tensor) -> None:
         """W [T, d, D], bias [T, D] in the context dtype (token t's projection of its slice)."""
         self.tok_d = int(W.shape[1])

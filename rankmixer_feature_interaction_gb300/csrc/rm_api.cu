@@ -15,6 +15,7 @@
 #include "rm_internal.h"
 #include "rm_moe.h"
 #include "rm_train.h"
+#include "rm_unimix.h"
 
 using namespace rm;
 
@@ -69,6 +70,13 @@ struct LayerW {
     // the training router of a dense-training / sparse-inference MoE layer
     float* Wg_train = nullptr;   // [T][E][D]
     float* bg_train = nullptr;   // [T][E]
+    // UniMixing in place of TokenMixing (set by rm_set_unimixing; um_bs = 0:
+    // TokenMixing): the constrained weights, WG [nb][nb] in float32 and in the
+    // operand type of the global product, WB [nb][bs][bs] in float32
+    int um_bs = 0;
+    float* umWG32 = nullptr;
+    void* umWGop = nullptr;      // fp16 (bf16 contexts); aliases umWG32 in float32 contexts
+    float* umWB = nullptr;
 };
 
 // Activations one layer's backward reads (token-major [T][Bcap][W]): the
@@ -144,6 +152,13 @@ struct rm_ctx {
     void* dX0h = nullptr;        // tokenization backward: s_t dX0 in fp16 [Bcap][T][D] (bf16 contexts)
     float* tok_part = nullptr;   // [T][kTokParts] per-token maxima
     float* tok_inv = nullptr;    // [T] 1 / s_t
+    // UniMixing workspace: the local outputs H and the global product Yt
+    // ([nb][Npitch] each, operand type, Npitch = Bcap bs rounded up to 256),
+    // and a layer input after LN2 ([Bcap][T][D], operand type)
+    void* umH = nullptr;
+    void* umYt = nullptr;
+    void* umX = nullptr;
+    size_t um_bytes = 0;         // bytes of umH (and of umYt)
     // host-entry staging: device copies of X0 and pooled, the copy streams and
     // per-chunk events of the pipelined host entry
     void* X0_dev = nullptr;
@@ -186,7 +201,10 @@ void free_ctx(rm_ctx* c) {
         cudaFree(l.g1); cudaFree(l.be1); cudaFree(l.g2); cudaFree(l.be2);
         moe_free_weights(l.moe);
         cudaFree(l.W1t); cudaFree(l.W2t); cudaFree(l.Wg_train); cudaFree(l.bg_train);
+        if (l.umWGop != l.umWG32) cudaFree(l.umWGop);
+        cudaFree(l.umWG32); cudaFree(l.umWB);
     }
+    cudaFree(c->umH); cudaFree(c->umYt); cudaFree(c->umX);
     {
         TrainWS& t = c->tw;
         for (auto& sl : t.slots) {
@@ -348,11 +366,29 @@ MixLnArgs mix_args(const rm_ctx* c, int layer, int B) {
     return a;
 }
 
+// UniMixing layers (defined with the backward helpers below)
+XType caller_xtype(const rm_ctx* c);
+XType op_xtype(const rm_ctx* c);
+rm_status unimix_mix_ln1(rm_ctx* c, int layer, const void* X, XType xt, int B, cudaStream_t s);
+
 rm_status stack_device(rm_ctx* c, const void* X0, float* pooled, void* XL, int B, cudaStream_t s) {
     const rm_config& g = c->cfg;
     for (int n = 0; n < g.L; ++n) {
         MixLnArgs a = mix_args(c, n, B);
-        if (n == 0) {
+        if (c->layers[n].um_bs) {
+            const void* xin = X0;
+            XType xt = caller_xtype(c);
+            if (n > 0) {
+                ProfScope ps(c, RM_K_LN2_OUT, s);
+                RM_CHECK_CUDA(launch_ln2_out_op(c->act, c->Z, c->rows, c->layers[n - 1].g2, c->layers[n - 1].be2,
+                                                c->umX, B, g.T, g.D, c->Bcap, g.ln_eps, c->num_sms, s),
+                              "ln2 (unimixing layer input)");
+                xin = c->umX;
+                xt = op_xtype(c);
+            }
+            rm_status st = unimix_mix_ln1(c, n, xin, xt, B, s);
+            if (st != RM_OK) return st;
+        } else if (n == 0) {
             a.X = X0;
             ProfScope ps(c, RM_K_MIX_LN1, s);
             RM_CHECK_CUDA(launch_mix_ln1(c->act, false, a, c->num_sms, s), "mix+ln1");
@@ -681,7 +717,50 @@ rm_status check_backward(rm_ctx* c, int B) {
     rm_status st;
     if ((st = check_ctx(c)) != RM_OK) return st;
     if (!c->cfg.training) return fail(RM_ERR_UNSUPPORTED, "the context was created without cfg.training");
+    for (const auto& l : c->layers)
+        if (l.um_bs) return fail(RM_ERR_UNSUPPORTED, "UniMixing layers have no training path");
     return check_batch(c, B);
+}
+
+// ---- UniMixing ("UniMixer" section 4.3) ------------------------------------------
+long long um_pitch(const rm_ctx* c, int bs) { return ((long long)c->Bcap * bs + 255) / 256 * 256; }
+
+XType caller_xtype(const rm_ctx* c) { return c->act == Act::F32 ? XType::F32 : XType::BF16; }
+XType op_xtype(const rm_ctx* c) { return c->act == Act::F32 ? XType::F32 : XType::F16; }
+
+// Local step and global product of layer `layer` for B samples of X (type xt,
+// sample-major [B][T][D]) into c->umYt [nb][Npitch].
+rm_status unimix_global(rm_ctx* c, int layer, const void* X, XType xt, int B, cudaStream_t s) {
+    const rm_config& g = c->cfg;
+    const LayerW& w = c->layers[layer];
+    const int bs = w.um_bs;
+    const int nb = g.T * g.D / bs;
+    const long long Npitch = um_pitch(c, bs);
+    const long long Npad = ((long long)B * bs + 255) / 256 * 256;
+    RM_CHECK_CUDA(launch_unimix_local(xt, c->act, X, (long long)g.T * g.D, w.umWB, c->umH, B, nb, bs, Npitch, Npad, s),
+                  "unimixing local step");
+    TrainGemm m = train_gemm_base(c);
+    m.G = 1;
+    m.M = nb; m.N = (int)Npad; m.K = nb; m.m_valid = nb;
+    m.a = {w.umWGop, nb, nb, 0, false};                    // WG [i][j], K-major
+    m.b = {c->umH, (int)Npad, nb, 0, true, Npitch};        // H [j][n], MN-major
+    m.c_gpitch = 0; m.c_ld = Npitch;
+    m.c0 = c->umYt;
+    return run_train_gemm(c, TE_F16, m, nullptr, "unimixing global product", s);
+}
+
+// S = LN1(X + UniMixing(X)) for layer `layer` (its mixing step, in place of
+// mix + LN1).  X: the layer input in type xt, sample-major.
+rm_status unimix_mix_ln1(rm_ctx* c, int layer, const void* X, XType xt, int B, cudaStream_t s) {
+    const rm_config& g = c->cfg;
+    const LayerW& w = c->layers[layer];
+    ProfScope ps(c, RM_K_UNIMIX, s);
+    rm_status st = unimix_global(c, layer, X, xt, B, s);
+    if (st != RM_OK) return st;
+    RM_CHECK_CUDA(launch_unimix_ln1(xt, c->act, X, c->umYt, c->S, w.g1, w.be1, B, g.T, g.D, w.um_bs,
+                                    um_pitch(c, w.um_bs), c->Bcap, g.ln_eps, c->num_sms, s),
+                  "unimixing residual + ln1");
+    return RM_OK;
 }
 
 }  // namespace
@@ -793,9 +872,11 @@ rm_status rm_block_forward(rm_ctx* c, int layer, const void* X_in, void* X_out, 
     cudaSetDevice(c->device);
     cudaStream_t s = as_stream(stream);
     const rm_config& g = c->cfg;
-    MixLnArgs a = mix_args(c, layer, B);
-    a.X = X_in;
-    {
+    if (c->layers[layer].um_bs) {
+        if ((st = unimix_mix_ln1(c, layer, X_in, caller_xtype(c), B, s)) != RM_OK) return st;
+    } else {
+        MixLnArgs a = mix_args(c, layer, B);
+        a.X = X_in;
         ProfScope ps(c, RM_K_MIX_LN1, s);
         RM_CHECK_CUDA(launch_mix_ln1(c->act, false, a, c->num_sms, s), "mix+ln1");
     }
@@ -1022,6 +1103,99 @@ rm_status rm_set_tokenizer(rm_ctx* c, const void* W, const void* bias, int d) {
     RM_CHECK_CUDA(launch_to_f32(c->act, bias, c->btok, (size_t)g.T * g.D, 0), "copy tokenizer bias");
     RM_CHECK_CUDA(cudaDeviceSynchronize(), "rm_set_tokenizer");
     c->tok_d = d;
+    return RM_OK;
+}
+
+rm_status rm_set_unimixing(rm_ctx* c, int layer, const float* WG, const float* WB, int bs, float tau, int iters,
+                           void* stream) {
+    rm_status st;
+    if ((st = check_ctx(c)) != RM_OK) return st;
+    const rm_config& g = c->cfg;
+    if (layer < 0 || layer >= g.L) return fail(RM_ERR_INVALID_ARG, "layer %d out of range", layer);
+    if (!WG || !WB) return fail(RM_ERR_INVALID_ARG, "WG / WB is NULL");
+    const long long L = (long long)g.T * g.D;
+    if (bs < 1 || L % bs != 0) return fail(RM_ERR_INVALID_ARG, "bs (%d) must divide T * D (%lld)", bs, L);
+    if (!(tau > 0.f) || !std::isfinite(tau)) return fail(RM_ERR_INVALID_ARG, "tau must be positive and finite");
+    if (iters < 0) return fail(RM_ERR_INVALID_ARG, "iters must be >= 0");
+    if (g.D > 48 * 32) return fail(RM_ERR_UNSUPPORTED, "UniMixing rows support D <= 1536");
+    const int nb = (int)(L / bs);
+    cudaSetDevice(c->device);
+    cudaStream_t s = as_stream(stream);
+    RM_CHECK_CUDA(cudaStreamSynchronize(s), "rm_set_unimixing (drain the stream)");
+    LayerW& w = c->layers[layer];
+    if (w.umWGop != w.umWG32) cudaFree(w.umWGop);
+    cudaFree(w.umWG32); cudaFree(w.umWB);
+    w.umWG32 = nullptr; w.umWGop = nullptr; w.umWB = nullptr; w.um_bs = 0;
+    const size_t nG = (size_t)nb * nb, nB = (size_t)nb * bs * bs;
+    if ((st = dmalloc(c, (void**)&w.umWG32, nG * 4, &c->weight_bytes)) != RM_OK) return st;
+    if ((st = dmalloc(c, (void**)&w.umWB, nB * 4, &c->weight_bytes)) != RM_OK) return st;
+    if (c->act == Act::F32)
+        w.umWGop = w.umWG32;
+    else if ((st = dmalloc(c, &w.umWGop, nG * 2, &c->weight_bytes)) != RM_OK)
+        return st;
+    // workspace for the largest pitch so far
+    const size_t hy = (size_t)nb * (size_t)um_pitch(c, bs) * op_size(c->act);
+    if (hy > c->um_bytes) {
+        cudaFree(c->umH); cudaFree(c->umYt);
+        c->umH = nullptr; c->umYt = nullptr; c->um_bytes = 0;
+        if ((st = dmalloc(c, &c->umH, hy, &c->ws_bytes)) != RM_OK) return st;
+        if ((st = dmalloc(c, &c->umYt, hy, &c->ws_bytes)) != RM_OK) return st;
+        c->um_bytes = hy;
+    }
+    if (!c->umX && (st = dmalloc(c, &c->umX, (size_t)c->Bcap * L * op_size(c->act), &c->ws_bytes)) != RM_OK)
+        return st;
+    // Sinkhorn-Knopp scratch, freed again below
+    float *C = nullptr, *f = nullptr, *gv = nullptr;
+    const size_t nmax = nG > nB ? nG : nB;
+    const size_t vmax = (size_t)nb * (size_t)(bs > 1 ? bs : 1) > (size_t)nb ? (size_t)nb * bs : (size_t)nb;
+    if ((st = dmalloc(c, (void**)&C, nmax * 4, nullptr)) != RM_OK) return st;
+    if ((st = dmalloc(c, (void**)&f, vmax * 4, nullptr)) != RM_OK || (st = dmalloc(c, (void**)&gv, vmax * 4, nullptr)) != RM_OK) {
+        cudaFree(C); cudaFree(f);
+        return st;
+    }
+    cudaError_t e = launch_sinkhorn(WG, 1, nb, tau, iters, C, f, gv, w.umWG32, c->act == Act::F32 ? nullptr : w.umWGop, s);
+    if (e == cudaSuccess) e = launch_sinkhorn(WB, nb, bs, tau, iters, C, f, gv, w.umWB, nullptr, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    cudaFree(C); cudaFree(f); cudaFree(gv);
+    if (e != cudaSuccess) return cuda_fail(e, "rm_set_unimixing (Sinkhorn-Knopp)");
+    w.um_bs = bs;
+    return RM_OK;
+}
+
+rm_status rm_unimixing_weights(rm_ctx* c, int layer, float* WG_out, float* WB_out, void* stream) {
+    rm_status st;
+    if ((st = check_ctx(c)) != RM_OK) return st;
+    const rm_config& g = c->cfg;
+    if (layer < 0 || layer >= g.L) return fail(RM_ERR_INVALID_ARG, "layer %d out of range", layer);
+    const LayerW& w = c->layers[layer];
+    if (!w.um_bs) return fail(RM_ERR_INVALID_ARG, "layer %d uses TokenMixing (no rm_set_unimixing)", layer);
+    if (!WG_out && !WB_out) return fail(RM_ERR_INVALID_ARG, "WG_out and WB_out are NULL");
+    const size_t nb = (size_t)g.T * g.D / w.um_bs;
+    cudaSetDevice(c->device);
+    cudaStream_t s = as_stream(stream);
+    if (WG_out) RM_CHECK_CUDA(cudaMemcpyAsync(WG_out, w.umWG32, nb * nb * 4, cudaMemcpyDeviceToDevice, s), "copy WG");
+    if (WB_out)
+        RM_CHECK_CUDA(cudaMemcpyAsync(WB_out, w.umWB, nb * w.um_bs * w.um_bs * 4, cudaMemcpyDeviceToDevice, s),
+                      "copy WB");
+    return RM_OK;
+}
+
+rm_status rm_unimixing(rm_ctx* c, int layer, const void* X, void* Y, int B, void* stream) {
+    rm_status st;
+    if ((st = check_ctx(c)) != RM_OK) return st;
+    const rm_config& g = c->cfg;
+    if (layer < 0 || layer >= g.L) return fail(RM_ERR_INVALID_ARG, "layer %d out of range", layer);
+    if (!c->layers[layer].um_bs) return fail(RM_ERR_INVALID_ARG, "layer %d uses TokenMixing (no rm_set_unimixing)", layer);
+    if ((st = check_batch(c, B)) != RM_OK) return st;
+    if (!X || !Y) return fail(RM_ERR_INVALID_ARG, "X / Y is NULL");
+    if (!aligned16(X) || !aligned16(Y)) return fail(RM_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+    cudaSetDevice(c->device);
+    cudaStream_t s = as_stream(stream);
+    ProfScope ps(c, RM_K_UNIMIX, s);
+    if ((st = unimix_global(c, layer, X, caller_xtype(c), B, s)) != RM_OK) return st;
+    const int bs = c->layers[layer].um_bs;
+    RM_CHECK_CUDA(launch_unimix_gather(c->act, c->umYt, Y, B, g.T, g.D, bs, um_pitch(c, bs), c->num_sms, s),
+                  "unimixing output");
     return RM_OK;
 }
 

@@ -15,6 +15,7 @@
 #include "rm_common.cuh"
 #include "rm_internal.h"
 #include "rm_train.h"
+#include "rm_unimix.h"
 
 namespace rm {
 namespace {
@@ -877,6 +878,19 @@ cudaError_t launch_ln2_out(Act act, const void* Z, const float2* stats, const fl
     else
         ln2_out_kernel<float, float><<<grid, 256, 0, s>>>((const float*)Z, stats, g2, be2, (float*)X_out, B, T, D,
                                                           Bcap, nchunk, cw, eps);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ln2_out_op(Act act, const void* Z, const float2* stats, const float* g2, const float* be2,
+                              void* X_out, int B, int T, int D, int Bcap, float eps, int num_sms, cudaStream_t s) {
+    if (B <= 0) return cudaSuccess;
+    const int grid = grid_for((long long)B * T * 32, 256, num_sms * 8);
+    if (act == Act::BF16)
+        ln2_out_kernel<__half, __half><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2, (__half*)X_out, B, T, D,
+                                                            Bcap, 1, D, eps);
+    else
+        ln2_out_kernel<float, float><<<grid, 256, 0, s>>>((const float*)Z, stats, g2, be2, (float*)X_out, B, T, D,
+                                                          Bcap, 1, D, eps);
     return cudaGetLastError();
 }
 

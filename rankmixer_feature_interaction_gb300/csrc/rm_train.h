@@ -49,6 +49,7 @@ enum TrainEpi {
     TE_DRESID = 4,   // C0 = acc + R           (float; R float)
     TE_F32 = 5,      // C0 = acc               (float)
     TE_BIAS_IO = 6,  // C0 = acc + bias        (the context's caller dtype: bf16 or float)
+    TE_F16 = 7,      // C0 = acc               (operand type: fp16, or float for float32 contexts)
 };
 
 struct TrainGemm {

@@ -90,6 +90,8 @@ train_gemm_simt_kernel(const TrainGemm g) {
                     reinterpret_cast<float*>(g.c0)[off] = o;
                 else
                     reinterpret_cast<__nv_bfloat16*>(g.c0)[off] = __float2bfloat16_rn(o);
+            } else if (EPI == TE_F16) {        // the operand type (fp16, or float for float32 contexts)
+                reinterpret_cast<Top*>(g.c0)[off] = from_f32<Top>(v);
             } else {
                 reinterpret_cast<float*>(g.c0)[off] = v;
             }
@@ -121,6 +123,7 @@ cudaError_t run_simt(int epi, const TrainGemm& g, cudaStream_t s) {
         case TE_DRESID: train_gemm_simt_kernel<Top, Taux, TE_DRESID><<<grid, 256, 0, s>>>(g); break;
         case TE_F32: train_gemm_simt_kernel<Top, Taux, TE_F32><<<grid, 256, 0, s>>>(g); break;
         case TE_BIAS_IO: train_gemm_simt_kernel<Top, Taux, TE_BIAS_IO><<<grid, 256, 0, s>>>(g); break;
+        case TE_F16: train_gemm_simt_kernel<Top, Taux, TE_F16><<<grid, 256, 0, s>>>(g); break;
         default: return cudaErrorInvalidValue;
     }
     cudaError_t e = cudaGetLastError();

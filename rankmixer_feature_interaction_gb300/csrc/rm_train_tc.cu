@@ -335,6 +335,13 @@ __device__ __forceinline__ void epilogue(const KArgs& a, int g, int m, bool vali
                 }
                 store16x32(reinterpret_cast<__nv_bfloat16*>(a.c0) + off, p);
             }
+        } else if (EPI == TE_F16) {
+            if (valid) {
+                uint32_t p[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) p[j] = f16x2_bits(v[2 * j] * inv_s, v[2 * j + 1] * inv_s);
+                store16x32(reinterpret_cast<__half*>(a.c0) + off, p);
+            }
         } else {   // TE_F32
             if (valid) {
                 float4* d4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(a.c0) + off);
@@ -739,6 +746,9 @@ cudaError_t launch_train_gemm_tc(int epi, const TrainGemm& g, int num_sms, cudaS
             break;
         case TE_BIAS_IO:
             if (!amn && bmn) RM_TRAIN_RUN(TE_BIAS_IO, false, true);
+            break;
+        case TE_F16:
+            if (!amn && bmn) RM_TRAIN_RUN(TE_F16, false, true);
             break;
         default: break;
     }

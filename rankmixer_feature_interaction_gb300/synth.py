@@ -145,6 +145,16 @@ def make_stack(T: int, D: int, k: int, L: int, seed: int, dtype: str = "bf16", d
     return [make_layer(T, D, k, seed * 131 + n, dtype, device, E, Fe, active) for n in range(L)]
 
 
+def make_unimix_weights(T: int, D: int, bs: int, seed: int, device="cpu") -> tuple:
+    """Raw (unconstrained) UniMixing weights for block size bs: WG [nb, nb] and
+    WB [nb, bs, bs], nb = T D / bs, every entry N(0, 1), float32."""
+    nb = T * D // bs
+    g = _gen(seed, device)
+    WG = _normal((nb, nb), 1.0, g, device, torch.float32)
+    WB = _normal((nb, bs, bs), 1.0, g, device, torch.float32)
+    return WG, WB
+
+
 def to_f64(p):
     """Tensor or dict/list of tensors -> numpy float64 (values exactly as rounded to their dtype)."""
     if isinstance(p, dict):
