@@ -41,6 +41,10 @@ L2_BYTES = 129 * 1024 * 1024
 # unchanged; otherwise the traffic is unknown (null).
 # embedding coordinates per token for --pass score (the tokenizer's slice length d)
 SCORE_SLICE = {"rankmixer_1b": 512, "rankmixer_100m": 256}
+# --pass unimix: UniMixing in every layer at block size D / T (the TokenMixing
+# granularity), the pages' final temperature and a fixed Sinkhorn-Knopp round count
+UNIMIX_TAU = 0.05
+UNIMIX_ITERS = 20
 
 KERNEL_SOURCES = ("rankmixer_feature_interaction_gb300/csrc/rm_gemm_tc.cu",
                   "rankmixer_feature_interaction_gb300/csrc/rm_common.cuh",
@@ -212,8 +216,9 @@ def run_ours(args):
     moe = args.config == "moe_1b"
     train = args.pass_ == "train"
     score = args.pass_ == "score"
-    if moe and score:
-        raise SystemExit("--pass score runs the dense stack (rankmixer_1b / rankmixer_100m)")
+    unimix = args.pass_ == "unimix"
+    if moe and (score or unimix):
+        raise SystemExit("--pass score / unimix run the dense stack (rankmixer_1b / rankmixer_100m)")
     L = args.layers or c["L"]
     E, Fe = c.get("E", 0), c.get("Fe", 0)
     # weak scaling: the job's batch is world * B samples, rank r owns shard r
@@ -224,6 +229,12 @@ def run_ours(args):
     m = RankMixer(T, D, k, layers, dtype="bf16", max_batch=B, n_experts=E, expert_hidden=Fe,
                   training=train and not moe)
     del layers
+    bs_um = D // T
+    if unimix:
+        for n in range(L):
+            WG, WB = synth.make_unimix_weights(T, D, bs_um, 4245 + n, dev)
+            m.set_unimixing(n, WG, WB, tau=UNIMIX_TAU, iters=UNIMIX_ITERS)
+            del WG, WB
     torch.cuda.empty_cache()
     X0 = synth.make_input_shard(world * B, start, stop, T, D, 20260101, "bf16", dev)
     pooled = torch.empty((B, D), dtype=torch.float32, device=dev)
@@ -408,8 +419,22 @@ def run_ours(args):
                     "peak_source": f"{peak_src} bf16_tflops_sustained",
                     "avg_launch_ms": round(avg_ms, 4)}
     flops_executed = None
+    unimix_info = None
     if not moe:
         flops_step = 4.0 * k * L * T * D * D * B
+        if unimix:
+            # per layer and sample: the global product 2 nb^2 bs = 2 (T D)^2 / bs and the
+            # local products 2 (T D) bs
+            um_sample = 2.0 * (T * D) ** 2 / bs_um + 2.0 * T * D * bs_um
+            flops_step += L * B * um_sample
+            n_um, t_um = kstats["unimix"]
+            if n_um:
+                um_ms = t_um / n_um
+                unimix_info = {"bs": bs_um, "nb": T * D // bs_um, "tau": UNIMIX_TAU, "iters": UNIMIX_ITERS,
+                               "ms_per_layer": round(um_ms, 4),
+                               "global_product_gflop_per_layer": round(2.0 * (T * D) ** 2 / bs_um * B / 1e9, 1),
+                               "tflops_scope": round(B * um_sample / (um_ms / 1e3) / 1e12, 1),
+                               "scope": "local block products + global product (tcgen05) + residual + LN1"}
         if score:
             flops_step += 2.0 * T * d_tok * D * B + 2.0 * D * B      # tokenizer + head
         if train:
@@ -419,7 +444,7 @@ def run_ours(args):
             flops_step = 3.0 * flops_step
     gpu_launches = int(sum(v[0] for kk, v in kstats.items() if kk != "misc"))
     what = ("DTSI train forward" if moe else "train step: fwd + bwd") if train else (
-        "score: tokenize + fwd + head" if score else "fwd")
+        "score: tokenize + fwd + head" if score else ("fwd with UniMixing" if unimix else "fwd"))
 
     out = {
         "metric": f"samples/s (RankMixer-1B-shape block stack {what})" if args.config == "rankmixer_1b"
@@ -436,7 +461,8 @@ def run_ours(args):
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) inputs, N(0,1/fan_in) weights; random-init)",
         "config": {"workload": f"{args.config} B={B} T={T} D={D} k={k} L={L}" + (f" E={E} Fe={Fe}" if moe else "")
-                   + (f" d={d_tok}" if score else ""),
+                   + (f" d={d_tok}" if score else "")
+                   + (f" unimixing bs={bs_um} tau={UNIMIX_TAU}" if unimix else ""),
                    "batch_per_gpu": B, "global_batch": B * world, "parallelism": f"replicas x{world} (batch sharded" + (", gradients all-reduced)" if train and not moe and world > 1
                                                                         else ")"),
                    "l2": "inputs larger than L2 (X0 %.0f MB, weights %.0f MB > 129 MB)" % (
@@ -450,11 +476,13 @@ def run_ours(args):
         "kernels_ms_per_step": {kk: round(v[1] / args.steps, 4) for kk, v in kstats.items() if v[0]},
         "gpu_launches": gpu_launches,
         "moe_mean_active_experts": round(active / (B * T), 3) if moe else None,
+        "unimix": unimix_info,
         "clocks": clk,
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(args.config, B, args.cpu_seconds, train=train, score=score)
+        out["cpu_baseline"] = cpu_baseline(args.config, B, args.cpu_seconds, train=train, score=score,
+                                           unimix=unimix)
     if rank == 0:
         print(json.dumps(out), flush=True)
     m.close()
@@ -466,7 +494,7 @@ def run_ours(args):
 # CPU oracle baseline (bounded sample)
 # ----------------------------------------------------------------------------
 def cpu_baseline(config: str, B_full: int, seconds: float, n_steps: int = 1, train: bool = False,
-                 score: bool = False) -> dict:
+                 score: bool = False, unimix: bool = False) -> dict:
     import numpy as np
 
     import oracle
@@ -485,6 +513,11 @@ def cpu_baseline(config: str, B_full: int, seconds: float, n_steps: int = 1, tra
         Wtok = r.standard_normal((T, d_tok, D)) / d_tok ** 0.5
         btok = 0.1 * r.standard_normal((T, D))
         hw = r.standard_normal(D) / D ** 0.5
+    if unimix:
+        for n, p in enumerate(layers):
+            WG, WB = synth.make_unimix_weights(T, D, D // T, 4245 + n, "cpu")
+            p["WG"] = oracle.sinkhorn(synth.to_f64(WG), UNIMIX_TAU, UNIMIX_ITERS)
+            p["WB"] = oracle.sinkhorn(synth.to_f64(WB), UNIMIX_TAU, UNIMIX_ITERS)
     cores = oracle.num_threads()
 
     def run(nb):
@@ -503,6 +536,8 @@ def cpu_baseline(config: str, B_full: int, seconds: float, n_steps: int = 1, tra
         elif train:
             oracle.stack_forward(X, layers)
             oracle.stack_backward(X, np.full((nb, D), 1.0 / nb), layers)
+        elif unimix:
+            oracle.stack_forward_unimix(X, layers)
         else:
             oracle.stack_forward(X, layers)
         return time.perf_counter() - t0
@@ -519,7 +554,7 @@ def cpu_baseline(config: str, B_full: int, seconds: float, n_steps: int = 1, tra
         total_n += nb
     return {"value": round(total_n / total_t, 3), "unit": "samples/s", "cores": cores, "kind": "oracle",
             "sample": f"{nb} samples of the {config} workload per step (of B={B_full}), float64 oracle"
-                      f"{' forward + backward' if train else ''}, "
+                      f"{' forward + backward' if train else ''}{' with UniMixing' if unimix else ''}, "
                       f"OpenMP over samples on {cores} host threads, {n_steps} step(s), {total_t:.1f} s"}
 
 
@@ -535,14 +570,15 @@ def run_reference(args):
     per_step_s = min(args.cpu_seconds, 150.0 / (steps + args.warmup))
     train = args.pass_ == "train"
     score = args.pass_ == "score"
+    unimix = args.pass_ == "unimix"
     moe = args.config == "moe_1b"
-    cb = cpu_baseline(args.config, B, per_step_s, n_steps=steps, train=train, score=score)
+    cb = cpu_baseline(args.config, B, per_step_s, n_steps=steps, train=train, score=score, unimix=unimix)
     what = ("DTSI train forward" if moe else "train step: fwd + bwd") if train else (
-        "score: tokenize + fwd + head" if score else "fwd")
+        "score: tokenize + fwd + head" if score else ("fwd with UniMixing" if unimix else "fwd"))
     out = {
         "impl": "reference",
         "metric": f"samples/s (RankMixer-1B-shape block stack {what})" if args.config == "rankmixer_1b"
-        else f"samples/s ({args.config}{' ' + what if (train or score) else ''})",
+        else f"samples/s ({args.config}{' ' + what if (train or score or unimix) else ''})",
         "value": cb["value"], "unit": "samples/s", "n_gpus": world, "steps": steps, "warmup": args.warmup,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)",
@@ -564,9 +600,10 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=0, help="override the number of layers (profiling captures)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU oracle budget per measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--pass", dest="pass_", choices=["fwd", "train", "score"], default="fwd",
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "train", "score", "unimix"], default="fwd",
                     help="fwd: the forward stack (the headline); train: forward + backward of the stack (with "
-                         "moe_1b: the dense-training MoE forward); score: tokenization + stack + head")
+                         "moe_1b: the dense-training MoE forward); score: tokenization + stack + head; unimix: "
+                         "the forward stack with UniMixing in place of TokenMixing in every layer")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -77,6 +77,8 @@ struct LayerW {
     float* umWG32 = nullptr;
     void* umWGop = nullptr;      // fp16 (bf16 contexts); aliases umWG32 in float32 contexts
     float* umWB = nullptr;
+    void* umWBt16 = nullptr;     // bf16 contexts: WB transposed ([j][r][s]) in fp16, the tensor-core
+                                 // local step's B operand
 };
 
 // Activations one layer's backward reads (token-major [T][Bcap][W]): the
@@ -202,7 +204,7 @@ void free_ctx(rm_ctx* c) {
         moe_free_weights(l.moe);
         cudaFree(l.W1t); cudaFree(l.W2t); cudaFree(l.Wg_train); cudaFree(l.bg_train);
         if (l.umWGop != l.umWG32) cudaFree(l.umWGop);
-        cudaFree(l.umWG32); cudaFree(l.umWB);
+        cudaFree(l.umWG32); cudaFree(l.umWB); cudaFree(l.umWBt16);
     }
     cudaFree(c->umH); cudaFree(c->umYt); cudaFree(c->umX);
     {
@@ -729,7 +731,7 @@ XType caller_xtype(const rm_ctx* c) { return c->act == Act::F32 ? XType::F32 : X
 XType op_xtype(const rm_ctx* c) { return c->act == Act::F32 ? XType::F32 : XType::F16; }
 
 // Local step and global product of layer `layer` for B samples of X (type xt,
-// sample-major [B][T][D]) into c->umYt [nb][Npitch].
+// sample-major [B][T][D]) into c->umYt as Y [B][T D] (operand type).
 rm_status unimix_global(rm_ctx* c, int layer, const void* X, XType xt, int B, cudaStream_t s) {
     const rm_config& g = c->cfg;
     const LayerW& w = c->layers[layer];
@@ -737,7 +739,8 @@ rm_status unimix_global(rm_ctx* c, int layer, const void* X, XType xt, int B, cu
     const int nb = g.T * g.D / bs;
     const long long Npitch = um_pitch(c, bs);
     const long long Npad = ((long long)B * bs + 255) / 256 * 256;
-    RM_CHECK_CUDA(launch_unimix_local(xt, c->act, X, (long long)g.T * g.D, w.umWB, c->umH, B, nb, bs, Npitch, Npad, s),
+    RM_CHECK_CUDA(launch_unimix_local(xt, c->act, X, (long long)g.T * g.D, w.umWB, w.umWBt16, c->umH, B, nb, bs,
+                                      Npitch, Npad, s),
                   "unimixing local step");
     TrainGemm m = train_gemm_base(c);
     m.G = 1;
@@ -746,7 +749,8 @@ rm_status unimix_global(rm_ctx* c, int layer, const void* X, XType xt, int B, cu
     m.b = {c->umH, (int)Npad, nb, 0, true, Npitch};        // H [j][n], MN-major
     m.c_gpitch = 0; m.c_ld = Npitch;
     m.c0 = c->umYt;
-    return run_train_gemm(c, TE_F16, m, nullptr, "unimixing global product", s);
+    m.um_bs = bs; m.um_B = B; m.um_L = (long long)g.T * g.D;
+    return run_train_gemm(c, TE_F16T, m, nullptr, "unimixing global product", s);
 }
 
 // S = LN1(X + UniMixing(X)) for layer `layer` (its mixing step, in place of
@@ -757,8 +761,8 @@ rm_status unimix_mix_ln1(rm_ctx* c, int layer, const void* X, XType xt, int B, c
     ProfScope ps(c, RM_K_UNIMIX, s);
     rm_status st = unimix_global(c, layer, X, xt, B, s);
     if (st != RM_OK) return st;
-    RM_CHECK_CUDA(launch_unimix_ln1(xt, c->act, X, c->umYt, c->S, w.g1, w.be1, B, g.T, g.D, w.um_bs,
-                                    um_pitch(c, w.um_bs), c->Bcap, g.ln_eps, c->num_sms, s),
+    RM_CHECK_CUDA(launch_unimix_ln1(xt, c->act, X, c->umYt, c->S, w.g1, w.be1, B, g.T, g.D, c->Bcap, g.ln_eps,
+                                    c->num_sms, s),
                   "unimixing residual + ln1");
     return RM_OK;
 }
@@ -1124,14 +1128,17 @@ rm_status rm_set_unimixing(rm_ctx* c, int layer, const float* WG, const float* W
     RM_CHECK_CUDA(cudaStreamSynchronize(s), "rm_set_unimixing (drain the stream)");
     LayerW& w = c->layers[layer];
     if (w.umWGop != w.umWG32) cudaFree(w.umWGop);
-    cudaFree(w.umWG32); cudaFree(w.umWB);
-    w.umWG32 = nullptr; w.umWGop = nullptr; w.umWB = nullptr; w.um_bs = 0;
+    cudaFree(w.umWG32); cudaFree(w.umWB); cudaFree(w.umWBt16);
+    w.umWG32 = nullptr; w.umWGop = nullptr; w.umWB = nullptr; w.umWBt16 = nullptr; w.um_bs = 0;
     const size_t nG = (size_t)nb * nb, nB = (size_t)nb * bs * bs;
     if ((st = dmalloc(c, (void**)&w.umWG32, nG * 4, &c->weight_bytes)) != RM_OK) return st;
     if ((st = dmalloc(c, (void**)&w.umWB, nB * 4, &c->weight_bytes)) != RM_OK) return st;
     if (c->act == Act::F32)
         w.umWGop = w.umWG32;
     else if ((st = dmalloc(c, &w.umWGop, nG * 2, &c->weight_bytes)) != RM_OK)
+        return st;
+    if (c->act != Act::F32 && unimix_local_mma_ok(bs) &&
+        (st = dmalloc(c, &w.umWBt16, nB * 2, &c->weight_bytes)) != RM_OK)
         return st;
     // workspace for the largest pitch so far
     const size_t hy = (size_t)nb * (size_t)um_pitch(c, bs) * op_size(c->act);
@@ -1155,6 +1162,7 @@ rm_status rm_set_unimixing(rm_ctx* c, int layer, const float* WG, const float* W
     }
     cudaError_t e = launch_sinkhorn(WG, 1, nb, tau, iters, C, f, gv, w.umWG32, c->act == Act::F32 ? nullptr : w.umWGop, s);
     if (e == cudaSuccess) e = launch_sinkhorn(WB, nb, bs, tau, iters, C, f, gv, w.umWB, nullptr, s);
+    if (e == cudaSuccess && w.umWBt16) e = launch_unimix_pack_wb(w.umWB, w.umWBt16, nb, bs, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     cudaFree(C); cudaFree(f); cudaFree(gv);
     if (e != cudaSuccess) return cuda_fail(e, "rm_set_unimixing (Sinkhorn-Knopp)");
@@ -1193,9 +1201,7 @@ rm_status rm_unimixing(rm_ctx* c, int layer, const void* X, void* Y, int B, void
     cudaStream_t s = as_stream(stream);
     ProfScope ps(c, RM_K_UNIMIX, s);
     if ((st = unimix_global(c, layer, X, caller_xtype(c), B, s)) != RM_OK) return st;
-    const int bs = c->layers[layer].um_bs;
-    RM_CHECK_CUDA(launch_unimix_gather(c->act, c->umYt, Y, B, g.T, g.D, bs, um_pitch(c, bs), c->num_sms, s),
-                  "unimixing output");
+    RM_CHECK_CUDA(launch_unimix_out(c->act, c->umYt, Y, (long long)B * g.T * g.D, s), "unimixing output");
     return RM_OK;
 }
 

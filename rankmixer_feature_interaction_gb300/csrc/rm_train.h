@@ -50,6 +50,9 @@ enum TrainEpi {
     TE_F32 = 5,      // C0 = acc               (float)
     TE_BIAS_IO = 6,  // C0 = acc + bias        (the context's caller dtype: bf16 or float)
     TE_F16 = 7,      // C0 = acc               (operand type: fp16, or float for float32 contexts)
+    TE_F16T = 8,     // as TE_F16, stored for UniMixing's sample-major layout: column n = b um_bs + r
+                     //      of row m goes to C0[b um_L + m um_bs + r], columns with b >= um_B are
+                     //      dropped (um_bs a multiple of 8 on the tensor-core path)
 };
 
 struct TrainGemm {
@@ -69,6 +72,8 @@ struct TrainGemm {
     float* colpart;
     int* err;
     unsigned long long timeout_ns;
+    int um_bs = 0, um_B = 0;    // TE_F16T: block size, samples
+    long long um_L = 0;         // TE_F16T: values per sample
 };
 
 // Rows of C summed into one TE_DGELU partial on the tensor-core path.

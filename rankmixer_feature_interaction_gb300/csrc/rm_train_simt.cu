@@ -92,6 +92,11 @@ train_gemm_simt_kernel(const TrainGemm g) {
                     reinterpret_cast<__nv_bfloat16*>(g.c0)[off] = __float2bfloat16_rn(o);
             } else if (EPI == TE_F16) {        // the operand type (fp16, or float for float32 contexts)
                 reinterpret_cast<Top*>(g.c0)[off] = from_f32<Top>(v);
+            } else if (EPI == TE_F16T) {       // column n = b bs + r of row m -> Y[b][m bs + r]
+                const int b = n / g.um_bs;
+                if (b < g.um_B)
+                    reinterpret_cast<Top*>(g.c0)[(size_t)b * g.um_L + (size_t)m * g.um_bs + (n - b * g.um_bs)] =
+                        from_f32<Top>(v);
             } else {
                 reinterpret_cast<float*>(g.c0)[off] = v;
             }
@@ -124,6 +129,7 @@ cudaError_t run_simt(int epi, const TrainGemm& g, cudaStream_t s) {
         case TE_F32: train_gemm_simt_kernel<Top, Taux, TE_F32><<<grid, 256, 0, s>>>(g); break;
         case TE_BIAS_IO: train_gemm_simt_kernel<Top, Taux, TE_BIAS_IO><<<grid, 256, 0, s>>>(g); break;
         case TE_F16: train_gemm_simt_kernel<Top, Taux, TE_F16><<<grid, 256, 0, s>>>(g); break;
+        case TE_F16T: train_gemm_simt_kernel<Top, Taux, TE_F16T><<<grid, 256, 0, s>>>(g); break;
         default: return cudaErrorInvalidValue;
     }
     cudaError_t e = cudaGetLastError();

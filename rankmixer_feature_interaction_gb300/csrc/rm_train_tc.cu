@@ -97,6 +97,8 @@ struct KArgs {
     const float* inv_scale;
     float* colpart;
     int colpart_rows;      // partial rows per group: ceil(M / 32)
+    int um_bs, um_B;       // TE_F16T: block size and samples
+    long long um_L;        // TE_F16T: values per sample
     int* err;
     unsigned long long timeout_ns;
 };
@@ -334,6 +336,26 @@ __device__ __forceinline__ void epilogue(const KArgs& a, int g, int m, bool vali
                     p[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&h1);
                 }
                 store16x32(reinterpret_cast<__nv_bfloat16*>(a.c0) + off, p);
+            }
+        } else if (EPI == TE_F16T) {
+            // column n = b bs + r of row m -> Y[b][m bs + r]: 8-column groups never
+            // straddle samples (bs % 8 == 0), each one 16-byte store
+            if (valid) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int n = n0 + 32 * c + 8 * q;
+                    const int b = n / a.um_bs;
+                    if (b < a.um_B) {
+                        const int r = n - b * a.um_bs;
+                        uint4 w;
+                        w.x = f16x2_bits(v[8 * q] * inv_s, v[8 * q + 1] * inv_s);
+                        w.y = f16x2_bits(v[8 * q + 2] * inv_s, v[8 * q + 3] * inv_s);
+                        w.z = f16x2_bits(v[8 * q + 4] * inv_s, v[8 * q + 5] * inv_s);
+                        w.w = f16x2_bits(v[8 * q + 6] * inv_s, v[8 * q + 7] * inv_s);
+                        *reinterpret_cast<uint4*>(reinterpret_cast<__half*>(a.c0) + (size_t)b * a.um_L +
+                                                  (size_t)m * a.um_bs + r) = w;
+                    }
+                }
             }
         } else if (EPI == TE_F16) {
             if (valid) {
@@ -691,6 +713,7 @@ bool train_tc_supported(const TrainGemm& g) {
     if (g.a.gpitch % 8 != 0 || g.b.gpitch % 8 != 0) return false;
     if (g.a.ld % 8 != 0 || g.b.ld % 8 != 0) return false;         // 16-byte row pitches for TMA
     if ((g.c_ld ? g.c_ld : g.N) % 8 != 0 || g.c_gpitch % 8 != 0) return false;   // 16-byte vector stores
+    if (g.um_bs % 8 != 0 || g.um_L % 8 != 0) return false;   // TE_F16T: 8-column groups inside one sample
     return true;
 }
 
@@ -720,6 +743,9 @@ cudaError_t launch_train_gemm_tc(int epi, const TrainGemm& g, int num_sms, cudaS
     ka.bias = g.bias;
     ka.inv_scale = g.inv_scale;
     ka.colpart = g.colpart;
+    ka.um_bs = g.um_bs;
+    ka.um_B = g.um_B;
+    ka.um_L = g.um_L;
     ka.colpart_rows = train_colpart_rows(g, num_sms);
     ka.err = g.err;
     ka.timeout_ns = g.timeout_ns;
@@ -749,6 +775,9 @@ cudaError_t launch_train_gemm_tc(int epi, const TrainGemm& g, int num_sms, cudaS
             break;
         case TE_F16:
             if (!amn && bmn) RM_TRAIN_RUN(TE_F16, false, true);
+            break;
+        case TE_F16T:
+            if (!amn && bmn && g.um_bs % 8 == 0 && g.um_bs > 0) RM_TRAIN_RUN(TE_F16T, false, true);
             break;
         default: break;
     }

@@ -1,16 +1,19 @@
 // UniMixing kernels ("UniMixer: A Unified Architecture for Scaling Laws in
 // Recommendation Systems", section 4.3): the Sinkhorn-Knopp constraint of the
 // mixing weights (Eq. 15), the per-block local step h_j = x_j WB_j (Eq. 13)
-// and, after the global step Yt = WG H on the tensor cores, the residual +
-// LN1 that feeds the per-token FFN (or a plain gather back to [B][T][D]).
+// and, after the global step WG H on the tensor cores (stored straight into
+// the sample-major layout by its epilogue), the residual + LN1 that feeds the
+// per-token FFN.
 //
 // All three are memory-bound or tiny: the local step reads each sample once
 // and writes H once (bs^2 multiply-adds per block of bs values, packed fp32x2
 // FMAs on a bs x bs weight tile in shared memory); the row kernel reads X and
-// Yt once and writes S once.
+// Y once, contiguously, and writes S once.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
+
+#include <type_traits>
 
 #include "rm_common.cuh"
 #include "rm_unimix.h"
@@ -110,44 +113,71 @@ __device__ __forceinline__ void store4(float* p, float a, float b, float c, floa
     *reinterpret_cast<float4*>(p) = make_float4(a, b, c, d);
 }
 
-// bs % 4 == 0, bs <= 64.  CTA (sample tile, block j): WB_j and the tile's x_j
-// rows in shared memory; thread (sg, rg) computes samples sg + k SG (k < SPT)
-// x columns 4 rg .. 4 rg + 3, so a warp's stores cover consecutive samples'
-// contiguous bs-wide runs of H's row j.
-template <typename Tx, typename Top, int SPT>
-__global__ void __launch_bounds__(256)
+// bs % 8 == 0, bs <= 64.  CTA (sample tile, block j): WB_j (float32) and the
+// tile's x_j rows in shared memory, each x stored twice as an (x, x) pair so
+// that one 8-byte load feeds the packed fp32x2 FMAs.  Thread (sg, rg) computes
+// samples sg + k SG (k < 8) x columns 8 rg .. 8 rg + 7: per s, 8 pair loads,
+// two 16-byte weight loads and 32 packed FMAs (64 multiply-adds).  A warp's
+// stores for one k cover consecutive samples' contiguous bs-wide runs of H's
+// row j.  The x rows are bs + 1 pairs apart (an odd stride: the sample groups
+// of a warp read distinct banks).
+template <typename Tx, typename Top>
+__global__ void __launch_bounds__(128)
 unimix_local_kernel(const Tx* __restrict__ X, long long x_stride, const float* __restrict__ WB, Top* __restrict__ H,
                     int B, int bs, long long Npitch, long long Npad) {
-    extern __shared__ float smem[];
+    constexpr int SPT = 8;
+    extern __shared__ float4 smem4[];
+    float* smem = reinterpret_cast<float*>(smem4);
     const int j = blockIdx.y;
-    const int rq = bs >> 2;
+    const int rq = bs >> 3;
     const int SG = blockDim.x / rq;
     const int SB = SG * SPT;
-    const int ldx = bs + 1;
-    float* sW = smem;                   // [bs][bs]
-    float* sX = smem + bs * bs;         // [SB][bs + 1]
+    const int ldx = bs + 1;                       // in pairs
+    float* sW = smem;                             // [bs][bs]
+    float2* sX = reinterpret_cast<float2*>(smem + bs * bs);   // [SB][bs + 1] pairs (x, x)
     const float* wsrc = WB + (size_t)j * bs * bs;
     for (int e = threadIdx.x; e < bs * bs; e += blockDim.x) sW[e] = wsrc[e];
     const long long b0 = (long long)blockIdx.x * SB;
-    for (int e = threadIdx.x; e < SB * bs; e += blockDim.x) {
-        const int bb = e / bs, ss = e - bb * bs;
+    constexpr int VE = 16 / (int)sizeof(Tx);     // values per 16-byte load (bs % VE == 0)
+    const int nseg = bs / VE;
+    for (int e = threadIdx.x; e < SB * nseg; e += blockDim.x) {
+        const int bb = e / nseg, s0 = (e - bb * nseg) * VE;
         const long long b = b0 + bb;
-        sX[bb * ldx + ss] = b < B ? XLoad<Tx>::at(X + b * x_stride + (long long)j * bs + ss) : 0.f;
+        float2* dst = sX + bb * ldx + s0;
+        if (b < B) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(X + b * x_stride + (long long)j * bs + s0));
+            const Tx* pv = reinterpret_cast<const Tx*>(&v);
+#pragma unroll
+            for (int u = 0; u < VE; ++u) {
+                const float x = XLoad<Tx>::at(pv + u);
+                dst[u] = make_float2(x, x);
+            }
+        } else {
+#pragma unroll
+            for (int u = 0; u < VE; ++u) dst[u] = make_float2(0.f, 0.f);
+        }
     }
     __syncthreads();
     const int rg = threadIdx.x % rq, sg = threadIdx.x / rq;
     if (sg < SG) {
-        uint64_t a01[SPT], a23[SPT];
+        uint64_t acc[SPT][4];
 #pragma unroll
-        for (int k = 0; k < SPT; ++k) a01[k] = a23[k] = 0ull;
+        for (int k = 0; k < SPT; ++k)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[k][q] = 0ull;
+        const float2* xs = sX + sg * ldx;
         for (int s = 0; s < bs; ++s) {
-            const float4 w = *reinterpret_cast<const float4*>(sW + s * bs + 4 * rg);
-            const uint64_t w01 = f2_pack(w.x, w.y), w23 = f2_pack(w.z, w.w);
+            const float4 wa = *reinterpret_cast<const float4*>(sW + s * bs + 8 * rg);
+            const float4 wb = *reinterpret_cast<const float4*>(sW + s * bs + 8 * rg + 4);
+            const uint64_t w0 = f2_pack(wa.x, wa.y), w1 = f2_pack(wa.z, wa.w);
+            const uint64_t w2 = f2_pack(wb.x, wb.y), w3 = f2_pack(wb.z, wb.w);
 #pragma unroll
             for (int k = 0; k < SPT; ++k) {
-                const uint64_t xv = f2_splat(sX[(sg + SG * k) * ldx + s]);
-                a01[k] = f2_fma(xv, w01, a01[k]);
-                a23[k] = f2_fma(xv, w23, a23[k]);
+                const uint64_t xv = *reinterpret_cast<const uint64_t*>(xs + (size_t)SG * k * ldx + s);
+                acc[k][0] = f2_fma(xv, w0, acc[k][0]);
+                acc[k][1] = f2_fma(xv, w1, acc[k][1]);
+                acc[k][2] = f2_fma(xv, w2, acc[k][2]);
+                acc[k][3] = f2_fma(xv, w3, acc[k][3]);
             }
         }
         Top* hrow = H + (size_t)j * Npitch;
@@ -155,16 +185,122 @@ unimix_local_kernel(const Tx* __restrict__ X, long long x_stride, const float* _
         for (int k = 0; k < SPT; ++k) {
             const long long b = b0 + sg + SG * k;
             if (b < B) {
-                float v0, v1, v2, v3;
-                f2_unpack(a01[k], v0, v1);
-                f2_unpack(a23[k], v2, v3);
-                store4(hrow + b * bs + 4 * rg, v0, v1, v2, v3);
+                float v[8];
+                f2_unpack(acc[k][0], v[0], v[1]);
+                f2_unpack(acc[k][1], v[2], v[3]);
+                f2_unpack(acc[k][2], v[4], v[5]);
+                f2_unpack(acc[k][3], v[6], v[7]);
+                store4(hrow + b * bs + 8 * rg, v[0], v[1], v[2], v[3]);
+                store4(hrow + b * bs + 8 * rg + 4, v[4], v[5], v[6], v[7]);
             }
         }
     }
     if (blockIdx.x == 0) {
         Top* hrow = H + (size_t)j * Npitch;
         for (long long n = (long long)B * bs + threadIdx.x; n < Npad; n += blockDim.x) hrow[n] = from_f32<Top>(0.f);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Local step on the tensor cores (warp-level mma.sync m16n8k16, fp16
+// operands, fp32 accumulate): 2-byte inputs, BS a multiple of 16 up to 64.
+// A warp keeps WB_j's fragments (BS / 16 k-steps x BS / 8 column tiles, from
+// the transposed fp16 copy WBt[j][r][s]) in registers for its block j and
+// streams tiles of 16 samples: A fragments straight from X (rows b, columns
+// j BS + k; bf16 inputs converted to fp16, exact for every bf16 value of
+// magnitude 2^-14 .. 65504), the 16 x BS result to H's row j as fp16 pairs.
+// fp16 rather than bf16 weights: near-uniform (high-temperature) weights
+// average the signal down over BS terms but not the weights' rounding, which
+// at bf16's 8 significant bits reached 2.3e-2 of the output's rms at the 1B
+// shape.  The step is bound by reading X and writing H; the products are a
+// few percent of the tensor-core time.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                 "{%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two packed 16-bit inputs -> a packed fp16 pair.
+template <typename Tin> __device__ __forceinline__ uint32_t to_f16x2(uint32_t v);
+template <> __device__ __forceinline__ uint32_t to_f16x2<__half>(uint32_t v) { return v; }
+template <> __device__ __forceinline__ uint32_t to_f16x2<__nv_bfloat16>(uint32_t v) {
+    return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+
+constexpr int kMmaWarps = 4;
+constexpr int kMmaTilesPerWarp = 4;      // 16-sample tiles per warp per CTA
+
+template <typename Tin, int BS>
+__global__ void __launch_bounds__(32 * kMmaWarps)
+unimix_local_mma_kernel(const Tin* __restrict__ X, long long x_stride, const __half* __restrict__ WBt,
+                        __half* __restrict__ H, int B, long long Npitch, long long Npad) {
+    constexpr int KS = BS / 16, NT = BS / 8;
+    const int j = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    // B fragments: B[k][n] = WB_j[k][n] = WBt[j][n][k]
+    uint32_t bf[KS][NT][2];
+    const __half* w = WBt + (size_t)j * BS * BS;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const __half* row = w + (size_t)(nt * 8 + g) * BS + ks * 16 + 2 * c;
+            bf[ks][nt][0] = __ldg(reinterpret_cast<const uint32_t*>(row));
+            bf[ks][nt][1] = __ldg(reinterpret_cast<const uint32_t*>(row + 8));
+        }
+    __half* hrow = H + (size_t)j * Npitch;
+    const long long tile0 = ((long long)blockIdx.x * kMmaWarps + warp) * kMmaTilesPerWarp;
+#pragma unroll 1
+    for (int it = 0; it < kMmaTilesPerWarp; ++it) {
+        const long long b0 = (tile0 + it) * 16;
+        if (b0 >= B) break;
+        const long long r0 = b0 + g, r1 = b0 + g + 8;
+        const bool v0 = r0 < B, v1 = r1 < B;
+        const Tin* x0 = X + r0 * x_stride + (long long)j * BS + 2 * c;
+        const Tin* x1 = X + r1 * x_stride + (long long)j * BS + 2 * c;
+        uint32_t af[KS][4];
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            af[ks][0] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(x0 + ks * 16)) : 0u;
+            af[ks][1] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(x1 + ks * 16)) : 0u;
+            af[ks][2] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(x0 + ks * 16 + 8)) : 0u;
+            af[ks][3] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(x1 + ks * 16 + 8)) : 0u;
+        }
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) af[ks][q] = to_f16x2<Tin>(af[ks][q]);
+        float acc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_f16(acc[nt], af[ks], bf[ks][nt][0], bf[ks][nt][1]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            if (v0) *reinterpret_cast<uint32_t*>(hrow + r0 * BS + nt * 8 + 2 * c) = pack_f16x2(acc[nt][0], acc[nt][1]);
+            if (v1) *reinterpret_cast<uint32_t*>(hrow + r1 * BS + nt * 8 + 2 * c) = pack_f16x2(acc[nt][2], acc[nt][3]);
+        }
+    }
+    if (blockIdx.x == 0) {
+        for (long long n = (long long)B * BS + threadIdx.x; n < Npad; n += blockDim.x) hrow[n] = __float2half_rn(0.f);
+    }
+}
+
+// WBt16[j][r][s] = fp16(WB[j][s][r]).
+__global__ void pack_wb_kernel(const float* __restrict__ WB, __half* __restrict__ WBt16, int nb, int bs) {
+    const long long total = (long long)nb * bs * bs;
+    for (long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const long long j = idx / ((long long)bs * bs);
+        const int rem = (int)(idx - j * bs * bs);
+        const int r = rem / bs, s = rem - r * bs;
+        const float v = WB[(size_t)j * bs * bs + (size_t)s * bs + r];
+        WBt16[idx] = __float2half_rn(v);
     }
 }
 
@@ -191,26 +327,100 @@ __global__ void unimix_local_generic_kernel(const Tx* __restrict__ X, long long 
 }
 
 // ---------------------------------------------------------------------------
-// Rows after the global step: one warp per (b, t) row of D values.  Element p
-// = t D + d of sample b sits in Yt at (p / bs, b bs + p % bs); a lane walks its
-// elements 32 apart, carrying (block, offset) forward instead of dividing.
-// LN: S[t][b][:] = LN1(X + Y) in the operand type; otherwise Y in Tout.
+// Residual + LN1 after the global step, one warp per (b, t) row of D values:
+// S[t][b][:] = LN1(X[b][t][:] + Y[b][t][:]) in the operand type, token-major.
+// Y is the global product in the sample-major layout (operand type).
 // ---------------------------------------------------------------------------
-template <typename Tx, typename Top, typename Tout, bool LN, int NI>
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&o)[8]) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const float2 f = __bfloat1622float2(h[u]);
+        o[2 * u] = f.x;
+        o[2 * u + 1] = f.y;
+    }
+}
+__device__ __forceinline__ void load8(const __half* p, float (&o)[8]) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p));
+    const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const float2 f = __half22float2(h[u]);
+        o[2 * u] = f.x;
+        o[2 * u + 1] = f.y;
+    }
+}
+
+// 2-byte types, D = 256 NG: lane l holds values 256 k + 8 l .. + 7 of the row.
+template <typename Tx, int NG>
 __global__ void __launch_bounds__(256)
-unimix_rows_kernel(const Tx* __restrict__ X, const Top* __restrict__ Yt, Tout* __restrict__ out,
-                   const float* __restrict__ g1, const float* __restrict__ be1, int B, int T, int D, int bs,
-                   long long Npitch, int Bcap, float eps) {
+unimix_ln1_vec_kernel(const Tx* __restrict__ X, const __half* __restrict__ Y, __half* __restrict__ S,
+                      const float* __restrict__ g1, const float* __restrict__ be1, int B, int T, int D, int Bcap,
+                      float eps) {
     const int lane = threadIdx.x & 31;
     const long long rows = (long long)B * T;
     for (long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < rows;
          row += ((long long)gridDim.x * blockDim.x) >> 5) {
         const long long b = row / T;
         const int t = (int)(row - b * T);
-        const long long p = (long long)t * D + lane;
-        long long i = p / bs;
-        int r = (int)(p - i * bs);
-        const Top* ycol = Yt + b * bs;
+        float v[NG][8];
+        float sum = 0.f;
+#pragma unroll
+        for (int k = 0; k < NG; ++k) {
+            const int d = 256 * k + 8 * lane;
+            float x[8];
+            load8(X + row * D + d, x);
+            load8(Y + row * D + d, v[k]);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                v[k][u] += x[u];
+                sum += v[k][u];
+            }
+        }
+        const float mean = warp_sum(sum) / (float)D;
+        float sq = 0.f;
+#pragma unroll
+        for (int k = 0; k < NG; ++k)
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const float e = v[k][u] - mean;
+                sq += e * e;
+            }
+        const float rstd = rsqrtf(warp_sum(sq) / (float)D + eps);
+        __half* srow = S + ((size_t)t * Bcap + b) * D;
+#pragma unroll
+        for (int k = 0; k < NG; ++k) {
+            const int d = 256 * k + 8 * lane;
+            const float4 ga = __ldg(reinterpret_cast<const float4*>(g1 + d));
+            const float4 gb = __ldg(reinterpret_cast<const float4*>(g1 + d + 4));
+            const float4 ba = __ldg(reinterpret_cast<const float4*>(be1 + d));
+            const float4 bb = __ldg(reinterpret_cast<const float4*>(be1 + d + 4));
+            const float gg[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+            const float be[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
+            uint4 w;
+            uint32_t* pw = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                pw[u] = pack_f16x2(fmaf((v[k][2 * u] - mean) * rstd, gg[2 * u], be[2 * u]),
+                                   fmaf((v[k][2 * u + 1] - mean) * rstd, gg[2 * u + 1], be[2 * u + 1]));
+            *reinterpret_cast<uint4*>(srow + d) = w;
+        }
+    }
+}
+
+// Any D <= 32 NI and type: lane l holds values l + 32 k.
+template <typename Tx, typename Top, int NI>
+__global__ void __launch_bounds__(256)
+unimix_ln1_kernel(const Tx* __restrict__ X, const Top* __restrict__ Y, Top* __restrict__ S,
+                  const float* __restrict__ g1, const float* __restrict__ be1, int B, int T, int D, int Bcap,
+                  float eps) {
+    const int lane = threadIdx.x & 31;
+    const long long rows = (long long)B * T;
+    for (long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; row < rows;
+         row += ((long long)gridDim.x * blockDim.x) >> 5) {
+        const long long b = row / T;
+        const int t = (int)(row - b * T);
         float v[NI];
         float sum = 0.f;
 #pragma unroll
@@ -218,75 +428,85 @@ unimix_rows_kernel(const Tx* __restrict__ X, const Top* __restrict__ Yt, Tout* _
             const int d = lane + 32 * k;
             v[k] = 0.f;
             if (d < D) {
-                float y = to_f32(ycol[i * Npitch + r]);
-                if (LN) y += XLoad<Tx>::at(X + row * D + d);
-                v[k] = y;
-                sum += y;
-            }
-            r += 32;
-            while (r >= bs) {
-                r -= bs;
-                ++i;
+                v[k] = to_f32(Y[row * D + d]) + XLoad<Tx>::at(X + row * D + d);
+                sum += v[k];
             }
         }
-        if (LN) {
-            const float mean = warp_sum(sum) / (float)D;
-            float sq = 0.f;
+        const float mean = warp_sum(sum) / (float)D;
+        float sq = 0.f;
 #pragma unroll
-            for (int k = 0; k < NI; ++k)
-                if (lane + 32 * k < D) {
-                    const float e = v[k] - mean;
-                    sq += e * e;
-                }
-            const float rstd = rsqrtf(warp_sum(sq) / (float)D + eps);
-            Tout* srow = out + ((size_t)t * Bcap + b) * D;
-#pragma unroll
-            for (int k = 0; k < NI; ++k) {
-                const int d = lane + 32 * k;
-                if (d < D) srow[d] = from_f32<Tout>(fmaf((v[k] - mean) * rstd, g1[d], be1[d]));
+        for (int k = 0; k < NI; ++k)
+            if (lane + 32 * k < D) {
+                const float e = v[k] - mean;
+                sq += e * e;
             }
-        } else {
-            Tout* yrow = out + row * D;
+        const float rstd = rsqrtf(warp_sum(sq) / (float)D + eps);
+        Top* srow = S + ((size_t)t * Bcap + b) * D;
 #pragma unroll
-            for (int k = 0; k < NI; ++k) {
-                const int d = lane + 32 * k;
-                if (d < D) yrow[d] = from_f32<Tout>(v[k]);
-            }
+        for (int k = 0; k < NI; ++k) {
+            const int d = lane + 32 * k;
+            if (d < D) srow[d] = from_f32<Top>(fmaf((v[k] - mean) * rstd, g1[d], be1[d]));
         }
     }
 }
 
-template <typename Tx, typename Top, typename Tout, bool LN>
-cudaError_t launch_rows(const void* X, const void* Yt, void* out, const float* g1, const float* be1, int B, int T,
-                        int D, int bs, long long Npitch, int Bcap, float eps, int num_sms, cudaStream_t s) {
-    const long long rows = (long long)B * T;
+template <typename Top, typename Tout>
+__global__ void convert_kernel(const Top* __restrict__ in, Tout* __restrict__ out, long long n) {
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+        out[i] = from_f32<Tout>(to_f32(in[i]));
+}
+
+int rows_grid(long long rows, int num_sms) {
     long long grid = (rows + 7) / 8;
     if (grid > (long long)num_sms * 16) grid = (long long)num_sms * 16;
-    if (grid < 1) grid = 1;
-#define RM_ROWS(NI)                                                                                            \
-    unimix_rows_kernel<Tx, Top, Tout, LN, NI><<<(int)grid, 256, 0, s>>>(                                       \
-        (const Tx*)X, (const Top*)Yt, (Tout*)out, g1, be1, B, T, D, bs, Npitch, Bcap, eps)
+    return grid < 1 ? 1 : (int)grid;
+}
+
+template <typename Tx, typename Top>
+cudaError_t launch_ln1_t(const void* X, const void* Y, void* S, const float* g1, const float* be1, int B, int T,
+                         int D, int Bcap, float eps, int num_sms, cudaStream_t s) {
+    const int grid = rows_grid((long long)B * T, num_sms);
+    if constexpr (sizeof(Tx) == 2 && std::is_same<Top, __half>::value) {
+        if (D % 256 == 0 && D <= 1536) {
+#define RM_LN1V(NG)                                                                                            \
+    unimix_ln1_vec_kernel<Tx, NG><<<grid, 256, 0, s>>>((const Tx*)X, (const __half*)Y, (__half*)S, g1, be1, B, T, \
+                                                       D, Bcap, eps)
+            switch (D / 256) {
+                case 1: RM_LN1V(1); break;
+                case 2: RM_LN1V(2); break;
+                case 3: RM_LN1V(3); break;
+                case 4: RM_LN1V(4); break;
+                case 5: RM_LN1V(5); break;
+                default: RM_LN1V(6); break;
+            }
+#undef RM_LN1V
+            return cudaGetLastError();
+        }
+    }
+#define RM_LN1(NI)                                                                                          \
+    unimix_ln1_kernel<Tx, Top, NI><<<grid, 256, 0, s>>>((const Tx*)X, (const Top*)Y, (Top*)S, g1, be1, B, T, D, \
+                                                        Bcap, eps)
     const int ni = (D + 31) / 32;
-    if (ni <= 8) RM_ROWS(8);
-    else if (ni <= 16) RM_ROWS(16);
-    else if (ni <= 32) RM_ROWS(32);
-    else if (ni <= 48) RM_ROWS(48);
+    if (ni <= 8) RM_LN1(8);
+    else if (ni <= 16) RM_LN1(16);
+    else if (ni <= 32) RM_LN1(32);
+    else if (ni <= 48) RM_LN1(48);
     else return cudaErrorNotSupported;
-#undef RM_ROWS
+#undef RM_LN1
     return cudaGetLastError();
 }
 
 template <typename Tx, typename Top>
 cudaError_t launch_local_t(const void* X, long long x_stride, const float* WB, void* H, int B, int nb, int bs,
                            long long Npitch, long long Npad, cudaStream_t s) {
-    if (bs % 4 == 0 && bs <= 64) {
-        constexpr int SPT = 8;
-        const int rq = bs / 4;
-        const int SG = 256 / rq;
+    constexpr int VE = 16 / (int)sizeof(Tx);
+    if (bs % 8 == 0 && bs % VE == 0 && bs <= 64) {
+        const int rq = bs / 8;
+        const int SG = 128 / rq;
         const int threads = SG * rq;
-        const int SB = SG * SPT;
-        const size_t smem = ((size_t)bs * bs + (size_t)SB * (bs + 1)) * sizeof(float);
-        auto k = unimix_local_kernel<Tx, Top, SPT>;
+        const int SB = SG * 8;
+        const size_t smem = (size_t)bs * bs * sizeof(float) + (size_t)SB * (bs + 1) * sizeof(float2);
+        auto k = unimix_local_kernel<Tx, Top>;
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         const dim3 grid((unsigned)((B + SB - 1) / SB), (unsigned)nb);
@@ -318,9 +538,41 @@ cudaError_t launch_sinkhorn(const float* W, int count, int n, float tau, int ite
     return cudaGetLastError();
 }
 
-cudaError_t launch_unimix_local(XType xt, Act act, const void* X, long long x_stride, const float* WB, void* H, int B,
-                                int nb, int bs, long long Npitch, long long Npad, cudaStream_t s) {
+template <typename Tin>
+cudaError_t launch_mma_t(const void* X, long long x_stride, const void* WBt16, void* H, int B, int nb, int bs,
+                         long long Npitch, long long Npad, cudaStream_t s) {
+    const long long per_cta = 16LL * kMmaWarps * kMmaTilesPerWarp;
+    const dim3 grid((unsigned)((B + per_cta - 1) / per_cta), (unsigned)nb);
+#define RM_MMA(BSV)                                                                                          \
+    unimix_local_mma_kernel<Tin, BSV><<<grid, 32 * kMmaWarps, 0, s>>>((const Tin*)X, x_stride, (const __half*)WBt16, \
+                                                                       (__half*)H, B, Npitch, Npad)
+    switch (bs) {
+        case 16: RM_MMA(16); break;
+        case 32: RM_MMA(32); break;
+        case 48: RM_MMA(48); break;
+        case 64: RM_MMA(64); break;
+        default: return cudaErrorNotSupported;
+    }
+#undef RM_MMA
+    return cudaGetLastError();
+}
+
+bool unimix_local_mma_ok(int bs) { return bs == 16 || bs == 32 || bs == 48 || bs == 64; }
+
+cudaError_t launch_unimix_pack_wb(const float* WB, void* WBt16, int nb, int bs, cudaStream_t s) {
+    pack_wb_kernel<<<grid_of((long long)nb * bs * bs, 256), 256, 0, s>>>(WB, (__half*)WBt16, nb, bs);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_unimix_local(XType xt, Act act, const void* X, long long x_stride, const float* WB,
+                                const void* WBt16, void* H, int B, int nb, int bs, long long Npitch, long long Npad,
+                                cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
+    if (act != Act::F32 && WBt16 && unimix_local_mma_ok(bs) && x_stride % 8 == 0) {
+        if (xt == XType::BF16)
+            return launch_mma_t<__nv_bfloat16>(X, x_stride, WBt16, H, B, nb, bs, Npitch, Npad, s);
+        if (xt == XType::F16) return launch_mma_t<__half>(X, x_stride, WBt16, H, B, nb, bs, Npitch, Npad, s);
+    }
     if (act == Act::F32) {
         if (xt != XType::F32) return cudaErrorInvalidValue;
         return launch_local_t<float, float>(X, x_stride, WB, H, B, nb, bs, Npitch, Npad, s);
@@ -330,31 +582,25 @@ cudaError_t launch_unimix_local(XType xt, Act act, const void* X, long long x_st
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_unimix_ln1(XType xt, Act act, const void* X, const void* Yt, void* S, const float* g1,
-                              const float* be1, int B, int T, int D, int bs, long long Npitch, int Bcap, float eps,
-                              int num_sms, cudaStream_t s) {
+cudaError_t launch_unimix_ln1(XType xt, Act act, const void* X, const void* Y, void* S, const float* g1,
+                              const float* be1, int B, int T, int D, int Bcap, float eps, int num_sms,
+                              cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     if (act == Act::F32) {
         if (xt != XType::F32) return cudaErrorInvalidValue;
-        return launch_rows<float, float, float, true>(X, Yt, S, g1, be1, B, T, D, bs, Npitch, Bcap, eps, num_sms, s);
+        return launch_ln1_t<float, float>(X, Y, S, g1, be1, B, T, D, Bcap, eps, num_sms, s);
     }
-    if (xt == XType::BF16)
-        return launch_rows<__nv_bfloat16, __half, __half, true>(X, Yt, S, g1, be1, B, T, D, bs, Npitch, Bcap, eps,
-                                                                num_sms, s);
-    if (xt == XType::F16)
-        return launch_rows<__half, __half, __half, true>(X, Yt, S, g1, be1, B, T, D, bs, Npitch, Bcap, eps, num_sms,
-                                                         s);
+    if (xt == XType::BF16) return launch_ln1_t<__nv_bfloat16, __half>(X, Y, S, g1, be1, B, T, D, Bcap, eps, num_sms, s);
+    if (xt == XType::F16) return launch_ln1_t<__half, __half>(X, Y, S, g1, be1, B, T, D, Bcap, eps, num_sms, s);
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_unimix_gather(Act act, const void* Yt, void* Y, int B, int T, int D, int bs, long long Npitch,
-                                 int num_sms, cudaStream_t s) {
-    if (B <= 0) return cudaSuccess;
+cudaError_t launch_unimix_out(Act act, const void* Y, void* out, long long n, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
     if (act == Act::F32)
-        return launch_rows<float, float, float, false>(nullptr, Yt, Y, nullptr, nullptr, B, T, D, bs, Npitch, B, 0.f,
-                                                       num_sms, s);
-    return launch_rows<__half, __half, __nv_bfloat16, false>(nullptr, Yt, Y, nullptr, nullptr, B, T, D, bs, Npitch, B,
-                                                             0.f, num_sms, s);
+        return cudaMemcpyAsync(out, Y, (size_t)n * sizeof(float), cudaMemcpyDeviceToDevice, s);
+    convert_kernel<__half, __nv_bfloat16><<<grid_of(n, 256), 256, 0, s>>>((const __half*)Y, (__nv_bfloat16*)out, n);
+    return cudaGetLastError();
 }
 
 }  // namespace rm

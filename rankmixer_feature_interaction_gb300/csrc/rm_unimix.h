@@ -8,7 +8,8 @@
 // is out_i = sum_j WG[i][j] h_j (WG nb x nb).  On the device the local outputs
 // of all samples are laid out as one matrix H [nb][Npitch] with column
 // b * bs + r holding h_j[r] of sample b, so that the global step is a single
-// dense product Yt = WG H (M = nb, N = B bs, K = nb) on the tensor cores.
+// dense product WG H (M = nb, N = B bs, K = nb) on the tensor cores, whose
+// epilogue stores element (i, b bs + r) at Y[b][i bs + r] (sample-major).
 #pragma once
 
 #include <cuda_runtime.h>
@@ -32,19 +33,26 @@ cudaError_t launch_sinkhorn(const float* W, int count, int n, float tau, int ite
 // and 0 for the padding columns B bs <= n < Npad of every row.  X holds B
 // samples of L = nb bs values, `x_stride` apart, in type xt (caller dtype or
 // the operand type); H is the operand type of act (fp16 for bf16 contexts).
+// bf16 contexts with bs in {16, 32, 48, 64} run it on the tensor cores
+// (mma.sync, fp16 operands) from the transposed fp16 copy WBt16 [nb][bs][bs]
+// (row r, column s = WB[j][s][r], see launch_unimix_pack_wb), otherwise on the
+// CUDA cores from WB (float32).
 enum class XType { BF16, F16, F32 };
-cudaError_t launch_unimix_local(XType xt, Act act, const void* X, long long x_stride, const float* WB, void* H, int B,
-                                int nb, int bs, long long Npitch, long long Npad, cudaStream_t s);
+cudaError_t launch_unimix_local(XType xt, Act act, const void* X, long long x_stride, const float* WB,
+                                const void* WBt16, void* H, int B, int nb, int bs, long long Npitch, long long Npad,
+                                cudaStream_t s);
+bool unimix_local_mma_ok(int bs);
+cudaError_t launch_unimix_pack_wb(const float* WB, void* WBt16, int nb, int bs, cudaStream_t s);
 
 // Residual + LN1 after the global step: S[t][b][:] = LN1(X[b][t][:] + Y[b][t][:])
-// in the operand type (token-major [T][Bcap][D]) with Y[b][p] = Yt[p / bs][b bs + p % bs].
-cudaError_t launch_unimix_ln1(XType xt, Act act, const void* X, const void* Yt, void* S, const float* g1,
-                              const float* be1, int B, int T, int D, int bs, long long Npitch, int Bcap, float eps,
-                              int num_sms, cudaStream_t s);
+// in the operand type (token-major [T][Bcap][D]); Y is the global product,
+// sample-major [B][T D] in the operand type.
+cudaError_t launch_unimix_ln1(XType xt, Act act, const void* X, const void* Y, void* S, const float* g1,
+                              const float* be1, int B, int T, int D, int Bcap, float eps, int num_sms,
+                              cudaStream_t s);
 
-// Y[b][p] = Yt[p / bs][b bs + p % bs] in the caller dtype (sample-major [B][T D]).
-cudaError_t launch_unimix_gather(Act act, const void* Yt, void* Y, int B, int T, int D, int bs, long long Npitch,
-                                 int num_sms, cudaStream_t s);
+// out[i] = Y[i] in the caller dtype (n values).
+cudaError_t launch_unimix_out(Act act, const void* Y, void* out, long long n, cudaStream_t s);
 
 // X_out[b][t][:] = LN2(Z[t][b][:]) in the operand type (fp16 for bf16
 // contexts): a UniMixing layer's input when it follows another layer.
