@@ -693,7 +693,7 @@ cudaError_t run(const TrainGemm& g, const KArgs& ka, int num_sms, cudaStream_t s
 // 1756 -> 1815, dS 1529 -> 1606) and keep one CTA per tile.  Pairs need at
 // least two 128-row blocks (and whole 256-row tiles of an MN-major A).
 bool use_pair(int epi, const TrainGemm& g, int num_sms) {
-    const bool wanted = epi == TE_GELU2 || (epi == TE_F32 && g.a.mn && g.b.mn);
+    const bool wanted = epi == TE_GELU2 || epi == TE_F16T || (epi == TE_F32 && g.a.mn && g.b.mn);
     return wanted && num_sms >= 2 && g.m_valid > BM && (!g.a.mn || g.M % (2 * BM) == 0);
 }
 
