@@ -609,6 +609,66 @@ __global__ void ln2_out_kernel(const Tz* __restrict__ Z, const float2* __restric
     }
 }
 
+// The same for fp16 Z and D a multiple of 256: lane l finalises values
+// 256 k + 8 l .. + 7 of the row with 16-byte loads and stores (the scalar
+// kernel moves 2 bytes per lane per instruction).  Same expression, same
+// row statistics: bit-identical outputs.
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&o)[8]) {
+    uint4 w;
+    w.x = pack_bf16x2(o[0], o[1]);
+    w.y = pack_bf16x2(o[2], o[3]);
+    w.z = pack_bf16x2(o[4], o[5]);
+    w.w = pack_bf16x2(o[6], o[7]);
+    *reinterpret_cast<uint4*>(p) = w;
+}
+__device__ __forceinline__ void store8(__half* p, const float (&o)[8]) {
+    uint4 w;
+    w.x = pack_f16x2(o[0], o[1]);
+    w.y = pack_f16x2(o[2], o[3]);
+    w.z = pack_f16x2(o[4], o[5]);
+    w.w = pack_f16x2(o[6], o[7]);
+    *reinterpret_cast<uint4*>(p) = w;
+}
+__device__ __forceinline__ void store8(float* p, const float (&o)[8]) {
+    reinterpret_cast<float4*>(p)[0] = make_float4(o[0], o[1], o[2], o[3]);
+    reinterpret_cast<float4*>(p)[1] = make_float4(o[4], o[5], o[6], o[7]);
+}
+
+template <typename Tout>
+__global__ void ln2_out_vec_kernel(const __half* __restrict__ Z, const float2* __restrict__ stats,
+                                   const float* __restrict__ g2, const float* __restrict__ be2, Tout* __restrict__ X,
+                                   int B, int T, int D, int Bcap, int nchunk, int cw, float eps) {
+    const int lane = threadIdx.x & 31;
+    const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+    for (long long r = wid; r < (long long)B * T; r += nw) {
+        const int b = (int)(r / T), t = (int)(r % T);
+        const size_t zr = (size_t)t * Bcap + b;
+        float mean, rstd;
+        merge_row_stats(stats + zr * nchunk, nchunk, cw, D, eps, lane, mean, rstd);
+        const __half* z = Z + zr * D;
+        Tout* x = X + ((size_t)b * T + t) * D;
+        for (int d = 8 * lane; d < D; d += 256) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(z + d));
+            const __half2* h = reinterpret_cast<const __half2*>(&v);
+            const float4 ga = __ldg(reinterpret_cast<const float4*>(g2 + d));
+            const float4 gb = __ldg(reinterpret_cast<const float4*>(g2 + d + 4));
+            const float4 ba = __ldg(reinterpret_cast<const float4*>(be2 + d));
+            const float4 bb = __ldg(reinterpret_cast<const float4*>(be2 + d + 4));
+            const float gg[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+            const float be[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
+            float o[8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 f = __half22float2(h[u]);
+                o[2 * u] = ln_apply(f.x, mean, rstd, gg[2 * u], be[2 * u]);
+                o[2 * u + 1] = ln_apply(f.y, mean, rstd, gg[2 * u + 1], be[2 * u + 1]);
+            }
+            store8(x + d, o);
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Last LN2 finalisation + mean pooling over tokens, one CTA per sample.  The
 // mean is taken over the float32 LN2 outputs in token order; XL (optional)
@@ -871,7 +931,10 @@ cudaError_t launch_ln2_out(Act act, const void* Z, const float2* stats, const fl
                            cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     const int grid = grid_for((long long)B * T * 32, 256, num_sms * 8);
-    if (act == Act::BF16)
+    if (act == Act::BF16 && D % 256 == 0)
+        ln2_out_vec_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2,
+                                                               (__nv_bfloat16*)X_out, B, T, D, Bcap, nchunk, cw, eps);
+    else if (act == Act::BF16)
         ln2_out_kernel<__half, __nv_bfloat16><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2,
                                                                    (__nv_bfloat16*)X_out, B, T, D, Bcap, nchunk, cw,
                                                                    eps);
@@ -885,7 +948,10 @@ cudaError_t launch_ln2_out_op(Act act, const void* Z, const float2* stats, const
                               void* X_out, int B, int T, int D, int Bcap, float eps, int num_sms, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     const int grid = grid_for((long long)B * T * 32, 256, num_sms * 8);
-    if (act == Act::BF16)
+    if (act == Act::BF16 && D % 256 == 0)
+        ln2_out_vec_kernel<__half><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2, (__half*)X_out, B, T, D,
+                                                        Bcap, 1, D, eps);
+    else if (act == Act::BF16)
         ln2_out_kernel<__half, __half><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2, (__half*)X_out, B, T, D,
                                                             Bcap, 1, D, eps);
     else
@@ -898,8 +964,12 @@ cudaError_t launch_ln2_out_f32(const void* Z, const float2* stats, const float* 
                                int B, int T, int D, int Bcap, float eps, int num_sms, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     const int grid = grid_for((long long)B * T * 32, 256, num_sms * 8);
-    ln2_out_kernel<__half, float><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2, X_out, B, T, D, Bcap, 1, D,
+    if (D % 256 == 0)
+        ln2_out_vec_kernel<float><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2, X_out, B, T, D, Bcap, 1, D,
                                                        eps);
+    else
+        ln2_out_kernel<__half, float><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2, X_out, B, T, D, Bcap, 1,
+                                                           D, eps);
     return cudaGetLastError();
 }
 
