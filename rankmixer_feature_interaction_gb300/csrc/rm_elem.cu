@@ -910,6 +910,67 @@ inline int grid_for(long long n, int threads, int cap = 152 * 16) {
     return (int)g;
 }
 
+// Pooled output only (no X_L), fp16 Z, D % 8 == 0: the same fp16-pair sums as
+// pool_kernel's first branch with 16-byte loads, thread l owning columns
+// 8 l .. 8 l + 7 and a CTA of D / 8 threads per sample, so that several
+// CTAs per SM keep more loads in flight.  Same operations in the same order:
+// bit-identical to pool_kernel.
+template <int TB>
+__global__ void __launch_bounds__(256)
+pool_vec_kernel(const __half* __restrict__ Z, const float2* __restrict__ stats, const float* __restrict__ g2,
+                const float* __restrict__ be2, float* __restrict__ pooled, int B, int T, int D, int Bcap, int nchunk,
+                int cw, float eps) {
+    __shared__ __half2 s_rh[kMaxT], s_nmrh[kMaxT];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nwarps = blockDim.x >> 5;
+    const int j = 8 * threadIdx.x;
+    const size_t tstride = (size_t)Bcap * D;
+    for (int b = blockIdx.x; b < B; b += gridDim.x) {
+        for (int t = warp; t < T; t += nwarps) {
+            float mean, rstd;
+            merge_row_stats(stats + ((size_t)t * Bcap + b) * nchunk, nchunk, cw, D, eps, lane, mean, rstd);
+            if (lane == 0) {
+                s_rh[t] = __float2half2_rn(rstd);
+                s_nmrh[t] = __float2half2_rn(-mean * rstd);
+            }
+        }
+        __syncthreads();
+        if (j < D) {
+            const __half* zc = Z + (size_t)b * D + j;
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            for (int t0 = 0; t0 < T; t0 += TB) {
+                uint4 zz[TB];
+#pragma unroll
+                for (int u = 0; u < TB; ++u)
+                    if (t0 + u < T) zz[u] = __ldg(reinterpret_cast<const uint4*>(zc + (size_t)(t0 + u) * tstride));
+                __half2 part[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) part[q] = __float2half2_rn(0.f);
+#pragma unroll
+                for (int u = 0; u < TB; ++u)
+                    if (t0 + u < T) {
+                        const __half2* h = reinterpret_cast<const __half2*>(&zz[u]);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) part[q] = __hadd2(part[q], __hfma2(h[q], s_rh[t0 + u], s_nmrh[t0 + u]));
+                    }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float2 pf = __half22float2(part[q]);
+                    acc[2 * q] += pf.x;
+                    acc[2 * q + 1] += pf.y;
+                }
+            }
+            float o[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) o[u] = fmaf(g2[j + u], acc[u] / (float)T, be2[j + u]);
+            float4* dst = reinterpret_cast<float4*>(pooled + (size_t)b * D + j);
+            dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+            dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+        }
+        __syncthreads();
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_mix_ln1(Act act, bool from_z, const MixLnArgs& a, int num_sms, cudaStream_t s) {
@@ -978,6 +1039,14 @@ cudaError_t launch_pool(Act act, const void* Z, const float2* stats, const float
                         int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     if (T > kMaxT) return cudaErrorNotSupported;
+    if (act == Act::BF16 && XL == nullptr && D % 8 == 0 && D <= 8 * 256) {
+        int threads = (D / 8 + 31) / 32 * 32;
+        if (threads < 64) threads = 64;
+        const int grid = B < num_sms * 10 ? B : num_sms * 10;
+        pool_vec_kernel<kPoolBatch><<<grid, threads, 0, s>>>((const __half*)Z, stats, g2, be2, pooled, B, T, D, Bcap,
+                                                             nchunk, cw, eps);
+        return cudaGetLastError();
+    }
     const int grid = B < num_sms * 8 ? B : num_sms * 8;
     if (act == Act::BF16)
         pool_kernel<__half, __nv_bfloat16><<<grid, kPoolThreads, 0, s>>>((const __half*)Z, stats, g2, be2, pooled,
