@@ -419,20 +419,22 @@ ln2_backward_vec_kernel(const Tz* __restrict__ Z, const float* __restrict__ G, c
 }
 
 // Double-buffered variant (D a multiple of 8, two chunks fit in shared
-// memory): a chunk is 8 rows of one token; while the CTA computes chunk i from
-// one buffer, chunk i + 1 arrives in the other by bulk copies (the 8 Z rows
-// are one contiguous block; the 8 G rows are T D floats apart), completion
-// counted on that buffer's mbarrier with a bounded wait.
-template <typename Tz>
-__global__ void __launch_bounds__(kLn2Threads, 1)
+// memory): a chunk is CH rows of one token; while the CTA computes chunk i
+// from one buffer, chunk i + 1 arrives in the other by bulk copies (the CH Z
+// rows are one contiguous block; the CH G rows are T D floats apart),
+// completion counted on that buffer's mbarrier with a bounded wait.  CH = 4
+// keeps a CTA at 74 KB for the 1B width, so three share an SM and keep three
+// chunks in flight.
+template <typename Tz, int CH>
+__global__ void __launch_bounds__(kLn2Threads)
 ln2_backward_db_kernel(const Tz* __restrict__ Z, const float* __restrict__ G, const float* __restrict__ g2,
                        float* __restrict__ dZ, float* __restrict__ part_db2, float* __restrict__ part_dg2,
                        float* __restrict__ part_dbe2, float* __restrict__ part_max, int B, int T, int D, int Bcap,
                        float eps, int rows_per_cta, int* err, unsigned long long timeout_ns) {
     extern __shared__ float4 smem4[];
-    float4* st = smem4;                                            // [kLn2Chunk]
-    float* gbuf = reinterpret_cast<float*>(smem4 + kLn2Chunk);     // 2 x [kLn2Chunk][D]
-    Tz* zbuf = reinterpret_cast<Tz*>(gbuf + 2 * (size_t)kLn2Chunk * D);   // 2 x [kLn2Chunk][D]
+    float4* st = smem4;                                            // [CH]
+    float* gbuf = reinterpret_cast<float*>(smem4 + CH);     // 2 x [CH][D]
+    Tz* zbuf = reinterpret_cast<Tz*>(gbuf + 2 * (size_t)CH * D);   // 2 x [CH][D]
     __shared__ __align__(8) uint64_t bars[2];
     __shared__ int s_abort;
     __shared__ float wmax[kLn2Threads / 32];
@@ -453,18 +455,18 @@ ln2_backward_db_kernel(const Tz* __restrict__ Z, const float* __restrict__ G, co
     }
     __syncthreads();
     auto issue = [&](int chunk, int buf) {     // thread 0: chunk `chunk` of this CTA into buffer `buf`
-        const int b0 = b_begin + chunk * kLn2Chunk;
-        const int nrows = min(kLn2Chunk, b_end - b0);
+        const int b0 = b_begin + chunk * CH;
+        const int nrows = min(CH, b_end - b0);
         const uint32_t bar = smem_u32(&bars[buf]);
         const uint32_t zbytes = (uint32_t)(nrows * D * sizeof(Tz)), gbytes = (uint32_t)(D * sizeof(float));
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(bar, zbytes + gbytes * (uint32_t)nrows);
-        bulk_copy_g2s(smem_u32(zbuf + (size_t)buf * kLn2Chunk * D), Z + ((size_t)t * Bcap + b0) * D, zbytes, bar);
+        bulk_copy_g2s(smem_u32(zbuf + (size_t)buf * CH * D), Z + ((size_t)t * Bcap + b0) * D, zbytes, bar);
         for (int r = 0; r < nrows; ++r)
-            bulk_copy_g2s(smem_u32(gbuf + ((size_t)buf * kLn2Chunk + r) * D), G + ((size_t)(b0 + r) * T + t) * D,
+            bulk_copy_g2s(smem_u32(gbuf + ((size_t)buf * CH + r) * D), G + ((size_t)(b0 + r) * T + t) * D,
                           gbytes, bar);
     };
-    const int nchunks = b_end > b_begin ? (b_end - b_begin + kLn2Chunk - 1) / kLn2Chunk : 0;
+    const int nchunks = b_end > b_begin ? (b_end - b_begin + CH - 1) / CH : 0;
     if (threadIdx.x == 0 && nchunks > 0) issue(0, 0);
     for (int i = 0; i < nchunks; ++i) {
         const int buf = i & 1;
@@ -477,10 +479,10 @@ ln2_backward_db_kernel(const Tz* __restrict__ Z, const float* __restrict__ G, co
             }
             break;
         }
-        const int b0 = b_begin + i * kLn2Chunk;
-        const int nrows = min(kLn2Chunk, b_end - b0);
-        const Tz* zs = zbuf + (size_t)buf * kLn2Chunk * D;
-        const float* gs = gbuf + (size_t)buf * kLn2Chunk * D;
+        const int b0 = b_begin + i * CH;
+        const int nrows = min(CH, b_end - b0);
+        const Tz* zs = zbuf + (size_t)buf * CH * D;
+        const float* gs = gbuf + (size_t)buf * CH * D;
         if (warp < nrows) {
             const Tz* z = zs + (size_t)warp * D;
             const float* gr = gs + (size_t)warp * D;
@@ -982,16 +984,30 @@ cudaError_t launch_ln1_recompute(Act act, bool x_f32, const void* X, void* S, vo
 }
 
 constexpr int kLn2DbSmemLimit = 220 * 1024;
+constexpr int kLn2DbChunk = 4;             // rows per chunk of the double-buffered kernel
 
-bool ln2_bwd_double_buffered(Act act, int D) {
+size_t ln2_db_bytes(Act act, int D) {
     const size_t zsz = act == Act::F32 ? 4 : 2;
-    return D % 8 == 0 && kLn2Chunk * sizeof(float4) + 2 * (size_t)kLn2Chunk * D * (4 + zsz) <= (size_t)kLn2DbSmemLimit;
+    return kLn2DbChunk * sizeof(float4) + 2 * (size_t)kLn2DbChunk * D * (4 + zsz);
 }
 
+bool ln2_bwd_double_buffered(Act act, int D) {
+    return D % 8 == 0 && ln2_db_bytes(act, D) <= (size_t)kLn2DbSmemLimit;
+}
+
+// CTAs per token: as many as fill the SMs in one wave (rounded down, so that
+// no CTA waits for a second wave), at most one per chunk.
 int ln2_bwd_blocks(Act act, int B, int T, int D, int num_sms) {
-    const int per_sm = ln2_bwd_double_buffered(act, D) ? 1 : 3;
-    const int want = (per_sm * num_sms + T - 1) / T;
-    const int most = (B + kLn2Chunk - 1) / kLn2Chunk;
+    int per_sm = 3;
+    int chunk = kLn2Chunk;
+    if (ln2_bwd_double_buffered(act, D)) {
+        per_sm = (int)((227 * 1024) / (ln2_db_bytes(act, D) + 1024));
+        if (per_sm > 3) per_sm = 3;
+        if (per_sm < 1) per_sm = 1;
+        chunk = kLn2DbChunk;
+    }
+    const int want = per_sm * num_sms / T;
+    const int most = (B + chunk - 1) / chunk;
     const int n = want < most ? want : most;
     return n < 1 ? 1 : n;
 }
@@ -1002,19 +1018,19 @@ cudaError_t launch_ln2_backward(Act act, const void* Z, const float* G, const fl
     if (B <= 0) return cudaSuccess;
     if (D > kLn2MaxCols * kLn2Threads) return cudaErrorNotSupported;
     const int nbx = ln2_bwd_blocks(act, B, T, D, num_sms);
-    const int per = ((B + nbx - 1) / nbx + kLn2Chunk - 1) / kLn2Chunk * kLn2Chunk;
     const dim3 grid(nbx, T);
     const size_t zsz = act == Act::F32 ? 4 : 2;
     if (ln2_bwd_double_buffered(act, D)) {
-        const size_t dbytes = kLn2Chunk * sizeof(float4) + 2 * (size_t)kLn2Chunk * D * (4 + zsz);
+        const int per = ((B + nbx - 1) / nbx + kLn2DbChunk - 1) / kLn2DbChunk * kLn2DbChunk;
+        const size_t dbytes = ln2_db_bytes(act, D);
         if (act == Act::F32) {
-            auto k = ln2_backward_db_kernel<float>;
+            auto k = ln2_backward_db_kernel<float, kLn2DbChunk>;
             cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dbytes);
             if (e != cudaSuccess) return e;
             k<<<grid, kLn2Threads, dbytes, s>>>((const float*)Z, G, g2, dZ, part_db2, part_dg2, part_dbe2, part_max,
                                                 B, T, D, Bcap, eps, per, err, timeout_ns);
         } else {
-            auto k = ln2_backward_db_kernel<__half>;
+            auto k = ln2_backward_db_kernel<__half, kLn2DbChunk>;
             cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dbytes);
             if (e != cudaSuccess) return e;
             k<<<grid, kLn2Threads, dbytes, s>>>((const __half*)Z, G, g2, dZ, part_db2, part_dg2, part_dbe2, part_max,
@@ -1022,6 +1038,7 @@ cudaError_t launch_ln2_backward(Act act, const void* Z, const float* G, const fl
         }
         return cudaGetLastError();
     }
+    const int per = ((B + nbx - 1) / nbx + kLn2Chunk - 1) / kLn2Chunk * kLn2Chunk;
     const size_t bytes = kLn2Chunk * sizeof(float4) + (size_t)kLn2Chunk * D * (4 + zsz);
     const bool vec = D % 8 == 0;               // whole 16-byte lines of fp16 rows and float4 of float rows
     if (vec) {
