@@ -152,7 +152,7 @@ def test_deterministic_reruns():
     assert torch.equal(p1, p2) and torch.equal(x1, x2)
 
 
-@pytest.mark.parametrize("B", [100, 2500])      # one shot; three pipelined chunks (1024, 1024, 452)
+@pytest.mark.parametrize("B", [100, 2500])      # one shot; three pipelined chunks (512, 1024, 964)
 def test_host_entry_matches_device_entry(B):
     T, D, k, L = 8, 512, 4, 2
     m, _, X = _build(T, D, k, L, B, 23, "bf16")
