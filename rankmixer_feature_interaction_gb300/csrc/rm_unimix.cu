@@ -88,10 +88,11 @@ __global__ void sk_fin_kernel(const float* __restrict__ C, const float* __restri
     }
 }
 
+// Blocks for a grid-stride loop over `work` items (capped: the loops stride).
 int grid_of(long long work, int threads) {
     long long g = (work + threads - 1) / threads;
     if (g < 1) g = 1;
-    if (g > 152 * 32) g = 152 * 32;
+    if (g > 4096) g = 4096;
     return (int)g;
 }
 
