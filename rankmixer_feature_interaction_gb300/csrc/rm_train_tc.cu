@@ -99,6 +99,7 @@ struct KArgs {
     int colpart_rows;      // partial rows per group: ceil(M / 32)
     int um_bs, um_B;       // TE_F16T: block size and samples
     long long um_L;        // TE_F16T: values per sample
+    int m_fast;            // tile order: M tiles fastest (else N tiles fastest)
     int* err;
     unsigned long long timeout_ns;
 };
@@ -139,8 +140,13 @@ __device__ __forceinline__ void tile_of(long long tile, const KArgs& a, int& g, 
     const long long per_group = (long long)a.m_tiles * a.n_tiles;
     g = (int)(tile / per_group);
     const int rem = (int)(tile - (long long)g * per_group);
-    mb = rem / a.n_tiles;          // N tiles fastest: neighbouring CTAs share the A tile
-    nb = rem - mb * a.n_tiles;
+    if (a.m_fast) {                // M tiles fastest: neighbouring CTAs share the B tile
+        nb = rem / a.m_tiles;
+        mb = rem - nb * a.m_tiles;
+    } else {                       // N tiles fastest: neighbouring CTAs share the A tile
+        mb = rem / a.n_tiles;
+        nb = rem - mb * a.n_tiles;
+    }
 }
 
 // Two floats to an fp16 pair, saturating at +-65504 instead of overflowing.
@@ -746,6 +752,15 @@ cudaError_t launch_train_gemm_tc(int epi, const TrainGemm& g, int num_sms, cudaS
     ka.um_bs = g.um_bs;
     ka.um_B = g.um_B;
     ka.um_L = g.um_L;
+    // Tile order.  N tiles fastest re-reads a group's whole B operand once per M
+    // tile, which costs DRAM traffic only when B outgrows L2; then walk M fastest
+    // if A is the smaller operand (UniMixing's global product: A 2 MB, B 403 MB
+    // at the 1B shape read 4x from DRAM in N order).  Every other product here has
+    // per-group operands within L2 and keeps N order.
+    {
+        const double a_bytes = 2.0 * (double)g.m_valid * g.K, b_bytes = 2.0 * (double)g.N * g.K;
+        ka.m_fast = (b_bytes > 64.0 * 1024 * 1024 && a_bytes < b_bytes && ka.m_tiles > 1) ? 1 : 0;
+    }
     ka.colpart_rows = train_colpart_rows(g, num_sms);
     ka.err = g.err;
     ka.timeout_ns = g.timeout_ns;
