@@ -163,6 +163,63 @@ ln1_recompute_pair_kernel(const Tx* __restrict__ X, Top* __restrict__ S, Tyh* __
     }
 }
 
+// The same with the sample staged in shared memory: a CTA of 1024 threads
+// loads sample b's T x D inputs once with 16-byte loads, then a warp per token
+// row runs both passes from there (the pair kernel above reads each sample's
+// rows about four times through L2).  Same arithmetic in the same order.
+constexpr int kLn1RecThreads = 1024;
+constexpr size_t kLn1RecSmemLimit = 200 * 1024;
+
+template <typename Tx, typename Top, typename Tyh>
+__global__ void __launch_bounds__(kLn1RecThreads, 1)
+ln1_recompute_staged_kernel(const Tx* __restrict__ X, Top* __restrict__ S, Tyh* __restrict__ Yh,
+                            float* __restrict__ rstd_out, const float* __restrict__ g1, const float* __restrict__ be1,
+                            int B, int T, int D, int Bcap, float eps, QDiv qd) {
+    extern __shared__ uint4 xs4[];
+    const Tx* xs = reinterpret_cast<const Tx*>(xs4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nw = blockDim.x >> 5;
+    const int q = (int)qd.q;
+    const int n16 = (int)((size_t)T * D * sizeof(Tx) / 16);
+    for (int b = blockIdx.x; b < B; b += gridDim.x) {
+        __syncthreads();                       // the previous sample's rows are no longer read
+        const uint4* src = reinterpret_cast<const uint4*>(X + (size_t)b * T * D);
+#pragma unroll 4
+        for (int i = threadIdx.x; i < n16; i += blockDim.x) xs4[i] = __ldg(src + i);
+        __syncthreads();
+        for (int t = warp; t < T; t += nw) {
+            const Tx* Xt = xs + (size_t)t * D;
+            const float shift = to_f32(xs[(size_t)t * q]) + to_f32(Xt[0]);
+            float s1 = 0.f, s2 = 0.f;
+            for (int k = 2 * lane; k < D; k += 64) {
+                const int c = qd.div(k), r = k - c * q;
+                const float2 m = ld_pair<Tx>(xs + (size_t)c * D + (size_t)t * q + r);
+                const float2 x = ld_pair<Tx>(Xt + k);
+                const float d0 = m.x + x.x - shift, d1 = m.y + x.y - shift;
+                s1 += d0 + d1;
+                s2 = fmaf(d0, d0, fmaf(d1, d1, s2));
+            }
+            s1 = warp_sum(s1);
+            s2 = warp_sum(s2);
+            const float dm = s1 / (float)D;
+            const float mean = shift + dm;
+            const float rstd = rsqrtf(fmaxf(s2 / (float)D - dm * dm, 0.f) + eps);
+            const size_t o = ((size_t)t * Bcap + b) * D;
+            for (int k = 2 * lane; k < D; k += 64) {
+                const int c = qd.div(k), r = k - c * q;
+                const float2 m = ld_pair<Tx>(xs + (size_t)c * D + (size_t)t * q + r);
+                const float2 x = ld_pair<Tx>(Xt + k);
+                const float2 ga = *reinterpret_cast<const float2*>(g1 + k);
+                const float2 be = *reinterpret_cast<const float2*>(be1 + k);
+                const float y0 = (m.x + x.x - mean) * rstd, y1 = (m.y + x.y - mean) * rstd;
+                st_pair<Top>(S + o + k, fmaf(ga.x, y0, be.x), fmaf(ga.y, y1, be.y));
+                st_pair<Tyh>(Yh + o + k, y0, y1);
+            }
+            if (lane == 0) rstd_out[(size_t)t * Bcap + b] = rstd;
+        }
+    }
+}
+
 // ---- LN2 backward ----------------------------------------------------------------
 // Grid (nbx, T): CTA (x, t) walks its share of token t's rows in chunks of 8,
 // each chunk staged in shared memory (Z and G rows) so both passes read it
@@ -959,6 +1016,29 @@ cudaError_t launch_ln1_recompute(Act act, bool x_f32, const void* X, void* S, vo
     if (B <= 0) return cudaSuccess;
     const int grid = grid_for((long long)B * T, 8, num_sms * 8);
     const QDiv qd = make_qdiv(D / T);
+    const size_t esz = (act == Act::F32 || x_f32) ? 4 : 2;
+    const size_t smem = (size_t)T * D * esz;
+    if ((D / T) % 2 == 0 && smem % 16 == 0 && smem <= kLn1RecSmemLimit && act != Act::F32) {
+        // two CTAs of 512 threads per SM when two samples fit (bf16 inputs at the
+        // 1B width), else one of 1024 (float32 inputs)
+        const int per_sm = smem <= 100 * 1024 ? 2 : 1;
+        const int threads = per_sm == 2 ? kLn1RecThreads / 2 : kLn1RecThreads;
+        const int sgrid = B < num_sms * per_sm ? B : num_sms * per_sm;
+        if (x_f32) {
+            auto k = ln1_recompute_staged_kernel<float, __half, __half>;
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            k<<<sgrid, threads, smem, s>>>((const float*)X, (__half*)S, (__half*)Yh, rstd, g1, be1, B, T, D, Bcap,
+                                            eps, qd);
+        } else {
+            auto k = ln1_recompute_staged_kernel<__nv_bfloat16, __half, __half>;
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            k<<<sgrid, threads, smem, s>>>((const __nv_bfloat16*)X, (__half*)S, (__half*)Yh, rstd, g1, be1, B, T, D,
+                                            Bcap, eps, qd);
+        }
+        return cudaGetLastError();
+    }
     if ((D / T) % 2 == 0) {
         if (act == Act::F32)
             ln1_recompute_pair_kernel<float, float, float><<<grid, 256, 0, s>>>(
