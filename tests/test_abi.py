@@ -114,6 +114,10 @@ def test_null_context_calls(lib):
     assert lib.rm_stack_backward_saved(None, None, None, ctypes.byref(grads), 1, None) == _lib.RM_ERR_INVALID_ARG
     assert lib.rm_debug_gelu_grad(None, None, -1, None) == _lib.RM_ERR_INVALID_ARG   # n < 0
     assert lib.rm_debug_gelu_grad(None, None, 3, None) == _lib.RM_ERR_INVALID_ARG    # NULL buffers
+    assert lib.rm_set_unimixing(None, 0, None, None, 4, 1.0, 5, None) == _lib.RM_ERR_INVALID_ARG
+    assert lib.rm_unimixing_weights(None, 0, None, None, None) == _lib.RM_ERR_INVALID_ARG
+    assert lib.rm_unimixing(None, 0, None, None, 1, None) == _lib.RM_ERR_INVALID_ARG
+    assert "ctx is NULL" in _lib.rm_last_error()
 
 
 def test_config_struct_matches_the_header(lib):
