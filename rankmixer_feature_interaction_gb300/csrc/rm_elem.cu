@@ -215,18 +215,6 @@ mix_ln1_staged_kernel(const MixLnArgs a) {
 //   - both LN affines staged in shared memory once per CTA;
 //   - (FROM_Z) LN2 finalised in place, once per element, before mixing.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void to_f32x8(const uint4 v, bool is_bf16, float (&o)[8]) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        float2 f;
-        if (is_bf16) f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
-        else f = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
-        o[2 * k] = f.x;
-        o[2 * k + 1] = f.y;
-    }
-}
-
 // Shared-memory layout of the 8-wide kernel.  Each staged row of D 16-bit
 // elements is padded to a stride RS with RS = q (mod 64): an 8-lane phase of a
 // 16-byte load covers 64 consecutive mixed columns, which may span two source
@@ -235,8 +223,6 @@ __device__ __forceinline__ void to_f32x8(const uint4 v, bool is_bf16, float (&o)
 // distinct 16-byte bank groups.  The LN affines are kept as fp16 (exact: they
 // arrive as bf16 values), so a lane's 8 affines are one 16-byte load.
 __host__ __device__ __forceinline__ int v8_row_stride(int D, int q) { return D + (q & 63); }
-
-__device__ __forceinline__ void f16x8_to_f32(const uint4 v, float (&o)[8]) { to_f32x8(v, false, o); }
 
 // A 32-bit word of two 16-bit values (bf16 or fp16, low half first) -> packed fp32 pair.
 template <bool BF16>
