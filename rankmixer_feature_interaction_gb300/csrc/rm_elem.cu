@@ -889,7 +889,11 @@ __global__ void debug_wait_kernel(const int* flag, int* err, unsigned long long 
     }
 }
 
-inline int grid_for(long long n, int threads, int cap = 152 * 16) {
+// Default cap on the blocks of a grid-stride loop (16 per SM of the 152-SM
+// part; the loops stride, so the cap only bounds the launch size).
+constexpr int kGridStrideCap = 152 * 16;
+
+inline int grid_for(long long n, int threads, int cap = kGridStrideCap) {
     long long g = (n + threads - 1) / threads;
     if (g < 1) g = 1;
     if (g > cap) g = cap;

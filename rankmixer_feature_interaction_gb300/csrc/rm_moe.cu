@@ -705,8 +705,9 @@ cudaError_t moe_forward(const MoeLaunch& ml, const MoeWeights& w, MoeWorkspace& 
 cudaError_t moe_residual_z(Act act, const float* V, const void* S, void* Z, int B, int T, int D, int Bcap,
                            cudaStream_t s) {
     const long long n = (long long)T * B * D;
+    constexpr int kGridStrideCap = 152 * 16;   // blocks of the grid-stride loop (it strides; a launch-size bound)
     int grid = (int)((n + 255) / 256);
-    if (grid > 152 * 16) grid = 152 * 16;
+    if (grid > kGridStrideCap) grid = kGridStrideCap;
     if (act == Act::BF16)
         residual_z_kernel<__half><<<grid, 256, 0, s>>>(V, (const __half*)S, (__half*)Z, B, T, D, Bcap);
     else
