@@ -389,7 +389,9 @@ RM_API rm_status rm_score(rm_ctx *ctx, const void *E, const float *head_w, float
  *     element a call uses is written earlier in the same call, so nothing
  *     needs clearing, but calls that overlap on the GPU (other streams, other
  *     threads, other contexts) race on it: serialise them.
- *   - Dense layers only (RM_ERR_UNSUPPORTED for a Sparse-MoE layer).
+ *   - Dense TokenMixing layers only (RM_ERR_UNSUPPORTED for a Sparse-MoE
+ *     layer, and for a layer set to UniMixing by rm_set_unimixing, whose
+ *     mixing uses the context's workspace).
  * X_in, X_out: device [B][T][D] in the context dtype, 16-byte aligned, not
  * overlapping.  Asynchronous on `stream`. */
 RM_API rm_status rm_block_forward_noalloc(rm_ctx *ctx, int layer, const void *X_in, void *X_out, int B,

@@ -1516,6 +1516,8 @@ rm_status rm_block_forward_noalloc(rm_ctx* c, int layer, const void* X_in, void*
     if (layer < 0 || layer >= g.L) return fail(RM_ERR_INVALID_ARG, "layer %d out of range", layer);
     if (g.moe_layer_mask & (1u << layer))
         return fail(RM_ERR_UNSUPPORTED, "the allocation-free entry point runs dense layers only");
+    if (c->layers[layer].um_bs)   // its mixing needs the context's UniMixing workspace
+        return fail(RM_ERR_UNSUPPORTED, "the allocation-free entry point runs TokenMixing layers only");
     if (B < 1) return fail(RM_ERR_INVALID_ARG, "B must be >= 1");
     if (!X_in || !X_out) return fail(RM_ERR_INVALID_ARG, "X_in / X_out is NULL");
     if (!aligned16(X_in) || !aligned16(X_out)) return fail(RM_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");

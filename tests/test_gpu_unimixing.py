@@ -149,6 +149,12 @@ def test_unimixing_argument_errors():
     with pytest.raises(_lib.RankMixerError) as e:              # layer out of range
         _lib.rm_set_unimixing(m.ctx, 1, WG.data_ptr(), WB.data_ptr(), 16, 1.0, 5, 0)
     assert e.value.status == _lib.RM_ERR_INVALID_ARG
+    # the allocation-free entry point runs TokenMixing layers only
+    m.set_unimixing(0, WG, WB, tau=1.0, iters=5)
+    Y = torch.empty_like(X)
+    with pytest.raises(_lib.RankMixerError) as e:
+        _lib.rm_block_forward_noalloc(m.ctx, 0, X.data_ptr(), Y.data_ptr(), X.shape[0], 0)
+    assert e.value.status == _lib.RM_ERR_UNSUPPORTED
     # training contexts refuse UniMixing layers in their training calls
     mt = RankMixer(T, D, 2, layers, dtype="bf16", max_batch=8, training=True)
     mt.set_unimixing(0, WG, WB, tau=1.0, iters=5)
