@@ -695,7 +695,8 @@ cudaError_t run(const TrainGemm& g, const KArgs& ka, int num_sms, cudaStream_t s
 // device time): the weight gradients, both operands MN-major with six TMA
 // boxes per single-CTA stage (1658 -> 1595 us), and the Gelu / Gelu' product,
 // whose epilogue staging leaves a single CTA only 3 stages (about 1.84 ->
-// 1.71 ms).  The other products ran slower as pairs (Z 1406 -> 1539 us, dU
+// 1.71 ms), and UniMixing's global product (16 k-blocks per tile: 522 -> 339
+// us).  The other products ran slower as pairs (Z 1406 -> 1539 us, dU
 // 1756 -> 1815, dS 1529 -> 1606) and keep one CTA per tile.  Pairs need at
 // least two 128-row blocks (and whole 256-row tiles of an MN-major A).
 bool use_pair(int epi, const TrainGemm& g, int num_sms) {
