@@ -84,6 +84,26 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+# A timed region shorter than this runs as a burst before the power cap pulls
+# the clock down (the dense-GEMM peak measured back to back for seconds is the
+# lower, sustained figure).
+BURST_SECONDS = 1.0
+
+
+def pick_tensor_peak(peaks: dict, src: str, timed_s: float, clk: dict) -> tuple[float, str]:
+    """The dense bf16 peak the timed region ran against: the burst figure when the region
+    lasted under BURST_SECONDS or its median SM clock sat at the maximum, otherwise the
+    sustained (power-capped) figure."""
+    sm, smax = clk.get("sm_mhz"), clk.get("sm_max_mhz")
+    at_max = sm is not None and smax and sm >= 0.97 * smax
+    if timed_s < BURST_SECONDS or at_max:
+        why = f"timed region {timed_s:.2f} s" if timed_s < BURST_SECONDS else f"median SM clock {sm:.0f} MHz (max)"
+        return float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])), f"{src} bf16_tflops (burst: {why})"
+    why = f"timed region {timed_s:.1f} s at median SM clock {sm if sm is not None else 'unknown'} MHz"
+    return (float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])),
+            f"{src} bf16_tflops_sustained ({why})")
+
+
 # ----------------------------------------------------------------------------
 # Clock sampling during the timed region
 # ----------------------------------------------------------------------------
@@ -382,6 +402,7 @@ def run_ours(args):
 
     # ---- roofline of the dominant kernel ------------------------------------------
     peaks, peak_src = load_peaks()
+    peak, peak_why = pick_tensor_peak(peaks, peak_src, ms_max / 1e3, clk)
     flops_gemm = 2.0 * B * T * D * (k * D)          # one GEMM launch of the dense PFFN (either layer)
     gemm_kinds = ["moe_gemm1", "moe_gemm2"] if moe else ["gemm1", "gemm2"]
     # flops per timed scope: one GEMM, or two (the backward's data-gradient pair and recompute pair)
@@ -410,13 +431,13 @@ def run_ours(args):
     if launches > 0 and flops_launch:
         avg_ms = tot_ms / launches
         achieved = flops_launch / (avg_ms / 1e3) / 1e12
-        peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
         kname = {"bwd_wgrad": "train_gemm_wgrad_tcgen05", "bwd_dgrad": "train_gemm_dgrad_tcgen05 (x2 per scope)",
                  "bwd_recompute": "train_gemm_forward_tcgen05 (x2 per scope)"}.get(dom, f"pffn_{dom}_tcgen05")
         roofline = {"kernel": kname, "bound": "tensor", "achieved": round(achieved, 1),
                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                     "traffic": captured_traffic(args.config, B, L, dom) if not (moe and train) else None,
-                    "peak_source": f"{peak_src} bf16_tflops_sustained",
+                    "peak_source": peak_why,
+                    "sm_mhz": clk.get("sm_mhz"),
                     "avg_launch_ms": round(avg_ms, 4)}
     flops_executed = None
     unimix_info = None
@@ -470,8 +491,7 @@ def run_ours(args):
         "tflops": round(flops_step * args.steps * world / (ms_max / 1e3) / 1e12, 1),
         "tflops_executed": round(flops_executed * args.steps * world / (ms_max / 1e3) / 1e12, 1)
         if flops_executed else None,
-        "frac_of_peak_step": round(
-            flops_step * args.steps / (ms_max / 1e3) / 1e12 / peaks.get("bf16_tflops_sustained", 1700.0), 4),
+        "frac_of_peak_step": round(flops_step * args.steps / (ms_max / 1e3) / 1e12 / peak, 4),
         "roofline": roofline,
         "kernels_ms_per_step": {kk: round(v[1] / args.steps, 4) for kk, v in kstats.items() if v[0]},
         "gpu_launches": gpu_launches,
@@ -589,7 +609,23 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def free_port() -> int:
+    import socket
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as so:
+        so.bind(("127.0.0.1", 0))
+        return so.getsockname()[1]
+
+
+def launch_ranks(n: int, argv: list[str]) -> int:
+    """Run this script as n ranks on this node (one process per GPU) under
+    torch.distributed.run, rendezvous on 127.0.0.1; returns its exit status."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(free_port()), os.path.abspath(__file__)] + list(argv)
+    return subprocess.call(cmd)
+
+
 def main(argv=None):
+    argv = list(sys.argv[1:] if argv is None else argv)
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
@@ -607,6 +643,13 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    if "WORLD_SIZE" not in os.environ:
+        if args.gpus > 1:               # N ranks, one per GPU, launched here
+            raise SystemExit(launch_ranks(args.gpus, argv))
+    elif int(os.environ["WORLD_SIZE"]) != args.gpus:
+        ap.error(f"--gpus {args.gpus} disagrees with WORLD_SIZE={os.environ['WORLD_SIZE']} of the launcher")
     if args.impl == "reference":
         run_reference(args)
     else:

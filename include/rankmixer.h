@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define RM_ABI_VERSION 2
+#define RM_ABI_VERSION 3
 
 /* Public symbols are the only ones the shared library exports. */
 #if defined(__GNUC__)
@@ -191,18 +191,26 @@ RM_API rm_status rm_create(const rm_config *cfg, const rm_layer_params *layers, 
 RM_API rm_status rm_destroy(rm_ctx *ctx);
 
 /* One block ("RankMixer" Eq. 1) of layer `layer`: X_out = LN2(PFFN(S) + S) with
- * S = LN1(Mix(X_in) + X_in).  X_in, X_out: device [B][T][D]; they may not
- * overlap.  S_out (nullable): device [B][T][D] receives S in the context
- * dtype.  1 <= B <= max_batch. */
+ * S = LN1(Mix(X_in) + X_in).  X_in: device [B][T][D] in the context dtype.
+ * X_out: device [B][T][D] in out_dtype; it may not overlap X_in.  S_out
+ * (nullable): device [B][T][D] receives S in out_dtype.  out_dtype is the
+ * context dtype or RM_F32: a bf16 context then writes the float32 values
+ * that it otherwise rounds to bf16 (round to nearest even), so the two
+ * outputs of the same call agree bit for bit after that rounding.  A float32
+ * context takes RM_F32 only.  1 <= B <= max_batch.  RM_ERR_INVALID_ARG for
+ * another out_dtype. */
 RM_API rm_status rm_block_forward(rm_ctx *ctx, int layer, const void *X_in, void *X_out, void *S_out,
-                           int B, void *stream);
+                                  rm_dtype out_dtype, int B, void *stream);
 
 /* The whole stack and the mean pooling ("RankMixer" section 3.1): pooled
- * (device float32 [B][D]) = mean_t X_L; XL (nullable, device [B][T][D]) receives
- * X_L.  X0: device [B][T][D].  Agrees with chaining rm_block_forward over the
- * layers up to the rounding of each intermediate X_n (the stack keeps them in
- * fp16 on the device, the chained calls round them to the context dtype). */
-RM_API rm_status rm_stack_forward(rm_ctx *ctx, const void *X0, float *pooled, void *XL, int B, void *stream);
+ * (device float32 [B][D]) = mean_t X_L; XL (nullable, device [B][T][D])
+ * receives X_L in xl_dtype (the context dtype, or RM_F32 for the float32
+ * values before their rounding, as in rm_block_forward).  X0: device
+ * [B][T][D] in the context dtype.  Agrees with chaining rm_block_forward over
+ * the layers up to the rounding of each intermediate X_n (the stack keeps them
+ * in fp16 on the device, the chained calls round them to their out_dtype). */
+RM_API rm_status rm_stack_forward(rm_ctx *ctx, const void *X0, float *pooled, void *XL, rm_dtype xl_dtype, int B,
+                                  void *stream);
 
 /* rm_stack_forward from HOST buffers: copies X0_host ([B][T][D], context dtype)
  * to the device, runs the stack, copies the pooled float32 [B][D] result to
@@ -331,12 +339,14 @@ RM_API rm_status rm_head_forward(const float *pooled, const float *w, float b, c
  * Training calls return RM_ERR_UNSUPPORTED on contexts with UniMixing layers.
  * rm_unimixing_weights: copies the constrained weights (device float32, same
  * layouts; either output may be NULL).  rm_unimixing: Y = UniMixing(X) of
- * layer `layer`, X and Y device [B][T][D] in the context dtype.  Asynchronous
- * on `stream`. */
+ * layer `layer`, X device [B][T][D] in the context dtype, Y device [B][T][D] in
+ * out_dtype (the context dtype, or RM_F32 for the values before their bf16
+ * rounding).  Asynchronous on `stream`. */
 RM_API rm_status rm_set_unimixing(rm_ctx *ctx, int layer, const float *WG, const float *WB, int bs, float tau,
                                   int iters, void *stream);
 RM_API rm_status rm_unimixing_weights(rm_ctx *ctx, int layer, float *WG_out, float *WB_out, void *stream);
-RM_API rm_status rm_unimixing(rm_ctx *ctx, int layer, const void *X, void *Y, int B, void *stream);
+RM_API rm_status rm_unimixing(rm_ctx *ctx, int layer, const void *X, void *Y, rm_dtype out_dtype, int B,
+                              void *stream);
 
 /* Feature tokenization ("RankMixer" section 3.2 Eq. 2; "RankMixer 详解（1）"
  * section 2.4): token t of a sample is the t-th slice of d coordinates of its
@@ -379,12 +389,15 @@ RM_API rm_status rm_score(rm_ctx *ctx, const void *E, const float *head_w, float
  * the library instead of the context's workspace, and allocates nothing.
  *   - The array exists on every GPU that loads the library until the process
  *     exits.  B is limited by it: a call whose intermediates exceed 32 MiB
- *     returns RM_ERR_INVALID_ARG and names the limit (about B <= 48 at
- *     T=32, D=1536, k=4; about B <= 190 at T=16, D=768, k=4).  B is not
- *     limited by cfg.max_batch.
- *   - The first call on a device looks up the array's device address (once
- *     per device, with that device current); make that first call before
- *     any stream capture.
+ *     returns RM_ERR_INVALID_ARG and names the largest B that fits (on the
+ *     tensor-core path B <= 56 at T=32, D=1536, k=4 and B <= 226 at T=16,
+ *     D=768, k=4).  B is not limited by cfg.max_batch.
+ *   - Each call made outside stream capture looks up the array's device
+ *     address on the context's device (a lookup that allocates nothing); a
+ *     call under capture reuses the address of the last uncaptured call on
+ *     that device.  So make the first call on a device before any stream
+ *     capture (a captured first call returns RM_ERR_INVALID_ARG), and after a
+ *     device reset make one uncaptured call before capturing again.
  *   - All calls share the array and it keeps the last call's contents.  Every
  *     element a call uses is written earlier in the same call, so nothing
  *     needs clearing, but calls that overlap on the GPU (other streams, other
@@ -401,6 +414,22 @@ RM_API rm_status rm_block_forward_noalloc(rm_ctx *ctx, int layer, const void *X_
  * q = D / H, for any H dividing D (Y is [B][H][T q]).  A pure permutation of
  * element bits, exact for both dtypes.  X, Y: device, non-overlapping. */
 RM_API rm_status rm_token_mix(const void *X, void *Y, int B, int T, int D, int H, rm_dtype dtype, void *stream);
+
+/* Test hook for the mixing inside the fused mix + LN1 kernel ("RankMixer"
+ * Eq. 3-5; "RankMixer 详解（1）" section 3.1): runs that kernel's gather and
+ * residual sum y[h][t q + r] = X[t][h q + r] + X[h][t q + r] (H = T, q = D/T)
+ * and writes y (device float32, token-major [T][B][D]: row h of sample b at
+ * (h B + b) D) in place of LN1.
+ *   from_z = 0: X is bf16, sample-major [B][T][D] (the first layer's input);
+ *               y is the float32 sum of the two gathered values.
+ *   from_z = 1: X is fp16, token-major [T][B][D] (the form in which a later
+ *               layer's input arrives); the kernel's LN2 finalisation runs as
+ *               the identity and y is the fp16 sum (round to nearest even) of
+ *               the two gathered values, widened to float32.
+ * Needs D % 256 == 0 and (D/T) % 8 == 0 (the shapes the staged kernel
+ * serves; RM_ERR_UNSUPPORTED otherwise).  X, Y: device, 16-byte aligned, not
+ * overlapping.  Runs on the current device; asynchronous on `stream`. */
+RM_API rm_status rm_debug_mix_residual(const void *X, int from_z, float *Y, int B, int T, int D, void *stream);
 
 /* Synchronise `stream`, then report and clear the context's device error
  * word: RM_OK, RM_ERR_TIMEOUT or RM_ERR_DEVICE (or RM_ERR_CUDA if the
@@ -423,6 +452,20 @@ RM_API rm_status rm_profile_read(rm_ctx *ctx, rm_kernel_stat *stats);
  * when the wait runs out the kernel latches RM_ERR_TIMEOUT in the context's
  * error word and returns.  The next rm_sync_status() reports it. */
 RM_API rm_status rm_debug_wait_timeout(rm_ctx *ctx, int timeout_us, void *stream);
+
+/* Test hooks for allocation failures (host side; no GPU fault is involved).
+ * Every device allocation the library makes (context creation and the
+ * workspaces its calls allocate on first use) goes through one allocator.
+ * rm_debug_fail_alloc(after): with after >= 0, the next `after` allocations
+ * succeed and the one after them fails as if the device were out of memory
+ * (once; the calling entry point returns RM_ERR_OOM with "injected failure" in
+ * rm_last_error()); after < 0 disarms.  RM_FAULT_INJECT=alloc:N in the
+ * environment arms the same countdown at the library's first allocation.
+ * rm_debug_alloc_stats: allocations made since the library was loaded, and
+ * the number and bytes of those still live (any output may be NULL).
+ * Process-wide, not per context; thread-safe. */
+RM_API rm_status rm_debug_fail_alloc(long long after);
+RM_API rm_status rm_debug_alloc_stats(long long *made, long long *live_count, long long *live_bytes);
 
 /* Test hook: out[i] = the GELU the library's GEMM epilogues apply, for n
  * float32 device values (u * Phi(u), "RankMixer 详解（1）" section 4.1, with

@@ -44,7 +44,8 @@ EXPORTED = ["rm_create", "rm_destroy", "rm_block_forward", "rm_stack_forward", "
             "rm_block_forward_noalloc", "rm_debug_gelu", "rm_block_backward", "rm_stack_backward",
             "rm_debug_gelu_grad", "rm_stack_forward_train", "rm_stack_backward_saved", "rm_head_forward",
             "rm_set_tokenizer", "rm_tokenize", "rm_score", "rm_moe_pffn_forward_train", "rm_tokenize_backward",
-            "rm_set_unimixing", "rm_unimixing_weights", "rm_unimixing"]
+            "rm_set_unimixing", "rm_unimixing_weights", "rm_unimixing", "rm_debug_mix_residual",
+            "rm_debug_fail_alloc", "rm_debug_alloc_stats"]
 
 
 class rm_config(ctypes.Structure):
@@ -99,8 +100,8 @@ def load() -> ctypes.CDLL:
     sig = {
         "rm_create": (st, [ctypes.POINTER(rm_config), ctypes.POINTER(rm_layer_params), i, ctypes.POINTER(vp)]),
         "rm_destroy": (st, [vp]),
-        "rm_block_forward": (st, [vp, i, vp, vp, vp, i, vp]),
-        "rm_stack_forward": (st, [vp, vp, vp, vp, i, vp]),
+        "rm_block_forward": (st, [vp, i, vp, vp, vp, i, i, vp]),
+        "rm_stack_forward": (st, [vp, vp, vp, vp, i, i, vp]),
         "rm_stack_forward_host": (st, [vp, vp, vp, i, vp]),
         "rm_moe_pffn_forward": (st, [vp, i, vp, vp, vp, i, vp]),
         "rm_token_mix": (st, [vp, vp, i, i, i, i, i, vp]),
@@ -126,7 +127,10 @@ def load() -> ctypes.CDLL:
         "rm_stack_backward_saved": (st, [vp, vp, vp, ctypes.POINTER(rm_layer_grads), i, vp]),
         "rm_set_unimixing": (st, [vp, i, vp, vp, i, ctypes.c_float, i, vp]),
         "rm_unimixing_weights": (st, [vp, i, vp, vp, vp]),
-        "rm_unimixing": (st, [vp, i, vp, vp, i, vp]),
+        "rm_unimixing": (st, [vp, i, vp, vp, i, i, vp]),
+        "rm_debug_mix_residual": (st, [vp, i, vp, i, i, i, vp]),
+        "rm_debug_fail_alloc": (st, [ctypes.c_longlong]),
+        "rm_debug_alloc_stats": (st, [ctypes.POINTER(ctypes.c_longlong)] * 3),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -155,16 +159,17 @@ def rm_destroy(ctx: int) -> None:
     check(load().rm_destroy(ctx), "rm_destroy")
 
 
-def rm_block_forward(ctx: int, layer: int, X_in: int, X_out: int, S_out: int | None, B: int, stream: int) -> None:
-    check(load().rm_block_forward(ctx, layer, X_in, X_out, S_out, B, stream), "rm_block_forward")
+def rm_block_forward(ctx: int, layer: int, X_in: int, X_out: int, S_out: int | None, out_dtype: int, B: int,
+                     stream: int) -> None:
+    check(load().rm_block_forward(ctx, layer, X_in, X_out, S_out, out_dtype, B, stream), "rm_block_forward")
 
 
 def rm_block_forward_noalloc(ctx: int, layer: int, X_in: int, X_out: int, B: int, stream: int) -> None:
     check(load().rm_block_forward_noalloc(ctx, layer, X_in, X_out, B, stream), "rm_block_forward_noalloc")
 
 
-def rm_stack_forward(ctx: int, X0: int, pooled: int, XL: int | None, B: int, stream: int) -> None:
-    check(load().rm_stack_forward(ctx, X0, pooled, XL, B, stream), "rm_stack_forward")
+def rm_stack_forward(ctx: int, X0: int, pooled: int, XL: int | None, xl_dtype: int, B: int, stream: int) -> None:
+    check(load().rm_stack_forward(ctx, X0, pooled, XL, xl_dtype, B, stream), "rm_stack_forward")
 
 
 def rm_stack_forward_host(ctx: int, X0_host: int, pooled_host: int, B: int, stream: int) -> None:
@@ -264,8 +269,23 @@ def rm_unimixing_weights(ctx: int, layer: int, WG_out: int | None, WB_out: int |
     check(load().rm_unimixing_weights(ctx, layer, WG_out, WB_out, stream), "rm_unimixing_weights")
 
 
-def rm_unimixing(ctx: int, layer: int, X: int, Y: int, B: int, stream: int) -> None:
-    check(load().rm_unimixing(ctx, layer, X, Y, B, stream), "rm_unimixing")
+def rm_unimixing(ctx: int, layer: int, X: int, Y: int, out_dtype: int, B: int, stream: int) -> None:
+    check(load().rm_unimixing(ctx, layer, X, Y, out_dtype, B, stream), "rm_unimixing")
+
+
+def rm_debug_mix_residual(X: int, from_z: bool, Y: int, B: int, T: int, D: int, stream: int) -> None:
+    check(load().rm_debug_mix_residual(X, 1 if from_z else 0, Y, B, T, D, stream), "rm_debug_mix_residual")
+
+
+def rm_debug_fail_alloc(after: int) -> None:
+    check(load().rm_debug_fail_alloc(after), "rm_debug_fail_alloc")
+
+
+def rm_debug_alloc_stats() -> tuple[int, int, int]:
+    """(allocations made since load, live allocations, live bytes)."""
+    v = [ctypes.c_longlong() for _ in range(3)]
+    check(load().rm_debug_alloc_stats(*[ctypes.byref(x) for x in v]), "rm_debug_alloc_stats")
+    return v[0].value, v[1].value, v[2].value
 
 
 def rm_debug_gelu_grad(u: int, out: int, n: int, stream: int) -> None:

@@ -22,6 +22,13 @@ def _stream() -> int:
     return torch.cuda.current_stream().cuda_stream
 
 
+def _out_dtype(name: str | None, ctx_tdtype: torch.dtype) -> tuple[torch.dtype, int]:
+    """Output tensor dtype and rm_dtype code: None -> the context dtype, "f32" -> float32."""
+    if name is None:
+        return ctx_tdtype, (_lib.RM_F32 if ctx_tdtype == torch.float32 else _lib.RM_BF16)
+    return _DTYPES[name]
+
+
 def _ptr(t: torch.Tensor | None) -> int | None:
     if t is None:
         return None
@@ -80,18 +87,24 @@ class RankMixer:
         return "tcgen05" if self.info.gemm_path == _lib.RM_PATH_TCGEN05 else "simt"
 
     # -- forward calls -----------------------------------------------------------
-    def block_forward(self, layer: int, X: torch.Tensor, out: torch.Tensor | None = None, return_S: bool = False):
+    def block_forward(self, layer: int, X: torch.Tensor, out: torch.Tensor | None = None, return_S: bool = False,
+                      out_dtype: str | None = None):
+        """X_out (and S with return_S) in the context dtype, or float32 with out_dtype="f32"."""
         B = X.shape[0]
-        out = torch.empty_like(X) if out is None else out
-        S = torch.empty_like(X) if return_S else None
-        _lib.rm_block_forward(self.ctx, layer, _ptr(X), _ptr(out), _ptr(S), B, _stream())
+        tdt, code = _out_dtype(out_dtype, self.tdtype)
+        out = torch.empty(X.shape, dtype=tdt, device=X.device) if out is None else out
+        S = torch.empty(X.shape, dtype=tdt, device=X.device) if return_S else None
+        _lib.rm_block_forward(self.ctx, layer, _ptr(X), _ptr(out), _ptr(S), code, B, _stream())
         return (out, S) if return_S else out
 
-    def stack_forward(self, X0: torch.Tensor, pooled: torch.Tensor | None = None, return_XL: bool = False):
+    def stack_forward(self, X0: torch.Tensor, pooled: torch.Tensor | None = None, return_XL: bool = False,
+                      xl_dtype: str | None = None):
+        """pooled (float32), and X_L with return_XL in the context dtype or float32 (xl_dtype="f32")."""
         B = X0.shape[0]
         pooled = torch.empty((B, self.D), dtype=torch.float32, device=X0.device) if pooled is None else pooled
-        XL = torch.empty_like(X0) if return_XL else None
-        _lib.rm_stack_forward(self.ctx, _ptr(X0), _ptr(pooled), _ptr(XL), B, _stream())
+        tdt, code = _out_dtype(xl_dtype, self.tdtype)
+        XL = torch.empty(X0.shape, dtype=tdt, device=X0.device) if return_XL else None
+        _lib.rm_stack_forward(self.ctx, _ptr(X0), _ptr(pooled), _ptr(XL), code, B, _stream())
         return (pooled, XL) if return_XL else pooled
 
     def stack_forward_host(self, X0_host: torch.Tensor, pooled_host: torch.Tensor | None = None) -> torch.Tensor:
@@ -224,10 +237,13 @@ class RankMixer:
         _lib.rm_unimixing_weights(self.ctx, layer, _ptr(WG), _ptr(WB), _stream())
         return WG, WB
 
-    def unimixing(self, layer: int, X: torch.Tensor, Y: torch.Tensor | None = None) -> torch.Tensor:
-        """Y = UniMixing(X) of layer ``layer``: X [B, T, D] in the context dtype."""
-        Y = torch.empty_like(X) if Y is None else Y
-        _lib.rm_unimixing(self.ctx, layer, _ptr(X), _ptr(Y), X.shape[0], _stream())
+    def unimixing(self, layer: int, X: torch.Tensor, Y: torch.Tensor | None = None,
+                  out_dtype: str | None = None) -> torch.Tensor:
+        """Y = UniMixing(X) of layer ``layer``: X [B, T, D] in the context dtype; Y in the
+        context dtype or float32 (out_dtype="f32")."""
+        tdt, code = _out_dtype(out_dtype, self.tdtype)
+        Y = torch.empty(X.shape, dtype=tdt, device=X.device) if Y is None else Y
+        _lib.rm_unimixing(self.ctx, layer, _ptr(X), _ptr(Y), code, X.shape[0], _stream())
         return Y
 
     def set_tokenizer(self, W: torch.Tensor, bias: torch.Tensor) -> None:
@@ -282,6 +298,19 @@ def token_mix(X: torch.Tensor, H: int | None = None) -> torch.Tensor:
     Y = torch.empty((B, H, T * (D // H)), dtype=X.dtype, device=X.device)
     dt = _lib.RM_BF16 if X.dtype == torch.bfloat16 else _lib.RM_F32
     _lib.rm_token_mix(_ptr(X), _ptr(Y), B, T, D, H, dt, _stream())
+    return Y
+
+
+def debug_mix_residual(X: torch.Tensor, from_z: bool = False) -> torch.Tensor:
+    """Test hook: y = Mix(X) + X from the fused mixing kernel's gather (float32,
+    token-major [T, B, D]).  from_z=False: X bf16 [B, T, D]; from_z=True: X fp16
+    token-major [T, B, D] and y the fp16 sum widened to float32."""
+    if from_z:
+        T, B, D = X.shape
+    else:
+        B, T, D = X.shape
+    Y = torch.empty((T, B, D), dtype=torch.float32, device=X.device)
+    _lib.rm_debug_mix_residual(_ptr(X), from_z, _ptr(Y), B, T, D, _stream())
     return Y
 
 

@@ -9,6 +9,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <unordered_map>
 #include <vector>
 
 #include "../../include/rankmixer.h"
@@ -18,6 +19,13 @@
 #include "rm_unimix.h"
 
 using namespace rm;
+
+namespace {
+struct AllocBook;
+AllocBook& book();
+void read_fault_env(AllocBook& b);
+bool alloc_failure_was_injected();
+}  // namespace
 
 namespace {
 
@@ -34,7 +42,9 @@ rm_status fail(rm_status st, const char* fmt, ...) {
 }
 
 rm_status cuda_fail(cudaError_t e, const char* what) {
-    if (e == cudaErrorMemoryAllocation) return fail(RM_ERR_OOM, "%s: %s", what, cudaGetErrorString(e));
+    if (e == cudaErrorMemoryAllocation)
+        return fail(RM_ERR_OOM, "%s: %s", what,
+                    alloc_failure_was_injected() ? "injected failure (device allocation)" : cudaGetErrorString(e));
     if (e == cudaErrorNotSupported) return fail(RM_ERR_UNSUPPORTED, "%s: shape not supported by this kernel", what);
     return fail(RM_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
@@ -53,6 +63,41 @@ constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
 // chunks (at most kHostChunksMax; the schedule is in rm_stack_forward_host).
 constexpr int kHostChunksMax = 4;
 constexpr int kHostChunkMin = 1024;
+
+// ---- device allocations: bookkeeping and injected failures ------------------------
+struct AllocBook {
+    std::mutex mu;
+    std::unordered_map<void*, size_t> live;
+    long long made = 0;        // successful allocations since load
+    long long live_bytes = 0;
+    long long fail_after = -1; // >= 0: that many more allocations succeed, then one fails
+    bool env_read = false;
+    bool last_injected = false;
+};
+AllocBook& book() {
+    static AllocBook b;
+    return b;
+}
+
+// RM_FAULT_INJECT=alloc:N arms the injection once, at the first allocation.
+void read_fault_env(AllocBook& b) {
+    if (b.env_read) return;
+    b.env_read = true;
+    const char* v = getenv("RM_FAULT_INJECT");
+    if (v && strncmp(v, "alloc:", 6) == 0) {
+        char* end = nullptr;
+        const long long n = strtoll(v + 6, &end, 10);
+        if (end != v + 6 && n >= 0) b.fail_after = n;
+    }
+}
+
+// Whether the last failed device allocation was an injected one (read once).
+bool alloc_failure_was_injected() {
+    std::lock_guard<std::mutex> lk(book().mu);
+    const bool r = book().last_injected;
+    book().last_injected = false;
+    return r;
+}
 
 struct LayerW {
     void* W1p = nullptr;   // [T][F][D]  (K-major for GEMM1)
@@ -184,15 +229,25 @@ namespace {
 rm_status dmalloc(rm_ctx* c, void** p, size_t bytes, long long* counter) {
     *p = nullptr;
     if (bytes == 0) return RM_OK;
-    cudaError_t e = cudaMalloc(p, bytes);
+    cudaError_t e = device_alloc(p, bytes);
     if (e != cudaSuccess) {
         *p = nullptr;
         cudaGetLastError();
-        return fail(RM_ERR_OOM, "cudaMalloc(%zu bytes) failed: %s", bytes, cudaGetErrorString(e));
+        return fail(RM_ERR_OOM, "device allocation of %zu bytes failed: %s", bytes,
+                    e == cudaErrorMemoryAllocation && alloc_failure_was_injected() ? "injected failure"
+                                                                                    : cudaGetErrorString(e));
     }
     if (counter) *counter += (long long)bytes;
     (void)c;
     return RM_OK;
+}
+
+// dmalloc for a lazily allocated buffer: keeps one that an earlier call
+// already allocated (a call that failed part way through a group of buffers
+// leaves the ones it got; the next call completes the group).
+rm_status ensure(rm_ctx* c, void** p, size_t bytes, long long* counter) {
+    if (*p) return RM_OK;
+    return dmalloc(c, p, bytes, counter);
 }
 
 void free_ctx(rm_ctx* c) {
@@ -200,35 +255,35 @@ void free_ctx(rm_ctx* c) {
     cudaSetDevice(c->device);
     cudaDeviceSynchronize();
     for (auto& l : c->layers) {
-        cudaFree(l.W1p); cudaFree(l.W2p); cudaFree(l.b1); cudaFree(l.b2);
-        cudaFree(l.g1); cudaFree(l.be1); cudaFree(l.g2); cudaFree(l.be2);
+        device_free(l.W1p); device_free(l.W2p); device_free(l.b1); device_free(l.b2);
+        device_free(l.g1); device_free(l.be1); device_free(l.g2); device_free(l.be2);
         moe_free_weights(l.moe);
-        cudaFree(l.W1t); cudaFree(l.W2t); cudaFree(l.Wg_train); cudaFree(l.bg_train);
-        if (l.umWGop != l.umWG32) cudaFree(l.umWGop);
-        cudaFree(l.umWG32); cudaFree(l.umWB); cudaFree(l.umWBt16);
+        device_free(l.W1t); device_free(l.W2t); device_free(l.Wg_train); device_free(l.bg_train);
+        if (l.umWGop != l.umWG32) device_free(l.umWGop);
+        device_free(l.umWG32); device_free(l.umWB); device_free(l.umWBt16);
     }
-    cudaFree(c->umH); cudaFree(c->umYt); cudaFree(c->umX);
+    device_free(c->umH); device_free(c->umYt); device_free(c->umX);
     {
         TrainWS& t = c->tw;
         for (auto& sl : t.slots) {
-            cudaFree(sl.S); cudaFree(sl.Yh); cudaFree(sl.rstd1); cudaFree(sl.A); cudaFree(sl.Gp); cudaFree(sl.Z);
+            device_free(sl.S); device_free(sl.Yh); device_free(sl.rstd1); device_free(sl.A); device_free(sl.Gp); device_free(sl.Z);
         }
-        cudaFree(t.dZ32); cudaFree(t.dZ); cudaFree(t.dS); cudaFree(t.pmax); cudaFree(t.inv_scale);
-        cudaFree(t.part2); cudaFree(t.tmpTD); cudaFree(t.colpart); cudaFree(t.part1);
-        cudaFree(t.Xn); cudaFree(t.G0); cudaFree(t.G1); cudaFree(t.pooled);
+        device_free(t.dZ32); device_free(t.dZ); device_free(t.dS); device_free(t.pmax); device_free(t.inv_scale);
+        device_free(t.part2); device_free(t.tmpTD); device_free(t.colpart); device_free(t.part1);
+        device_free(t.Xn); device_free(t.G0); device_free(t.G1); device_free(t.pooled);
     }
-    cudaFree(c->Wtok); cudaFree(c->btok); cudaFree(c->Etok); cudaFree(c->X0ws); cudaFree(c->pooled_ws);
-    cudaFree(c->ginfer); cudaFree(c->dX0h); cudaFree(c->tok_part); cudaFree(c->tok_inv);
+    device_free(c->Wtok); device_free(c->btok); device_free(c->Etok); device_free(c->X0ws); device_free(c->pooled_ws);
+    device_free(c->ginfer); device_free(c->dX0h); device_free(c->tok_part); device_free(c->tok_inv);
     moe_free_workspace(c->moe_ws);
-    cudaFree(c->S); cudaFree(c->Hid); cudaFree(c->Z); cudaFree(c->stats); cudaFree(c->rows); cudaFree(c->V);
-    cudaFree(c->X0_dev); cudaFree(c->pooled_dev);
+    device_free(c->S); device_free(c->Hid); device_free(c->Z); device_free(c->stats); device_free(c->rows); device_free(c->V);
+    device_free(c->X0_dev); device_free(c->pooled_dev);
     for (int i = 0; i < kHostChunksMax; ++i) {
         if (c->ev_in[i]) cudaEventDestroy(c->ev_in[i]);
         if (c->ev_done[i]) cudaEventDestroy(c->ev_done[i]);
     }
     if (c->s_in) cudaStreamDestroy(c->s_in);
     if (c->s_out) cudaStreamDestroy(c->s_out);
-    cudaFree(c->d_err); cudaFree(c->d_flag);
+    device_free(c->d_err); device_free(c->d_flag);
     for (auto& e : c->ev_pool) { cudaEventDestroy(e.a); cudaEventDestroy(e.b); }
     delete c;
 }
@@ -290,6 +345,16 @@ rm_status check_ctx(const rm_ctx* c) {
 
 rm_status check_batch(const rm_ctx* c, int B) {
     if (B < 1 || B > c->Bcap) return fail(RM_ERR_INVALID_ARG, "B (%d) must be in [1, max_batch=%d]", B, c->Bcap);
+    return RM_OK;
+}
+
+// Activation outputs come in the context dtype or in float32 (the values
+// before their rounding to bf16 in a bf16 context).
+rm_status check_out_dtype(const rm_ctx* c, rm_dtype d, bool* out_f32) {
+    if (d != RM_F32 && d != RM_BF16) return fail(RM_ERR_INVALID_ARG, "unknown output dtype %d", (int)d);
+    if (d == RM_BF16 && c->act == Act::F32)
+        return fail(RM_ERR_INVALID_ARG, "a float32 context writes float32 outputs (out_dtype RM_F32)");
+    *out_f32 = d == RM_F32;
     return RM_OK;
 }
 
@@ -374,7 +439,7 @@ XType caller_xtype(const rm_ctx* c);
 XType op_xtype(const rm_ctx* c);
 rm_status unimix_mix_ln1(rm_ctx* c, int layer, const void* X, XType xt, int B, cudaStream_t s);
 
-rm_status stack_device(rm_ctx* c, const void* X0, float* pooled, void* XL, int B, cudaStream_t s) {
+rm_status stack_device(rm_ctx* c, const void* X0, float* pooled, void* XL, bool xl_f32, int B, cudaStream_t s) {
     const rm_config& g = c->cfg;
     for (int n = 0; n < g.L; ++n) {
         MixLnArgs a = mix_args(c, n, B);
@@ -410,9 +475,9 @@ rm_status stack_device(rm_ctx* c, const void* X0, float* pooled, void* XL, int B
     }
     const int last = g.L - 1;
     ProfScope ps(c, RM_K_POOL, s);
-    RM_CHECK_CUDA(launch_pool(c->act, c->Z, c->rows, c->layers[last].g2, c->layers[last].be2, pooled, XL, B, g.T,
-                              g.D, c->Bcap, layer_nchunk(c, last), layer_cw(c, last), g.ln_eps, c->num_sms, c->d_err,
-                              kWaitTimeoutNs, s),
+    RM_CHECK_CUDA(launch_pool(c->act, c->Z, c->rows, c->layers[last].g2, c->layers[last].be2, pooled, XL, xl_f32, B,
+                              g.T, g.D, c->Bcap, layer_nchunk(c, last), layer_cw(c, last), g.ln_eps, c->num_sms,
+                              c->d_err, kWaitTimeoutNs, s),
                   "ln2+pool");
     return RM_OK;
 }
@@ -480,34 +545,38 @@ rm_status train_ws_ready(rm_ctx* c, int nslots, bool stack) {
         t.nblk2 = ln2_bwd_blocks(c->act, c->Bcap, g.T, g.D, c->num_sms);
         t.colrows = (c->Bcap + 255) / 256 * (256 / kTrainColpartRows);   // covers 128- and 256-row tiles
         t.grid1 = ln1_bwd_grid(c->Bcap, g.T, g.D, c->num_sms);
-        if ((st = dmalloc(c, (void**)&t.dZ32, T * Bc * D * 4, &c->ws_bytes)) != RM_OK ||
-            (c->act != Act::F32 && (st = dmalloc(c, &t.dZ, T * Bc * D * osz, &c->ws_bytes)) != RM_OK) ||
-            (st = dmalloc(c, (void**)&t.dS, T * Bc * D * 4, &c->ws_bytes)) != RM_OK ||
-            (st = dmalloc(c, (void**)&t.pmax, T * (size_t)t.nblk2 * 4, &c->ws_bytes)) != RM_OK ||
-            (st = dmalloc(c, (void**)&t.inv_scale, T * 4, &c->ws_bytes)) != RM_OK ||
-            (st = dmalloc(c, (void**)&t.part2, 3 * T * (size_t)t.nblk2 * D * 4, &c->ws_bytes)) != RM_OK ||
-            (st = dmalloc(c, (void**)&t.tmpTD, T * D * 4, &c->ws_bytes)) != RM_OK ||
-            (st = dmalloc(c, (void**)&t.colpart, T * (size_t)t.colrows * F * 4, &c->ws_bytes)) != RM_OK ||
-            (st = dmalloc(c, (void**)&t.part1, 2 * (size_t)t.grid1 * D * 4, &c->ws_bytes)) != RM_OK)
+        if ((st = ensure(c, (void**)&t.dZ32, T * Bc * D * 4, &c->ws_bytes)) != RM_OK ||
+            (c->act != Act::F32 && (st = ensure(c, &t.dZ, T * Bc * D * osz, &c->ws_bytes)) != RM_OK) ||
+            (st = ensure(c, (void**)&t.dS, T * Bc * D * 4, &c->ws_bytes)) != RM_OK ||
+            (st = ensure(c, (void**)&t.pmax, T * (size_t)t.nblk2 * 4, &c->ws_bytes)) != RM_OK ||
+            (st = ensure(c, (void**)&t.inv_scale, T * 4, &c->ws_bytes)) != RM_OK ||
+            (st = ensure(c, (void**)&t.part2, 3 * T * (size_t)t.nblk2 * D * 4, &c->ws_bytes)) != RM_OK ||
+            (st = ensure(c, (void**)&t.tmpTD, T * D * 4, &c->ws_bytes)) != RM_OK ||
+            (st = ensure(c, (void**)&t.colpart, T * (size_t)t.colrows * F * 4, &c->ws_bytes)) != RM_OK ||
+            (st = ensure(c, (void**)&t.part1, 2 * (size_t)t.grid1 * D * 4, &c->ws_bytes)) != RM_OK)
             return st;
         t.ready = true;
     }
     while ((int)t.slots.size() < nslots) {
-        t.slots.emplace_back();
-        TrainSlot& sl = t.slots.back();
+        TrainSlot sl;
         if ((st = dmalloc(c, &sl.S, T * Bc * D * osz, &c->ws_bytes)) != RM_OK ||
             (st = dmalloc(c, &sl.Yh, T * Bc * D * osz, &c->ws_bytes)) != RM_OK ||
             (st = dmalloc(c, (void**)&sl.rstd1, T * Bc * 4, &c->ws_bytes)) != RM_OK ||
             (st = dmalloc(c, &sl.A, T * Bc * F * osz, &c->ws_bytes)) != RM_OK ||
             (st = dmalloc(c, &sl.Gp, T * Bc * F * osz, &c->ws_bytes)) != RM_OK ||
-            (st = dmalloc(c, &sl.Z, T * Bc * D * osz, &c->ws_bytes)) != RM_OK)
+            (st = dmalloc(c, &sl.Z, T * Bc * D * osz, &c->ws_bytes)) != RM_OK) {
+            // a slot is used whole or not at all
+            device_free(sl.S); device_free(sl.Yh); device_free(sl.rstd1); device_free(sl.A); device_free(sl.Gp);
+            device_free(sl.Z);
             return st;
+        }
+        t.slots.push_back(sl);
     }
-    if (stack && !t.Xn) {
-        if ((st = dmalloc(c, (void**)&t.Xn, Bc * T * D * 4, &c->ws_bytes)) != RM_OK ||
-            (st = dmalloc(c, (void**)&t.G0, Bc * T * D * 4, &c->ws_bytes)) != RM_OK ||
-            (st = dmalloc(c, (void**)&t.G1, Bc * T * D * 4, &c->ws_bytes)) != RM_OK ||
-            (st = dmalloc(c, (void**)&t.pooled, Bc * D * 4, &c->ws_bytes)) != RM_OK)
+    if (stack) {
+        if ((st = ensure(c, (void**)&t.Xn, Bc * T * D * 4, &c->ws_bytes)) != RM_OK ||
+            (st = ensure(c, (void**)&t.G0, Bc * T * D * 4, &c->ws_bytes)) != RM_OK ||
+            (st = ensure(c, (void**)&t.G1, Bc * T * D * 4, &c->ws_bytes)) != RM_OK ||
+            (st = ensure(c, (void**)&t.pooled, Bc * D * 4, &c->ws_bytes)) != RM_OK)
             return st;
     }
     return RM_OK;
@@ -674,18 +743,14 @@ rm_status stack_forward_train_impl(rm_ctx* c, const void* X0, float* pooled, int
         }
         if (n + 1 < g.L) {
             ProfScope ps(c, RM_K_LN2_OUT, s);
-            if (c->act == Act::F32)
-                RM_CHECK_CUDA(launch_ln2_out(c->act, sl.Z, c->rows, c->layers[n].g2, c->layers[n].be2, t.Xn, B, g.T,
-                                             g.D, c->Bcap, 1, g.D, g.ln_eps, c->num_sms, s),
-                              "ln2 out");
-            else
-                RM_CHECK_CUDA(launch_ln2_out_f32(sl.Z, c->rows, c->layers[n].g2, c->layers[n].be2, t.Xn, B, g.T, g.D,
-                                                 c->Bcap, g.ln_eps, c->num_sms, s),
-                              "ln2 out");
+            RM_CHECK_CUDA(launch_ln2_out(c->act, sl.Z, c->rows, c->layers[n].g2, c->layers[n].be2, t.Xn,
+                                         /*out_f32*/ true, B, g.T, g.D, c->Bcap, 1, g.D, g.ln_eps, c->num_sms, s),
+                          "ln2 out");
         } else {
             ProfScope ps(c, RM_K_POOL, s);
-            RM_CHECK_CUDA(launch_pool(c->act, sl.Z, c->rows, c->layers[n].g2, c->layers[n].be2, pooled, nullptr, B,
-                                      g.T, g.D, c->Bcap, 1, g.D, g.ln_eps, c->num_sms, c->d_err, kWaitTimeoutNs, s),
+            RM_CHECK_CUDA(launch_pool(c->act, sl.Z, c->rows, c->layers[n].g2, c->layers[n].be2, pooled, nullptr,
+                                      false, B, g.T, g.D, c->Bcap, 1, g.D, g.ln_eps, c->num_sms, c->d_err,
+                                      kWaitTimeoutNs, s),
                           "ln2 + pool");
         }
     }
@@ -769,6 +834,44 @@ rm_status unimix_mix_ln1(rm_ctx* c, int layer, const void* X, XType xt, int B, c
 }
 
 }  // namespace
+
+cudaError_t rm::device_alloc(void** p, size_t bytes) {
+    *p = nullptr;
+    AllocBook& b = book();
+    {
+        std::lock_guard<std::mutex> lk(b.mu);
+        read_fault_env(b);
+        b.last_injected = false;
+        if (b.fail_after == 0) {
+            b.fail_after = -1;          // one failure per arming
+            b.last_injected = true;
+            return cudaErrorMemoryAllocation;
+        }
+        if (b.fail_after > 0) --b.fail_after;
+    }
+    cudaError_t e = cudaMalloc(p, bytes);
+    if (e != cudaSuccess) {
+        *p = nullptr;
+        return e;
+    }
+    std::lock_guard<std::mutex> lk(b.mu);
+    b.live[*p] = bytes;
+    b.made += 1;
+    b.live_bytes += (long long)bytes;
+    return cudaSuccess;
+}
+
+void rm::device_free(void* p) {
+    if (!p) return;
+    cudaFree(p);
+    AllocBook& b = book();
+    std::lock_guard<std::mutex> lk(b.mu);
+    auto it = b.live.find(p);
+    if (it != b.live.end()) {
+        b.live_bytes -= (long long)it->second;
+        b.live.erase(it);
+    }
+}
 
 // =============================================================================
 // Public entry points
@@ -862,18 +965,22 @@ rm_status rm_destroy(rm_ctx* ctx) {
     return RM_OK;
 }
 
-rm_status rm_block_forward(rm_ctx* c, int layer, const void* X_in, void* X_out, void* S_out, int B, void* stream) {
+rm_status rm_block_forward(rm_ctx* c, int layer, const void* X_in, void* X_out, void* S_out, rm_dtype out_dtype, int B,
+                           void* stream) {
     rm_status st;
     if ((st = check_ctx(c)) != RM_OK) return st;
     if (layer < 0 || layer >= c->cfg.L) return fail(RM_ERR_INVALID_ARG, "layer %d out of range", layer);
     if ((st = check_batch(c, B)) != RM_OK) return st;
+    bool out_f32 = false;
+    if ((st = check_out_dtype(c, out_dtype, &out_f32)) != RM_OK) return st;
     if (!X_in || !X_out) return fail(RM_ERR_INVALID_ARG, "X_in / X_out is NULL");
     if (!aligned16(X_in) || !aligned16(X_out) || (S_out && !aligned16(S_out)))
         return fail(RM_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
-    const size_t bytes = (size_t)B * c->cfg.T * c->cfg.D * c->esz;
+    const size_t in_bytes = (size_t)B * c->cfg.T * c->cfg.D * c->esz;
+    const size_t out_bytes = (size_t)B * c->cfg.T * c->cfg.D * (out_f32 ? 4 : c->esz);
     const char* xi = (const char*)X_in;
     const char* xo = (const char*)X_out;
-    if (xi < xo + bytes && xo < xi + bytes) return fail(RM_ERR_INVALID_ARG, "X_in and X_out overlap");
+    if (xi < xo + out_bytes && xo < xi + in_bytes) return fail(RM_ERR_INVALID_ARG, "X_in and X_out overlap");
     cudaSetDevice(c->device);
     cudaStream_t s = as_stream(stream);
     const rm_config& g = c->cfg;
@@ -887,25 +994,28 @@ rm_status rm_block_forward(rm_ctx* c, int layer, const void* X_in, void* X_out, 
     }
     if (S_out) {
         ProfScope ps(c, RM_K_MISC, s);
-        RM_CHECK_CUDA(launch_token_to_sample(c->act, c->S, S_out, B, g.T, g.D, c->Bcap, s), "copy S");
+        RM_CHECK_CUDA(launch_token_to_sample(c->act, c->S, S_out, out_f32, B, g.T, g.D, c->Bcap, s), "copy S");
     }
     if ((st = run_pffn(c, layer, B, s)) != RM_OK) return st;
     ProfScope ps(c, RM_K_LN2_OUT, s);
-    RM_CHECK_CUDA(launch_ln2_out(c->act, c->Z, c->rows, c->layers[layer].g2, c->layers[layer].be2, X_out, B, g.T,
-                                 g.D, c->Bcap, layer_nchunk(c, layer), layer_cw(c, layer), g.ln_eps, c->num_sms, s),
+    RM_CHECK_CUDA(launch_ln2_out(c->act, c->Z, c->rows, c->layers[layer].g2, c->layers[layer].be2, X_out, out_f32, B,
+                                 g.T, g.D, c->Bcap, layer_nchunk(c, layer), layer_cw(c, layer), g.ln_eps, c->num_sms,
+                                 s),
                   "ln2 out");
     return RM_OK;
 }
 
-rm_status rm_stack_forward(rm_ctx* c, const void* X0, float* pooled, void* XL, int B, void* stream) {
+rm_status rm_stack_forward(rm_ctx* c, const void* X0, float* pooled, void* XL, rm_dtype xl_dtype, int B, void* stream) {
     rm_status st;
     if ((st = check_ctx(c)) != RM_OK) return st;
     if ((st = check_batch(c, B)) != RM_OK) return st;
+    bool xl_f32 = false;
+    if ((st = check_out_dtype(c, xl_dtype, &xl_f32)) != RM_OK) return st;
     if (!X0 || !pooled) return fail(RM_ERR_INVALID_ARG, "X0 / pooled is NULL");
     if (!aligned16(X0) || !aligned16(pooled) || (XL && !aligned16(XL)))
         return fail(RM_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
     cudaSetDevice(c->device);
-    return stack_device(c, X0, pooled, XL, B, as_stream(stream));
+    return stack_device(c, X0, pooled, XL, xl_f32, B, as_stream(stream));
 }
 
 rm_status rm_stack_forward_host(rm_ctx* c, const void* X0_host, float* pooled_host, int B, void* stream) {
@@ -915,10 +1025,8 @@ rm_status rm_stack_forward_host(rm_ctx* c, const void* X0_host, float* pooled_ho
     if (!X0_host || !pooled_host) return fail(RM_ERR_INVALID_ARG, "X0_host / pooled_host is NULL");
     cudaSetDevice(c->device);
     const rm_config& g = c->cfg;
-    if (!c->X0_dev) {
-        if ((st = dmalloc(c, &c->X0_dev, (size_t)c->Bcap * g.T * g.D * c->esz, &c->ws_bytes)) != RM_OK) return st;
-        if ((st = dmalloc(c, (void**)&c->pooled_dev, (size_t)c->Bcap * g.D * 4, &c->ws_bytes)) != RM_OK) return st;
-    }
+    if ((st = ensure(c, &c->X0_dev, (size_t)c->Bcap * g.T * g.D * c->esz, &c->ws_bytes)) != RM_OK) return st;
+    if ((st = ensure(c, (void**)&c->pooled_dev, (size_t)c->Bcap * g.D * 4, &c->ws_bytes)) != RM_OK) return st;
     cudaStream_t s = as_stream(stream);
     const size_t row_in = (size_t)g.T * g.D * c->esz, row_out = (size_t)g.D * 4;
     char* x_dev = static_cast<char*>(c->X0_dev);
@@ -949,7 +1057,7 @@ rm_status rm_stack_forward_host(rm_ctx* c, const void* X0_host, float* pooled_ho
             ProfScope ps(c, RM_K_MISC, s);
             RM_CHECK_CUDA(cudaMemcpyAsync(c->X0_dev, X0_host, (size_t)B * row_in, cudaMemcpyHostToDevice, s), "H2D X0");
         }
-        if ((st = stack_device(c, c->X0_dev, c->pooled_dev, nullptr, B, s)) != RM_OK) return st;
+        if ((st = stack_device(c, c->X0_dev, c->pooled_dev, nullptr, false, B, s)) != RM_OK) return st;
         {
             ProfScope ps(c, RM_K_MISC, s);
             RM_CHECK_CUDA(cudaMemcpyAsync(pooled_host, c->pooled_dev, (size_t)B * row_out, cudaMemcpyDeviceToHost, s),
@@ -979,7 +1087,7 @@ rm_status rm_stack_forward_host(rm_ctx* c, const void* X0_host, float* pooled_ho
     for (int i = 0; i < nchunks; ++i) {
         const int b0 = bounds[i], bn = bounds[i + 1] - bounds[i];
         RM_CHECK_CUDA(cudaStreamWaitEvent(s, c->ev_in[i], 0), "wait");
-        if ((st = stack_device(c, x_dev + (size_t)b0 * row_in, c->pooled_dev + (size_t)b0 * g.D, nullptr, bn, s)) !=
+        if ((st = stack_device(c, x_dev + (size_t)b0 * row_in, c->pooled_dev + (size_t)b0 * g.D, nullptr, false, bn, s)) !=
             RM_OK)
             return st;
         RM_CHECK_CUDA(cudaEventRecord(c->ev_done[i], s), "event");
@@ -1105,7 +1213,7 @@ rm_status rm_set_tokenizer(rm_ctx* c, const void* W, const void* bias, int d) {
     if (d < 1) return fail(RM_ERR_INVALID_ARG, "d must be positive");
     const rm_config& g = c->cfg;
     cudaSetDevice(c->device);
-    cudaFree(c->Wtok); cudaFree(c->btok); cudaFree(c->Etok);
+    device_free(c->Wtok); device_free(c->btok); device_free(c->Etok);
     c->Wtok = nullptr; c->btok = nullptr; c->Etok = nullptr; c->tok_d = 0;
     const long long n = (long long)g.T * d * g.D;
     if ((st = dmalloc(c, &c->Wtok, (size_t)n * c->esz, &c->weight_bytes)) != RM_OK) return st;
@@ -1139,8 +1247,8 @@ rm_status rm_set_unimixing(rm_ctx* c, int layer, const float* WG, const float* W
     cudaStream_t s = as_stream(stream);
     RM_CHECK_CUDA(cudaStreamSynchronize(s), "rm_set_unimixing (drain the stream)");
     LayerW& w = c->layers[layer];
-    if (w.umWGop != w.umWG32) cudaFree(w.umWGop);
-    cudaFree(w.umWG32); cudaFree(w.umWB); cudaFree(w.umWBt16);
+    if (w.umWGop != w.umWG32) device_free(w.umWGop);
+    device_free(w.umWG32); device_free(w.umWB); device_free(w.umWBt16);
     w.umWG32 = nullptr; w.umWGop = nullptr; w.umWB = nullptr; w.umWBt16 = nullptr; w.um_bs = 0;
     const size_t nG = (size_t)nb * nb, nB = (size_t)nb * bs * bs;
     if ((st = dmalloc(c, (void**)&w.umWG32, nG * 4, &c->weight_bytes)) != RM_OK) return st;
@@ -1155,7 +1263,7 @@ rm_status rm_set_unimixing(rm_ctx* c, int layer, const float* WG, const float* W
     // workspace for the largest pitch so far
     const size_t hy = (size_t)nb * (size_t)um_pitch(c, bs) * op_size(c->act);
     if (hy > c->um_bytes) {
-        cudaFree(c->umH); cudaFree(c->umYt);
+        device_free(c->umH); device_free(c->umYt);
         c->umH = nullptr; c->umYt = nullptr; c->um_bytes = 0;
         if ((st = dmalloc(c, &c->umH, hy, &c->ws_bytes)) != RM_OK) return st;
         if ((st = dmalloc(c, &c->umYt, hy, &c->ws_bytes)) != RM_OK) return st;
@@ -1169,14 +1277,14 @@ rm_status rm_set_unimixing(rm_ctx* c, int layer, const float* WG, const float* W
     const size_t vmax = (size_t)nb * (size_t)(bs > 1 ? bs : 1) > (size_t)nb ? (size_t)nb * bs : (size_t)nb;
     if ((st = dmalloc(c, (void**)&C, nmax * 4, nullptr)) != RM_OK) return st;
     if ((st = dmalloc(c, (void**)&f, vmax * 4, nullptr)) != RM_OK || (st = dmalloc(c, (void**)&gv, vmax * 4, nullptr)) != RM_OK) {
-        cudaFree(C); cudaFree(f);
+        device_free(C); device_free(f);
         return st;
     }
     cudaError_t e = launch_sinkhorn(WG, 1, nb, tau, iters, C, f, gv, w.umWG32, c->act == Act::F32 ? nullptr : w.umWGop, s);
     if (e == cudaSuccess) e = launch_sinkhorn(WB, nb, bs, tau, iters, C, f, gv, w.umWB, nullptr, s);
     if (e == cudaSuccess && w.umWBt16) e = launch_unimix_pack_wb(w.umWB, w.umWBt16, nb, bs, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    cudaFree(C); cudaFree(f); cudaFree(gv);
+    device_free(C); device_free(f); device_free(gv);
     if (e != cudaSuccess) return cuda_fail(e, "rm_set_unimixing (Sinkhorn-Knopp)");
     w.um_bs = bs;
     return RM_OK;
@@ -1200,9 +1308,11 @@ rm_status rm_unimixing_weights(rm_ctx* c, int layer, float* WG_out, float* WB_ou
     return RM_OK;
 }
 
-rm_status rm_unimixing(rm_ctx* c, int layer, const void* X, void* Y, int B, void* stream) {
+rm_status rm_unimixing(rm_ctx* c, int layer, const void* X, void* Y, rm_dtype out_dtype, int B, void* stream) {
     rm_status st;
     if ((st = check_ctx(c)) != RM_OK) return st;
+    bool out_f32 = false;
+    if ((st = check_out_dtype(c, out_dtype, &out_f32)) != RM_OK) return st;
     const rm_config& g = c->cfg;
     if (layer < 0 || layer >= g.L) return fail(RM_ERR_INVALID_ARG, "layer %d out of range", layer);
     if (!c->layers[layer].um_bs) return fail(RM_ERR_INVALID_ARG, "layer %d uses TokenMixing (no rm_set_unimixing)", layer);
@@ -1213,7 +1323,7 @@ rm_status rm_unimixing(rm_ctx* c, int layer, const void* X, void* Y, int B, void
     cudaStream_t s = as_stream(stream);
     ProfScope ps(c, RM_K_UNIMIX, s);
     if ((st = unimix_global(c, layer, X, caller_xtype(c), B, s)) != RM_OK) return st;
-    RM_CHECK_CUDA(launch_unimix_out(c->act, c->umYt, Y, (long long)B * g.T * g.D, s), "unimixing output");
+    RM_CHECK_CUDA(launch_unimix_out(c->act, c->umYt, Y, out_f32, (long long)B * g.T * g.D, s), "unimixing output");
     return RM_OK;
 }
 
@@ -1267,11 +1377,9 @@ rm_status rm_tokenize_backward(rm_ctx* c, const void* E, const float* dX0, float
     const void* Gop = dX0;
     const float* inv = nullptr;
     if (c->act != Act::F32) {
-        if (!c->dX0h) {
-            if ((st = dmalloc(c, &c->dX0h, (size_t)c->Bcap * T * D * 2, &c->ws_bytes)) != RM_OK) return st;
-            if ((st = dmalloc(c, (void**)&c->tok_part, (size_t)T * kTokParts * 4, &c->ws_bytes)) != RM_OK) return st;
-            if ((st = dmalloc(c, (void**)&c->tok_inv, (size_t)T * 4, &c->ws_bytes)) != RM_OK) return st;
-        }
+        if ((st = ensure(c, &c->dX0h, (size_t)c->Bcap * T * D * 2, &c->ws_bytes)) != RM_OK) return st;
+        if ((st = ensure(c, (void**)&c->tok_part, (size_t)T * kTokParts * 4, &c->ws_bytes)) != RM_OK) return st;
+        if ((st = ensure(c, (void**)&c->tok_inv, (size_t)T * 4, &c->ws_bytes)) != RM_OK) return st;
         RM_CHECK_CUDA(launch_bf16_to_f16(E, c->Etok, (long long)B * T * d, s), "embeddings to fp16");
         RM_CHECK_CUDA(launch_token_grad_scale(dX0, c->tok_part, kTokParts, c->tok_inv, c->dX0h, B, T, D, s),
                       "token gradient scale");
@@ -1308,13 +1416,11 @@ rm_status rm_score(rm_ctx* c, const void* E, const float* head_w, float head_b, 
     if (c->cfg.moe_layer_mask != 0) return fail(RM_ERR_UNSUPPORTED, "rm_score runs dense stacks");
     cudaSetDevice(c->device);
     const rm_config& g = c->cfg;
-    if (!c->X0ws) {
-        if ((st = dmalloc(c, &c->X0ws, (size_t)c->Bcap * g.T * g.D * c->esz, &c->ws_bytes)) != RM_OK) return st;
-        if ((st = dmalloc(c, (void**)&c->pooled_ws, (size_t)c->Bcap * g.D * 4, &c->ws_bytes)) != RM_OK) return st;
-    }
+    if ((st = ensure(c, &c->X0ws, (size_t)c->Bcap * g.T * g.D * c->esz, &c->ws_bytes)) != RM_OK) return st;
+    if ((st = ensure(c, (void**)&c->pooled_ws, (size_t)c->Bcap * g.D * 4, &c->ws_bytes)) != RM_OK) return st;
     cudaStream_t s = as_stream(stream);
     if ((st = tokenize_impl(c, E, c->X0ws, B, s)) != RM_OK) return st;
-    if ((st = stack_device(c, c->X0ws, c->pooled_ws, nullptr, B, s)) != RM_OK) return st;
+    if ((st = stack_device(c, c->X0ws, c->pooled_ws, nullptr, false, B, s)) != RM_OK) return st;
     ProfScope ps(c, RM_K_HEAD, s);
     RM_CHECK_CUDA(launch_head(c->pooled_ws, head_w, head_b, nullptr, p, nullptr, nullptr, 1.0f, B, g.D, s), "head");
     return RM_OK;
@@ -1379,6 +1485,39 @@ rm_status rm_token_mix(const void* X, void* Y, int B, int T, int D, int H, rm_dt
     const char* y = (const char*)Y;
     if (x < y + bytes && y < x + bytes) return fail(RM_ERR_INVALID_ARG, "X and Y overlap");
     RM_CHECK_CUDA(launch_token_mix(X, Y, B, T, D, H, esz, as_stream(stream)), "token mix");
+    return RM_OK;
+}
+
+rm_status rm_debug_mix_residual(const void* X, int from_z, float* Y, int B, int T, int D, void* stream) {
+    if (!X || !Y) return fail(RM_ERR_INVALID_ARG, "X / Y is NULL");
+    if (B < 1 || T < 1 || D < 1) return fail(RM_ERR_INVALID_ARG, "sizes must be positive");
+    if (D % T != 0) return fail(RM_ERR_INVALID_ARG, "D (%d) must be divisible by T (%d)", D, T);
+    if (!aligned16(X) || !aligned16(Y)) return fail(RM_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+    const size_t in_bytes = (size_t)B * T * D * 2, out_bytes = (size_t)B * T * D * 4;
+    const char* x = (const char*)X;
+    const char* y = (const char*)Y;
+    if (x < y + out_bytes && y < x + in_bytes) return fail(RM_ERR_INVALID_ARG, "X and Y overlap");
+    int dev = 0, nsm = 0;
+    RM_CHECK_CUDA(cudaGetDevice(&dev), "cudaGetDevice");
+    RM_CHECK_CUDA(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev), "SM count");
+    MixLnArgs a{};
+    if (from_z)
+        a.Z = X;
+    else
+        a.X = X;
+    a.B = B;
+    a.T = T;
+    a.D = D;
+    a.q = D / T;
+    a.Bcap = B;
+    a.nchunk = 1;
+    a.cw = D;
+    a.Ydbg = Y;
+    a.timeout_ns = kWaitTimeoutNs;
+    cudaError_t e = launch_mix_residual_debug(from_z != 0, a, nsm, as_stream(stream));
+    if (e == cudaErrorNotSupported)
+        return fail(RM_ERR_UNSUPPORTED, "the staged 8-wide mixing kernel needs D/T %% 8 == 0 and D %% 256 == 0");
+    RM_CHECK_CUDA(e, "debug mix residual");
     return RM_OK;
 }
 
@@ -1448,6 +1587,23 @@ rm_status rm_debug_gelu(const float* u, float* out, long long n, int form, void*
     return RM_OK;
 }
 
+rm_status rm_debug_fail_alloc(long long after) {
+    AllocBook& b = book();
+    std::lock_guard<std::mutex> lk(b.mu);
+    b.env_read = true;           // an explicit setting overrides RM_FAULT_INJECT
+    b.fail_after = after >= 0 ? after : -1;
+    return RM_OK;
+}
+
+rm_status rm_debug_alloc_stats(long long* made, long long* live_count, long long* live_bytes) {
+    AllocBook& b = book();
+    std::lock_guard<std::mutex> lk(b.mu);
+    if (made) *made = b.made;
+    if (live_count) *live_count = (long long)b.live.size();
+    if (live_bytes) *live_bytes = b.live_bytes;
+    return RM_OK;
+}
+
 rm_status rm_debug_wait_timeout(rm_ctx* c, int timeout_us, void* stream) {
     rm_status st;
     if ((st = check_ctx(c)) != RM_OK) return st;
@@ -1487,13 +1643,21 @@ std::mutex g_noalloc_mu;
 void* g_noalloc_base[kNoAllocMaxDevices] = {};
 
 // Device address of g_noalloc_scratch on `device` (which must be current).
-// Looked up once per device; the host-side name of the array is not a
-// device address and must never be handed to a kernel.
-rm_status noalloc_scratch(int device, void** out) {
+// The host-side name of the array is not a device address and must never be
+// handed to a kernel.  The address is looked up again on every call made
+// outside stream capture (the lookup allocates nothing), so a module reloaded
+// after a device reset is picked up; under capture the address of the last
+// uncaptured call on this device is used.
+rm_status noalloc_scratch(int device, cudaStream_t s, void** out) {
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
     if (device < 0 || device >= kNoAllocMaxDevices)
         return fail(RM_ERR_UNSUPPORTED, "allocation-free entry point supports devices 0..%d", kNoAllocMaxDevices - 1);
-    if (!g_noalloc_base[device]) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    RM_CHECK_CUDA(cudaStreamIsCapturing(s, &cap), "cudaStreamIsCapturing");
+    if (cap == cudaStreamCaptureStatusNone || !g_noalloc_base[device]) {
+        if (cap != cudaStreamCaptureStatusNone)
+            return fail(RM_ERR_INVALID_ARG,
+                        "the first allocation-free call on a device must come before any stream capture");
         void* p = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || p == nullptr) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
@@ -1504,6 +1668,35 @@ rm_status noalloc_scratch(int device, void** out) {
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Layout of the static scratch for B samples (token-major, rows between tokens
+// = B): S, Hid and Z in the operand type, the GEMM2 chunk statistics (tensor-
+// core path only) and the merged row statistics, each 256-byte aligned.
+struct NoAllocLayout {
+    size_t S, H, Z, T, R;
+    size_t total() const { return S + H + Z + T + R; }
+};
+
+NoAllocLayout noalloc_layout(const rm_ctx* c, size_t B) {
+    const size_t T = c->cfg.T, D = c->cfg.D, F = c->F, osz = op_size(c->act);
+    NoAllocLayout l;
+    l.S = align256(T * B * D * osz);
+    l.H = align256(T * B * F * osz);
+    l.Z = align256(T * B * D * osz);
+    l.T = c->use_tc ? align256(T * B * (size_t)c->nchunk * sizeof(float2)) : 0;
+    l.R = align256(T * B * sizeof(float2));
+    return l;
+}
+
+// Largest batch whose intermediates fit the static scratch.
+int noalloc_max_batch(const rm_ctx* c) {
+    size_t lo = 0, hi = kNoAllocScratchBytes;   // the answer is below hi (every sample takes > 1 byte)
+    while (lo < hi) {
+        const size_t mid = (lo + hi + 1) / 2;
+        if (noalloc_layout(c, mid).total() <= kNoAllocScratchBytes) lo = mid; else hi = mid - 1;
+    }
+    return lo > (size_t)INT32_MAX ? INT32_MAX : (int)lo;
+}
 
 }  // namespace
 
@@ -1521,35 +1714,29 @@ rm_status rm_block_forward_noalloc(rm_ctx* c, int layer, const void* X_in, void*
     if (B < 1) return fail(RM_ERR_INVALID_ARG, "B must be >= 1");
     if (!X_in || !X_out) return fail(RM_ERR_INVALID_ARG, "X_in / X_out is NULL");
     if (!aligned16(X_in) || !aligned16(X_out)) return fail(RM_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
-    const size_t T = g.T, D = g.D, F = c->F, Bs = (size_t)B;
+    const size_t T = g.T, D = g.D, Bs = (size_t)B;
     const size_t io_bytes = Bs * T * D * c->esz;
     const char* xi = (const char*)X_in;
     const char* xo = (const char*)X_out;
     if (xi < xo + io_bytes && xo < xi + io_bytes) return fail(RM_ERR_INVALID_ARG, "X_in and X_out overlap");
-    // scratch layout (token-major, rows between tokens = B): S, Hid, Z, chunk statistics, row statistics
-    const size_t bS = align256(T * Bs * D * op_size(c->act));
-    const size_t bH = align256(T * Bs * F * op_size(c->act));
-    const size_t bZ = align256(T * Bs * D * op_size(c->act));
-    const size_t bT = align256(T * Bs * (size_t)c->nchunk * sizeof(float2));
-    const size_t bR = align256(T * Bs * sizeof(float2));
-    const size_t need = bS + bH + bZ + bT + bR;
-    if (need > kNoAllocScratchBytes) {
-        const size_t per = need / Bs + 1;
+    const NoAllocLayout lay = noalloc_layout(c, Bs);
+    const size_t need = lay.total();
+    if (need > kNoAllocScratchBytes)
         return fail(RM_ERR_INVALID_ARG,
-                    "B=%d needs %zu bytes of scratch; the static scratch holds %zu bytes (about B <= %zu here)", B,
-                    need, kNoAllocScratchBytes, kNoAllocScratchBytes / per);
-    }
+                    "B=%d needs %zu bytes of scratch; the static scratch holds %zu bytes (B <= %d for this "
+                    "configuration)",
+                    B, need, kNoAllocScratchBytes, noalloc_max_batch(c));
     RM_CHECK_CUDA(cudaSetDevice(c->device), "cudaSetDevice");
+    cudaStream_t s = as_stream(stream);
     void* base = nullptr;
-    if ((st = noalloc_scratch(c->device, &base)) != RM_OK) return st;
+    if ((st = noalloc_scratch(c->device, s, &base)) != RM_OK) return st;
     char* p = static_cast<char*>(base);
     void* S = p;
-    void* Hid = p + bS;
-    void* Z = p + bS + bH;
-    float2* stats = reinterpret_cast<float2*>(p + bS + bH + bZ);
-    float2* rows = reinterpret_cast<float2*>(p + bS + bH + bZ + bT);
+    void* Hid = p + lay.S;
+    void* Z = p + lay.S + lay.H;
+    float2* stats = reinterpret_cast<float2*>(p + lay.S + lay.H + lay.Z);
+    float2* rows = reinterpret_cast<float2*>(p + lay.S + lay.H + lay.Z + lay.T);
 
-    cudaStream_t s = as_stream(stream);
     const LayerW& w = c->layers[layer];
     MixLnArgs a = mix_args(c, layer, B);
     a.X = X_in;
@@ -1570,8 +1757,8 @@ rm_status rm_block_forward_noalloc(rm_ctx* c, int layer, const void* X_in, void*
         RM_CHECK_CUDA(launch_gemm2_simt(c->act, Hid, w.W2p, w.b2, S, Z, B, g.T, g.D, c->F, B, s), "gemm2 (simt)");
         RM_CHECK_CUDA(launch_rowstats(c->act, Z, rows, B, g.T, g.D, B, c->num_sms, s), "row stats");
     }
-    RM_CHECK_CUDA(launch_ln2_out(c->act, Z, rows, w.g2, w.be2, X_out, B, g.T, g.D, B, 1, g.D, g.ln_eps, c->num_sms,
-                                 s),
+    RM_CHECK_CUDA(launch_ln2_out(c->act, Z, rows, w.g2, w.be2, X_out, false, B, g.T, g.D, B, 1, g.D, g.ln_eps,
+                                 c->num_sms, s),
                   "ln2 out");
     return RM_OK;
 }

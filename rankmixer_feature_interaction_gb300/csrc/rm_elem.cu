@@ -241,7 +241,11 @@ size_t v8_smem_bytes(bool, int T, int D, int q, int) {
     return 2 * (size_t)T * v8_row_stride(D, q) * 2 + 4 * (size_t)D * 2 + 16 + 2 * kMaxT * 4 + 16;
 }
 
-template <bool FROM_Z, int NV>
+// DBG (test hook): write the residual sum y = Mix(X) + X as float32 to
+// a.Ydbg instead of LN1; with FROM_Z the LN2 finalisation runs with mean 0,
+// rstd 1, gamma 1, beta 0 (the identity on fp16 values), so the gather and
+// the fp16 sum are checked bit for bit.
+template <bool FROM_Z, int NV, bool DBG = false>
 __global__ void __launch_bounds__(512)
 mix_ln1_v8_kernel(const MixLnArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -264,6 +268,11 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
     __half* S = reinterpret_cast<__half*>(a.S);
 
     for (int j = threadIdx.x; j < D; j += blockDim.x) {
+        if constexpr (DBG) {
+            sg2[j] = __float2half_rn(1.0f);
+            sb2[j] = __float2half_rn(0.0f);
+            continue;
+        }
         sg1[j] = __float2half_rn(a.g1[j]);
         sb1[j] = __float2half_rn(a.be1[j]);
         if (FROM_Z) {
@@ -293,11 +302,11 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
 
     // FROM_Z with merged row statistics (one (mean, M2) per row): lane k of warp w
     // holds row w + k nwarps of the next sample, loaded one sample ahead
-    const bool merged = FROM_Z && a.nchunk == 1;
+    const bool merged = FROM_Z && (DBG || a.nchunk == 1);
     const int pre_t = warp + lane * nwarps;
     const bool pre_lane = merged && pre_t < T;
     float2 pre = make_float2(0.f, 0.f);
-    if (pre_lane && (int)blockIdx.x < a.B) pre = __ldg(a.stats + (size_t)pre_t * a.Bcap + blockIdx.x);
+    if (!DBG && pre_lane && (int)blockIdx.x < a.B) pre = __ldg(a.stats + (size_t)pre_t * a.Bcap + blockIdx.x);
 
     if (warp == 0 && (int)blockIdx.x < a.B) issue(blockIdx.x, 0);
     int it = 0;
@@ -305,7 +314,10 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
         const int slot = it & 1;
         if (warp == 0 && b + (int)gridDim.x < a.B) issue(b + gridDim.x, slot ^ 1);
         if (merged) {
-            if (pre_lane) {
+            if (pre_lane && DBG) {
+                s_mean[pre_t] = 0.0f;
+                s_rstd[pre_t] = 1.0f;
+            } else if (pre_lane) {
                 s_mean[pre_t] = pre.x;
                 s_rstd[pre_t] = rsqrtf(pre.y / (float)D + a.eps);
                 if (b + (int)gridDim.x < a.B) pre = __ldg(a.stats + (size_t)pre_t * a.Bcap + b + gridDim.x);
@@ -371,6 +383,20 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
                     }
                 }
             }
+            if constexpr (DBG) {
+                float* yrow = a.Ydbg + ((size_t)h * a.Bcap + b) * D;
+#pragma unroll
+                for (int i = 0; i < NV; ++i)
+                    if (i < nv) {
+                        const int j0 = (i << 8) + (lane << 3);
+                        float o[8];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) f2_unpack(y[4 * i + k], o[2 * k], o[2 * k + 1]);
+                        reinterpret_cast<float4*>(yrow + j0)[0] = make_float4(o[0], o[1], o[2], o[3]);
+                        reinterpret_cast<float4*>(yrow + j0)[1] = make_float4(o[4], o[5], o[6], o[7]);
+                    }
+                continue;
+            }
             float lo, hi;
             f2_unpack(s2, lo, hi);
             const float mean = warp_sum(lo + hi) / (float)D;
@@ -416,9 +442,9 @@ bool v8_ok(bool from_z, const MixLnArgs& a) {
            v8_smem_bytes(from_z, a.T, a.D, a.q, a.nchunk) <= 226 * 1024;
 }
 
-template <bool FROM_Z, int NV>
+template <bool FROM_Z, int NV, bool DBG = false>
 cudaError_t launch_v8(const MixLnArgs& a, int num_sms, cudaStream_t s) {
-    auto k = mix_ln1_v8_kernel<FROM_Z, NV>;
+    auto k = mix_ln1_v8_kernel<FROM_Z, NV, DBG>;
     const size_t smem = v8_smem_bytes(FROM_Z, a.T, a.D, a.q, a.nchunk);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -434,16 +460,16 @@ cudaError_t launch_v8(const MixLnArgs& a, int num_sms, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <bool FROM_Z>
+template <bool FROM_Z, bool DBG = false>
 cudaError_t launch_v8_dispatch(const MixLnArgs& a, int num_sms, cudaStream_t s) {
     const int nv = a.D / 256;
-    if (nv <= 1) return launch_v8<FROM_Z, 1>(a, num_sms, s);
-    if (nv <= 2) return launch_v8<FROM_Z, 2>(a, num_sms, s);
-    if (nv <= 3) return launch_v8<FROM_Z, 3>(a, num_sms, s);
-    if (nv <= 4) return launch_v8<FROM_Z, 4>(a, num_sms, s);
-    if (nv <= 6) return launch_v8<FROM_Z, 6>(a, num_sms, s);
-    if (nv <= 8) return launch_v8<FROM_Z, 8>(a, num_sms, s);
-    return launch_v8<FROM_Z, 12>(a, num_sms, s);
+    if (nv <= 1) return launch_v8<FROM_Z, 1, DBG>(a, num_sms, s);
+    if (nv <= 2) return launch_v8<FROM_Z, 2, DBG>(a, num_sms, s);
+    if (nv <= 3) return launch_v8<FROM_Z, 3, DBG>(a, num_sms, s);
+    if (nv <= 4) return launch_v8<FROM_Z, 4, DBG>(a, num_sms, s);
+    if (nv <= 6) return launch_v8<FROM_Z, 6, DBG>(a, num_sms, s);
+    if (nv <= 8) return launch_v8<FROM_Z, 8, DBG>(a, num_sms, s);
+    return launch_v8<FROM_Z, 12, DBG>(a, num_sms, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -977,21 +1003,37 @@ cudaError_t launch_mix_ln1(Act act, bool from_z, const MixLnArgs& a, int num_sms
                   : launch_direct_dispatch<float, float, false>(a, num_sms, s);
 }
 
+cudaError_t launch_mix_residual_debug(bool from_z, const MixLnArgs& a, int num_sms, cudaStream_t s) {
+    if (a.B <= 0) return cudaSuccess;
+    if (!a.Ydbg || !v8_ok(from_z, a)) return cudaErrorNotSupported;
+    return from_z ? launch_v8_dispatch<true, true>(a, num_sms, s) : launch_v8_dispatch<false, true>(a, num_sms, s);
+}
+
 cudaError_t launch_ln2_out(Act act, const void* Z, const float2* stats, const float* g2, const float* be2,
-                           void* X_out, int B, int T, int D, int Bcap, int nchunk, int cw, float eps, int num_sms,
-                           cudaStream_t s) {
+                           void* X_out, bool out_f32, int B, int T, int D, int Bcap, int nchunk, int cw, float eps,
+                           int num_sms, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     const int grid = grid_for((long long)B * T * 32, 256, num_sms * 8);
-    if (act == Act::BF16 && D % 256 == 0)
-        ln2_out_vec_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2,
-                                                               (__nv_bfloat16*)X_out, B, T, D, Bcap, nchunk, cw, eps);
-    else if (act == Act::BF16)
-        ln2_out_kernel<__half, __nv_bfloat16><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2,
+    if (act == Act::BF16 && D % 256 == 0) {
+        if (out_f32)
+            ln2_out_vec_kernel<float><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2, (float*)X_out, B, T, D,
+                                                           Bcap, nchunk, cw, eps);
+        else
+            ln2_out_vec_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2,
                                                                    (__nv_bfloat16*)X_out, B, T, D, Bcap, nchunk, cw,
                                                                    eps);
-    else
+    } else if (act == Act::BF16) {
+        if (out_f32)
+            ln2_out_kernel<__half, float><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2, (float*)X_out, B, T,
+                                                               D, Bcap, nchunk, cw, eps);
+        else
+            ln2_out_kernel<__half, __nv_bfloat16><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2,
+                                                                       (__nv_bfloat16*)X_out, B, T, D, Bcap, nchunk,
+                                                                       cw, eps);
+    } else {
         ln2_out_kernel<float, float><<<grid, 256, 0, s>>>((const float*)Z, stats, g2, be2, (float*)X_out, B, T, D,
                                                           Bcap, nchunk, cw, eps);
+    }
     return cudaGetLastError();
 }
 
@@ -1011,22 +1053,9 @@ cudaError_t launch_ln2_out_op(Act act, const void* Z, const float2* stats, const
     return cudaGetLastError();
 }
 
-cudaError_t launch_ln2_out_f32(const void* Z, const float2* stats, const float* g2, const float* be2, float* X_out,
-                               int B, int T, int D, int Bcap, float eps, int num_sms, cudaStream_t s) {
-    if (B <= 0) return cudaSuccess;
-    const int grid = grid_for((long long)B * T * 32, 256, num_sms * 8);
-    if (D % 256 == 0)
-        ln2_out_vec_kernel<float><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2, X_out, B, T, D, Bcap, 1, D,
-                                                       eps);
-    else
-        ln2_out_kernel<__half, float><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2, X_out, B, T, D, Bcap, 1,
-                                                           D, eps);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_pool(Act act, const void* Z, const float2* stats, const float* g2, const float* be2,
-                        float* pooled, void* XL, int B, int T, int D, int Bcap, int nchunk, int cw, float eps,
-                        int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s) {
+                        float* pooled, void* XL, bool xl_f32, int B, int T, int D, int Bcap, int nchunk, int cw,
+                        float eps, int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     if (T > kMaxT) return cudaErrorNotSupported;
     if (act == Act::BF16 && XL == nullptr && D % 8 == 0 && D <= 8 * 256) {
@@ -1038,7 +1067,10 @@ cudaError_t launch_pool(Act act, const void* Z, const float2* stats, const float
         return cudaGetLastError();
     }
     const int grid = B < num_sms * 8 ? B : num_sms * 8;
-    if (act == Act::BF16)
+    if (act == Act::BF16 && xl_f32)
+        pool_kernel<__half, float><<<grid, kPoolThreads, 0, s>>>((const __half*)Z, stats, g2, be2, pooled, (float*)XL,
+                                                                 B, T, D, Bcap, nchunk, cw, eps);
+    else if (act == Act::BF16)
         pool_kernel<__half, __nv_bfloat16><<<grid, kPoolThreads, 0, s>>>((const __half*)Z, stats, g2, be2, pooled,
                                                                          (__nv_bfloat16*)XL, B, T, D, Bcap, nchunk,
                                                                          cw, eps);
@@ -1067,11 +1099,13 @@ cudaError_t launch_rowstats(Act act, const void* Z, float2* stats, int B, int T,
     return cudaGetLastError();
 }
 
-cudaError_t launch_token_to_sample(Act act, const void* src, void* dst, int B, int T, int D, int Bcap,
+cudaError_t launch_token_to_sample(Act act, const void* src, void* dst, bool out_f32, int B, int T, int D, int Bcap,
                                    cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     const int grid = grid_for((long long)B * T * D, 256);
-    if (act == Act::BF16)
+    if (act == Act::BF16 && out_f32)
+        token_to_sample_kernel<__half, float><<<grid, 256, 0, s>>>((const __half*)src, (float*)dst, B, T, D, Bcap);
+    else if (act == Act::BF16)
         token_to_sample_kernel<__half, __nv_bfloat16><<<grid, 256, 0, s>>>((const __half*)src, (__nv_bfloat16*)dst,
                                                                            B, T, D, Bcap);
     else

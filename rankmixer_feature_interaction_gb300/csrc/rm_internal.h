@@ -19,6 +19,13 @@ constexpr int kDevErrOther = 6;
 inline size_t act_size(Act a) { return a == Act::F32 ? 4 : 2; }
 inline size_t op_size(Act a) { return a == Act::F32 ? 4 : 2; }
 
+// Every device allocation of the library goes through these two: device_alloc
+// counts live allocations and can be made to fail on purpose (a host-side
+// injection for the failure-detection tests: RM_FAULT_INJECT=alloc:N in the
+// environment, or rm_debug_fail_alloc), device_free releases (nullptr: no-op).
+cudaError_t device_alloc(void** p, size_t bytes);
+void device_free(void* p);
+
 // Token-major workspace: element (t, b, j) of a [T][Bcap][W] buffer sits at
 // (t * Bcap + b) * W + j.
 
@@ -39,21 +46,33 @@ struct MixLnArgs {
     float eps;
     int* err;                        // device error word for bounded waits (nullable)
     unsigned long long timeout_ns;
+    // test hook only (launch_mix_residual_debug): y = Mix(X) + X as float32,
+    // token-major [T][Bcap][D], instead of S
+    float* Ydbg;
 };
 
 // S = LN1(Mix(X) + X).
 cudaError_t launch_mix_ln1(Act act, bool from_z, const MixLnArgs& a, int num_sms, cudaStream_t s);
 
-// X_out[b][t][:] = LN2(Z[t][b][:]) in the caller dtype (Z in the operand type).
+// Test hook: the staged 8-wide mixing kernel's residual sum y = Mix(X) + X,
+// written as float32 to a.Ydbg ([T][Bcap][D]) in place of LN1.  from_z: the
+// source rows are fp16 token-major (a.Z) and the kernel's LN2 finalisation is
+// the identity (mean 0, rstd 1, gamma 1, beta 0), so y is the fp16 sum of the
+// two gathered fp16 values; otherwise a.X is bf16 sample-major and y is their
+// float32 sum.  cudaErrorNotSupported for shapes the 8-wide kernel does not take.
+cudaError_t launch_mix_residual_debug(bool from_z, const MixLnArgs& a, int num_sms, cudaStream_t s);
+
+// X_out[b][t][:] = LN2(Z[t][b][:]) in the caller dtype (Z in the operand type),
+// or in float32 when out_f32 (the same float32 values before any rounding).
 cudaError_t launch_ln2_out(Act act, const void* Z, const float2* stats, const float* g2, const float* be2,
-                           void* X_out, int B, int T, int D, int Bcap, int nchunk, int cw, float eps,
+                           void* X_out, bool out_f32, int B, int T, int D, int Bcap, int nchunk, int cw, float eps,
                            int num_sms, cudaStream_t s);
 
 // pooled[b][:] = (1/T) sum_t X_L[b][t][:] with X_L = LN2(Z) in float32; XL (optional)
-// receives X_L sample-major, rounded to the caller dtype.
+// receives X_L sample-major, rounded to the caller dtype, or as float32 when xl_f32.
 cudaError_t launch_pool(Act act, const void* Z, const float2* stats, const float* g2, const float* be2,
-                        float* pooled, void* XL, int B, int T, int D, int Bcap, int nchunk, int cw, float eps,
-                        int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s);
+                        float* pooled, void* XL, bool xl_f32, int B, int T, int D, int Bcap, int nchunk, int cw,
+                        float eps, int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s);
 
 // Merge each row's nchunk chunk partials (GEMM2 epilogue) into (mean, M2) of the row.
 cudaError_t launch_stats_finalize(const float2* part, float2* out, int B, int T, int Bcap, int nchunk, int cw,
@@ -63,8 +82,9 @@ cudaError_t launch_stats_finalize(const float2* part, float2* out, int B, int T,
 cudaError_t launch_rowstats(Act act, const void* Z, float2* stats, int B, int T, int D, int Bcap, int num_sms,
                             cudaStream_t s);
 
-// Token-major operand-type [T][Bcap][D] -> sample-major caller-dtype [B][T][D].
-cudaError_t launch_token_to_sample(Act act, const void* src, void* dst, int B, int T, int D, int Bcap,
+// Token-major operand-type [T][Bcap][D] -> sample-major caller-dtype [B][T][D]
+// (float32 when out_f32: the operand values exactly).
+cudaError_t launch_token_to_sample(Act act, const void* src, void* dst, bool out_f32, int B, int T, int D, int Bcap,
                                    cudaStream_t s);
 
 // Y[b][h][t q + r] = X[b][t][h q + r] on raw element bits (esz 2 or 4).

@@ -474,7 +474,7 @@ template <typename T>
 cudaError_t dalloc(T** p, size_t n, long long* bytes) {
     *p = nullptr;
     if (n == 0) return cudaSuccess;
-    cudaError_t e = cudaMalloc((void**)p, n * sizeof(T));
+    cudaError_t e = device_alloc((void**)p, n * sizeof(T));
     if (e != cudaSuccess) {
         *p = nullptr;
         return e;
@@ -485,7 +485,7 @@ cudaError_t dalloc(T** p, size_t n, long long* bytes) {
 
 cudaError_t dalloc_bytes(void** p, size_t n, long long* bytes) {
     *p = nullptr;
-    cudaError_t e = cudaMalloc(p, n);
+    cudaError_t e = device_alloc(p, n);
     if (e != cudaSuccess) {
         *p = nullptr;
         return e;
@@ -521,7 +521,7 @@ cudaError_t moe_pack_weights(const MoeShape& ms, const void* Wg, const void* bg,
     e = launch_to_f32(ms.act, Wg, tmp, (size_t)ms.T * ms.D * ms.E, s);
     if (e == cudaSuccess) e = launch_transpose_f32(tmp, w.Wg, ms.T, ms.D, ms.E, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    cudaFree(tmp);
+    device_free(tmp);
     return e;
 }
 
@@ -536,12 +536,12 @@ cudaError_t moe_pack_router(const MoeShape& ms, const void* Wg, const void* bg, 
     e = launch_to_f32(ms.act, Wg, tmp, (size_t)ms.T * ms.D * ms.E, s);
     if (e == cudaSuccess) e = launch_transpose_f32(tmp, *Wg_out, ms.T, ms.D, ms.E, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    cudaFree(tmp);
+    device_free(tmp);
     return e;
 }
 
 void moe_free_weights(MoeWeights& w) {
-    cudaFree(w.W1p); cudaFree(w.W2p); cudaFree(w.b1); cudaFree(w.b2); cudaFree(w.Wg); cudaFree(w.bg);
+    device_free(w.W1p); device_free(w.W2p); device_free(w.b1); device_free(w.b2); device_free(w.Wg); device_free(w.bg);
     w = MoeWeights{};
 }
 
@@ -563,8 +563,8 @@ cudaError_t moe_alloc_workspace(const MoeShape& ms, int Bcap, MoeWorkspace& ws, 
 }
 
 void moe_free_workspace(MoeWorkspace& ws) {
-    cudaFree(ws.gates); cudaFree(ws.counts); cudaFree(ws.offsets); cudaFree(ws.row_gate); cudaFree(ws.slot_of);
-    cudaFree(ws.tile_prefix); cudaFree(ws.tile_prefix256); cudaFree(ws.Sg); cudaFree(ws.Hm);
+    device_free(ws.gates); device_free(ws.counts); device_free(ws.offsets); device_free(ws.row_gate); device_free(ws.slot_of);
+    device_free(ws.tile_prefix); device_free(ws.tile_prefix256); device_free(ws.Sg); device_free(ws.Hm);
     ws = MoeWorkspace{};
 }
 

@@ -103,11 +103,6 @@ cudaError_t launch_ln1_recompute(Act act, bool x_f32, const void* X, void* S, vo
                                  const float* be1, int B, int T, int D, int Bcap, float eps, int num_sms,
                                  cudaStream_t s);
 
-// X_out[b][t][:] = LN2(Z[t][b][:]) in float32 from fp16 Z and merged row
-// statistics (the stack backward keeps every layer input in float32).
-cudaError_t launch_ln2_out_f32(const void* Z, const float2* stats, const float* g2, const float* be2, float* X_out,
-                               int B, int T, int D, int Bcap, float eps, int num_sms, cudaStream_t s);
-
 // LN2 backward.  Z [T][Bcap][D] (aux type), G sample-major [B][T][D] float:
 // dZ = LN2 backward of G (float, token-major); per (token, CTA) partial sums
 // [T][nblk][D] of dZ, G * zhat and G, and the largest |dZ| of each (token,

@@ -596,11 +596,15 @@ cudaError_t launch_unimix_ln1(XType xt, Act act, const void* X, const void* Y, v
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_unimix_out(Act act, const void* Y, void* out, long long n, cudaStream_t s) {
+cudaError_t launch_unimix_out(Act act, const void* Y, void* out, bool out_f32, long long n, cudaStream_t s) {
     if (n <= 0) return cudaSuccess;
     if (act == Act::F32)
         return cudaMemcpyAsync(out, Y, (size_t)n * sizeof(float), cudaMemcpyDeviceToDevice, s);
-    convert_kernel<__half, __nv_bfloat16><<<grid_of(n, 256), 256, 0, s>>>((const __half*)Y, (__nv_bfloat16*)out, n);
+    if (out_f32)
+        convert_kernel<__half, float><<<grid_of(n, 256), 256, 0, s>>>((const __half*)Y, (float*)out, n);
+    else
+        convert_kernel<__half, __nv_bfloat16><<<grid_of(n, 256), 256, 0, s>>>((const __half*)Y, (__nv_bfloat16*)out,
+                                                                              n);
     return cudaGetLastError();
 }
 

@@ -51,8 +51,8 @@ cudaError_t launch_unimix_ln1(XType xt, Act act, const void* X, const void* Y, v
                               const float* be1, int B, int T, int D, int Bcap, float eps, int num_sms,
                               cudaStream_t s);
 
-// out[i] = Y[i] in the caller dtype (n values).
-cudaError_t launch_unimix_out(Act act, const void* Y, void* out, long long n, cudaStream_t s);
+// out[i] = Y[i] in the caller dtype, or float32 when out_f32 (n values).
+cudaError_t launch_unimix_out(Act act, const void* Y, void* out, bool out_f32, long long n, cudaStream_t s);
 
 // X_out[b][t][:] = LN2(Z[t][b][:]) in the operand type (fp16 for bf16
 // contexts): a UniMixing layer's input when it follows another layer.

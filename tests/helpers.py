@@ -1,4 +1,4 @@
-"""Shared helpers for the parity tests: the error metrics."""
+"""Shared helpers for the parity tests: the error metrics and the bf16 rounding check."""
 from __future__ import annotations
 
 import numpy as np
@@ -6,25 +6,17 @@ import numpy as np
 # Tolerances (written here, used by every parity test):
 #   float32 path: max over elements of |g - o| / max(|o|, rms(o)) <= 1e-4;
 #   bf16 path:    max over elements of |g - o| / rms(o) <= 2e-2, rms over the compared output.
-# A result the library STORES in bf16 carries its own rounding: a value computed
-# exactly and then correctly rounded to bf16 is off by up to half an ulp, which
-# for |o| >= 8 is already 2^-5 ~ 2.8e-2 * rms for unit-rms outputs.  For such
-# outputs the bar applies to the computation: the half-ulp of bf16 at the value
-# is allowed on top, |g - o| <= 2e-2 rms(o) + ulp_bf16(|o|) / 2.  Results stored
-# in float32 (the pooled output, the MoE PFFN output) are held to the bare bound.
+# Both bars apply to the computation.  Where a bf16 context stores an output in
+# bf16, the tests ask the library for the same output in float32 (out_dtype
+# RM_F32: the values before their last rounding), hold that to the bar, and
+# check the bf16 output bit for bit against round-to-nearest-even of it
+# (assert_bf16_rounding).
 TOL_F32 = 1e-4
 TOL_BF16 = 2e-2
 
 
 def rms(o: np.ndarray) -> float:
     return float(np.sqrt(np.mean(np.square(o))))
-
-
-def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
-    """Half the spacing of bf16 numbers (8 significant bits) at |x|."""
-    ax = np.abs(np.asarray(x, dtype=np.float64))
-    e = np.floor(np.log2(np.maximum(ax, 2.0 ** -126)))
-    return np.ldexp(1.0, (e - 8).astype(np.int64))
 
 
 def rel_err_f32(g: np.ndarray, o: np.ndarray) -> float:
@@ -34,17 +26,11 @@ def rel_err_f32(g: np.ndarray, o: np.ndarray) -> float:
     return float(np.max(np.abs(g - o) / np.maximum(np.abs(o), floor)))
 
 
-def rel_err_bf16(g: np.ndarray, o: np.ndarray, stored_bf16: bool = False, both_stored: bool = False) -> float:
-    """max |g - o| / rms(o); stored_bf16: g was rounded to bf16 by the library (half an
-    ulp allowed); both_stored: g and o are two such results (half an ulp each)."""
+def rel_err_bf16(g: np.ndarray, o: np.ndarray) -> float:
+    """max |g - o| / rms(o)."""
     g = np.asarray(g, dtype=np.float64)
     o = np.asarray(o, dtype=np.float64)
-    d = np.abs(g - o)
-    if stored_bf16 or both_stored:
-        # (1 + 2^-14): the store rounds a float32 value, not the exact one
-        d = np.maximum(d - half_ulp_bf16(np.maximum(np.abs(o), np.abs(g))) * (1 + 2.0 ** -14) * (2 if both_stored else 1),
-                       0.0)
-    return float(np.max(d) / max(rms(o), 1e-30))
+    return float(np.max(np.abs(g - o)) / max(rms(o), 1e-30))
 
 
 def _as_np(g):
@@ -57,18 +43,29 @@ def _as_np(g):
     return np.asarray(g, dtype=np.float64), False
 
 
-def check(g, o, dtype: str, what: str, tol: float | None = None, both_stored: bool = False) -> float:
+def check(g, o, dtype: str, what: str, tol: float | None = None) -> float:
     """g: GPU result (torch tensor or array), o: oracle result; dtype: the path ("f32" or "bf16").
-    both_stored: o is itself a bf16-stored GPU result (a comparison of two paths)."""
+    The bare bar of the path, with no allowance for the storage format."""
     g, stored_bf16 = _as_np(g)
     if dtype == "f32":
         err = rel_err_f32(g, o)
         tol = TOL_F32 if tol is None else tol
     else:
-        err = rel_err_bf16(g, o, stored_bf16, both_stored=both_stored and stored_bf16)
+        err = rel_err_bf16(g, o)
         tol = TOL_BF16 if tol is None else tol
     assert np.all(np.isfinite(g)), f"{what}: non-finite GPU values"
-    raw = rel_err_bf16(g, o) if dtype != "f32" else err
-    print(f"[parity] {what}: {err:.3e} (tol {tol:.1e}; max|g-o|/rms {raw:.3e}{', bf16-stored' if stored_bf16 else ''})")
+    print(f"[parity] {what}: {err:.3e} (tol {tol:.1e}{', bf16-stored' if stored_bf16 else ''})")
     assert err <= tol, f"{what}: error {err:.3e} > {tol:.1e}"
     return err
+
+
+def assert_bf16_rounding(g_bf16, g_f32, what: str) -> None:
+    """The bf16 output equals round-to-nearest-even of the float32 output of the same
+    computation, bit for bit (torch's float32 -> bfloat16 conversion rounds to nearest even)."""
+    import torch
+    assert g_bf16.dtype == torch.bfloat16 and g_f32.dtype == torch.float32, what
+    want = g_f32.to(torch.bfloat16)
+    same = torch.eq(g_bf16.view(torch.int16), want.view(torch.int16))
+    n_bad = int((~same).sum().item())
+    print(f"[parity] {what}: bf16 output == RNE(float32 output) for {g_bf16.numel() - n_bad}/{g_bf16.numel()}")
+    assert n_bad == 0, f"{what}: {n_bad} bf16 values differ from the rounded float32 result"

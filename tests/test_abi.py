@@ -46,7 +46,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert _lib.rm_abi_version() == 2
+    assert _lib.rm_abi_version() == 3
 
 
 def _cfg(**kw):
@@ -98,8 +98,8 @@ def test_null_context_calls(lib):
     assert lib.rm_destroy(None) == _lib.RM_OK
     info = _lib.rm_info()
     assert lib.rm_get_info(None, ctypes.byref(info)) == _lib.RM_ERR_INVALID_ARG
-    assert lib.rm_block_forward(None, 0, None, None, None, 1, None) == _lib.RM_ERR_INVALID_ARG
-    assert lib.rm_stack_forward(None, None, None, None, 1, None) == _lib.RM_ERR_INVALID_ARG
+    assert lib.rm_block_forward(None, 0, None, None, None, _lib.RM_BF16, 1, None) == _lib.RM_ERR_INVALID_ARG
+    assert lib.rm_stack_forward(None, None, None, None, _lib.RM_BF16, 1, None) == _lib.RM_ERR_INVALID_ARG
     assert lib.rm_moe_pffn_forward(None, 0, None, None, None, 1, None) == _lib.RM_ERR_INVALID_ARG
     assert lib.rm_sync_status(None, None) == _lib.RM_ERR_INVALID_ARG
     assert lib.rm_profile_enable(None, 1) == _lib.RM_ERR_INVALID_ARG
@@ -116,8 +116,18 @@ def test_null_context_calls(lib):
     assert lib.rm_debug_gelu_grad(None, None, 3, None) == _lib.RM_ERR_INVALID_ARG    # NULL buffers
     assert lib.rm_set_unimixing(None, 0, None, None, 4, 1.0, 5, None) == _lib.RM_ERR_INVALID_ARG
     assert lib.rm_unimixing_weights(None, 0, None, None, None) == _lib.RM_ERR_INVALID_ARG
-    assert lib.rm_unimixing(None, 0, None, None, 1, None) == _lib.RM_ERR_INVALID_ARG
+    assert lib.rm_unimixing(None, 0, None, None, _lib.RM_BF16, 1, None) == _lib.RM_ERR_INVALID_ARG
     assert "ctx is NULL" in _lib.rm_last_error()
+
+
+def test_debug_mix_residual_rejects_bad_arguments_on_host(lib):
+    buf = ctypes.create_string_buffer(1 << 16)
+    p = (ctypes.addressof(buf) + 15) // 16 * 16
+    assert lib.rm_debug_mix_residual(None, 0, None, 1, 4, 256, None) == _lib.RM_ERR_INVALID_ARG   # NULL
+    assert lib.rm_debug_mix_residual(p, 0, p + 8192, 1, 3, 256, None) == _lib.RM_ERR_INVALID_ARG  # D % T
+    assert lib.rm_debug_mix_residual(p, 0, p + 8192, 0, 4, 256, None) == _lib.RM_ERR_INVALID_ARG  # B = 0
+    assert lib.rm_debug_mix_residual(p, 0, p + 1024, 1, 4, 256, None) == _lib.RM_ERR_INVALID_ARG  # overlap
+    assert lib.rm_debug_mix_residual(p + 2, 0, p + 8192, 1, 4, 256, None) == _lib.RM_ERR_INVALID_ARG   # alignment
 
 
 def test_config_struct_matches_the_header(lib):
@@ -136,3 +146,14 @@ def test_binding_raises_with_status_and_message(lib):
         _lib.rm_token_mix(0, 0, 1, 4, 8, 4, _lib.RM_F32, 0)
     assert e.value.status == _lib.RM_ERR_INVALID_ARG
     assert "NULL" in str(e.value)
+
+
+def test_allocation_hooks_answer_without_a_device(lib):
+    made = ctypes.c_longlong(-1)
+    live = ctypes.c_longlong(-1)
+    nbytes = ctypes.c_longlong(-1)
+    assert lib.rm_debug_alloc_stats(ctypes.byref(made), ctypes.byref(live), ctypes.byref(nbytes)) == _lib.RM_OK
+    assert made.value >= 0 and live.value >= 0 and nbytes.value >= 0
+    assert lib.rm_debug_alloc_stats(None, None, None) == _lib.RM_OK
+    assert lib.rm_debug_fail_alloc(3) == _lib.RM_OK
+    assert lib.rm_debug_fail_alloc(-1) == _lib.RM_OK

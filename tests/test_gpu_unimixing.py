@@ -13,7 +13,7 @@ import torch
 import oracle
 from rankmixer_feature_interaction_gb300 import _lib, synth
 from rankmixer_feature_interaction_gb300.api import RankMixer
-from tests.helpers import check
+from tests.helpers import assert_bf16_rounding, check
 
 pytestmark = pytest.mark.gpu
 
@@ -71,12 +71,17 @@ def test_unimixing_op_matches_oracle(dtype, path, T, D, bs, B, tau):
     WG, WB = synth.make_unimix_weights(T, D, bs, 6 + bs, DEV)
     m.set_unimixing(0, WG, WB, tau=tau, iters=ITERS)
     X = synth.make_input(B, T, D, 7, dtype, DEV)
-    Y = m.unimixing(0, X)
+    Y = m.unimixing(0, X, out_dtype="f32")
+    Yc = m.unimixing(0, X)                     # the context dtype
     torch.cuda.synchronize()
     assert m.sync_status() == _lib.RM_OK
     oWG, oWB = _constrained(WG, WB, tau)
     ref = oracle.unimixing(_np(X), oWG, oWB)
     check(Y, ref, dtype, f"unimixing {dtype} T={T} D={D} bs={bs} B={B} tau={tau}")
+    if dtype == "bf16":
+        assert_bf16_rounding(Yc, Y, "unimixing output")
+    else:
+        assert torch.equal(Yc, Y)
 
 
 @pytest.mark.parametrize("dtype,T,D,k,B,bs", [
@@ -92,10 +97,16 @@ def test_stack_and_block_with_unimixing_match_oracle(dtype, T, D, k, B, bs):
     tau = 0.3
     m.set_unimixing(0, WG, WB, tau=tau, iters=ITERS)          # layer 1 keeps TokenMixing
     X0 = synth.make_input(B, T, D, 11, dtype, DEV)
-    pooled, XL = m.stack_forward(X0, return_XL=True)
-    X1 = m.block_forward(0, X0)
+    pooled, XL = m.stack_forward(X0, return_XL=True, xl_dtype="f32")
+    X1 = m.block_forward(0, X0, out_dtype="f32")
+    if dtype == "bf16":
+        _, XLb = m.stack_forward(X0, return_XL=True)
+        X1b = m.block_forward(0, X0)
     torch.cuda.synchronize()
     assert m.sync_status() == _lib.RM_OK
+    if dtype == "bf16":
+        assert_bf16_rounding(XLb, XL, "X_L with UniMixing")
+        assert_bf16_rounding(X1b, X1, "block 0 with UniMixing")
     oWG, oWB = _constrained(WG, WB, tau)
     ref = synth.to_f64(layers)
     ref[0]["WG"], ref[0]["WB"] = oWG, oWB
