@@ -159,8 +159,21 @@ def _lazy_calls(layers):
 
 
 def test_lazy_workspaces_survive_every_allocation_failure():
+    """Each allocation of each lazily allocating call fails once on a fresh context: the
+    call returns RM_ERR_OOM, the retry completes the workspace and computes the result of
+    a context that never saw a failure, and closing the context frees everything.  Then
+    on one context every retry fails at its first new allocation until the workspace is
+    complete (a failed call keeps the buffers it got)."""
     layers = _layers()
     live0 = _live()
+
+    def same(got, want, name):
+        for a, b in zip(got, want):
+            a64 = a.detach().to("cpu", torch.float64).numpy()
+            b64 = b.detach().to("cpu", torch.float64).numpy()
+            scale = max(float(np.sqrt(np.mean(b64 ** 2))), 1e-30)
+            assert np.max(np.abs(a64 - b64)) <= 1e-5 * scale, f"{name}: result after failures differs"
+
     for name, lay, kw, setup, call in _lazy_calls(layers):
         ref_m = _create(lay, **kw)
         if setup:
@@ -170,20 +183,34 @@ def test_lazy_workspaces_survive_every_allocation_failure():
         torch.cuda.synchronize()
         ref_m.close()
         assert n >= 1, name
-        m = _create(lay, **kw)
-        if setup:
-            setup(m)
         for i in range(n):
+            m = _create(lay, **kw)
+            if setup:
+                setup(m)
             _lib.rm_debug_fail_alloc(i)
             _expect_oom(lambda: call(m), f"{name}, allocation {i}")
             _lib.rm_debug_fail_alloc(-1)
-        got = call(m)
+            got = call(m)
+            torch.cuda.synchronize()
+            assert m.sync_status() == _lib.RM_OK, name
+            same(got, want, f"{name}, failure at allocation {i}")
+            m.close()
+            assert _live() == live0, f"{name}: allocations leaked after a failure at allocation {i}"
+        if name == "UniMixing":
+            continue          # rm_set_unimixing replaces the layer's weights whole on every call
+        m = _create(lay, **kw)
+        if setup:
+            setup(m)
+        for attempt in range(n + 1):
+            _lib.rm_debug_fail_alloc(0)
+            try:
+                got = call(m)
+                break
+            except _lib.RankMixerError as e:
+                assert e.status == _lib.RM_ERR_OOM, f"{name}: {e}"
+        _lib.rm_debug_fail_alloc(-1)
+        assert attempt >= 1, f"{name}: the first call allocated nothing"
         torch.cuda.synchronize()
-        assert m.sync_status() == _lib.RM_OK, name
-        for a, b in zip(got, want):
-            a64 = a.detach().to("cpu", torch.float64).numpy()
-            b64 = b.detach().to("cpu", torch.float64).numpy()
-            scale = max(float(np.sqrt(np.mean(b64 ** 2))), 1e-30)
-            assert np.max(np.abs(a64 - b64)) <= 1e-5 * scale, f"{name}: result after failures differs"
+        same(got, want, f"{name}, progressive failures")
         m.close()
         assert _live() == live0, f"{name}: allocations leaked"

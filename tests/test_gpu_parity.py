@@ -149,21 +149,25 @@ def test_bf16_block_and_stack(path, T, D, k, L, B):
 
 @pytest.mark.parametrize("path", ["tcgen05", "simt"])
 def test_stack_matches_chained_blocks(path):
-    """The stack keeps X_n on the device between layers; chaining rm_block_forward feeds
-    each block its input rounded to bf16 (at most 2^-9 relative per value).  The float32
-    outputs of both must agree to 3e-2 * RMS, and the pooled output must be the token mean
-    of X_L."""
+    """Chaining rm_block_forward feeds each block its input rounded to bf16, the stack
+    keeps X_n on the device in fp16: the two are different computations, so each is
+    held to the oracle on its own inputs -- every chained block against the oracle's
+    block on the bf16 input it actually received, the stack against the oracle's
+    stack -- and the pooled output must be the token mean of X_L."""
     T, D, k, L, B = 4, 256, 2, 3, 200
     m, layers, X = _build(T, D, k, L, B, 5, "bf16", path=path)
+    p64 = synth.to_f64(layers)
     pooled, XL = m.stack_forward(X, return_XL=True, xl_dtype="f32")
     Xn = X
-    for n in range(L - 1):
-        Xn = m.block_forward(n, Xn)
-    XLc = m.block_forward(L - 1, Xn, out_dtype="f32")
-    torch.cuda.synchronize()
-    check(XL, _np(XLc), "bf16", "stack vs chained blocks", tol=3e-2)
+    for n in range(L):
+        out32 = m.block_forward(n, Xn, out_dtype="f32")
+        out = m.block_forward(n, Xn)
+        torch.cuda.synchronize()
+        check(out32, oracle.block_forward(_np(Xn), p64[n]), "bf16", f"chained block {n}")
+        assert_bf16_rounding(out, out32, f"chained block {n}")
+        Xn = out
     torch.testing.assert_close(pooled, XL.mean(dim=1), rtol=0, atol=2e-3)
-    pr, xr = oracle.stack_forward(_np(X), synth.to_f64(layers), return_XL=True)
+    pr, xr = oracle.stack_forward(_np(X), p64, return_XL=True)
     check(XL, xr, "bf16", "stack X_L (L=3)")
     check(pooled, pr, "bf16", "pooled (L=3)")
 
@@ -483,18 +487,20 @@ print("ok")
 
 
 @pytest.mark.parametrize("tuning", [{},                                            # pairs, 2 k-blocks per stage
+                                    {"RM_GEMM_SCHED": "static"},                    # pairs, static tile order
                                     {"RM_GEMM_PAIR": "0"},                          # one CTA per tile
                                     {"RM_GEMM_PAIR": "2"},                          # pairs for GEMM2 only
                                     {"RM_GEMM_KSUB": "1"},                          # one k-block per stage
                                     {"RM_GEMM1_EPW": "16"},                         # 16 GELU epilogue warps
                                     {"RM_GEMM1_EPW": "16", "RM_GEMM_KSUB": "1"}])
-@pytest.mark.parametrize("shape", [(4, 256, 2, 2, 300), (2, 192, 2, 1, 300)])
+@pytest.mark.parametrize("shape", [(4, 256, 2, 2, 300), (2, 192, 2, 1, 300), (8, 512, 2, 2, 1100)])
 def test_every_gemm_tile_dispatch(tuning, shape):
     import os
     import subprocess
     import sys
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    env = {k: v for k, v in os.environ.items() if k not in ("RM_GEMM_PAIR", "RM_GEMM_KSUB", "RM_GEMM1_EPW")}
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("RM_GEMM_PAIR", "RM_GEMM_KSUB", "RM_GEMM1_EPW", "RM_GEMM_SCHED")}
     env.update(tuning)
     r = subprocess.run([sys.executable, "-c", _DISPATCH_CHILD.format(root=root, shape=shape)], env=env, cwd=root,
                        capture_output=True, text=True, timeout=600)
