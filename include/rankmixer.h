@@ -398,12 +398,10 @@ RM_API rm_status rm_score(rm_ctx *ctx, const void *E, const float *head_w, float
  *     that device.  So make the first call on a device before any stream
  *     capture (a captured first call returns RM_ERR_INVALID_ARG), and after a
  *     device reset make one uncaptured call before capturing again.
- *   - All calls share the array and it keeps the last call's contents.  The
- *     two tile counters of the tensor-core GEMMs in it are cleared at the
- *     start of each call (cudaMemsetAsync on `stream`, which allocates
- *     nothing); every other element a call uses is written earlier in the
- *     same call.  Calls that overlap on the GPU (other streams, other threads,
- *     other contexts) race on it: serialise them.
+ *   - All calls share the array and it keeps the last call's contents.  Every
+ *     element a call uses is written earlier in the same call, so nothing
+ *     needs clearing, but calls that overlap on the GPU (other streams, other
+ *     threads, other contexts) race on it: serialise them.
  *   - Dense TokenMixing layers only (RM_ERR_UNSUPPORTED for a Sparse-MoE
  *     layer, and for a layer set to UniMixing by rm_set_unimixing, whose
  *     mixing uses the context's workspace).

@@ -213,11 +213,9 @@ struct rm_ctx {
     float* pooled_dev = nullptr;
     cudaStream_t s_in = nullptr, s_out = nullptr;
     cudaEvent_t ev_in[kHostChunksMax] = {}, ev_done[kHostChunksMax] = {};
-    // error word, the debug flag nothing sets, and the tile counters of the two
-    // dense GEMMs (kSchedWords ints each; zero between launches)
+    // error word and the debug flag nothing sets
     int* d_err = nullptr;
     int* d_flag = nullptr;
-    int* d_sched = nullptr;
     long long weight_bytes = 0, ws_bytes = 0;
     // profiling
     bool prof = false;
@@ -285,7 +283,7 @@ void free_ctx(rm_ctx* c) {
     }
     if (c->s_in) cudaStreamDestroy(c->s_in);
     if (c->s_out) cudaStreamDestroy(c->s_out);
-    device_free(c->d_err); device_free(c->d_flag); device_free(c->d_sched);
+    device_free(c->d_err); device_free(c->d_flag);
     for (auto& e : c->ev_pool) { cudaEventDestroy(e.a); cudaEventDestroy(e.b); }
     delete c;
 }
@@ -386,13 +384,13 @@ rm_status run_pffn(rm_ctx* c, int layer, int B, cudaStream_t s) {
         {
             ProfScope ps(c, RM_K_GEMM1, s);
             cudaError_t e = launch_gemm1_tc(c->S, w.W1p, w.b1, c->Hid, B, g.T, g.D, c->F, c->Bcap, c->num_sms,
-                                            c->d_sched, c->d_err, kWaitTimeoutNs, s);
+                                            c->d_err, kWaitTimeoutNs, s);
             if (e != cudaSuccess) return cuda_fail(e, (std::string("gemm1 (tcgen05) ") + tc_last_error()).c_str());
         }
         {
             ProfScope ps(c, RM_K_GEMM2, s);
             cudaError_t e = launch_gemm2_tc(c->Hid, w.W2p, w.b2, c->S, c->Z, c->stats, B, g.T, g.D, c->F, c->Bcap,
-                                            c->num_sms, c->d_sched + kSchedWords, c->d_err, kWaitTimeoutNs, s);
+                                            c->num_sms, c->d_err, kWaitTimeoutNs, s);
             if (e != cudaSuccess) return cuda_fail(e, (std::string("gemm2 (tcgen05) ") + tc_last_error()).c_str());
         }
         ProfScope ps(c, RM_K_ROWSTATS, s);
@@ -925,8 +923,7 @@ rm_status rm_create(const rm_config* cfg, const rm_layer_params* layers, int dev
         (st = dmalloc(c, (void**)&c->stats, T * Bc * (size_t)c->nchunk * sizeof(float2), &c->ws_bytes)) != RM_OK ||
         (st = dmalloc(c, (void**)&c->rows, T * Bc * sizeof(float2), &c->ws_bytes)) != RM_OK ||
         (st = dmalloc(c, (void**)&c->d_err, sizeof(int), nullptr)) != RM_OK ||
-        (st = dmalloc(c, (void**)&c->d_flag, sizeof(int), nullptr)) != RM_OK ||
-        (st = dmalloc(c, (void**)&c->d_sched, 2 * kSchedWords * sizeof(int), nullptr)) != RM_OK) {
+        (st = dmalloc(c, (void**)&c->d_flag, sizeof(int), nullptr)) != RM_OK) {
         free_ctx(c);
         return st;
     }
@@ -945,7 +942,6 @@ rm_status rm_create(const rm_config* cfg, const rm_layer_params* layers, int dev
     }
     cudaMemset(c->d_err, 0, sizeof(int));
     cudaMemset(c->d_flag, 0, sizeof(int));
-    cudaMemset(c->d_sched, 0, 2 * kSchedWords * sizeof(int));
     c->layers.resize(cfg->L);
     for (int n = 0; n < cfg->L; ++n) {
         st = pack_layer(c, layers[n], c->layers[n], 0);
@@ -1534,8 +1530,6 @@ rm_status rm_sync_status(rm_ctx* c, void* stream) {
     RM_CHECK_CUDA(cudaMemcpy(&code, c->d_err, sizeof(int), cudaMemcpyDeviceToHost), "read error word");
     if (code != 0) {
         RM_CHECK_CUDA(cudaMemset(c->d_err, 0, sizeof(int)), "clear error word");
-        // a kernel that gave up may have left its tile counter part way
-        RM_CHECK_CUDA(cudaMemset(c->d_sched, 0, 2 * kSchedWords * sizeof(int)), "clear tile counters");
         RM_CHECK_CUDA(cudaDeviceSynchronize(), "clear error word");
         if (code == kDevErrTimeout) return fail(RM_ERR_TIMEOUT, "a device-side wait ran out of time");
         return fail(RM_ERR_DEVICE, "device error code %d", code);
@@ -1679,8 +1673,8 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // = B): S, Hid and Z in the operand type, the GEMM2 chunk statistics (tensor-
 // core path only) and the merged row statistics, each 256-byte aligned.
 struct NoAllocLayout {
-    size_t S, H, Z, T, R, Q;
-    size_t total() const { return S + H + Z + T + R + Q; }
+    size_t S, H, Z, T, R;
+    size_t total() const { return S + H + Z + T + R; }
 };
 
 NoAllocLayout noalloc_layout(const rm_ctx* c, size_t B) {
@@ -1691,7 +1685,6 @@ NoAllocLayout noalloc_layout(const rm_ctx* c, size_t B) {
     l.Z = align256(T * B * D * osz);
     l.T = c->use_tc ? align256(T * B * (size_t)c->nchunk * sizeof(float2)) : 0;
     l.R = align256(T * B * sizeof(float2));
-    l.Q = c->use_tc ? 256 : 0;           // the two GEMMs' tile counters
     return l;
 }
 
@@ -1743,7 +1736,6 @@ rm_status rm_block_forward_noalloc(rm_ctx* c, int layer, const void* X_in, void*
     void* Z = p + lay.S + lay.H;
     float2* stats = reinterpret_cast<float2*>(p + lay.S + lay.H + lay.Z);
     float2* rows = reinterpret_cast<float2*>(p + lay.S + lay.H + lay.Z + lay.T);
-    int* sched = reinterpret_cast<int*>(p + lay.S + lay.H + lay.Z + lay.T + lay.R);
 
     const LayerW& w = c->layers[layer];
     MixLnArgs a = mix_args(c, layer, B);
@@ -1752,13 +1744,11 @@ rm_status rm_block_forward_noalloc(rm_ctx* c, int layer, const void* X_in, void*
     a.Bcap = B;
     RM_CHECK_CUDA(launch_mix_ln1(c->act, false, a, c->num_sms, s), "mix+ln1");
     if (c->use_tc) {
-        // the tile counters start at zero (a call that gave up part way may have left them set)
-        RM_CHECK_CUDA(cudaMemsetAsync(sched, 0, 2 * kSchedWords * sizeof(int), s), "clear tile counters");
-        cudaError_t e = launch_gemm1_tc(S, w.W1p, w.b1, Hid, B, g.T, g.D, c->F, B, c->num_sms, sched, c->d_err,
+        cudaError_t e = launch_gemm1_tc(S, w.W1p, w.b1, Hid, B, g.T, g.D, c->F, B, c->num_sms, c->d_err,
                                         kWaitTimeoutNs, s);
         if (e != cudaSuccess) return cuda_fail(e, (std::string("gemm1 (tcgen05) ") + tc_last_error()).c_str());
-        e = launch_gemm2_tc(Hid, w.W2p, w.b2, S, Z, stats, B, g.T, g.D, c->F, B, c->num_sms, sched + kSchedWords,
-                            c->d_err, kWaitTimeoutNs, s);
+        e = launch_gemm2_tc(Hid, w.W2p, w.b2, S, Z, stats, B, g.T, g.D, c->F, B, c->num_sms, c->d_err,
+                            kWaitTimeoutNs, s);
         if (e != cudaSuccess) return cuda_fail(e, (std::string("gemm2 (tcgen05) ") + tc_last_error()).c_str());
         RM_CHECK_CUDA(launch_stats_finalize(stats, rows, B, g.T, B, c->nchunk, c->cw, c->num_sms, s),
                       "row statistics");

@@ -424,47 +424,6 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
-// Wait on a local mbarrier with acquire semantics at cluster scope (its phase
-// may be completed by an arrival from the peer CTA that releases data written
-// into this CTA's shared memory); bounded as mbar_wait_bounded.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ bool mbar_wait_bounded_cluster(uint32_t bar, uint32_t parity, volatile int* abort,
-                                                          int* err, uint64_t timeout_ns) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
-        if ((it & 255u) == 0u) {
-            if (*abort) return false;
-            if (globaltimer_ns() - t0 > timeout_ns) {
-                *abort = 1;
-                latch_error(err, kDevErrTimeout);
-                return false;
-            }
-        }
-    }
-}
-
-// 32-bit store to a shared::cluster address (this CTA's or a peer's).
-__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
-    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
-}
-__device__ __forceinline__ int ld_shared_s32(uint32_t addr) {
-    int v;
-    asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-    return v;
-}
-
 // Tiled TMA load into this CTA's shared memory whose completion is counted on
 // an mbarrier that may live in the peer CTA of the pair (cta_group::2).
 __device__ __forceinline__ void tma_load_3d_pair(const CUtensorMap* m, uint32_t dst, uint32_t bar_cluster, int x, int y,

@@ -88,11 +88,6 @@ struct Args {
     float2* stats;            // EPI_RESID row partials [row][nchunk]
     int nchunk;
     const float* row_gate;    // EPI_GATED: gate of each packed row (same row index as A)
-    // CTA-pair kernel, uniform groups: dynamic tile order.  sched[0] is the next tile
-    // to hand out and sched[1] counts the pairs that have finished; both are 0 when the
-    // kernel starts and the last pair to finish puts them back to 0.  nullptr: each
-    // pair takes tiles pair, pair + npairs, ... (static round robin).
-    int* sched;
     int* err;
     unsigned long long timeout_ns;
 };
@@ -484,24 +479,6 @@ pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 
 
 // ----------------------------------------------------------------------------
-// Dynamic tile order for the CTA-pair kernel.  The even CTA's producer warp
-// draws the pair's next tile from a global counter (atomicAdd) only when it is
-// about to load that tile, and publishes it through a ring of kSchedSlots
-// slots in both CTAs' shared memory: slot value + "full" mbarrier in each CTA
-// (one arrival, from the drawing producer), and an "empty" mbarrier in the
-// even CTA counting every other role that reads the slot (the MMA warp, the
-// odd CTA's producer and both CTAs' epilogue warps), which must all have read
-// a slot before it is refilled.  Tiles are thus handed out in order to the
-// pairs as they become ready, so the N tiles of one row block start within a
-// few microseconds of each other and read its A rows from L2 (with the static
-// round robin the pairs sharing a row block drift apart over the launch, and
-// A was read about twice from DRAM in the second GEMM).  A drawn index past
-// the last tile is published as -1, which ends every role's loop.
-// ----------------------------------------------------------------------------
-constexpr int kSchedSlots = 4;
-constexpr int kSchedBytes = 128;   // kSchedSlots x (full, empty) mbarriers + slot values
-
-// ----------------------------------------------------------------------------
 // CTA-pair variant for the dense PFFN (uniform groups): a cluster of 2 CTAs
 // on two SMs computes a 256 x BN tile with tcgen05.mma.cta_group::2.  CTA r
 // of the pair loads A rows [128 r, 128 r + 128) of the tile and B rows
@@ -534,9 +511,8 @@ struct Cfg2 {
     static constexpr int TMEM_COLS = 2 * BN;
     static constexpr int BAR_BYTES = 256;
     static constexpr int EPI_BYTES = EPW * 2 * 2048;
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES + kSchedBytes;
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES;
     static constexpr int COLS_PER_WARP = BN / (EPW / 4);   // EPW / 4 warps share a TMEM lane quadrant
-    static constexpr int SCHED_READERS = 2 + 2 * EPW;       // MMA warp, odd producer, both CTAs' epilogue warps
     static_assert(EPW == 8 || EPW == 16, "epilogue warps");
     static_assert(KSUB == 1 || KSUB == 2, "k-blocks per stage");
     static_assert(COLS_PER_WARP % 32 == 0, "whole 32-column chunks per warp");
@@ -544,7 +520,6 @@ struct Cfg2 {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "pair MMA N");
     static_assert(2 * STAGES * 8 + 4 * 8 + 8 <= BAR_BYTES, "barrier area");
-    static_assert(kSchedSlots * (8 + 8 + 4) <= kSchedBytes, "scheduler area");
 };
 
 template <int BN, int EPI, int EPW, int KSUB>
@@ -567,17 +542,12 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     uint32_t* tmem_holder =
         reinterpret_cast<uint32_t*>(base_ptr + C::STAGES * C::STAGE_BYTES + C::EPI_BYTES + 8 * (2 * C::STAGES + 4));
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-    const uint32_t sched0 = bar0 + C::BAR_BYTES;
-    auto sfull_bar = [&](int q) { return sched0 + 8u * q; };
-    auto sempty_bar = [&](int q) { return sched0 + 8u * (kSchedSlots + q); };
-    auto sval = [&](int q) { return sched0 + 16u * kSchedSlots + 4u * q; };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();          // 0: issues the pair MMAs
     const long long pair = blockIdx.x >> 1;
     const long long npairs = gridDim.x >> 1;
-    const bool dyn = args.sched != nullptr;
 
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
@@ -589,10 +559,6 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
             mbar_init(tempty_bar(a), 2 * EPW);
-        }
-        for (int q = 0; q < kSchedSlots; ++q) {
-            mbar_init(sfull_bar(q), 1);
-            mbar_init(sempty_bar(q), C::SCHED_READERS);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -611,62 +577,13 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     const long long tiles =
         args.tile_prefix ? (long long)__ldg(args.tile_prefix + args.ngroups) * args.n_tiles : args.tiles;
 
-    // Tile sequence of one role.  Static: pair, pair + npairs, ...  Dynamic: the
-    // even CTA's producer draws (draw = true, whole warp), every other role reads
-    // the ring (whole warp; lane 0 then releases the slot).  Returns -1 at the end
-    // (and on a timeout, with the abort flag set).
-    int sq = 0;
-    uint32_t sphase = 0;
-    long long st_next = pair;
-    auto next_tile = [&](bool draw) -> long long {
-        if (!dyn) {
-            const long long t = st_next;
-            st_next += npairs;
-            return t < tiles ? t : -1;
-        }
-        long long t;
-        if (draw) {
-            if (!mbar_wait_bounded(sempty_bar(sq), sphase ^ 1u, abort_flag, args.err, args.timeout_ns)) return -1;
-            int idx = 0;
-            if (lane == 0) idx = atomicAdd(args.sched, 1);
-            idx = __shfl_sync(0xffffffffu, idx, 0);
-            t = idx < tiles ? idx : -1;
-            if (lane == 0) {
-                st_shared_cluster_u32(mapa_shared(sval(sq), 0), (uint32_t)(int)t);
-                st_shared_cluster_u32(mapa_shared(sval(sq), 1), (uint32_t)(int)t);
-                mbar_arrive_cluster(mapa_shared(sfull_bar(sq), 0));
-                mbar_arrive_cluster(mapa_shared(sfull_bar(sq), 1));
-                if (t < 0) {
-                    // this pair has drawn its last index; the last pair to get here
-                    // puts the counter back for the next launch
-                    __threadfence();
-                    if (atomicAdd(args.sched + 1, 1) == (int)npairs - 1) {
-                        atomicExch(args.sched, 0);
-                        atomicExch(args.sched + 1, 0);
-                    }
-                }
-            }
-            __syncwarp();
-        } else {
-            if (!mbar_wait_bounded_cluster(sfull_bar(sq), sphase, abort_flag, args.err, args.timeout_ns)) return -1;
-            t = ld_shared_s32(sval(sq));
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa_shared(sempty_bar(sq), 0));
-        }
-        if (++sq == kSchedSlots) {
-            sq = 0;
-            sphase ^= 1u;
-        }
-        return t;
-    };
-
     if (warp == 0) {
         // ---------------------------- TMA producer (both CTAs) ----------------------------
         {
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (long long tile = next_tile(rank == 0); ok && tile >= 0; tile = next_tile(rank == 0)) {
+            for (long long tile = pair; ok && tile < tiles; tile += npairs) {
                 const TileCoord tc = decode_tile(tile, args);
                 const int arow = args.tile_prefix ? (int)(tc.row0 + (long long)tc.mb * BM2 + 128 * (int)rank)
                                                   : tc.mb * BM2 + 128 * (int)rank;
@@ -704,7 +621,7 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (long long tile = next_tile(false); ok && tile >= 0; tile = next_tile(false)) {
+            for (long long tile = pair; ok && tile < tiles; tile += npairs) {
                 if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.err, args.timeout_ns)) {
                     ok = false;
                     break;
@@ -752,7 +669,7 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         int sbuf = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (long long tile = next_tile(false); tile >= 0; tile = next_tile(false)) {
+        for (long long tile = pair; tile < tiles; tile += npairs) {
             const TileCoord tc = decode_tile(tile, args);
             // every lane waits (the warp stays converged for tcgen05.ld)
             if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err, args.timeout_ns)) break;
@@ -923,7 +840,6 @@ cudaError_t run_pair(const void* A, long long a_rows_total, const void* W, int n
     } else {                               // variable groups: a.tile_prefix counts 256-row tiles,
         a.tiles = 0;                       // the kernel reads the total; persistent grid
         a.hid_tma = 0;
-        a.sched = nullptr;
     }
     CUtensorMap mA, mB, mC;
     const bool a_uniform = a.tile_prefix == nullptr;
@@ -977,18 +893,6 @@ bool use_pair(int M, int epi) {
     }
     if (M < BM2 || env == 0) return false;
     return env == 1 || epi == EPI_RESID;
-}
-
-// Tile order of the pair kernel: dynamic (a global counter, see the kernel) by
-// default; RM_GEMM_SCHED=static in the environment selects the static round
-// robin (a tuning and diagnosis switch; the same result either way).
-bool dynamic_sched() {
-    static int env = -1;
-    if (env < 0) {
-        const char* v = getenv("RM_GEMM_SCHED");
-        env = (v && v[0] == 's') ? 0 : 1;
-    }
-    return env == 1;
 }
 
 // Two 64-deep k-blocks per pipeline stage (when K allows): half the barrier
@@ -1068,11 +972,9 @@ const char* tc_last_error() {
 }
 
 cudaError_t launch_gemm1_tc(const void* S, const void* W1p, const float* b1, void* Hid, int B, int T, int D, int F,
-                            int Bcap, int num_sms, int* sched, int* err, unsigned long long timeout_ns,
-                            cudaStream_t s) {
+                            int Bcap, int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     tc::Args a{};
-    a.sched = tc::dynamic_sched() ? sched : nullptr;
     a.N = F;
     a.K = D;
     a.ngroups = T;
@@ -1089,13 +991,12 @@ cudaError_t launch_gemm1_tc(const void* S, const void* W1p, const float* b1, voi
 }
 
 cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, const void* S, void* Z,
-                            float2* stats, int B, int T, int D, int F, int Bcap, int num_sms, int* sched, int* err,
+                            float2* stats, int B, int T, int D, int F, int Bcap, int num_sms, int* err,
                             unsigned long long timeout_ns, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     const int bn = tc::pick_bn(D);
     if (bn == 0) return cudaErrorNotSupported;
     tc::Args a{};
-    a.sched = tc::dynamic_sched() ? sched : nullptr;
     a.N = D;
     a.K = F;
     a.ngroups = T;

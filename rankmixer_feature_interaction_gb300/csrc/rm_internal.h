@@ -116,18 +116,13 @@ cudaError_t launch_gemm1_simt(Act act, const void* S, const void* W1p, const flo
 cudaError_t launch_gemm2_simt(Act act, const void* Hid, const void* W2p, const float* b2, const void* S, void* Z,
                               int B, int T, int D, int F, int Bcap, cudaStream_t s);
 
-// tcgen05 path (fp16 operands; BF16 contexts only).  sched: two device ints,
-// zero, owned by the caller for this launch kind (the CTA-pair kernel's dynamic
-// tile counter; it leaves them zero when it completes, and rm_sync_status zeroes
-// them after a device error); nullptr gives the static tile order.
+// tcgen05 path (fp16 operands; BF16 contexts only).
 bool tc_supported(int D, int F);
 int tc_stats_chunk_width(int D);   // chunk width of the LN2 partial statistics written by GEMM2
-constexpr int kSchedWords = 2;     // ints per launch kind
 cudaError_t launch_gemm1_tc(const void* S, const void* W1p, const float* b1, void* Hid, int B, int T, int D, int F,
-                            int Bcap, int num_sms, int* sched, int* err, unsigned long long timeout_ns,
-                            cudaStream_t s);
+                            int Bcap, int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s);
 cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, const void* S, void* Z,
-                            float2* stats, int B, int T, int D, int F, int Bcap, int num_sms, int* sched, int* err,
+                            float2* stats, int B, int T, int D, int F, int Bcap, int num_sms, int* err,
                             unsigned long long timeout_ns, cudaStream_t s);
 
 // Set by the tensor-map encoder when the driver call fails (host-side message).

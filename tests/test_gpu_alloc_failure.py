@@ -141,8 +141,14 @@ def _lazy_calls(layers):
         return [m.stack_forward(X)]
 
     def moe_train(m):
-        out = m.moe_pffn_forward_train(0, X)
-        return [out["V"], out["G_infer"], out["lreg"]]
+        # without a gates_infer buffer the call keeps the inference-router gates in a
+        # context-owned buffer, allocated at the first such call
+        V = torch.empty((B, T, D), dtype=torch.float32, device=DEV)
+        lreg = torch.empty(B, dtype=torch.float32, device=DEV)
+        A = torch.empty(E, dtype=torch.float32, device=DEV)
+        _lib.rm_moe_pffn_forward_train(m.ctx, 0, X.data_ptr(), V.data_ptr(), None, None, lreg.data_ptr(),
+                                       A.data_ptr(), B, torch.cuda.current_stream().cuda_stream)
+        return [V, lreg, A]
 
     def set_tok(m):
         m.set_tokenizer(Wt, bt)

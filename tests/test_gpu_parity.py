@@ -487,7 +487,6 @@ print("ok")
 
 
 @pytest.mark.parametrize("tuning", [{},                                            # pairs, 2 k-blocks per stage
-                                    {"RM_GEMM_SCHED": "static"},                    # pairs, static tile order
                                     {"RM_GEMM_PAIR": "0"},                          # one CTA per tile
                                     {"RM_GEMM_PAIR": "2"},                          # pairs for GEMM2 only
                                     {"RM_GEMM_KSUB": "1"},                          # one k-block per stage
@@ -500,7 +499,7 @@ def test_every_gemm_tile_dispatch(tuning, shape):
     import sys
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     env = {k: v for k, v in os.environ.items()
-           if k not in ("RM_GEMM_PAIR", "RM_GEMM_KSUB", "RM_GEMM1_EPW", "RM_GEMM_SCHED")}
+           if k not in ("RM_GEMM_PAIR", "RM_GEMM_KSUB", "RM_GEMM1_EPW")}
     env.update(tuning)
     r = subprocess.run([sys.executable, "-c", _DISPATCH_CHILD.format(root=root, shape=shape)], env=env, cwd=root,
                        capture_output=True, text=True, timeout=600)
