@@ -964,7 +964,21 @@ bool tc_supported(int D, int F) {
     return D % tc::BK == 0 && F % tc::BK == 0 && tc::pick_bn(F) != 0 && tc::pick_bn(D) != 0;
 }
 
-int tc_stats_chunk_width(int D) { return tc::pick_bn(D) / 2; }
+// Tile width of the second GEMM (N = D): the widest of 256, 128, 64 dividing D;
+// RM_GEMM2_BN=128|64 in the environment narrows it (a tuning switch; the
+// statistics chunks follow the tile, so every choice gives the same rows).
+int gemm2_bn(int D) {
+    static int env = -1;
+    if (env < 0) {
+        const char* v = getenv("RM_GEMM2_BN");
+        env = v ? atoi(v) : 0;
+    }
+    const int bn = tc::pick_bn(D);
+    if ((env == 128 || env == 64) && env < bn && D % env == 0) return env;
+    return bn;
+}
+
+int tc_stats_chunk_width(int D) { return gemm2_bn(D) / 2; }
 
 const char* tc_last_error() {
     std::lock_guard<std::mutex> lk(tc::g_mu);
@@ -994,7 +1008,7 @@ cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, c
                             float2* stats, int B, int T, int D, int F, int Bcap, int num_sms, int* err,
                             unsigned long long timeout_ns, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
-    const int bn = tc::pick_bn(D);
+    const int bn = gemm2_bn(D);
     if (bn == 0) return cudaErrorNotSupported;
     tc::Args a{};
     a.N = D;

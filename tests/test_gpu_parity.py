@@ -488,6 +488,8 @@ print("ok")
 
 @pytest.mark.parametrize("tuning", [{},                                            # pairs, 2 k-blocks per stage
                                     {"RM_GEMM_PAIR": "0"},                          # one CTA per tile
+                                    {"RM_GEMM2_BN": "128"},                         # narrower second-GEMM tiles
+                                    {"RM_GEMM_SMALL_BN": "128"},                    # narrower one-CTA tiles
                                     {"RM_GEMM_PAIR": "2"},                          # pairs for GEMM2 only
                                     {"RM_GEMM_KSUB": "1"},                          # one k-block per stage
                                     {"RM_GEMM1_EPW": "16"},                         # 16 GELU epilogue warps
@@ -499,7 +501,7 @@ def test_every_gemm_tile_dispatch(tuning, shape):
     import sys
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     env = {k: v for k, v in os.environ.items()
-           if k not in ("RM_GEMM_PAIR", "RM_GEMM_KSUB", "RM_GEMM1_EPW")}
+           if k not in ("RM_GEMM_PAIR", "RM_GEMM_KSUB", "RM_GEMM1_EPW", "RM_GEMM2_BN", "RM_GEMM_SMALL_BN")}
     env.update(tuning)
     r = subprocess.run([sys.executable, "-c", _DISPATCH_CHILD.format(root=root, shape=shape)], env=env, cwd=root,
                        capture_output=True, text=True, timeout=600)
