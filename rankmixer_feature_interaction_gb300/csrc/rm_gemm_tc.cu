@@ -636,42 +636,51 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     const long long tiles =
         args.tile_prefix ? (long long)__ldg(args.tile_prefix + args.ngroups) * args.n_tiles : args.tiles;
 
-    // Work items of this pair.  Static order: whole tiles pair, pair + npairs, ...
-    // Stream-K (args.sk): the tiles x kblocks k-steps are cut into npairs equal
-    // contiguous ranges, pair p taking steps [W p / P, W (p + 1) / P); a range
-    // is walked as items (tile, kb0, kb1).  An item that starts a tile (kb0 = 0)
-    // but ends before its last k-step is the tile's owner: it adds the partial
-    // accumulators of the pairs that hold the rest of the tile (whose ranges
-    // begin inside it, so each of them has it as its first item), in pair order,
-    // then runs the epilogue.  An item with kb0 > 0 is such a partial: its
-    // accumulator goes to the pair's slot and the pair's flag is set to the
-    // launch's epoch.  A pair's partial is the first thing it computes and the
-    // owner's item is the last thing its owner computes, so the owner rarely
-    // waits.  Every role walks the same items.
-    const long long W = tiles * (long long)kblocks;
-    const long long sk_begin = args.sk ? W * pair / npairs : 0;
-    const long long sk_end = args.sk ? W * (pair + 1) / npairs : 0;
+    // Work items of this pair.  Whole tiles in the static order pair, pair +
+    // npairs, ... (neighbouring pairs on neighbouring tiles, which share operand
+    // tiles in L2) for the first dp_tiles = dp_rounds x npairs tiles; with
+    // stream-K (args.sk) the remaining tiles -- the last full round and the
+    // partial one -- are cut along k: their tiles x kblocks k-steps form npairs
+    // equal contiguous ranges, pair p taking steps [W p / P, W (p + 1) / P) of
+    // that region, walked as items (tile, kb0, kb1).  An item that starts a tile
+    // (kb0 = 0) but ends before its last k-step is the tile's owner: it adds the
+    // partial accumulators of the pairs that hold the rest of the tile (whose
+    // ranges begin inside it, so each of them has it as its first stream-K
+    // item), in pair order, then runs the epilogue.  An item with kb0 > 0 is such
+    // a partial: its accumulator goes to the pair's slot and the pair's flag is
+    // set to the launch's epoch.  A pair's partial is the first thing it computes
+    // in the stream-K region and the owner's item the last thing its owner
+    // computes, so the owner rarely waits.  Every role walks the same items.
+    const long long full_rounds = tiles / npairs;
+    const long long dp_rounds = args.sk ? (full_rounds > 0 ? full_rounds - 1 : 0) : (tiles + npairs - 1) / npairs;
+    const long long dp_tiles = dp_rounds * npairs;
+    const long long W = args.sk ? (tiles - dp_tiles) * (long long)kblocks : 0;     // stream-K k-steps
+    const long long sk_begin = W * pair / npairs;
+    const long long sk_end = W * (pair + 1) / npairs;
     struct Item {
         long long tile;
         int kb0, kb1;
     };
-    auto first_unit = [&]() -> long long { return args.sk ? sk_begin : pair; };
-    // advance: u is the next k-step (stream-K) or the next tile (static)
+    // u < dp_rounds: the u-th whole tile of this pair; then the stream-K k-step
+    // (dp_rounds + sk_begin + i) - dp_rounds
+    auto first_unit = [&]() -> long long { return 0; };
     auto next_item = [&](long long& u, Item& it) -> bool {
-        if (args.sk) {
-            if (u >= sk_end) return false;
-            it.tile = u / kblocks;
-            it.kb0 = (int)(u - it.tile * kblocks);
-            const long long left = sk_end - u;
-            it.kb1 = left < (long long)(kblocks - it.kb0) ? it.kb0 + (int)left : kblocks;
-            u += it.kb1 - it.kb0;
+        if (u < dp_rounds) {
+            it.tile = pair + u * npairs;
+            ++u;
+            if (it.tile >= tiles) return false;      // static order: past the last tile
+            it.kb0 = 0;
+            it.kb1 = kblocks;
             return true;
         }
-        if (u >= tiles) return false;
-        it.tile = u;
-        it.kb0 = 0;
-        it.kb1 = kblocks;
-        u += npairs;
+        const long long step = sk_begin + (u - dp_rounds);
+        if (step >= sk_end) return false;
+        const long long t = step / kblocks;
+        it.tile = dp_tiles + t;
+        it.kb0 = (int)(step - t * kblocks);
+        const long long left = sk_end - step;
+        it.kb1 = left < (long long)(kblocks - it.kb0) ? it.kb0 + (int)left : kblocks;
+        u += it.kb1 - it.kb0;
         return true;
     };
 
@@ -798,7 +807,7 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                 PartIn pin{nullptr, 0, 0};
                 if (it.kb1 < kblocks) {
                     // owner: the partners are the pairs whose ranges begin inside this tile
-                    const long long tile_end = (it.tile + 1) * (long long)kblocks;
+                    const long long tile_end = (it.tile - dp_tiles + 1) * (long long)kblocks;
                     int n = 0;
                     for (long long q = pair + 1; q < npairs && W * q / npairs < tile_end; ++q) {
                         // wait until partner q has published this launch's partial (bounded)

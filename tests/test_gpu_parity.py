@@ -194,9 +194,10 @@ def test_deterministic_reruns():
 @pytest.mark.parametrize("B", [100, 2500])      # one shot; three pipelined chunks (512, 1024, 964)
 def test_host_entry_matches_device_entry(B):
     """The host entry runs large batches as chunks.  Each chunk is its own launch, whose
-    tensor-core GEMMs may cut their k-loops at other points (stream-K) than the whole
-    batch's, so the results agree to float32 rounding of the k-sums; two calls of the same
-    batch agree bit for bit."""
+    tensor-core GEMMs may cut their last k-loops at other points (stream-K) than the
+    whole batch's; a different float32 sum can round an fp16 intermediate the other way,
+    so the chunked and whole results are each held to the oracle (and to each other at
+    the same bar), while two calls of the same batch agree bit for bit."""
     T, D, k, L = 8, 512, 4, 2
     m, layers, X = _build(T, D, k, L, B, 23, "bf16")
     dev = m.stack_forward(X)
@@ -205,9 +206,12 @@ def test_host_entry_matches_device_entry(B):
     host2 = m.stack_forward_host(Xh)          # a second call reuses the staging buffers
     torch.cuda.synchronize()
     assert torch.equal(host, host2)
-    check(host, _np(dev), "bf16", f"host entry vs device entry B={B}", tol=1e-3)
-    idx = np.array([0, B // 2, B - 1])
-    check(host[idx], oracle.stack_forward(_np(X[idx]), synth.to_f64(layers)), "bf16", f"host entry B={B}")
+    check(host, _np(dev), "bf16", f"host entry vs device entry B={B}")
+    rng = np.random.default_rng(B)
+    idx = np.unique(np.concatenate([[0, B - 1], rng.choice(B, size=min(24, B), replace=False)]))
+    ref = oracle.stack_forward(_np(X[idx]), synth.to_f64(layers))
+    check(host[idx], ref, "bf16", f"host entry B={B}")
+    check(dev.cpu()[idx], ref, "bf16", f"device entry B={B}")
 
 
 # ----------------------------------------------------------------------------
