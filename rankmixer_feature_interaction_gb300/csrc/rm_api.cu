@@ -213,8 +213,6 @@ struct rm_ctx {
     float* pooled_dev = nullptr;
     cudaStream_t s_in = nullptr, s_out = nullptr;
     cudaEvent_t ev_in[kHostChunksMax] = {}, ev_done[kHostChunksMax] = {};
-    // stream-K workspace of the CTA-pair GEMMs (tensor-core contexts)
-    SkWorkspace sk;
     // error word and the debug flag nothing sets
     int* d_err = nullptr;
     int* d_flag = nullptr;
@@ -286,7 +284,6 @@ void free_ctx(rm_ctx* c) {
     if (c->s_in) cudaStreamDestroy(c->s_in);
     if (c->s_out) cudaStreamDestroy(c->s_out);
     device_free(c->d_err); device_free(c->d_flag);
-    device_free(c->sk.part); device_free(c->sk.flag);
     for (auto& e : c->ev_pool) { cudaEventDestroy(e.a); cudaEventDestroy(e.b); }
     delete c;
 }
@@ -387,13 +384,13 @@ rm_status run_pffn(rm_ctx* c, int layer, int B, cudaStream_t s) {
         {
             ProfScope ps(c, RM_K_GEMM1, s);
             cudaError_t e = launch_gemm1_tc(c->S, w.W1p, w.b1, c->Hid, B, g.T, g.D, c->F, c->Bcap, c->num_sms,
-                                            &c->sk, c->d_err, kWaitTimeoutNs, s);
+                                            c->d_err, kWaitTimeoutNs, s);
             if (e != cudaSuccess) return cuda_fail(e, (std::string("gemm1 (tcgen05) ") + tc_last_error()).c_str());
         }
         {
             ProfScope ps(c, RM_K_GEMM2, s);
             cudaError_t e = launch_gemm2_tc(c->Hid, w.W2p, w.b2, c->S, c->Z, c->stats, B, g.T, g.D, c->F, c->Bcap,
-                                            c->num_sms, &c->sk, c->d_err, kWaitTimeoutNs, s);
+                                            c->num_sms, c->d_err, kWaitTimeoutNs, s);
             if (e != cudaSuccess) return cuda_fail(e, (std::string("gemm2 (tcgen05) ") + tc_last_error()).c_str());
         }
         ProfScope ps(c, RM_K_ROWSTATS, s);
@@ -934,16 +931,6 @@ rm_status rm_create(const rm_config* cfg, const rm_layer_params* layers, int dev
         (st = dmalloc(c, (void**)&c->V, T * Bc * D * 4, &c->ws_bytes)) != RM_OK) {
         free_ctx(c);
         return st;
-    }
-    if (c->use_tc) {
-        // one pair per two SMs at most (a pair CTA takes a whole SM)
-        c->sk.max_pairs = c->num_sms / 2;
-        if ((st = dmalloc(c, (void**)&c->sk.part, sk_part_bytes(c->sk.max_pairs), &c->ws_bytes)) != RM_OK ||
-            (st = dmalloc(c, (void**)&c->sk.flag, sk_flag_bytes(c->sk.max_pairs), &c->ws_bytes)) != RM_OK) {
-            free_ctx(c);
-            return st;
-        }
-        cudaMemset(c->sk.flag, 0, sk_flag_bytes(c->sk.max_pairs));
     }
     if (cfg->n_experts > 0) {
         MoeShape ms{c->act, cfg->T, cfg->D, cfg->n_experts, cfg->expert_hidden};
@@ -1757,11 +1744,10 @@ rm_status rm_block_forward_noalloc(rm_ctx* c, int layer, const void* X_in, void*
     a.Bcap = B;
     RM_CHECK_CUDA(launch_mix_ln1(c->act, false, a, c->num_sms, s), "mix+ln1");
     if (c->use_tc) {
-        // no stream-K workspace here: whole tiles in the static order
-        cudaError_t e = launch_gemm1_tc(S, w.W1p, w.b1, Hid, B, g.T, g.D, c->F, B, c->num_sms, nullptr, c->d_err,
+        cudaError_t e = launch_gemm1_tc(S, w.W1p, w.b1, Hid, B, g.T, g.D, c->F, B, c->num_sms, c->d_err,
                                         kWaitTimeoutNs, s);
         if (e != cudaSuccess) return cuda_fail(e, (std::string("gemm1 (tcgen05) ") + tc_last_error()).c_str());
-        e = launch_gemm2_tc(Hid, w.W2p, w.b2, S, Z, stats, B, g.T, g.D, c->F, B, c->num_sms, nullptr, c->d_err,
+        e = launch_gemm2_tc(Hid, w.W2p, w.b2, S, Z, stats, B, g.T, g.D, c->F, B, c->num_sms, c->d_err,
                             kWaitTimeoutNs, s);
         if (e != cudaSuccess) return cuda_fail(e, (std::string("gemm2 (tcgen05) ") + tc_last_error()).c_str());
         RM_CHECK_CUDA(launch_stats_finalize(stats, rows, B, g.T, B, c->nchunk, c->cw, c->num_sms, s),

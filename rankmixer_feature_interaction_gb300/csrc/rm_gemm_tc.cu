@@ -88,47 +88,9 @@ struct Args {
     float2* stats;            // EPI_RESID row partials [row][nchunk]
     int nchunk;
     const float* row_gate;    // EPI_GATED: gate of each packed row (same row index as A)
-    // CTA-pair kernel, uniform groups: stream-K split of the k-loop (sk != 0).
-    // sk_part: one slot of kSkSlotFloats floats per (pair, CTA) for a partial
-    // accumulator; sk_flag: one int per (pair, CTA), set to sk_epoch when its
-    // slot holds this launch's partial.
-    int sk;
-    float* sk_part;
-    int* sk_flag;
-    unsigned sk_epoch;
     int* err;
     unsigned long long timeout_ns;
 };
-
-// Stream-K slot: the 128 rows x (at most) 256 fp32 accumulator columns of one CTA.
-constexpr long long kSkSlotFloats = 128 * 256;
-
-// Partial accumulators of a stream-K owner item, added to the warp's TMEM
-// values chunk by chunk: n partners, the first partner's slot at p (already
-// offset to this warp's part), the next ones stride floats further.
-struct PartIn {
-    const float* p;
-    long long stride;
-    int n;
-};
-
-// Index of (chunk c, float4 j) of a warp's slot part for this lane: 32 lanes
-// write 32 consecutive float4 (one 512-byte line per instruction).
-__device__ __forceinline__ long long sk_idx(int c, int j, int lane) { return ((long long)(c * 8 + j) * 32 + lane) * 4; }
-
-__device__ __forceinline__ void add_parts(float (&v)[32], const PartIn& pin, int c, int lane) {
-    for (int q = 0; q < pin.n; ++q) {
-        const float* src = pin.p + q * pin.stride;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float4 w = __ldcg(reinterpret_cast<const float4*>(src + sk_idx(c, j, lane)));
-            v[4 * j] += w.x;
-            v[4 * j + 1] += w.y;
-            v[4 * j + 2] += w.z;
-            v[4 * j + 3] += w.w;
-        }
-    }
-}
 
 // v[0..31] += 32 consecutive fp16 values at p (64-byte aligned).
 __device__ __forceinline__ void add_f16x32(float (&v)[32], const __half* p) {
@@ -198,7 +160,7 @@ __device__ __forceinline__ TileCoord decode_tile(long long tile, const Args& a) 
 template <int COLS, bool PREFETCH>
 __device__ __forceinline__ void epilogue_gelu_tma(const Args& args, const TileCoord& tc, const CUtensorMap* tmC,
                                                   uint32_t tbase, int n0, int m_warp, uint32_t stage, int lane,
-                                                  int& sbuf, const PartIn& pin) {
+                                                  int& sbuf) {
     constexpr int NC = COLS / 32;
     const float* bias = args.bias + (size_t)tc.wg * args.N + n0;
     const bool any_valid = m_warp < tc.Mg;
@@ -217,17 +179,16 @@ __device__ __forceinline__ void epilogue_gelu_tma(const Args& args, const TileCo
             tmem_ld32_nowait(tbase + 32u * c, r[0]);
             tmem_wait_ld();
         }
-        float v[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[c % (PREFETCH ? 2 : 1)][i]);
-        if (pin.n) add_parts(v, pin, c, lane);
+        const uint32_t* v = r[c % (PREFETCH ? 2 : 1)];
         uint32_t p[16];
         const float4* b4 = reinterpret_cast<const float4*>(bias + 32 * c);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const float4 bb = __ldg(b4 + j);
-            p[2 * j] = pack_f16x2_from_f2(gelu_erf_x2(f2_pack(v[4 * j], v[4 * j + 1]), f2_pack(bb.x, bb.y)));
-            p[2 * j + 1] = pack_f16x2_from_f2(gelu_erf_x2(f2_pack(v[4 * j + 2], v[4 * j + 3]), f2_pack(bb.z, bb.w)));
+            p[2 * j] = pack_f16x2_from_f2(gelu_erf_x2(f2_pack(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1])),
+                                                      f2_pack(bb.x, bb.y)));
+            p[2 * j + 1] = pack_f16x2_from_f2(
+                gelu_erf_x2(f2_pack(__uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])), f2_pack(bb.z, bb.w)));
         }
         if (lane == 0) bulk_wait_group_read<1>();
         __syncwarp();
@@ -253,7 +214,7 @@ __device__ __forceinline__ void epilogue_gelu_tma(const Args& args, const TileCo
 // loads; only rows inside the group (valid) are stored.
 template <int COLS, int EPI>
 __device__ __forceinline__ void epilogue_tile(const Args& args, const TileCoord& tc, bool valid, long long arow,
-                                              uint32_t tbase, int n0, const PartIn& pin, int lane) {
+                                              uint32_t tbase, int n0) {
     const size_t orow = (size_t)arow * (size_t)args.N + n0;
     const float* bias = args.bias + (size_t)tc.wg * args.N + n0;
     if (EPI == EPI_GELU) {
@@ -261,7 +222,6 @@ __device__ __forceinline__ void epilogue_tile(const Args& args, const TileCoord&
         for (int c = 0; c < (COLS / 32); ++c) {
             float v[32];
             tmem_ld32(tbase + 32u * c, v);
-            if (pin.n) add_parts(v, pin, c, lane);
             if (valid) {
                 uint32_t p[16];
                 const float4* b4 = reinterpret_cast<const float4*>(bias + 32 * c);
@@ -284,7 +244,6 @@ __device__ __forceinline__ void epilogue_tile(const Args& args, const TileCoord&
         for (int c = 0; c < (COLS / 32); ++c) {
             float v[32];
             tmem_ld32(tbase + 32u * c, v);
-            if (pin.n) add_parts(v, pin, c, lane);
             if (valid) {
                 const float4* b4 = reinterpret_cast<const float4*>(bias + 32 * c);
                 add_f16x32(v, args.resid + orow + 32 * c);
@@ -329,7 +288,6 @@ __device__ __forceinline__ void epilogue_tile(const Args& args, const TileCoord&
         for (int c = 0; c < (COLS / 32); ++c) {
             float v[32];
             tmem_ld32(tbase + 32u * c, v);
-            if (pin.n) add_parts(v, pin, c, lane);
             if (valid) {
                 const float4* b4 = reinterpret_cast<const float4*>(bias + 32 * c);
                 uint32_t p[16];
@@ -345,21 +303,6 @@ __device__ __forceinline__ void epilogue_tile(const Args& args, const TileCoord&
                     dst[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
             }
         }
-    }
-}
-
-// Stream-K partial item: this warp's 32 rows x COLS accumulator columns go to
-// its part of the slot, as fp32, in the layout add_parts reads.
-template <int COLS>
-__device__ __forceinline__ void epilogue_store_partial(uint32_t tbase, float* dst, int lane) {
-#pragma unroll 1
-    for (int c = 0; c < COLS / 32; ++c) {
-        float v[32];
-        tmem_ld32(tbase + 32u * c, v);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            __stcg(reinterpret_cast<float4*>(dst + sk_idx(c, j, lane)),
-                   make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
     }
 }
 
@@ -514,12 +457,10 @@ pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const uint32_t tbase =
                 tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN + half * C::COLS_PER_WARP);
             const int n0 = tc.nb * BN + half * C::COLS_PER_WARP;
-            const PartIn none{nullptr, 0, 0};
             if (EPI == EPI_GELU && args.hid_tma)
-                epilogue_gelu_tma<C::COLS_PER_WARP, true>(args, tc, &tmC, tbase, n0, m - lane, stage, lane, sbuf,
-                                                          none);
+                epilogue_gelu_tma<C::COLS_PER_WARP, true>(args, tc, &tmC, tbase, n0, m - lane, stage, lane, sbuf);
             else
-                epilogue_tile<C::COLS_PER_WARP, EPI>(args, tc, valid, arow, tbase, n0, none, lane);
+                epilogue_tile<C::COLS_PER_WARP, EPI>(args, tc, valid, arow, tbase, n0);
             tc_fence_before();
             mbar_arrive(tempty_bar(acc));
             acc ^= 1;
@@ -636,69 +577,19 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     const long long tiles =
         args.tile_prefix ? (long long)__ldg(args.tile_prefix + args.ngroups) * args.n_tiles : args.tiles;
 
-    // Work items of this pair.  Whole tiles in the static order pair, pair +
-    // npairs, ... (neighbouring pairs on neighbouring tiles, which share operand
-    // tiles in L2) for the first dp_tiles = dp_rounds x npairs tiles; with
-    // stream-K (args.sk) the remaining tiles -- the last full round and the
-    // partial one -- are cut along k: their tiles x kblocks k-steps form npairs
-    // equal contiguous ranges, pair p taking steps [W p / P, W (p + 1) / P) of
-    // that region, walked as items (tile, kb0, kb1).  An item that starts a tile
-    // (kb0 = 0) but ends before its last k-step is the tile's owner: it adds the
-    // partial accumulators of the pairs that hold the rest of the tile (whose
-    // ranges begin inside it, so each of them has it as its first stream-K
-    // item), in pair order, then runs the epilogue.  An item with kb0 > 0 is such
-    // a partial: its accumulator goes to the pair's slot and the pair's flag is
-    // set to the launch's epoch.  A pair's partial is the first thing it computes
-    // in the stream-K region and the owner's item the last thing its owner
-    // computes, so the owner rarely waits.  Every role walks the same items.
-    const long long full_rounds = tiles / npairs;
-    const long long dp_rounds = args.sk ? (full_rounds > 0 ? full_rounds - 1 : 0) : (tiles + npairs - 1) / npairs;
-    const long long dp_tiles = dp_rounds * npairs;
-    const long long W = args.sk ? (tiles - dp_tiles) * (long long)kblocks : 0;     // stream-K k-steps
-    const long long sk_begin = W * pair / npairs;
-    const long long sk_end = W * (pair + 1) / npairs;
-    struct Item {
-        long long tile;
-        int kb0, kb1;
-    };
-    // u < dp_rounds: the u-th whole tile of this pair; then the stream-K k-step
-    // (dp_rounds + sk_begin + i) - dp_rounds
-    auto first_unit = [&]() -> long long { return 0; };
-    auto next_item = [&](long long& u, Item& it) -> bool {
-        if (u < dp_rounds) {
-            it.tile = pair + u * npairs;
-            ++u;
-            if (it.tile >= tiles) return false;      // static order: past the last tile
-            it.kb0 = 0;
-            it.kb1 = kblocks;
-            return true;
-        }
-        const long long step = sk_begin + (u - dp_rounds);
-        if (step >= sk_end) return false;
-        const long long t = step / kblocks;
-        it.tile = dp_tiles + t;
-        it.kb0 = (int)(step - t * kblocks);
-        const long long left = sk_end - step;
-        it.kb1 = left < (long long)(kblocks - it.kb0) ? it.kb0 + (int)left : kblocks;
-        u += it.kb1 - it.kb0;
-        return true;
-    };
-
     if (warp == 0) {
         // ---------------------------- TMA producer (both CTAs) ----------------------------
         {
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            long long u = first_unit();
-            Item it;
-            while (ok && next_item(u, it)) {
-                const TileCoord tc = decode_tile(it.tile, args);
+            for (long long tile = pair; ok && tile < tiles; tile += npairs) {
+                const TileCoord tc = decode_tile(tile, args);
                 const int arow = args.tile_prefix ? (int)(tc.row0 + (long long)tc.mb * BM2 + 128 * (int)rank)
                                                   : tc.mb * BM2 + 128 * (int)rank;
                 const int agrp = args.tile_prefix ? 0 : tc.j;
                 const int brow = tc.nb * BN + (BN / 2) * (int)rank;
-                for (int kb = it.kb0; kb < it.kb1; ++kb) {
+                for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, args.err, args.timeout_ns)) {
                         ok = false;
                         break;
@@ -730,16 +621,14 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            long long u = first_unit();
-            Item it;
-            while (ok && next_item(u, it)) {
+            for (long long tile = pair; ok && tile < tiles; tile += npairs) {
                 if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.err, args.timeout_ns)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
-                for (int kb = it.kb0; kb < it.kb1; ++kb) {
+                for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, args.err, args.timeout_ns)) {
                         ok = false;
                         break;
@@ -754,7 +643,7 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
                             for (int k = 0; k < BK / 16; ++k)
                                 umma_f16_pair(d_tmem, make_sw128_desc(a0 + ks * C::A_SUB + 32u * k),
                                               make_sw128_desc(b0 + ks * C::B_SUB + 32u * k), idesc,
-                                              (kb > it.kb0 || ks > 0 || k > 0) ? 1u : 0u);
+                                              (kb > 0 || ks > 0 || k > 0) ? 1u : 0u);
                         umma_commit_pair_mc(empty_bar(stage), (uint16_t)0x3);
                     }
                     __syncwarp();
@@ -777,71 +666,25 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
         const int half = ew >> 2;               // which COLS_PER_WARP columns of the tile
         const int row_in_tile = quad * 32 + lane;
         const uint32_t stage = sEpi + (uint32_t)ew * 4096u;
-        // this warp's part of a slot: 32 rows x COLS_PER_WARP columns
-        const long long part_off = (long long)ew * 32 * C::COLS_PER_WARP;
         int sbuf = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
-        long long u = first_unit();
-        Item it;
-        bool ok = true;
-        while (ok && next_item(u, it)) {
-            const TileCoord tc = decode_tile(it.tile, args);
+        for (long long tile = pair; tile < tiles; tile += npairs) {
+            const TileCoord tc = decode_tile(tile, args);
             // every lane waits (the warp stays converged for tcgen05.ld)
             if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err, args.timeout_ns)) break;
             tc_fence_after();
+            const int m = tc.mb * BM2 + 128 * (int)rank + row_in_tile;
+            const bool valid = m < tc.Mg;
+            const long long arow = tc.row0 + m;
             const uint32_t tbase =
                 tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN + half * C::COLS_PER_WARP);
-            if (it.kb0 > 0) {
-                // stream-K partial: accumulator to this pair's slot, then (all epilogue
-                // warps of the CTA done) the flag
-                float* dst = args.sk_part + (pair * 2 + rank) * kSkSlotFloats + part_off;
-                epilogue_store_partial<C::COLS_PER_WARP>(tbase, dst, lane);
-                __threadfence();
-                asm volatile("bar.sync 1, %0;" ::"r"(EPW * 32) : "memory");
-                if (ew == 0 && lane == 0)
-                    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(args.sk_flag + pair * 2 + rank),
-                                 "r"(args.sk_epoch)
-                                 : "memory");
-            } else {
-                PartIn pin{nullptr, 0, 0};
-                if (it.kb1 < kblocks) {
-                    // owner: the partners are the pairs whose ranges begin inside this tile
-                    const long long tile_end = (it.tile - dp_tiles + 1) * (long long)kblocks;
-                    int n = 0;
-                    for (long long q = pair + 1; q < npairs && W * q / npairs < tile_end; ++q) {
-                        // wait until partner q has published this launch's partial (bounded)
-                        const int* fl = args.sk_flag + q * 2 + rank;
-                        const uint64_t t0 = globaltimer_ns();
-                        for (uint32_t spin = 0;; ++spin) {
-                            unsigned v;
-                            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(fl) : "memory");
-                            if (v == args.sk_epoch) break;
-                            if ((spin & 63u) == 63u && (*abort_flag || globaltimer_ns() - t0 > args.timeout_ns)) {
-                                *abort_flag = 1;
-                                latch_error(args.err, kDevErrTimeout);
-                                ok = false;
-                                break;
-                            }
-                        }
-                        if (!ok) break;
-                        ++n;
-                    }
-                    pin = PartIn{args.sk_part + ((pair + 1) * 2 + rank) * kSkSlotFloats + part_off,
-                                 2 * kSkSlotFloats, n};
-                }
-                if (ok) {
-                    const int m = tc.mb * BM2 + 128 * (int)rank + row_in_tile;
-                    const bool valid = m < tc.Mg;
-                    const long long arow = tc.row0 + m;
-                    const int n0 = tc.nb * BN + half * C::COLS_PER_WARP;
-                    if (EPI == EPI_GELU && args.hid_tma)
-                        epilogue_gelu_tma<C::COLS_PER_WARP, EPW == 8>(args, tc, &tmC, tbase, n0, m - lane, stage,
-                                                                       lane, sbuf, pin);
-                    else
-                        epilogue_tile<C::COLS_PER_WARP, EPI>(args, tc, valid, arow, tbase, n0, pin, lane);
-                }
-            }
+            const int n0 = tc.nb * BN + half * C::COLS_PER_WARP;
+            if (EPI == EPI_GELU && args.hid_tma)
+                epilogue_gelu_tma<C::COLS_PER_WARP, EPW == 8>(args, tc, &tmC, tbase, n0, m - lane, stage, lane,
+                                                               sbuf);
+            else
+                epilogue_tile<C::COLS_PER_WARP, EPI>(args, tc, valid, arow, tbase, n0);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
@@ -983,27 +826,9 @@ cudaError_t run_bn(int bn, const void* A, long long a_rows_total, const void* W,
 
 // CTA-pair launch for uniform groups (dense PFFN).  Grid = 2 x the number of
 // pairs that can be resident at once (persistent).
-// Stream-K for uniform groups: RM_GEMM_STREAMK=0 never, 1 whenever legal (at
-// least one tile per pair), otherwise when the static order's last round
-// would leave more than kSkAutoLoss of the pair-rounds idle (a tuning switch;
-// results agree up to the fp32 rounding of the split k-sums).
-constexpr double kSkAutoLoss = 0.03;
-
-bool want_stream_k(long long tiles, long long pairs) {
-    static int env = -1;
-    if (env < 0) {
-        const char* v = getenv("RM_GEMM_STREAMK");
-        env = !v ? 2 : (v[0] == '0' ? 0 : (v[0] == '1' ? 1 : 2));
-    }
-    if (env == 0 || pairs < 2 || tiles < pairs) return false;
-    if (env == 1) return true;
-    const long long rounds = (tiles + pairs - 1) / pairs;
-    return (double)(rounds * pairs) / (double)tiles - 1.0 > kSkAutoLoss;
-}
-
 template <int BN, int EPI, int EPW, int KSUB>
 cudaError_t run_pair(const void* A, long long a_rows_total, const void* W, int n_wgroups, Args a, int num_sms,
-                     SkWorkspace* sk, cudaStream_t s) {
+                     cudaStream_t s) {
     using C = Cfg2<BN, EPW, KSUB>;
     if (a.K % (BK * KSUB) != 0) return cudaErrorInvalidValue;
     a.n_tiles = a.N / BN;
@@ -1052,14 +877,6 @@ cudaError_t run_pair(const void* A, long long a_rows_total, const void* W, int n
         max_pairs = n;
     }
     long long pairs = (a.tile_prefix == nullptr && a.tiles < max_pairs) ? a.tiles : max_pairs;
-    a.sk = 0;
-    if (sk && sk->part && a.tile_prefix == nullptr && pairs <= sk->max_pairs && want_stream_k(a.tiles, pairs)) {
-        a.sk = 1;
-        a.sk_part = sk->part;
-        a.sk_flag = sk->flag;
-        if (++sk->epoch == 0) ++sk->epoch;      // 0 is the flags' initial value
-        a.sk_epoch = sk->epoch;
-    }
     k<<<(int)(2 * pairs), C::THREADS, C::SMEM_BYTES, s>>>(mA, mB, mC, a);
     return cudaGetLastError();
 }
@@ -1108,29 +925,29 @@ bool gelu_pair_epw16() {
 
 template <int EPI, int EPW>
 cudaError_t run_pair_bn(int bn, bool k2, const void* A, long long a_rows_total, const void* W, int n_wgroups,
-                        const Args& a, int num_sms, SkWorkspace* sk, cudaStream_t s) {
+                        const Args& a, int num_sms, cudaStream_t s) {
     switch (bn) {
         case 256:
-            return k2 ? run_pair<256, EPI, EPW, 2>(A, a_rows_total, W, n_wgroups, a, num_sms, sk, s)
-                      : run_pair<256, EPI, EPW, 1>(A, a_rows_total, W, n_wgroups, a, num_sms, sk, s);
+            return k2 ? run_pair<256, EPI, EPW, 2>(A, a_rows_total, W, n_wgroups, a, num_sms, s)
+                      : run_pair<256, EPI, EPW, 1>(A, a_rows_total, W, n_wgroups, a, num_sms, s);
         case 128:
-            return k2 ? run_pair<128, EPI, EPW, 2>(A, a_rows_total, W, n_wgroups, a, num_sms, sk, s)
-                      : run_pair<128, EPI, EPW, 1>(A, a_rows_total, W, n_wgroups, a, num_sms, sk, s);
+            return k2 ? run_pair<128, EPI, EPW, 2>(A, a_rows_total, W, n_wgroups, a, num_sms, s)
+                      : run_pair<128, EPI, EPW, 1>(A, a_rows_total, W, n_wgroups, a, num_sms, s);
         case 64:
-            return k2 ? run_pair<64, EPI, 8, 2>(A, a_rows_total, W, n_wgroups, a, num_sms, sk, s)
-                      : run_pair<64, EPI, 8, 1>(A, a_rows_total, W, n_wgroups, a, num_sms, sk, s);
+            return k2 ? run_pair<64, EPI, 8, 2>(A, a_rows_total, W, n_wgroups, a, num_sms, s)
+                      : run_pair<64, EPI, 8, 1>(A, a_rows_total, W, n_wgroups, a, num_sms, s);
         default: return cudaErrorNotSupported;
     }
 }
 
 template <int EPI>
 cudaError_t run_dense(int bn, const void* A, long long a_rows_total, const void* W, int n_wgroups, const Args& a,
-                      int num_sms, SkWorkspace* sk, cudaStream_t s) {
+                      int num_sms, cudaStream_t s) {
     if (use_pair(a.M, EPI)) {
         const bool k2 = use_ksub2(a.K, EPI);
         if (EPI == EPI_GELU && gelu_pair_epw16())
-            return run_pair_bn<EPI, 16>(bn, k2, A, a_rows_total, W, n_wgroups, a, num_sms, sk, s);
-        return run_pair_bn<EPI, 8>(bn, k2, A, a_rows_total, W, n_wgroups, a, num_sms, sk, s);
+            return run_pair_bn<EPI, 16>(bn, k2, A, a_rows_total, W, n_wgroups, a, num_sms, s);
+        return run_pair_bn<EPI, 8>(bn, k2, A, a_rows_total, W, n_wgroups, a, num_sms, s);
     }
     static int small_bn = -1;   // RM_GEMM_SMALL_BN=64|128: narrower one-CTA tiles (a tuning switch)
     if (small_bn < 0) {
@@ -1163,17 +980,13 @@ int gemm2_bn(int D) {
 
 int tc_stats_chunk_width(int D) { return gemm2_bn(D) / 2; }
 
-size_t sk_part_bytes(int max_pairs) { return (size_t)max_pairs * 2 * (size_t)tc::kSkSlotFloats * sizeof(float); }
-size_t sk_flag_bytes(int max_pairs) { return (size_t)max_pairs * 2 * sizeof(int); }
-
 const char* tc_last_error() {
     std::lock_guard<std::mutex> lk(tc::g_mu);
     return tc::g_err.c_str();
 }
 
 cudaError_t launch_gemm1_tc(const void* S, const void* W1p, const float* b1, void* Hid, int B, int T, int D, int F,
-                            int Bcap, int num_sms, SkWorkspace* sk, int* err, unsigned long long timeout_ns,
-                            cudaStream_t s) {
+                            int Bcap, int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     tc::Args a{};
     a.N = F;
@@ -1188,12 +1001,12 @@ cudaError_t launch_gemm1_tc(const void* S, const void* W1p, const float* b1, voi
     a.hid_tma = 1;
     a.err = err;
     a.timeout_ns = timeout_ns;
-    return tc::run_dense<tc::EPI_GELU>(tc::pick_bn(F), S, (long long)T * Bcap, W1p, T, a, num_sms, sk, s);
+    return tc::run_dense<tc::EPI_GELU>(tc::pick_bn(F), S, (long long)T * Bcap, W1p, T, a, num_sms, s);
 }
 
 cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, const void* S, void* Z,
-                            float2* stats, int B, int T, int D, int F, int Bcap, int num_sms, SkWorkspace* sk,
-                            int* err, unsigned long long timeout_ns, cudaStream_t s) {
+                            float2* stats, int B, int T, int D, int F, int Bcap, int num_sms, int* err,
+                            unsigned long long timeout_ns, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     const int bn = gemm2_bn(D);
     if (bn == 0) return cudaErrorNotSupported;
@@ -1212,7 +1025,7 @@ cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, c
     a.nchunk = D / (bn / 2);
     a.err = err;
     a.timeout_ns = timeout_ns;
-    return tc::run_dense<tc::EPI_RESID>(bn, Hid, (long long)T * Bcap, W2p, T, a, num_sms, sk, s);
+    return tc::run_dense<tc::EPI_RESID>(bn, Hid, (long long)T * Bcap, W2p, T, a, num_sms, s);
 }
 
 cudaError_t launch_moe_gemm1_tc(const void* Sg, long long rows_total, const void* W1p, const float* b1, void* Hm,
@@ -1235,7 +1048,7 @@ cudaError_t launch_moe_gemm1_tc(const void* Sg, long long rows_total, const void
     if (tile_prefix256 && tc::pick_bn(Fe) >= 128) {     // CTA-pair tiles over 256-row tiles
         a.tile_prefix = tile_prefix256;
         return tc::run_pair_bn<tc::EPI_GELU, 8>(tc::pick_bn(Fe), tc::use_ksub2(D, tc::EPI_GELU), Sg, rows_total,
-                                                W1p, groups, a, num_sms, nullptr, s);
+                                                W1p, groups, a, num_sms, s);
     }
     return tc::run_bn<tc::EPI_GELU>(tc::pick_bn(Fe), Sg, rows_total, W1p, groups, a, num_sms, s);
 }
@@ -1261,7 +1074,7 @@ cudaError_t launch_moe_gemm2_tc(const void* Hm, long long rows_total, const void
     if (tile_prefix256 && tc::pick_bn(D) >= 128) {      // CTA-pair tiles over 256-row tiles
         a.tile_prefix = tile_prefix256;
         return tc::run_pair_bn<tc::EPI_GATED, 8>(tc::pick_bn(D), tc::use_ksub2(Fe, tc::EPI_GATED), Hm, rows_total,
-                                                 W2p, groups, a, num_sms, nullptr, s);
+                                                 W2p, groups, a, num_sms, s);
     }
     return tc::run_bn<tc::EPI_GATED>(tc::pick_bn(D), Hm, rows_total, W2p, groups, a, num_sms, s);
 }

@@ -193,11 +193,9 @@ def test_deterministic_reruns():
 
 @pytest.mark.parametrize("B", [100, 2500])      # one shot; three pipelined chunks (512, 1024, 964)
 def test_host_entry_matches_device_entry(B):
-    """The host entry runs large batches as chunks.  Each chunk is its own launch, whose
-    tensor-core GEMMs may cut their last k-loops at other points (stream-K) than the
-    whole batch's; a different float32 sum can round an fp16 intermediate the other way,
-    so the chunked and whole results are each held to the oracle (and to each other at
-    the same bar), while two calls of the same batch agree bit for bit."""
+    """The host entry runs large batches as chunks.  Every sample's arithmetic is the same
+    whatever the batch (the tile shapes and k-loops do not depend on it), so the chunked
+    call equals the device call bit for bit; both are also held to the oracle."""
     T, D, k, L = 8, 512, 4, 2
     m, layers, X = _build(T, D, k, L, B, 23, "bf16")
     dev = m.stack_forward(X)
@@ -205,8 +203,7 @@ def test_host_entry_matches_device_entry(B):
     host = m.stack_forward_host(Xh)
     host2 = m.stack_forward_host(Xh)          # a second call reuses the staging buffers
     torch.cuda.synchronize()
-    assert torch.equal(host, host2)
-    check(host, _np(dev), "bf16", f"host entry vs device entry B={B}")
+    assert torch.equal(host, host2) and torch.equal(dev.cpu(), host)
     rng = np.random.default_rng(B)
     idx = np.unique(np.concatenate([[0, B - 1], rng.choice(B, size=min(24, B), replace=False)]))
     ref = oracle.stack_forward(_np(X[idx]), synth.to_f64(layers))
@@ -497,8 +494,6 @@ print("ok")
 
 
 @pytest.mark.parametrize("tuning", [{},                                            # pairs, 2 k-blocks per stage
-                                    {"RM_GEMM_STREAMK": "0"},                       # pairs, whole tiles only
-                                    {"RM_GEMM_STREAMK": "1"},                       # pairs, stream-K when legal
                                     {"RM_GEMM_PAIR": "0"},                          # one CTA per tile
                                     {"RM_GEMM2_BN": "128"},                         # narrower second-GEMM tiles
                                     {"RM_GEMM_SMALL_BN": "128"},                    # narrower one-CTA tiles
@@ -513,8 +508,7 @@ def test_every_gemm_tile_dispatch(tuning, shape):
     import sys
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     env = {k: v for k, v in os.environ.items()
-           if k not in ("RM_GEMM_PAIR", "RM_GEMM_KSUB", "RM_GEMM1_EPW", "RM_GEMM2_BN", "RM_GEMM_SMALL_BN",
-                        "RM_GEMM_STREAMK")}
+           if k not in ("RM_GEMM_PAIR", "RM_GEMM_KSUB", "RM_GEMM1_EPW", "RM_GEMM2_BN", "RM_GEMM_SMALL_BN")}
     env.update(tuning)
     r = subprocess.run([sys.executable, "-c", _DISPATCH_CHILD.format(root=root, shape=shape)], env=env, cwd=root,
                        capture_output=True, text=True, timeout=600)
