@@ -895,32 +895,43 @@ bool use_pair(int M, int epi) {
     return env == 1 || epi == EPI_RESID;
 }
 
+// The GELU pair kernel's epilogue (a 128 x BN tile per CTA through 8 warps)
+// takes about as long as the MMAs of a 256 x 256 x 768 tile: with K = D <=
+// kShortK the tile's k-loop is too short to hide it, so that GEMM runs 16
+// epilogue warps and, to fit their staging, 5 stages of one k-block each.
+// Measured on GB300 at the 100M shape (T=16, D=768, B=2048): GEMM1 4-5% faster
+// than with 8 warps and 3 two-k-block stages; at D = 1536 the 8-warp form is
+// 16% faster.
+constexpr int kShortK = 1024;
+
 // Two 64-deep k-blocks per pipeline stage (when K allows): half the barrier
 // waits and commits per MMA, 3 stages of 64 KB per CTA.  Measured on GB300
 // (ncu, B = 2048 at the 1B shape, tensor pipe busy): the first GEMM 91.8%
 // against 80.2% with 6 stages of one k-block (74.2% with one CTA per tile),
-// the second 88.6% against 86.8%.  RM_GEMM_KSUB=1 in the environment forces
-// one k-block per stage (a tuning switch; the same result either way).
+// the second 88.6% against 86.8%.  RM_GEMM_KSUB=1|2 in the environment forces
+// one or two k-blocks per stage (a tuning switch; the same result either way).
 bool use_ksub2(int K, int epi) {
-    (void)epi;
     static int env = -1;
     if (env < 0) {
         const char* v = getenv("RM_GEMM_KSUB");
-        env = (v && v[0] == '1') ? 1 : 2;
+        env = !v ? 0 : (v[0] == '1' ? 1 : (v[0] == '2' ? 2 : 0));
     }
-    return env == 2 && K % (2 * BK) == 0;
+    if (K % (2 * BK) != 0) return false;
+    if (env != 0) return env == 2;
+    return !(epi == EPI_GELU && K <= kShortK);
 }
 
-// Epilogue warps of the GELU pair kernel: 8 by default (with two k-blocks per
-// stage, 3 stages fit beside their staging), RM_GEMM1_EPW=16 in the
-// environment for 16 (a tuning switch; the same result either way).
-bool gelu_pair_epw16() {
+// Epilogue warps of the GELU pair kernel: 16 when K <= kShortK, else 8;
+// RM_GEMM1_EPW=8|16 in the environment forces either (a tuning switch; the
+// same result either way).
+bool gelu_pair_epw16(int K) {
     static int env = -1;
     if (env < 0) {
         const char* v = getenv("RM_GEMM1_EPW");
-        env = (v && v[0] == '1' && v[1] == '6') ? 16 : 8;
+        env = !v ? 0 : ((v[0] == '1' && v[1] == '6') ? 16 : (v[0] == '8' ? 8 : 0));
     }
-    return env == 16;
+    if (env != 0) return env == 16;
+    return K <= kShortK;
 }
 
 template <int EPI, int EPW>
@@ -945,7 +956,7 @@ cudaError_t run_dense(int bn, const void* A, long long a_rows_total, const void*
                       int num_sms, cudaStream_t s) {
     if (use_pair(a.M, EPI)) {
         const bool k2 = use_ksub2(a.K, EPI);
-        if (EPI == EPI_GELU && gelu_pair_epw16())
+        if (EPI == EPI_GELU && gelu_pair_epw16(a.K))
             return run_pair_bn<EPI, 16>(bn, k2, A, a_rows_total, W, n_wgroups, a, num_sms, s);
         return run_pair_bn<EPI, 8>(bn, k2, A, a_rows_total, W, n_wgroups, a, num_sms, s);
     }

@@ -500,6 +500,7 @@ print("ok")
                                     {"RM_GEMM_PAIR": "2"},                          # pairs for GEMM2 only
                                     {"RM_GEMM_KSUB": "1"},                          # one k-block per stage
                                     {"RM_GEMM1_EPW": "16"},                         # 16 GELU epilogue warps
+                                    {"RM_GEMM1_EPW": "8", "RM_GEMM_KSUB": "2"},     # 8 warps at short K
                                     {"RM_GEMM1_EPW": "16", "RM_GEMM_KSUB": "1"}])
 @pytest.mark.parametrize("shape", [(4, 256, 2, 2, 300), (2, 192, 2, 1, 300), (8, 512, 2, 2, 1100)])
 def test_every_gemm_tile_dispatch(tuning, shape):
