@@ -951,9 +951,304 @@ cudaError_t run_pair_bn(int bn, bool k2, const void* A, long long a_rows_total, 
     }
 }
 
+// ----------------------------------------------------------------------------
+// Small batches: the weights as the MMA's M side.  With B rows per token group
+// the 128-row activation tile of the kernels above is mostly zeros: the time
+// goes into streaming the weights, and the A tile's shared-memory slots (16 KB
+// a stage, loaded as zero fill) crowd out weight stages.  Here D^T = W^T S^T:
+// a work unit is 128 output features of one token group; the MMA takes 128
+// weight rows (A, K-major, as packed) against NB activation rows (B, K-major,
+// NB = B rounded up to a legal N), accumulates 128 x NB in TMEM, and a stage
+// is 16 KB of weights + NB x 128 B of activations, so 8-11 stages of weights
+// are in flight per SM.  Units walk the feature blocks of a token group
+// fastest (its activation rows stay in L2).
+//   warp 0      TMA producer
+//   warp 1      MMA issuer (one thread)
+//   warp 2      TMEM allocator
+//   warps 4-7   epilogue: warp 4 + q reads TMEM lanes 32 q .. 32 q + 31 (one
+//               feature per lane) and the NB batch columns; GEMM1 stores
+//               Gelu(acc + b1) per (row, feature), GEMM2 stores acc + b2 + S and
+//               the (mean, M2) of each row over the unit's 128 features (the
+//               128-column statistics chunk of the two-phase LN2), the four
+//               warps' partial moments merged by Chan's formula in shared memory.
+// ----------------------------------------------------------------------------
+template <int NB>
+struct CfgS {
+    static constexpr int A_BYTES = 128 * BK * 2;
+    static constexpr int B_BYTES = NB * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = (200 * 1024) / STAGE_BYTES > 12 ? 12 : (200 * 1024) / STAGE_BYTES;
+    static constexpr int TMEM_COLS = 2 * NB < 32 ? 32 : 2 * NB;
+    static constexpr int THREADS = 256;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int STAT_BYTES = 2 * 2 * 4 * NB * 4;     // (mean, M2) x 2 buffers x 4 warps x NB
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + STAT_BYTES;
+    static_assert(NB % 16 == 0 && NB >= 16 && NB <= 256, "MMA N for M = 128");
+    static_assert(B_BYTES % 1024 == 0, "swizzle atoms of the activation tile");
+    static_assert((TMEM_COLS & (TMEM_COLS - 1)) == 0 && TMEM_COLS <= 512, "TMEM allocation");
+    static_assert(2 * STAGES * 8 + 4 * 8 + 8 <= BAR_BYTES, "barrier area");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+// 16 consecutive fp32 TMEM columns of this thread's lane (32x32b shape, x16).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <int NB, int EPI>
+__global__ void __launch_bounds__(CfgS<NB>::THREADS, 1)
+pffn_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                      const Args args) {
+    using C = CfgS<NB>;
+    constexpr int CW = NB < 32 ? NB : 32;        // TMEM columns per load
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t* base_ptr = smem_raw + (base - raw_addr);
+    const uint32_t sA = base;
+    const uint32_t sB = base + C::STAGES * C::A_BYTES;
+    const uint32_t bar0 = base + C::STAGES * C::STAGE_BYTES;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + C::STAGES * C::STAGE_BYTES + 8 * (2 * C::STAGES + 4));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    // per-warp row moments of the last GEMM's units: [buffer][mean | M2][warp][NB]
+    float* s_stat = reinterpret_cast<float*>(base_ptr + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmX);
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 4);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
+
+    const int kblocks = args.K / BK;
+    const long long units = args.tiles;             // token groups x feature blocks
+    const int nfb = args.n_tiles;                   // feature blocks of 128 per group
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------------
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (long long u = blockIdx.x; ok && u < units; u += gridDim.x) {
+            const int j = (int)(u / nfb);
+            const int fb = (int)(u - (long long)j * nfb);
+            const int wg = args.group_base + j * args.group_stride;
+            for (int kb = 0; kb < kblocks; ++kb) {
+                if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, args.err, args.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(full_bar(stage), (uint32_t)C::STAGE_BYTES);
+                    tma_load_3d(&tmW, sA + stage * C::A_BYTES, full_bar(stage), kb * BK, fb * 128, wg);
+                    tma_load_3d(&tmX, sB + stage * C::B_BYTES, full_bar(stage), kb * BK, 0, j);
+                }
+                __syncwarp();
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer --------------------------------
+        constexpr uint32_t idesc = make_idesc_f16_f32(128, NB);
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (long long u = blockIdx.x; ok && u < units; u += gridDim.x) {
+            if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.err, args.timeout_ns)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * NB);
+            for (int kb = 0; kb < kblocks; ++kb) {
+                if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, args.err, args.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a0 = sA + stage * C::A_BYTES;
+                const uint32_t b0 = sB + stage * C::B_BYTES;
+                if (lane == 0) {
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        umma_f16(d_tmem, make_sw128_desc(a0 + 32u * k), make_sw128_desc(b0 + 32u * k), idesc,
+                                 (kb > 0 || k > 0) ? 1u : 0u);
+                    umma_commit(empty_bar(stage));
+                }
+                __syncwarp();
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            if (lane == 0) umma_commit(tfull_bar(acc));
+            __syncwarp();
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    } else if (warp >= 4) {
+        // ------------------------------ epilogue ----------------------------------
+        const int q = warp & 3;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+            const int j = (int)(u / nfb);
+            const int fb = (int)(u - (long long)j * nfb);
+            const int wg = args.group_base + j * args.group_stride;
+            const int f = fb * 128 + q * 32 + lane;                      // this lane's output feature
+            const float bf = __ldg(args.bias + (size_t)wg * args.N + f);
+            const size_t row0 = (size_t)j * (size_t)args.a_group_rows;   // row of batch 0 of this group
+            if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err, args.timeout_ns)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * NB);
+            float* st_mean = s_stat + (size_t)acc * 2 * 4 * NB + (size_t)q * NB;
+            float* st_m2 = st_mean + 4 * NB;
+#pragma unroll 1
+            for (int c = 0; c < NB / CW; ++c) {
+                float v[CW];
+                if constexpr (CW == 32) {
+                    tmem_ld32(tbase + 32u * c, v);
+                } else {
+                    tmem_ld16(tbase + 16u * c, v);
+                }
+#pragma unroll
+                for (int i = 0; i < CW; ++i) {
+                    const int b = c * CW + i;                              // batch row (warp-uniform)
+                    if (b >= args.M) break;
+                    const size_t o = (row0 + b) * (size_t)args.N + f;
+                    if (EPI == EPI_GELU) {
+                        args.hid[o] = __float2half_rn(sat_f16(gelu_erf(v[i] + bf)));
+                    } else {   // EPI_RESID
+                        const float z = v[i] + bf + __half2float(args.resid[o]);
+                        args.z[o] = __float2half_rn(sat_f16(z));
+                        // this warp's 32 features: mean and M2 about it
+                        const float mw = warp_sum(z) * (1.0f / 32.0f);
+                        const float d = z - mw;
+                        const float m2w = warp_sum(d * d);
+                        if (lane == 0) {
+                            st_mean[b] = mw;
+                            st_m2[b] = m2w;
+                        }
+                    }
+                }
+            }
+            if (EPI == EPI_RESID) {
+                // the four warps' moments -> (mean, M2) of the 128 features, one lane per row
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (q == 0) {
+                    const float* sm = s_stat + (size_t)acc * 2 * 4 * NB;
+                    const float* s2 = sm + 4 * NB;
+                    for (int b = lane; b < args.M && b < NB; b += 32) {
+                        const float m0 = sm[b], m1 = sm[NB + b], m2 = sm[2 * NB + b], m3 = sm[3 * NB + b];
+                        const float mean = 0.25f * (m0 + m1 + m2 + m3);
+                        const float d0 = m0 - mean, d1 = m1 - mean, d2 = m2 - mean, d3 = m3 - mean;
+                        const float M2 = s2[b] + s2[NB + b] + s2[2 * NB + b] + s2[3 * NB + b] +
+                                         32.0f * (d0 * d0 + d1 * d1 + d2 * d2 + d3 * d3);
+                        args.stats[(row0 + b) * (size_t)args.nchunk + fb] = make_float2(mean, M2);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// Largest batch that takes the weight-as-M path (RM_GEMM_SWAP_MAX in the
+// environment overrides; 0 turns it off -- a tuning switch, the same result
+// up to the fp32 summation order).
+int swap_max_batch() {
+    static int env = -1;
+    if (env < 0) {
+        const char* v = getenv("RM_GEMM_SWAP_MAX");
+        env = v ? atoi(v) : 64;
+        if (env > 256) env = 256;
+    }
+    return env;
+}
+
+template <int NB, int EPI>
+cudaError_t run_swap(const void* A, const void* W, int n_wgroups, Args a, int num_sms, cudaStream_t s) {
+    using C = CfgS<NB>;
+    a.n_tiles = a.N / 128;
+    a.tiles = (long long)a.ngroups * a.n_tiles;
+    if (a.tiles == 0) return cudaSuccess;
+    CUtensorMap mW, mX;
+    if (!make_map(&mW, W, a.K, a.N, n_wgroups, a.N, 128)) return cudaErrorInvalidValue;
+    if (!make_map(&mX, A, a.K, a.M, a.ngroups, a.a_group_rows, NB)) return cudaErrorInvalidValue;
+    auto k = pffn_gemm_swap_kernel<NB, EPI>;
+    static bool attr_done = false;  // once per template instance
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    const long long grid = a.tiles < num_sms ? a.tiles : num_sms;
+    k<<<(int)grid, C::THREADS, C::SMEM_BYTES, s>>>(mW, mX, a);
+    return cudaGetLastError();
+}
+
+template <int EPI>
+cudaError_t run_swap_nb(const void* A, const void* W, int n_wgroups, const Args& a, int num_sms, cudaStream_t s) {
+    if (a.M <= 16) return run_swap<16, EPI>(A, W, n_wgroups, a, num_sms, s);
+    if (a.M <= 32) return run_swap<32, EPI>(A, W, n_wgroups, a, num_sms, s);
+    if (a.M <= 64) return run_swap<64, EPI>(A, W, n_wgroups, a, num_sms, s);
+    if (a.M <= 128) return run_swap<128, EPI>(A, W, n_wgroups, a, num_sms, s);
+    return run_swap<256, EPI>(A, W, n_wgroups, a, num_sms, s);
+}
+
 template <int EPI>
 cudaError_t run_dense(int bn, const void* A, long long a_rows_total, const void* W, int n_wgroups, const Args& a,
                       int num_sms, cudaStream_t s) {
+    // weights as the MMA's M side for small batches; the second GEMM's row
+    // statistics then come in 128-column chunks, which must be the context's
+    if (a.M <= swap_max_batch() && a.N % 128 == 0 && a.K % BK == 0 &&
+        (EPI == EPI_GELU || (EPI == EPI_RESID && a.nchunk * 128 == a.N)))
+        return run_swap_nb<EPI>(A, W, n_wgroups, a, num_sms, s);
     if (use_pair(a.M, EPI)) {
         const bool k2 = use_ksub2(a.K, EPI);
         if (EPI == EPI_GELU && gelu_pair_epw16(a.K))

@@ -478,39 +478,46 @@ import oracle
 from rankmixer_feature_interaction_gb300 import synth
 from rankmixer_feature_interaction_gb300.api import RankMixer
 from tests.helpers import check
-T, D, k, L, B = {shape}
-layers = synth.make_stack(T, D, k, L, 123, "bf16", "cuda")
-m = RankMixer(T, D, k, layers, max_batch=B, gemm_path="tcgen05")
-X = synth.make_input(B, T, D, 124, "bf16", "cuda")
-pooled, XL = m.stack_forward(X, return_XL=True, xl_dtype="f32")
-torch.cuda.synchronize()
-assert m.sync_status() == 0
-p64 = synth.to_f64(layers)
-ref_pool, ref_XL = oracle.stack_forward(X.cpu().double().numpy(), p64, return_XL=True)
-check(XL, ref_XL, "bf16", "X_L")
-check(pooled, ref_pool, "bf16", "pooled")
+for T, D, k, L, B in {shapes}:
+    layers = synth.make_stack(T, D, k, L, 123, "bf16", "cuda")
+    m = RankMixer(T, D, k, layers, max_batch=B, gemm_path="tcgen05")
+    X = synth.make_input(B, T, D, 124, "bf16", "cuda")
+    pooled, XL = m.stack_forward(X, return_XL=True, xl_dtype="f32")
+    torch.cuda.synchronize()
+    assert m.sync_status() == 0
+    p64 = synth.to_f64(layers)
+    ref_pool, ref_XL = oracle.stack_forward(X.cpu().double().numpy(), p64, return_XL=True)
+    check(XL, ref_XL, "bf16", f"X_L {{(T, D, k, L, B)}}")
+    check(pooled, ref_pool, "bf16", f"pooled {{(T, D, k, L, B)}}")
+    m.close()
 print("ok")
 """
 
+# shapes that reach every tile form: CTA pairs with BN 256 / 128 (GEMM1) and 64 (GEMM2), one-CTA
+# tiles (129..255 rows), the weights-as-M path (1..64 rows, and up to 256 when widened)
+_DISPATCH_SHAPES = [(4, 256, 2, 2, 300), (2, 192, 2, 1, 300), (8, 512, 2, 2, 1100), (4, 256, 2, 2, 13),
+                    (4, 256, 2, 2, 40), (4, 512, 2, 1, 150)]
+_TUNING_KEYS = ("RM_GEMM_PAIR", "RM_GEMM_KSUB", "RM_GEMM1_EPW", "RM_GEMM2_BN", "RM_GEMM_SMALL_BN", "RM_GEMM_SWAP_MAX")
 
-@pytest.mark.parametrize("tuning", [{},                                            # pairs, 2 k-blocks per stage
+
+@pytest.mark.parametrize("tuning", [{},                                            # the defaults
                                     {"RM_GEMM_PAIR": "0"},                          # one CTA per tile
                                     {"RM_GEMM2_BN": "128"},                         # narrower second-GEMM tiles
                                     {"RM_GEMM_SMALL_BN": "128"},                    # narrower one-CTA tiles
+                                    {"RM_GEMM_SWAP_MAX": "0"},                      # no weights-as-M path
+                                    {"RM_GEMM_SWAP_MAX": "256"},                    # weights-as-M up to 256 rows
                                     {"RM_GEMM_PAIR": "2"},                          # pairs for GEMM2 only
                                     {"RM_GEMM_KSUB": "1"},                          # one k-block per stage
                                     {"RM_GEMM1_EPW": "16"},                         # 16 GELU epilogue warps
                                     {"RM_GEMM1_EPW": "8", "RM_GEMM_KSUB": "2"},     # 8 warps at short K
                                     {"RM_GEMM1_EPW": "16", "RM_GEMM_KSUB": "1"}])
-@pytest.mark.parametrize("shape", [(4, 256, 2, 2, 300), (2, 192, 2, 1, 300), (8, 512, 2, 2, 1100)])
-def test_every_gemm_tile_dispatch(tuning, shape):
+def test_every_gemm_tile_dispatch(tuning):
     import os
     import subprocess
     import sys
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    env = {k: v for k, v in os.environ.items()
-           if k not in ("RM_GEMM_PAIR", "RM_GEMM_KSUB", "RM_GEMM1_EPW", "RM_GEMM2_BN", "RM_GEMM_SMALL_BN")}
+    env = {k: v for k, v in os.environ.items() if k not in _TUNING_KEYS}
     env.update(tuning)
-    r = subprocess.run([sys.executable, "-c", _DISPATCH_CHILD.format(root=root, shape=shape)], env=env, cwd=root,
-                       capture_output=True, text=True, timeout=600)
+    r = subprocess.run([sys.executable, "-c", _DISPATCH_CHILD.format(root=root, shapes=_DISPATCH_SHAPES)], env=env,
+                       cwd=root, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
