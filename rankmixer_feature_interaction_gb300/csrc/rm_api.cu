@@ -59,6 +59,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // Default bound of every device-side wait (2 s of global time).
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
+// Up to this batch the dense PFFN leaves its LN2 row statistics as the GEMM2
+// chunk partials and the consumers merge them (no separate merge launch).
+constexpr int kMergeInConsumerMaxB = 256;
 // Pipelined host entry: batches of at least 2 kHostChunkMin samples run as
 // chunks (at most kHostChunksMax; the schedule is in rm_stack_forward_host).
 constexpr int kHostChunksMax = 4;
@@ -186,6 +189,10 @@ struct rm_ctx {
     void* Z = nullptr;           // pre-LN2 rows, operand type
     float2* stats = nullptr;     // GEMM2 epilogue partials: [T][Bcap][nchunk] (mean, M2) per column chunk
     float2* rows = nullptr;      // merged: [T][Bcap] (mean, M2) of each full pre-LN2 row
+    // where the last PFFN left its LN2 row statistics for the consumers: the
+    // merged rows, or (small batches) the GEMM2 chunk partials themselves
+    const float2* ln2_st = nullptr;
+    int ln2_nchunk = 1, ln2_cw = 0;
     float* V = nullptr;          // MoE PFFN output inside the stack
     MoeWorkspace moe_ws;
     TrainWS tw;
@@ -378,6 +385,9 @@ rm_status run_pffn(rm_ctx* c, int layer, int B, cudaStream_t s) {
         RM_CHECK_CUDA(moe_residual_z(c->act, c->V, c->S, c->Z, B, g.T, g.D, c->Bcap, s), "moe residual");
         ProfScope ps2(c, RM_K_ROWSTATS, s);
         RM_CHECK_CUDA(launch_rowstats(c->act, c->Z, c->rows, B, g.T, g.D, c->Bcap, c->num_sms, s), "row stats");
+        c->ln2_st = c->rows;
+        c->ln2_nchunk = 1;
+        c->ln2_cw = g.D;
         return RM_OK;
     }
     if (c->use_tc) {
@@ -392,6 +402,14 @@ rm_status run_pffn(rm_ctx* c, int layer, int B, cudaStream_t s) {
             cudaError_t e = launch_gemm2_tc(c->Hid, w.W2p, w.b2, c->S, c->Z, c->stats, B, g.T, g.D, c->F, c->Bcap,
                                             c->num_sms, c->d_err, kWaitTimeoutNs, s);
             if (e != cudaSuccess) return cuda_fail(e, (std::string("gemm2 (tcgen05) ") + tc_last_error()).c_str());
+        }
+        if (B <= kMergeInConsumerMaxB) {
+            // small batches: the consumers merge the chunk partials themselves (one
+            // launch fewer; the merge costs them next to nothing at this size)
+            c->ln2_st = c->stats;
+            c->ln2_nchunk = c->nchunk;
+            c->ln2_cw = c->cw;
+            return RM_OK;
         }
         ProfScope ps(c, RM_K_ROWSTATS, s);
         RM_CHECK_CUDA(launch_stats_finalize(c->stats, c->rows, B, g.T, c->Bcap, c->nchunk, c->cw, c->num_sms, s),
@@ -410,12 +428,11 @@ rm_status run_pffn(rm_ctx* c, int layer, int B, cudaStream_t s) {
         ProfScope ps(c, RM_K_ROWSTATS, s);
         RM_CHECK_CUDA(launch_rowstats(c->act, c->Z, c->rows, B, g.T, g.D, c->Bcap, c->num_sms, s), "row stats");
     }
+    c->ln2_st = c->rows;
+    c->ln2_nchunk = 1;
+    c->ln2_cw = g.D;
     return RM_OK;
 }
-
-// The LN2 consumers read c->rows: one merged (mean, M2) per row.
-int layer_nchunk(const rm_ctx*, int) { return 1; }
-int layer_cw(const rm_ctx* c, int) { return c->cfg.D; }
 
 MixLnArgs mix_args(const rm_ctx* c, int layer, int B) {
     MixLnArgs a{};
@@ -448,7 +465,8 @@ rm_status stack_device(rm_ctx* c, const void* X0, float* pooled, void* XL, bool 
             XType xt = caller_xtype(c);
             if (n > 0) {
                 ProfScope ps(c, RM_K_LN2_OUT, s);
-                RM_CHECK_CUDA(launch_ln2_out_op(c->act, c->Z, c->rows, c->layers[n - 1].g2, c->layers[n - 1].be2,
+                RM_CHECK_CUDA(launch_ln2_out_op(c->act, c->Z, c->ln2_st, c->ln2_nchunk, c->ln2_cw,
+                                                c->layers[n - 1].g2, c->layers[n - 1].be2,
                                                 c->umX, B, g.T, g.D, c->Bcap, g.ln_eps, c->num_sms, s),
                               "ln2 (unimixing layer input)");
                 xin = c->umX;
@@ -462,11 +480,11 @@ rm_status stack_device(rm_ctx* c, const void* X0, float* pooled, void* XL, bool 
             RM_CHECK_CUDA(launch_mix_ln1(c->act, false, a, c->num_sms, s), "mix+ln1");
         } else {
             a.Z = c->Z;
-            a.stats = c->rows;
+            a.stats = c->ln2_st;
             a.g2 = c->layers[n - 1].g2;
             a.be2 = c->layers[n - 1].be2;
-            a.nchunk = layer_nchunk(c, n - 1);
-            a.cw = layer_cw(c, n - 1);
+            a.nchunk = c->ln2_nchunk;
+            a.cw = c->ln2_cw;
             ProfScope ps(c, RM_K_MIX_LN1, s);
             RM_CHECK_CUDA(launch_mix_ln1(c->act, true, a, c->num_sms, s), "ln2+mix+ln1");
         }
@@ -475,8 +493,8 @@ rm_status stack_device(rm_ctx* c, const void* X0, float* pooled, void* XL, bool 
     }
     const int last = g.L - 1;
     ProfScope ps(c, RM_K_POOL, s);
-    RM_CHECK_CUDA(launch_pool(c->act, c->Z, c->rows, c->layers[last].g2, c->layers[last].be2, pooled, XL, xl_f32, B,
-                              g.T, g.D, c->Bcap, layer_nchunk(c, last), layer_cw(c, last), g.ln_eps, c->num_sms,
+    RM_CHECK_CUDA(launch_pool(c->act, c->Z, c->ln2_st, c->layers[last].g2, c->layers[last].be2, pooled, XL, xl_f32,
+                              B, g.T, g.D, c->Bcap, c->ln2_nchunk, c->ln2_cw, g.ln_eps, c->num_sms,
                               c->d_err, kWaitTimeoutNs, s),
                   "ln2+pool");
     return RM_OK;
@@ -998,8 +1016,8 @@ rm_status rm_block_forward(rm_ctx* c, int layer, const void* X_in, void* X_out, 
     }
     if ((st = run_pffn(c, layer, B, s)) != RM_OK) return st;
     ProfScope ps(c, RM_K_LN2_OUT, s);
-    RM_CHECK_CUDA(launch_ln2_out(c->act, c->Z, c->rows, c->layers[layer].g2, c->layers[layer].be2, X_out, out_f32, B,
-                                 g.T, g.D, c->Bcap, layer_nchunk(c, layer), layer_cw(c, layer), g.ln_eps, c->num_sms,
+    RM_CHECK_CUDA(launch_ln2_out(c->act, c->Z, c->ln2_st, c->layers[layer].g2, c->layers[layer].be2, X_out, out_f32,
+                                 B, g.T, g.D, c->Bcap, c->ln2_nchunk, c->ln2_cw, g.ln_eps, c->num_sms,
                                  s),
                   "ln2 out");
     return RM_OK;

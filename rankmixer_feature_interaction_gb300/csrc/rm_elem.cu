@@ -1037,19 +1037,20 @@ cudaError_t launch_ln2_out(Act act, const void* Z, const float2* stats, const fl
     return cudaGetLastError();
 }
 
-cudaError_t launch_ln2_out_op(Act act, const void* Z, const float2* stats, const float* g2, const float* be2,
-                              void* X_out, int B, int T, int D, int Bcap, float eps, int num_sms, cudaStream_t s) {
+cudaError_t launch_ln2_out_op(Act act, const void* Z, const float2* stats, int nchunk, int cw, const float* g2,
+                              const float* be2, void* X_out, int B, int T, int D, int Bcap, float eps, int num_sms,
+                              cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     const int grid = grid_for((long long)B * T * 32, 256, num_sms * 8);
     if (act == Act::BF16 && D % 256 == 0)
         ln2_out_vec_kernel<__half><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2, (__half*)X_out, B, T, D,
-                                                        Bcap, 1, D, eps);
+                                                        Bcap, nchunk, cw, eps);
     else if (act == Act::BF16)
         ln2_out_kernel<__half, __half><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2, (__half*)X_out, B, T, D,
-                                                            Bcap, 1, D, eps);
+                                                            Bcap, nchunk, cw, eps);
     else
         ln2_out_kernel<float, float><<<grid, 256, 0, s>>>((const float*)Z, stats, g2, be2, (float*)X_out, B, T, D,
-                                                          Bcap, 1, D, eps);
+                                                          Bcap, nchunk, cw, eps);
     return cudaGetLastError();
 }
 

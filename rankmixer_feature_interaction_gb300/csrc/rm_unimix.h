@@ -55,8 +55,10 @@ cudaError_t launch_unimix_ln1(XType xt, Act act, const void* X, const void* Y, v
 cudaError_t launch_unimix_out(Act act, const void* Y, void* out, bool out_f32, long long n, cudaStream_t s);
 
 // X_out[b][t][:] = LN2(Z[t][b][:]) in the operand type (fp16 for bf16
-// contexts): a UniMixing layer's input when it follows another layer.
-cudaError_t launch_ln2_out_op(Act act, const void* Z, const float2* stats, const float* g2, const float* be2,
-                              void* X_out, int B, int T, int D, int Bcap, float eps, int num_sms, cudaStream_t s);
+// contexts): a UniMixing layer's input when it follows another layer.  stats:
+// nchunk (mean, M2) partials of cw columns per row (nchunk = 1: merged rows).
+cudaError_t launch_ln2_out_op(Act act, const void* Z, const float2* stats, int nchunk, int cw, const float* g2,
+                              const float* be2, void* X_out, int B, int T, int D, int Bcap, float eps, int num_sms,
+                              cudaStream_t s);
 
 }  // namespace rm
