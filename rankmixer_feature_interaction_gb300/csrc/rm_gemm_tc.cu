@@ -1145,6 +1145,15 @@ pffn_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
                 } else {
                     tmem_ld16(tbase + 16u * c, v);
                 }
+                // the residuals of the chunk's rows first, all loads in flight together
+                float rres[EPI == EPI_RESID ? CW : 1];
+                if (EPI == EPI_RESID) {
+#pragma unroll
+                    for (int i = 0; i < CW; ++i) {
+                        const int b = c * CW + i;
+                        rres[i] = b < args.M ? __half2float(args.resid[(row0 + b) * (size_t)args.N + f]) : 0.f;
+                    }
+                }
 #pragma unroll
                 for (int i = 0; i < CW; ++i) {
                     const int b = c * CW + i;                              // batch row (warp-uniform)
@@ -1153,7 +1162,7 @@ pffn_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
                     if (EPI == EPI_GELU) {
                         args.hid[o] = __float2half_rn(sat_f16(gelu_erf(v[i] + bf)));
                     } else {   // EPI_RESID
-                        const float z = v[i] + bf + __half2float(args.resid[o]);
+                        const float z = v[i] + bf + rres[i];
                         args.z[o] = __float2half_rn(sat_f16(z));
                         // this warp's 32 features: mean and M2 about it
                         const float mw = warp_sum(z) * (1.0f / 32.0f);
@@ -1255,12 +1264,15 @@ cudaError_t run_dense(int bn, const void* A, long long a_rows_total, const void*
             return run_pair_bn<EPI, 16>(bn, k2, A, a_rows_total, W, n_wgroups, a, num_sms, s);
         return run_pair_bn<EPI, 8>(bn, k2, A, a_rows_total, W, n_wgroups, a, num_sms, s);
     }
-    static int small_bn = -1;   // RM_GEMM_SMALL_BN=64|128: narrower one-CTA tiles (a tuning switch)
+    // RM_GEMM_SMALL_BN=64|128: narrower one-CTA tiles for the first GEMM (a tuning
+    // switch; the second GEMM's tile width fixes its statistics chunks, see gemm2_bn)
+    static int small_bn = -1;
     if (small_bn < 0) {
         const char* v = getenv("RM_GEMM_SMALL_BN");
         small_bn = v ? atoi(v) : 0;
     }
-    if ((small_bn == 64 || small_bn == 128) && small_bn < bn && a.N % small_bn == 0) bn = small_bn;
+    if (EPI == EPI_GELU && (small_bn == 64 || small_bn == 128) && small_bn < bn && a.N % small_bn == 0)
+        bn = small_bn;
     return run_bn<EPI>(bn, A, a_rows_total, W, n_wgroups, a, num_sms, s);
 }
 
