@@ -183,6 +183,18 @@ __device__ __forceinline__ void merge_row_stats(const float2* __restrict__ st, i
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  The forward-path kernels are launched with
+// programmatic stream serialization (launch_k in rm_internal.h): such a kernel
+// may start while the previous kernel of the stream is still running, so it
+// calls pdl_wait() before its first access to anything earlier work on the
+// stream wrote or still reads (it returns at once for a normal launch), and
+// pdl_launch_next() to let the next kernel begin launching (its CTAs then
+// take SMs as this kernel's CTAs leave them, and run their set-up).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // Bounded waiting
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint64_t globaltimer_ns() {

@@ -10,6 +10,7 @@
 // Types: Tin is the caller's activation dtype (bf16 or float), Top the
 // operand type of the GEMMs (fp16 for bf16 contexts, float for float32
 // contexts).  The pre-LN2 rows Z are stored in Top as well.
+#include <cstdlib>
 #include <type_traits>
 
 #include "rm_common.cuh"
@@ -176,6 +177,8 @@ mix_ln1_staged_kernel(const MixLnArgs a) {
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_wait();
+    pdl_launch_next();
 
     auto issue = [&](int b, int slot) {   // thread 0 only
         const uint32_t bar = smem_u32(&bars[slot]);
@@ -287,6 +290,8 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_wait();              // the layer input and its statistics come from the previous kernel
+    pdl_launch_next();
 
     auto issue = [&](int b, int slot) {   // warp 0: lane 0 arms the barrier, lane t copies row t
         const uint32_t bar = smem_u32(&bars[slot]);
@@ -306,13 +311,20 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
     const int pre_t = warp + lane * nwarps;
     const bool pre_lane = merged && pre_t < T;
     float2 pre = make_float2(0.f, 0.f);
-    if (!DBG && pre_lane && (int)blockIdx.x < a.B) pre = __ldg(a.stats + (size_t)pre_t * a.Bcap + blockIdx.x);
+    // work items w = (sample w / rsplit, output rows of part w % rsplit); with small
+    // batches a sample's rows are spread over rsplit CTAs (each stages the whole sample)
+    const int rsplit = a.rsplit > 0 ? a.rsplit : 1;
+    const int nitems = a.B * rsplit;
+    if (!DBG && pre_lane && (int)blockIdx.x < nitems)
+        pre = __ldg(a.stats + (size_t)pre_t * a.Bcap + (int)blockIdx.x / rsplit);
 
-    if (warp == 0 && (int)blockIdx.x < a.B) issue(blockIdx.x, 0);
+    if (warp == 0 && (int)blockIdx.x < nitems) issue((int)blockIdx.x / rsplit, 0);
     int it = 0;
-    for (int b = blockIdx.x; b < a.B; b += gridDim.x, ++it) {
+    for (int w = blockIdx.x; w < nitems; w += gridDim.x, ++it) {
+        const int b = w / rsplit, part = w - b * rsplit;
+        const int bn = (w + (int)gridDim.x) / rsplit;          // sample of this CTA's next item
         const int slot = it & 1;
-        if (warp == 0 && b + (int)gridDim.x < a.B) issue(b + gridDim.x, slot ^ 1);
+        if (warp == 0 && w + (int)gridDim.x < nitems) issue(bn, slot ^ 1);
         if (merged) {
             if (pre_lane && DBG) {
                 s_mean[pre_t] = 0.0f;
@@ -320,7 +332,7 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
             } else if (pre_lane) {
                 s_mean[pre_t] = pre.x;
                 s_rstd[pre_t] = rsqrtf(pre.y / (float)D + a.eps);
-                if (b + (int)gridDim.x < a.B) pre = __ldg(a.stats + (size_t)pre_t * a.Bcap + b + gridDim.x);
+                if (w + (int)gridDim.x < nitems) pre = __ldg(a.stats + (size_t)pre_t * a.Bcap + bn);
             }
         } else if (FROM_Z) {
             sample_row_stats(a, b, s_mean, s_rstd, warp, nwarps, lane);
@@ -356,7 +368,8 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
         // float32 pair fma to (y - mean) rstd, then one fp16 pair fma with the fp16
         // gamma, beta (S is stored in fp16)
         const int nv = D >> 8;
-        for (int h = warp; h < T; h += nwarps) {
+        const int h0 = part * T / rsplit, h1 = (part + 1) * T / rsplit;
+        for (int h = h0 + warp; h < h1; h += nwarps) {
             const uint16_t* xh = xs + (size_t)h * RS;
             uint64_t y[4 * NV];
             uint64_t s2 = f2_splat(0.f);
@@ -454,10 +467,19 @@ cudaError_t launch_v8(const MixLnArgs& a, int num_sms, cudaStream_t s) {
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, threads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
-    int grid = num_sms * per_sm;
-    if (grid > a.B) grid = a.B;
-    k<<<grid, threads, smem, s>>>(a);
-    return cudaGetLastError();
+    // small batches: spread each sample's output rows over several CTAs (at least
+    // two rows each) so that more SMs work on it
+    MixLnArgs b = a;
+    const int slots = num_sms * per_sm;
+    b.rsplit = 1;
+    if (a.B < slots) {
+        int r = slots / a.B;
+        if (r > a.T / 2) r = a.T / 2;
+        b.rsplit = r > 1 ? r : 1;
+    }
+    int grid = slots;
+    if (grid > a.B * b.rsplit) grid = a.B * b.rsplit;
+    return launch_k(k, dim3(grid), dim3(threads), smem, s, b);
 }
 
 template <bool FROM_Z, bool DBG = false>
@@ -487,6 +509,8 @@ mix_ln1_direct_kernel(const MixLnArgs a) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int T = a.T, D = a.D, q = a.q;
     Top* S = reinterpret_cast<Top*>(a.S);
+    pdl_wait();
+    pdl_launch_next();
     for (int b = blockIdx.x; b < a.B; b += gridDim.x) {
         // source rows: X sample-major (row stride D) or Z token-major (row stride Bcap D)
         const Tin* X = reinterpret_cast<const Tin*>(a.X) + (size_t)b * T * D;
@@ -544,8 +568,7 @@ template <typename Tin, typename Top, bool FROM_Z, int VEC, int NI>
 cudaError_t launch_direct(const MixLnArgs& a, int num_sms, cudaStream_t s) {
     int grid = num_sms * 8;
     if (grid > a.B) grid = a.B;
-    mix_ln1_direct_kernel<Tin, Top, FROM_Z, VEC, NI><<<grid, kMixThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_k(mix_ln1_direct_kernel<Tin, Top, FROM_Z, VEC, NI>, dim3(grid), dim3(kMixThreads), 0, s, a);
 }
 
 template <typename Tin, typename Top, bool FROM_Z>
@@ -581,8 +604,7 @@ cudaError_t launch_staged(const MixLnArgs& a, int num_sms, cudaStream_t s) {
     if (per_sm < 1) per_sm = 1;
     int grid = num_sms * per_sm;
     if (grid > a.B) grid = a.B;
-    k<<<grid, threads, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_k(k, dim3(grid), dim3(threads), smem, s, a);
 }
 
 template <typename Tsrc, bool FROM_Z>
@@ -606,6 +628,8 @@ template <typename Tz, typename Tout>
 __global__ void ln2_out_kernel(const Tz* __restrict__ Z, const float2* __restrict__ stats,
                                const float* __restrict__ g2, const float* __restrict__ be2, Tout* __restrict__ X,
                                int B, int T, int D, int Bcap, int nchunk, int cw, float eps) {
+    pdl_wait();
+    pdl_launch_next();
     const int lane = threadIdx.x & 31;
     const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
@@ -650,6 +674,8 @@ template <typename Tout>
 __global__ void ln2_out_vec_kernel(const __half* __restrict__ Z, const float2* __restrict__ stats,
                                    const float* __restrict__ g2, const float* __restrict__ be2, Tout* __restrict__ X,
                                    int B, int T, int D, int Bcap, int nchunk, int cw, float eps) {
+    pdl_wait();
+    pdl_launch_next();
     const int lane = threadIdx.x & 31;
     const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
@@ -697,6 +723,8 @@ pool_kernel(const Tz* __restrict__ Z, const float2* __restrict__ stats, const fl
     __shared__ float s_mean[kMaxT], s_rstd[kMaxT];
     __shared__ __half2 s_rh[kMaxT], s_nmrh[kMaxT];     // rstd and -mean rstd as fp16 pairs
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_wait();
+    pdl_launch_next();
     for (int b = blockIdx.x; b < B; b += gridDim.x) {
         for (int t = warp; t < T; t += kPoolThreads / 32) {
             float mean, rstd;
@@ -793,6 +821,8 @@ pool_kernel(const Tz* __restrict__ Z, const float2* __restrict__ stats, const fl
 // ---------------------------------------------------------------------------
 __global__ void stats_finalize_kernel(const float2* __restrict__ part, float2* __restrict__ out, int B, int T,
                                       int Bcap, int nchunk, int cw) {
+    pdl_wait();
+    pdl_launch_next();
     const long long n = (long long)T * B;
     for (long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x; r < n; r += (long long)gridDim.x * blockDim.x) {
         const int t = (int)(r / B), b = (int)(r % B);
@@ -814,6 +844,8 @@ __global__ void stats_finalize_kernel(const float2* __restrict__ part, float2* _
 // ---------------------------------------------------------------------------
 template <typename Tz>
 __global__ void rowstats_kernel(const Tz* __restrict__ Z, float2* __restrict__ stats, int B, int T, int D, int Bcap) {
+    pdl_wait();
+    pdl_launch_next();
     const int lane = threadIdx.x & 31;
     const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
@@ -941,6 +973,8 @@ pool_vec_kernel(const __half* __restrict__ Z, const float2* __restrict__ stats, 
     const int nwarps = blockDim.x >> 5;
     const int j = 8 * threadIdx.x;
     const size_t tstride = (size_t)Bcap * D;
+    pdl_wait();
+    pdl_launch_next();
     for (int b = blockIdx.x; b < B; b += gridDim.x) {
         for (int t = warp; t < T; t += nwarps) {
             float mean, rstd;
@@ -989,6 +1023,15 @@ pool_vec_kernel(const __half* __restrict__ Z, const float2* __restrict__ stats, 
 
 }  // namespace
 
+bool pdl_enabled() {
+    static int env = -1;
+    if (env < 0) {
+        const char* v = getenv("RM_PDL");
+        env = (v && v[0] == '0') ? 0 : 1;
+    }
+    return env == 1;
+}
+
 cudaError_t launch_mix_ln1(Act act, bool from_z, const MixLnArgs& a, int num_sms, cudaStream_t s) {
     if (a.B <= 0) return cudaSuccess;
     if (act == Act::BF16) {
@@ -1016,23 +1059,21 @@ cudaError_t launch_ln2_out(Act act, const void* Z, const float2* stats, const fl
     const int grid = grid_for((long long)B * T * 32, 256, num_sms * 8);
     if (act == Act::BF16 && D % 256 == 0) {
         if (out_f32)
-            ln2_out_vec_kernel<float><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2, (float*)X_out, B, T, D,
-                                                           Bcap, nchunk, cw, eps);
+            launch_k(ln2_out_vec_kernel<float>, dim3(grid), dim3(256), 0, s, (const __half*)Z, stats, g2, be2,
+                     (float*)X_out, B, T, D, Bcap, nchunk, cw, eps);
         else
-            ln2_out_vec_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2,
-                                                                   (__nv_bfloat16*)X_out, B, T, D, Bcap, nchunk, cw,
-                                                                   eps);
+            launch_k(ln2_out_vec_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, s, (const __half*)Z, stats, g2, be2,
+                     (__nv_bfloat16*)X_out, B, T, D, Bcap, nchunk, cw, eps);
     } else if (act == Act::BF16) {
         if (out_f32)
-            ln2_out_kernel<__half, float><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2, (float*)X_out, B, T,
-                                                               D, Bcap, nchunk, cw, eps);
+            launch_k(ln2_out_kernel<__half, float>, dim3(grid), dim3(256), 0, s, (const __half*)Z, stats, g2, be2,
+                     (float*)X_out, B, T, D, Bcap, nchunk, cw, eps);
         else
-            ln2_out_kernel<__half, __nv_bfloat16><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2,
-                                                                       (__nv_bfloat16*)X_out, B, T, D, Bcap, nchunk,
-                                                                       cw, eps);
+            launch_k(ln2_out_kernel<__half, __nv_bfloat16>, dim3(grid), dim3(256), 0, s, (const __half*)Z, stats, g2,
+                     be2, (__nv_bfloat16*)X_out, B, T, D, Bcap, nchunk, cw, eps);
     } else {
-        ln2_out_kernel<float, float><<<grid, 256, 0, s>>>((const float*)Z, stats, g2, be2, (float*)X_out, B, T, D,
-                                                          Bcap, nchunk, cw, eps);
+        launch_k(ln2_out_kernel<float, float>, dim3(grid), dim3(256), 0, s, (const float*)Z, stats, g2, be2,
+                 (float*)X_out, B, T, D, Bcap, nchunk, cw, eps);
     }
     return cudaGetLastError();
 }
@@ -1043,14 +1084,14 @@ cudaError_t launch_ln2_out_op(Act act, const void* Z, const float2* stats, int n
     if (B <= 0) return cudaSuccess;
     const int grid = grid_for((long long)B * T * 32, 256, num_sms * 8);
     if (act == Act::BF16 && D % 256 == 0)
-        ln2_out_vec_kernel<__half><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2, (__half*)X_out, B, T, D,
-                                                        Bcap, nchunk, cw, eps);
+        launch_k(ln2_out_vec_kernel<__half>, dim3(grid), dim3(256), 0, s, (const __half*)Z, stats, g2, be2,
+                 (__half*)X_out, B, T, D, Bcap, nchunk, cw, eps);
     else if (act == Act::BF16)
-        ln2_out_kernel<__half, __half><<<grid, 256, 0, s>>>((const __half*)Z, stats, g2, be2, (__half*)X_out, B, T, D,
-                                                            Bcap, nchunk, cw, eps);
+        launch_k(ln2_out_kernel<__half, __half>, dim3(grid), dim3(256), 0, s, (const __half*)Z, stats, g2, be2,
+                 (__half*)X_out, B, T, D, Bcap, nchunk, cw, eps);
     else
-        ln2_out_kernel<float, float><<<grid, 256, 0, s>>>((const float*)Z, stats, g2, be2, (float*)X_out, B, T, D,
-                                                          Bcap, nchunk, cw, eps);
+        launch_k(ln2_out_kernel<float, float>, dim3(grid), dim3(256), 0, s, (const float*)Z, stats, g2, be2,
+                 (float*)X_out, B, T, D, Bcap, nchunk, cw, eps);
     return cudaGetLastError();
 }
 
@@ -1063,29 +1104,28 @@ cudaError_t launch_pool(Act act, const void* Z, const float2* stats, const float
         int threads = (D / 8 + 31) / 32 * 32;
         if (threads < 64) threads = 64;
         const int grid = B < num_sms * 10 ? B : num_sms * 10;
-        pool_vec_kernel<kPoolBatch><<<grid, threads, 0, s>>>((const __half*)Z, stats, g2, be2, pooled, B, T, D, Bcap,
-                                                             nchunk, cw, eps);
+        launch_k(pool_vec_kernel<kPoolBatch>, dim3(grid), dim3(threads), 0, s, (const __half*)Z, stats, g2, be2,
+                 pooled, B, T, D, Bcap, nchunk, cw, eps);
         return cudaGetLastError();
     }
     const int grid = B < num_sms * 8 ? B : num_sms * 8;
     if (act == Act::BF16 && xl_f32)
-        pool_kernel<__half, float><<<grid, kPoolThreads, 0, s>>>((const __half*)Z, stats, g2, be2, pooled, (float*)XL,
-                                                                 B, T, D, Bcap, nchunk, cw, eps);
+        launch_k(pool_kernel<__half, float>, dim3(grid), dim3(kPoolThreads), 0, s, (const __half*)Z, stats, g2, be2,
+                 pooled, (float*)XL, B, T, D, Bcap, nchunk, cw, eps);
     else if (act == Act::BF16)
-        pool_kernel<__half, __nv_bfloat16><<<grid, kPoolThreads, 0, s>>>((const __half*)Z, stats, g2, be2, pooled,
-                                                                         (__nv_bfloat16*)XL, B, T, D, Bcap, nchunk,
-                                                                         cw, eps);
+        launch_k(pool_kernel<__half, __nv_bfloat16>, dim3(grid), dim3(kPoolThreads), 0, s, (const __half*)Z, stats,
+                 g2, be2, pooled, (__nv_bfloat16*)XL, B, T, D, Bcap, nchunk, cw, eps);
     else
-        pool_kernel<float, float><<<grid, kPoolThreads, 0, s>>>((const float*)Z, stats, g2, be2, pooled, (float*)XL,
-                                                                B, T, D, Bcap, nchunk, cw, eps);
+        launch_k(pool_kernel<float, float>, dim3(grid), dim3(kPoolThreads), 0, s, (const float*)Z, stats, g2, be2,
+                 pooled, (float*)XL, B, T, D, Bcap, nchunk, cw, eps);
     return cudaGetLastError();
 }
 
 cudaError_t launch_stats_finalize(const float2* part, float2* out, int B, int T, int Bcap, int nchunk, int cw,
                                   int num_sms, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
-    stats_finalize_kernel<<<grid_for((long long)B * T, 256, num_sms * 8), 256, 0, s>>>(part, out, B, T, Bcap, nchunk,
-                                                                                        cw);
+    launch_k(stats_finalize_kernel, dim3(grid_for((long long)B * T, 256, num_sms * 8)), dim3(256), 0, s, part, out, B,
+             T, Bcap, nchunk, cw);
     return cudaGetLastError();
 }
 
@@ -1094,9 +1134,9 @@ cudaError_t launch_rowstats(Act act, const void* Z, float2* stats, int B, int T,
     if (B <= 0) return cudaSuccess;
     const int grid = grid_for((long long)B * T * 32, 256, num_sms * 8);
     if (act == Act::BF16)
-        rowstats_kernel<__half><<<grid, 256, 0, s>>>((const __half*)Z, stats, B, T, D, Bcap);
+        launch_k(rowstats_kernel<__half>, dim3(grid), dim3(256), 0, s, (const __half*)Z, stats, B, T, D, Bcap);
     else
-        rowstats_kernel<float><<<grid, 256, 0, s>>>((const float*)Z, stats, B, T, D, Bcap);
+        launch_k(rowstats_kernel<float>, dim3(grid), dim3(256), 0, s, (const float*)Z, stats, B, T, D, Bcap);
     return cudaGetLastError();
 }
 

@@ -353,6 +353,8 @@ pffn_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
+    pdl_wait();              // operands and outputs are shared with the previous kernels of the stream
+    pdl_launch_next();
 
     const int kblocks = args.K / BK;
     const long long tiles =
@@ -572,6 +574,8 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
     cluster_sync_all();            // barriers and TMEM of both CTAs exist before any cross-CTA use
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
+    pdl_wait();              // operands and outputs are shared with the previous kernels of the stream
+    pdl_launch_next();
 
     const int kblocks = args.K / (BK * KSUB);
     const long long tiles =
@@ -808,8 +812,7 @@ cudaError_t run(const void* A, long long a_rows_total, const void* W, int n_wgro
     }
     long long grid = num_sms;
     if (a.tile_prefix == nullptr && a.tiles < grid) grid = a.tiles;
-    k<<<(int)grid, kThreads, C::SMEM_BYTES, s>>>(mA, mB, mC, a);
-    return cudaGetLastError();
+    return launch_k(k, dim3((unsigned)grid), dim3(kThreads), C::SMEM_BYTES, s, mA, mB, mC, a);
 }
 
 template <int EPI>
@@ -877,8 +880,7 @@ cudaError_t run_pair(const void* A, long long a_rows_total, const void* W, int n
         max_pairs = n;
     }
     long long pairs = (a.tile_prefix == nullptr && a.tiles < max_pairs) ? a.tiles : max_pairs;
-    k<<<(int)(2 * pairs), C::THREADS, C::SMEM_BYTES, s>>>(mA, mB, mC, a);
-    return cudaGetLastError();
+    return launch_k(k, dim3((unsigned)(2 * pairs)), dim3(C::THREADS), C::SMEM_BYTES, s, mA, mB, mC, a);
 }
 
 // Pair tiles (256 x BN per CTA pair) for both GEMMs when every token group
@@ -1050,6 +1052,8 @@ pffn_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
+    pdl_wait();              // operands and outputs are shared with the previous kernels of the stream
+    pdl_launch_next();
 
     const int kblocks = args.K / BK;
     const long long units = args.tiles;             // token groups x feature blocks
@@ -1237,8 +1241,7 @@ cudaError_t run_swap(const void* A, const void* W, int n_wgroups, Args a, int nu
         attr_done = true;
     }
     const long long grid = a.tiles < num_sms ? a.tiles : num_sms;
-    k<<<(int)grid, C::THREADS, C::SMEM_BYTES, s>>>(mW, mX, a);
-    return cudaGetLastError();
+    return launch_k(k, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM_BYTES, s, mW, mX, a);
 }
 
 template <int EPI>

@@ -26,6 +26,26 @@ inline size_t op_size(Act a) { return a == Act::F32 ? 4 : 2; }
 cudaError_t device_alloc(void** p, size_t bytes);
 void device_free(void* p);
 
+// Kernel launch with programmatic stream serialization (the kernel may begin
+// while the stream's previous kernel finishes; it must call pdl_wait() before
+// touching memory earlier work wrote or reads).  RM_PDL=0 in the environment
+// turns the attribute off (ordinary stream order; the same results).
+bool pdl_enabled();
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k, static_cast<Args&&>(args)...);
+}
+
 // Token-major workspace: element (t, b, j) of a [T][Bcap][W] buffer sits at
 // (t * Bcap + b) * W + j.
 
@@ -49,6 +69,8 @@ struct MixLnArgs {
     // test hook only (launch_mix_residual_debug): y = Mix(X) + X as float32,
     // token-major [T][Bcap][D], instead of S
     float* Ydbg;
+    // staged 8-wide kernel: CTAs per sample (set by its launcher; 0 or 1: one)
+    int rsplit;
 };
 
 // S = LN1(Mix(X) + X).
