@@ -153,33 +153,34 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// Merge per-chunk LayerNorm partials into row (mean, rstd).  Each chunk c of
-// width cw holds (mean_c, M2_c) with M2_c = sum over the chunk of (z - mean_c)^2.
-// Chan et al.'s pairwise update, written for equal chunk sizes:
-//   mean = (1/n) sum_c cw mean_c,  M2 = sum_c M2_c + cw sum_c (mean_c - mean)^2.
-// Called by a full warp; every lane returns the same values.  The summation
-// order is fixed (lane-strided, then a butterfly), so every kernel that calls
-// this for the same row gets bit-identical results.
+// Merge per-chunk LayerNorm partials into the row's (mean, M2).  Each chunk c
+// of width cw holds (mean_c, M2_c) with M2_c = sum over the chunk of
+// (z - mean_c)^2.  Chan et al.'s pairwise update, written for equal chunk
+// sizes:  mean = (1/nchunk) sum_c mean_c,  M2 = sum_c (M2_c + cw (mean_c - mean)^2).
+// The sums run over c in order with explicit fused multiply-adds, so that every
+// kernel that merges a row (the merge kernel, or a consumer that merges the
+// partials itself) gets the same bits.
+__device__ __forceinline__ float2 merge_chunks(const float2* __restrict__ st, int nchunk, int cw) {
+    float s = 0.f;
+    for (int c = 0; c < nchunk; ++c) s = __fadd_rn(s, st[c].x);
+    const float mean = __fdiv_rn(s, (float)nchunk);
+    float m2 = 0.f;
+    for (int c = 0; c < nchunk; ++c) {
+        const float2 v = st[c];
+        const float d = __fsub_rn(v.x, mean);
+        m2 = __fadd_rn(m2, __fmaf_rn(__fmul_rn((float)cw, d), d, v.y));
+    }
+    return make_float2(mean, m2);
+}
+
+// Row (mean, rstd) from nchunk partials (nchunk = 1: already merged).  Every
+// lane of the calling warp returns the same values.
 __device__ __forceinline__ void merge_row_stats(const float2* __restrict__ st, int nchunk, int cw, int D,
                                                 float eps, int lane, float& mean, float& rstd) {
-    if (nchunk == 1) {           // already merged: (mean, M2) of the whole row
-        const float2 v = st[0];
-        mean = v.x;
-        rstd = rsqrtf(v.y / (float)D + eps);
-        return;
-    }
-    float s = 0.f;
-    for (int c = lane; c < nchunk; c += 32) s += st[c].x;
-    s = warp_sum(s);
-    mean = s * (float)cw / (float)D;
-    float m2 = 0.f;
-    for (int c = lane; c < nchunk; c += 32) {
-        const float2 v = st[c];
-        const float d = v.x - mean;
-        m2 += v.y + (float)cw * d * d;
-    }
-    m2 = warp_sum(m2);
-    rstd = rsqrtf(m2 / (float)D + eps);
+    (void)lane;
+    const float2 v = nchunk == 1 ? st[0] : merge_chunks(st, nchunk, cw);
+    mean = v.x;
+    rstd = rsqrtf(v.y / (float)D + eps);
 }
 
 // ---------------------------------------------------------------------------

@@ -816,8 +816,9 @@ pool_kernel(const Tz* __restrict__ Z, const float2* __restrict__ stats, const fl
 
 // ---------------------------------------------------------------------------
 // (mean, M2) of each full row from its nchunk chunk partials (mean, M2 over cw
-// columns each), merged by Chan's formula; one thread per row (the rows of the
-// first B samples of every token).  Consumers then read one value per row.
+// columns each), merged by Chan's formula (merge_chunks, the same bits as a
+// consumer that merges the partials itself); one thread per row (the rows of
+// the first B samples of every token).  Consumers then read one value per row.
 // ---------------------------------------------------------------------------
 __global__ void stats_finalize_kernel(const float2* __restrict__ part, float2* __restrict__ out, int B, int T,
                                       int Bcap, int nchunk, int cw) {
@@ -826,16 +827,7 @@ __global__ void stats_finalize_kernel(const float2* __restrict__ part, float2* _
     const long long n = (long long)T * B;
     for (long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x; r < n; r += (long long)gridDim.x * blockDim.x) {
         const int t = (int)(r / B), b = (int)(r % B);
-        const float2* p = part + ((size_t)t * Bcap + b) * nchunk;
-        float s = 0.f;
-        for (int c = 0; c < nchunk; ++c) s += p[c].x;
-        const float mean = s / (float)nchunk;
-        float m2 = 0.f;
-        for (int c = 0; c < nchunk; ++c) {
-            const float d = p[c].x - mean;
-            m2 += p[c].y + (float)cw * d * d;
-        }
-        out[(size_t)t * Bcap + b] = make_float2(mean, m2);
+        out[(size_t)t * Bcap + b] = merge_chunks(part + ((size_t)t * Bcap + b) * nchunk, nchunk, cw);
     }
 }
 

@@ -967,8 +967,10 @@ cudaError_t run_pair_bn(int bn, bool k2, const void* A, long long a_rows_total, 
 //   warp 0      TMA producer
 //   warp 1      MMA issuer (one thread)
 //   warp 2      TMEM allocator
-//   warps 4-7   epilogue: warp 4 + q reads TMEM lanes 32 q .. 32 q + 31 (one
-//               feature per lane) and the NB batch columns; GEMM1 stores
+//   warps 4..   epilogue, 4 warps (8 for NB >= 64, two per TMEM lane quadrant
+//               splitting the columns): warp 4 + e reads TMEM lanes 32 q .. 32 q
+//               + 31 (q = e mod 4, one feature per lane) and its share of the NB
+//               batch columns; GEMM1 stores
 //               Gelu(acc + b1) per (row, feature), GEMM2 stores acc + b2 + S and
 //               the (mean, M2) of each row over the unit's 128 features (the
 //               128-column statistics chunk of the two-phase LN2), the four
@@ -981,7 +983,9 @@ struct CfgS {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = (200 * 1024) / STAGE_BYTES > 12 ? 12 : (200 * 1024) / STAGE_BYTES;
     static constexpr int TMEM_COLS = 2 * NB < 32 ? 32 : 2 * NB;
-    static constexpr int THREADS = 256;
+    static constexpr int EPW = NB >= 64 ? 8 : 4;             // epilogue warps
+    static constexpr int CPW = NB / (EPW / 4);               // batch columns per epilogue warp
+    static constexpr int THREADS = 128 + 32 * EPW;
     static constexpr int BAR_BYTES = 256;
     static constexpr int STAT_BYTES = 2 * 2 * 4 * NB * 4;     // (mean, M2) x 2 buffers x 4 warps x NB
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + STAT_BYTES;
@@ -1039,7 +1043,7 @@ pffn_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), 4);
+            mbar_init(tempty_bar(a), C::EPW);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -1126,7 +1130,9 @@ pffn_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
         }
     } else if (warp >= 4) {
         // ------------------------------ epilogue ----------------------------------
-        const int q = warp & 3;
+        const int e = warp - 4;
+        const int q = warp & 3;                       // TMEM lane quadrant
+        const int col0 = (e >> 2) * C::CPW;           // this warp's first batch column
         int acc = 0;
         uint32_t acc_phase = 0;
         for (long long u = blockIdx.x; u < units; u += gridDim.x) {
@@ -1142,32 +1148,38 @@ pffn_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
             float* st_mean = s_stat + (size_t)acc * 2 * 4 * NB + (size_t)q * NB;
             float* st_m2 = st_mean + 4 * NB;
 #pragma unroll 1
-            for (int c = 0; c < NB / CW; ++c) {
+            for (int c = col0; c < col0 + C::CPW && c < args.M; c += CW) {
                 float v[CW];
                 if constexpr (CW == 32) {
-                    tmem_ld32(tbase + 32u * c, v);
+                    tmem_ld32(tbase + (uint32_t)c, v);
                 } else {
-                    tmem_ld16(tbase + 16u * c, v);
+                    tmem_ld16(tbase + (uint32_t)c, v);
                 }
-                // the residuals of the chunk's rows first, all loads in flight together
-                float rres[EPI == EPI_RESID ? CW : 1];
-                if (EPI == EPI_RESID) {
+                if (EPI == EPI_GELU) {
+                    // two batch rows at a time through the packed GELU
+#pragma unroll
+                    for (int i = 0; i < CW; i += 2) {
+                        const int b = c + i;                               // batch row (warp-uniform)
+                        if (b >= args.M) break;
+                        float g0, g1;
+                        f2_unpack(gelu_erf_x2(f2_pack(v[i], v[i + 1]), f2_splat(bf)), g0, g1);
+                        args.hid[(row0 + b) * (size_t)args.N + f] = __float2half_rn(sat_f16(g0));
+                        if (b + 1 < args.M) args.hid[(row0 + b + 1) * (size_t)args.N + f] = __float2half_rn(sat_f16(g1));
+                    }
+                } else {   // EPI_RESID
+                    // the residuals of the chunk's rows first, all loads in flight together
+                    float rres[CW];
 #pragma unroll
                     for (int i = 0; i < CW; ++i) {
-                        const int b = c * CW + i;
+                        const int b = c + i;
                         rres[i] = b < args.M ? __half2float(args.resid[(row0 + b) * (size_t)args.N + f]) : 0.f;
                     }
-                }
 #pragma unroll
-                for (int i = 0; i < CW; ++i) {
-                    const int b = c * CW + i;                              // batch row (warp-uniform)
-                    if (b >= args.M) break;
-                    const size_t o = (row0 + b) * (size_t)args.N + f;
-                    if (EPI == EPI_GELU) {
-                        args.hid[o] = __float2half_rn(sat_f16(gelu_erf(v[i] + bf)));
-                    } else {   // EPI_RESID
+                    for (int i = 0; i < CW; ++i) {
+                        const int b = c + i;                               // batch row (warp-uniform)
+                        if (b >= args.M) break;
                         const float z = v[i] + bf + rres[i];
-                        args.z[o] = __float2half_rn(sat_f16(z));
+                        args.z[(row0 + b) * (size_t)args.N + f] = __float2half_rn(sat_f16(z));
                         // this warp's 32 features: mean and M2 about it
                         const float mw = warp_sum(z) * (1.0f / 32.0f);
                         const float d = z - mw;
@@ -1180,12 +1192,13 @@ pffn_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
                 }
             }
             if (EPI == EPI_RESID) {
-                // the four warps' moments -> (mean, M2) of the 128 features, one lane per row
-                asm volatile("bar.sync 1, 128;" ::: "memory");
+                // the four quadrants' moments -> (mean, M2) of the 128 features, one lane
+                // per row, each q = 0 warp for its own columns
+                asm volatile("bar.sync 1, %0;" ::"r"(C::EPW * 32) : "memory");
                 if (q == 0) {
                     const float* sm = s_stat + (size_t)acc * 2 * 4 * NB;
                     const float* s2 = sm + 4 * NB;
-                    for (int b = lane; b < args.M && b < NB; b += 32) {
+                    for (int b = col0 + lane; b < args.M && b < col0 + C::CPW; b += 32) {
                         const float m0 = sm[b], m1 = sm[NB + b], m2 = sm[2 * NB + b], m3 = sm[3 * NB + b];
                         const float mean = 0.25f * (m0 + m1 + m2 + m3);
                         const float d0 = m0 - mean, d1 = m1 - mean, d2 = m2 - mean, d3 = m3 - mean;
