@@ -221,6 +221,25 @@ RM_API rm_status rm_stack_forward(rm_ctx *ctx, const void *X0, float *pooled, vo
  * streams); pinned host buffers let the copies run asynchronously. */
 RM_API rm_status rm_stack_forward_host(rm_ctx *ctx, const void *X0_host, float *pooled_host, int B, void *stream);
 
+/* Pipelined host entry for a stream of batches (serving): enqueue the stack
+ * forward of one batch and return without waiting.  The copy of X0_host
+ * ([B][T][D], context dtype) to the device runs on a context-owned copy stream
+ * while the previously enqueued batch computes on `stream`; the pooled float32
+ * [B][D] result is copied to pooled_host on a second copy stream.  *ticket
+ * receives the batch's number; rm_host_wait(ctx, ticket) returns once its
+ * pooled_host is written.  Two batches can be in flight (two device staging
+ * buffers of max_batch samples, allocated at the first call): a call whose
+ * slot still holds the batch two calls back first waits for that batch.  The
+ * caller keeps X0_host and pooled_host alive and unmodified until the ticket
+ * has been waited for (pinned host memory lets the copies run asynchronously).
+ * One batch's arithmetic is that of rm_stack_forward for the same B.
+ * rm_host_wait: RM_ERR_INVALID_ARG for a ticket this context never issued;
+ * waiting twice, or for a batch that a later call already waited for, returns
+ * RM_OK at once. */
+RM_API rm_status rm_stack_forward_host_async(rm_ctx *ctx, const void *X0_host, float *pooled_host, int B,
+                                             void *stream, long long *ticket);
+RM_API rm_status rm_host_wait(rm_ctx *ctx, long long ticket);
+
 /* Sparse-MoE per-token FFN of layer `layer` ("RankMixer" Eq. 10, inference
  * router): V[b,t] = sum_e G[b,t,e] * FFN_{t,e}(S[b,t]) with
  * G = ReLU(S[b,t] Wg_t + bg_t).  Only experts with G > 0 are computed.

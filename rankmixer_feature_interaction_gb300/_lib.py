@@ -45,7 +45,7 @@ EXPORTED = ["rm_create", "rm_destroy", "rm_block_forward", "rm_stack_forward", "
             "rm_debug_gelu_grad", "rm_stack_forward_train", "rm_stack_backward_saved", "rm_head_forward",
             "rm_set_tokenizer", "rm_tokenize", "rm_score", "rm_moe_pffn_forward_train", "rm_tokenize_backward",
             "rm_set_unimixing", "rm_unimixing_weights", "rm_unimixing", "rm_debug_mix_residual",
-            "rm_debug_fail_alloc", "rm_debug_alloc_stats"]
+            "rm_debug_fail_alloc", "rm_debug_alloc_stats", "rm_stack_forward_host_async", "rm_host_wait"]
 
 
 class rm_config(ctypes.Structure):
@@ -103,6 +103,8 @@ def load() -> ctypes.CDLL:
         "rm_block_forward": (st, [vp, i, vp, vp, vp, i, i, vp]),
         "rm_stack_forward": (st, [vp, vp, vp, vp, i, i, vp]),
         "rm_stack_forward_host": (st, [vp, vp, vp, i, vp]),
+        "rm_stack_forward_host_async": (st, [vp, vp, vp, i, vp, ctypes.POINTER(ctypes.c_longlong)]),
+        "rm_host_wait": (st, [vp, ctypes.c_longlong]),
         "rm_moe_pffn_forward": (st, [vp, i, vp, vp, vp, i, vp]),
         "rm_token_mix": (st, [vp, vp, i, i, i, i, i, vp]),
         "rm_sync_status": (st, [vp, vp]),
@@ -174,6 +176,17 @@ def rm_stack_forward(ctx: int, X0: int, pooled: int, XL: int | None, xl_dtype: i
 
 def rm_stack_forward_host(ctx: int, X0_host: int, pooled_host: int, B: int, stream: int) -> None:
     check(load().rm_stack_forward_host(ctx, X0_host, pooled_host, B, stream), "rm_stack_forward_host")
+
+
+def rm_stack_forward_host_async(ctx: int, X0_host: int, pooled_host: int, B: int, stream: int) -> int:
+    t = ctypes.c_longlong(-1)
+    check(load().rm_stack_forward_host_async(ctx, X0_host, pooled_host, B, stream, ctypes.byref(t)),
+          "rm_stack_forward_host_async")
+    return t.value
+
+
+def rm_host_wait(ctx: int, ticket: int) -> None:
+    check(load().rm_host_wait(ctx, ticket), "rm_host_wait")
 
 
 def rm_moe_pffn_forward(ctx: int, layer: int, S: int, V_out: int, gates: int | None, B: int, stream: int) -> None:

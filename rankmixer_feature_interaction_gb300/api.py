@@ -115,6 +115,17 @@ class RankMixer:
         _lib.rm_stack_forward_host(self.ctx, _ptr(X0_host), _ptr(pooled_host), B, _stream())
         return pooled_host
 
+    def stack_forward_host_async(self, X0_host: torch.Tensor, pooled_host: torch.Tensor) -> int:
+        """Enqueue the stack forward of a host batch (pinned CPU tensors; the copy in runs while
+        the previous batch computes); returns a ticket for host_wait.  Keep both tensors alive
+        and unmodified until the ticket has been waited for."""
+        return _lib.rm_stack_forward_host_async(self.ctx, _ptr(X0_host), _ptr(pooled_host), X0_host.shape[0],
+                                                _stream())
+
+    def host_wait(self, ticket: int) -> None:
+        """Return once the batch of `ticket` has its pooled output in its host tensor."""
+        _lib.rm_host_wait(self.ctx, ticket)
+
     def moe_pffn_forward(self, layer: int, S: torch.Tensor, V: torch.Tensor | None = None,
                          return_gates: bool = False):
         B = S.shape[0]

@@ -220,6 +220,14 @@ struct rm_ctx {
     float* pooled_dev = nullptr;
     cudaStream_t s_in = nullptr, s_out = nullptr;
     cudaEvent_t ev_in[kHostChunksMax] = {}, ev_done[kHostChunksMax] = {};
+    // pipelined host entry (rm_stack_forward_host_async): two device staging
+    // slots, each with its copy-in, compute and copy-out events, and the ticket
+    // that holds it (-1: free)
+    void* hx_dev[2] = {};
+    float* hp_dev[2] = {};
+    cudaEvent_t hx_in[2] = {}, hx_done[2] = {}, hx_out[2] = {};
+    long long h_next = 0;
+    long long h_slot[2] = {-1, -1};
     // error word and the debug flag nothing sets
     int* d_err = nullptr;
     int* d_flag = nullptr;
@@ -246,6 +254,32 @@ rm_status dmalloc(rm_ctx* c, void** p, size_t bytes, long long* counter) {
     }
     if (counter) *counter += (long long)bytes;
     (void)c;
+    return RM_OK;
+}
+
+rm_status cuda_fail(cudaError_t e, const char* what);
+
+// The host entries' two copy streams and per-chunk events (created at first use).
+rm_status copy_streams(rm_ctx* c) {
+    if (c->s_in) return RM_OK;
+    cudaError_t e = cudaStreamCreateWithFlags(&c->s_in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->s_out, cudaStreamNonBlocking);
+    for (int i = 0; e == cudaSuccess && i < kHostChunksMax; ++i) {
+        e = cudaEventCreateWithFlags(&c->ev_in[i], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->ev_done[i], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) {
+        // leave nothing half made: the next call starts again
+        if (c->s_in) cudaStreamDestroy(c->s_in);
+        if (c->s_out) cudaStreamDestroy(c->s_out);
+        c->s_in = c->s_out = nullptr;
+        for (int i = 0; i < kHostChunksMax; ++i) {
+            if (c->ev_in[i]) cudaEventDestroy(c->ev_in[i]);
+            if (c->ev_done[i]) cudaEventDestroy(c->ev_done[i]);
+            c->ev_in[i] = c->ev_done[i] = nullptr;
+        }
+        return cuda_fail(e, "copy streams");
+    }
     return RM_OK;
 }
 
@@ -287,6 +321,13 @@ void free_ctx(rm_ctx* c) {
     for (int i = 0; i < kHostChunksMax; ++i) {
         if (c->ev_in[i]) cudaEventDestroy(c->ev_in[i]);
         if (c->ev_done[i]) cudaEventDestroy(c->ev_done[i]);
+    }
+    for (int k = 0; k < 2; ++k) {
+        device_free(c->hx_dev[k]);
+        device_free(c->hp_dev[k]);
+        if (c->hx_in[k]) cudaEventDestroy(c->hx_in[k]);
+        if (c->hx_done[k]) cudaEventDestroy(c->hx_done[k]);
+        if (c->hx_out[k]) cudaEventDestroy(c->hx_out[k]);
     }
     if (c->s_in) cudaStreamDestroy(c->s_in);
     if (c->s_out) cudaStreamDestroy(c->s_out);
@@ -1036,6 +1077,58 @@ rm_status rm_stack_forward(rm_ctx* c, const void* X0, float* pooled, void* XL, r
     return stack_device(c, X0, pooled, XL, xl_f32, B, as_stream(stream));
 }
 
+rm_status rm_stack_forward_host_async(rm_ctx* c, const void* X0_host, float* pooled_host, int B, void* stream,
+                                      long long* ticket) {
+    rm_status st;
+    if ((st = check_ctx(c)) != RM_OK) return st;
+    if ((st = check_batch(c, B)) != RM_OK) return st;
+    if (!X0_host || !pooled_host || !ticket) return fail(RM_ERR_INVALID_ARG, "X0_host / pooled_host / ticket is NULL");
+    cudaSetDevice(c->device);
+    const rm_config& g = c->cfg;
+    const size_t row_in = (size_t)g.T * g.D * c->esz, row_out = (size_t)g.D * 4;
+    if ((st = copy_streams(c)) != RM_OK) return st;
+    const int k = (int)(c->h_next & 1);
+    if ((st = ensure(c, &c->hx_dev[k], (size_t)c->Bcap * row_in, &c->ws_bytes)) != RM_OK) return st;
+    if ((st = ensure(c, (void**)&c->hp_dev[k], (size_t)c->Bcap * row_out, &c->ws_bytes)) != RM_OK) return st;
+    if (!c->hx_in[k]) {
+        RM_CHECK_CUDA(cudaEventCreateWithFlags(&c->hx_in[k], cudaEventDisableTiming), "event");
+        RM_CHECK_CUDA(cudaEventCreateWithFlags(&c->hx_done[k], cudaEventDisableTiming), "event");
+        RM_CHECK_CUDA(cudaEventCreateWithFlags(&c->hx_out[k], cudaEventDisableTiming), "event");
+    }
+    if (c->h_slot[k] >= 0) {            // the batch two calls back still holds this slot
+        RM_CHECK_CUDA(cudaEventSynchronize(c->hx_out[k]), "wait for the slot's previous batch");
+        c->h_slot[k] = -1;
+    }
+    cudaStream_t s = as_stream(stream);
+    // the copy runs on its own stream while the previous batch computes on `stream`
+    RM_CHECK_CUDA(cudaMemcpyAsync(c->hx_dev[k], X0_host, (size_t)B * row_in, cudaMemcpyHostToDevice, c->s_in),
+                  "H2D X0");
+    RM_CHECK_CUDA(cudaEventRecord(c->hx_in[k], c->s_in), "event");
+    RM_CHECK_CUDA(cudaStreamWaitEvent(s, c->hx_in[k], 0), "wait");
+    if ((st = stack_device(c, c->hx_dev[k], c->hp_dev[k], nullptr, false, B, s)) != RM_OK) return st;
+    RM_CHECK_CUDA(cudaEventRecord(c->hx_done[k], s), "event");
+    RM_CHECK_CUDA(cudaStreamWaitEvent(c->s_out, c->hx_done[k], 0), "wait");
+    RM_CHECK_CUDA(cudaMemcpyAsync(pooled_host, c->hp_dev[k], (size_t)B * row_out, cudaMemcpyDeviceToHost, c->s_out),
+                  "D2H pooled");
+    RM_CHECK_CUDA(cudaEventRecord(c->hx_out[k], c->s_out), "event");
+    c->h_slot[k] = c->h_next;
+    *ticket = c->h_next++;
+    return RM_OK;
+}
+
+rm_status rm_host_wait(rm_ctx* c, long long ticket) {
+    rm_status st;
+    if ((st = check_ctx(c)) != RM_OK) return st;
+    if (ticket < 0 || ticket >= c->h_next)
+        return fail(RM_ERR_INVALID_ARG, "ticket %lld was not issued by this context", ticket);
+    const int k = (int)(ticket & 1);
+    if (c->h_slot[k] != ticket) return RM_OK;      // already waited for, or its slot has been reused since
+    cudaSetDevice(c->device);
+    RM_CHECK_CUDA(cudaEventSynchronize(c->hx_out[k]), "wait for the batch");
+    c->h_slot[k] = -1;
+    return RM_OK;
+}
+
 rm_status rm_stack_forward_host(rm_ctx* c, const void* X0_host, float* pooled_host, int B, void* stream) {
     rm_status st;
     if ((st = check_ctx(c)) != RM_OK) return st;
@@ -1084,14 +1177,7 @@ rm_status rm_stack_forward_host(rm_ctx* c, const void* X0_host, float* pooled_ho
         RM_CHECK_CUDA(cudaStreamSynchronize(s), "stream sync");
         return RM_OK;
     }
-    if (!c->s_in) {
-        RM_CHECK_CUDA(cudaStreamCreateWithFlags(&c->s_in, cudaStreamNonBlocking), "copy stream");
-        RM_CHECK_CUDA(cudaStreamCreateWithFlags(&c->s_out, cudaStreamNonBlocking), "copy stream");
-        for (int i = 0; i < kHostChunksMax; ++i) {
-            RM_CHECK_CUDA(cudaEventCreateWithFlags(&c->ev_in[i], cudaEventDisableTiming), "event");
-            RM_CHECK_CUDA(cudaEventCreateWithFlags(&c->ev_done[i], cudaEventDisableTiming), "event");
-        }
-    }
+    if ((st = copy_streams(c)) != RM_OK) return st;
     // the staging buffers may still be read by an earlier call's work on `stream`
     RM_CHECK_CUDA(cudaEventRecord(c->ev_done[0], s), "event");
     RM_CHECK_CUDA(cudaStreamWaitEvent(c->s_in, c->ev_done[0], 0), "wait");

@@ -521,3 +521,35 @@ def test_every_gemm_tile_dispatch(tuning):
     r = subprocess.run([sys.executable, "-c", _DISPATCH_CHILD.format(root=root, shapes=_DISPATCH_SHAPES)], env=env,
                        cwd=root, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
+
+
+def test_pipelined_host_entry():
+    """Batches enqueued back to back through the pipelined host entry (copy of batch n + 1
+    while batch n computes, two in flight) give each batch the device call's result, bit
+    for bit; tickets can be waited for late, twice, or not at all before their slot is
+    reused."""
+    T, D, k, L, B = 8, 512, 4, 2, 300
+    m, layers, _ = _build(T, D, k, L, B, 29, "bf16")
+    Xs = [synth.make_input(B, T, D, 300 + i, "bf16", DEV) for i in range(5)]
+    want = [m.stack_forward(X).cpu() for X in Xs]
+    Xh = [X.cpu().pin_memory() for X in Xs]
+    outs = [torch.empty((B, D), dtype=torch.float32).pin_memory() for _ in Xs]
+    tickets = []
+    for i in range(len(Xs)):
+        tickets.append(m.stack_forward_host_async(Xh[i], outs[i]))
+        if i >= 1:
+            m.host_wait(tickets[i - 1])
+            assert torch.equal(outs[i - 1], want[i - 1]), f"batch {i - 1}"
+    m.host_wait(tickets[-1])
+    m.host_wait(tickets[-1])                  # twice: returns at once
+    m.host_wait(tickets[0])                   # long since waited for
+    assert torch.equal(outs[-1], want[-1])
+    t = m.stack_forward_host_async(Xh[0], outs[0])     # a new batch into a reused slot, never waited
+    t2 = m.stack_forward_host_async(Xh[1], outs[1])
+    m.host_wait(t2)
+    m.host_wait(t)
+    assert torch.equal(outs[0], want[0]) and torch.equal(outs[1], want[1])
+    with pytest.raises(_lib.RankMixerError) as e:
+        m.host_wait(t2 + 5)
+    assert e.value.status == _lib.RM_ERR_INVALID_ARG
+    assert m.sync_status() == _lib.RM_OK
