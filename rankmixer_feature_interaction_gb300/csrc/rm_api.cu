@@ -12,6 +12,8 @@
 #include <unordered_map>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/rankmixer.h"
 #include "rm_internal.h"
 #include "rm_moe.h"
@@ -337,12 +339,33 @@ void free_ctx(rm_ctx* c) {
 }
 
 // ---- profiling --------------------------------------------------------------
+// NVTX ranges around each kernel class's launches (host timeline, for nsys and
+// similar tools), when RM_NVTX=1 is in the environment; names as in rm_kernel_kind.
+const char* const kKindNames[RM_K_COUNT] = {
+    "rm:mix_ln1", "rm:gemm1", "rm:gemm2", "rm:ln2_out", "rm:pool", "rm:rowstats", "rm:moe_route", "rm:moe_gemm1",
+    "rm:moe_gemm2", "rm:misc", "rm:moe_combine", "rm:bwd_recompute", "rm:bwd_dgrad", "rm:bwd_wgrad",
+    "rm:bwd_rows", "rm:tokenize", "rm:head", "rm:unimix"};
+
+bool nvtx_on() {
+    static int env = -1;
+    if (env < 0) {
+        const char* v = getenv("RM_NVTX");
+        env = (v && v[0] == '1') ? 1 : 0;
+    }
+    return env == 1;
+}
+
 struct ProfScope {
     rm_ctx* c;
     int kind;
     cudaStream_t s;
     int idx = -1;
+    bool nvtx = false;
     ProfScope(rm_ctx* c_, int kind_, cudaStream_t s_) : c(c_), kind(kind_), s(s_) {
+        if (nvtx_on() && kind >= 0 && kind < RM_K_COUNT) {
+            nvtxRangePushA(kKindNames[kind]);
+            nvtx = true;
+        }
         if (!c->prof) return;
         if (c->ev_used.size() >= c->ev_pool.size()) {
             Event e;
@@ -355,6 +378,7 @@ struct ProfScope {
     }
     ~ProfScope() {
         if (idx >= 0) cudaEventRecord(c->ev_pool[idx].b, s);
+        if (nvtx) nvtxRangePop();
     }
 };
 
