@@ -238,21 +238,17 @@ __device__ __forceinline__ uint64_t pair16_to_f2(uint32_t w) {
     }
 }
 
-// NBUF row buffers, the four fp16 affines, two mbarriers, the row mean / rstd
+// Two row buffers, the four fp16 affines, two mbarriers, the row mean / rstd
 // arrays and the abort flag.
-size_t v8_smem_bytes(int nbuf, int T, int D, int q) {
-    return (size_t)nbuf * T * v8_row_stride(D, q) * 2 + 4 * (size_t)D * 2 + 16 + 2 * kMaxT * 4 + 16;
+size_t v8_smem_bytes(int T, int D, int q) {
+    return 2 * (size_t)T * v8_row_stride(D, q) * 2 + 4 * (size_t)D * 2 + 16 + 2 * kMaxT * 4 + 16;
 }
 
 // DBG (test hook): write the residual sum y = Mix(X) + X as float32 to
 // a.Ydbg instead of LN1; with FROM_Z the LN2 finalisation runs with mean 0,
 // rstd 1, gamma 1, beta 0 (the identity on fp16 values), so the gather and
 // the fp16 sum are checked bit for bit.
-// NBUF = 2: one CTA per SM, the next sample's copy overlapping this sample's
-// work; NBUF = 1: one buffer per CTA and two CTAs per SM, each CTA copying its
-// next sample after it has finished with the current one (the other CTA's work
-// covers the copy).
-template <bool FROM_Z, int NV, bool DBG = false, int NBUF = 2>
+template <bool FROM_Z, int NV, bool DBG = false>
 __global__ void __launch_bounds__(512)
 mix_ln1_v8_kernel(const MixLnArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -260,8 +256,8 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
     const int RS = v8_row_stride(D, q);
     const uint32_t row_bytes = (uint32_t)D * 2u;
     const uint32_t buf_elems = (uint32_t)T * RS;
-    uint16_t* buf = reinterpret_cast<uint16_t*>(smem);                       // [NBUF][T][RS] 16-bit
-    __half* sg1 = reinterpret_cast<__half*>(smem + 2 * NBUF * (size_t)buf_elems);   // [D] each
+    uint16_t* buf = reinterpret_cast<uint16_t*>(smem);                       // [2][T][RS] 16-bit
+    __half* sg1 = reinterpret_cast<__half*>(smem + 4 * (size_t)buf_elems);    // [D] each
     __half* sb1 = sg1 + D;
     __half* sg2 = sb1 + D;                                                    // FROM_Z only
     __half* sb2 = sg2 + D;
@@ -327,8 +323,8 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
     for (int w = blockIdx.x; w < nitems; w += gridDim.x, ++it) {
         const int b = w / rsplit, part = w - b * rsplit;
         const int bn = (w + (int)gridDim.x) / rsplit;          // sample of this CTA's next item
-        const int slot = NBUF == 2 ? (it & 1) : 0;
-        if (NBUF == 2 && warp == 0 && w + (int)gridDim.x < nitems) issue(bn, slot ^ 1);
+        const int slot = it & 1;
+        if (warp == 0 && w + (int)gridDim.x < nitems) issue(bn, slot ^ 1);
         if (merged) {
             if (pre_lane && DBG) {
                 s_mean[pre_t] = 0.0f;
@@ -341,8 +337,7 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
         } else if (FROM_Z) {
             sample_row_stats(a, b, s_mean, s_rstd, warp, nwarps, lane);
         }
-        mbar_wait_bounded(smem_u32(&bars[slot]), NBUF == 2 ? ((uint32_t)(it >> 1) & 1u) : ((uint32_t)it & 1u),
-                          s_abort, a.err, a.timeout_ns);
+        mbar_wait_bounded(smem_u32(&bars[slot]), (uint32_t)(it >> 1) & 1u, s_abort, a.err, a.timeout_ns);
         __syncthreads();
         if (*s_abort) break;
         uint16_t* xs = buf + (size_t)slot * buf_elems;
@@ -452,30 +447,17 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
                 }
         }
         __syncthreads();    // the slot and the row statistics are reused by later samples
-        if (NBUF == 1 && warp == 0 && w + (int)gridDim.x < nitems) issue(bn, 0);
     }
 }
 
 bool v8_ok(bool, const MixLnArgs& a) {
-    return a.q % 8 == 0 && a.D % 256 == 0 && a.D <= 3072 && a.T <= kMaxT &&
-           v8_smem_bytes(2, a.T, a.D, a.q) <= 226 * 1024;
+    return a.q % 8 == 0 && a.D % 256 == 0 && a.D <= 3072 && a.T <= kMaxT && v8_smem_bytes(a.T, a.D, a.q) <= 226 * 1024;
 }
 
-// Buffers per CTA of the staged mixing kernel: RM_MIX_NBUF=1|2 in the
-// environment (a tuning switch; the same result either way), else 2.
-int mix_nbuf() {
-    static int env = -1;
-    if (env < 0) {
-        const char* v = getenv("RM_MIX_NBUF");
-        env = (v && v[0] == '1') ? 1 : 2;
-    }
-    return env;
-}
-
-template <bool FROM_Z, int NV, bool DBG = false, int NBUF = 2>
+template <bool FROM_Z, int NV, bool DBG = false>
 cudaError_t launch_v8(const MixLnArgs& a, int num_sms, cudaStream_t s) {
-    auto k = mix_ln1_v8_kernel<FROM_Z, NV, DBG, NBUF>;
-    const size_t smem = v8_smem_bytes(NBUF, a.T, a.D, a.q);
+    auto k = mix_ln1_v8_kernel<FROM_Z, NV, DBG>;
+    const size_t smem = v8_smem_bytes(a.T, a.D, a.q);
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     int threads = 32 * (a.T < 16 ? a.T : 16);
@@ -499,22 +481,16 @@ cudaError_t launch_v8(const MixLnArgs& a, int num_sms, cudaStream_t s) {
     return launch_k(k, dim3(grid), dim3(threads), smem, s, b);
 }
 
-template <bool FROM_Z, bool DBG, int NBUF>
-cudaError_t launch_v8_nv(const MixLnArgs& a, int num_sms, cudaStream_t s) {
-    const int nv = a.D / 256;
-    if (nv <= 1) return launch_v8<FROM_Z, 1, DBG, NBUF>(a, num_sms, s);
-    if (nv <= 2) return launch_v8<FROM_Z, 2, DBG, NBUF>(a, num_sms, s);
-    if (nv <= 3) return launch_v8<FROM_Z, 3, DBG, NBUF>(a, num_sms, s);
-    if (nv <= 4) return launch_v8<FROM_Z, 4, DBG, NBUF>(a, num_sms, s);
-    if (nv <= 6) return launch_v8<FROM_Z, 6, DBG, NBUF>(a, num_sms, s);
-    if (nv <= 8) return launch_v8<FROM_Z, 8, DBG, NBUF>(a, num_sms, s);
-    return launch_v8<FROM_Z, 12, DBG, NBUF>(a, num_sms, s);
-}
-
 template <bool FROM_Z, bool DBG = false>
 cudaError_t launch_v8_dispatch(const MixLnArgs& a, int num_sms, cudaStream_t s) {
-    if (mix_nbuf() == 1) return launch_v8_nv<FROM_Z, DBG, 1>(a, num_sms, s);
-    return launch_v8_nv<FROM_Z, DBG, 2>(a, num_sms, s);
+    const int nv = a.D / 256;
+    if (nv <= 1) return launch_v8<FROM_Z, 1, DBG>(a, num_sms, s);
+    if (nv <= 2) return launch_v8<FROM_Z, 2, DBG>(a, num_sms, s);
+    if (nv <= 3) return launch_v8<FROM_Z, 3, DBG>(a, num_sms, s);
+    if (nv <= 4) return launch_v8<FROM_Z, 4, DBG>(a, num_sms, s);
+    if (nv <= 6) return launch_v8<FROM_Z, 6, DBG>(a, num_sms, s);
+    if (nv <= 8) return launch_v8<FROM_Z, 8, DBG>(a, num_sms, s);
+    return launch_v8<FROM_Z, 12, DBG>(a, num_sms, s);
 }
 
 // ---------------------------------------------------------------------------
