@@ -981,13 +981,15 @@ struct CfgS {
     static constexpr int A_BYTES = 128 * BK * 2;
     static constexpr int B_BYTES = NB * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (200 * 1024) / STAGE_BYTES > 12 ? 12 : (200 * 1024) / STAGE_BYTES;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int STAT_BYTES = 2 * 2 * 4 * NB * 4;     // (mean, M2) x 2 buffers x 4 warps x NB
+    // as many stages (weight bytes in flight) as shared memory takes, at most 12
+    static constexpr int STAGE_ROOM = (227 * 1024 - 1024 - BAR_BYTES - STAT_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES = STAGE_ROOM > 12 ? 12 : STAGE_ROOM;
     static constexpr int TMEM_COLS = 2 * NB < 32 ? 32 : 2 * NB;
     static constexpr int EPW = NB >= 64 ? 8 : 4;             // epilogue warps
     static constexpr int CPW = NB / (EPW / 4);               // batch columns per epilogue warp
     static constexpr int THREADS = 128 + 32 * EPW;
-    static constexpr int BAR_BYTES = 256;
-    static constexpr int STAT_BYTES = 2 * 2 * 4 * NB * 4;     // (mean, M2) x 2 buffers x 4 warps x NB
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + STAT_BYTES;
     static_assert(NB % 16 == 0 && NB >= 16 && NB <= 256, "MMA N for M = 128");
     static_assert(B_BYTES % 1024 == 0, "swizzle atoms of the activation tile");
@@ -1332,7 +1334,14 @@ cudaError_t launch_gemm1_tc(const void* S, const void* W1p, const float* b1, voi
     a.a_group_rows = Bcap;
     a.bias = b1;
     a.hid = reinterpret_cast<__half*>(Hid);
-    a.hid_tma = 1;
+    // GELU outputs through shared memory and TMA tensor stores; RM_GEMM1_TMA_STORE=0
+    // in the environment stores them from registers (a tuning switch; the same result)
+    static int tma_store = -1;
+    if (tma_store < 0) {
+        const char* v = getenv("RM_GEMM1_TMA_STORE");
+        tma_store = (v && v[0] == '0') ? 0 : 1;
+    }
+    a.hid_tma = tma_store;
     a.err = err;
     a.timeout_ns = timeout_ns;
     return tc::run_dense<tc::EPI_GELU>(tc::pick_bn(F), S, (long long)T * Bcap, W1p, T, a, num_sms, s);
