@@ -409,21 +409,18 @@ RM_API rm_status rm_score(rm_ctx *ctx, const void *E, const float *head_w, float
  *   - The array exists on every GPU that loads the library until the process
  *     exits.  B is limited by it: a call whose intermediates exceed 32 MiB
  *     returns RM_ERR_INVALID_ARG and names the largest B that fits (on the
- *     tensor-core path of a 152-SM GB300, B <= 48 at T=32, D=1536, k=4 and
- *     B <= 226 at T=16, D=768, k=4; small batches also keep the GEMMs' split-k
- *     partial sums there, about 5 MB).  B is not limited by cfg.max_batch.
+ *     tensor-core path B <= 56 at T=32, D=1536, k=4 and B <= 226 at T=16,
+ *     D=768, k=4).  B is not limited by cfg.max_batch.
  *   - Each call made outside stream capture looks up the array's device
  *     address on the context's device (a lookup that allocates nothing); a
  *     call under capture reuses the address of the last uncaptured call on
  *     that device.  So make the first call on a device before any stream
  *     capture (a captured first call returns RM_ERR_INVALID_ARG), and after a
  *     device reset make one uncaptured call before capturing again.
- *   - All calls share the array and it keeps the last call's contents.  The
- *     split-k flags in it are cleared at the start of each call
- *     (cudaMemsetAsync on `stream`, which allocates nothing); every other
- *     element a call uses is written earlier in the same call.  Calls that
- *     overlap on the GPU (other streams, other threads, other contexts) race
- *     on it: serialise them.
+ *   - All calls share the array and it keeps the last call's contents.  Every
+ *     element a call uses is written earlier in the same call, so nothing
+ *     needs clearing, but calls that overlap on the GPU (other streams, other
+ *     threads, other contexts) race on it: serialise them.
  *   - Dense TokenMixing layers only (RM_ERR_UNSUPPORTED for a Sparse-MoE
  *     layer, and for a layer set to UniMixing by rm_set_unimixing, whose
  *     mixing uses the context's workspace).

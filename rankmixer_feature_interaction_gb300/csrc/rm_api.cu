@@ -230,8 +230,6 @@ struct rm_ctx {
     cudaEvent_t hx_in[2] = {}, hx_done[2] = {}, hx_out[2] = {};
     long long h_next = 0;
     long long h_slot[2] = {-1, -1};
-    // split-k workspace of the small-batch GEMMs (tensor-core contexts)
-    SkWorkspace sk;
     // error word and the debug flag nothing sets
     int* d_err = nullptr;
     int* d_flag = nullptr;
@@ -336,7 +334,6 @@ void free_ctx(rm_ctx* c) {
     if (c->s_in) cudaStreamDestroy(c->s_in);
     if (c->s_out) cudaStreamDestroy(c->s_out);
     device_free(c->d_err); device_free(c->d_flag);
-    device_free(c->sk.part); device_free(c->sk.flag);
     for (auto& e : c->ev_pool) { cudaEventDestroy(e.a); cudaEventDestroy(e.b); }
     delete c;
 }
@@ -462,13 +459,13 @@ rm_status run_pffn(rm_ctx* c, int layer, int B, cudaStream_t s) {
         {
             ProfScope ps(c, RM_K_GEMM1, s);
             cudaError_t e = launch_gemm1_tc(c->S, w.W1p, w.b1, c->Hid, B, g.T, g.D, c->F, c->Bcap, c->num_sms,
-                                            &c->sk, c->d_err, kWaitTimeoutNs, s);
+                                            c->d_err, kWaitTimeoutNs, s);
             if (e != cudaSuccess) return cuda_fail(e, (std::string("gemm1 (tcgen05) ") + tc_last_error()).c_str());
         }
         {
             ProfScope ps(c, RM_K_GEMM2, s);
             cudaError_t e = launch_gemm2_tc(c->Hid, w.W2p, w.b2, c->S, c->Z, c->stats, B, g.T, g.D, c->F, c->Bcap,
-                                            c->num_sms, &c->sk, c->d_err, kWaitTimeoutNs, s);
+                                            c->num_sms, c->d_err, kWaitTimeoutNs, s);
             if (e != cudaSuccess) return cuda_fail(e, (std::string("gemm2 (tcgen05) ") + tc_last_error()).c_str());
         }
         if (B <= kMergeInConsumerMaxB) {
@@ -1017,15 +1014,6 @@ rm_status rm_create(const rm_config* cfg, const rm_layer_params* layers, int dev
         (st = dmalloc(c, (void**)&c->V, T * Bc * D * 4, &c->ws_bytes)) != RM_OK) {
         free_ctx(c);
         return st;
-    }
-    if (c->use_tc) {
-        c->sk.max_ctas = c->num_sms;
-        if ((st = dmalloc(c, (void**)&c->sk.part, sk_part_bytes(c->sk.max_ctas), &c->ws_bytes)) != RM_OK ||
-            (st = dmalloc(c, (void**)&c->sk.flag, sk_flag_bytes(c->sk.max_ctas), &c->ws_bytes)) != RM_OK) {
-            free_ctx(c);
-            return st;
-        }
-        cudaMemset(c->sk.flag, 0, sk_flag_bytes(c->sk.max_ctas));
     }
     if (cfg->n_experts > 0) {
         MoeShape ms{c->act, cfg->T, cfg->D, cfg->n_experts, cfg->expert_hidden};
@@ -1811,11 +1799,10 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Layout of the static scratch for B samples (token-major, rows between tokens
 // = B): S, Hid and Z in the operand type, the GEMM2 chunk statistics (tensor-
-// core path only), the merged row statistics, and (tensor-core path, small
-// batches) the split-k slots and flags of the GEMMs, each 256-byte aligned.
+// core path only) and the merged row statistics, each 256-byte aligned.
 struct NoAllocLayout {
-    size_t S, H, Z, T, R, K, Q;
-    size_t total() const { return S + H + Z + T + R + K + Q; }
+    size_t S, H, Z, T, R;
+    size_t total() const { return S + H + Z + T + R; }
 };
 
 NoAllocLayout noalloc_layout(const rm_ctx* c, size_t B) {
@@ -1826,17 +1813,17 @@ NoAllocLayout noalloc_layout(const rm_ctx* c, size_t B) {
     l.Z = align256(T * B * D * osz);
     l.T = c->use_tc ? align256(T * B * (size_t)c->nchunk * sizeof(float2)) : 0;
     l.R = align256(T * B * sizeof(float2));
-    l.K = c->use_tc ? align256(sk_part_bytes_for((int)B, c->num_sms)) : 0;
-    l.Q = l.K ? align256(sk_flag_bytes(c->num_sms)) : 0;
     return l;
 }
 
-// Largest batch such that every batch up to it fits the static scratch (the
-// split-k slots make the size step down past the small-batch range).
+// Largest batch whose intermediates fit the static scratch.
 int noalloc_max_batch(const rm_ctx* c) {
-    int b = 0;
-    while (b < INT32_MAX && noalloc_layout(c, (size_t)b + 1).total() <= kNoAllocScratchBytes) ++b;
-    return b;
+    size_t lo = 0, hi = kNoAllocScratchBytes;   // the answer is below hi (every sample takes > 1 byte)
+    while (lo < hi) {
+        const size_t mid = (lo + hi + 1) / 2;
+        if (noalloc_layout(c, mid).total() <= kNoAllocScratchBytes) lo = mid; else hi = mid - 1;
+    }
+    return lo > (size_t)INT32_MAX ? INT32_MAX : (int)lo;
 }
 
 }  // namespace
@@ -1877,17 +1864,6 @@ rm_status rm_block_forward_noalloc(rm_ctx* c, int layer, const void* X_in, void*
     void* Z = p + lay.S + lay.H;
     float2* stats = reinterpret_cast<float2*>(p + lay.S + lay.H + lay.Z);
     float2* rows = reinterpret_cast<float2*>(p + lay.S + lay.H + lay.Z + lay.T);
-    // split-k slots in the scratch; the flags start at zero in every call, so
-    // any non-zero epoch marks this call's values
-    SkWorkspace skw;
-    SkWorkspace* sk = nullptr;
-    if (lay.K) {
-        skw.part = reinterpret_cast<float*>(p + lay.S + lay.H + lay.Z + lay.T + lay.R);
-        skw.flag = reinterpret_cast<int*>(p + lay.S + lay.H + lay.Z + lay.T + lay.R + lay.K);
-        skw.max_ctas = c->num_sms;
-        sk = &skw;
-        RM_CHECK_CUDA(cudaMemsetAsync(skw.flag, 0, sk_flag_bytes(c->num_sms), s), "clear split-k flags");
-    }
 
     const LayerW& w = c->layers[layer];
     MixLnArgs a = mix_args(c, layer, B);
@@ -1896,10 +1872,10 @@ rm_status rm_block_forward_noalloc(rm_ctx* c, int layer, const void* X_in, void*
     a.Bcap = B;
     RM_CHECK_CUDA(launch_mix_ln1(c->act, false, a, c->num_sms, s), "mix+ln1");
     if (c->use_tc) {
-        cudaError_t e = launch_gemm1_tc(S, w.W1p, w.b1, Hid, B, g.T, g.D, c->F, B, c->num_sms, sk, c->d_err,
+        cudaError_t e = launch_gemm1_tc(S, w.W1p, w.b1, Hid, B, g.T, g.D, c->F, B, c->num_sms, c->d_err,
                                         kWaitTimeoutNs, s);
         if (e != cudaSuccess) return cuda_fail(e, (std::string("gemm1 (tcgen05) ") + tc_last_error()).c_str());
-        e = launch_gemm2_tc(Hid, w.W2p, w.b2, S, Z, stats, B, g.T, g.D, c->F, B, c->num_sms, sk, c->d_err,
+        e = launch_gemm2_tc(Hid, w.W2p, w.b2, S, Z, stats, B, g.T, g.D, c->F, B, c->num_sms, c->d_err,
                             kWaitTimeoutNs, s);
         if (e != cudaSuccess) return cuda_fail(e, (std::string("gemm2 (tcgen05) ") + tc_last_error()).c_str());
         RM_CHECK_CUDA(launch_stats_finalize(stats, rows, B, g.T, B, c->nchunk, c->cw, c->num_sms, s),

@@ -88,13 +88,6 @@ struct Args {
     float2* stats;            // EPI_RESID row partials [row][nchunk]
     int nchunk;
     const float* row_gate;    // EPI_GATED: gate of each packed row (same row index as A)
-    // weights-as-M kernel: k-steps split evenly over the CTAs (sk != 0); a CTA's
-    // partial accumulator goes to its slot of sk_part (128 x NB floats) and its
-    // flag in sk_flag is set to sk_epoch when the slot holds this launch's values
-    int sk;
-    float* sk_part;
-    int* sk_flag;
-    unsigned sk_epoch;
     int* err;
     unsigned long long timeout_ns;
 };
@@ -1072,53 +1065,16 @@ pffn_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
     const long long units = args.tiles;             // token groups x feature blocks
     const int nfb = args.n_tiles;                   // feature blocks of 128 per group
 
-    // Work items (unit, kb0, kb1).  Whole units u = blockIdx.x, + gridDim.x, ...;
-    // or, with args.sk, the units x kblocks k-steps cut into gridDim.x equal
-    // contiguous ranges: an SM streams its weights at a bounded rate, so a last
-    // round with some SMs idle costs as long as a full one, and even ranges keep
-    // every SM streaming to the end.  A unit split between two CTAs (ranges are at
-    // least a unit long) has an owner, the CTA holding its first k-step (its last
-    // item), and a partner, the next CTA (its first item): the partner's
-    // accumulator goes to its slot, the owner adds it to its own and runs the
-    // epilogue.  Sum order fixed: owner's k-steps, then the partner's.
-    const long long Wk = units * (long long)kblocks;
-    const long long rb = args.sk ? Wk * blockIdx.x / gridDim.x : 0;
-    const long long re = args.sk ? Wk * (blockIdx.x + 1) / gridDim.x : 0;
-    struct Item {
-        long long unit;
-        int kb0, kb1;
-    };
-    auto next_item = [&](long long& u, Item& it) -> bool {
-        if (args.sk) {
-            if (u >= re) return false;
-            it.unit = u / kblocks;
-            it.kb0 = (int)(u - it.unit * kblocks);
-            const long long left = re - u;
-            it.kb1 = left < (long long)(kblocks - it.kb0) ? it.kb0 + (int)left : kblocks;
-            u += it.kb1 - it.kb0;
-            return true;
-        }
-        if (u >= units) return false;
-        it.unit = u;
-        it.kb0 = 0;
-        it.kb1 = kblocks;
-        u += gridDim.x;
-        return true;
-    };
-    const long long u_first = args.sk ? rb : (long long)blockIdx.x;
-
     if (warp == 0) {
         // ------------------------------ TMA producer ------------------------------
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        long long u = u_first;
-        Item it;
-        while (ok && next_item(u, it)) {
-            const int j = (int)(it.unit / nfb);
-            const int fb = (int)(it.unit - (long long)j * nfb);
+        for (long long u = blockIdx.x; ok && u < units; u += gridDim.x) {
+            const int j = (int)(u / nfb);
+            const int fb = (int)(u - (long long)j * nfb);
             const int wg = args.group_base + j * args.group_stride;
-            for (int kb = it.kb0; kb < it.kb1; ++kb) {
+            for (int kb = 0; kb < kblocks; ++kb) {
                 if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, args.err, args.timeout_ns)) {
                     ok = false;
                     break;
@@ -1143,13 +1099,11 @@ pffn_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
-        long long u = u_first;
-        Item it;
-        while (ok && next_item(u, it)) {
+        for (long long u = blockIdx.x; ok && u < units; u += gridDim.x) {
             if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, args.err, args.timeout_ns)) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * NB);
-            for (int kb = it.kb0; kb < it.kb1; ++kb) {
+            for (int kb = 0; kb < kblocks; ++kb) {
                 if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, args.err, args.timeout_ns)) {
                     ok = false;
                     break;
@@ -1161,7 +1115,7 @@ pffn_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
                         umma_f16(d_tmem, make_sw128_desc(a0 + 32u * k), make_sw128_desc(b0 + 32u * k), idesc,
-                                 (kb > it.kb0 || k > 0) ? 1u : 0u);
+                                 (kb > 0 || k > 0) ? 1u : 0u);
                     umma_commit(empty_bar(stage));
                 }
                 __syncwarp();
@@ -1183,16 +1137,9 @@ pffn_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
         const int col0 = (e >> 2) * C::CPW;           // this warp's first batch column
         int acc = 0;
         uint32_t acc_phase = 0;
-        long long u = u_first;
-        Item it;
-        bool ok = true;
-        // slot element (column b, feature lane of quadrant q): 32 lanes, 128 bytes per column
-        auto slot_at = [&](long long cta, int b) -> float* {
-            return args.sk_part + (size_t)cta * 128 * NB + ((size_t)b * 4 + q) * 32 + lane;
-        };
-        while (ok && next_item(u, it)) {
-            const int j = (int)(it.unit / nfb);
-            const int fb = (int)(it.unit - (long long)j * nfb);
+        for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+            const int j = (int)(u / nfb);
+            const int fb = (int)(u - (long long)j * nfb);
             const int wg = args.group_base + j * args.group_stride;
             const int f = fb * 128 + q * 32 + lane;                      // this lane's output feature
             const float bf = __ldg(args.bias + (size_t)wg * args.N + f);
@@ -1200,103 +1147,66 @@ pffn_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
             if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err, args.timeout_ns)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * NB);
-            if (it.kb0 > 0) {
-                // partner: the accumulator to this CTA's slot, then (every epilogue warp
-                // done) the flag
-                for (int c = col0; c < col0 + C::CPW && c < args.M; c += CW) {
-                    float v[CW];
-                    if constexpr (CW == 32) tmem_ld32(tbase + (uint32_t)c, v); else tmem_ld16(tbase + (uint32_t)c, v);
-#pragma unroll
-                    for (int i = 0; i < CW; ++i)
-                        if (c + i < args.M) __stcg(slot_at(blockIdx.x, c + i), v[i]);
-                }
-                __threadfence();
-                asm volatile("bar.sync 1, %0;" ::"r"(C::EPW * 32) : "memory");
-                if (e == 0 && lane == 0)
-                    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(args.sk_flag + blockIdx.x),
-                                 "r"(args.sk_epoch)
-                                 : "memory");
-            } else {
-                const bool owner = it.kb1 < kblocks;     // the partner (next CTA) holds the rest
-                if (owner) {
-                    const int* fl = args.sk_flag + blockIdx.x + 1;
-                    const uint64_t t0 = globaltimer_ns();
-                    for (uint32_t spin = 0;; ++spin) {
-                        unsigned fv;
-                        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(fv) : "l"(fl) : "memory");
-                        if (fv == args.sk_epoch) break;
-                        if ((spin & 63u) == 63u && (*abort_flag || globaltimer_ns() - t0 > args.timeout_ns)) {
-                            *abort_flag = 1;
-                            latch_error(args.err, kDevErrTimeout);
-                            ok = false;
-                            break;
-                        }
-                    }
-                }
-                float* st_mean = s_stat + (size_t)acc * 2 * 4 * NB + (size_t)q * NB;
-                float* st_m2 = st_mean + 4 * NB;
+            float* st_mean = s_stat + (size_t)acc * 2 * 4 * NB + (size_t)q * NB;
+            float* st_m2 = st_mean + 4 * NB;
 #pragma unroll 1
-                for (int c = col0; ok && c < col0 + C::CPW && c < args.M; c += CW) {
-                    float v[CW];
-                    if constexpr (CW == 32) tmem_ld32(tbase + (uint32_t)c, v); else tmem_ld16(tbase + (uint32_t)c, v);
-                    if (owner) {
+            for (int c = col0; c < col0 + C::CPW && c < args.M; c += CW) {
+                float v[CW];
+                if constexpr (CW == 32) {
+                    tmem_ld32(tbase + (uint32_t)c, v);
+                } else {
+                    tmem_ld16(tbase + (uint32_t)c, v);
+                }
+                if (EPI == EPI_GELU) {
+                    // two batch rows at a time through the packed GELU
 #pragma unroll
-                        for (int i = 0; i < CW; ++i)
-                            if (c + i < args.M) v[i] += __ldcg(slot_at(blockIdx.x + 1, c + i));
+                    for (int i = 0; i < CW; i += 2) {
+                        const int b = c + i;                               // batch row (warp-uniform)
+                        if (b >= args.M) break;
+                        float g0, g1;
+                        f2_unpack(gelu_erf_x2(f2_pack(v[i], v[i + 1]), f2_splat(bf)), g0, g1);
+                        args.hid[(row0 + b) * (size_t)args.N + f] = __float2half_rn(sat_f16(g0));
+                        if (b + 1 < args.M) args.hid[(row0 + b + 1) * (size_t)args.N + f] = __float2half_rn(sat_f16(g1));
                     }
-                    if (EPI == EPI_GELU) {
-                        // two batch rows at a time through the packed GELU
+                } else {   // EPI_RESID
+                    // the residuals of the chunk's rows first, all loads in flight together
+                    float rres[CW];
 #pragma unroll
-                        for (int i = 0; i < CW; i += 2) {
-                            const int b = c + i;                               // batch row (warp-uniform)
-                            if (b >= args.M) break;
-                            float g0, g1;
-                            f2_unpack(gelu_erf_x2(f2_pack(v[i], v[i + 1]), f2_splat(bf)), g0, g1);
-                            args.hid[(row0 + b) * (size_t)args.N + f] = __float2half_rn(sat_f16(g0));
-                            if (b + 1 < args.M)
-                                args.hid[(row0 + b + 1) * (size_t)args.N + f] = __float2half_rn(sat_f16(g1));
-                        }
-                    } else {   // EPI_RESID
-                        // the residuals of the chunk's rows first, all loads in flight together
-                        float rres[CW];
+                    for (int i = 0; i < CW; ++i) {
+                        const int b = c + i;
+                        rres[i] = b < args.M ? __half2float(args.resid[(row0 + b) * (size_t)args.N + f]) : 0.f;
+                    }
 #pragma unroll
-                        for (int i = 0; i < CW; ++i) {
-                            const int b = c + i;
-                            rres[i] = b < args.M ? __half2float(args.resid[(row0 + b) * (size_t)args.N + f]) : 0.f;
-                        }
-#pragma unroll
-                        for (int i = 0; i < CW; ++i) {
-                            const int b = c + i;                               // batch row (warp-uniform)
-                            if (b >= args.M) break;
-                            const float z = v[i] + bf + rres[i];
-                            args.z[(row0 + b) * (size_t)args.N + f] = __float2half_rn(sat_f16(z));
-                            // this warp's 32 features: mean and M2 about it
-                            const float mw = warp_sum(z) * (1.0f / 32.0f);
-                            const float d = z - mw;
-                            const float m2w = warp_sum(d * d);
-                            if (lane == 0) {
-                                st_mean[b] = mw;
-                                st_m2[b] = m2w;
-                            }
+                    for (int i = 0; i < CW; ++i) {
+                        const int b = c + i;                               // batch row (warp-uniform)
+                        if (b >= args.M) break;
+                        const float z = v[i] + bf + rres[i];
+                        args.z[(row0 + b) * (size_t)args.N + f] = __float2half_rn(sat_f16(z));
+                        // this warp's 32 features: mean and M2 about it
+                        const float mw = warp_sum(z) * (1.0f / 32.0f);
+                        const float d = z - mw;
+                        const float m2w = warp_sum(d * d);
+                        if (lane == 0) {
+                            st_mean[b] = mw;
+                            st_m2[b] = m2w;
                         }
                     }
                 }
-                if (EPI == EPI_RESID) {
-                    // the four quadrants' moments -> (mean, M2) of the 128 features, one lane
-                    // per row, each q = 0 warp for its own columns (every warp meets the
-                    // barrier, also one that gave up waiting)
-                    asm volatile("bar.sync 1, %0;" ::"r"(C::EPW * 32) : "memory");
-                    if (q == 0 && ok) {
-                        const float* sm = s_stat + (size_t)acc * 2 * 4 * NB;
-                        const float* s2 = sm + 4 * NB;
-                        for (int b = col0 + lane; b < args.M && b < col0 + C::CPW; b += 32) {
-                            const float m0 = sm[b], m1 = sm[NB + b], m2 = sm[2 * NB + b], m3 = sm[3 * NB + b];
-                            const float mean = 0.25f * (m0 + m1 + m2 + m3);
-                            const float d0 = m0 - mean, d1 = m1 - mean, d2 = m2 - mean, d3 = m3 - mean;
-                            const float M2 = s2[b] + s2[NB + b] + s2[2 * NB + b] + s2[3 * NB + b] +
-                                             32.0f * (d0 * d0 + d1 * d1 + d2 * d2 + d3 * d3);
-                            args.stats[(row0 + b) * (size_t)args.nchunk + fb] = make_float2(mean, M2);
-                        }
+            }
+            if (EPI == EPI_RESID) {
+                // the four quadrants' moments -> (mean, M2) of the 128 features, one lane
+                // per row, each q = 0 warp for its own columns
+                asm volatile("bar.sync 1, %0;" ::"r"(C::EPW * 32) : "memory");
+                if (q == 0) {
+                    const float* sm = s_stat + (size_t)acc * 2 * 4 * NB;
+                    const float* s2 = sm + 4 * NB;
+                    for (int b = col0 + lane; b < args.M && b < col0 + C::CPW; b += 32) {
+                        const float m0 = sm[b], m1 = sm[NB + b], m2 = sm[2 * NB + b], m3 = sm[3 * NB + b];
+                        const float mean = 0.25f * (m0 + m1 + m2 + m3);
+                        const float d0 = m0 - mean, d1 = m1 - mean, d2 = m2 - mean, d3 = m3 - mean;
+                        const float M2 = s2[b] + s2[NB + b] + s2[2 * NB + b] + s2[3 * NB + b] +
+                                         32.0f * (d0 * d0 + d1 * d1 + d2 * d2 + d3 * d3);
+                        args.stats[(row0 + b) * (size_t)args.nchunk + fb] = make_float2(mean, M2);
                     }
                 }
             }
@@ -1329,33 +1239,12 @@ int swap_max_batch() {
     return env;
 }
 
-// Even k-ranges for the weights-as-M kernel whenever every CTA gets at least
-// one unit; RM_GEMM_SWAP_SK=0 in the environment keeps whole units (a tuning
-// switch; results agree to the fp32 rounding of the split k-sums).
-bool swap_stream_k() {
-    static int env = -1;
-    if (env < 0) {
-        const char* v = getenv("RM_GEMM_SWAP_SK");
-        env = (v && v[0] == '0') ? 0 : 1;
-    }
-    return env == 1;
-}
-
 template <int NB, int EPI>
-cudaError_t run_swap(const void* A, const void* W, int n_wgroups, Args a, int num_sms, SkWorkspace* sk,
-                     cudaStream_t s) {
+cudaError_t run_swap(const void* A, const void* W, int n_wgroups, Args a, int num_sms, cudaStream_t s) {
     using C = CfgS<NB>;
     a.n_tiles = a.N / 128;
     a.tiles = (long long)a.ngroups * a.n_tiles;
     if (a.tiles == 0) return cudaSuccess;
-    a.sk = 0;
-    if (sk && sk->part && swap_stream_k() && a.tiles >= num_sms && num_sms <= sk->max_ctas) {
-        a.sk = 1;
-        a.sk_part = sk->part;
-        a.sk_flag = sk->flag;
-        if (++sk->epoch == 0) ++sk->epoch;      // 0 is the flags' initial value
-        a.sk_epoch = sk->epoch;
-    }
     CUtensorMap mW, mX;
     if (!make_map(&mW, W, a.K, a.N, n_wgroups, a.N, 128)) return cudaErrorInvalidValue;
     if (!make_map(&mX, A, a.K, a.M, a.ngroups, a.a_group_rows, NB)) return cudaErrorInvalidValue;
@@ -1371,23 +1260,22 @@ cudaError_t run_swap(const void* A, const void* W, int n_wgroups, Args a, int nu
 }
 
 template <int EPI>
-cudaError_t run_swap_nb(const void* A, const void* W, int n_wgroups, const Args& a, int num_sms, SkWorkspace* sk,
-                        cudaStream_t s) {
-    if (a.M <= 16) return run_swap<16, EPI>(A, W, n_wgroups, a, num_sms, sk, s);
-    if (a.M <= 32) return run_swap<32, EPI>(A, W, n_wgroups, a, num_sms, sk, s);
-    if (a.M <= 64) return run_swap<64, EPI>(A, W, n_wgroups, a, num_sms, sk, s);
-    if (a.M <= 128) return run_swap<128, EPI>(A, W, n_wgroups, a, num_sms, sk, s);
-    return run_swap<256, EPI>(A, W, n_wgroups, a, num_sms, sk, s);
+cudaError_t run_swap_nb(const void* A, const void* W, int n_wgroups, const Args& a, int num_sms, cudaStream_t s) {
+    if (a.M <= 16) return run_swap<16, EPI>(A, W, n_wgroups, a, num_sms, s);
+    if (a.M <= 32) return run_swap<32, EPI>(A, W, n_wgroups, a, num_sms, s);
+    if (a.M <= 64) return run_swap<64, EPI>(A, W, n_wgroups, a, num_sms, s);
+    if (a.M <= 128) return run_swap<128, EPI>(A, W, n_wgroups, a, num_sms, s);
+    return run_swap<256, EPI>(A, W, n_wgroups, a, num_sms, s);
 }
 
 template <int EPI>
 cudaError_t run_dense(int bn, const void* A, long long a_rows_total, const void* W, int n_wgroups, const Args& a,
-                      int num_sms, SkWorkspace* sk, cudaStream_t s) {
+                      int num_sms, cudaStream_t s) {
     // weights as the MMA's M side for small batches; the second GEMM's row
     // statistics then come in 128-column chunks, which must be the context's
     if (a.M <= swap_max_batch() && a.N % 128 == 0 && a.K % BK == 0 &&
         (EPI == EPI_GELU || (EPI == EPI_RESID && a.nchunk * 128 == a.N)))
-        return run_swap_nb<EPI>(A, W, n_wgroups, a, num_sms, sk, s);
+        return run_swap_nb<EPI>(A, W, n_wgroups, a, num_sms, s);
     if (use_pair(a.M, EPI)) {
         const bool k2 = use_ksub2(a.K, EPI);
         if (EPI == EPI_GELU && gelu_pair_epw16(a.K))
@@ -1428,23 +1316,13 @@ int gemm2_bn(int D) {
 
 int tc_stats_chunk_width(int D) { return gemm2_bn(D) / 2; }
 
-size_t sk_part_bytes(int max_ctas) { return (size_t)max_ctas * 128 * 256 * sizeof(float); }
-
-size_t sk_part_bytes_for(int M, int num_ctas) {
-    if (M > tc::swap_max_batch()) return 0;
-    const int nb = M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : (M <= 128 ? 128 : 256)));
-    return (size_t)num_ctas * 128 * nb * sizeof(float);
-}
-size_t sk_flag_bytes(int max_ctas) { return (size_t)max_ctas * sizeof(int); }
-
 const char* tc_last_error() {
     std::lock_guard<std::mutex> lk(tc::g_mu);
     return tc::g_err.c_str();
 }
 
 cudaError_t launch_gemm1_tc(const void* S, const void* W1p, const float* b1, void* Hid, int B, int T, int D, int F,
-                            int Bcap, int num_sms, SkWorkspace* sk, int* err, unsigned long long timeout_ns,
-                            cudaStream_t s) {
+                            int Bcap, int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     tc::Args a{};
     a.N = F;
@@ -1456,15 +1334,22 @@ cudaError_t launch_gemm1_tc(const void* S, const void* W1p, const float* b1, voi
     a.a_group_rows = Bcap;
     a.bias = b1;
     a.hid = reinterpret_cast<__half*>(Hid);
-    a.hid_tma = 1;
+    // GELU outputs through shared memory and TMA tensor stores; RM_GEMM1_TMA_STORE=0
+    // in the environment stores them from registers (a tuning switch; the same result)
+    static int tma_store = -1;
+    if (tma_store < 0) {
+        const char* v = getenv("RM_GEMM1_TMA_STORE");
+        tma_store = (v && v[0] == '0') ? 0 : 1;
+    }
+    a.hid_tma = tma_store;
     a.err = err;
     a.timeout_ns = timeout_ns;
-    return tc::run_dense<tc::EPI_GELU>(tc::pick_bn(F), S, (long long)T * Bcap, W1p, T, a, num_sms, sk, s);
+    return tc::run_dense<tc::EPI_GELU>(tc::pick_bn(F), S, (long long)T * Bcap, W1p, T, a, num_sms, s);
 }
 
 cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, const void* S, void* Z,
-                            float2* stats, int B, int T, int D, int F, int Bcap, int num_sms, SkWorkspace* sk,
-                            int* err, unsigned long long timeout_ns, cudaStream_t s) {
+                            float2* stats, int B, int T, int D, int F, int Bcap, int num_sms, int* err,
+                            unsigned long long timeout_ns, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     const int bn = gemm2_bn(D);
     if (bn == 0) return cudaErrorNotSupported;
@@ -1483,7 +1368,7 @@ cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, c
     a.nchunk = D / (bn / 2);
     a.err = err;
     a.timeout_ns = timeout_ns;
-    return tc::run_dense<tc::EPI_RESID>(bn, Hid, (long long)T * Bcap, W2p, T, a, num_sms, sk, s);
+    return tc::run_dense<tc::EPI_RESID>(bn, Hid, (long long)T * Bcap, W2p, T, a, num_sms, s);
 }
 
 cudaError_t launch_moe_gemm1_tc(const void* Sg, long long rows_total, const void* W1p, const float* b1, void* Hm,

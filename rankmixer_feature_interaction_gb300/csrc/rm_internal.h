@@ -141,30 +141,11 @@ cudaError_t launch_gemm2_simt(Act act, const void* Hid, const void* W2p, const f
 // tcgen05 path (fp16 operands; BF16 contexts only).
 bool tc_supported(int D, int F);
 int tc_stats_chunk_width(int D);   // chunk width of the LN2 partial statistics written by GEMM2
-
-// Split-k workspace of the small-batch (weights-as-M) GEMMs, owned by the
-// caller and used by one stream at a time: a partial-accumulator slot (128 x
-// 256 floats) and a flag per CTA for up to max_ctas CTAs, and the count of the
-// launches that used it (each launch's epoch; a flag holds the epoch of the
-// launch that wrote it, so flags never need clearing).  Without one (nullptr)
-// those GEMMs take whole units of work.
-struct SkWorkspace {
-    float* part = nullptr;
-    int* flag = nullptr;       // zero when allocated
-    int max_ctas = 0;
-    unsigned epoch = 0;
-};
-size_t sk_part_bytes(int max_ctas);
-size_t sk_flag_bytes(int max_ctas);
-// Slot bytes a batch of M rows needs on num_ctas CTAs (0: M takes no split-k).
-size_t sk_part_bytes_for(int M, int num_ctas);
-
 cudaError_t launch_gemm1_tc(const void* S, const void* W1p, const float* b1, void* Hid, int B, int T, int D, int F,
-                            int Bcap, int num_sms, SkWorkspace* sk, int* err, unsigned long long timeout_ns,
-                            cudaStream_t s);
+                            int Bcap, int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s);
 cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, const void* S, void* Z,
-                            float2* stats, int B, int T, int D, int F, int Bcap, int num_sms, SkWorkspace* sk,
-                            int* err, unsigned long long timeout_ns, cudaStream_t s);
+                            float2* stats, int B, int T, int D, int F, int Bcap, int num_sms, int* err,
+                            unsigned long long timeout_ns, cudaStream_t s);
 
 // Set by the tensor-map encoder when the driver call fails (host-side message).
 const char* tc_last_error();
