@@ -1334,14 +1334,7 @@ cudaError_t launch_gemm1_tc(const void* S, const void* W1p, const float* b1, voi
     a.a_group_rows = Bcap;
     a.bias = b1;
     a.hid = reinterpret_cast<__half*>(Hid);
-    // GELU outputs through shared memory and TMA tensor stores; RM_GEMM1_TMA_STORE=0
-    // in the environment stores them from registers (a tuning switch; the same result)
-    static int tma_store = -1;
-    if (tma_store < 0) {
-        const char* v = getenv("RM_GEMM1_TMA_STORE");
-        tma_store = (v && v[0] == '0') ? 0 : 1;
-    }
-    a.hid_tma = tma_store;
+    a.hid_tma = 1;
     a.err = err;
     a.timeout_ns = timeout_ns;
     return tc::run_dense<tc::EPI_GELU>(tc::pick_bn(F), S, (long long)T * Bcap, W1p, T, a, num_sms, s);

@@ -496,9 +496,9 @@ print("ok")
 # shapes that reach every tile form: CTA pairs with BN 256 / 128 (GEMM1) and 64 (GEMM2), one-CTA
 # tiles (129..255 rows), the weights-as-M path (1..64 rows, and up to 256 when widened)
 _DISPATCH_SHAPES = [(4, 256, 2, 2, 300), (2, 192, 2, 1, 300), (8, 512, 2, 2, 1100), (4, 256, 2, 2, 13),
-                    (4, 256, 2, 2, 40), (4, 512, 2, 1, 150)]
+                    (4, 256, 2, 2, 40), (4, 512, 2, 1, 150), (32, 768, 1, 1, 20)]
 _TUNING_KEYS = ("RM_GEMM_PAIR", "RM_GEMM_KSUB", "RM_GEMM1_EPW", "RM_GEMM2_BN", "RM_GEMM_SMALL_BN", "RM_GEMM_SWAP_MAX",
-                "RM_PDL", "RM_NVTX", "RM_GEMM1_TMA_STORE")
+                "RM_PDL", "RM_NVTX")
 
 
 @pytest.mark.parametrize("tuning", [{},                                            # the defaults
@@ -508,7 +508,6 @@ _TUNING_KEYS = ("RM_GEMM_PAIR", "RM_GEMM_KSUB", "RM_GEMM1_EPW", "RM_GEMM2_BN", "
                                     {"RM_GEMM_SWAP_MAX": "0"},                      # no weights-as-M path
                                     {"RM_GEMM_SWAP_MAX": "256"},                    # weights-as-M up to 256 rows
                                     {"RM_PDL": "0"},                                # plain stream order
-                                    {"RM_GEMM1_TMA_STORE": "0"},                    # GELU outputs from registers
                                     {"RM_NVTX": "1"},                               # NVTX ranges around launches
                                     {"RM_GEMM_PAIR": "2"},                          # pairs for GEMM2 only
                                     {"RM_GEMM_KSUB": "1"},                          # one k-block per stage
