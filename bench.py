@@ -48,8 +48,7 @@ UNIMIX_TAU = 0.05
 UNIMIX_ITERS = 20
 
 KERNEL_SOURCES = ("rankmixer_feature_interaction_gb300/csrc/rm_gemm_tc.cu",
-                  "rankmixer_feature_interaction_gb300/csrc/rm_common.cuh",
-                  "rankmixer_feature_interaction_gb300/csrc/rm_internal.h")
+                  "rankmixer_feature_interaction_gb300/csrc/rm_common.cuh")
 TRAFFIC = {
     # ncu --metrics gpu__time_duration.sum,dram__bytes_read.sum,dram__bytes_write.sum on
     # "bench.py --steps 3 --warmup 3" (and --config moe_1b), averaged over the captured launches
