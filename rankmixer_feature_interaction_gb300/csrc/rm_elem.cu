@@ -341,7 +341,8 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
         __syncthreads();
         if (*s_abort) break;
         uint16_t* xs = buf + (size_t)slot * buf_elems;
-        if (FROM_Z) {
+        const bool inplace = FROM_Z && a.ln2_inplace;
+        if (inplace) {
             // X_{n-1} = LN2(Z) in place (fp16), 8 elements per lane
             for (int t = warp; t < T; t += nwarps) {
                 const float mt = s_mean[t], rt = s_rstd[t];
@@ -373,6 +374,12 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
             const uint16_t* xh = xs + (size_t)h * RS;
             uint64_t y[4 * NV];
             uint64_t s2 = f2_splat(0.f);
+            // LN2 of row h (the residual operand) when it is applied as the values are read
+            __half2 mh2 = __float2half2_rn(0.f), rh2 = mh2;
+            if (FROM_Z && !inplace) {
+                mh2 = __float2half2_rn(s_mean[h]);
+                rh2 = __float2half2_rn(s_rstd[h]);
+            }
 #pragma unroll
             for (int i = 0; i < NV; ++i) {
                 if (i < nv) {
@@ -381,7 +388,29 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
                     const int r = j0 - t * q;
                     const uint4 mv = *reinterpret_cast<const uint4*>(xs + (size_t)t * RS + h * q + r);
                     const uint4 xv = *reinterpret_cast<const uint4*>(xh + j0);
-                    const uint32_t mw[4] = {mv.x, mv.y, mv.z, mv.w}, xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                    uint32_t mw[4] = {mv.x, mv.y, mv.z, mv.w}, xw[4] = {xv.x, xv.y, xv.z, xv.w};
+                    if (FROM_Z && !inplace) {
+                        // (z - mean) (rstd gamma) + beta in fp16 pairs, the operations of the
+                        // in-place pass: source row t at columns h q + r.., row h at j0..
+                        const uint4 gs = *reinterpret_cast<const uint4*>(sg2 + h * q + r);
+                        const uint4 bs = *reinterpret_cast<const uint4*>(sb2 + h * q + r);
+                        const uint4 gx = *reinterpret_cast<const uint4*>(sg2 + j0);
+                        const uint4 bx = *reinterpret_cast<const uint4*>(sb2 + j0);
+                        const __half2 mt2 = __float2half2_rn(s_mean[t]), rt2 = __float2half2_rn(s_rstd[t]);
+                        const __half2* gsh = reinterpret_cast<const __half2*>(&gs);
+                        const __half2* bsh = reinterpret_cast<const __half2*>(&bs);
+                        const __half2* gxh = reinterpret_cast<const __half2*>(&gx);
+                        const __half2* bxh = reinterpret_cast<const __half2*>(&bx);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const __half2 zm = __hfma2(__hsub2(*reinterpret_cast<const __half2*>(&mw[k]), mt2),
+                                                       __hmul2(rt2, gsh[k]), bsh[k]);
+                            const __half2 zx = __hfma2(__hsub2(*reinterpret_cast<const __half2*>(&xw[k]), mh2),
+                                                       __hmul2(rh2, gxh[k]), bxh[k]);
+                            mw[k] = *reinterpret_cast<const uint32_t*>(&zm);
+                            xw[k] = *reinterpret_cast<const uint32_t*>(&zx);
+                        }
+                    }
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         if constexpr (FROM_Z) {     // fp16 rows: add in fp16, convert once
@@ -454,6 +483,19 @@ bool v8_ok(bool, const MixLnArgs& a) {
     return a.q % 8 == 0 && a.D % 256 == 0 && a.D <= 3072 && a.T <= kMaxT && v8_smem_bytes(a.T, a.D, a.q) <= 226 * 1024;
 }
 
+// From Z, LN2 is applied to each value as the mixing reads it (no in-place pass
+// over the staged sample and one barrier fewer per sample);
+// RM_MIX_LN2_INPLACE=1 in the environment selects the in-place pass (a tuning
+// switch; the same result either way).
+bool mix_ln2_inplace() {
+    static int env = -1;
+    if (env < 0) {
+        const char* v = getenv("RM_MIX_LN2_INPLACE");
+        env = (v && v[0] == '1') ? 1 : 0;
+    }
+    return env == 1;
+}
+
 template <bool FROM_Z, int NV, bool DBG = false>
 cudaError_t launch_v8(const MixLnArgs& a, int num_sms, cudaStream_t s) {
     auto k = mix_ln1_v8_kernel<FROM_Z, NV, DBG>;
@@ -471,6 +513,7 @@ cudaError_t launch_v8(const MixLnArgs& a, int num_sms, cudaStream_t s) {
     MixLnArgs b = a;
     const int slots = num_sms * per_sm;
     b.rsplit = 1;
+    b.ln2_inplace = mix_ln2_inplace() ? 1 : 0;
     if (a.B < slots) {
         int r = slots / a.B;
         if (r > a.T / 2) r = a.T / 2;
