@@ -216,9 +216,11 @@ RM_API rm_status rm_stack_forward(rm_ctx *ctx, const void *X0, float *pooled, vo
  * to the device, runs the stack, copies the pooled float32 [B][D] result to
  * pooled_host.  Returns after the result is in pooled_host (synchronises the
  * stream).  Uses context-owned device staging buffers.  From B = 2048 on, the
- * batch runs as up to 4 chunks of at least 1024 samples, the copy of each chunk
- * overlapping the computation of the previous one (two context-owned copy
- * streams); pinned host buffers let the copies run asynchronously. */
+ * batch runs as three chunks, B/8, 3B/8 and the rest (rounded up to multiples
+ * of 256 samples), the copy of each chunk overlapping the computation of the
+ * previous one (two context-owned copy streams); pinned host buffers let the
+ * copies run asynchronously.  Each sample's arithmetic is that of
+ * rm_stack_forward. */
 RM_API rm_status rm_stack_forward_host(rm_ctx *ctx, const void *X0_host, float *pooled_host, int B, void *stream);
 
 /* Pipelined host entry for a stream of batches (serving): enqueue the stack
