@@ -10,7 +10,10 @@ import ctypes
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "librankmixer.so")
+# RM_LIBRARY=debug selects the bounds-checked build librankmixer_debug.so
+# (python -m rankmixer_feature_interaction_gb300.build --debug-bounds)
+LIB_NAME = "librankmixer_debug.so" if os.environ.get("RM_LIBRARY") == "debug" else "librankmixer.so"
+LIB_PATH = os.path.join(_HERE, LIB_NAME)
 
 # rm_status
 RM_OK = 0
@@ -88,12 +91,13 @@ _lib = None
 
 
 def load() -> ctypes.CDLL:
-    """Load librankmixer.so; raise if it is missing (build it with __graft_entry__.build())."""
+    """Load librankmixer.so (or the bounds-checked build under RM_LIBRARY=debug); raise if it
+    is missing (build it with __graft_entry__.build())."""
     global _lib
     if _lib is not None:
         return _lib
     if not os.path.exists(LIB_PATH):
-        raise RuntimeError(f"librankmixer.so not built at {LIB_PATH}; run `python -c 'import __graft_entry__ as g; "
+        raise RuntimeError(f"{LIB_NAME} not built at {LIB_PATH}; run `python -c 'import __graft_entry__ as g; "
                            f"g.build()'` (there is no non-CUDA fallback)")
     lib = ctypes.CDLL(LIB_PATH)
     vp, i, st = ctypes.c_void_p, ctypes.c_int, ctypes.c_int

@@ -43,7 +43,25 @@ rm_status fail(rm_status st, const char* fmt, ...) {
     return st;
 }
 
+// The condition text of the last failed launcher check of the debug build
+// (thread-local: set and read within one API call on one thread).
+thread_local const char* t_bounds_what = nullptr;
+
+}  // namespace
+
+cudaError_t rm::debug_bounds_fail(const char* what) {
+    t_bounds_what = what;
+    return cudaErrorInvalidValue;
+}
+
+namespace {
+
 rm_status cuda_fail(cudaError_t e, const char* what) {
+    if (e == cudaErrorInvalidValue && t_bounds_what) {
+        const char* cond = t_bounds_what;
+        t_bounds_what = nullptr;
+        return fail(RM_ERR_INVALID_ARG, "%s: bounds check failed: %s", what, cond);
+    }
     if (e == cudaErrorMemoryAllocation)
         return fail(RM_ERR_OOM, "%s: %s", what,
                     alloc_failure_was_injected() ? "injected failure (device allocation)" : cudaGetErrorString(e));
@@ -1660,6 +1678,8 @@ rm_status rm_sync_status(rm_ctx* c, void* stream) {
         RM_CHECK_CUDA(cudaMemset(c->d_err, 0, sizeof(int)), "clear error word");
         RM_CHECK_CUDA(cudaDeviceSynchronize(), "clear error word");
         if (code == kDevErrTimeout) return fail(RM_ERR_TIMEOUT, "a device-side wait ran out of time");
+        if (code == kDevErrBounds)
+            return fail(RM_ERR_DEVICE, "a device-side bounds guard fired (bounds-checked build); the access was skipped");
         return fail(RM_ERR_DEVICE, "device error code %d", code);
     }
     return RM_OK;

@@ -208,6 +208,18 @@ __device__ __forceinline__ void latch_error(int* err, int code) {
     if (err) atomicCAS(err, 0, code);
 }
 
+// Device-side guard of the bounds-checked debug build: true when the access
+// may proceed; otherwise latches kDevErrBounds and the caller skips it.
+__device__ __forceinline__ bool in_bounds(bool ok, int* err) {
+    if (!ok) latch_error(err, kDevErrBounds);
+    return ok;
+}
+#ifdef RM_DEBUG_BOUNDS
+#define RM_IN_BOUNDS(cond, err) ::rm::in_bounds((cond), (err))
+#else
+#define RM_IN_BOUNDS(cond, err) true
+#endif
+
 // ---------------------------------------------------------------------------
 // Shared-memory addresses, mbarriers
 // ---------------------------------------------------------------------------

@@ -301,7 +301,9 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
         __syncwarp();
         for (int t = lane; t < T; t += 32) {
             const uint16_t* row = FROM_Z ? src + ((size_t)t * a.Bcap + b) * D : src + ((size_t)b * T + t) * D;
-            bulk_copy_g2s(dst + (uint32_t)t * (uint32_t)RS * 2u, row, row_bytes, bar);
+            // (a skipped copy leaves the barrier short: the bounded wait then ends the sample)
+            if (RM_IN_BOUNDS(b >= 0 && b < a.B && b < a.Bcap, a.err))
+                bulk_copy_g2s(dst + (uint32_t)t * (uint32_t)RS * 2u, row, row_bytes, bar);
         }
     };
 
@@ -386,8 +388,10 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
                     const int j0 = (i << 8) + (lane << 3);
                     const int t = j0 / q;
                     const int r = j0 - t * q;
-                    const uint4 mv = *reinterpret_cast<const uint4*>(xs + (size_t)t * RS + h * q + r);
-                    const uint4 xv = *reinterpret_cast<const uint4*>(xh + j0);
+                    const bool gok = RM_IN_BOUNDS(t < T && h * q + r + 8 <= RS && j0 + 8 <= RS, a.err);
+                    const uint4 mv = gok ? *reinterpret_cast<const uint4*>(xs + (size_t)t * RS + h * q + r)
+                                         : make_uint4(0u, 0u, 0u, 0u);
+                    const uint4 xv = gok ? *reinterpret_cast<const uint4*>(xh + j0) : make_uint4(0u, 0u, 0u, 0u);
                     uint32_t mw[4] = {mv.x, mv.y, mv.z, mv.w}, xw[4] = {xv.x, xv.y, xv.z, xv.w};
                     if (FROM_Z && !inplace) {
                         // (z - mean) (rstd gamma) + beta in fp16 pairs, the operations of the
@@ -434,8 +438,10 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
                         float o[8];
 #pragma unroll
                         for (int k = 0; k < 4; ++k) f2_unpack(y[4 * i + k], o[2 * k], o[2 * k + 1]);
-                        reinterpret_cast<float4*>(yrow + j0)[0] = make_float4(o[0], o[1], o[2], o[3]);
-                        reinterpret_cast<float4*>(yrow + j0)[1] = make_float4(o[4], o[5], o[6], o[7]);
+                        if (RM_IN_BOUNDS(b < a.Bcap && j0 + 8 <= D, a.err)) {
+                            reinterpret_cast<float4*>(yrow + j0)[0] = make_float4(o[0], o[1], o[2], o[3]);
+                            reinterpret_cast<float4*>(yrow + j0)[1] = make_float4(o[4], o[5], o[6], o[7]);
+                        }
                     }
                 continue;
             }
@@ -472,7 +478,8 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
                         const __half2 v = __hfma2(*reinterpret_cast<const __half2*>(&nh), g2h[k], b2h[k]);
                         o[k] = *reinterpret_cast<const uint32_t*>(&v);
                     }
-                    *reinterpret_cast<uint4*>(srow + j0) = make_uint4(o[0], o[1], o[2], o[3]);
+                    if (RM_IN_BOUNDS(b < a.Bcap && j0 + 8 <= D, a.err))
+                        *reinterpret_cast<uint4*>(srow + j0) = make_uint4(o[0], o[1], o[2], o[3]);
                 }
         }
         __syncthreads();    // the slot and the row statistics are reused by later samples
@@ -1067,8 +1074,24 @@ bool pdl_enabled() {
     return env == 1;
 }
 
+// Launcher checks of the bounds-checked build: the sizes describe the buffers
+// the kernels index (token-major [T][Bcap][D] rows, per-row chunk statistics).
+cudaError_t check_mix_args(bool from_z, const MixLnArgs& a) {
+    RM_HOST_BOUNDS(a.B <= a.Bcap && a.T >= 1 && a.T <= kMaxT && a.D >= 1 && a.q >= 1 && a.q * a.T == a.D);
+    RM_HOST_BOUNDS(a.S != nullptr && a.g1 != nullptr && a.be1 != nullptr);
+    RM_HOST_BOUNDS(from_z ? (a.Z != nullptr && a.stats != nullptr && a.g2 != nullptr && a.be2 != nullptr &&
+                             a.nchunk >= 1 && a.cw >= 1 && a.nchunk * a.cw == a.D)
+                          : a.X != nullptr);
+    RM_HOST_BOUNDS(((reinterpret_cast<uintptr_t>(from_z ? a.Z : a.X) | reinterpret_cast<uintptr_t>(a.S)) & 15u) == 0);
+    return cudaSuccess;
+}
+
 cudaError_t launch_mix_ln1(Act act, bool from_z, const MixLnArgs& a, int num_sms, cudaStream_t s) {
     if (a.B <= 0) return cudaSuccess;
+    if (kDebugBounds) {
+        const cudaError_t e = check_mix_args(from_z, a);
+        if (e != cudaSuccess) return e;
+    }
     if (act == Act::BF16) {
         if (v8_ok(from_z, a)) return from_z ? launch_v8_dispatch<true>(a, num_sms, s) : launch_v8_dispatch<false>(a, num_sms, s);
         if (staged_ok(a))
@@ -1083,6 +1106,7 @@ cudaError_t launch_mix_ln1(Act act, bool from_z, const MixLnArgs& a, int num_sms
 
 cudaError_t launch_mix_residual_debug(bool from_z, const MixLnArgs& a, int num_sms, cudaStream_t s) {
     if (a.B <= 0) return cudaSuccess;
+    RM_HOST_BOUNDS(a.B <= a.Bcap && a.T <= kMaxT && a.q * a.T == a.D);
     if (!a.Ydbg || !v8_ok(from_z, a)) return cudaErrorNotSupported;
     return from_z ? launch_v8_dispatch<true, true>(a, num_sms, s) : launch_v8_dispatch<false, true>(a, num_sms, s);
 }
@@ -1091,6 +1115,7 @@ cudaError_t launch_ln2_out(Act act, const void* Z, const float2* stats, const fl
                            void* X_out, bool out_f32, int B, int T, int D, int Bcap, int nchunk, int cw, float eps,
                            int num_sms, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
+    RM_HOST_BOUNDS(B <= Bcap && nchunk >= 1 && nchunk * cw == D && Z != nullptr && stats != nullptr && X_out != nullptr);
     const int grid = grid_for((long long)B * T * 32, 256, num_sms * 8);
     if (act == Act::BF16 && D % 256 == 0) {
         if (out_f32)
@@ -1117,6 +1142,7 @@ cudaError_t launch_ln2_out_op(Act act, const void* Z, const float2* stats, int n
                               const float* be2, void* X_out, int B, int T, int D, int Bcap, float eps, int num_sms,
                               cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
+    RM_HOST_BOUNDS(B <= Bcap && nchunk >= 1 && nchunk * cw == D && Z != nullptr && stats != nullptr && X_out != nullptr);
     const int grid = grid_for((long long)B * T * 32, 256, num_sms * 8);
     if (act == Act::BF16 && D % 256 == 0)
         launch_k(ln2_out_vec_kernel<__half>, dim3(grid), dim3(256), 0, s, (const __half*)Z, stats, g2, be2,
@@ -1135,6 +1161,7 @@ cudaError_t launch_pool(Act act, const void* Z, const float2* stats, const float
                         float eps, int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     if (T > kMaxT) return cudaErrorNotSupported;
+    RM_HOST_BOUNDS(B <= Bcap && nchunk >= 1 && nchunk * cw == D && Z != nullptr && stats != nullptr && pooled != nullptr);
     if (act == Act::BF16 && XL == nullptr && D % 8 == 0 && D <= 8 * 256) {
         int threads = (D / 8 + 31) / 32 * 32;
         if (threads < 64) threads = 64;
@@ -1159,6 +1186,7 @@ cudaError_t launch_pool(Act act, const void* Z, const float2* stats, const float
 cudaError_t launch_stats_finalize(const float2* part, float2* out, int B, int T, int Bcap, int nchunk, int cw,
                                   int num_sms, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
+    RM_HOST_BOUNDS(B <= Bcap && nchunk >= 1 && cw >= 1 && part != nullptr && out != nullptr);
     launch_k(stats_finalize_kernel, dim3(grid_for((long long)B * T, 256, num_sms * 8)), dim3(256), 0, s, part, out, B,
              T, Bcap, nchunk, cw);
     return cudaGetLastError();

@@ -83,6 +83,7 @@ struct Args {
     const float* bias;        // [weight groups][N]
     __half* hid;              // EPI_GELU output rows (same row index as A), fp16
     int hid_tma;              // EPI_GELU, uniform groups: store through shared memory with TMA (output map)
+    long long rows_cap;       // rows of the output, residual and statistics buffers (bounds-checked build)
     const __half* resid;      // EPI_RESID residual rows (same row index as A), fp16
     __half* z;                // EPI_RESID output rows (fp16)
     float2* stats;            // EPI_RESID row partials [row][nchunk]
@@ -215,6 +216,8 @@ __device__ __forceinline__ void epilogue_gelu_tma(const Args& args, const TileCo
 template <int COLS, int EPI>
 __device__ __forceinline__ void epilogue_tile(const Args& args, const TileCoord& tc, bool valid, long long arow,
                                               uint32_t tbase, int n0) {
+    // bounds-checked build: a row inside the group must lie inside the buffers
+    if (valid && !RM_IN_BOUNDS(arow >= 0 && arow < args.rows_cap && n0 + COLS <= args.N, args.err)) valid = false;
     const size_t orow = (size_t)arow * (size_t)args.N + n0;
     const float* bias = args.bias + (size_t)tc.wg * args.N + n0;
     if (EPI == EPI_GELU) {
@@ -1144,6 +1147,9 @@ pffn_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
             const int f = fb * 128 + q * 32 + lane;                      // this lane's output feature
             const float bf = __ldg(args.bias + (size_t)wg * args.N + f);
             const size_t row0 = (size_t)j * (size_t)args.a_group_rows;   // row of batch 0 of this group
+            // bounds-checked build: the unit's rows and features lie inside the buffers
+            const bool uok = RM_IN_BOUNDS((long long)row0 + args.M <= args.rows_cap && args.M <= args.a_group_rows &&
+                                              fb * 128 + 128 <= args.N, args.err);
             if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err, args.timeout_ns)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * NB);
@@ -1165,8 +1171,9 @@ pffn_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
                         if (b >= args.M) break;
                         float g0, g1;
                         f2_unpack(gelu_erf_x2(f2_pack(v[i], v[i + 1]), f2_splat(bf)), g0, g1);
-                        args.hid[(row0 + b) * (size_t)args.N + f] = __float2half_rn(sat_f16(g0));
-                        if (b + 1 < args.M) args.hid[(row0 + b + 1) * (size_t)args.N + f] = __float2half_rn(sat_f16(g1));
+                        if (uok) args.hid[(row0 + b) * (size_t)args.N + f] = __float2half_rn(sat_f16(g0));
+                        if (uok && b + 1 < args.M)
+                            args.hid[(row0 + b + 1) * (size_t)args.N + f] = __float2half_rn(sat_f16(g1));
                     }
                 } else {   // EPI_RESID
                     // the residuals of the chunk's rows first, all loads in flight together
@@ -1174,14 +1181,14 @@ pffn_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
 #pragma unroll
                     for (int i = 0; i < CW; ++i) {
                         const int b = c + i;
-                        rres[i] = b < args.M ? __half2float(args.resid[(row0 + b) * (size_t)args.N + f]) : 0.f;
+                        rres[i] = (uok && b < args.M) ? __half2float(args.resid[(row0 + b) * (size_t)args.N + f]) : 0.f;
                     }
 #pragma unroll
                     for (int i = 0; i < CW; ++i) {
                         const int b = c + i;                               // batch row (warp-uniform)
                         if (b >= args.M) break;
                         const float z = v[i] + bf + rres[i];
-                        args.z[(row0 + b) * (size_t)args.N + f] = __float2half_rn(sat_f16(z));
+                        if (uok) args.z[(row0 + b) * (size_t)args.N + f] = __float2half_rn(sat_f16(z));
                         // this warp's 32 features: mean and M2 about it
                         const float mw = warp_sum(z) * (1.0f / 32.0f);
                         const float d = z - mw;
@@ -1206,7 +1213,7 @@ pffn_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
                         const float d0 = m0 - mean, d1 = m1 - mean, d2 = m2 - mean, d3 = m3 - mean;
                         const float M2 = s2[b] + s2[NB + b] + s2[2 * NB + b] + s2[3 * NB + b] +
                                          32.0f * (d0 * d0 + d1 * d1 + d2 * d2 + d3 * d3);
-                        args.stats[(row0 + b) * (size_t)args.nchunk + fb] = make_float2(mean, M2);
+                        if (uok) args.stats[(row0 + b) * (size_t)args.nchunk + fb] = make_float2(mean, M2);
                     }
                 }
             }
@@ -1335,8 +1342,12 @@ cudaError_t launch_gemm1_tc(const void* S, const void* W1p, const float* b1, voi
     a.bias = b1;
     a.hid = reinterpret_cast<__half*>(Hid);
     a.hid_tma = 1;
+    a.rows_cap = (long long)T * Bcap;
     a.err = err;
     a.timeout_ns = timeout_ns;
+    RM_HOST_BOUNDS(B <= Bcap && D % tc::BK == 0 && F % tc::BK == 0 && S && W1p && b1 && Hid);
+    RM_HOST_BOUNDS(((reinterpret_cast<uintptr_t>(S) | reinterpret_cast<uintptr_t>(W1p) | reinterpret_cast<uintptr_t>(Hid)) &
+                    15u) == 0);
     return tc::run_dense<tc::EPI_GELU>(tc::pick_bn(F), S, (long long)T * Bcap, W1p, T, a, num_sms, s);
 }
 
@@ -1359,8 +1370,12 @@ cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, c
     a.z = reinterpret_cast<__half*>(Z);
     a.stats = stats;
     a.nchunk = D / (bn / 2);
+    a.rows_cap = (long long)T * Bcap;
     a.err = err;
     a.timeout_ns = timeout_ns;
+    RM_HOST_BOUNDS(B <= Bcap && D % tc::BK == 0 && F % tc::BK == 0 && Hid && W2p && b2 && S && Z && stats);
+    RM_HOST_BOUNDS(((reinterpret_cast<uintptr_t>(Hid) | reinterpret_cast<uintptr_t>(W2p) | reinterpret_cast<uintptr_t>(S) |
+                     reinterpret_cast<uintptr_t>(Z)) & 15u) == 0);
     return tc::run_dense<tc::EPI_RESID>(bn, Hid, (long long)T * Bcap, W2p, T, a, num_sms, s);
 }
 
@@ -1379,8 +1394,10 @@ cudaError_t launch_moe_gemm1_tc(const void* Sg, long long rows_total, const void
     a.tile_prefix = tile_prefix;
     a.bias = b1;
     a.hid = reinterpret_cast<__half*>(Hm);
+    a.rows_cap = rows_total;
     a.err = err;
     a.timeout_ns = timeout_ns;
+    RM_HOST_BOUNDS(D % tc::BK == 0 && Fe % tc::BK == 0 && Sg && W1p && b1 && Hm && g_count && g_off && tile_prefix);
     if (tile_prefix256 && tc::pick_bn(Fe) >= 128) {     // CTA-pair tiles over 256-row tiles
         a.tile_prefix = tile_prefix256;
         return tc::run_pair_bn<tc::EPI_GELU, 8>(tc::pick_bn(Fe), tc::use_ksub2(D, tc::EPI_GELU), Sg, rows_total,
@@ -1405,8 +1422,10 @@ cudaError_t launch_moe_gemm2_tc(const void* Hm, long long rows_total, const void
     a.bias = b2;
     a.hid = reinterpret_cast<__half*>(Y);
     a.row_gate = row_gate;
+    a.rows_cap = rows_total;
     a.err = err;
     a.timeout_ns = timeout_ns;
+    RM_HOST_BOUNDS(D % tc::BK == 0 && Fe % tc::BK == 0 && Hm && W2p && b2 && Y && row_gate && g_count && g_off);
     if (tile_prefix256 && tc::pick_bn(D) >= 128) {      // CTA-pair tiles over 256-row tiles
         a.tile_prefix = tile_prefix256;
         return tc::run_pair_bn<tc::EPI_GATED, 8>(tc::pick_bn(D), tc::use_ksub2(Fe, tc::EPI_GATED), Hm, rows_total,

@@ -15,6 +15,26 @@ enum class Act { F32 = 0, BF16 = 1 };
 // Device error word values (latched with atomicCAS from 0).
 constexpr int kDevErrTimeout = 5;
 constexpr int kDevErrOther = 6;
+constexpr int kDevErrBounds = 7;    // a device-side bounds guard of the debug build fired
+
+// Bounds-checked debug build (compiled with -DRM_DEBUG_BOUNDS, library
+// librankmixer_debug.so): the launchers check their sizes, strides and
+// alignments against the buffers they describe before any launch, and the
+// kernels guard their global-memory accesses with RM_IN_BOUNDS, which latches
+// kDevErrBounds in the context's error word and skips the access.  In the
+// normal build both compile to nothing.
+#ifdef RM_DEBUG_BOUNDS
+constexpr bool kDebugBounds = true;
+#else
+constexpr bool kDebugBounds = false;
+#endif
+// Host-side launcher check of the debug build: a failed condition returns
+// cudaErrorInvalidValue from the launcher with the condition's text recorded.
+cudaError_t debug_bounds_fail(const char* what);
+#define RM_HOST_BOUNDS(cond)                                                   \
+    do {                                                                       \
+        if (::rm::kDebugBounds && !(cond)) return ::rm::debug_bounds_fail(#cond); \
+    } while (0)
 
 inline size_t act_size(Act a) { return a == Act::F32 ? 4 : 2; }
 inline size_t op_size(Act a) { return a == Act::F32 ? 4 : 2; }

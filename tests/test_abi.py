@@ -157,3 +157,16 @@ def test_allocation_hooks_answer_without_a_device(lib):
     assert lib.rm_debug_alloc_stats(None, None, None) == _lib.RM_OK
     assert lib.rm_debug_fail_alloc(3) == _lib.RM_OK
     assert lib.rm_debug_fail_alloc(-1) == _lib.RM_OK
+
+
+def test_binding_selects_the_bounds_checked_build_by_environment():
+    import subprocess
+    import sys
+    code = ("import sys; sys.path.insert(0, %r); from rankmixer_feature_interaction_gb300 import _lib; "
+            "print(_lib.LIB_NAME)" % ROOT)
+    for env_value, want in ((None, "librankmixer.so"), ("debug", "librankmixer_debug.so")):
+        env = {k: v for k, v in os.environ.items() if k != "RM_LIBRARY"}
+        if env_value:
+            env["RM_LIBRARY"] = env_value
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=120)
+        assert r.returncode == 0 and r.stdout.strip() == want, r.stdout + r.stderr
