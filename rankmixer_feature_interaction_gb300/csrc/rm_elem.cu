@@ -320,6 +320,17 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
     if (!DBG && pre_lane && (int)blockIdx.x < nitems)
         pre = __ldg(a.stats + (size_t)pre_t * a.Bcap + (int)blockIdx.x / rsplit);
 
+    // the lane's gather offsets inside a staged sample, one per 8-column group i:
+    // output column j0 = 256 i + 8 lane of row h reads row t = j0 / q at column
+    // h q + (j0 - t q) -- the same t and remainder for every row h and sample
+    int goff[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int j0 = (i << 8) + (lane << 3);
+        const int t = j0 / q;
+        goff[i] = t * RS + (j0 - t * q);
+    }
+
     if (warp == 0 && (int)blockIdx.x < nitems) issue((int)blockIdx.x / rsplit, 0);
     int it = 0;
     for (int w = blockIdx.x; w < nitems; w += gridDim.x, ++it) {
@@ -343,25 +354,33 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
         __syncthreads();
         if (*s_abort) break;
         uint16_t* xs = buf + (size_t)slot * buf_elems;
-        const bool inplace = FROM_Z && a.ln2_inplace;
-        if (inplace) {
+        if (FROM_Z) {
             // X_{n-1} = LN2(Z) in place (fp16), 8 elements per lane
+            const int nvz = D >> 8;
             for (int t = warp; t < T; t += nwarps) {
                 const float mt = s_mean[t], rt = s_rstd[t];
                 uint16_t* row = xs + (size_t)t * RS;
                 // (z - mean) (rstd gamma) + beta on fp16 pairs: the result is stored in
-                // fp16, and the row statistics themselves were merged in fp32
+                // fp16, and the row statistics themselves were merged in fp32.  All of
+                // the lane's 16-byte groups of the row are loaded before any is used.
                 const __half2 m2 = __float2half2_rn(mt), r2 = __float2half2_rn(rt);
-                for (int c = lane * 8; c < D; c += 256) {
-                    uint4 zv = *reinterpret_cast<const uint4*>(row + c);
-                    const uint4 gv = *reinterpret_cast<const uint4*>(sg2 + c);
-                    const uint4 bv = *reinterpret_cast<const uint4*>(sb2 + c);
-                    __half2* z2 = reinterpret_cast<__half2*>(&zv);
-                    const __half2* g2h = reinterpret_cast<const __half2*>(&gv);
-                    const __half2* b2h = reinterpret_cast<const __half2*>(&bv);
+                uint4 zv[NV];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) z2[k] = __hfma2(__hsub2(z2[k], m2), __hmul2(r2, g2h[k]), b2h[k]);
-                    *reinterpret_cast<uint4*>(row + c) = zv;
+                for (int i = 0; i < NV; ++i)
+                    if (i < nvz) zv[i] = *reinterpret_cast<const uint4*>(row + (i << 8) + lane * 8);
+#pragma unroll
+                for (int i = 0; i < NV; ++i) {
+                    if (i < nvz) {
+                        const int c = (i << 8) + lane * 8;
+                        const uint4 gv = *reinterpret_cast<const uint4*>(sg2 + c);
+                        const uint4 bv = *reinterpret_cast<const uint4*>(sb2 + c);
+                        __half2* z2 = reinterpret_cast<__half2*>(&zv[i]);
+                        const __half2* g2h = reinterpret_cast<const __half2*>(&gv);
+                        const __half2* b2h = reinterpret_cast<const __half2*>(&bv);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) z2[k] = __hfma2(__hsub2(z2[k], m2), __hmul2(r2, g2h[k]), b2h[k]);
+                        *reinterpret_cast<uint4*>(row + c) = zv[i];
+                    }
                 }
             }
             __syncthreads();
@@ -376,45 +395,15 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
             const uint16_t* xh = xs + (size_t)h * RS;
             uint64_t y[4 * NV];
             uint64_t s2 = f2_splat(0.f);
-            // LN2 of row h (the residual operand) when it is applied as the values are read
-            __half2 mh2 = __float2half2_rn(0.f), rh2 = mh2;
-            if (FROM_Z && !inplace) {
-                mh2 = __float2half2_rn(s_mean[h]);
-                rh2 = __float2half2_rn(s_rstd[h]);
-            }
 #pragma unroll
             for (int i = 0; i < NV; ++i) {
                 if (i < nv) {
                     const int j0 = (i << 8) + (lane << 3);
-                    const int t = j0 / q;
-                    const int r = j0 - t * q;
-                    const bool gok = RM_IN_BOUNDS(t < T && h * q + r + 8 <= RS && j0 + 8 <= RS, a.err);
-                    const uint4 mv = gok ? *reinterpret_cast<const uint4*>(xs + (size_t)t * RS + h * q + r)
+                    const bool gok = RM_IN_BOUNDS(goff[i] + h * q + 8 <= T * RS && j0 + 8 <= RS, a.err);
+                    const uint4 mv = gok ? *reinterpret_cast<const uint4*>(xs + goff[i] + h * q)
                                          : make_uint4(0u, 0u, 0u, 0u);
                     const uint4 xv = gok ? *reinterpret_cast<const uint4*>(xh + j0) : make_uint4(0u, 0u, 0u, 0u);
-                    uint32_t mw[4] = {mv.x, mv.y, mv.z, mv.w}, xw[4] = {xv.x, xv.y, xv.z, xv.w};
-                    if (FROM_Z && !inplace) {
-                        // (z - mean) (rstd gamma) + beta in fp16 pairs, the operations of the
-                        // in-place pass: source row t at columns h q + r.., row h at j0..
-                        const uint4 gs = *reinterpret_cast<const uint4*>(sg2 + h * q + r);
-                        const uint4 bs = *reinterpret_cast<const uint4*>(sb2 + h * q + r);
-                        const uint4 gx = *reinterpret_cast<const uint4*>(sg2 + j0);
-                        const uint4 bx = *reinterpret_cast<const uint4*>(sb2 + j0);
-                        const __half2 mt2 = __float2half2_rn(s_mean[t]), rt2 = __float2half2_rn(s_rstd[t]);
-                        const __half2* gsh = reinterpret_cast<const __half2*>(&gs);
-                        const __half2* bsh = reinterpret_cast<const __half2*>(&bs);
-                        const __half2* gxh = reinterpret_cast<const __half2*>(&gx);
-                        const __half2* bxh = reinterpret_cast<const __half2*>(&bx);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const __half2 zm = __hfma2(__hsub2(*reinterpret_cast<const __half2*>(&mw[k]), mt2),
-                                                       __hmul2(rt2, gsh[k]), bsh[k]);
-                            const __half2 zx = __hfma2(__hsub2(*reinterpret_cast<const __half2*>(&xw[k]), mh2),
-                                                       __hmul2(rh2, gxh[k]), bxh[k]);
-                            mw[k] = *reinterpret_cast<const uint32_t*>(&zm);
-                            xw[k] = *reinterpret_cast<const uint32_t*>(&zx);
-                        }
-                    }
+                    const uint32_t mw[4] = {mv.x, mv.y, mv.z, mv.w}, xw[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         if constexpr (FROM_Z) {     // fp16 rows: add in fp16, convert once
@@ -490,20 +479,6 @@ bool v8_ok(bool, const MixLnArgs& a) {
     return a.q % 8 == 0 && a.D % 256 == 0 && a.D <= 3072 && a.T <= kMaxT && v8_smem_bytes(a.T, a.D, a.q) <= 226 * 1024;
 }
 
-// From Z, LN2 is finalised in place over the staged sample before the mixing
-// pass.  RM_MIX_LN2_INPLACE=0 in the environment applies it instead to each
-// value as the mixing reads it (one barrier fewer per sample, twice the LN2
-// arithmetic): the same bits, and no faster in measurement (within 0.5% per
-// step either way at the 1B shape), so a tuning switch only.
-bool mix_ln2_inplace() {
-    static int env = -1;
-    if (env < 0) {
-        const char* v = getenv("RM_MIX_LN2_INPLACE");
-        env = (v && v[0] == '0') ? 0 : 1;
-    }
-    return env == 1;
-}
-
 template <bool FROM_Z, int NV, bool DBG = false>
 cudaError_t launch_v8(const MixLnArgs& a, int num_sms, cudaStream_t s) {
     auto k = mix_ln1_v8_kernel<FROM_Z, NV, DBG>;
@@ -521,7 +496,6 @@ cudaError_t launch_v8(const MixLnArgs& a, int num_sms, cudaStream_t s) {
     MixLnArgs b = a;
     const int slots = num_sms * per_sm;
     b.rsplit = 1;
-    b.ln2_inplace = mix_ln2_inplace() ? 1 : 0;
     if (a.B < slots) {
         int r = slots / a.B;
         if (r > a.T / 2) r = a.T / 2;

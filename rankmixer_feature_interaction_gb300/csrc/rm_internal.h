@@ -91,10 +91,6 @@ struct MixLnArgs {
     float* Ydbg;
     // staged 8-wide kernel: CTAs per sample (set by its launcher; 0 or 1: one)
     int rsplit;
-    // staged 8-wide kernel from Z: 1 finalises LN2 in place over the staged
-    // sample before mixing (set by its launcher); 0 applies it to each value as
-    // the mixing reads it (the same fp16 operations, so the same bits)
-    int ln2_inplace;
 };
 
 // S = LN1(Mix(X) + X).
