@@ -355,31 +355,39 @@ mix_ln1_v8_kernel(const MixLnArgs a) {
         if (*s_abort) break;
         uint16_t* xs = buf + (size_t)slot * buf_elems;
         if (FROM_Z) {
-            // X_{n-1} = LN2(Z) in place (fp16), 8 elements per lane
-            const int nvz = D >> 8;
-            for (int t = warp; t < T; t += nwarps) {
-                const float mt = s_mean[t], rt = s_rstd[t];
-                uint16_t* row = xs + (size_t)t * RS;
-                // (z - mean) (rstd gamma) + beta on fp16 pairs: the result is stored in
-                // fp16, and the row statistics themselves were merged in fp32.  All of
-                // the lane's 16-byte groups of the row are loaded before any is used.
-                const __half2 m2 = __float2half2_rn(mt), r2 = __float2half2_rn(rt);
-                uint4 zv[NV];
+            // X_{n-1} = LN2(Z) in place (fp16), 8 columns per thread: a thread keeps one
+            // 8-column group (its gamma2 / beta2 loaded once) and walks every nsl-th
+            // row, so the affines cost one shared-memory load per group instead of
+            // one per group and row; rows are loaded four at a time before use.
+            // (z - mean) (rstd gamma) + beta on fp16 pairs: the result is stored in
+            // fp16, and the row statistics themselves were merged in fp32.
+            const int ngr = D >> 3;
+            const int nsl = blockDim.x >= ngr ? (int)blockDim.x / ngr : 1;
+            for (int wi = threadIdx.x; wi < ngr * nsl; wi += blockDim.x) {
+                const int cg = wi % ngr, sl = wi / ngr;
+                const int c = cg << 3;
+                const uint4 gv = *reinterpret_cast<const uint4*>(sg2 + c);
+                const uint4 bv = *reinterpret_cast<const uint4*>(sb2 + c);
+                const __half2* g2h = reinterpret_cast<const __half2*>(&gv);
+                const __half2* b2h = reinterpret_cast<const __half2*>(&bv);
+                for (int t0 = sl; t0 < T; t0 += 4 * nsl) {
+                    uint4 zv[4];
 #pragma unroll
-                for (int i = 0; i < NV; ++i)
-                    if (i < nvz) zv[i] = *reinterpret_cast<const uint4*>(row + (i << 8) + lane * 8);
+                    for (int u = 0; u < 4; ++u) {
+                        const int t = t0 + u * nsl;
+                        if (t < T) zv[u] = *reinterpret_cast<const uint4*>(xs + (size_t)t * RS + c);
+                    }
 #pragma unroll
-                for (int i = 0; i < NV; ++i) {
-                    if (i < nvz) {
-                        const int c = (i << 8) + lane * 8;
-                        const uint4 gv = *reinterpret_cast<const uint4*>(sg2 + c);
-                        const uint4 bv = *reinterpret_cast<const uint4*>(sb2 + c);
-                        __half2* z2 = reinterpret_cast<__half2*>(&zv[i]);
-                        const __half2* g2h = reinterpret_cast<const __half2*>(&gv);
-                        const __half2* b2h = reinterpret_cast<const __half2*>(&bv);
+                    for (int u = 0; u < 4; ++u) {
+                        const int t = t0 + u * nsl;
+                        if (t < T) {
+                            const __half2 m2 = __float2half2_rn(s_mean[t]), r2 = __float2half2_rn(s_rstd[t]);
+                            __half2* z2 = reinterpret_cast<__half2*>(&zv[u]);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) z2[k] = __hfma2(__hsub2(z2[k], m2), __hmul2(r2, g2h[k]), b2h[k]);
-                        *reinterpret_cast<uint4*>(row + c) = zv[i];
+                            for (int k = 0; k < 4; ++k)
+                                z2[k] = __hfma2(__hsub2(z2[k], m2), __hmul2(r2, g2h[k]), b2h[k]);
+                            *reinterpret_cast<uint4*>(xs + (size_t)t * RS + c) = zv[u];
+                        }
                     }
                 }
             }
