@@ -231,49 +231,74 @@ template <> __device__ __forceinline__ uint32_t to_f16x2<__nv_bfloat16>(uint32_t
 }
 
 constexpr int kMmaWarps = 4;
-constexpr int kMmaTilesPerWarp = 4;      // 16-sample tiles per warp per CTA
+constexpr int kMmaTilesPerWarp = 8;      // 16-sample tiles per warp per CTA (the fragments of W_B^j are loaded once per warp)
 
+// K and N are permuted inside each 16 x BS tile so that a lane's operands and
+// results are contiguous in memory: lane (g, c) holds, for its rows g and
+// g + 8, the physical input columns [4 KS c, 4 KS (c + 1)) -- in k-step ks the
+// fragment slots a0/a1 take columns 4 KS c + 4 ks + {0, 1} and a2/a3 take
+// + {2, 3} -- and writes the physical output columns [2 NT c, 2 NT (c + 1)),
+// n-tile nt's pair at 2 NT c + 2 nt.  The B fragments read W_B^j under the same
+// two maps (logical column n = 8 nt + g of an n-tile is physical column
+// 2 NT (g >> 1) + 2 nt + (g & 1)), so every output is the sum over the same k
+// of the same products.  A lane then loads KS 8-byte words per row and stores
+// NT / 2 8-byte words per row, and the next tile's words are loaded before the
+// current tile's products.
 template <typename Tin, int BS>
 __global__ void __launch_bounds__(32 * kMmaWarps)
 unimix_local_mma_kernel(const Tin* __restrict__ X, long long x_stride, const __half* __restrict__ WBt,
                         __half* __restrict__ H, int B, long long Npitch, long long Npad) {
     constexpr int KS = BS / 16, NT = BS / 8;
+    static_assert(NT % 2 == 0, "output words of two n-tiles");
     const int j = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
-    // B fragments: B[k][n] = WB_j[k][n] = WBt[j][n][k]
+    // B fragments: B[k][n] = WB_j[k][n] = WBt[j][n][k], physical k and n as above
     uint32_t bf[KS][NT][2];
     const __half* w = WBt + (size_t)j * BS * BS;
+    const int ncol0 = (g >> 1) * 2 * NT + (g & 1);
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            const __half* row = w + (size_t)(nt * 8 + g) * BS + ks * 16 + 2 * c;
+            const __half* row = w + (size_t)(ncol0 + 2 * nt) * BS + 4 * KS * c + 4 * ks;
             bf[ks][nt][0] = __ldg(reinterpret_cast<const uint32_t*>(row));
-            bf[ks][nt][1] = __ldg(reinterpret_cast<const uint32_t*>(row + 8));
+            bf[ks][nt][1] = __ldg(reinterpret_cast<const uint32_t*>(row + 2));
         }
     __half* hrow = H + (size_t)j * Npitch;
     const long long tile0 = ((long long)blockIdx.x * kMmaWarps + warp) * kMmaTilesPerWarp;
+    // this lane's words of a tile: rows b0 + g and b0 + g + 8, KS 8-byte words each
+    auto load_tile = [&](long long b0, uint2 (&x0w)[KS], uint2 (&x1w)[KS]) {
+        const long long r0 = b0 + g, r1 = b0 + g + 8;
+        const Tin* x0 = X + r0 * x_stride + (long long)j * BS + 4 * KS * c;
+        const Tin* x1 = X + r1 * x_stride + (long long)j * BS + 4 * KS * c;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            x0w[ks] = r0 < B ? __ldg(reinterpret_cast<const uint2*>(x0) + ks) : make_uint2(0u, 0u);
+            x1w[ks] = r1 < B ? __ldg(reinterpret_cast<const uint2*>(x1) + ks) : make_uint2(0u, 0u);
+        }
+    };
+    uint2 n0w[KS], n1w[KS];
+    if (tile0 * 16 < B) load_tile(tile0 * 16, n0w, n1w);
 #pragma unroll 1
     for (int it = 0; it < kMmaTilesPerWarp; ++it) {
         const long long b0 = (tile0 + it) * 16;
         if (b0 >= B) break;
-        const long long r0 = b0 + g, r1 = b0 + g + 8;
-        const bool v0 = r0 < B, v1 = r1 < B;
-        const Tin* x0 = X + r0 * x_stride + (long long)j * BS + 2 * c;
-        const Tin* x1 = X + r1 * x_stride + (long long)j * BS + 2 * c;
+        uint2 x0w[KS], x1w[KS];
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            x0w[ks] = n0w[ks];
+            x1w[ks] = n1w[ks];
+        }
+        if (it + 1 < kMmaTilesPerWarp && b0 + 16 < B) load_tile(b0 + 16, n0w, n1w);
         uint32_t af[KS][4];
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
-            af[ks][0] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(x0 + ks * 16)) : 0u;
-            af[ks][1] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(x1 + ks * 16)) : 0u;
-            af[ks][2] = v0 ? __ldg(reinterpret_cast<const uint32_t*>(x0 + ks * 16 + 8)) : 0u;
-            af[ks][3] = v1 ? __ldg(reinterpret_cast<const uint32_t*>(x1 + ks * 16 + 8)) : 0u;
+            af[ks][0] = to_f16x2<Tin>(x0w[ks].x);
+            af[ks][1] = to_f16x2<Tin>(x1w[ks].x);
+            af[ks][2] = to_f16x2<Tin>(x0w[ks].y);
+            af[ks][3] = to_f16x2<Tin>(x1w[ks].y);
         }
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) af[ks][q] = to_f16x2<Tin>(af[ks][q]);
         float acc[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
@@ -281,10 +306,15 @@ unimix_local_mma_kernel(const Tin* __restrict__ X, long long x_stride, const __h
         for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) mma_f16(acc[nt], af[ks], bf[ks][nt][0], bf[ks][nt][1]);
+        const long long r0 = b0 + g, r1 = b0 + g + 8;
+        uint2* o0 = reinterpret_cast<uint2*>(hrow + r0 * BS + 2 * NT * c);
+        uint2* o1 = reinterpret_cast<uint2*>(hrow + r1 * BS + 2 * NT * c);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            if (v0) *reinterpret_cast<uint32_t*>(hrow + r0 * BS + nt * 8 + 2 * c) = pack_f16x2(acc[nt][0], acc[nt][1]);
-            if (v1) *reinterpret_cast<uint32_t*>(hrow + r1 * BS + nt * 8 + 2 * c) = pack_f16x2(acc[nt][2], acc[nt][3]);
+        for (int m = 0; m < NT / 2; ++m) {
+            if (r0 < B)
+                o0[m] = make_uint2(pack_f16x2(acc[2 * m][0], acc[2 * m][1]), pack_f16x2(acc[2 * m + 1][0], acc[2 * m + 1][1]));
+            if (r1 < B)
+                o1[m] = make_uint2(pack_f16x2(acc[2 * m][2], acc[2 * m][3]), pack_f16x2(acc[2 * m + 1][2], acc[2 * m + 1][3]));
         }
     }
     if (blockIdx.x == 0) {
