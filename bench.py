@@ -505,8 +505,9 @@ def run_ours(args):
         "config": {"workload": f"{args.config} B={B} T={T} D={D} k={k} L={L}" + (f" E={E} Fe={Fe}" if moe else "")
                    + (f" d={d_tok}" if score else "")
                    + (f" unimixing bs={bs_um} tau={UNIMIX_TAU}" if unimix else ""),
-                   "batch_per_gpu": B, "global_batch": B * world, "parallelism": f"replicas x{world} (batch sharded" + (", gradients all-reduced)" if train and not moe and world > 1
-                                                                        else ")"),
+                   "batch_per_gpu": B, "global_batch": B * world,
+                   "parallelism": f"replicas x{world} (batch sharded"
+                   + (", gradients all-reduced)" if train and not moe and world > 1 else ")"),
                    "l2": "inputs larger than L2 (X0 %.0f MB, weights %.0f MB > 129 MB)" % (
                        X0.numel() * 2 / 1e6, m.info.weight_bytes / 1e6)},
         "tflops": round(flops_step * args.steps * world / (ms_max / 1e3) / 1e12, 1),
