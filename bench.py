@@ -425,9 +425,10 @@ def run_ours(args):
     peaks, peak_src = load_peaks()
     peak, peak_why = pick_tensor_peak(peaks, peak_src, ms_max / 1e3, clk)
     flops_gemm = 2.0 * B * T * D * (k * D)          # one GEMM launch of the dense PFFN (either layer)
-    gemm_kinds = ["moe_gemm1", "moe_gemm2"] if moe else ["gemm1", "gemm2"]
-    # flops per timed scope: one GEMM, or two (the backward's data-gradient pair and recompute pair)
-    scope_flops = {"gemm1": flops_gemm, "gemm2": flops_gemm, "bwd_wgrad": flops_gemm,
+    gemm_kinds = ["moe_gemm1", "moe_gemm2"] if moe else ["gemm1", "gemm2", "pffn"]
+    # flops per timed scope: one GEMM, or two (both FFN GEMMs of a layer in one launch, the
+    # backward's data-gradient pair and recompute pair)
+    scope_flops = {"gemm1": flops_gemm, "gemm2": flops_gemm, "pffn": 2 * flops_gemm, "bwd_wgrad": flops_gemm,
                    "bwd_dgrad": 2 * flops_gemm, "bwd_recompute": 2 * flops_gemm}
     # (bwd_recompute times the training forward of a layer: LN1 and both FFN layers)
     if train and not moe:
@@ -453,7 +454,8 @@ def run_ours(args):
         avg_ms = tot_ms / launches
         achieved = flops_launch / (avg_ms / 1e3) / 1e12
         kname = {"bwd_wgrad": "train_gemm_wgrad_tcgen05", "bwd_dgrad": "train_gemm_dgrad_tcgen05 (x2 per scope)",
-                 "bwd_recompute": "train_gemm_forward_tcgen05 (x2 per scope)"}.get(dom, f"pffn_{dom}_tcgen05")
+                 "bwd_recompute": "train_gemm_forward_tcgen05 (x2 per scope)",
+                 "pffn": "pffn_layer_tcgen05 (both FFN GEMMs of a layer)"}.get(dom, f"pffn_{dom}_tcgen05")
         roofline = {"kernel": kname, "bound": "tensor", "achieved": round(achieved, 1),
                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                     "traffic": captured_traffic(args.config, B, L, dom) if not (moe and train) else None,

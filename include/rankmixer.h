@@ -46,7 +46,7 @@
 extern "C" {
 #endif
 
-#define RM_ABI_VERSION 3
+#define RM_ABI_VERSION 4
 
 /* Public symbols are the only ones the shared library exports. */
 #if defined(__GNUC__)
@@ -169,7 +169,9 @@ typedef enum rm_kernel_kind {
     RM_K_TOKENIZE = 15,    /* feature tokenization: per-token projection of the embedding slices */
     RM_K_HEAD = 16,        /* prediction head on the pooled output */
     RM_K_UNIMIX = 17,      /* UniMixing: local block products, global product, residual + LN1 */
-    RM_K_COUNT = 18
+    RM_K_PFFN = 18,        /* both per-token FFN layers of a dense layer in one launch (B >= 256 on the
+                              tensor-core path): the work of RM_K_GEMM1 and RM_K_GEMM2 */
+    RM_K_COUNT = 19
 } rm_kernel_kind;
 
 typedef struct rm_kernel_stat {

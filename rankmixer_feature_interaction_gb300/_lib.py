@@ -38,7 +38,7 @@ RM_PATH_TCGEN05 = 2
 # rm_kernel_kind
 KERNEL_KINDS = ["mix_ln1", "gemm1", "gemm2", "ln2_out", "pool", "rowstats", "moe_route", "moe_gemm1",
                 "moe_gemm2", "misc", "moe_combine", "bwd_recompute", "bwd_dgrad", "bwd_wgrad", "bwd_rows",
-                "tokenize", "head", "unimix"]
+                "tokenize", "head", "unimix", "pffn"]
 RM_K_COUNT = len(KERNEL_KINDS)
 
 EXPORTED = ["rm_create", "rm_destroy", "rm_block_forward", "rm_stack_forward", "rm_stack_forward_host",

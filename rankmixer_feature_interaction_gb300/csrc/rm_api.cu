@@ -208,6 +208,9 @@ struct rm_ctx {
     void* Hid = nullptr;         // operand type
     void* Z = nullptr;           // pre-LN2 rows, operand type
     float2* stats = nullptr;     // GEMM2 epilogue partials: [T][Bcap][nchunk] (mean, M2) per column chunk
+    // row-block counters of the fused layer GEMM ([T][ceil(Bcap / 256)], only grow) and its launch count
+    unsigned* dep_cnt = nullptr;
+    unsigned dep_epoch = 0;
     float2* rows = nullptr;      // merged: [T][Bcap] (mean, M2) of each full pre-LN2 row
     // where the last PFFN left its LN2 row statistics for the consumers: the
     // merged rows, or (small batches) the GEMM2 chunk partials themselves
@@ -337,6 +340,7 @@ void free_ctx(rm_ctx* c) {
     device_free(c->ginfer); device_free(c->dX0h); device_free(c->tok_part); device_free(c->tok_inv);
     moe_free_workspace(c->moe_ws);
     device_free(c->S); device_free(c->Hid); device_free(c->Z); device_free(c->stats); device_free(c->rows); device_free(c->V);
+    device_free(c->dep_cnt);
     device_free(c->X0_dev); device_free(c->pooled_dev);
     for (int i = 0; i < kHostChunksMax; ++i) {
         if (c->ev_in[i]) cudaEventDestroy(c->ev_in[i]);
@@ -362,7 +366,7 @@ void free_ctx(rm_ctx* c) {
 const char* const kKindNames[RM_K_COUNT] = {
     "rm:mix_ln1", "rm:gemm1", "rm:gemm2", "rm:ln2_out", "rm:pool", "rm:rowstats", "rm:moe_route", "rm:moe_gemm1",
     "rm:moe_gemm2", "rm:misc", "rm:moe_combine", "rm:bwd_recompute", "rm:bwd_dgrad", "rm:bwd_wgrad",
-    "rm:bwd_rows", "rm:tokenize", "rm:head", "rm:unimix"};
+    "rm:bwd_rows", "rm:tokenize", "rm:head", "rm:unimix", "rm:pffn"};
 
 bool nvtx_on() {
     static int env = -1;
@@ -473,7 +477,14 @@ rm_status run_pffn(rm_ctx* c, int layer, int B, cudaStream_t s) {
         c->ln2_cw = g.D;
         return RM_OK;
     }
-    if (c->use_tc) {
+    if (c->use_tc && c->dep_cnt && layer_tc_fusable(B, g.D, c->F)) {
+        // both GEMMs in one launch (the same bits as the two launches below)
+        ProfScope ps(c, RM_K_PFFN, s);
+        cudaError_t e = launch_layer_tc(c->S, w.W1p, w.b1, c->Hid, w.W2p, w.b2, c->Z, c->stats, B, g.T, g.D, c->F,
+                                        c->Bcap, c->num_sms, c->dep_cnt, c->dep_epoch, c->d_err, kWaitTimeoutNs, s);
+        if (e != cudaSuccess) return cuda_fail(e, (std::string("ffn layer (tcgen05) ") + tc_last_error()).c_str());
+        ++c->dep_epoch;
+    } else if (c->use_tc) {
         {
             ProfScope ps(c, RM_K_GEMM1, s);
             cudaError_t e = launch_gemm1_tc(c->S, w.W1p, w.b1, c->Hid, B, g.T, g.D, c->F, c->Bcap, c->num_sms,
@@ -486,6 +497,8 @@ rm_status run_pffn(rm_ctx* c, int layer, int B, cudaStream_t s) {
                                             c->num_sms, c->d_err, kWaitTimeoutNs, s);
             if (e != cudaSuccess) return cuda_fail(e, (std::string("gemm2 (tcgen05) ") + tc_last_error()).c_str());
         }
+    }
+    if (c->use_tc) {
         if (B <= kMergeInConsumerMaxB) {
             // small batches: the consumers merge the chunk partials themselves (one
             // launch fewer; the merge costs them next to nothing at this size)
@@ -1027,6 +1040,18 @@ rm_status rm_create(const rm_config* cfg, const rm_layer_params* layers, int dev
         (st = dmalloc(c, (void**)&c->d_flag, sizeof(int), nullptr)) != RM_OK) {
         free_ctx(c);
         return st;
+    }
+    if (c->use_tc) {
+        const size_t ndep = T * (size_t)((Bc + 255) / 256);
+        if ((st = dmalloc(c, (void**)&c->dep_cnt, ndep * sizeof(unsigned), nullptr)) != RM_OK) {
+            free_ctx(c);
+            return st;
+        }
+        cudaError_t e = cudaMemset(c->dep_cnt, 0, ndep * sizeof(unsigned));
+        if (e != cudaSuccess) {
+            free_ctx(c);
+            return cuda_fail(e, "clear layer counters");
+        }
     }
     if (cfg->moe_layer_mask != 0 &&
         (st = dmalloc(c, (void**)&c->V, T * Bc * D * 4, &c->ws_bytes)) != RM_OK) {
@@ -1676,6 +1701,12 @@ rm_status rm_sync_status(rm_ctx* c, void* stream) {
     RM_CHECK_CUDA(cudaMemcpy(&code, c->d_err, sizeof(int), cudaMemcpyDeviceToHost), "read error word");
     if (code != 0) {
         RM_CHECK_CUDA(cudaMemset(c->d_err, 0, sizeof(int)), "clear error word");
+        // a launch that gave up may have left the fused layer's counters part-way: start them again
+        if (c->dep_cnt) {
+            const size_t ndep = (size_t)c->cfg.T * (size_t)((c->Bcap + 255) / 256);
+            RM_CHECK_CUDA(cudaMemset(c->dep_cnt, 0, ndep * sizeof(unsigned)), "clear layer counters");
+            c->dep_epoch = 0;
+        }
         RM_CHECK_CUDA(cudaDeviceSynchronize(), "clear error word");
         if (code == kDevErrTimeout) return fail(RM_ERR_TIMEOUT, "a device-side wait ran out of time");
         if (code == kDevErrBounds)

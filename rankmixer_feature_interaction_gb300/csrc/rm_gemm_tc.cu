@@ -711,6 +711,286 @@ pffn_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_const
 }
 
 // ----------------------------------------------------------------------------
+// Both FFN GEMMs of a dense layer in one launch (CTA pairs, 256 x 256 tiles,
+// 8 epilogue warps): the tile list is every GEMM1 tile (token-major) followed
+// by every GEMM2 tile, taken in a static order as in the kernel above.  A
+// GEMM2 tile (token j, row block mb) reads the hidden rows that the GEMM1
+// tiles (j, mb, every column block) wrote, so:
+//   - each epilogue warp of a GEMM1 tile, once its tensor stores of the tile
+//     are complete, adds 1 to the row block's counter dep[j m_tiles + mb]
+//     (async-proxy fence, then a device-scope fence, then the atomic);
+//   - the producer of a GEMM2 tile waits (bounded) until that counter has
+//     grown by n_tiles1 x 2 x 8 in this launch, then loads through TMA after
+//     an async-proxy fence.
+// A warp defers the signal of a GEMM1 tile to its next GEMM1 tile (by then
+// the stores have long landed) unless its next tile is not a GEMM1 tile.
+// Every GEMM1 tile depends on nothing, and every CTA is resident (one CTA per
+// SM, grid <= the SM count), so every wait ends; the bound turns a broken
+// assumption into an error instead of a hang.  Counters only grow: launch e
+// waits for base + target with base = e x target (wrap-safe comparison); the
+// counters of row blocks past this launch's batch get their target too (one
+// thread, at the end), so every counter grows by the same amount per launch
+// whatever the batch.
+// The per-tile arithmetic is that of the two separate launches, so the
+// results are the same bits.
+// ----------------------------------------------------------------------------
+struct LayerDep {
+    unsigned* cnt;        // [groups][m_cap]
+    unsigned base;        // counter value of a row block at the start of this launch
+    unsigned target;      // GEMM1 signals per row block and launch
+    int m_cap;            // row blocks per group the counters cover (the context's capacity)
+};
+
+__device__ __forceinline__ bool wait_counter_bounded(const unsigned* p, unsigned want, volatile int* abort, int* err,
+                                                     uint64_t timeout_ns) {
+    if ((int)(ld_acquire_gpu(p) - want) >= 0) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        __nanosleep(128);
+        if ((int)(ld_acquire_gpu(p) - want) >= 0) return true;
+        if ((it & 31u) == 0u) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > timeout_ns) {
+                *abort = 1;
+                latch_error(err, kDevErrTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+template <int KSUB>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg2<256, 8, KSUB>::THREADS, 1)
+pffn_layer_tc2_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
+                      const __grid_constant__ CUtensorMap tmC1, const __grid_constant__ CUtensorMap tmA2,
+                      const __grid_constant__ CUtensorMap tmB2, const Args a1, const Args a2, const LayerDep dep) {
+    constexpr int BN = 256, EPW = 8;
+    using C = Cfg2<BN, EPW, KSUB>;
+    constexpr int kGroupsPerTile = C::COLS_PER_WARP / 32;     // tensor-store groups a warp commits per GEMM1 tile
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t* base_ptr = smem_raw + (base - raw_addr);
+    const uint32_t sA = base;
+    const uint32_t sB = base + C::STAGES * C::A_BYTES;
+    const uint32_t sEpi = base + C::STAGES * C::STAGE_BYTES;
+    const uint32_t bar0 = sEpi + C::EPI_BYTES;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
+    uint32_t* tmem_holder =
+        reinterpret_cast<uint32_t*>(base_ptr + C::STAGES * C::STAGE_BYTES + C::EPI_BYTES + 8 * (2 * C::STAGES + 4));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const long long pair = blockIdx.x >> 1;
+    const long long npairs = gridDim.x >> 1;
+
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA1);
+        tma_prefetch_desc(&tmB1);
+        tma_prefetch_desc(&tmA2);
+        tma_prefetch_desc(&tmB2);
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 2 * EPW);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 2) {
+        tmem_alloc_pair(smem_u32(tmem_holder), C::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
+    pdl_wait();              // S comes from the previous kernel of the stream
+    pdl_launch_next();
+
+    const long long tiles1 = a1.tiles, tiles = a1.tiles + a2.tiles;
+    const int kblocks1 = a1.K / (BK * KSUB), kblocks2 = a2.K / (BK * KSUB);
+
+    if (warp == 0) {
+        // ---------------------------- TMA producer (both CTAs) ----------------------------
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (long long tile = pair; ok && tile < tiles; tile += npairs) {
+            const bool g1 = tile < tiles1;
+            const Args& a = g1 ? a1 : a2;
+            const TileCoord tc = decode_tile(g1 ? tile : tile - tiles1, a);
+            const CUtensorMap* mA = g1 ? &tmA1 : &tmA2;
+            const CUtensorMap* mB = g1 ? &tmB1 : &tmB2;
+            if (!g1) {
+                // the hidden rows of (j, mb): every GEMM1 tile of the row block has signalled
+                int done = 1;
+                if (lane == 0) {
+                    done = wait_counter_bounded(dep.cnt + (size_t)tc.j * dep.m_cap + tc.mb, dep.base + dep.target,
+                                                abort_flag, a.err, a.timeout_ns) ? 1 : 0;
+                    fence_proxy_async_global();
+                }
+                done = __shfl_sync(0xffffffffu, done, 0);
+                if (!done) break;
+            }
+            const int arow = tc.mb * BM2 + 128 * (int)rank;
+            const int brow = tc.nb * BN + (BN / 2) * (int)rank;
+            const int kblocks = g1 ? kblocks1 : kblocks2;
+            for (int kb = 0; kb < kblocks; ++kb) {
+                if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, a.err, a.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    const uint32_t fb = mapa_shared(full_bar(stage), 0);
+                    if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), (uint32_t)(2 * C::STAGE_BYTES));
+#pragma unroll
+                    for (int ks = 0; ks < KSUB; ++ks) {
+                        const int kx = (kb * KSUB + ks) * BK;
+                        tma_load_3d_pair(mA, sA + stage * C::A_BYTES + ks * C::A_SUB, fb, kx, arow, tc.j);
+                        tma_load_3d_pair(mB, sB + stage * C::B_BYTES + ks * C::B_SUB, fb, kx, brow, tc.wg);
+                    }
+                }
+                __syncwarp();
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------- pair MMA issuer (even CTA) --------------------------
+        if (rank == 0) {
+            constexpr uint32_t idesc = make_idesc_f16_f32(BM2, BN);
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            for (long long tile = pair; ok && tile < tiles; tile += npairs) {
+                const int kblocks = tile < tiles1 ? kblocks1 : kblocks2;
+                if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, a1.err, a1.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, a1.err, a1.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = sA + stage * C::A_BYTES;
+                    const uint32_t b0 = sB + stage * C::B_BYTES;
+                    if (lane == 0) {
+#pragma unroll
+                        for (int ks = 0; ks < KSUB; ++ks)
+#pragma unroll
+                            for (int k = 0; k < BK / 16; ++k)
+                                umma_f16_pair(d_tmem, make_sw128_desc(a0 + ks * C::A_SUB + 32u * k),
+                                              make_sw128_desc(b0 + ks * C::B_SUB + 32u * k), idesc,
+                                              (kb > 0 || ks > 0 || k > 0) ? 1u : 0u);
+                        umma_commit_pair_mc(empty_bar(stage), (uint16_t)0x3);
+                    }
+                    __syncwarp();
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                if (lane == 0) umma_commit_pair_mc(tfull_bar(acc), (uint16_t)0x3);
+                __syncwarp();
+                acc ^= 1;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+        }
+    } else if (warp >= 4) {
+        // ---------------------------- epilogue (both CTAs) --------------------------------
+        const int ew = warp - 4;
+        const int quad = warp & 3;
+        const int half = ew >> 2;
+        const int row_in_tile = quad * 32 + lane;
+        const uint32_t stage = sEpi + (uint32_t)ew * 4096u;
+        int sbuf = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        long long pending = -1;                 // counter of this warp's last GEMM1 tile, not yet signalled
+        auto signal = [&](long long idx) {      // lane 0: the stores are complete before this call
+            fence_proxy_async_global();
+            __threadfence();
+            atomicAdd(dep.cnt + idx, 1u);
+        };
+        for (long long tile = pair; tile < tiles; tile += npairs) {
+            const bool g1 = tile < tiles1;
+            const Args& a = g1 ? a1 : a2;
+            const TileCoord tc = decode_tile(g1 ? tile : tile - tiles1, a);
+            if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, a.err, a.timeout_ns)) break;
+            tc_fence_after();
+            const int m = tc.mb * BM2 + 128 * (int)rank + row_in_tile;
+            const bool valid = m < tc.Mg;
+            const long long arow = tc.row0 + m;
+            const uint32_t tbase =
+                tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN + half * C::COLS_PER_WARP);
+            const int n0 = tc.nb * BN + half * C::COLS_PER_WARP;
+            if (g1)
+                epilogue_gelu_tma<C::COLS_PER_WARP, true>(a1, tc, &tmC1, tbase, n0, m - lane, stage, lane, sbuf);
+            else
+                epilogue_tile<C::COLS_PER_WARP, EPI_RESID>(a2, tc, valid, arow, tbase, n0);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(tempty_bar(acc), 0));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+            if (g1) {
+                if (pending >= 0) {          // the previous GEMM1 tile: all but this tile's groups are complete
+                    if (lane == 0) {
+                        bulk_wait_group<kGroupsPerTile>();
+                        signal(pending);
+                    }
+                    __syncwarp();
+                }
+                pending = (long long)tc.j * dep.m_cap + tc.mb;
+                if (tile + npairs >= tiles1) {   // the next tile of this pair may wait on this one: signal now
+                    if (lane == 0) {
+                        bulk_wait_group<0>();
+                        signal(pending);
+                    }
+                    __syncwarp();
+                    pending = -1;
+                }
+            }
+        }
+        if (lane == 0) {
+            bulk_wait_group<0>();   // this warp's tensor stores have landed
+            if (pending >= 0) signal(pending);
+        }
+    } else if (warp == 3 && blockIdx.x == 0 && lane == 0) {
+        // the row blocks past this batch: no tile signals them, so they get their target here
+        for (int j = 0; j < a1.ngroups; ++j)
+            for (int mb = a1.m_tiles; mb < dep.m_cap; ++mb) atomicAdd(dep.cnt + (size_t)j * dep.m_cap + mb, dep.target);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// ----------------------------------------------------------------------------
 // Host side
 // ----------------------------------------------------------------------------
 std::mutex g_mu;
@@ -1301,7 +1581,124 @@ cudaError_t run_dense(int bn, const void* A, long long a_rows_total, const void*
     return run_bn<EPI>(bn, A, a_rows_total, W, n_wgroups, a, num_sms, s);
 }
 
+// Both FFN GEMMs of a layer in one launch (pffn_layer_tc2_kernel) whenever
+// both would run as 256 x 256 CTA-pair tiles; RM_GEMM_FUSED=0 in the
+// environment keeps the two launches (a tuning switch: the same bits).
+bool fused_enabled() {
+    static int env = -1;
+    if (env < 0) {
+        const char* v = getenv("RM_GEMM_FUSED");
+        env = (v && v[0] == '0') ? 0 : 1;
+    }
+    return env == 1;
+}
+
+template <int KSUB>
+cudaError_t run_layer(const void* S, const void* W1p, const void* W2p, Args a1, Args a2, unsigned* dep_cnt,
+                      unsigned dep_epoch, int num_sms, cudaStream_t s) {
+    using C = Cfg2<256, 8, KSUB>;
+    CUtensorMap mA1, mB1, mC1, mA2, mB2;
+    if (!make_map(&mA1, S, a1.K, a1.M, a1.ngroups, a1.a_group_rows, 128) ||
+        !make_map(&mB1, W1p, a1.K, a1.N, a1.ngroups, a1.N, 128) ||
+        !make_map_out(&mC1, a1.hid, a1.N, a1.M, a1.ngroups, a1.a_group_rows) ||
+        !make_map(&mA2, a1.hid, a2.K, a2.M, a2.ngroups, a2.a_group_rows, 128) ||
+        !make_map(&mB2, W2p, a2.K, a2.N, a2.ngroups, a2.N, 128))
+        return cudaErrorInvalidValue;
+    LayerDep dep;
+    dep.cnt = dep_cnt;
+    dep.target = (unsigned)a1.n_tiles * 2u * 8u;
+    dep.base = dep_epoch * dep.target;
+    dep.m_cap = (int)((a1.a_group_rows + BM2 - 1) / BM2);
+    auto k = pffn_layer_tc2_kernel<KSUB>;
+    static int max_pairs = 0;   // once per template instance
+    if (max_pairs == 0) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(2 * (num_sms / 2)), 1, 1);
+        cfg.blockDim = dim3(C::THREADS, 1, 1);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess || n <= 0) {
+            cudaGetLastError();
+            n = num_sms / 2;
+        }
+        max_pairs = n;
+    }
+    const long long tiles = a1.tiles + a2.tiles;
+    const long long pairs = tiles < max_pairs ? tiles : max_pairs;
+    return launch_k(k, dim3((unsigned)(2 * pairs)), dim3(C::THREADS), C::SMEM_BYTES, s, mA1, mB1, mC1, mA2, mB2, a1,
+                    a2, dep);
+}
+
 }  // namespace tc
+
+int gemm2_bn(int D);
+
+bool layer_tc_fusable(int B, int D, int F) {
+    return tc::fused_enabled() && B > tc::swap_max_batch() && tc::use_pair(B, tc::EPI_GELU) &&
+           tc::use_pair(B, tc::EPI_RESID) && tc::pick_bn(F) == 256 && gemm2_bn(D) == 256 && D % (2 * tc::BK) == 0 &&
+           F % (2 * tc::BK) == 0;
+}
+
+cudaError_t launch_layer_tc(const void* S, const void* W1p, const float* b1, void* Hid, const void* W2p,
+                            const float* b2, void* Z, float2* stats, int B, int T, int D, int F, int Bcap, int num_sms,
+                            unsigned* dep_cnt, unsigned dep_epoch, int* err, unsigned long long timeout_ns,
+                            cudaStream_t s) {
+    if (B <= 0) return cudaSuccess;
+    if (!layer_tc_fusable(B, D, F) || !dep_cnt) return cudaErrorNotSupported;
+    RM_HOST_BOUNDS(B <= Bcap && S && W1p && b1 && Hid && W2p && b2 && Z && stats);
+    RM_HOST_BOUNDS(((reinterpret_cast<uintptr_t>(S) | reinterpret_cast<uintptr_t>(W1p) | reinterpret_cast<uintptr_t>(Hid) |
+                     reinterpret_cast<uintptr_t>(W2p) | reinterpret_cast<uintptr_t>(Z)) & 15u) == 0);
+    tc::Args a1{}, a2{};
+    a1.N = F;
+    a1.K = D;
+    a1.ngroups = T;
+    a1.group_base = 0;
+    a1.group_stride = 1;
+    a1.M = B;
+    a1.a_group_rows = Bcap;
+    a1.bias = b1;
+    a1.hid = reinterpret_cast<__half*>(Hid);
+    a1.hid_tma = 1;
+    a1.rows_cap = (long long)T * Bcap;
+    a1.err = err;
+    a1.timeout_ns = timeout_ns;
+    a1.n_tiles = F / 256;
+    a1.m_tiles = (B + tc::BM2 - 1) / tc::BM2;
+    a1.tiles = (long long)T * a1.m_tiles * a1.n_tiles;
+    a1.n_fastest = a1.M > a1.N ? 1 : 0;
+    a2.N = D;
+    a2.K = F;
+    a2.ngroups = T;
+    a2.group_base = 0;
+    a2.group_stride = 1;
+    a2.M = B;
+    a2.a_group_rows = Bcap;
+    a2.bias = b2;
+    a2.resid = reinterpret_cast<const __half*>(S);
+    a2.z = reinterpret_cast<__half*>(Z);
+    a2.stats = stats;
+    a2.nchunk = D / 128;
+    a2.rows_cap = (long long)T * Bcap;
+    a2.err = err;
+    a2.timeout_ns = timeout_ns;
+    a2.n_tiles = D / 256;
+    a2.m_tiles = a1.m_tiles;
+    a2.tiles = (long long)T * a2.m_tiles * a2.n_tiles;
+    a2.n_fastest = a2.M > a2.N ? 1 : 0;
+    // one stage depth for both GEMMs: two k-blocks a stage unless RM_GEMM_KSUB=1
+    const bool k2 = tc::use_ksub2(F, tc::EPI_RESID) && D % (2 * tc::BK) == 0;
+    return k2 ? tc::run_layer<2>(S, W1p, W2p, a1, a2, dep_cnt, dep_epoch, num_sms, s)
+              : tc::run_layer<1>(S, W1p, W2p, a1, a2, dep_cnt, dep_epoch, num_sms, s);
+}
 
 bool tc_supported(int D, int F) {
     return D % tc::BK == 0 && F % tc::BK == 0 && tc::pick_bn(F) != 0 && tc::pick_bn(D) != 0;

@@ -167,6 +167,18 @@ cudaError_t launch_gemm2_tc(const void* Hid, const void* W2p, const float* b2, c
                             float2* stats, int B, int T, int D, int F, int Bcap, int num_sms, int* err,
                             unsigned long long timeout_ns, cudaStream_t s);
 
+// Both FFN GEMMs of a dense layer in one launch (tensor-core CTA pairs, B >=
+// 256 rows per token): the same results as launch_gemm1_tc + launch_gemm2_tc.
+// dep_cnt: [T][ceil(Bcap / 256)] counters that only grow, dep_epoch the number
+// of fused launches made on them before (both owned by the caller; zero the
+// counters and the epoch together).  cudaErrorNotSupported when the shape or
+// batch does not qualify (layer_tc_fusable).
+bool layer_tc_fusable(int B, int D, int F);
+cudaError_t launch_layer_tc(const void* S, const void* W1p, const float* b1, void* Hid, const void* W2p,
+                            const float* b2, void* Z, float2* stats, int B, int T, int D, int F, int Bcap, int num_sms,
+                            unsigned* dep_cnt, unsigned dep_epoch, int* err, unsigned long long timeout_ns,
+                            cudaStream_t s);
+
 // Set by the tensor-map encoder when the driver call fails (host-side message).
 const char* tc_last_error();
 

@@ -46,7 +46,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert _lib.rm_abi_version() == 3
+    assert _lib.rm_abi_version() == 4
 
 
 def _cfg(**kw):

@@ -498,7 +498,7 @@ print("ok")
 _DISPATCH_SHAPES = [(4, 256, 2, 2, 300), (2, 192, 2, 1, 300), (8, 512, 2, 2, 1100), (4, 256, 2, 2, 13),
                     (4, 256, 2, 2, 40), (4, 512, 2, 1, 150), (32, 768, 1, 1, 20)]
 _TUNING_KEYS = ("RM_GEMM_PAIR", "RM_GEMM_KSUB", "RM_GEMM1_EPW", "RM_GEMM2_BN", "RM_GEMM_SMALL_BN", "RM_GEMM_SWAP_MAX",
-                "RM_PDL", "RM_NVTX")
+                "RM_PDL", "RM_NVTX", "RM_GEMM_FUSED")
 
 
 @pytest.mark.parametrize("tuning", [{},                                            # the defaults
@@ -507,6 +507,7 @@ _TUNING_KEYS = ("RM_GEMM_PAIR", "RM_GEMM_KSUB", "RM_GEMM1_EPW", "RM_GEMM2_BN", "
                                     {"RM_GEMM_SMALL_BN": "128"},                    # narrower one-CTA tiles
                                     {"RM_GEMM_SWAP_MAX": "0"},                      # no weights-as-M path
                                     {"RM_GEMM_SWAP_MAX": "256"},                    # weights-as-M up to 256 rows
+                                    {"RM_GEMM_FUSED": "0"},                         # the two FFN GEMMs apart
                                     {"RM_PDL": "0"},                                # plain stream order
                                     {"RM_NVTX": "1"},                               # NVTX ranges around launches
                                     {"RM_GEMM_PAIR": "2"},                          # pairs for GEMM2 only
@@ -557,3 +558,70 @@ def test_pipelined_host_entry():
     assert e.value.status == _lib.RM_ERR_INVALID_ARG
     assert m.sync_status() == _lib.RM_OK
 
+
+
+# ----------------------------------------------------------------------------
+# Both FFN GEMMs of a layer in one launch (B >= 256 on the tensor-core path) run
+# the per-tile arithmetic of the two separate launches: every output bit agrees
+# ----------------------------------------------------------------------------
+
+_FUSED_CHILD = r"""
+import sys, numpy as np, torch
+sys.path.insert(0, {root!r})
+from rankmixer_feature_interaction_gb300 import _lib, synth
+from rankmixer_feature_interaction_gb300.api import RankMixer
+out = {{}}
+for T, D, k, L, B, Bcap in {shapes}:
+    layers = synth.make_stack(T, D, k, L, 411, "bf16", "cuda")
+    m = RankMixer(T, D, k, layers, max_batch=Bcap)
+    m.profile(True)
+    X = synth.make_input(B, T, D, 412, "bf16", "cuda")
+    pooled, XL = m.stack_forward(X, return_XL=True, xl_dtype="f32")
+    Xo, S = m.block_forward(0, X, return_S=True, out_dtype="f32")
+    # a smaller batch on the same context, then the full one again (the counters of the
+    # row blocks past a batch keep pace)
+    Xs = X[: max(256, B // 2)].contiguous()
+    ps_, XLs = m.stack_forward(Xs, return_XL=True, xl_dtype="f32")
+    pooled2 = m.stack_forward(X)
+    torch.cuda.synchronize()
+    assert m.sync_status() == 0
+    prof = m.profile_read()
+    key = f"{{T}}_{{D}}_{{B}}"
+    out["XL_" + key] = XL.cpu().numpy()
+    out["pooled_" + key] = pooled.float().cpu().numpy()
+    out["Xo_" + key] = Xo.cpu().numpy()
+    out["S_" + key] = S.float().cpu().numpy()
+    out["XLs_" + key] = XLs.cpu().numpy()
+    out["pooled2_" + key] = pooled2.float().cpu().numpy()
+    print(key, "pffn launches", prof["pffn"][0], "gemm1 launches", prof["gemm1"][0])
+    m.close()
+np.savez(sys.argv[1], **out)
+print("ok")
+"""
+
+# (T, D, k, L, B, max_batch): ragged row blocks, a context larger than the batch, both model widths
+_FUSED_SHAPES = [(4, 256, 2, 3, 300, 300), (8, 512, 2, 2, 1100, 1500), (16, 768, 4, 2, 512, 512),
+                 (32, 1536, 1, 2, 300, 600)]
+
+
+def test_fused_layer_gemm_bit_identical_to_two_launches(tmp_path):
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    got, logs = {}, {}
+    for mode in ("1", "0"):
+        env = {k: v for k, v in os.environ.items() if k not in _TUNING_KEYS}
+        env["RM_GEMM_FUSED"] = mode
+        path = str(tmp_path / f"fused_{mode}.npz")
+        r = subprocess.run([sys.executable, "-c", _FUSED_CHILD.format(root=root, shapes=_FUSED_SHAPES), path],
+                           env=env, cwd=root, capture_output=True, text=True, timeout=900)
+        assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
+        got[mode] = dict(np.load(path))
+        logs[mode] = r.stdout
+    # the fused launch ran when enabled, and only the separate GEMMs when not
+    assert "pffn launches 0" not in logs["1"] and "gemm1 launches 0" in logs["1"], logs["1"]
+    assert "pffn launches 0" in logs["0"], logs["0"]
+    for key in got["1"]:
+        a, b = got["1"][key], got["0"][key]
+        assert a.shape == b.shape and np.array_equal(a.view(np.uint32), b.view(np.uint32)), key
