@@ -23,7 +23,7 @@ def test_traffic_is_reported_only_while_the_kernel_sources_are_unchanged(monkeyp
 def test_recorded_traffic_entries_are_well_formed():
     for (config, batch, layers, kind), (nbytes, digest) in bench.TRAFFIC.items():
         assert config in ("rankmixer_1b", "rankmixer_100m", "moe_1b") and batch > 0 and layers > 0
-        assert kind in ("gemm1", "gemm2", "moe_gemm1", "moe_gemm2")
+        assert kind in ("gemm1", "gemm2", "pffn", "moe_gemm1", "moe_gemm2")
         assert nbytes > 0 and len(digest) == 64
 
 
