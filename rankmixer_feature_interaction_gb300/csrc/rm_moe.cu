@@ -306,6 +306,157 @@ route2_kernel(const Tin* __restrict__ S, long long s_sb, long long s_st, const f
     }
 }
 
+// ---- 1b: route on the tensor cores -----------------------------------------------
+// For 16-bit S, E <= 8 and D % 32 == 0: a warp takes 16 samples of token t and
+// forms their 16 x E gate pre-activations as one chain of m16n8k16 MMAs over
+// D (fp32 accumulation), instead of per-lane dot products that re-read Wg_t
+// for every pair of rows.  Wg_t (fp32) enters as two fp16 parts, hi = fp16(w)
+// and lo = fp16(w - hi), both multiplied in, so the weights keep about 21
+// significant bits; S is exact in fp16 (bf16 LayerNorm outputs; values below
+// fp16's normal range lose bits below 6e-8).  K is permuted inside each
+// 32-column group so that a lane reads its rows as one 16-byte word per group:
+// lane (g, c) holds columns 32 q + 8 c .. + 7 of rows g and g + 8, and k-step
+// 2 q + h takes columns 32 q + 8 c + 4 h + {0, 1} into fragment slots a0 / a1
+// and + {2, 3} into a2 / a3; the B fragments (precomputed per CTA in shared
+// memory, hi and lo) follow the same map, so each gate sums the same products.
+// Then the gates, slot claims and copies as in route_kernel; the copies re-read
+// the open rows (from L2), a 16-byte word per lane.
+constexpr int kRouteMmaWarps = 8;
+constexpr int kRouteMmaTiles = 2;                                        // 16-sample tiles per warp
+constexpr int kRouteMmaSamples = kRouteMmaWarps * kRouteMmaTiles * 16;   // per CTA
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                 "{%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two packed 16-bit inputs -> a packed fp16 pair (exact for bf16 values in fp16's range).
+template <typename Tin> __device__ __forceinline__ uint32_t route_f16x2(uint32_t v);
+template <> __device__ __forceinline__ uint32_t route_f16x2<__half>(uint32_t v) { return v; }
+template <> __device__ __forceinline__ uint32_t route_f16x2<__nv_bfloat16>(uint32_t v) {
+    return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
+template <typename Tin>
+__device__ __forceinline__ uint4 route_f16x8(uint4 v) {
+    return make_uint4(route_f16x2<Tin>(v.x), route_f16x2<Tin>(v.y), route_f16x2<Tin>(v.z), route_f16x2<Tin>(v.w));
+}
+
+size_t route_mma_smem(int D) { return (size_t)(D / 16) * 32 * sizeof(uint4); }
+
+template <typename Tin>
+__global__ void __launch_bounds__(kRouteMmaWarps * 32)
+route_mma_kernel(const Tin* __restrict__ S, long long s_sb, long long s_st, const float* __restrict__ Wg,
+                 const float* __restrict__ bg, float* __restrict__ gates, int* __restrict__ counts,
+                 float* __restrict__ row_gate, int* __restrict__ slot_of, __half* __restrict__ Sg, int B, int T,
+                 int D, int E, int Bcap) {
+    extern __shared__ uint4 s_frag[];                 // [D / 16 k-steps][32 lanes]: b0, b1 hi; b0, b1 lo
+    const int t = blockIdx.y;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, c = lane & 3;
+    const int nks = D >> 4, nq = D >> 5;
+    for (int i = threadIdx.x; i < nks * 32; i += blockDim.x) {
+        const int ks = i >> 5, ln = i & 31;
+        const int gg = ln >> 2, cc = ln & 3;
+        const int d0 = 32 * (ks >> 1) + 8 * cc + 4 * (ks & 1);     // physical columns d0 .. d0 + 3
+        float w[4] = {0.f, 0.f, 0.f, 0.f};
+        if (gg < E) {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(Wg + ((size_t)t * E + gg) * D + d0));
+            w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+        }
+        uint32_t hi[2], lo[2];
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            const __half h0 = __float2half_rn(w[2 * p]), h1 = __float2half_rn(w[2 * p + 1]);
+            const __half l0 = __float2half_rn(w[2 * p] - __half2float(h0));
+            const __half l1 = __float2half_rn(w[2 * p + 1] - __half2float(h1));
+            hi[p] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+            lo[p] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+        }
+        s_frag[i] = make_uint4(hi[0], hi[1], lo[0], lo[1]);
+    }
+    __syncthreads();
+    pdl_wait();              // S comes from the previous kernel of the stream
+    pdl_launch_next();
+
+    for (int tile = 0; tile < kRouteMmaTiles; ++tile) {
+        const int b0 = blockIdx.x * kRouteMmaSamples + (warp * kRouteMmaTiles + tile) * 16;
+        if (b0 >= B) break;
+        const int r0 = b0 + g, r1 = b0 + g + 8;
+        const bool ok0 = r0 < B, ok1 = r1 < B;
+        const Tin* x0 = S + (long long)(ok0 ? r0 : b0) * s_sb + (long long)t * s_st + 8 * c;
+        const Tin* x1 = S + (long long)(ok1 ? r1 : b0) * s_sb + (long long)t * s_st + 8 * c;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int q0 = 0; q0 < nq; q0 += 4) {
+            uint4 v0[4], v1[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const bool in = q0 + u < nq;
+                v0[u] = (in && ok0) ? __ldg(reinterpret_cast<const uint4*>(x0 + 32 * (q0 + u))) : make_uint4(0u, 0u, 0u, 0u);
+                v1[u] = (in && ok1) ? __ldg(reinterpret_cast<const uint4*>(x1 + 32 * (q0 + u))) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (q0 + u < nq) {
+                    const uint4 h0 = route_f16x8<Tin>(v0[u]), h1 = route_f16x8<Tin>(v1[u]);
+                    const uint4 f0 = s_frag[(2 * (q0 + u)) * 32 + lane];
+                    const uint4 f1 = s_frag[(2 * (q0 + u) + 1) * 32 + lane];
+                    const uint32_t a0[4] = {h0.x, h1.x, h0.y, h1.y};
+                    const uint32_t a1[4] = {h0.z, h1.z, h0.w, h1.w};
+                    mma_f16_16816(acc, a0, f0.x, f0.y);
+                    mma_f16_16816(acc, a0, f0.z, f0.w);
+                    mma_f16_16816(acc, a1, f1.x, f1.y);
+                    mma_f16_16816(acc, a1, f1.z, f1.w);
+                }
+            }
+        }
+        // lane (g, c): acc[0], acc[1] = row g, experts 2c, 2c + 1; acc[2], acc[3] = row g + 8
+        int slot[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int row = (j < 2 ? r0 : r1), e = 2 * c + (j & 1);
+            const bool mine = e < E && (j < 2 ? ok0 : ok1);
+            const float gt = mine ? fmaxf(acc[j] + __ldg(bg + (size_t)t * E + e), 0.f) : 0.f;
+            if (mine) gates[((size_t)row * T + t) * E + e] = gt;
+            slot[j] = -1;
+            if (mine && gt > 0.f) {
+                const int grp = t * E + e;
+                slot[j] = atomicAdd(counts + grp, 1);
+                row_gate[(size_t)grp * Bcap + slot[j]] = gt;
+            }
+            if (mine) slot_of[((size_t)row * T + t) * E + e] = slot[j];
+        }
+        // the copies: one open (row, expert) at a time, the whole warp on its row
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            unsigned m = __ballot_sync(0xffffffffu, slot[j] >= 0);
+            while (m) {
+                const int l = __ffs(m) - 1;
+                m &= m - 1;
+                const int sl = __shfl_sync(0xffffffffu, slot[j], l);
+                const int row = b0 + (l >> 2) + (j < 2 ? 0 : 8);
+                const int grp = t * E + 2 * (l & 3) + (j & 1);
+                const Tin* src = S + (long long)row * s_sb + (long long)t * s_st;
+                __half* dst = Sg + ((size_t)grp * Bcap + sl) * D;
+                for (int k = 8 * lane; k < D; k += 256)
+                    *reinterpret_cast<uint4*>(dst + k) = route_f16x8<Tin>(__ldg(reinterpret_cast<const uint4*>(src + k)));
+            }
+        }
+    }
+}
+
+// RM_MOE_ROUTE=dot in the environment keeps the per-lane dot-product router (a
+// tuning switch: gates equal to float32 rounding, the same experts open).
+bool route_mma_enabled() {
+    static int env = -1;
+    if (env < 0) {
+        const char* v = getenv("RM_MOE_ROUTE");
+        env = (v && v[0] == 'd') ? 0 : 1;
+    }
+    return env == 1;
+}
+
 // ---- 2: tile prefixes -------------------------------------------------------------
 // offsets[g] = g Bcap (fixed blocks); tile_prefix[0 .. G] over g = t E + e, the
 // exclusive prefix of 128-row tiles (both expert layers tile their packed rows
@@ -614,7 +765,28 @@ cudaError_t moe_forward(const MoeLaunch& ml, const MoeWeights& w, MoeWorkspace& 
         case 7: RM_ROUTE2(TIN, 7); break;                                                                    \
         default: RM_ROUTE2(TIN, 8); break;                                                                   \
     }
-        if (ml.act == Act::F32) {
+        const bool mma = ml.act != Act::F32 && vec && E <= 8 && D % 32 == 0 && route_mma_enabled() &&
+                         route_mma_smem(D) <= 96 * 1024;
+        const dim3 mgrid((B + kRouteMmaSamples - 1) / kRouteMmaSamples, T);
+        if (mma) {
+            const size_t smem = route_mma_smem(D);
+            cudaError_t ee;
+            if (ml.S_sample_major) {
+                ee = cudaFuncSetAttribute(route_mma_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)smem);
+                if (ee != cudaSuccess) return ee;
+                launch_k(route_mma_kernel<__nv_bfloat16>, mgrid, dim3(kRouteMmaWarps * 32), smem, s,
+                         (const __nv_bfloat16*)ml.S, s_sb, s_st, (const float*)w.Wg, (const float*)w.bg, ws.gates,
+                         ws.counts, ws.row_gate, ws.slot_of, (__half*)ws.Sg, B, T, D, E, ws.Bcap);
+            } else {
+                ee = cudaFuncSetAttribute(route_mma_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)smem);
+                if (ee != cudaSuccess) return ee;
+                launch_k(route_mma_kernel<__half>, mgrid, dim3(kRouteMmaWarps * 32), smem, s, (const __half*)ml.S,
+                         s_sb, s_st, (const float*)w.Wg, (const float*)w.bg, ws.gates, ws.counts, ws.row_gate,
+                         ws.slot_of, (__half*)ws.Sg, B, T, D, E, ws.Bcap);
+            }
+        } else if (ml.act == Act::F32) {
             if (vec) RM_ROUTE(float, float, 4); else RM_ROUTE(float, float, 1);
         } else if (ml.S_sample_major) {   // the caller's bf16 S
             if (regs) { RM_ROUTE2_N(__nv_bfloat16) }
