@@ -439,8 +439,16 @@ route_mma_kernel(const Tin* __restrict__ S, long long s_sb, long long s_st, cons
                 const int grp = t * E + 2 * (l & 3) + (j & 1);
                 const Tin* src = S + (long long)row * s_sb + (long long)t * s_st;
                 __half* dst = Sg + ((size_t)grp * Bcap + sl) * D;
-                for (int k = 8 * lane; k < D; k += 256)
-                    *reinterpret_cast<uint4*>(dst + k) = route_f16x8<Tin>(__ldg(reinterpret_cast<const uint4*>(src + k)));
+                // up to 8 16-byte words per lane in flight before any is stored
+                for (int k0 = 8 * lane; k0 < D; k0 += 2048) {
+                    uint4 w[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (k0 + 256 * i < D) w[i] = __ldg(reinterpret_cast<const uint4*>(src + k0 + 256 * i));
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (k0 + 256 * i < D) *reinterpret_cast<uint4*>(dst + k0 + 256 * i) = route_f16x8<Tin>(w[i]);
+                }
             }
         }
     }
