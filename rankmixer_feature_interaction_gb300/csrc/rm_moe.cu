@@ -576,6 +576,59 @@ moe_gemm_simt_kernel(const Tin* __restrict__ A, const Tin* __restrict__ W, const
     }
 }
 
+// ---- 5b: combine, 16-bit rows held whole -------------------------------------------------
+// The same sums for fp16 rows with D % 256 == 0 and D <= 8 * 256: a lane loads
+// all its 8-column words of one open expert's row before adding any (up to 8
+// 16-byte loads in flight instead of one), then the next expert, ascending e,
+// so every element is summed in the same order as in combine_kernel.
+template <int NCH>
+__global__ void __launch_bounds__(256)
+combine_rows_kernel(const __half* __restrict__ Y, const int* __restrict__ slot_of, float* __restrict__ V,
+                    long long v_sb, long long v_st, int B, int T, int D, int E, int Bcap) {
+    const int lane = threadIdx.x & 31;
+    const long long w0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+    for (long long r = w0; r < (long long)B * T; r += nw) {
+        const int b = (int)(r / T), t = (int)(r % T);
+        const int* so = slot_of + r * E;
+        float* vrow = V + (long long)b * v_sb + (long long)t * v_st;
+        float acc[NCH][8];
+#pragma unroll
+        for (int i = 0; i < NCH; ++i)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) acc[i][k] = 0.f;
+        for (int e = 0; e < E; ++e) {
+            const int sl = __ldg(so + e);
+            if (sl < 0) continue;
+            const __half* y = Y + ((size_t)(t * E + e) * Bcap + sl) * D + 8 * lane;
+            uint4 w[NCH];
+#pragma unroll
+            for (int i = 0; i < NCH; ++i)
+                if (256 * i < D) w[i] = __ldg(reinterpret_cast<const uint4*>(y + 256 * i));
+#pragma unroll
+            for (int i = 0; i < NCH; ++i) {
+                if (256 * i < D) {
+                    const __half2* h = reinterpret_cast<const __half2*>(&w[i]);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 f = __half22float2(h[q]);
+                        acc[i][2 * q] += f.x;
+                        acc[i][2 * q + 1] += f.y;
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+            if (256 * i < D) {
+                float4* dst = reinterpret_cast<float4*>(vrow + 8 * lane + 256 * i);
+                dst[0] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+                dst[1] = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+            }
+        }
+    }
+}
+
 // ---- 5: combine -----------------------------------------------------------------------
 // V[b, t] = sum over the open experts e of (b, t), ascending, of their gated rows
 // Y[slot_of[b][t][e] of group t E + e] (zero when none is open).  One warp per
@@ -863,7 +916,19 @@ cudaError_t moe_forward(const MoeLaunch& ml, const MoeWeights& w, MoeWorkspace& 
         int grid = (int)(((long long)B * T * 32 + 255) / 256);
         if (grid > ml.num_sms * 16) grid = ml.num_sms * 16;
         const bool vec = D % 8 == 0 && (v_sb % 4 == 0) && (v_st % 4 == 0) && ((uintptr_t)V % 16 == 0);
-        if (ml.act == Act::BF16) {
+        if (ml.act == Act::BF16 && vec && D % 256 == 0 && D <= 8 * 256) {
+            const __half* Y = (const __half*)ws.Sg;
+            switch (D / 256) {
+                case 1: combine_rows_kernel<1><<<grid, 256, 0, s>>>(Y, ws.slot_of, V, v_sb, v_st, B, T, D, E, ws.Bcap); break;
+                case 2: combine_rows_kernel<2><<<grid, 256, 0, s>>>(Y, ws.slot_of, V, v_sb, v_st, B, T, D, E, ws.Bcap); break;
+                case 3: combine_rows_kernel<3><<<grid, 256, 0, s>>>(Y, ws.slot_of, V, v_sb, v_st, B, T, D, E, ws.Bcap); break;
+                case 4: combine_rows_kernel<4><<<grid, 256, 0, s>>>(Y, ws.slot_of, V, v_sb, v_st, B, T, D, E, ws.Bcap); break;
+                case 5: combine_rows_kernel<5><<<grid, 256, 0, s>>>(Y, ws.slot_of, V, v_sb, v_st, B, T, D, E, ws.Bcap); break;
+                case 6: combine_rows_kernel<6><<<grid, 256, 0, s>>>(Y, ws.slot_of, V, v_sb, v_st, B, T, D, E, ws.Bcap); break;
+                case 7: combine_rows_kernel<7><<<grid, 256, 0, s>>>(Y, ws.slot_of, V, v_sb, v_st, B, T, D, E, ws.Bcap); break;
+                default: combine_rows_kernel<8><<<grid, 256, 0, s>>>(Y, ws.slot_of, V, v_sb, v_st, B, T, D, E, ws.Bcap); break;
+            }
+        } else if (ml.act == Act::BF16) {
             if (vec)
                 combine_kernel<__half, 8><<<grid, 256, 0, s>>>((const __half*)ws.Sg, ws.slot_of, V, v_sb, v_st, B, T,
                                                                D, E, ws.Bcap);
