@@ -54,6 +54,9 @@ TRAFFIC = {
     # "bench.py --steps 3 --warmup 3 --no-cpu-baseline", averaged over the captured launches
     # (the fused layer kernel: both FFN GEMMs of a layer per launch)
     ("rankmixer_1b", 4096, 2, "pffn"): (6333877376, "604b07e919d81cabc278a5f8cfc6a5113d48437a882a3aad5a9f94e7931f37e2"),
+    # the expert GEMMs of "bench.py --config moe_1b --steps 3 --warmup 3 --no-cpu-baseline"
+    ("moe_1b", 4096, 1, "moe_gemm1"): (4686283776, "604b07e919d81cabc278a5f8cfc6a5113d48437a882a3aad5a9f94e7931f37e2"),
+    ("moe_1b", 4096, 1, "moe_gemm2"): (5295223552, "604b07e919d81cabc278a5f8cfc6a5113d48437a882a3aad5a9f94e7931f37e2"),
 }
 
 
