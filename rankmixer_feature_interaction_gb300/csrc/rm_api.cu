@@ -920,7 +920,7 @@ rm_status unimix_global(rm_ctx* c, int layer, const void* X, XType xt, int B, cu
     const long long Npitch = um_pitch(c, bs);
     const long long Npad = ((long long)B * bs + 255) / 256 * 256;
     RM_CHECK_CUDA(launch_unimix_local(xt, c->act, X, (long long)g.T * g.D, w.umWB, w.umWBt16, c->umH, B, nb, bs,
-                                      Npitch, Npad, s),
+                                      Npitch, Npad, c->num_sms, c->d_err, kWaitTimeoutNs, s),
                   "unimixing local step");
     TrainGemm m = train_gemm_base(c);
     m.G = 1;

@@ -12,6 +12,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
 
 #include <type_traits>
 
@@ -322,6 +324,204 @@ unimix_local_mma_kernel(const Tin* __restrict__ X, long long x_stride, const __h
     }
 }
 
+// ---------------------------------------------------------------------------
+// The same local step with the samples staged in shared memory by bulk copies
+// (the same products in the same order as unimix_local_mma_kernel, so the same
+// bits), for a deep, register-free read pipeline and whole-line writes.
+//
+// Work item: a group of kLsJ consecutive blocks j and 16 consecutive samples.
+// Each CTA takes a contiguous run of items in group-major order, so its warps
+// reload their W_B^j fragments only when the group changes.  A producer warp
+// fills up to STAGES items ahead: per sample row one 1-D bulk copy of the
+// group's kLsJ BS contiguous values (a 768-byte run at BS = 48), into a row
+// pitch padded so that the 8-byte fragment loads of a half-warp fall on
+// distinct banks (BS = 16 and 48; 2-way at 32 and 64).  Compute warp w takes
+// block kLsJ g + w of every item of group g: A fragments from the staged rows
+// under the K permutation above, the products, then the 16 x BS fp16 result
+// into a per-warp staging buffer (two, alternating) and one bulk store into
+// H's row j, where the 16 samples' BS values are contiguous.
+// ---------------------------------------------------------------------------
+// 1-D bulk copy shared -> global (both 16-byte aligned, size a multiple of 16)
+// in the thread's current bulk async group.
+__device__ __forceinline__ void bulk_copy_s2g(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 ::"l"(reinterpret_cast<uint64_t>(dst)), "r"(src), "r"(bytes)
+                 : "memory");
+}
+
+constexpr int kLsJ = 8;          // blocks per group = compute warps per CTA
+constexpr int kLsRows = 16;      // samples per item (one m16 tile)
+
+template <int BS>
+struct LsCfg {
+    static constexpr int ROW_BYTES = kLsJ * BS * 2;
+    // row pitch = 24 (BS = 48) or 8 (BS = 16) 4-byte words mod 32
+    static constexpr int PAD = BS == 48 ? 96 : (BS == 16 ? 32 : 16);
+    static constexpr int PITCH = (ROW_BYTES + 127) / 128 * 128 + PAD;
+    static constexpr int STAGE_BYTES = kLsRows * PITCH;
+    static constexpr int OUT_BYTES = kLsRows * BS * 2;   // one warp's 16 x BS result
+    static constexpr int STAGES = BS <= 48 ? 6 : 4;
+    static constexpr int OUT_OFF = STAGES * STAGE_BYTES;
+    static constexpr int BAR_OFF = OUT_OFF + kLsJ * 2 * OUT_BYTES;
+    static constexpr int SMEM = BAR_OFF + 2 * STAGES * 8 + 16;
+    static constexpr int THREADS = 32 * (kLsJ + 1);
+    static constexpr int MIN_BLOCKS = BS <= 48 ? 2 : 1;
+    static_assert(PITCH % 16 == 0 && OUT_OFF % 16 == 0 && OUT_BYTES % 16 == 0, "bulk-copy alignment");
+    static_assert(MIN_BLOCKS * (SMEM + 1024) <= 228 * 1024, "shared memory per SM");
+};
+
+template <typename Tin, int BS>
+__global__ void __launch_bounds__(LsCfg<BS>::THREADS, LsCfg<BS>::MIN_BLOCKS)
+unimix_local_staged_kernel(const Tin* __restrict__ X, long long x_stride, const __half* __restrict__ WBt,
+                           __half* __restrict__ H, int B, int nb, long long Npitch, long long Npad, int* err,
+                           unsigned long long timeout_ns) {
+    using C = LsCfg<BS>;
+    constexpr int KS = BS / 16, NT = BS / 8;
+    extern __shared__ __align__(128) uint8_t ls_smem[];
+    const uint32_t sbase = smem_u32(ls_smem);
+    volatile int* abort = reinterpret_cast<volatile int*>(ls_smem + C::BAR_OFF + 2 * C::STAGES * 8);
+    auto full = [&](int s) { return sbase + (uint32_t)C::BAR_OFF + 8u * (uint32_t)s; };
+    auto empty = [&](int s) { return sbase + (uint32_t)C::BAR_OFF + 8u * (uint32_t)(C::STAGES + s); };
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ngroups = (nb + kLsJ - 1) / kLsJ;
+    const int ntiles = (B + kLsRows - 1) / kLsRows;
+    const int items = ngroups * ntiles;   // < 2^31 (checked by the launcher)
+    const int i0 = (int)((long long)items * blockIdx.x / gridDim.x);
+    const int i1 = (int)((long long)items * (blockIdx.x + 1) / gridDim.x);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), kLsJ * 32);
+        }
+        *abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kLsJ) {
+        // ---- producer ----
+        int i = i0;
+        for (; i < i1; ++i) {
+            const int n = i - i0;
+            const int s = n % C::STAGES;
+            const uint32_t ph = (uint32_t)(n / C::STAGES) & 1u;
+            if (n >= C::STAGES && !mbar_wait_bounded(empty(s), ph ^ 1u, abort, err, timeout_ns)) break;
+            const int jg = i / ntiles, bt = i - jg * ntiles;
+            const int jv = min(kLsJ, nb - jg * kLsJ);
+            const int b0 = bt * kLsRows, rows = min(kLsRows, B - b0);
+            const uint32_t bytes = (uint32_t)jv * BS * 2u;
+            if (lane == 0) mbar_arrive_expect_tx(full(s), (uint32_t)rows * bytes);
+            __syncwarp();
+            if (lane < rows)
+                bulk_copy_g2s(sbase + (uint32_t)s * C::STAGE_BYTES + (uint32_t)lane * C::PITCH,
+                              X + (long long)(b0 + lane) * x_stride + (long long)jg * kLsJ * BS, bytes, full(s));
+        }
+        // The CTA may exit only after the copies it issued have landed.  The
+        // compute warps wait for every stage they use; after an abort some are
+        // not used, so wait (bounded, whatever the abort flag) on the last
+        // fill of each stage.
+        const int issued = i - i0;
+        if (lane == 0) {
+            for (int n = issued - 1; n >= 0 && n >= issued - C::STAGES; --n) {
+                const int s = n % C::STAGES;
+                const uint32_t ph = (uint32_t)(n / C::STAGES) & 1u;
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(full(s), ph) && globaltimer_ns() - t0 < timeout_ns) {
+                }
+            }
+        }
+        return;
+    }
+
+    // ---- compute warp: block j = kLsJ g + warp of each item of group g ----
+    const int g = lane >> 2, c = lane & 3;
+    const int ncol0 = (g >> 1) * 2 * NT + (g & 1);
+    uint32_t bf[KS][NT][2];
+    int cur_jg = -1;
+    int sbuf = 0;
+    const int obase = C::OUT_OFF + warp * 2 * C::OUT_BYTES;
+    for (int i = i0; i < i1; ++i) {
+        const int n = i - i0;
+        const int s = n % C::STAGES;
+        const uint32_t ph = (uint32_t)(n / C::STAGES) & 1u;
+        const int jg = i / ntiles, bt = i - jg * ntiles;
+        const int j = jg * kLsJ + warp;
+        const bool active = j < nb;
+        if (active && jg != cur_jg) {
+            // B[k][n] = WB_j[k][n] = WBt[j][n][k], physical k and n as in unimix_local_mma_kernel
+            const __half* w = WBt + (size_t)j * BS * BS;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const __half* row = w + (size_t)(ncol0 + 2 * nt) * BS + 4 * KS * c + 4 * ks;
+                    bf[ks][nt][0] = __ldg(reinterpret_cast<const uint32_t*>(row));
+                    bf[ks][nt][1] = __ldg(reinterpret_cast<const uint32_t*>(row + 2));
+                }
+            cur_jg = jg;
+        }
+        if (!mbar_wait_bounded(full(s), ph, abort, err, timeout_ns)) break;
+        float acc[NT][4];
+        if (active) {
+            const uint8_t* r0 = ls_smem + s * C::STAGE_BYTES + g * C::PITCH + warp * BS * 2 + 8 * KS * c;
+            const uint8_t* r1 = r0 + 8 * C::PITCH;
+            uint2 x0w[KS], x1w[KS];
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                x0w[ks] = *reinterpret_cast<const uint2*>(r0 + 8 * ks);
+                x1w[ks] = *reinterpret_cast<const uint2*>(r1 + 8 * ks);
+            }
+            uint32_t af[KS][4];
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                af[ks][0] = to_f16x2<Tin>(x0w[ks].x);
+                af[ks][1] = to_f16x2<Tin>(x1w[ks].x);
+                af[ks][2] = to_f16x2<Tin>(x0w[ks].y);
+                af[ks][3] = to_f16x2<Tin>(x1w[ks].y);
+            }
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma_f16(acc[nt], af[ks], bf[ks][nt][0], bf[ks][nt][1]);
+        }
+        // Every lane releases the stage only after MMAs that take its loaded
+        // words as operands have issued, i.e. after its shared-memory loads
+        // have returned.  Arriving right after issuing the loads (by one lane
+        // or by each) measured stage contents overwritten by the next copy
+        // before some loads had read them.
+        mbar_arrive(empty(s));
+        if (!active) continue;
+        const int b0 = bt * kLsRows, rows = min(kLsRows, B - b0);
+        const int ob = obase + sbuf * C::OUT_BYTES;
+        if (lane == 0) bulk_wait_group_read<1>();   // the store that last read this buffer
+        __syncwarp();
+        uint8_t* o0 = ls_smem + ob + g * BS * 2 + 4 * NT * c;
+        uint8_t* o1 = o0 + 8 * BS * 2;
+#pragma unroll
+        for (int m = 0; m < NT / 2; ++m) {
+            *reinterpret_cast<uint2*>(o0 + 8 * m) =
+                make_uint2(pack_f16x2(acc[2 * m][0], acc[2 * m][1]), pack_f16x2(acc[2 * m + 1][0], acc[2 * m + 1][1]));
+            *reinterpret_cast<uint2*>(o1 + 8 * m) =
+                make_uint2(pack_f16x2(acc[2 * m][2], acc[2 * m][3]), pack_f16x2(acc[2 * m + 1][2], acc[2 * m + 1][3]));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            bulk_copy_s2g(H + (long long)j * Npitch + (long long)b0 * BS, sbase + (uint32_t)ob,
+                          (uint32_t)rows * BS * 2u);
+            bulk_commit_group();
+        }
+        sbuf ^= 1;
+        if (bt == ntiles - 1) {   // row j's padding columns
+            __half* hrow = H + (long long)j * Npitch;
+            for (long long q = (long long)B * BS + lane; q < Npad; q += 32) hrow[q] = __float2half_rn(0.f);
+        }
+    }
+    if (lane == 0) bulk_wait_group<0>();
+}
+
 // WBt16[j][r][s] = fp16(WB[j][s][r]).
 __global__ void pack_wb_kernel(const float* __restrict__ WB, __half* __restrict__ WBt16, int nb, int bs) {
     const long long total = (long long)nb * bs * bs;
@@ -590,6 +790,47 @@ cudaError_t launch_mma_t(const void* X, long long x_stride, const void* WBt16, v
 
 bool unimix_local_mma_ok(int bs) { return bs == 16 || bs == 32 || bs == 48 || bs == 64; }
 
+// RM_UNIMIX_LOCAL=regs in the environment keeps the register-prefetch local
+// step (a tuning switch: the same products, the same bits).
+bool local_staged_enabled() {
+    static int env = -1;
+    if (env < 0) {
+        const char* v = getenv("RM_UNIMIX_LOCAL");
+        env = (v && v[0] == 'r') ? 0 : 1;
+    }
+    return env == 1;
+}
+
+template <typename Tin, int BS>
+cudaError_t launch_staged_bs(const void* X, long long x_stride, const void* WBt16, void* H, int B, int nb,
+                             long long Npitch, long long Npad, int num_sms, int* err, unsigned long long timeout_ns,
+                             cudaStream_t s) {
+    using C = LsCfg<BS>;
+    auto k = unimix_local_staged_kernel<Tin, BS>;
+    static cudaError_t attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (attr != cudaSuccess) return attr;
+    const long long items = (long long)((nb + kLsJ - 1) / kLsJ) * ((B + kLsRows - 1) / kLsRows);
+    if (items >= (1LL << 31)) return cudaErrorNotSupported;
+    const long long slots = (long long)C::MIN_BLOCKS * (num_sms > 0 ? num_sms : 1);
+    const int grid = (int)(items < slots ? items : slots);
+    k<<<grid, C::THREADS, C::SMEM, s>>>((const Tin*)X, x_stride, (const __half*)WBt16, (__half*)H, B, nb, Npitch,
+                                         Npad, err, timeout_ns);
+    return cudaGetLastError();
+}
+
+template <typename Tin>
+cudaError_t launch_staged_t(const void* X, long long x_stride, const void* WBt16, void* H, int B, int nb, int bs,
+                            long long Npitch, long long Npad, int num_sms, int* err, unsigned long long timeout_ns,
+                            cudaStream_t s) {
+    switch (bs) {
+        case 16: return launch_staged_bs<Tin, 16>(X, x_stride, WBt16, H, B, nb, Npitch, Npad, num_sms, err, timeout_ns, s);
+        case 32: return launch_staged_bs<Tin, 32>(X, x_stride, WBt16, H, B, nb, Npitch, Npad, num_sms, err, timeout_ns, s);
+        case 48: return launch_staged_bs<Tin, 48>(X, x_stride, WBt16, H, B, nb, Npitch, Npad, num_sms, err, timeout_ns, s);
+        case 64: return launch_staged_bs<Tin, 64>(X, x_stride, WBt16, H, B, nb, Npitch, Npad, num_sms, err, timeout_ns, s);
+        default: return cudaErrorNotSupported;
+    }
+}
+
 cudaError_t launch_unimix_pack_wb(const float* WB, void* WBt16, int nb, int bs, cudaStream_t s) {
     pack_wb_kernel<<<grid_of((long long)nb * bs * bs, 256), 256, 0, s>>>(WB, (__half*)WBt16, nb, bs);
     return cudaGetLastError();
@@ -597,9 +838,18 @@ cudaError_t launch_unimix_pack_wb(const float* WB, void* WBt16, int nb, int bs, 
 
 cudaError_t launch_unimix_local(XType xt, Act act, const void* X, long long x_stride, const float* WB,
                                 const void* WBt16, void* H, int B, int nb, int bs, long long Npitch, long long Npad,
-                                cudaStream_t s) {
+                                int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s) {
     if (B <= 0) return cudaSuccess;
     if (act != Act::F32 && WBt16 && unimix_local_mma_ok(bs) && x_stride % 8 == 0) {
+        // the staged kernel's bulk copies: 16-byte aligned rows in X and in H
+        const bool aligned16 = ((uintptr_t)X % 16 == 0) && ((uintptr_t)H % 16 == 0) && Npitch % 8 == 0;
+        if (aligned16 && local_staged_enabled() && xt != XType::F32) {
+            RM_HOST_BOUNDS(Npitch >= (long long)B * bs && Npad <= Npitch && x_stride >= (long long)nb * bs);
+            if (xt == XType::BF16)
+                return launch_staged_t<__nv_bfloat16>(X, x_stride, WBt16, H, B, nb, bs, Npitch, Npad, num_sms, err,
+                                                      timeout_ns, s);
+            return launch_staged_t<__half>(X, x_stride, WBt16, H, B, nb, bs, Npitch, Npad, num_sms, err, timeout_ns, s);
+        }
         if (xt == XType::BF16)
             return launch_mma_t<__nv_bfloat16>(X, x_stride, WBt16, H, B, nb, bs, Npitch, Npad, s);
         if (xt == XType::F16) return launch_mma_t<__half>(X, x_stride, WBt16, H, B, nb, bs, Npitch, Npad, s);

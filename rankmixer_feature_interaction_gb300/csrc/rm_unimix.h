@@ -36,11 +36,13 @@ cudaError_t launch_sinkhorn(const float* W, int count, int n, float tau, int ite
 // bf16 contexts with bs in {16, 32, 48, 64} run it on the tensor cores
 // (mma.sync, fp16 operands) from the transposed fp16 copy WBt16 [nb][bs][bs]
 // (row r, column s = WB[j][s][r], see launch_unimix_pack_wb), otherwise on the
-// CUDA cores from WB (float32).
+// CUDA cores from WB (float32).  The tensor-core step stages X through shared
+// memory when X and H are 16-byte aligned (bounded waits: a stalled copy
+// latches kDevErrTimeout in *err after timeout_ns and the kernel returns).
 enum class XType { BF16, F16, F32 };
 cudaError_t launch_unimix_local(XType xt, Act act, const void* X, long long x_stride, const float* WB,
                                 const void* WBt16, void* H, int B, int nb, int bs, long long Npitch, long long Npad,
-                                cudaStream_t s);
+                                int num_sms, int* err, unsigned long long timeout_ns, cudaStream_t s);
 bool unimix_local_mma_ok(int bs);
 cudaError_t launch_unimix_pack_wb(const float* WB, void* WBt16, int nb, int bs, cudaStream_t s);
 

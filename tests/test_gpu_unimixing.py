@@ -172,3 +172,60 @@ def test_unimixing_argument_errors():
     with pytest.raises(_lib.RankMixerError) as e:
         mt.stack_forward_train(X)
     assert e.value.status == _lib.RM_ERR_UNSUPPORTED
+
+
+_LOCAL_CHILD = r"""
+import sys
+import numpy as np
+import torch
+sys.path.insert(0, {root!r})
+from rankmixer_feature_interaction_gb300 import synth
+from rankmixer_feature_interaction_gb300.api import RankMixer
+out = {{}}
+for T, D, bs, B, Bcap in {shapes}:
+    layers = synth.make_stack(T, D, 2, 2, 21, "bf16", "cuda")
+    m = RankMixer(T, D, 2, layers, dtype="bf16", max_batch=Bcap)
+    for n in range(2):
+        WG, WB = synth.make_unimix_weights(T, D, bs, 22 + n, "cuda")
+        m.set_unimixing(n, WG, WB, tau=0.3, iters=5)
+    X = synth.make_input(B, T, D, 24, "bf16", "cuda")
+    Y = m.unimixing(0, X, out_dtype="f32")                            # bf16 samples in
+    pooled, XL = m.stack_forward(X, return_XL=True, xl_dtype="f32")   # layer 1: fp16 samples in
+    torch.cuda.synchronize()
+    assert m.sync_status() == 0
+    key = f"{{T}}_{{D}}_{{bs}}_{{B}}"
+    out["Y_" + key] = Y.cpu().numpy()
+    out["XL_" + key] = XL.cpu().numpy()
+    out["pooled_" + key] = pooled.float().cpu().numpy()
+    m.close()
+np.savez(sys.argv[1], **out)
+print("ok")
+"""
+
+# (T, D, bs, B, max_batch): every tensor-core block size, a partial last group of
+# blocks (nb = 25), ragged sample tiles, many items per CTA at the 1B shape
+_LOCAL_SHAPES = [(8, 512, 64, 301, 301), (8, 512, 32, 129, 200), (32, 1536, 48, 700, 700), (5, 240, 48, 77, 100),
+                 (4, 64, 16, 33, 33), (16, 768, 48, 130, 130)]
+
+
+def test_staged_local_step_bit_identical_to_register_kernel(tmp_path):
+    """The local step staged through shared memory by bulk copies and the
+    register-prefetch kernel (RM_UNIMIX_LOCAL=regs) form the same products in
+    the same order: the mixing output and the stack built on it agree bit for bit."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    got = {}
+    for mode in ("staged", "regs"):
+        env = {k: v for k, v in os.environ.items() if k != "RM_UNIMIX_LOCAL"}
+        if mode == "regs":
+            env["RM_UNIMIX_LOCAL"] = "regs"
+        path = str(tmp_path / f"local_{mode}.npz")
+        r = subprocess.run([sys.executable, "-c", _LOCAL_CHILD.format(root=root, shapes=_LOCAL_SHAPES), path],
+                           env=env, cwd=root, capture_output=True, text=True, timeout=900)
+        assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
+        got[mode] = dict(np.load(path))
+    for key in got["staged"]:
+        a, b = got["staged"][key], got["regs"][key]
+        assert a.shape == b.shape and np.array_equal(a.view(np.uint32), b.view(np.uint32)), key
