@@ -1295,12 +1295,86 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// One work unit's epilogue for one epilogue warp of the weights-as-M kernels:
+// TMEM lanes 32 q .. 32 q + 31 (feature f = 128 fb + 32 q + lane of this lane)
+// and the warp's batch columns col0 .. col0 + CPW - 1 of the accumulator at
+// tbase; s_stat_acc is the accumulator buffer's slice of the row-moment area.
+template <int NB, int EPI>
+__device__ __forceinline__ void swap_epilogue_unit(const Args& args, int fb, int f, float bf, size_t row0, bool uok,
+                                                   uint32_t tbase, float* s_stat_acc, int q, int col0, int lane) {
+    using C = CfgS<NB>;
+    constexpr int CW = NB < 32 ? NB : 32;        // TMEM columns per load
+    float* st_mean = s_stat_acc + (size_t)q * NB;
+    float* st_m2 = st_mean + 4 * NB;
+#pragma unroll 1
+    for (int c = col0; c < col0 + C::CPW && c < args.M; c += CW) {
+        float v[CW];
+        if constexpr (CW == 32) {
+            tmem_ld32(tbase + (uint32_t)c, v);
+        } else {
+            tmem_ld16(tbase + (uint32_t)c, v);
+        }
+        if (EPI == EPI_GELU) {
+            // two batch rows at a time through the packed GELU
+#pragma unroll
+            for (int i = 0; i < CW; i += 2) {
+                const int b = c + i;                               // batch row (warp-uniform)
+                if (b >= args.M) break;
+                float g0, g1;
+                f2_unpack(gelu_erf_x2(f2_pack(v[i], v[i + 1]), f2_splat(bf)), g0, g1);
+                if (uok) args.hid[(row0 + b) * (size_t)args.N + f] = __float2half_rn(sat_f16(g0));
+                if (uok && b + 1 < args.M)
+                    args.hid[(row0 + b + 1) * (size_t)args.N + f] = __float2half_rn(sat_f16(g1));
+            }
+        } else {   // EPI_RESID
+            // the residuals of the chunk's rows first, all loads in flight together
+            float rres[CW];
+#pragma unroll
+            for (int i = 0; i < CW; ++i) {
+                const int b = c + i;
+                rres[i] = (uok && b < args.M) ? __half2float(args.resid[(row0 + b) * (size_t)args.N + f]) : 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < CW; ++i) {
+                const int b = c + i;                               // batch row (warp-uniform)
+                if (b >= args.M) break;
+                const float z = v[i] + bf + rres[i];
+                if (uok) args.z[(row0 + b) * (size_t)args.N + f] = __float2half_rn(sat_f16(z));
+                // this warp's 32 features: mean and M2 about it
+                const float mw = warp_sum(z) * (1.0f / 32.0f);
+                const float d = z - mw;
+                const float m2w = warp_sum(d * d);
+                if (lane == 0) {
+                    st_mean[b] = mw;
+                    st_m2[b] = m2w;
+                }
+            }
+        }
+    }
+    if (EPI == EPI_RESID) {
+        // the four quadrants' moments -> (mean, M2) of the 128 features, one lane
+        // per row, each q = 0 warp for its own columns
+        asm volatile("bar.sync 1, %0;" ::"r"(C::EPW * 32) : "memory");
+        if (q == 0) {
+            const float* sm = s_stat_acc;
+            const float* s2 = sm + 4 * NB;
+            for (int b = col0 + lane; b < args.M && b < col0 + C::CPW; b += 32) {
+                const float m0 = sm[b], m1 = sm[NB + b], m2 = sm[2 * NB + b], m3 = sm[3 * NB + b];
+                const float mean = 0.25f * (m0 + m1 + m2 + m3);
+                const float d0 = m0 - mean, d1 = m1 - mean, d2 = m2 - mean, d3 = m3 - mean;
+                const float M2 = s2[b] + s2[NB + b] + s2[2 * NB + b] + s2[3 * NB + b] +
+                                 32.0f * (d0 * d0 + d1 * d1 + d2 * d2 + d3 * d3);
+                if (uok) args.stats[(row0 + b) * (size_t)args.nchunk + fb] = make_float2(mean, M2);
+            }
+        }
+    }
+}
+
 template <int NB, int EPI>
 __global__ void __launch_bounds__(CfgS<NB>::THREADS, 1)
 pffn_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                       const Args args) {
     using C = CfgS<NB>;
-    constexpr int CW = NB < 32 ? NB : 32;        // TMEM columns per load
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -1433,76 +1507,229 @@ pffn_gemm_swap_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_cons
             if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, args.err, args.timeout_ns)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * NB);
-            float* st_mean = s_stat + (size_t)acc * 2 * 4 * NB + (size_t)q * NB;
-            float* st_m2 = st_mean + 4 * NB;
-#pragma unroll 1
-            for (int c = col0; c < col0 + C::CPW && c < args.M; c += CW) {
-                float v[CW];
-                if constexpr (CW == 32) {
-                    tmem_ld32(tbase + (uint32_t)c, v);
-                } else {
-                    tmem_ld16(tbase + (uint32_t)c, v);
-                }
-                if (EPI == EPI_GELU) {
-                    // two batch rows at a time through the packed GELU
-#pragma unroll
-                    for (int i = 0; i < CW; i += 2) {
-                        const int b = c + i;                               // batch row (warp-uniform)
-                        if (b >= args.M) break;
-                        float g0, g1;
-                        f2_unpack(gelu_erf_x2(f2_pack(v[i], v[i + 1]), f2_splat(bf)), g0, g1);
-                        if (uok) args.hid[(row0 + b) * (size_t)args.N + f] = __float2half_rn(sat_f16(g0));
-                        if (uok && b + 1 < args.M)
-                            args.hid[(row0 + b + 1) * (size_t)args.N + f] = __float2half_rn(sat_f16(g1));
-                    }
-                } else {   // EPI_RESID
-                    // the residuals of the chunk's rows first, all loads in flight together
-                    float rres[CW];
-#pragma unroll
-                    for (int i = 0; i < CW; ++i) {
-                        const int b = c + i;
-                        rres[i] = (uok && b < args.M) ? __half2float(args.resid[(row0 + b) * (size_t)args.N + f]) : 0.f;
-                    }
-#pragma unroll
-                    for (int i = 0; i < CW; ++i) {
-                        const int b = c + i;                               // batch row (warp-uniform)
-                        if (b >= args.M) break;
-                        const float z = v[i] + bf + rres[i];
-                        if (uok) args.z[(row0 + b) * (size_t)args.N + f] = __float2half_rn(sat_f16(z));
-                        // this warp's 32 features: mean and M2 about it
-                        const float mw = warp_sum(z) * (1.0f / 32.0f);
-                        const float d = z - mw;
-                        const float m2w = warp_sum(d * d);
-                        if (lane == 0) {
-                            st_mean[b] = mw;
-                            st_m2[b] = m2w;
-                        }
-                    }
-                }
-            }
-            if (EPI == EPI_RESID) {
-                // the four quadrants' moments -> (mean, M2) of the 128 features, one lane
-                // per row, each q = 0 warp for its own columns
-                asm volatile("bar.sync 1, %0;" ::"r"(C::EPW * 32) : "memory");
-                if (q == 0) {
-                    const float* sm = s_stat + (size_t)acc * 2 * 4 * NB;
-                    const float* s2 = sm + 4 * NB;
-                    for (int b = col0 + lane; b < args.M && b < col0 + C::CPW; b += 32) {
-                        const float m0 = sm[b], m1 = sm[NB + b], m2 = sm[2 * NB + b], m3 = sm[3 * NB + b];
-                        const float mean = 0.25f * (m0 + m1 + m2 + m3);
-                        const float d0 = m0 - mean, d1 = m1 - mean, d2 = m2 - mean, d3 = m3 - mean;
-                        const float M2 = s2[b] + s2[NB + b] + s2[2 * NB + b] + s2[3 * NB + b] +
-                                         32.0f * (d0 * d0 + d1 * d1 + d2 * d2 + d3 * d3);
-                        if (uok) args.stats[(row0 + b) * (size_t)args.nchunk + fb] = make_float2(mean, M2);
-                    }
-                }
-            }
+            swap_epilogue_unit<NB, EPI>(args, fb, f, bf, row0, uok, tbase, s_stat + (size_t)acc * 2 * 4 * NB, q, col0,
+                                        lane);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(acc));
             acc ^= 1;
             if (acc == 0) acc_phase ^= 1u;
         }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// ----------------------------------------------------------------------------
+// Both FFN GEMMs of a dense layer in one launch for small batches (weights as
+// M, the units of the kernel above): the unit list is every GEMM1 unit (token
+// j, 128 hidden features; token-major) followed by every GEMM2 unit (token j,
+// 128 output features), taken in a static order, so the second GEMM's units
+// fill the SMs that the first leaves idle instead of starting a launch of
+// their own with 2.5 rounds of units.  A GEMM2 unit of token j reads the
+// hidden rows of every GEMM1 unit of token j:
+//   - each epilogue warp of a GEMM1 unit, after its stores of the unit, makes
+//     them visible device-wide (every lane fences) and adds 8 / EPW to the
+//     token's counter dep[j m_cap], so a unit adds 8 and a token F / 16 --
+//     the target per row block of the CTA-pair layer kernel, whose counters
+//     and epochs these are (row block 0; the others get their target from
+//     one thread);
+//   - the producer of a GEMM2 unit waits (bounded) until the counter has
+//     grown by the target in this launch, then loads through TMA after an
+//     async-proxy fence.
+// GEMM1 units wait on nothing and every CTA is resident (one per SM, grid <=
+// the SM count), so every wait ends.  Per unit the arithmetic is that of the
+// two separate launches: the same bits.
+// ----------------------------------------------------------------------------
+template <int NB>
+__global__ void __launch_bounds__(CfgS<NB>::THREADS, 1)
+pffn_layer_swap_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmX1,
+                       const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmX2,
+                       const Args a1, const Args a2, const LayerDep dep) {
+    using C = CfgS<NB>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t base = (raw_addr + 1023u) & ~1023u;
+    uint8_t* base_ptr = smem_raw + (base - raw_addr);
+    const uint32_t sA = base;
+    const uint32_t sB = base + C::STAGES * C::A_BYTES;
+    const uint32_t bar0 = base + C::STAGES * C::STAGE_BYTES;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(base_ptr + C::STAGES * C::STAGE_BYTES + 8 * (2 * C::STAGES + 4));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    float* s_stat = reinterpret_cast<float*>(base_ptr + C::STAGES * C::STAGE_BYTES + C::BAR_BYTES);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmW1);
+        tma_prefetch_desc(&tmX1);
+        tma_prefetch_desc(&tmW2);
+        tma_prefetch_desc(&tmX2);
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), C::EPW);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(tmem_holder);
+    pdl_wait();              // S comes from the previous kernel of the stream
+    pdl_launch_next();
+
+    const int nfb1 = a1.n_tiles, nfb2 = a2.n_tiles;        // feature blocks of 128 per token
+    const long long units1 = a1.tiles, units = a1.tiles + a2.tiles;
+    const int kblocks1 = a1.K / BK, kblocks2 = a2.K / BK;
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer ------------------------------
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (long long u = blockIdx.x; ok && u < units; u += gridDim.x) {
+            const bool g1 = u < units1;
+            const Args& a = g1 ? a1 : a2;
+            const long long uu = g1 ? u : u - units1;
+            const int nfb = g1 ? nfb1 : nfb2;
+            const int j = (int)(uu / nfb);
+            const int fb = (int)(uu - (long long)j * nfb);
+            const int wg = a.group_base + j * a.group_stride;
+            if (!g1) {
+                // the hidden rows of token j: every GEMM1 unit of the token has signalled
+                int done = 1;
+                if (lane == 0) {
+                    done = wait_counter_bounded(dep.cnt + (size_t)j * dep.m_cap, dep.base + dep.target, abort_flag,
+                                                a.err, a.timeout_ns) ? 1 : 0;
+                    fence_proxy_async_global();
+                }
+                done = __shfl_sync(0xffffffffu, done, 0);
+                if (!done) break;
+            }
+            const CUtensorMap* mW = g1 ? &tmW1 : &tmW2;
+            const CUtensorMap* mX = g1 ? &tmX1 : &tmX2;
+            const int kblocks = g1 ? kblocks1 : kblocks2;
+            for (int kb = 0; kb < kblocks; ++kb) {
+                if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, a.err, a.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(full_bar(stage), (uint32_t)C::STAGE_BYTES);
+                    tma_load_3d(mW, sA + stage * C::A_BYTES, full_bar(stage), kb * BK, fb * 128, wg);
+                    tma_load_3d(mX, sB + stage * C::B_BYTES, full_bar(stage), kb * BK, 0, j);
+                }
+                __syncwarp();
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer --------------------------------
+        constexpr uint32_t idesc = make_idesc_f16_f32(128, NB);
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (long long u = blockIdx.x; ok && u < units; u += gridDim.x) {
+            const int kblocks = u < units1 ? kblocks1 : kblocks2;
+            if (!mbar_wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, a1.err, a1.timeout_ns)) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * NB);
+            for (int kb = 0; kb < kblocks; ++kb) {
+                if (!mbar_wait_bounded(full_bar(stage), phase, abort_flag, a1.err, a1.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a0 = sA + stage * C::A_BYTES;
+                const uint32_t b0 = sB + stage * C::B_BYTES;
+                if (lane == 0) {
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k)
+                        umma_f16(d_tmem, make_sw128_desc(a0 + 32u * k), make_sw128_desc(b0 + 32u * k), idesc,
+                                 (kb > 0 || k > 0) ? 1u : 0u);
+                    umma_commit(empty_bar(stage));
+                }
+                __syncwarp();
+                if (++stage == C::STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            if (lane == 0) umma_commit(tfull_bar(acc));
+            __syncwarp();
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+    } else if (warp >= 4) {
+        // ------------------------------ epilogue ----------------------------------
+        const int e = warp - 4;
+        const int q = warp & 3;                       // TMEM lane quadrant
+        const int col0 = (e >> 2) * C::CPW;           // this warp's first batch column
+        constexpr unsigned kSignal = 8u / (unsigned)C::EPW;   // per warp: 8 per unit
+        static_assert(8 % C::EPW == 0, "signal per unit");
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (long long u = blockIdx.x; u < units; u += gridDim.x) {
+            const bool g1 = u < units1;
+            const Args& a = g1 ? a1 : a2;
+            const long long uu = g1 ? u : u - units1;
+            const int nfb = g1 ? nfb1 : nfb2;
+            const int j = (int)(uu / nfb);
+            const int fb = (int)(uu - (long long)j * nfb);
+            const int wg = a.group_base + j * a.group_stride;
+            const int f = fb * 128 + q * 32 + lane;                      // this lane's output feature
+            const float bf = __ldg(a.bias + (size_t)wg * a.N + f);
+            const size_t row0 = (size_t)j * (size_t)a.a_group_rows;      // row of batch 0 of this group
+            const bool uok = RM_IN_BOUNDS((long long)row0 + a.M <= a.rows_cap && a.M <= a.a_group_rows &&
+                                              fb * 128 + 128 <= a.N, a.err);
+            if (!mbar_wait_bounded(tfull_bar(acc), acc_phase, abort_flag, a.err, a.timeout_ns)) break;
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * NB);
+            float* st = s_stat + (size_t)acc * 2 * 4 * NB;
+            if (g1)
+                swap_epilogue_unit<NB, EPI_GELU>(a1, fb, f, bf, row0, uok, tbase, st, q, col0, lane);
+            else
+                swap_epilogue_unit<NB, EPI_RESID>(a2, fb, f, bf, row0, uok, tbase, st, q, col0, lane);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(acc));
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1u;
+            if (g1) {
+                // this warp's hidden rows of the unit are stored: publish them, then count
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) atomicAdd(dep.cnt + (size_t)j * dep.m_cap, kSignal);
+            }
+        }
+    } else if (warp == 3 && blockIdx.x == 0 && lane == 0) {
+        // row blocks 1 .. m_cap - 1 of every token: no unit signals them, so they get their target here
+        for (int j = 0; j < a1.ngroups; ++j)
+            for (int mb = 1; mb < dep.m_cap; ++mb) atomicAdd(dep.cnt + (size_t)j * dep.m_cap + mb, dep.target);
     }
 
     tc_fence_before();
@@ -1638,14 +1865,50 @@ cudaError_t run_layer(const void* S, const void* W1p, const void* W2p, Args a1, 
                     a2, dep);
 }
 
+template <int NB>
+cudaError_t run_layer_swap(const void* S, const void* W1p, const void* W2p, Args a1, Args a2, unsigned* dep_cnt,
+                           unsigned dep_epoch, int num_sms, cudaStream_t s) {
+    using C = CfgS<NB>;
+    a1.n_tiles = a1.N / 128;
+    a1.tiles = (long long)a1.ngroups * a1.n_tiles;
+    a2.n_tiles = a2.N / 128;
+    a2.tiles = (long long)a2.ngroups * a2.n_tiles;
+    CUtensorMap mW1, mX1, mW2, mX2;
+    if (!make_map(&mW1, W1p, a1.K, a1.N, a1.ngroups, a1.N, 128) ||
+        !make_map(&mX1, S, a1.K, a1.M, a1.ngroups, a1.a_group_rows, NB) ||
+        !make_map(&mW2, W2p, a2.K, a2.N, a2.ngroups, a2.N, 128) ||
+        !make_map(&mX2, a1.hid, a2.K, a2.M, a2.ngroups, a2.a_group_rows, NB))
+        return cudaErrorInvalidValue;
+    LayerDep dep;
+    dep.cnt = dep_cnt;
+    dep.target = (unsigned)a1.n_tiles * 8u;     // = F / 16, the CTA-pair layer kernel's target
+    dep.base = dep_epoch * dep.target;
+    dep.m_cap = (int)((a1.a_group_rows + BM2 - 1) / BM2);
+    auto k = pffn_layer_swap_kernel<NB>;
+    static bool attr_done = false;  // once per template instance
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    const long long units = a1.tiles + a2.tiles;
+    const long long grid = units < num_sms ? units : num_sms;   // one CTA per SM: all resident
+    return launch_k(k, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM_BYTES, s, mW1, mX1, mW2, mX2, a1, a2, dep);
+}
+
 }  // namespace tc
 
 int gemm2_bn(int D);
 
 bool layer_tc_fusable(int B, int D, int F) {
-    return tc::fused_enabled() && B > tc::swap_max_batch() && tc::use_pair(B, tc::EPI_GELU) &&
-           tc::use_pair(B, tc::EPI_RESID) && tc::pick_bn(F) == 256 && gemm2_bn(D) == 256 && D % (2 * tc::BK) == 0 &&
-           F % (2 * tc::BK) == 0;
+    if (!tc::fused_enabled()) return false;
+    // weights as M (128-feature units, 128-column LN2 chunks): fused from B = 17 on.  At the
+    // 1B shape, B = 64: 0.451 against 0.466 ms per step; B = 1 and 8: 0.410 / 0.426 against
+    // 0.410 / 0.423 (the separate launches overlap more with their neighbours there).
+    if (B <= tc::swap_max_batch())
+        return B > 16 && D % 128 == 0 && F % 128 == 0 && gemm2_bn(D) == 256 && F % 256 == 0;
+    return tc::use_pair(B, tc::EPI_GELU) && tc::use_pair(B, tc::EPI_RESID) && tc::pick_bn(F) == 256 &&
+           gemm2_bn(D) == 256 && D % (2 * tc::BK) == 0 && F % (2 * tc::BK) == 0;
 }
 
 cudaError_t launch_layer_tc(const void* S, const void* W1p, const float* b1, void* Hid, const void* W2p,
@@ -1694,6 +1957,13 @@ cudaError_t launch_layer_tc(const void* S, const void* W1p, const float* b1, voi
     a2.m_tiles = a1.m_tiles;
     a2.tiles = (long long)T * a2.m_tiles * a2.n_tiles;
     a2.n_fastest = a2.M > a2.N ? 1 : 0;
+    if (B <= tc::swap_max_batch()) {
+        if (B <= 16) return tc::run_layer_swap<16>(S, W1p, W2p, a1, a2, dep_cnt, dep_epoch, num_sms, s);
+        if (B <= 32) return tc::run_layer_swap<32>(S, W1p, W2p, a1, a2, dep_cnt, dep_epoch, num_sms, s);
+        if (B <= 64) return tc::run_layer_swap<64>(S, W1p, W2p, a1, a2, dep_cnt, dep_epoch, num_sms, s);
+        if (B <= 128) return tc::run_layer_swap<128>(S, W1p, W2p, a1, a2, dep_cnt, dep_epoch, num_sms, s);
+        return tc::run_layer_swap<256>(S, W1p, W2p, a1, a2, dep_cnt, dep_epoch, num_sms, s);
+    }
     // one stage depth for both GEMMs: two k-blocks a stage unless RM_GEMM_KSUB=1
     const bool k2 = tc::use_ksub2(F, tc::EPI_RESID) && D % (2 * tc::BK) == 0;
     return k2 ? tc::run_layer<2>(S, W1p, W2p, a1, a2, dep_cnt, dep_epoch, num_sms, s)
