@@ -412,7 +412,9 @@ unimix_local_staged_kernel(const Tin* __restrict__ X, long long x_stride, const 
             const uint32_t bytes = (uint32_t)jv * BS * 2u;
             if (lane == 0) mbar_arrive_expect_tx(full(s), (uint32_t)rows * bytes);
             __syncwarp();
-            if (lane < rows)
+            // (bounds-checked build: a skipped copy leaves the stage short, and the
+            // compute warps' bounded wait then ends the launch with an error)
+            if (lane < rows && RM_IN_BOUNDS(b0 + lane < B && (long long)jg * kLsJ * BS + jv * BS <= x_stride, err))
                 bulk_copy_g2s(sbase + (uint32_t)s * C::STAGE_BYTES + (uint32_t)lane * C::PITCH,
                               X + (long long)(b0 + lane) * x_stride + (long long)jg * kLsJ * BS, bytes, full(s));
         }
@@ -509,12 +511,13 @@ unimix_local_staged_kernel(const Tin* __restrict__ X, long long x_stride, const 
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            bulk_copy_s2g(H + (long long)j * Npitch + (long long)b0 * BS, sbase + (uint32_t)ob,
-                          (uint32_t)rows * BS * 2u);
+            if (RM_IN_BOUNDS((long long)b0 * BS + (long long)rows * BS <= Npitch, err))
+                bulk_copy_s2g(H + (long long)j * Npitch + (long long)b0 * BS, sbase + (uint32_t)ob,
+                              (uint32_t)rows * BS * 2u);
             bulk_commit_group();
         }
         sbuf ^= 1;
-        if (bt == ntiles - 1) {   // row j's padding columns
+        if (bt == ntiles - 1 && RM_IN_BOUNDS(Npad <= Npitch, err)) {   // row j's padding columns
             __half* hrow = H + (long long)j * Npitch;
             for (long long q = (long long)B * BS + lane; q < Npad; q += 32) hrow[q] = __float2half_rn(0.f);
         }

@@ -45,6 +45,19 @@ for dt, path, T, D, k, L, B in [("bf16", "tcgen05", 4, 256, 2, 2, 300), ("bf16",
     out["XL_" + key] = XL.cpu().numpy()
     out["Xo_" + key] = Xo.cpu().numpy()
     m.close()
+# UniMixing in both layers (the staged tensor-core local step; bf16 and fp16 samples in)
+for T, D, bs, B in [(8, 512, 64, 37), (8, 512, 32, 100)]:
+    layers = synth.make_stack(T, D, 2, 2, 82, "bf16", "cuda")
+    m = RankMixer(T, D, 2, layers, max_batch=B)
+    for n in range(2):
+        WG, WB = synth.make_unimix_weights(T, D, bs, 83 + n, "cuda")
+        m.set_unimixing(n, WG, WB, tau=0.3, iters=5)
+    X = synth.make_input(B, T, D, 85, "bf16", "cuda")
+    pooled, XL = m.stack_forward(X, return_XL=True, xl_dtype="f32")
+    torch.cuda.synchronize()
+    assert m.sync_status() == 0
+    out[f"unimix_XL_{{T}}_{{D}}_{{bs}}_{{B}}"] = XL.cpu().numpy()
+    m.close()
 # the Sparse-MoE PFFN: one-CTA and CTA-pair expert tiles
 for B in (300, 600):
     T, D, E, Fe = 2, 256, 4, 256
