@@ -597,6 +597,16 @@ for T, D, k, L, B, Bcap in {shapes}:
     out["pooled2_" + key] = pooled2.float().cpu().numpy()
     print(key, "pffn launches", prof["pffn"][0], "gemm1 launches", prof["gemm1"][0])
     m.close()
+# one context through batches that alternate between the CTA-pair and the weights-as-M
+# layer kernels (the two share the dependency counters and their epochs)
+layers = synth.make_stack(8, 512, 2, 2, 413, "bf16", "cuda")
+m = RankMixer(8, 512, 2, layers, max_batch=600)
+X = synth.make_input(600, 8, 512, 414, "bf16", "cuda")
+for i, B in enumerate((600, 40, 300, 20, 64, 600)):
+    out[f"seq_{{i}}_{{B}}"] = m.stack_forward(X[:B].contiguous()).float().cpu().numpy()
+torch.cuda.synchronize()
+assert m.sync_status() == 0
+m.close()
 np.savez(sys.argv[1], **out)
 print("ok")
 """
