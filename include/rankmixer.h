@@ -35,6 +35,11 @@
  *     in a per-context error word and reported by the next rm_sync_status().
  *   - One context may be used by one host thread / one stream at a time; its
  *     workspace is shared by all calls on it.
+ *   - The dense forward calls (rm_block_forward, rm_stack_forward, rm_score)
+ *     may be captured into a CUDA graph once a first call outside capture has
+ *     made the context's lazy allocations: under capture each layer's FFN runs
+ *     as two GEMM launches instead of one fused launch (the same results),
+ *     because the fused launch depends on per-call host state.
  */
 #ifndef RANKMIXER_H_
 #define RANKMIXER_H_

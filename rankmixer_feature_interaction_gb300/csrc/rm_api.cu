@@ -477,7 +477,12 @@ rm_status run_pffn(rm_ctx* c, int layer, int B, cudaStream_t s) {
         c->ln2_cw = g.D;
         return RM_OK;
     }
-    if (c->use_tc && c->dep_cnt && layer_tc_fusable(B, g.D, c->F)) {
+    // Under stream capture the two launches run instead of the fused one: the
+    // fused launch waits for counter values that depend on how many fused
+    // launches came before (host state), which a replayed graph would not track.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    RM_CHECK_CUDA(cudaStreamIsCapturing(s, &cap), "cudaStreamIsCapturing");
+    if (c->use_tc && c->dep_cnt && cap == cudaStreamCaptureStatusNone && layer_tc_fusable(B, g.D, c->F)) {
         // both GEMMs in one launch (the same bits as the two launches below)
         ProfScope ps(c, RM_K_PFFN, s);
         cudaError_t e = launch_layer_tc(c->S, w.W1p, w.b1, c->Hid, w.W2p, w.b2, c->Z, c->stats, B, g.T, g.D, c->F,

@@ -191,6 +191,32 @@ def test_deterministic_reruns():
     assert torch.equal(p1, p2) and torch.equal(x1, x2)
 
 
+@pytest.mark.parametrize("B", [300, 40])      # the CTA-pair and the weights-as-M layer kernels eagerly
+def test_graph_captured_stack_replays_the_eager_result(B):
+    """The stack forward captured into a CUDA graph (after one eager call has made the
+    lazy allocations) replays the eager result bit for bit: under capture each layer's FFN
+    runs as two launches, which give the fused launch's bits."""
+    T, D, k, L = 8, 512, 2, 2
+    m, _, X = _build(T, D, k, L, B, 25, "bf16")
+    ref = m.stack_forward(X).clone()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        m.stack_forward(X)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        res = m.stack_forward(X)
+    for _ in range(3):
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(res, ref)
+    assert m.sync_status() == _lib.RM_OK
+    assert torch.equal(m.stack_forward(X), ref)   # eager again after the captures
+
+
 @pytest.mark.parametrize("B", [100, 2500])      # one shot; three pipelined chunks (512, 1024, 964)
 def test_host_entry_matches_device_entry(B):
     """The host entry runs large batches as chunks.  Every sample's arithmetic is the same
