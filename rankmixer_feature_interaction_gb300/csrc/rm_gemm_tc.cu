@@ -30,13 +30,60 @@
 #include <cudaTypedefs.h>
 
 #include <cstdlib>
+#include <map>
 #include <mutex>
 #include <string>
+#include <utility>
 
 #include "rm_common.cuh"
 #include "rm_internal.h"
 
 namespace rm {
+
+cudaError_t smem_attr_once(const void* func, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, int> done;
+    std::lock_guard<std::mutex> lk(mu);
+    auto key = std::make_pair(func, dev);
+    auto it = done.find(key);
+    if (it != done.end() && it->second >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done[key] = bytes;
+    return e;
+}
+
+int pair_occupancy_once(const void* func, int threads, int smem, int num_sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return num_sms / 2;
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, int> cache;
+    std::lock_guard<std::mutex> lk(mu);
+    auto key = std::make_pair(func, dev);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * (num_sms / 2)), 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, func, &cfg) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = num_sms / 2;
+    }
+    cache[key] = n;
+    return n;
+}
+
 namespace tc {
 
 constexpr int BM = 128;
@@ -1087,11 +1134,9 @@ cudaError_t run(const void* A, long long a_rows_total, const void* W, int n_wgro
         mC = mA;   // unused
     }
     auto k = pffn_gemm_tc_kernel<BN, EPI>;
-    static bool attr_done = false;  // once per template instance
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    {
+        cudaError_t e = smem_attr_once((const void*)k, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        attr_done = true;
     }
     long long grid = num_sms;
     if (a.tile_prefix == nullptr && a.tiles < grid) grid = a.tiles;
@@ -1140,28 +1185,11 @@ cudaError_t run_pair(const void* A, long long a_rows_total, const void* W, int n
         mC = mA;   // unused
     }
     auto k = pffn_gemm_tc2_kernel<BN, EPI, EPW, KSUB>;
-    static int max_pairs = 0;   // once per template instance
-    if (max_pairs == 0) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    {
+        cudaError_t e = smem_attr_once((const void*)k, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(2 * (num_sms / 2)), 1, 1);
-        cfg.blockDim = dim3(C::THREADS, 1, 1);
-        cfg.dynamicSmemBytes = C::SMEM_BYTES;
-        cudaLaunchAttribute attr;
-        attr.id = cudaLaunchAttributeClusterDimension;
-        attr.val.clusterDim.x = 2;
-        attr.val.clusterDim.y = 1;
-        attr.val.clusterDim.z = 1;
-        cfg.attrs = &attr;
-        cfg.numAttrs = 1;
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess || n <= 0) {
-            cudaGetLastError();
-            n = num_sms / 2;
-        }
-        max_pairs = n;
     }
+    const int max_pairs = pair_occupancy_once((const void*)k, C::THREADS, C::SMEM_BYTES, num_sms);
     long long pairs = (a.tile_prefix == nullptr && a.tiles < max_pairs) ? a.tiles : max_pairs;
     return launch_k(k, dim3((unsigned)(2 * pairs)), dim3(C::THREADS), C::SMEM_BYTES, s, mA, mB, mC, a);
 }
@@ -1763,11 +1791,9 @@ cudaError_t run_swap(const void* A, const void* W, int n_wgroups, Args a, int nu
     if (!make_map(&mW, W, a.K, a.N, n_wgroups, a.N, 128)) return cudaErrorInvalidValue;
     if (!make_map(&mX, A, a.K, a.M, a.ngroups, a.a_group_rows, NB)) return cudaErrorInvalidValue;
     auto k = pffn_gemm_swap_kernel<NB, EPI>;
-    static bool attr_done = false;  // once per template instance
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    {
+        cudaError_t e = smem_attr_once((const void*)k, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        attr_done = true;
     }
     const long long grid = a.tiles < num_sms ? a.tiles : num_sms;
     return launch_k(k, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM_BYTES, s, mW, mX, a);
@@ -1837,28 +1863,11 @@ cudaError_t run_layer(const void* S, const void* W1p, const void* W2p, Args a1, 
     dep.base = dep_epoch * dep.target;
     dep.m_cap = (int)((a1.a_group_rows + BM2 - 1) / BM2);
     auto k = pffn_layer_tc2_kernel<KSUB>;
-    static int max_pairs = 0;   // once per template instance
-    if (max_pairs == 0) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    {
+        cudaError_t e = smem_attr_once((const void*)k, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(2 * (num_sms / 2)), 1, 1);
-        cfg.blockDim = dim3(C::THREADS, 1, 1);
-        cfg.dynamicSmemBytes = C::SMEM_BYTES;
-        cudaLaunchAttribute attr;
-        attr.id = cudaLaunchAttributeClusterDimension;
-        attr.val.clusterDim.x = 2;
-        attr.val.clusterDim.y = 1;
-        attr.val.clusterDim.z = 1;
-        cfg.attrs = &attr;
-        cfg.numAttrs = 1;
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess || n <= 0) {
-            cudaGetLastError();
-            n = num_sms / 2;
-        }
-        max_pairs = n;
     }
+    const int max_pairs = pair_occupancy_once((const void*)k, C::THREADS, C::SMEM_BYTES, num_sms);
     const long long tiles = a1.tiles + a2.tiles;
     const long long pairs = tiles < max_pairs ? tiles : max_pairs;
     return launch_k(k, dim3((unsigned)(2 * pairs)), dim3(C::THREADS), C::SMEM_BYTES, s, mA1, mB1, mC1, mA2, mB2, a1,
@@ -1885,11 +1894,9 @@ cudaError_t run_layer_swap(const void* S, const void* W1p, const void* W2p, Args
     dep.base = dep_epoch * dep.target;
     dep.m_cap = (int)((a1.a_group_rows + BM2 - 1) / BM2);
     auto k = pffn_layer_swap_kernel<NB>;
-    static bool attr_done = false;  // once per template instance
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    {
+        cudaError_t e = smem_attr_once((const void*)k, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        attr_done = true;
     }
     const long long units = a1.tiles + a2.tiles;
     const long long grid = units < num_sms ? units : num_sms;   // one CTA per SM: all resident

@@ -36,6 +36,15 @@ cudaError_t debug_bounds_fail(const char* what);
         if (::rm::kDebugBounds && !(cond)) return ::rm::debug_bounds_fail(#cond); \
     } while (0)
 
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) acts on the current device:
+// set it once per (kernel, device), so that a process driving several GPUs
+// gets it on each.
+cudaError_t smem_attr_once(const void* func, int bytes);
+// Resident clusters of two CTAs of `func` on the current device at `smem`
+// bytes per CTA and `threads` per CTA, cached per (kernel, device); falls back
+// to half the SM count if the query fails.
+int pair_occupancy_once(const void* func, int threads, int smem, int num_sms);
+
 inline size_t act_size(Act a) { return a == Act::F32 ? 4 : 2; }
 inline size_t op_size(Act a) { return a == Act::F32 ? 4 : 2; }
 

@@ -666,11 +666,9 @@ cudaError_t run(const TrainGemm& g, const KArgs& ka, int num_sms, cudaStream_t s
     }
     auto k = train_gemm_tc_kernel<EPI, A_MN, B_MN, PAIR>;
     constexpr int smem = C::SMEM_BYTES;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    {
+        cudaError_t e = smem_attr_once((const void*)k, smem);
         if (e != cudaSuccess) return e;
-        attr_done = true;
     }
     // persistent: one CTA (or CTA pair) per SM (pair of SMs), at most one per tile
     const long long units = PAIR ? num_sms / 2 : num_sms;

@@ -810,7 +810,7 @@ cudaError_t launch_staged_bs(const void* X, long long x_stride, const void* WBt1
                              cudaStream_t s) {
     using C = LsCfg<BS>;
     auto k = unimix_local_staged_kernel<Tin, BS>;
-    static cudaError_t attr = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t attr = smem_attr_once((const void*)k, C::SMEM);
     if (attr != cudaSuccess) return attr;
     const long long items = (long long)((nb + kLsJ - 1) / kLsJ) * ((B + kLsRows - 1) / kLsRows);
     if (items >= (1LL << 31)) return cudaErrorNotSupported;
