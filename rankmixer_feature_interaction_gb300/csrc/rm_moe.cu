@@ -439,7 +439,9 @@ route_mma_kernel(const Tin* __restrict__ S, long long s_sb, long long s_st, cons
                 const int grp = t * E + 2 * (l & 3) + (j & 1);
                 const Tin* src = S + (long long)row * s_sb + (long long)t * s_st;
                 __half* dst = Sg + ((size_t)grp * Bcap + sl) * D;
-                // up to 8 16-byte words per lane in flight before any is stored
+                // up to 8 16-byte words per lane in flight before any is stored; the
+                // gathered rows are stored with the streaming hint, so that they do not
+                // push out of L2 the S rows still to be re-read for the copies
                 for (int k0 = 8 * lane; k0 < D; k0 += 2048) {
                     uint4 w[8];
 #pragma unroll
@@ -447,7 +449,7 @@ route_mma_kernel(const Tin* __restrict__ S, long long s_sb, long long s_st, cons
                         if (k0 + 256 * i < D) w[i] = __ldg(reinterpret_cast<const uint4*>(src + k0 + 256 * i));
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
-                        if (k0 + 256 * i < D) *reinterpret_cast<uint4*>(dst + k0 + 256 * i) = route_f16x8<Tin>(w[i]);
+                        if (k0 + 256 * i < D) __stcs(reinterpret_cast<uint4*>(dst + k0 + 256 * i), route_f16x8<Tin>(w[i]));
                 }
             }
         }
