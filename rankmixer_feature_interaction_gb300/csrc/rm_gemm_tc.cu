@@ -130,6 +130,7 @@ struct Args {
     const float* bias;        // [weight groups][N]
     __half* hid;              // EPI_GELU output rows (same row index as A), fp16
     int hid_tma;              // EPI_GELU, uniform groups: store through shared memory with TMA (output map)
+    int hid_evict_first;      // hid_tma: the tensor stores carry the L2 evict-first hint
     long long rows_cap;       // rows of the output, residual and statistics buffers (bounds-checked build)
     const __half* resid;      // EPI_RESID residual rows (same row index as A), fp16
     __half* z;                // EPI_RESID output rows (fp16)
@@ -139,6 +140,18 @@ struct Args {
     int* err;
     unsigned long long timeout_ns;
 };
+
+// Tiled TMA store whose lines L2 evicts first: written rows that no later
+// work of the launch reads soon (a hidden layer larger than L2) then push out
+// fewer of the operand tiles that neighbouring CTAs still re-read.
+__device__ __forceinline__ void tma_store_3d_evict_first(const CUtensorMap* m, uint32_t src, int x, int y, int z) {
+    asm volatile(
+        "{\n\t.reg .b64 pol;\n\t"
+        "createpolicy.fractional.L2::evict_first.b64 pol, 1.0;\n\t"
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], [%1], pol;\n\t}"
+        ::"l"(reinterpret_cast<uint64_t>(m)), "r"(src), "r"(x), "r"(y), "r"(z)
+        : "memory");
+}
 
 // v[0..31] += 32 consecutive fp16 values at p (64-byte aligned).
 __device__ __forceinline__ void add_f16x32(float (&v)[32], const __half* p) {
@@ -248,7 +261,12 @@ __device__ __forceinline__ void epilogue_gelu_tma(const Args& args, const TileCo
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-            if (any_valid) tma_store_3d(tmC, buf, n0 + 32 * c, m_warp, tc.j);
+            if (any_valid) {
+                if (args.hid_evict_first)
+                    tma_store_3d_evict_first(tmC, buf, n0 + 32 * c, m_warp, tc.j);
+                else
+                    tma_store_3d(tmC, buf, n0 + 32 * c, m_warp, tc.j);
+            }
             bulk_commit_group();
         }
         sbuf ^= 1;
@@ -1907,6 +1925,21 @@ cudaError_t run_layer_swap(const void* S, const void* W1p, const void* W2p, Args
 
 int gemm2_bn(int D);
 
+// The hidden layer's tensor stores carry the L2 evict-first hint when the
+// layer's hidden rows (B T F fp16 values) exceed 128 MB, i.e. L2: they are
+// read back only after every first-GEMM tile, so L2 could not keep them
+// anyway.  RM_HID_HINT=0 | 1 in the environment forces either (a tuning
+// switch: the same results).
+bool hid_evict_first(int B, int T, int F) {
+    static int env = -1;
+    if (env < 0) {
+        const char* v = getenv("RM_HID_HINT");
+        env = !v ? 2 : (v[0] == '0' ? 0 : 1);
+    }
+    if (env != 2) return env == 1;
+    return (long long)B * T * F * 2 > (128LL << 20);
+}
+
 bool layer_tc_fusable(int B, int D, int F) {
     if (!tc::fused_enabled()) return false;
     // weights as M (128-feature units, 128-column LN2 chunks): fused from B = 17 on.  At the
@@ -1938,6 +1971,7 @@ cudaError_t launch_layer_tc(const void* S, const void* W1p, const float* b1, voi
     a1.bias = b1;
     a1.hid = reinterpret_cast<__half*>(Hid);
     a1.hid_tma = 1;
+    a1.hid_evict_first = hid_evict_first(B, T, F) ? 1 : 0;
     a1.rows_cap = (long long)T * Bcap;
     a1.err = err;
     a1.timeout_ns = timeout_ns;
@@ -2016,6 +2050,7 @@ cudaError_t launch_gemm1_tc(const void* S, const void* W1p, const float* b1, voi
     a.bias = b1;
     a.hid = reinterpret_cast<__half*>(Hid);
     a.hid_tma = 1;
+    a.hid_evict_first = hid_evict_first(B, T, F) ? 1 : 0;
     a.rows_cap = (long long)T * Bcap;
     a.err = err;
     a.timeout_ns = timeout_ns;
