@@ -55,6 +55,9 @@ TRAFFIC = {
     # fused layer kernel (both FFN GEMMs of a layer per launch); between boxes the figure for
     # the same kernel code has ranged from 6.3 to 8.8 GB
     ("rankmixer_1b", 4096, 2, "pffn"): (6337070080, "51a917a84a212143feb9652766e6d06d29948d804904d2fc1e6e56f11462e771"),
+    # the expert GEMMs of "bench.py --config moe_1b --steps 3 --warmup 3 --no-cpu-baseline"
+    ("moe_1b", 4096, 1, "moe_gemm1"): (4679440384, "51a917a84a212143feb9652766e6d06d29948d804904d2fc1e6e56f11462e771"),
+    ("moe_1b", 4096, 1, "moe_gemm2"): (4784491776, "51a917a84a212143feb9652766e6d06d29948d804904d2fc1e6e56f11462e771"),
 }
 
 
