@@ -526,7 +526,7 @@ print("ok")
 _DISPATCH_SHAPES = [(4, 256, 2, 2, 300), (2, 192, 2, 1, 300), (8, 512, 2, 2, 1100), (4, 256, 2, 2, 13),
                     (4, 256, 2, 2, 40), (4, 512, 2, 1, 150), (32, 768, 1, 1, 20)]
 _TUNING_KEYS = ("RM_GEMM_PAIR", "RM_GEMM_KSUB", "RM_GEMM1_EPW", "RM_GEMM2_BN", "RM_GEMM_SMALL_BN", "RM_GEMM_SWAP_MAX",
-                "RM_PDL", "RM_NVTX", "RM_GEMM_FUSED")
+                "RM_PDL", "RM_NVTX", "RM_GEMM_FUSED", "RM_HID_HINT")
 
 
 @pytest.mark.parametrize("tuning", [{},                                            # the defaults
@@ -542,7 +542,8 @@ _TUNING_KEYS = ("RM_GEMM_PAIR", "RM_GEMM_KSUB", "RM_GEMM1_EPW", "RM_GEMM2_BN", "
                                     {"RM_GEMM_KSUB": "1"},                          # one k-block per stage
                                     {"RM_GEMM1_EPW": "16"},                         # 16 GELU epilogue warps
                                     {"RM_GEMM1_EPW": "8", "RM_GEMM_KSUB": "2"},     # 8 warps at short K
-                                    {"RM_GEMM1_EPW": "16", "RM_GEMM_KSUB": "1"}])
+                                    {"RM_GEMM1_EPW": "16", "RM_GEMM_KSUB": "1"},
+                                    {"RM_HID_HINT": "1"}])                          # evict-first hidden-row stores
 def test_every_gemm_tile_dispatch(tuning):
     import os
     import subprocess
